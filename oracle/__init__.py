@@ -1,0 +1,220 @@
+"""CPU oracle for block-sparse long-context decode attention.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` are the only callers.  The product path
+(``block_sparse_long_quest_gb300``) never imports this package, and this
+package never imports the product.
+
+The arithmetic lives in ``kt_oracle.c`` (plain single-threaded C, double
+precision); this module only compiles it and marshals numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kt_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+REP_MAX, REP_MEAN, REP_QUEST, REP_FIX, REP_DYNAMIC = 0, 1, 2, 3, 4
+HEAD_SHARED, HEAD_SEPARATE = 0, 1
+
+
+def build(force: bool = False) -> str:
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
+                               "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _KV(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("B", ctypes.c_int64), ("H_kv", ctypes.c_int64), ("d", ctypes.c_int64),
+                ("bs", ctypes.c_int64), ("max_blocks", ctypes.c_int64), ("P", ctypes.c_int64)]
+
+
+class _Params(ctypes.Structure):
+    _fields_ = [("H_q", ctypes.c_int64), ("initial_blocks", ctypes.c_int64),
+                ("local_blocks", ctypes.c_int64), ("top_k", ctypes.c_int64),
+                ("rep", ctypes.c_int64), ("head_mode", ctypes.c_int64),
+                ("num_reps", ctypes.c_int64), ("fix_stride", ctypes.c_int64),
+                ("softmax_scale", ctypes.c_double)]
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        L.orc_f16_to_double.restype = ctypes.c_double
+        L.orc_f16_to_double.argtypes = [ctypes.c_uint16]
+        L.orc_f16_array.restype = None
+        L.orc_f16_array.argtypes = [vp, vp, i64]
+        L.orc_partition.restype = None
+        L.orc_partition.argtypes = [i64, i64, i64, i64, vp, vp, vp]
+        L.orc_reps_per_block.restype = i64
+        L.orc_reps_per_block.argtypes = [vp, i64]
+        L.orc_block_reps.restype = None
+        L.orc_block_reps.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp]
+        L.orc_dynamic_token_scores.restype = None
+        L.orc_dynamic_token_scores.argtypes = [vp, i64, i64, vp, vp, i64, vp]
+        L.orc_head_block_score.restype = ctypes.c_double
+        L.orc_head_block_score.argtypes = [vp, vp, i64, i64, i64]
+        L.orc_select.restype = i64
+        L.orc_select.argtypes = [vp, i64, i64, i64, vp]
+        L.orc_attend.restype = None
+        L.orc_attend.argtypes = [vp, i64, i64, i64, vp, vp, i64, ctypes.c_double, vp]
+        L.orc_dense.restype = None
+        L.orc_dense.argtypes = [vp, vp, i64, ctypes.c_double, vp]
+        L.orc_sparse_step.restype = ctypes.c_int
+        L.orc_sparse_step.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, i64, i64]
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+class KV:
+    """Paged KV view handed to the C oracle (keeps the arrays alive)."""
+
+    def __init__(self, k_pool, v_pool, block_table, seq_lens, block_size=128):
+        self.k_pool = np.ascontiguousarray(k_pool, dtype=np.uint16)
+        self.v_pool = np.ascontiguousarray(v_pool, dtype=np.uint16)
+        self.block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+        self.seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        P, H_kv, bs, d = self.k_pool.shape
+        assert bs == block_size
+        self.H_kv, self.d, self.bs, self.P = H_kv, d, bs, P
+        self.B = self.seq_lens.size
+        self.max_blocks = self.block_table.shape[1]
+        self.s = _KV(self.k_pool.ctypes.data, self.v_pool.ctypes.data,
+                     self.block_table.ctypes.data, self.seq_lens.ctypes.data,
+                     self.B, H_kv, d, bs, self.max_blocks, P)
+
+    @classmethod
+    def of(cls, w):
+        return cls(w.k_pool, w.v_pool, w.block_table, w.seq_lens)
+
+
+def params(p) -> _Params:
+    return _Params(p.num_q_heads, p.initial_blocks, p.local_blocks, p.top_k, p.rep,
+                   p.head_mode, p.num_reps, p.fix_stride, float(p.softmax_scale))
+
+
+def f16_to_double(bits) -> np.ndarray:
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(bits.shape, dtype=np.float64)
+    lib().orc_f16_array(bits.ctypes.data, out.ctypes.data, bits.size)
+    return out
+
+
+def partition(n: int, initial_blocks: int, local_blocks: int, block_size: int = 128):
+    a = (ctypes.c_int64 * 3)()
+    lib().orc_partition(n, block_size, initial_blocks, local_blocks, ctypes.byref(a, 0),
+                        ctypes.byref(a, 8), ctypes.byref(a, 16))
+    return int(a[0]), int(a[1]), int(a[2])
+
+
+def reps_per_block(p, block_size: int = 128) -> int:
+    pp = params(p)
+    return int(lib().orc_reps_per_block(ctypes.byref(pp), block_size))
+
+
+def block_reps(kv: KV, p, b: int, j: int, h: int, dyn_scores=None):
+    pp = params(p)
+    R = reps_per_block(p, kv.bs)
+    h16 = np.zeros((R, kv.d), dtype=np.uint16)
+    f32 = np.zeros(kv.d, dtype=np.float32)
+    ds = None if dyn_scores is None else np.ascontiguousarray(dyn_scores, dtype=np.float64)
+    lib().orc_block_reps(ctypes.byref(kv.s), b, j, h, ctypes.byref(pp), _ptr(ds),
+                         h16.ctypes.data, f32.ctypes.data)
+    return f32 if p.rep == REP_MEAN else h16
+
+
+def dynamic_token_scores(kv: KV, p, b: int, h: int, q_local_b):
+    pp = params(p)
+    ql = np.ascontiguousarray(q_local_b, dtype=np.uint16)
+    n = int(kv.seq_lens[b])
+    acc = np.zeros(max(n, 1), dtype=np.float64)
+    lib().orc_dynamic_token_scores(ctypes.byref(kv.s), b, h, ctypes.byref(pp), ql.ctypes.data,
+                                   ql.shape[0], acc.ctypes.data)
+    return acc[:n]
+
+
+def head_block_score(q, reps, rep: int) -> float:
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    reps = np.ascontiguousarray(reps, dtype=np.float64)
+    R, d = reps.shape
+    return float(lib().orc_head_block_score(q.ctypes.data, reps.ctypes.data, R, d, rep))
+
+
+def select(scores, c0: int, k: int) -> np.ndarray:
+    s = np.ascontiguousarray(scores, dtype=np.float64)
+    sel = np.zeros(max(k, 1), dtype=np.int32)
+    cnt = lib().orc_select(s.ctypes.data, c0, s.size, k, sel.ctypes.data)
+    return sel[:cnt]
+
+
+def attend(kv: KV, b: int, hq: int, num_q_heads: int, q_bits, blocks, scale: float):
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    bl = np.ascontiguousarray(blocks, dtype=np.int32)
+    out = np.zeros(kv.d, dtype=np.float64)
+    lib().orc_attend(ctypes.byref(kv.s), b, hq, num_q_heads, q.ctypes.data, bl.ctypes.data,
+                     bl.size, scale, out.ctypes.data)
+    return out
+
+
+def dense(kv: KV, q, num_q_heads: int, scale: float) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    out = np.zeros((kv.B, num_q_heads, kv.d), dtype=np.float64)
+    lib().orc_dense(ctypes.byref(kv.s), q.ctypes.data, num_q_heads, scale, out.ctypes.data)
+    return out
+
+
+def sparse_step(kv: KV, q, p, q_local=None, *, units=None, want_reps=True,
+                want_dyn_scores=False):
+    """One decode step of the method; returns a dict of numpy outputs.
+
+    reps are indexed by LOGICAL block: [B][max_blocks][H_kv][R][d] (binary16
+    bits) or [B][max_blocks][H_kv][d] (Mean, binary32).  unit_scores is
+    [B][SEL][max_blocks] with NaN outside the context range.
+    """
+    pp = params(p)
+    B, H_kv, d, MB = kv.B, kv.H_kv, kv.d, kv.max_blocks
+    R = reps_per_block(p, kv.bs)
+    SEL = 1 if p.head_mode == HEAD_SHARED else H_kv
+    lo, hi = (0, SEL) if units is None else units
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    ql = None if q_local is None else np.ascontiguousarray(q_local, dtype=np.uint16)
+    T = 0 if ql is None else ql.shape[1]
+    reps_h16 = reps_f32 = None
+    if want_reps:
+        if p.rep == REP_MEAN:
+            reps_f32 = np.zeros((B, MB, H_kv, d), dtype=np.float32)
+        else:
+            reps_h16 = np.zeros((B, MB, H_kv, R, d), dtype=np.uint16)
+    dyn = np.zeros((B, H_kv, MB * kv.bs), dtype=np.float64) if want_dyn_scores else None
+    us = np.full((B, SEL, MB), np.nan, dtype=np.float64)
+    sel = np.full((B, SEL, max(p.top_k, 1)), -1, dtype=np.int32)
+    cnt = np.zeros((B, SEL), dtype=np.int32)
+    out = np.zeros((B, p.num_q_heads, d), dtype=np.float64)
+    rc = lib().orc_sparse_step(ctypes.byref(kv.s), q.ctypes.data, ctypes.byref(pp), _ptr(ql), T,
+                               _ptr(reps_h16), _ptr(reps_f32), _ptr(dyn), us.ctypes.data,
+                               sel.ctypes.data, cnt.ctypes.data, out.ctypes.data, lo, hi)
+    if rc != 0:
+        raise ValueError("oracle rejected the parameters")
+    return dict(reps=reps_f32 if p.rep == REP_MEAN else reps_h16, unit_scores=us, sel=sel,
+                cnt=cnt, out=out, dyn_scores=dyn)
