@@ -1,0 +1,226 @@
+"""Python binding of libkt (block-sparse long-context decode attention, GB300).
+
+Argument marshalling only: every step of the decode path runs in the CUDA
+kernels of libkt.so, behind the C ABI declared in include/kt.h.  Tensors are
+passed as raw device pointers together with torch's current CUDA stream.  If
+libkt.so is missing this module raises at import; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB as _LIB_PATH, build  # noqa: F401
+
+KT_OK = 0
+KT_ERR_INVALID_ARG = 1
+KT_ERR_UNSUPPORTED = 2
+KT_ERR_WORKSPACE_TOO_SMALL = 3
+KT_ERR_CUDA = 4
+KT_ERR_DEVICE_CHECK = 5
+KT_ERR_TIMEOUT = 6
+
+KT_REP_MAX, KT_REP_MEAN, KT_REP_QUEST, KT_REP_FIX, KT_REP_DYNAMIC = 0, 1, 2, 3, 4
+KT_HEAD_SHARED, KT_HEAD_SEPARATE = 0, 1
+(KT_OP_SCORE_SELECT, KT_OP_SPARSE_ATTN, KT_OP_DENSE_ATTN, KT_OP_SPARSE_STEP,
+ KT_OP_DYNAMIC_REPS) = 0, 1, 2, 3, 4
+
+# Every symbol declared in include/kt.h.
+EXPORTS = (
+    "kt_status_string", "kt_reps_per_block", "kt_reps_pool_bytes", "kt_workspace_bytes",
+    "kt_workspace_init", "kt_build_block_reps", "kt_build_dynamic_reps",
+    "kt_score_select_blocks", "kt_sparse_decode_attn", "kt_sparse_decode_step",
+    "kt_sparse_decode_step_host", "kt_dense_decode_attn", "kt_read_device_status",
+    "kt_selftest_bounded_wait",
+)
+
+
+class KtError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call}: {status_string(status)} (status {status})")
+
+
+class PagedKV(ctypes.Structure):
+    """kt_paged_kv: device pointers + shapes of the paged K/V pools."""
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("batch", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("num_pages", ctypes.c_int32)]
+
+
+class SparseParams(ctypes.Structure):
+    """kt_sparse_params."""
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("initial_blocks", ctypes.c_int32),
+                ("local_blocks", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("num_reps", ctypes.c_int32), ("fix_stride", ctypes.c_int32),
+                ("rep", ctypes.c_int32), ("head_mode", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float)]
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"libkt.so not built ({_LIB_PATH}); run "
+                          "block_sparse_long_quest_gb300.build() or __graft_entry__.build()")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i32, sz, P = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.POINTER
+    sig = {
+        "kt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "kt_reps_per_block": (i32, [P(SparseParams)]),
+        "kt_reps_pool_bytes": (sz, [P(PagedKV), P(SparseParams)]),
+        "kt_workspace_bytes": (ctypes.c_int, [ctypes.c_int, P(PagedKV), P(SparseParams), i32,
+                                              P(sz)]),
+        "kt_workspace_init": (ctypes.c_int, [vp, sz, vp]),
+        "kt_build_block_reps": (ctypes.c_int, [P(PagedKV), P(SparseParams), i32, i32, vp, vp]),
+        "kt_build_dynamic_reps": (ctypes.c_int, [P(PagedKV), P(SparseParams), vp, i32, i32, i32,
+                                                 vp, vp, vp, sz, vp]),
+        "kt_score_select_blocks": (ctypes.c_int, [vp, P(PagedKV), vp, P(SparseParams), vp, vp,
+                                                  vp, vp, sz, vp]),
+        "kt_sparse_decode_attn": (ctypes.c_int, [vp, P(PagedKV), P(SparseParams), vp, vp, vp,
+                                                 vp, sz, vp]),
+        "kt_sparse_decode_step": (ctypes.c_int, [vp, P(PagedKV), vp, P(SparseParams), vp, vp,
+                                                 vp, vp, sz, vp]),
+        "kt_sparse_decode_step_host": (ctypes.c_int, [vp, vp, P(PagedKV), vp, P(SparseParams),
+                                                      vp, vp, vp, vp, vp, sz, vp]),
+        "kt_dense_decode_attn": (ctypes.c_int, [vp, P(PagedKV), i32, ctypes.c_float, vp, vp, sz,
+                                                vp]),
+        "kt_read_device_status": (ctypes.c_int, [vp, sz, vp, P(i32)]),
+        "kt_selftest_bounded_wait": (ctypes.c_int, [vp, sz, i32, vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.kt_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(status, call):
+    if status != KT_OK:
+        raise KtError(status, call)
+
+
+def paged_kv(k_pool, v_pool, block_table, seq_lens) -> PagedKV:
+    """k_pool/v_pool: fp16 [P][H_kv][128][128]; block_table: int32 [B][MB]; seq_lens: int32 [B]."""
+    P, H_kv, bs, d = k_pool.shape
+    return PagedKV(_ptr(k_pool), _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
+                   int(seq_lens.shape[0]), H_kv, d, bs, int(block_table.shape[1]), P)
+
+
+def sparse_params(num_q_heads, initial_blocks, local_blocks, top_k, rep, head_mode, *,
+                  num_reps=1, fix_stride=32, softmax_scale=None) -> SparseParams:
+    if softmax_scale is None:
+        softmax_scale = 128 ** -0.5
+    return SparseParams(num_q_heads, initial_blocks, local_blocks, top_k, num_reps, fix_stride,
+                        rep, head_mode, softmax_scale)
+
+
+def kt_reps_per_block(params: SparseParams) -> int:
+    return int(lib.kt_reps_per_block(ctypes.byref(params)))
+
+
+def kt_reps_pool_bytes(kv: PagedKV, params: SparseParams) -> int:
+    return int(lib.kt_reps_pool_bytes(ctypes.byref(kv), ctypes.byref(params)))
+
+
+def kt_workspace_bytes(op: int, kv: PagedKV, params: SparseParams, T: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib.kt_workspace_bytes(op, ctypes.byref(kv), ctypes.byref(params), T, ctypes.byref(n)),
+           "kt_workspace_bytes")
+    return int(n.value)
+
+
+def kt_workspace_init(ws, stream=None):
+    _check(lib.kt_workspace_init(_ptr(ws), ws.numel(), _stream(stream)), "kt_workspace_init")
+
+
+def workspace(op: int, kv: PagedKV, params: SparseParams, T: int = 0, device="cuda"):
+    """A zero-filled workspace tensor (uint8) for `op`, allocated by torch."""
+    import torch
+    ws = torch.empty(kt_workspace_bytes(op, kv, params, T), dtype=torch.uint8, device=device)
+    kt_workspace_init(ws)
+    return ws
+
+
+def kt_build_block_reps(kv, params, first_block, num_blocks, reps_pool, stream=None):
+    _check(lib.kt_build_block_reps(ctypes.byref(kv), ctypes.byref(params), first_block,
+                                   num_blocks, _ptr(reps_pool), _stream(stream)),
+           "kt_build_block_reps")
+
+
+def kt_build_dynamic_reps(kv, params, q_local, T, first_block, num_blocks, reps_pool,
+                          token_scores, ws, stream=None):
+    _check(lib.kt_build_dynamic_reps(ctypes.byref(kv), ctypes.byref(params), _ptr(q_local), T,
+                                     first_block, num_blocks, _ptr(reps_pool),
+                                     _ptr(token_scores), _ptr(ws), ws.numel(), _stream(stream)),
+           "kt_build_dynamic_reps")
+
+
+def kt_score_select_blocks(q, kv, reps_pool, params, sel, cnt, sel_scores, ws, stream=None):
+    _check(lib.kt_score_select_blocks(_ptr(q), ctypes.byref(kv), _ptr(reps_pool),
+                                      ctypes.byref(params), _ptr(sel), _ptr(cnt),
+                                      _ptr(sel_scores), _ptr(ws), ws.numel(), _stream(stream)),
+           "kt_score_select_blocks")
+
+
+def kt_sparse_decode_attn(q, kv, params, sel, cnt, out, ws, stream=None):
+    _check(lib.kt_sparse_decode_attn(_ptr(q), ctypes.byref(kv), ctypes.byref(params), _ptr(sel),
+                                     _ptr(cnt), _ptr(out), _ptr(ws), ws.numel(),
+                                     _stream(stream)),
+           "kt_sparse_decode_attn")
+
+
+def kt_sparse_decode_step(q, kv, reps_pool, params, sel, cnt, out, ws, stream=None):
+    _check(lib.kt_sparse_decode_step(_ptr(q), ctypes.byref(kv), _ptr(reps_pool),
+                                     ctypes.byref(params), _ptr(sel), _ptr(cnt), _ptr(out),
+                                     _ptr(ws), ws.numel(), _stream(stream)),
+           "kt_sparse_decode_step")
+
+
+def kt_sparse_decode_step_host(q_host, q_dev, kv, reps_pool, params, sel, cnt, out_dev,
+                               out_host, ws, stream=None):
+    _check(lib.kt_sparse_decode_step_host(_ptr(q_host), _ptr(q_dev), ctypes.byref(kv),
+                                          _ptr(reps_pool), ctypes.byref(params), _ptr(sel),
+                                          _ptr(cnt), _ptr(out_dev), _ptr(out_host), _ptr(ws),
+                                          ws.numel(), _stream(stream)),
+           "kt_sparse_decode_step_host")
+
+
+def kt_dense_decode_attn(q, kv, num_q_heads, softmax_scale, out, ws, stream=None):
+    _check(lib.kt_dense_decode_attn(_ptr(q), ctypes.byref(kv), num_q_heads, softmax_scale,
+                                    _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+           "kt_dense_decode_attn")
+
+
+def kt_read_device_status(ws, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    _check(lib.kt_read_device_status(_ptr(ws), ws.numel(), _stream(stream), ctypes.byref(v)),
+           "kt_read_device_status")
+    return int(v.value)
+
+
+def kt_selftest_bounded_wait(ws, spin_limit, stream=None):
+    _check(lib.kt_selftest_bounded_wait(_ptr(ws), ws.numel(), spin_limit, _stream(stream)),
+           "kt_selftest_bounded_wait")

@@ -1,0 +1,447 @@
+// kt_api.cu — host side of the libkt C ABI: argument validation, workspace
+// layout, TMA tensor maps and kernel launches.  No allocation, no hidden
+// synchronisation (see kt.h for the contract of every call).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "kt_internal.cuh"
+
+namespace kt {
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kt_status check_kv(const kt_paged_kv* kv) {
+  if (!kv || !kv->k_pool || !kv->v_pool || !kv->block_table || !kv->seq_lens)
+    return KT_ERR_INVALID_ARG;
+  if (!aligned16(kv->k_pool) || !aligned16(kv->v_pool) || !aligned16(kv->block_table) ||
+      !aligned16(kv->seq_lens))
+    return KT_ERR_INVALID_ARG;
+  if (kv->batch < 1 || kv->num_kv_heads < 1 || kv->max_blocks_per_seq < 1 || kv->num_pages < 1)
+    return KT_ERR_INVALID_ARG;
+  if (kv->head_dim != D || kv->block_size != BS) return KT_ERR_UNSUPPORTED;
+  if ((long long)kv->batch * kv->num_kv_heads > MAX_SEGS || kv->batch > 65535)
+    return KT_ERR_UNSUPPORTED;
+  if ((long long)kv->num_pages * kv->num_kv_heads * BS > 0x7FFFFFFFLL) return KT_ERR_UNSUPPORTED;
+  if ((long long)kv->max_blocks_per_seq * BS > 0x7FFFFFFFLL) return KT_ERR_UNSUPPORTED;
+  return KT_OK;
+}
+
+kt_status check_heads(const kt_paged_kv* kv, int num_q_heads, float scale) {
+  if (num_q_heads < 1 || num_q_heads % kv->num_kv_heads != 0) return KT_ERR_INVALID_ARG;
+  if (num_q_heads / kv->num_kv_heads > MAX_G) return KT_ERR_UNSUPPORTED;
+  if (!(scale > 0.0f) || !std::isfinite(scale)) return KT_ERR_INVALID_ARG;
+  return KT_OK;
+}
+
+kt_status check_params(const kt_paged_kv* kv, const kt_sparse_params* p) {
+  if (!p) return KT_ERR_INVALID_ARG;
+  kt_status s = check_heads(kv, p->num_q_heads, p->softmax_scale);
+  if (s != KT_OK) return s;
+  if (p->initial_blocks < 0 || p->local_blocks < 0 || p->top_k < 1) return KT_ERR_INVALID_ARG;
+  if (p->local_blocks < 1 || p->top_k > MAX_TOPK) return KT_ERR_UNSUPPORTED;
+  if (p->head_mode != KT_HEAD_SHARED && p->head_mode != KT_HEAD_SEPARATE)
+    return KT_ERR_INVALID_ARG;
+  switch (p->rep) {
+    case KT_REP_MAX:
+    case KT_REP_MEAN:
+    case KT_REP_QUEST:
+      break;
+    case KT_REP_FIX:
+      if (p->fix_stride < 1 || p->fix_stride > BS || BS % p->fix_stride != 0)
+        return KT_ERR_INVALID_ARG;
+      break;
+    case KT_REP_DYNAMIC:
+      if (p->num_reps < 1) return KT_ERR_INVALID_ARG;
+      if (p->num_reps > MAX_DYN_REPS) return KT_ERR_UNSUPPORTED;
+      break;
+    default:
+      return KT_ERR_INVALID_ARG;
+  }
+  return KT_OK;
+}
+
+int reps_rows(const kt_sparse_params* p) {
+  switch (p->rep) {
+    case KT_REP_MAX:
+    case KT_REP_MEAN:
+      return 1;
+    case KT_REP_QUEST:
+      return 2;
+    case KT_REP_FIX:
+      return p->fix_stride >= 1 ? BS / p->fix_stride : 0;
+    case KT_REP_DYNAMIC:
+      return p->num_reps;
+    default:
+      return 0;
+  }
+}
+
+bool op_selects(kt_op op) { return op == KT_OP_SCORE_SELECT || op == KT_OP_SPARSE_STEP; }
+bool op_attends(kt_op op) {
+  return op == KT_OP_SPARSE_ATTN || op == KT_OP_DENSE_ATTN || op == KT_OP_SPARSE_STEP;
+}
+
+WsLayout layout(kt_op op, const kt_paged_kv* kv, const kt_sparse_params* p, int T) {
+  WsLayout L;
+  std::memset(&L, 0, sizeof(L));
+  const int B = kv->batch, H_kv = kv->num_kv_heads, S = B * H_kv;
+  const int G = p->num_q_heads / H_kv;
+  size_t off = 256;  // status header
+  L.status = 0;
+  if (op_selects(op)) {
+    L.sel = make_sel_plan(B, H_kv, kv->max_blocks_per_seq, p->initial_blocks, p->local_blocks,
+                          p->top_k, p->head_mode);
+    const size_t units = (size_t)B * L.sel.SEL;
+    L.sel_counters = off;
+    off = align256(off + units * 4);
+    L.sel_ncand = off;
+    off = align256(off + units * L.sel.nchunks * 4);
+    L.sel_cand = off;
+    off = align256(off + units * L.sel.nchunks * L.sel.kk * 8);
+  }
+  if (op_attends(op)) {
+    L.slot_floats = ((2 * G + G * D) + 3) & ~3;
+    L.attn_counters = off;
+    off = align256(off + (size_t)S * 4);
+    L.attn_parts = off;
+    off = align256(off + (size_t)2 * (MAX_ATTN_CTAS + S) * L.slot_floats * 4);
+  }
+  if (op == KT_OP_DYNAMIC_REPS) {
+    (void)T;
+    L.dyn = off;
+    L.dyn_bytes = 0;
+    off = align256(off + L.dyn_bytes);
+  }
+  L.total = off;
+  return L;
+}
+
+// ---- TMA tensor maps over the K / V pools ----------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// [rows = pages*heads*128][128 channels] fp16, boxes of 64 channels x 64 rows,
+// 128-byte swizzle (the attention kernel's ldmatrix addressing assumes it).
+bool make_pool_map(CUtensorMap* map, const void* pool, const kt_paged_kv* kv) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)kv->num_pages * kv->num_kv_heads * BS};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(pool), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+kt_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KT_OK : KT_ERR_CUDA; }
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+kt_status select_impl(const void* q, const kt_paged_kv* kv, const void* reps,
+                      const kt_sparse_params* p, int32_t* sel, int32_t* cnt, float* sel_scores,
+                      void* ws, const WsLayout& L, bool trigger, cudaStream_t stream) {
+  SelectLaunch a;
+  a.q = static_cast<const __half*>(q);
+  a.reps = reps;
+  a.table = kv->block_table;
+  a.seq_lens = kv->seq_lens;
+  a.sel = sel;
+  a.cnt = cnt;
+  a.sel_scores = sel_scores;
+  a.status = at<int>(ws, L.status);
+  a.counters = at<int>(ws, L.sel_counters);
+  a.ncand = at<int>(ws, L.sel_ncand);
+  a.cand = at<unsigned long long>(ws, L.sel_cand);
+  a.B = kv->batch;
+  a.H_kv = kv->num_kv_heads;
+  a.G = p->num_q_heads / kv->num_kv_heads;
+  a.max_blocks = kv->max_blocks_per_seq;
+  a.P = kv->num_pages;
+  a.I_b = p->initial_blocks;
+  a.L_b = p->local_blocks;
+  a.top_k = p->top_k;
+  a.rep = p->rep;
+  a.R = reps_rows(p);
+  a.head_mode = p->head_mode;
+  a.plan = L.sel;
+  a.trigger_dependents = trigger;
+  if (a.plan.chunk > SEL_MAX_CHUNK || select_smem_bytes(a) > 227 * 1024) return KT_ERR_UNSUPPORTED;
+  return cuda_status(launch_select(a, stream));
+}
+
+kt_status attn_impl(const void* q, const kt_paged_kv* kv, int num_q_heads, float scale,
+                    const kt_sparse_params* p, const int32_t* sel, const int32_t* cnt, float* out,
+                    void* ws, const WsLayout& L, bool dense, bool pdl, cudaStream_t stream) {
+  CUtensorMap kmap, vmap;
+  if (!make_pool_map(&kmap, kv->k_pool, kv) || !make_pool_map(&vmap, kv->v_pool, kv))
+    return KT_ERR_CUDA;
+  const int sms = num_sms();
+  if (sms <= 0) return KT_ERR_CUDA;
+  AttnLaunch a;
+  a.kmap = &kmap;
+  a.vmap = &vmap;
+  a.q = static_cast<const __half*>(q);
+  a.table = kv->block_table;
+  a.seq_lens = kv->seq_lens;
+  a.sel = sel;
+  a.cnt = cnt;
+  a.out = out;
+  a.status = at<int>(ws, L.status);
+  a.counters = at<int>(ws, L.attn_counters);
+  a.parts = at<float>(ws, L.attn_parts);
+  a.B = kv->batch;
+  a.H_kv = kv->num_kv_heads;
+  a.G = num_q_heads / kv->num_kv_heads;
+  a.max_blocks = kv->max_blocks_per_seq;
+  a.P = kv->num_pages;
+  a.I_b = dense ? 0 : p->initial_blocks;
+  a.L_b = dense ? 1 : p->local_blocks;
+  a.top_k = dense ? 1 : p->top_k;
+  a.SEL = dense ? 1 : (p->head_mode == KT_HEAD_SHARED ? 1 : kv->num_kv_heads);
+  a.dense = dense ? 1 : 0;
+  a.slot_floats = L.slot_floats;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  a.grid = sms < MAX_ATTN_CTAS ? sms : MAX_ATTN_CTAS;
+  a.pdl = pdl;
+  return cuda_status(launch_attention(a, stream));
+}
+
+}  // namespace
+}  // namespace kt
+
+using namespace kt;
+
+extern "C" {
+
+const char* kt_status_string(kt_status s) {
+  switch (s) {
+    case KT_OK: return "ok";
+    case KT_ERR_INVALID_ARG: return "invalid argument";
+    case KT_ERR_UNSUPPORTED: return "unsupported shape or method";
+    case KT_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case KT_ERR_CUDA: return "CUDA error";
+    case KT_ERR_DEVICE_CHECK: return "device-side bounds check failed";
+    case KT_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+int32_t kt_reps_per_block(const kt_sparse_params* p) { return p ? reps_rows(p) : 0; }
+
+size_t kt_reps_pool_bytes(const kt_paged_kv* kv, const kt_sparse_params* p) {
+  if (!kv || !p || kv->num_pages < 1 || kv->num_kv_heads < 1 || kv->head_dim < 1) return 0;
+  const int R = reps_rows(p);
+  if (R <= 0) return 0;
+  const size_t elem = p->rep == KT_REP_MEAN ? 4 : 2;
+  return (size_t)kv->num_pages * kv->num_kv_heads * R * kv->head_dim * elem;
+}
+
+kt_status kt_workspace_bytes(kt_op op, const kt_paged_kv* kv, const kt_sparse_params* p,
+                             int32_t T, size_t* bytes) {
+  if (!bytes) return KT_ERR_INVALID_ARG;
+  if (op < KT_OP_SCORE_SELECT || op > KT_OP_DYNAMIC_REPS) return KT_ERR_INVALID_ARG;
+  kt_status s = check_kv(kv);
+  if (s != KT_OK) return s;
+  if (op == KT_OP_DENSE_ATTN) {
+    if (!p) return KT_ERR_INVALID_ARG;
+    s = check_heads(kv, p->num_q_heads, p->softmax_scale);
+  } else {
+    s = check_params(kv, p);
+  }
+  if (s != KT_OK) return s;
+  if (op == KT_OP_DYNAMIC_REPS && T < 1) return KT_ERR_INVALID_ARG;
+  *bytes = layout(op, kv, p, T).total;
+  return KT_OK;
+}
+
+kt_status kt_workspace_init(void* ws, size_t ws_bytes, kt_stream_t stream) {
+  if (!ws || ws_bytes < 256) return KT_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream));
+}
+
+kt_status kt_build_block_reps(const kt_paged_kv* kv, const kt_sparse_params* p,
+                              int32_t first_block, int32_t num_blocks, void* reps_pool,
+                              kt_stream_t stream) {
+  kt_status s = check_kv(kv);
+  if (s != KT_OK) return s;
+  s = check_params(kv, p);
+  if (s != KT_OK) return s;
+  if (!reps_pool || !aligned16(reps_pool) || first_block < 0 || num_blocks < 0)
+    return KT_ERR_INVALID_ARG;
+  if (p->rep == KT_REP_DYNAMIC) return KT_ERR_INVALID_ARG;  // kt_build_dynamic_reps
+  if (num_blocks == 0) return KT_OK;
+  RepsLaunch a;
+  a.k_pool = static_cast<const __half*>(kv->k_pool);
+  a.table = kv->block_table;
+  a.seq_lens = kv->seq_lens;
+  a.reps = reps_pool;
+  a.B = kv->batch;
+  a.H_kv = kv->num_kv_heads;
+  a.max_blocks = kv->max_blocks_per_seq;
+  a.P = kv->num_pages;
+  a.rep = p->rep;
+  a.R = reps_rows(p);
+  a.fix_stride = p->fix_stride;
+  a.first_block = first_block;
+  const long long last = (long long)first_block + num_blocks;
+  a.num_blocks = (int)((last > kv->max_blocks_per_seq ? kv->max_blocks_per_seq : last) -
+                       first_block);
+  if (a.num_blocks <= 0) return KT_OK;
+  return cuda_status(launch_reps(a, (cudaStream_t)stream));
+}
+
+kt_status kt_build_dynamic_reps(const kt_paged_kv* kv, const kt_sparse_params* p,
+                                const void* q_local, int32_t T, int32_t first_block,
+                                int32_t num_blocks, void* reps_pool, float* token_scores,
+                                void* ws, size_t ws_bytes, kt_stream_t stream) {
+  (void)q_local; (void)T; (void)first_block; (void)num_blocks; (void)reps_pool;
+  (void)token_scores; (void)ws; (void)ws_bytes; (void)stream;
+  kt_status s = check_kv(kv);
+  if (s != KT_OK) return s;
+  s = check_params(kv, p);
+  if (s != KT_OK) return s;
+  return KT_ERR_UNSUPPORTED;
+}
+
+kt_status kt_score_select_blocks(const void* q, const kt_paged_kv* kv, const void* reps_pool,
+                                 const kt_sparse_params* p, int32_t* sel, int32_t* cnt,
+                                 float* sel_scores, void* ws, size_t ws_bytes,
+                                 kt_stream_t stream) {
+  kt_status s = check_kv(kv);
+  if (s != KT_OK) return s;
+  s = check_params(kv, p);
+  if (s != KT_OK) return s;
+  if (!q || !reps_pool || !sel || !cnt || !ws || !aligned16(q) || !aligned16(reps_pool) ||
+      !aligned16(ws))
+    return KT_ERR_INVALID_ARG;
+  const WsLayout L = layout(KT_OP_SCORE_SELECT, kv, p, 0);
+  if (ws_bytes < L.total) return KT_ERR_WORKSPACE_TOO_SMALL;
+  return select_impl(q, kv, reps_pool, p, sel, cnt, sel_scores, ws, L, false,
+                     (cudaStream_t)stream);
+}
+
+kt_status kt_sparse_decode_attn(const void* q, const kt_paged_kv* kv, const kt_sparse_params* p,
+                                const int32_t* sel, const int32_t* cnt, float* out, void* ws,
+                                size_t ws_bytes, kt_stream_t stream) {
+  kt_status s = check_kv(kv);
+  if (s != KT_OK) return s;
+  s = check_params(kv, p);
+  if (s != KT_OK) return s;
+  if (!q || !sel || !cnt || !out || !ws || !aligned16(q) || !aligned16(out) || !aligned16(ws))
+    return KT_ERR_INVALID_ARG;
+  const WsLayout L = layout(KT_OP_SPARSE_ATTN, kv, p, 0);
+  if (ws_bytes < L.total) return KT_ERR_WORKSPACE_TOO_SMALL;
+  return attn_impl(q, kv, p->num_q_heads, p->softmax_scale, p, sel, cnt, out, ws, L, false, false,
+                   (cudaStream_t)stream);
+}
+
+kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void* reps_pool,
+                                const kt_sparse_params* p, int32_t* sel, int32_t* cnt,
+                                float* out, void* ws, size_t ws_bytes, kt_stream_t stream) {
+  kt_status s = check_kv(kv);
+  if (s != KT_OK) return s;
+  s = check_params(kv, p);
+  if (s != KT_OK) return s;
+  if (!q || !reps_pool || !sel || !cnt || !out || !ws || !aligned16(q) ||
+      !aligned16(reps_pool) || !aligned16(out) || !aligned16(ws))
+    return KT_ERR_INVALID_ARG;
+  const WsLayout L = layout(KT_OP_SPARSE_STEP, kv, p, 0);
+  if (ws_bytes < L.total) return KT_ERR_WORKSPACE_TOO_SMALL;
+  s = select_impl(q, kv, reps_pool, p, sel, cnt, nullptr, ws, L, true, (cudaStream_t)stream);
+  if (s != KT_OK) return s;
+  return attn_impl(q, kv, p->num_q_heads, p->softmax_scale, p, sel, cnt, out, ws, L, false, true,
+                   (cudaStream_t)stream);
+}
+
+kt_status kt_sparse_decode_step_host(const void* q_host, void* q_dev, const kt_paged_kv* kv,
+                                     const void* reps_pool, const kt_sparse_params* p,
+                                     int32_t* sel, int32_t* cnt, float* out_dev,
+                                     float* out_host, void* ws, size_t ws_bytes,
+                                     kt_stream_t stream) {
+  kt_status s = check_kv(kv);
+  if (s != KT_OK) return s;
+  s = check_params(kv, p);
+  if (s != KT_OK) return s;
+  if (!q_host || !out_host) return KT_ERR_INVALID_ARG;
+  const size_t qbytes = (size_t)kv->batch * p->num_q_heads * D * 2;
+  const size_t obytes = (size_t)kv->batch * p->num_q_heads * D * 4;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (!q_dev || !out_dev) return KT_ERR_INVALID_ARG;
+  if (cudaMemcpyAsync(q_dev, q_host, qbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return KT_ERR_CUDA;
+  s = kt_sparse_decode_step(q_dev, kv, reps_pool, p, sel, cnt, out_dev, ws, ws_bytes, stream);
+  if (s != KT_OK) return s;
+  if (cudaMemcpyAsync(out_host, out_dev, obytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return KT_ERR_CUDA;
+  return cuda_status(cudaStreamSynchronize(st));
+}
+
+kt_status kt_dense_decode_attn(const void* q, const kt_paged_kv* kv, int32_t num_q_heads,
+                               float softmax_scale, float* out, void* ws, size_t ws_bytes,
+                               kt_stream_t stream) {
+  kt_status s = check_kv(kv);
+  if (s != KT_OK) return s;
+  s = check_heads(kv, num_q_heads, softmax_scale);
+  if (s != KT_OK) return s;
+  if (!q || !out || !ws || !aligned16(q) || !aligned16(out) || !aligned16(ws))
+    return KT_ERR_INVALID_ARG;
+  kt_sparse_params p;
+  std::memset(&p, 0, sizeof(p));
+  p.num_q_heads = num_q_heads;
+  p.softmax_scale = softmax_scale;
+  p.top_k = 1;
+  p.local_blocks = 1;
+  const WsLayout L = layout(KT_OP_DENSE_ATTN, kv, &p, 0);
+  if (ws_bytes < L.total) return KT_ERR_WORKSPACE_TOO_SMALL;
+  return attn_impl(q, kv, num_q_heads, softmax_scale, &p, nullptr, nullptr, out, ws, L, true,
+                   false, (cudaStream_t)stream);
+}
+
+kt_status kt_read_device_status(void* ws, size_t ws_bytes, kt_stream_t stream,
+                                int32_t* device_status) {
+  if (!ws || ws_bytes < 256 || !device_status) return KT_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KT_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return KT_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(v), st) != cudaSuccess) return KT_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KT_ERR_CUDA;
+  *device_status = v;
+  return KT_OK;
+}
+
+kt_status kt_selftest_bounded_wait(void* ws, size_t ws_bytes, int32_t spin_limit,
+                                   kt_stream_t stream) {
+  if (!ws || ws_bytes < 256 || spin_limit < 1) return KT_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_selftest_wait(static_cast<int*>(ws), spin_limit, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,275 @@
+// kt_internal.cuh — constants, workspace layout and sm_103a device helpers
+// shared by the libkt translation units (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kt.h"
+
+namespace kt {
+
+constexpr int D = 128;              // head_dim
+constexpr int BS = 128;             // tokens per KV block
+constexpr int MAX_G = 8;            // query heads per KV head
+constexpr int MAX_SEGS = 2048;      // batch * num_kv_heads
+constexpr int MAX_TOPK = 1024;
+constexpr int MAX_ATTN_CTAS = 1024; // workspace is sized for this many attention CTAs
+constexpr int SEL_TARGET_CTAS = 1024;
+constexpr int SEL_MAX_CAND = 8192;  // candidates merged by the last selection CTA
+constexpr int SEL_MAX_CHUNK = 4096; // context blocks scored by one selection CTA
+constexpr int MAX_DYN_REPS = 32;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s bound on any device-side wait
+
+// ---------------------------------------------------------------------------
+// Selection chunking and workspace layout.  Host sizing and device addressing
+// use this one description.  All regions are 256-byte aligned.
+// ---------------------------------------------------------------------------
+struct SelPlan {
+  int SEL;      // selection units per sequence (1 or H_kv)
+  int max_ctx;  // upper bound on Context blocks of a sequence
+  int chunk;    // Context blocks scored by one CTA
+  int nchunks;  // CTAs per unit
+  int kk;       // candidates kept per chunk
+};
+
+struct WsLayout {
+  size_t status;         // int32 status word, 256 B header
+  size_t sel_counters;   // int32 [B*SEL]
+  size_t sel_ncand;      // int32 [B*SEL*nchunks]
+  size_t sel_cand;       // uint64 [B*SEL*nchunks*kk]
+  size_t attn_counters;  // int32 [S]
+  size_t attn_parts;     // float [2*(MAX_ATTN_CTAS+S)][slot_floats]
+  size_t dyn;            // dynamic-rep scratch
+  size_t dyn_bytes;
+  size_t total;
+  int slot_floats;
+  SelPlan sel;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline int ceil_div_i(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+inline SelPlan make_sel_plan(int B, int H_kv, int max_blocks, int I, int L, int top_k,
+                             int head_mode) {
+  SelPlan s;
+  s.SEL = head_mode == KT_HEAD_SHARED ? 1 : H_kv;
+  const int mc = max_blocks - I - L;
+  s.max_ctx = mc > 0 ? mc : 0;
+  const long long total = (long long)B * s.SEL * (s.max_ctx > 0 ? s.max_ctx : 1);
+  int ch = ceil_div_i(total, SEL_TARGET_CTAS);
+  if (ch < 8) ch = 8;
+  int nch = s.max_ctx > 0 ? ceil_div_i(s.max_ctx, ch) : 1;
+  int kk = top_k < ch ? top_k : ch;
+  if ((long long)nch * kk > SEL_MAX_CAND) {
+    // larger chunks so that nchunks * top_k candidates fit the merge buffer
+    ch = ceil_div_i(s.max_ctx, SEL_MAX_CAND / (top_k > 0 ? top_k : 1));
+    if (ch < 8) ch = 8;
+    nch = ceil_div_i(s.max_ctx, ch);
+    kk = top_k < ch ? top_k : ch;
+  }
+  s.chunk = ch;
+  s.nchunks = nch;
+  s.kk = kk;
+  return s;
+}
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+__device__ __forceinline__ void set_status(int* st, int code) {
+  if (st) atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for phase `parity` of the barrier; gives up after WAIT_LIMIT_NS of
+// global time, records KT_ERR_TIMEOUT and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0 && globaltimer() - t0 > WAIT_LIMIT_NS) {
+      set_status(status, KT_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 2-D tiled TMA load (global -> shared), completion counted on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                            int32_t y, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// Untiled bulk copy (global -> shared); 16-byte aligned addresses and size.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                        uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                          uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D = A * B + D, m16n8k16, fp16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
+  return static_cast<uint32_t>(__half_as_ushort(lo)) |
+         (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+}
+
+// Order-preserving map float -> uint32 (larger float, larger key; -0 == +0).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  if (f == 0.0f) f = 0.0f;
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_float(uint32_t k) {
+  const uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+  return __uint_as_float(u);
+}
+
+#endif  // __CUDACC__
+
+// ---------------------------------------------------------------------------
+// Launch entry points implemented in the kernel translation units.
+// ---------------------------------------------------------------------------
+struct AttnLaunch {
+  const CUtensorMap* kmap;
+  const CUtensorMap* vmap;
+  const __half* q;
+  const int32_t* table;
+  const int32_t* seq_lens;
+  const int32_t* sel;
+  const int32_t* cnt;
+  float* out;
+  int* status;
+  int* counters;
+  float* parts;
+  int B, H_kv, G, max_blocks, P, I_b, L_b, top_k, SEL, dense, slot_floats;
+  float scale_log2;
+  int grid;
+  bool pdl;  // launched as a programmatic dependent of the previous kernel
+};
+cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream);
+
+struct SelectLaunch {
+  const __half* q;
+  const void* reps;
+  const int32_t* table;
+  const int32_t* seq_lens;
+  int32_t* sel;
+  int32_t* cnt;
+  float* sel_scores;
+  int* status;
+  int* counters;
+  int* ncand;
+  unsigned long long* cand;
+  int B, H_kv, G, max_blocks, P, I_b, L_b, top_k, rep, R, head_mode;
+  SelPlan plan;
+  bool trigger_dependents;
+};
+cudaError_t launch_select(const SelectLaunch& a, cudaStream_t stream);
+size_t select_smem_bytes(const SelectLaunch& a);
+
+struct RepsLaunch {
+  const __half* k_pool;
+  const int32_t* table;
+  const int32_t* seq_lens;
+  void* reps;
+  int B, H_kv, max_blocks, P, rep, R, fix_stride, first_block, num_blocks;
+};
+cudaError_t launch_reps(const RepsLaunch& a, cudaStream_t stream);
+
+cudaError_t launch_selftest_wait(int* status, int spin_limit, cudaStream_t stream);
+
+}  // namespace kt

@@ -1,0 +1,440 @@
+// select.cu — block scoring and deterministic top-k selection.
+//
+// For each selection unit (a sequence and, in SEPARATE mode, one KV head) every
+// Context block gets a unit score and the top-k blocks are chosen (article
+// "KTransformers 长上下文稀疏注意力实战…": Quest bound §3.1, similarity to the
+// representative tokens §4.3, top-k and head_select_mode §4.5).
+//
+//   head score   Quest      sum_c max(q_c kmax_c, q_c kmin_c)
+//                Max/Mean   q . rep
+//                Fix/Dyn    max_r q . rep_r
+//   unit score   sum of head scores over the unit's query heads
+//
+// Linear methods (Max, Mean, Quest) fold the query heads of a KV head into one
+// weight vector per representative row: for Quest max(q kmax, q kmin) equals
+// relu(q) kmax + min(q, 0) kmin exactly (kmax >= kmin), so the unit score is a
+// single dot product of the block's representative bytes with a precomputed
+// fp32 weight vector.  Fix and Dynamic keep per-head dot products.
+//
+// Grid (chunks, units, batch): each CTA scores a chunk of Context blocks, keeps
+// its chunk's top-k with a radix select over 64-bit keys
+// (score-order bits << 32 | ~block), and the CTA that takes the unit's last
+// ticket merges all chunk candidates, sorts the chosen blocks by id and writes
+// sel / cnt / sel_scores.  Ties go to the lower block id; the result does not
+// depend on CTA timing.
+#include "kt_internal.cuh"
+
+namespace kt {
+namespace {
+
+constexpr int THREADS = 256;
+constexpr int WARPS = THREADS / 32;
+
+struct Params {
+  const __half* q;
+  const void* reps;
+  const int32_t* table;
+  const int32_t* seq_lens;
+  int32_t* sel;
+  int32_t* cnt;
+  float* sel_scores;
+  int* status;
+  int* counters;
+  int* ncand;
+  unsigned long long* cand;
+  int B, H_kv, G, max_blocks, P, I_b, L_b, top_k, rep, R, head_mode;
+  int SEL, chunk, nchunks, kk;
+  int trigger;
+};
+
+__device__ __forceinline__ float dot8(const float* w, uint4 v) {
+  const __half2* h = reinterpret_cast<const __half2*>(&v);
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(h[i]);
+    s = fmaf(w[2 * i], f.x, s);
+    s = fmaf(w[2 * i + 1], f.y, s);
+  }
+  return s;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long make_key(float score, int block) {
+  return (static_cast<unsigned long long>(float_key(score)) << 32) |
+         static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(block));
+}
+
+// k-th largest of N distinct keys in shared memory (1 <= k <= N), all threads
+// of the CTA.  On return, a key is among the k largest iff
+// (key & *mask_out) >= *prefix_out.
+__device__ void radix_select(const unsigned long long* keys, int N, int k, unsigned int* hist,
+                             unsigned long long* sh_u64, int* sh_int,
+                             unsigned long long* prefix_out, unsigned long long* mask_out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned long long prefix = 0ull, mask = 0ull;
+  int need = k;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += THREADS) hist[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < N; i += THREADS) {
+      const unsigned long long key = keys[i];
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l holds digits 255-8l .. 248-8l (descending)
+      unsigned int c[8];
+      unsigned int local = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = hist[255 - 8 * lane - i];
+        local += c[i];
+      }
+      unsigned int incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const unsigned int excl = incl - local;
+      const bool hit = excl < (unsigned)need && (unsigned)need <= incl;
+      const unsigned int ball = __ballot_sync(0xffffffffu, hit);
+      const int src = __ffs(ball) - 1;
+      if (lane == src) {
+        unsigned int above = excl;
+        int digit = 0;
+        unsigned int bin = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (above + c[i] >= (unsigned)need) {
+            digit = 255 - 8 * lane - i;
+            bin = c[i];
+            break;
+          }
+          above += c[i];
+        }
+        const int need2 = need - (int)above;
+        sh_u64[0] = prefix | (static_cast<unsigned long long>(digit) << shift);
+        sh_u64[1] = mask | (0xFFull << shift);
+        sh_int[0] = need2;
+        sh_int[1] = (bin == (unsigned)need2) ? 1 : 0;
+      }
+    }
+    __syncthreads();
+    prefix = sh_u64[0];
+    mask = sh_u64[1];
+    need = sh_int[0];
+    const int done = sh_int[1];
+    __syncthreads();
+    if (done) break;
+  }
+  *prefix_out = prefix;
+  *mask_out = mask;
+}
+
+__global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ unsigned int hist[256];
+  __shared__ unsigned long long sh_u64[2];
+  __shared__ int sh_int[4];
+
+  if (p.trigger) griddep_launch_dependents();
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int chunk = blockIdx.x, u = blockIdx.y, b = blockIdx.z;
+  const int H_q = p.H_kv * p.G;
+  const int nkv = p.head_mode == KT_HEAD_SHARED ? p.H_kv : 1;  // KV heads in the unit
+  const int g0 = p.head_mode == KT_HEAD_SHARED ? 0 : u;
+  const bool linear = p.rep == KT_REP_MAX || p.rep == KT_REP_MEAN || p.rep == KT_REP_QUEST;
+  const int Rw = p.rep == KT_REP_QUEST ? 2 : 1;  // weight rows for linear methods
+
+  int n = p.seq_lens[b];
+  if (n < 0 || n > p.max_blocks * BS) {
+    set_status(p.status, KT_ERR_DEVICE_CHECK);
+    n = n < 0 ? 0 : p.max_blocks * BS;
+  }
+  const int nb = (n + BS - 1) / BS;
+  const int c0 = min(p.I_b, nb), c1 = max(c0, nb - p.L_b);
+  const int js = c0 + chunk * p.chunk, je = min(js + p.chunk, c1);
+  const int nloc = max(0, je - js);
+
+  // shared memory: weights (fp32) then keys (u64)
+  float* wts = reinterpret_cast<float*>(smem);
+  const int wfloats = linear ? nkv * Rw * D : (p.head_mode == KT_HEAD_SHARED ? H_q : p.G) * D;
+  unsigned long long* keys =
+      reinterpret_cast<unsigned long long*>(smem + ((wfloats * 4 + 15) & ~15));
+
+  const size_t unit_base = (size_t)b * p.SEL + u;
+  unsigned long long* my_cand = p.cand + (unit_base * p.nchunks + chunk) * p.kk;
+
+  if (nloc > 0) {
+    // ---- weights (query heads summed in ascending order)
+    for (int i = tid; i < wfloats; i += THREADS) {
+      if (linear) {
+        const int gi = i / (Rw * D), r = (i / D) % Rw, c = i % D;
+        const int g = g0 + gi;
+        float acc = 0.0f;
+        for (int hh = 0; hh < p.G; ++hh) {
+          const float qv = __half2float(p.q[((size_t)b * H_q + g * p.G + hh) * D + c]);
+          if (p.rep == KT_REP_QUEST)
+            acc += (r == 0) ? fminf(qv, 0.0f) : fmaxf(qv, 0.0f);
+          else
+            acc += qv;
+        }
+        wts[i] = acc;
+      } else {
+        const int hq = (p.head_mode == KT_HEAD_SHARED ? 0 : g0 * p.G) + i / D;
+        wts[i] = __half2float(p.q[((size_t)b * H_q + hq) * D + i % D]);
+      }
+    }
+    __syncthreads();
+
+    // ---- scores
+    if (linear) {
+      // the rep bytes of the unit's KV heads for one block are contiguous
+      const int elems = nkv * p.R * D;  // R == Rw here
+      const bool f32 = p.rep == KT_REP_MEAN;
+      const int vec_elems = f32 ? 4 : 8;
+      const int V = elems / vec_elems;  // 16-byte vectors per block
+      for (int j0 = js + warp * 4; j0 < je; j0 += WARPS * 4) {
+        int page[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int j = j0 + k;
+          page[k] = (j < je) ? p.table[(size_t)b * p.max_blocks + j] : -1;
+          if (j < je && (page[k] < 0 || page[k] >= p.P)) {
+            set_status(p.status, KT_ERR_DEVICE_CHECK);
+            page[k] = -2;
+          }
+        }
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int v0 = 0; v0 < V; v0 += 32) {
+          const int v = v0 + lane;
+          uint4 x[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            x[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (page[k] >= 0 && v < V) {
+              const uint4* src = reinterpret_cast<const uint4*>(
+                  static_cast<const uint8_t*>(p.reps) +
+                  ((size_t)page[k] * p.H_kv + g0) * p.R * D * (f32 ? 4 : 2));
+              x[k] = __ldg(src + v);
+            }
+          }
+          if (v < V) {
+            const float* w = wts + v * vec_elems;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              if (f32) {
+                const float4 f = *reinterpret_cast<const float4*>(&x[k]);
+                acc[k] = fmaf(w[0], f.x, acc[k]);
+                acc[k] = fmaf(w[1], f.y, acc[k]);
+                acc[k] = fmaf(w[2], f.z, acc[k]);
+                acc[k] = fmaf(w[3], f.w, acc[k]);
+              } else {
+                acc[k] += dot8(w, x[k]);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float s = warp_sum(acc[k]);
+          const int j = j0 + k;
+          if (lane == 0 && j < je) keys[j - js] = make_key(page[k] == -2 ? -INFINITY : s, j);
+        }
+      }
+    } else {
+      // Fix / Dynamic: per KV head, per query head, max over reps of q.rep;
+      // lane owns channels 4*lane .. 4*lane+3.
+      for (int j = js + warp; j < je; j += WARPS) {
+        const int page = p.table[(size_t)b * p.max_blocks + j];
+        float total = 0.0f;
+        if (page < 0 || page >= p.P) {
+          set_status(p.status, KT_ERR_DEVICE_CHECK);
+          total = -INFINITY;
+        } else {
+          for (int gi = 0; gi < nkv; ++gi) {
+            const int g = g0 + gi;
+            const __half* rp =
+                static_cast<const __half*>(p.reps) + ((size_t)page * p.H_kv + g) * p.R * D;
+            for (int hh = 0; hh < p.G; ++hh) {
+              const float* w =
+                  wts + ((p.head_mode == KT_HEAD_SHARED ? g * p.G : 0) + hh) * D + 4 * lane;
+              float best = -INFINITY;
+              for (int r = 0; r < p.R; ++r) {
+                const uint2 raw = __ldg(reinterpret_cast<const uint2*>(rp + r * D) + lane);
+                const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+                const float2 f0 = __half22float2(h2[0]), f1 = __half22float2(h2[1]);
+                float s = w[0] * f0.x;
+                s = fmaf(w[1], f0.y, s);
+                s = fmaf(w[2], f1.x, s);
+                s = fmaf(w[3], f1.y, s);
+                s = warp_sum(s);
+                best = fmaxf(best, s);
+              }
+              total += best;
+            }
+          }
+        }
+        if (lane == 0) keys[j - js] = make_key(total, j);
+      }
+    }
+    __syncthreads();
+
+    // ---- this chunk's top-kk candidates
+    if (nloc <= p.kk) {
+      for (int i = tid; i < nloc; i += THREADS) my_cand[i] = keys[i];
+    } else {
+      unsigned long long prefix, mask;
+      radix_select(keys, nloc, p.kk, hist, sh_u64, sh_int, &prefix, &mask);
+      if (tid == 0) sh_int[2] = 0;
+      __syncthreads();
+      for (int i = tid; i < nloc; i += THREADS) {
+        const unsigned long long key = keys[i];
+        if ((key & mask) >= prefix) {
+          const int pos = atomicAdd(&sh_int[2], 1);
+          if (pos < p.kk) my_cand[pos] = key; else set_status(p.status, KT_ERR_DEVICE_CHECK);
+        }
+      }
+    }
+  }
+  if (tid == 0) p.ncand[unit_base * p.nchunks + chunk] = min(nloc, p.kk);
+
+  // ---- ticket: the last chunk CTA of this unit merges
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int old = atomicAdd(p.counters + unit_base, 1);
+    sh_int[3] = (old == p.nchunks - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!sh_int[3]) return;
+  __threadfence();
+
+  // gather every candidate of the unit (chunk order) into shared memory
+  unsigned long long* all = keys;
+  if (tid == 0) {
+    int tot = 0;
+    for (int c = 0; c < p.nchunks; ++c) tot += __ldcg(p.ncand + unit_base * p.nchunks + c);
+    sh_int[0] = tot;
+  }
+  __syncthreads();
+  const int total = sh_int[0];
+  __syncthreads();
+  for (int c = warp; c < p.nchunks; c += WARPS) {
+    const int nc = __ldcg(p.ncand + unit_base * p.nchunks + c);
+    int off = 0;
+    for (int c2 = lane; c2 < c; c2 += 32) off += __ldcg(p.ncand + unit_base * p.nchunks + c2);
+    off = warp_sum_int(off);
+    for (int i = lane; i < nc; i += 32)
+      all[off + i] = __ldcg(p.cand + (unit_base * p.nchunks + c) * p.kk + i);
+  }
+  __syncthreads();
+
+  const int keff = min(p.top_k, total);
+  unsigned long long* chosen = all + total;  // keff entries
+  if (keff > 0) {
+    if (keff == total) {
+      for (int i = tid; i < total; i += THREADS) chosen[i] = all[i];
+    } else {
+      unsigned long long prefix, mask;
+      radix_select(all, total, keff, hist, sh_u64, sh_int, &prefix, &mask);
+      if (tid == 0) sh_int[2] = 0;
+      __syncthreads();
+      for (int i = tid; i < total; i += THREADS) {
+        const unsigned long long key = all[i];
+        if ((key & mask) >= prefix) {
+          const int pos = atomicAdd(&sh_int[2], 1);
+          if (pos < keff) chosen[pos] = key; else set_status(p.status, KT_ERR_DEVICE_CHECK);
+        }
+      }
+    }
+    __syncthreads();
+    // ascending block order: rank by counting
+    int32_t* sel_out = p.sel + unit_base * p.top_k;
+    float* sc_out = p.sel_scores ? p.sel_scores + unit_base * p.top_k : nullptr;
+    for (int i = tid; i < keff; i += THREADS) {
+      const unsigned long long ki = chosen[i];
+      const uint32_t id = 0xFFFFFFFFu - static_cast<uint32_t>(ki & 0xFFFFFFFFull);
+      int rank = 0;
+      for (int m = 0; m < keff; ++m) {
+        const uint32_t idm = 0xFFFFFFFFu - static_cast<uint32_t>(chosen[m] & 0xFFFFFFFFull);
+        rank += idm < id ? 1 : 0;
+      }
+      sel_out[rank] = static_cast<int32_t>(id);
+      if (sc_out) sc_out[rank] = key_float(static_cast<uint32_t>(ki >> 32));
+    }
+  }
+  if (tid == 0) {
+    p.cnt[unit_base] = keff;
+    p.counters[unit_base] = 0;
+  }
+}
+
+}  // namespace
+
+size_t select_smem_bytes(const SelectLaunch& a) {
+  const bool linear = a.rep == KT_REP_MAX || a.rep == KT_REP_MEAN || a.rep == KT_REP_QUEST;
+  const int nkv = a.head_mode == KT_HEAD_SHARED ? a.H_kv : 1;
+  const int Rw = a.rep == KT_REP_QUEST ? 2 : 1;
+  const int wfloats =
+      linear ? nkv * Rw * D : (a.head_mode == KT_HEAD_SHARED ? a.H_kv * a.G : a.G) * D;
+  const int chunk_keys = a.plan.chunk;
+  const int merged = a.plan.nchunks * a.plan.kk;
+  const int merge_keys = merged + (a.top_k < merged ? a.top_k : merged);
+  const int nkeys = chunk_keys > merge_keys ? chunk_keys : merge_keys;
+  return (size_t)((wfloats * 4 + 15) & ~15) + (size_t)nkeys * 8;
+}
+
+cudaError_t launch_select(const SelectLaunch& a, cudaStream_t stream) {
+  Params p;
+  p.q = a.q;
+  p.reps = a.reps;
+  p.table = a.table;
+  p.seq_lens = a.seq_lens;
+  p.sel = a.sel;
+  p.cnt = a.cnt;
+  p.sel_scores = a.sel_scores;
+  p.status = a.status;
+  p.counters = a.counters;
+  p.ncand = a.ncand;
+  p.cand = a.cand;
+  p.B = a.B;
+  p.H_kv = a.H_kv;
+  p.G = a.G;
+  p.max_blocks = a.max_blocks;
+  p.P = a.P;
+  p.I_b = a.I_b;
+  p.L_b = a.L_b;
+  p.top_k = a.top_k;
+  p.rep = a.rep;
+  p.R = a.R;
+  p.head_mode = a.head_mode;
+  p.SEL = a.plan.SEL;
+  p.chunk = a.plan.chunk;
+  p.nchunks = a.plan.nchunks;
+  p.kk = a.plan.kk;
+  p.trigger = a.trigger_dependents ? 1 : 0;
+  const size_t smem = select_smem_bytes(a);
+  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)(smem > 48 * 1024 ? smem : 48 * 1024));
+  if (e != cudaSuccess) return e;
+  const dim3 grid(a.plan.nchunks, a.plan.SEL, a.B);
+  select_kernel<<<grid, THREADS, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kt

@@ -1,0 +1,279 @@
+/*
+ * kt.h — C ABI of libkt: block-sparse long-context decode attention on GB300.
+ *
+ * The method (KTransformers long-context sparse attention; article
+ * "KTransformers 长上下文稀疏注意力实战：单张 24GB GPU 跑通 1M Token KVCache 的完整方案",
+ * cited below as [LC §N]) keeps the whole KV cache, cut into fixed-size blocks,
+ * and for each decode step attends to:
+ *   - the Initial blocks at the head of the sequence          [LC §4.2]
+ *   - the top-k Context blocks, ranked by representative keys [LC §4.3, §3.1]
+ *   - the Local window at the tail                            [LC §4.2]
+ * with exact softmax attention over that token set            [LC §4.6].
+ * Parameter names follow the attention constructor and YAML keys of
+ * "How to Implement Long Context Inference (Up to 139K Tokens) with
+ * KTransformers" (Step 1, Step 3) and the parameter list of [LC §4.5].
+ *
+ * Conventions for every call:
+ *   - All array pointers are DEVICE pointers unless a comment says otherwise.
+ *     The caller owns every buffer, the workspace and the stream; the library
+ *     never allocates or frees memory and never synchronises, except
+ *     kt_read_device_status, kt_workspace_init (which only memsets) and the
+ *     host-buffer convenience call kt_sparse_decode_step_host.
+ *   - Calls are asynchronous: they validate their arguments on the host, launch
+ *     on `stream` and return.  An invalid argument returns an error before any
+ *     launch and has no side effect.  A failed launch returns KT_ERR_CUDA.
+ *   - Device-side anomalies (a block-table entry outside the pool, a selected
+ *     block outside the context range, a wait that ran out) never trap: the
+ *     kernel records a kt_status code in the workspace's status word, skips the
+ *     affected work and returns.  Read it with kt_read_device_status.
+ *   - Element types: keys/values/queries are IEEE binary16 ("fp16"); outputs and
+ *     Mean representatives are binary32.
+ *   - Supported shapes: head_dim == 128, block_size == 128, num_q_heads a
+ *     multiple of num_kv_heads with a group size G = num_q_heads/num_kv_heads
+ *     of at most 8, batch * num_kv_heads <= 2048.  Other values return
+ *     KT_ERR_UNSUPPORTED.
+ *   - Alignment: every pointer must be 16-byte aligned (fp16 rows are 256 B).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ */
+#ifndef KT_H_
+#define KT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kt_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  KT_OK = 0,
+  KT_ERR_INVALID_ARG = 1,        /* null pointer, negative size, misaligned pointer */
+  KT_ERR_UNSUPPORTED = 2,        /* valid but outside the supported shapes/methods */
+  KT_ERR_WORKSPACE_TOO_SMALL = 3,
+  KT_ERR_CUDA = 4,               /* a CUDA runtime call or launch failed */
+  KT_ERR_DEVICE_CHECK = 5,       /* device-side bounds check failed (work skipped) */
+  KT_ERR_TIMEOUT = 6             /* a device-side bounded wait ran out */
+} kt_status;
+
+/* Representative-token methods [LC §4.3 table; Quest: §3.1]. */
+typedef enum {
+  KT_REP_MAX = 0,     /* per-channel max of the block's keys: 1 fp16 row */
+  KT_REP_MEAN = 1,    /* per-channel exact mean, rounded once: 1 fp32 row */
+  KT_REP_QUEST = 2,   /* per-channel min (row 0) and max (row 1): 2 fp16 rows */
+  KT_REP_FIX = 3,     /* key rows at offsets 0, s, 2s, ...: 128/s fp16 rows */
+  KT_REP_DYNAMIC = 4  /* key rows of the num_reps best-scored tokens, token order */
+} kt_rep_method;
+
+/* head_select_mode [LC §4.5]. */
+typedef enum {
+  KT_HEAD_SHARED = 0,   /* all query heads select one block set jointly */
+  KT_HEAD_SEPARATE = 1  /* each KV head selects for its own query-head group */
+} kt_head_mode;
+
+/* Operations whose workspace size kt_workspace_bytes reports. */
+typedef enum {
+  KT_OP_SCORE_SELECT = 0,
+  KT_OP_SPARSE_ATTN = 1,
+  KT_OP_DENSE_ATTN = 2,
+  KT_OP_SPARSE_STEP = 3,   /* score/select + sparse attention in one call */
+  KT_OP_DYNAMIC_REPS = 4
+} kt_op;
+
+/*
+ * Paged KV cache [LC §4.3: the context is cut into fixed-size blocks].
+ *   k_pool, v_pool : fp16 [num_pages][num_kv_heads][block_size][head_dim];
+ *                    each (page, kv head) slab is contiguous.
+ *   block_table    : int32 [batch][max_blocks_per_seq]; logical block j of
+ *                    sequence b lives in page block_table[b][j].  Only entries
+ *                    j < ceil(seq_lens[b] / block_size) are read.
+ *   seq_lens       : int32 [batch]; tokens cached for each sequence (the decode
+ *                    query attends to all of them, the current token included).
+ * Pool rows past seq_lens[b] in the last page may hold any finite values.
+ */
+typedef struct {
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int32_t batch;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t max_blocks_per_seq;
+  int32_t num_pages;
+} kt_paged_kv;
+
+/*
+ * Selection parameters [LC §4.5; YAML keys of the "How to Implement..." page,
+ * Step 1].
+ *   num_q_heads    : query heads; head h reads KV head h / G.
+ *   initial_blocks : Initial part, in blocks, always attended [LC §4.2].
+ *   local_blocks   : Local window, in blocks (local_windows_len / block_size),
+ *                    counted back from the last (possibly partial) block; >= 1.
+ *   top_k          : second_select_num: context blocks selected per unit, 1..1024.
+ *   num_reps       : anchor_num: reps per block for KT_REP_DYNAMIC (1..32).
+ *   fix_stride     : token interval for KT_REP_FIX; divides block_size.
+ *   rep            : kt_rep_method (anchor_type).
+ *   head_mode      : kt_head_mode (head_select_mode).
+ *   softmax_scale  : attention scale, normally 1/sqrt(head_dim) [LC §3.2].
+ * When ceil(n/block_size) <= initial_blocks + local_blocks there is no Context
+ * part and every block is attended.
+ */
+typedef struct {
+  int32_t num_q_heads;
+  int32_t initial_blocks;
+  int32_t local_blocks;
+  int32_t top_k;
+  int32_t num_reps;
+  int32_t fix_stride;
+  int32_t rep;
+  int32_t head_mode;
+  float softmax_scale;
+} kt_sparse_params;
+
+/* Human-readable name of a status code (static string). */
+const char* kt_status_string(kt_status s);
+
+/* Representative rows per block for `p` (1, 2, block_size/fix_stride or num_reps);
+ * 0 for an invalid method. */
+int32_t kt_reps_per_block(const kt_sparse_params* p);
+
+/*
+ * Bytes of the representative pool for `kv`/`p`: layout
+ * [num_pages][num_kv_heads][R][head_dim], fp16 (fp32 for KT_REP_MEAN).
+ * Returns 0 for invalid arguments.
+ */
+size_t kt_reps_pool_bytes(const kt_paged_kv* kv, const kt_sparse_params* p);
+
+/*
+ * Workspace bytes needed by `op` for these shapes (host-only computation; no
+ * device is touched).  T is the number of local queries for
+ * KT_OP_DYNAMIC_REPS and is ignored otherwise.  The workspace holds the device
+ * status word, cross-CTA candidate lists, tickets and split-K partials.  It must
+ * be zero-filled before its first use (kt_workspace_init); every call leaves it
+ * ready for the next.  Calls that share one workspace must not overlap on the
+ * GPU (issue them on one stream).
+ */
+kt_status kt_workspace_bytes(kt_op op, const kt_paged_kv* kv, const kt_sparse_params* p,
+                             int32_t T, size_t* bytes);
+
+/* Zero-fills the workspace on `stream` (cudaMemsetAsync). */
+kt_status kt_workspace_init(void* ws, size_t ws_bytes, kt_stream_t stream);
+
+/*
+ * Build representatives of logical blocks [first_block, first_block+num_blocks)
+ * of every sequence, for rep in {MAX, MEAN, QUEST, FIX} [LC §4.3 table,
+ * Quest: §3.1].  Only full blocks are built (partial tail blocks are always in
+ * the Local window and never scored).  Results are written per physical page:
+ * reps_pool[block_table[b][j]][kv_head][r][:].  Max/min are exact fp16 values
+ * under the binary16 total order (-0 < +0); Mean is the exact per-channel mean
+ * rounded once to fp32.  Reads K once (HBM-bound).  The device status word is
+ * not available to this call (it takes no workspace); a block-table entry
+ * outside the pool is skipped.
+ */
+kt_status kt_build_block_reps(const kt_paged_kv* kv, const kt_sparse_params* p,
+                              int32_t first_block, int32_t num_blocks, void* reps_pool,
+                              kt_stream_t stream);
+
+/*
+ * Dynamic representatives [LC §4.3 "Dynamic": accumulated attention score per
+ * token, top-k tokens per block].  q_local: fp16 [batch][T][num_q_heads][128],
+ * the queries of the last T positions n-T..n-1 of each sequence.  The score of
+ * token t for KV head h is the sum, over those T positions and the G query heads
+ * of h, of softmax(q . k * softmax_scale) where position pos sees tokens 0..pos.
+ * The p->num_reps best tokens of each full block in [first_block, first_block +
+ * num_blocks) (ties: lower index) become its reps, in token order.
+ * token_scores (nullable): fp32 [batch][num_kv_heads][max_blocks_per_seq*128],
+ * the accumulated scores (entries past seq_lens[b] are zero).
+ */
+kt_status kt_build_dynamic_reps(const kt_paged_kv* kv, const kt_sparse_params* p,
+                                const void* q_local, int32_t T, int32_t first_block,
+                                int32_t num_blocks, void* reps_pool, float* token_scores,
+                                void* ws, size_t ws_bytes, kt_stream_t stream);
+
+/*
+ * Score every Context block and select the top-k per unit [LC §3.1 Quest bound,
+ * §4.3 similarity to reps, §4.5 top-k and head_select_mode].
+ *   q          : fp16 [batch][num_q_heads][128], the decode queries.
+ *   reps_pool  : as written by kt_build_block_reps / kt_build_dynamic_reps.
+ *   sel        : int32 [batch][SEL][top_k], SEL = 1 (SHARED) or num_kv_heads;
+ *                the first cnt entries hold the chosen logical block ids in
+ *                ascending order; the rest are left untouched.
+ *   cnt        : int32 [batch][SEL] = min(top_k, number of Context blocks).
+ *   sel_scores : fp32 [batch][SEL][top_k] or NULL; the unit score of each
+ *                chosen block, aligned with sel.
+ * Head score: Quest sum_c max(q_c kmax_c, q_c kmin_c); Max/Mean q.rep;
+ * Fix/Dynamic max_r q.rep_r.  Unit score: sum of head scores over the unit's
+ * query heads (all heads for SHARED, the G heads of the KV head for SEPARATE).
+ * Order: score descending, then block id ascending (deterministic).
+ */
+kt_status kt_score_select_blocks(const void* q, const kt_paged_kv* kv, const void* reps_pool,
+                                 const kt_sparse_params* p, int32_t* sel, int32_t* cnt,
+                                 float* sel_scores, void* ws, size_t ws_bytes,
+                                 kt_stream_t stream);
+
+/*
+ * Exact attention over Initial + selected Context + Local blocks [LC §4.2,
+ * §4.6 attn(query, kvcache_after_retrieval)]: for query head h,
+ * out[b][h] = softmax(q_h K_S^T * softmax_scale) V_S over the valid tokens S of
+ * those blocks, fp32 accumulation.  sel/cnt as produced by
+ * kt_score_select_blocks (possibly from an earlier step: the token_step /
+ * layer_step reuse of [LC §4.6]); cnt is clamped to [0, min(top_k, C)].
+ * out: fp32 [batch][num_q_heads][128].
+ */
+kt_status kt_sparse_decode_attn(const void* q, const kt_paged_kv* kv, const kt_sparse_params* p,
+                                const int32_t* sel, const int32_t* cnt, float* out, void* ws,
+                                size_t ws_bytes, kt_stream_t stream);
+
+/*
+ * One decode step: kt_score_select_blocks then kt_sparse_decode_attn, the
+ * attention launched as a programmatic dependent of the selection so that the
+ * Initial/Local blocks stream while selection runs.  Workspace: KT_OP_SPARSE_STEP.
+ */
+kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void* reps_pool,
+                                const kt_sparse_params* p, int32_t* sel, int32_t* cnt,
+                                float* out, void* ws, size_t ws_bytes, kt_stream_t stream);
+
+/*
+ * The same step for callers whose query and output live in HOST memory:
+ * copies q_host (fp16 [batch][num_q_heads][128]) to q_dev, runs
+ * kt_sparse_decode_step, copies out_dev to out_host (fp32) and synchronises
+ * `stream`.  Host buffers should be pinned for asynchronous copies.
+ */
+kt_status kt_sparse_decode_step_host(const void* q_host, void* q_dev, const kt_paged_kv* kv,
+                                     const void* reps_pool, const kt_sparse_params* p,
+                                     int32_t* sel, int32_t* cnt, float* out_dev,
+                                     float* out_host, void* ws, size_t ws_bytes,
+                                     kt_stream_t stream);
+
+/*
+ * Dense decode attention over all n tokens of each sequence: the full scan
+ * that [LC §1] says the sparse method avoids; kept as the sparsity reference.
+ */
+kt_status kt_dense_decode_attn(const void* q, const kt_paged_kv* kv, int32_t num_q_heads,
+                               float softmax_scale, float* out, void* ws, size_t ws_bytes,
+                               kt_stream_t stream);
+
+/*
+ * Synchronises `stream`, stores the workspace status word (a kt_status value,
+ * KT_OK if no device-side anomaly was recorded since the last read) in
+ * *device_status and clears it.
+ */
+kt_status kt_read_device_status(void* ws, size_t ws_bytes, kt_stream_t stream,
+                                int32_t* device_status);
+
+/*
+ * Diagnostic: launches one CTA that waits on an mbarrier nobody completes,
+ * giving up after `spin_limit` polls; the kernel then records KT_ERR_TIMEOUT in
+ * the status word and returns.  Used to test the bounded-wait path.
+ */
+kt_status kt_selftest_bounded_wait(void* ws, size_t ws_bytes, int32_t spin_limit,
+                                   kt_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KT_H_ */

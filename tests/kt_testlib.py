@@ -1,0 +1,155 @@
+"""Helpers shared by the GPU tests: move a synthetic workload to the device,
+run the libkt calls through the binding, and compare against the oracle."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+
+TOL = 2e-3  # max normwise relative error per (sequence, query head) row
+ZONE = 1e-5  # selection boundary zone, relative to the k-th score
+
+
+def to_dev(a, dtype=None):
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.float16).cuda()
+    t = torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    return t if dtype is None else t.to(dtype)
+
+
+class DevWorkload:
+    """A synth.Workload on the GPU plus the binding's structs."""
+
+    def __init__(self, w: synth.Workload):
+        import block_sparse_long_quest_gb300 as kt
+        self.w = w
+        self.k = to_dev(w.k_pool)
+        self.v = to_dev(w.v_pool)
+        self.table = to_dev(w.block_table)
+        self.lens = to_dev(w.seq_lens)
+        self.q = to_dev(w.q)
+        self.q_local = to_dev(w.q_local) if w.q_local is not None else None
+        self.kv = kt.paged_kv(self.k, self.v, self.table, self.lens)
+        p = w.params
+        self.params = kt.sparse_params(p.num_q_heads, p.initial_blocks, p.local_blocks, p.top_k,
+                                       p.rep, p.head_mode, num_reps=p.num_reps,
+                                       fix_stride=p.fix_stride, softmax_scale=p.softmax_scale)
+
+    @property
+    def SEL(self):
+        return 1 if self.w.params.head_mode == synth.HEAD_SHARED else self.w.num_kv_heads
+
+    def build_reps(self):
+        import torch
+        import block_sparse_long_quest_gb300 as kt
+        n = kt.kt_reps_pool_bytes(self.kv, self.params)
+        self.reps = torch.zeros(n, dtype=torch.uint8, device="cuda")
+        kt.kt_build_block_reps(self.kv, self.params, 0, self.w.max_blocks, self.reps)
+        return self.reps
+
+    def reps_view(self):
+        """[P][H_kv][R][d] numpy view of the device reps (uint16 bits or float32)."""
+        R = synth.Params.reps_per_block(self.w.params)
+        a = self.reps.cpu().numpy()
+        if self.w.params.rep == synth.REP_MEAN:
+            return a.view(np.float32).reshape(self.w.num_pages, self.w.num_kv_heads, R, 128)
+        return a.view(np.uint16).reshape(self.w.num_pages, self.w.num_kv_heads, R, 128)
+
+    def select(self, ws=None):
+        import torch
+        import block_sparse_long_quest_gb300 as kt
+        B, k = self.w.batch, self.w.params.top_k
+        sel = torch.full((B, self.SEL, k), -1, dtype=torch.int32, device="cuda")
+        cnt = torch.full((B, self.SEL), -1, dtype=torch.int32, device="cuda")
+        sc = torch.zeros((B, self.SEL, k), dtype=torch.float32, device="cuda")
+        if ws is None:
+            ws = kt.workspace(kt.KT_OP_SCORE_SELECT, self.kv, self.params)
+        kt.kt_score_select_blocks(self.q, self.kv, self.reps, self.params, sel, cnt, sc, ws)
+        return sel, cnt, sc, ws
+
+    def attend(self, sel, cnt, ws=None):
+        import torch
+        import block_sparse_long_quest_gb300 as kt
+        out = torch.full((self.w.batch, self.w.params.num_q_heads, 128), float("nan"),
+                         dtype=torch.float32, device="cuda")
+        if ws is None:
+            ws = kt.workspace(kt.KT_OP_SPARSE_ATTN, self.kv, self.params)
+        kt.kt_sparse_decode_attn(self.q, self.kv, self.params, sel, cnt, out, ws)
+        return out, ws
+
+    def step(self, ws=None):
+        import torch
+        import block_sparse_long_quest_gb300 as kt
+        B, k = self.w.batch, self.w.params.top_k
+        sel = torch.full((B, self.SEL, k), -1, dtype=torch.int32, device="cuda")
+        cnt = torch.full((B, self.SEL), -1, dtype=torch.int32, device="cuda")
+        out = torch.full((B, self.w.params.num_q_heads, 128), float("nan"), dtype=torch.float32,
+                         device="cuda")
+        if ws is None:
+            ws = kt.workspace(kt.KT_OP_SPARSE_STEP, self.kv, self.params)
+        kt.kt_sparse_decode_step(self.q, self.kv, self.reps, self.params, sel, cnt, out, ws)
+        return sel, cnt, out, ws
+
+    def dense(self, ws=None):
+        import torch
+        import block_sparse_long_quest_gb300 as kt
+        out = torch.full((self.w.batch, self.w.params.num_q_heads, 128), float("nan"),
+                         dtype=torch.float32, device="cuda")
+        if ws is None:
+            ws = kt.workspace(kt.KT_OP_DENSE_ATTN, self.kv, self.params)
+        kt.kt_dense_decode_attn(self.q, self.kv, self.w.params.num_q_heads,
+                                self.w.params.softmax_scale, out, ws)
+        return out, ws
+
+
+def row_rel_err(got, want):
+    """max_i |a_i - r_i| / max_i |r_i| per row (last axis)."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    num = np.abs(got - want).max(axis=-1)
+    den = np.maximum(np.abs(want).max(axis=-1), 1e-30)
+    return num / den
+
+
+def check_reps(dw: DevWorkload, ref):
+    """GPU reps (per page) must equal the oracle's (per logical block) bit for bit."""
+    w = dw.w
+    got = dw.reps_view()
+    mism = 0
+    for b in range(w.batch):
+        n = int(w.seq_lens[b])
+        for j in range(n // 128):
+            page = w.block_table[b, j]
+            a = got[page]
+            r = ref[b, j]
+            if w.params.rep == synth.REP_MEAN:
+                ok = np.array_equal(a.reshape(r.shape).view(np.uint32), r.view(np.uint32))
+            else:
+                ok = np.array_equal(a, r)
+            mism += 0 if ok else 1
+    return mism
+
+
+def selection_agrees(gpu_sel, gpu_cnt, oracle_res, b, u):
+    """Set equality outside the boundary zone.  Returns (ok, exact_equal)."""
+    cnt = int(oracle_res["cnt"][b, u])
+    if int(gpu_cnt[b, u]) != cnt:
+        return False, False
+    want = set(oracle_res["sel"][b, u, :cnt].tolist())
+    got_list = gpu_sel[b, u, :cnt].tolist()
+    got = set(got_list)
+    if got_list != sorted(got_list) or len(got) != cnt:
+        return False, False
+    if got == want:
+        return True, True
+    scores = oracle_res["unit_scores"][b, u]
+    ctx = ~np.isnan(scores)
+    vals = np.sort(scores[ctx])[::-1]
+    sk = vals[cnt - 1]
+    zone = np.abs(scores - sk) <= ZONE * max(abs(sk), 1e-30)
+    for j in got.symmetric_difference(want):
+        if not zone[j]:
+            return False, False
+    return True, False
