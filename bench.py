@@ -1,0 +1,493 @@
+#!/usr/bin/env python
+"""Benchmark of the block-sparse decode step on GB300.
+
+One step = kt_sparse_decode_step on one layer: score every Context block
+against its representatives, select the top-k, and attend over Initial +
+selected + Local blocks (selection and attention kernels, the attention launched
+as a programmatic dependent of the selection).
+
+Default workload: the InternLM2.5-7B-1M-shaped 128K layer (32 query heads, 8 KV
+heads, head_dim 128, 131072 fp16 tokens in 128-token blocks, Initial 128,
+Local 4096, Quest reps, SHARED top-32), seeded synthetic data, eight distinct
+layers rotated so that the touched working set (8 x 38 MB) is larger than twice
+the L2 cache.  A second leg runs the 1M-token, 4-layer workload (SEPARATE
+top-32 per KV head, Quest and Max reps).
+
+value = algorithmic bytes per step (reps of every Context block + K/V of the
+attended tokens) / device time per step, in GB/s; us_per_step and
+ms_per_step give the time.  Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "sparse decode attention µs/step and achieved HBM GB/s at 128K and 1M context"
+BLOCK = 128
+D = 128
+
+
+# ----------------------------------------------------------------------------- sizes
+
+def step_bytes(w: synth.Workload) -> dict:
+    """Algorithmic bytes of one decode step: representative rows of every Context
+    block (each read once) + K and V of every attended valid token per KV head."""
+    p = w.params
+    R = p.reps_per_block()
+    rep_elem = 4 if p.rep == synth.REP_MEAN else 2
+    H_kv = w.num_kv_heads
+    reps = kv = 0
+    for n in w.seq_lens:
+        n = int(n)
+        nb = (n + BLOCK - 1) // BLOCK
+        c0 = min(p.initial_blocks, nb)
+        c1 = max(c0, nb - p.local_blocks)
+        C = c1 - c0
+        k = min(p.top_k, C)
+        reps += C * H_kv * R * D * rep_elem
+        tokens = c0 * BLOCK + k * BLOCK + (n - c1 * BLOCK)
+        kv += tokens * H_kv * D * 2 * 2
+    return {"reps": reps, "kv": kv, "total": reps + kv}
+
+
+# ----------------------------------------------------------------------------- device side
+
+class Layer:
+    """One layer's KV cache, reps and step buffers on the GPU."""
+
+    def __init__(self, w: synth.Workload, extra_reps=(), keep_host=False):
+        import torch
+
+        import block_sparse_long_quest_gb300 as kt
+        self.w = w
+
+        def dev(a):
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).view(torch.float16).cuda()
+            return torch.from_numpy(a).cuda()
+
+        self.k, self.v = dev(w.k_pool), dev(w.v_pool)
+        if not keep_host:
+            w.k_pool = w.v_pool = None
+        self.table, self.lens, self.q = dev(w.block_table), dev(w.seq_lens), dev(w.q)
+        self.kv = kt.paged_kv(self.k, self.v, self.table, self.lens)
+        self.variants = {}
+        for rep in (w.params.rep, *extra_reps):
+            p = w.params
+            params = kt.sparse_params(p.num_q_heads, p.initial_blocks, p.local_blocks, p.top_k,
+                                      rep, p.head_mode, num_reps=p.num_reps,
+                                      fix_stride=p.fix_stride, softmax_scale=p.softmax_scale)
+            reps = torch.zeros(kt.kt_reps_pool_bytes(self.kv, params), dtype=torch.uint8,
+                               device="cuda")
+            kt.kt_build_block_reps(self.kv, params, 0, w.max_blocks, reps)
+            SEL = 1 if p.head_mode == synth.HEAD_SHARED else w.num_kv_heads
+            self.variants[rep] = dict(
+                params=params, reps=reps,
+                sel=torch.zeros((w.batch, SEL, p.top_k), dtype=torch.int32, device="cuda"),
+                cnt=torch.zeros((w.batch, SEL), dtype=torch.int32, device="cuda"),
+                out=torch.zeros((w.batch, p.num_q_heads, D), dtype=torch.float32, device="cuda"),
+                ws=kt.workspace(kt.KT_OP_SPARSE_STEP, self.kv, params))
+
+    def step(self, rep):
+        import block_sparse_long_quest_gb300 as kt
+        v = self.variants[rep]
+        kt.kt_sparse_decode_step(self.q, self.kv, v["reps"], v["params"], v["sel"], v["cnt"],
+                                 v["out"], v["ws"])
+
+    def select(self, rep):
+        import block_sparse_long_quest_gb300 as kt
+        v = self.variants[rep]
+        kt.kt_score_select_blocks(self.q, self.kv, v["reps"], v["params"], v["sel"], v["cnt"],
+                                  None, v["ws"])
+
+    def attend(self, rep):
+        import block_sparse_long_quest_gb300 as kt
+        v = self.variants[rep]
+        kt.kt_sparse_decode_attn(self.q, self.kv, v["params"], v["sel"], v["cnt"], v["out"],
+                                 v["ws"])
+
+
+def graph_time(fn_list, count, warmup, stream, chunk=1000, sampler=None):
+    """Device seconds for `count` calls cycling through fn_list, captured in CUDA
+    graphs (chunks of `chunk` calls + a remainder graph), timed with events."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            fn_list[i % len(fn_list)]()
+    stream.synchronize()
+    graphs = []
+    c = min(chunk, count)
+    reps, rem = divmod(count, c)
+    for n in ([c] if reps else []) + ([rem] if rem else []):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                fn_list[i % len(fn_list)]()
+        graphs.append((g, n))
+    plan = [graphs[0][0]] * reps + ([graphs[-1][0]] if rem else [])
+    # one untimed replay of each graph
+    for g, _ in graphs:
+        g.replay()
+    stream.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark_start()
+    start.record(stream)
+    for g in plan:
+        g.replay()
+    end.record(stream)
+    end.synchronize()
+    if sampler:
+        sampler.mark_end()
+    return start.elapsed_time(end) / 1e3
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 20):
+        self.index, self.period_ms = index, period_ms
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.perf_counter()
+
+    def mark_end(self):
+        self.t_end = time.perf_counter()
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        t0 = getattr(self, "t_start", 0.0)
+        t1 = getattr(self, "t_end", float("inf"))
+        rows = []
+        for ts, l in self.lines:
+            parts = [x.strip() for x in l.split(",")]
+            if len(parts) == 7 and t0 <= ts <= t1 + 0.05:
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i] == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- CPU baseline
+
+def cpu_baseline(w: synth.Workload, budget_s: float = 12.0) -> dict:
+    """The oracle (single-threaded C) on the same work as one GPU step: score,
+    select and attend for one 128K layer, reps built beforehand (untimed)."""
+    import oracle
+    kv = oracle.KV.of(w)
+    st = oracle.StepTimer(kv, w.params, w.q_local)
+    st.step(w.q)  # warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        st.step(w.q)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= 200:
+            break
+    per = el / n
+    return {"value": step_bytes(w)["total"] / per / 1e9, "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "us_per_step": per * 1e6,
+            "sample": f"oracle score+select+attend, {w.name}, 1 layer, reps prebuilt "
+                      f"(untimed), {n} steps in {el:.1f} s"}
+
+
+def host_info():
+    try:
+        model = [l.split(":", 1)[1].strip() for l in open("/proc/cpuinfo")
+                 if l.lower().startswith(("model name", "cpu part"))][:1]
+    except OSError:
+        model = []
+    return {"nproc": os.cpu_count(), "cpu": model[0] if model else None}
+
+
+# ----------------------------------------------------------------------------- main
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Max of a float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference(args, world, rank):
+    """The oracle on the host cores, same workload/metric; rank 0 only."""
+    if rank != 0:
+        return
+    import oracle
+    w = synth.long128k(seq_len=args.seq_len)
+    kv = oracle.KV.of(w)
+    st = oracle.StepTimer(kv, w.params)
+    for _ in range(max(0, args.warmup)):
+        st.step(w.q)
+        break  # one warm step: each step takes a fraction of a second
+    t_one = time.perf_counter()
+    st.step(w.q)
+    t_one = time.perf_counter() - t_one
+    cap = max(1, int(90.0 / max(t_one, 1e-6)))
+    steps = min(args.steps, cap)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        st.step(w.q)
+    el = time.perf_counter() - t0
+    per = el / steps
+    value = step_bytes(w)["total"] / per / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": steps, "steps_requested": args.steps, "warmup": args.warmup,
+        "ms_per_step": per * 1e3, "us_per_step": per * 1e6, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": 1, "seq_len": args.seq_len,
+                   "parallelism": "single-thread CPU"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"oracle score+select+attend on one {w.name} layer, reps "
+                                   f"prebuilt, {steps} steps (capped to ~90 s)"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "host": host_info(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=8, help="rotated 128K layers")
+    ap.add_argument("--seq-len", type=int, default=131072)
+    ap.add_argument("--no-1m", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+
+    import block_sparse_long_quest_gb300 as kt  # fails loudly without libkt.so
+    torch.cuda.set_device(local)
+    stream = torch.cuda.Stream()
+
+    # ---- 128K workload: `layers` independent layers, rotated every step
+    layers = []
+    for l in range(args.layers):
+        w = synth.long128k(layer=l, seq_len=args.seq_len)
+        layers.append(Layer(w, keep_host=(l == 0)))
+    w0 = layers[0].w
+    rep = w0.params.rep
+    bytes_step = step_bytes(w0)
+    torch.cuda.synchronize()
+
+    # correctness guard: every layer's device status word is clean after a step
+    for L in layers:
+        L.step(rep)
+    for L in layers:
+        st = kt.kt_read_device_status(L.variants[rep]["ws"])
+        if st != kt.KT_OK:
+            raise RuntimeError(f"device status {kt.status_string(st)}")
+
+    # ---- timed region: exactly `steps` decode steps
+    steps_fns = [lambda L=L: L.step(rep) for L in layers]
+    n_layers = len(layers)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_step = graph_time(steps_fns, args.steps, args.warmup, stream, sampler=clocks)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_step = max_over_ranks(t_step, world)
+    per_step = t_step / args.steps
+    value = world * bytes_step["total"] * args.steps / t_step / 1e9
+
+    # ---- per-kernel device time (roofline of the dominant kernel: attention)
+    n_k = min(args.steps, 20000)
+    t_attn = graph_time([lambda L=L: L.attend(rep) for L in layers], n_k, args.warmup, stream)
+    t_sel = graph_time([lambda L=L: L.select(rep) for L in layers], n_k, args.warmup, stream)
+    attn_us, sel_us = t_attn / n_k * 1e6, t_sel / n_k * 1e6
+    peak, peak_kind = measured_peak()
+    attn_gbs = bytes_step["kv"] / (t_attn / n_k) / 1e9
+
+    # ---- end to end through the host-buffer entry point
+    v0 = layers[0].variants[rep]
+    q_host = torch.empty_like(layers[0].q, device="cpu").pin_memory()
+    out_host = torch.empty_like(v0["out"], device="cpu").pin_memory()
+    q_host.copy_(layers[0].q.cpu())
+    q_dev = [torch.empty_like(L.q) for L in layers]
+    n_e2e = min(args.steps, 3000)
+    for i in range(args.warmup):
+        L = layers[i % len(layers)]
+        v = L.variants[rep]
+        kt.kt_sparse_decode_step_host(q_host, q_dev[i % len(layers)], L.kv, v["reps"],
+                                      v["params"], v["sel"], v["cnt"], v["out"], out_host,
+                                      v["ws"], stream)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        L = layers[i % len(layers)]
+        v = L.variants[rep]
+        kt.kt_sparse_decode_step_host(q_host, q_dev[i % len(layers)], L.kv, v["reps"],
+                                      v["params"], v["sel"], v["cnt"], v["out"], out_host,
+                                      v["ws"], stream)
+    t_e2e = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_value = world * bytes_step["total"] * n_e2e / t_e2e / 1e9
+
+    extra = {}
+    # ---- 1M-token leg: 4 layers back to back, Quest and Max reps
+    if world == 1 and not args.no_1m:
+        del layers, steps_fns, q_dev
+        torch.cuda.empty_cache()
+        big = []
+        for l in range(4):
+            wb = synth.long1m(layer=l, rep=synth.REP_QUEST)
+            big.append(Layer(wb, extra_reps=(synth.REP_MAX,)))
+        res = {}
+        for r, name in ((synth.REP_QUEST, "quest"), (synth.REP_MAX, "max")):
+            for L in big:
+                L.step(r)
+            for L in big:
+                if kt.kt_read_device_status(L.variants[r]["ws"]) != kt.KT_OK:
+                    raise RuntimeError("device status after 1M step")
+            n1 = 2000
+            t1 = graph_time([lambda L=L, r=r: L.step(r) for L in big], n1, args.warmup, stream)
+            wq = big[0].w
+            wq.params.rep = r
+            b1 = step_bytes(wq)
+            per_layer = t1 / n1
+            res[name] = {"us_per_layer_step": per_layer * 1e6,
+                         "us_per_4layer_step": 4 * per_layer * 1e6,
+                         "gbs": b1["total"] / per_layer / 1e9,
+                         "bytes_per_layer_step": b1["total"]}
+            wq.params.rep = synth.REP_QUEST
+        extra["at_1m"] = {"workload": "1m-gqa4-separate-k32 (4 layers, 1048576 tokens each)",
+                          **res}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+        "us_per_step": per_step * 1e6, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": w0.name, "batch": 1, "seq_len": args.seq_len, "q_heads": 32,
+                   "kv_heads": 8, "head_dim": 128, "block_size": 128, "initial_tokens": 128,
+                   "local_tokens": 4096, "top_k": 32, "rep": "quest", "head_mode": "shared",
+                   "bytes_per_step": bytes_step,
+                   "l2": f"{n_layers} layers rotated, touched set "
+                         f"{n_layers * bytes_step['total'] / 1e6:.0f} MB > 2x L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "attn_kernel", "achieved": attn_gbs,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": attn_gbs / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": bytes_step["kv"],
+                     "us_per_launch": attn_us},
+        "kernels_us": {"select_kernel": sel_us, "attn_kernel": attn_us},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "us_per_step": t_e2e / n_e2e * 1e6,
+                "steps": n_e2e, "h2d_bytes_per_step": int(layers_q_bytes(w0)),
+                "d2h_bytes_per_step": int(w0.batch * w0.params.num_q_heads * D * 4)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+        **extra,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w0)
+        line["host"] = host_info()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier(world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def layers_q_bytes(w):
+    return w.batch * w.params.num_q_heads * D * 2
+
+
+if __name__ == "__main__":
+    main()

@@ -77,6 +77,10 @@ def lib():
         L.orc_attend.argtypes = [vp, i64, i64, i64, vp, vp, i64, ctypes.c_double, vp]
         L.orc_dense.restype = None
         L.orc_dense.argtypes = [vp, vp, i64, ctypes.c_double, vp]
+        L.orc_build_all_reps.restype = ctypes.c_int
+        L.orc_build_all_reps.argtypes = [vp, vp, vp, i64, vp, vp, vp, vp, i64, i64]
+        L.orc_score_select_attend.restype = ctypes.c_int
+        L.orc_score_select_attend.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64]
         L.orc_sparse_step.restype = ctypes.c_int
         L.orc_sparse_step.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, i64, i64]
         _lib = L
@@ -218,3 +222,36 @@ def sparse_step(kv: KV, q, p, q_local=None, *, units=None, want_reps=True,
         raise ValueError("oracle rejected the parameters")
     return dict(reps=reps_f32 if p.rep == REP_MEAN else reps_h16, unit_scores=us, sel=sel,
                 cnt=cnt, out=out, dyn_scores=dyn)
+
+
+class StepTimer:
+    """The per-step part of the oracle (score, select, attend) over reps built
+    once up front; used to time the CPU baseline on the same work as one GPU
+    decode step."""
+
+    def __init__(self, kv: KV, p, q_local=None):
+        self.kv, self.p = kv, p
+        self.pp = params(p)
+        R = reps_per_block(p, kv.bs)
+        self.rv = np.zeros((kv.B, kv.max_blocks, kv.H_kv, R, kv.d), dtype=np.float64)
+        ql = None if q_local is None else np.ascontiguousarray(q_local, dtype=np.uint16)
+        T = 0 if ql is None else ql.shape[1]
+        SEL = 1 if p.head_mode == HEAD_SHARED else kv.H_kv
+        rc = lib().orc_build_all_reps(ctypes.byref(kv.s), ctypes.byref(self.pp), _ptr(ql), T,
+                                      self.rv.ctypes.data, None, None, None, 0, SEL)
+        if rc != 0:
+            raise ValueError("oracle rejected the parameters")
+        self.SEL = SEL
+        self.sel = np.zeros((kv.B, SEL, max(p.top_k, 1)), dtype=np.int32)
+        self.cnt = np.zeros((kv.B, SEL), dtype=np.int32)
+        self.out = np.zeros((kv.B, p.num_q_heads, kv.d), dtype=np.float64)
+
+    def step(self, q):
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        rc = lib().orc_score_select_attend(ctypes.byref(self.kv.s), q.ctypes.data,
+                                           ctypes.byref(self.pp), self.rv.ctypes.data, None,
+                                           self.sel.ctypes.data, self.cnt.ctypes.data,
+                                           self.out.ctypes.data, 0, self.SEL)
+        if rc != 0:
+            raise ValueError("oracle rejected the parameters")
+        return self.out

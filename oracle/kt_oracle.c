@@ -354,9 +354,12 @@ void orc_dense(const orc_kv* kv, const uint16_t* q /* [B][H_q][d] */, int64_t H_
 
 /* ---- one decode step ---------------------------------------------------------
  * reps -> unit scores -> top-k -> attention over Initial + selected + Local.
+ * Split in two so that the (amortised) representative build can be timed apart
+ * from the per-step work.
  *
  *   q            [B][H_q][d]                 decode queries
  *   q_local      [B][T][H_q][d] or NULL      local-window queries (Dynamic only)
+ *   rv           [B][max_blocks][H_kv][R][d] representative values as doubles
  *   reps_h16     [B][max_blocks][H_kv][R][d] or NULL   binary16 reps (not Mean)
  *   reps_f32     [B][max_blocks][H_kv][d] or NULL      Mean reps
  *   dyn_scores   [B][H_kv][max_blocks*bs] or NULL      Dynamic token scores
@@ -365,35 +368,28 @@ void orc_dense(const orc_kv* kv, const uint16_t* q /* [B][H_q][d] */, int64_t H_
  *   out          [B][H_q][d]
  *   unit_lo/hi   only selection units in [unit_lo, unit_hi) and their query heads
  *                are computed (for sampled checks); pass 0, SEL for all.
- * Returns 0, or -1 on an unsupported argument.
+ * Each returns 0, or -1 on an unsupported argument.
  */
-int orc_sparse_step(const orc_kv* kv, const uint16_t* q, const orc_params* p,
-                    const uint16_t* q_local, int64_t T, uint16_t* reps_h16, float* reps_f32,
-                    double* dyn_scores, double* unit_scores, int32_t* sel, int32_t* cnt,
-                    double* out, int64_t unit_lo, int64_t unit_hi) {
-  const int64_t B = kv->B, H_kv = kv->H_kv, d = kv->d, bs = kv->bs, MB = kv->max_blocks;
-  const int64_t H_q = p->H_q, G = H_q / H_kv, R = orc_reps_per_block(p, bs);
-  const int64_t SEL = p->head_mode == ORC_SHARED ? 1 : H_kv;
-  if (H_q % H_kv != 0 || p->local_blocks < 1 || p->top_k < 0) return -1;
+static int check_args(const orc_kv* kv, const orc_params* p, const uint16_t* q_local,
+                      int64_t T) {
+  if (p->H_q % kv->H_kv != 0 || p->local_blocks < 1 || p->top_k < 0) return -1;
   if (p->rep == ORC_DYNAMIC && (q_local == NULL || T < 1)) return -1;
   if (p->rep == ORC_FIX && p->fix_stride < 1) return -1;
-  if (unit_lo < 0) unit_lo = 0;
-  if (unit_hi > SEL) unit_hi = SEL;
+  return 0;
+}
 
-  /* representative values, as doubles, per (block, head, rep, channel) */
-  double* rv = (double*)malloc(sizeof(double) * (size_t)(MB * H_kv * R * d));
+int orc_build_all_reps(const orc_kv* kv, const orc_params* p, const uint16_t* q_local, int64_t T,
+                       double* rv, uint16_t* reps_h16, float* reps_f32, double* dyn_scores,
+                       int64_t unit_lo, int64_t unit_hi) {
+  const int64_t B = kv->B, H_kv = kv->H_kv, d = kv->d, bs = kv->bs, MB = kv->max_blocks;
+  const int64_t H_q = p->H_q, R = orc_reps_per_block(p, bs);
+  if (check_args(kv, p, q_local, T)) return -1;
   uint16_t* hb = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(R * d));
   float* fb = (float*)malloc(sizeof(float) * (size_t)d);
-  double* dyn = NULL;
-  double* qd = (double*)malloc(sizeof(double) * (size_t)d);
-  double* score = (double*)malloc(sizeof(double) * (size_t)(MB > 0 ? MB : 1));
-  int32_t* list = (int32_t*)malloc(sizeof(int32_t) * (size_t)(MB + 1));
-  if (p->rep == ORC_DYNAMIC) dyn = (double*)malloc(sizeof(double) * (size_t)(MB * bs));
-
+  double* dyn = p->rep == ORC_DYNAMIC ? (double*)malloc(sizeof(double) * (size_t)(MB * bs)) : NULL;
   for (int64_t b = 0; b < B; ++b) {
     int64_t n = kv->seq_lens[b], nb, c0, c1;
     orc_partition(n, bs, p->initial_blocks, p->local_blocks, &nb, &c0, &c1);
-    /* heads needed: those of the requested units */
     for (int64_t h = 0; h < H_kv; ++h) {
       int64_t u = p->head_mode == ORC_SHARED ? 0 : h;
       if (u < unit_lo || u >= unit_hi) continue;
@@ -406,7 +402,7 @@ int orc_sparse_step(const orc_kv* kv, const uint16_t* q, const orc_params* p,
       for (int64_t j = 0; j < nb; ++j) {
         if ((j + 1) * bs > n) continue; /* reps exist for full blocks only */
         orc_block_reps(kv, b, j, h, p, dyn, hb, fb);
-        double* dst = rv + (j * H_kv + h) * R * d;
+        double* dst = rv + ((b * MB + j) * H_kv + h) * R * d;
         if (p->rep == ORC_MEAN) {
           for (int64_t c = 0; c < d; ++c) dst[c] = (double)fb[c];
           if (reps_f32) memcpy(reps_f32 + ((b * MB + j) * H_kv + h) * d, fb, sizeof(float) * (size_t)d);
@@ -417,6 +413,28 @@ int orc_sparse_step(const orc_kv* kv, const uint16_t* q, const orc_params* p,
         }
       }
     }
+  }
+  free(hb);
+  free(fb);
+  free(dyn);
+  return 0;
+}
+
+int orc_score_select_attend(const orc_kv* kv, const uint16_t* q, const orc_params* p,
+                            const double* rv, double* unit_scores, int32_t* sel, int32_t* cnt,
+                            double* out, int64_t unit_lo, int64_t unit_hi) {
+  const int64_t B = kv->B, H_kv = kv->H_kv, d = kv->d, bs = kv->bs, MB = kv->max_blocks;
+  const int64_t H_q = p->H_q, G = H_q / H_kv, R = orc_reps_per_block(p, bs);
+  const int64_t SEL = p->head_mode == ORC_SHARED ? 1 : H_kv;
+  if (p->H_q % kv->H_kv != 0 || p->local_blocks < 1 || p->top_k < 0) return -1;
+  if (unit_lo < 0) unit_lo = 0;
+  if (unit_hi > SEL) unit_hi = SEL;
+  double* qd = (double*)malloc(sizeof(double) * (size_t)d);
+  double* score = (double*)malloc(sizeof(double) * (size_t)(MB > 0 ? MB : 1));
+  int32_t* list = (int32_t*)malloc(sizeof(int32_t) * (size_t)(MB + 1));
+  for (int64_t b = 0; b < B; ++b) {
+    int64_t n = kv->seq_lens[b], nb, c0, c1;
+    orc_partition(n, bs, p->initial_blocks, p->local_blocks, &nb, &c0, &c1);
     for (int64_t u = unit_lo; u < unit_hi; ++u) {
       /* unit score of each context block: sum of head scores over the unit's
        * query heads, in ascending head order */
@@ -427,7 +445,8 @@ int orc_sparse_step(const orc_kv* kv, const uint16_t* q, const orc_params* p,
         int64_t h = hq / G;
         for (int64_t c = 0; c < d; ++c) qd[c] = dec(q[(b * H_q + hq) * d + c]);
         for (int64_t j = c0; j < c1; ++j)
-          score[j - c0] += orc_head_block_score(qd, rv + (j * H_kv + h) * R * d, R, d, p->rep);
+          score[j - c0] +=
+              orc_head_block_score(qd, rv + ((b * MB + j) * H_kv + h) * R * d, R, d, p->rep);
       }
       if (unit_scores)
         for (int64_t j = 0; j < MB; ++j)
@@ -445,14 +464,23 @@ int orc_sparse_step(const orc_kv* kv, const uint16_t* q, const orc_params* p,
                    out + (b * H_q + hq) * d);
     }
   }
-  free(rv);
-  free(hb);
-  free(fb);
-  free(dyn);
   free(qd);
   free(score);
   free(list);
   return 0;
+}
+
+int orc_sparse_step(const orc_kv* kv, const uint16_t* q, const orc_params* p,
+                    const uint16_t* q_local, int64_t T, uint16_t* reps_h16, float* reps_f32,
+                    double* dyn_scores, double* unit_scores, int32_t* sel, int32_t* cnt,
+                    double* out, int64_t unit_lo, int64_t unit_hi) {
+  const int64_t R = orc_reps_per_block(p, kv->bs);
+  if (check_args(kv, p, q_local, T)) return -1;
+  double* rv = (double*)calloc((size_t)(kv->B * kv->max_blocks * kv->H_kv * R * kv->d), sizeof(double));
+  int rc = orc_build_all_reps(kv, p, q_local, T, rv, reps_h16, reps_f32, dyn_scores, unit_lo, unit_hi);
+  if (rc == 0) rc = orc_score_select_attend(kv, q, p, rv, unit_scores, sel, cnt, out, unit_lo, unit_hi);
+  free(rv);
+  return rc;
 }
 
 /* Vector form of orc_f16_to_double, for the tests. */
