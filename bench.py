@@ -79,8 +79,8 @@ class Layer:
             return torch.from_numpy(a).cuda()
 
         self.k, self.v = dev(w.k_pool), dev(w.v_pool)
-        if not keep_host:
-            w.k_pool = w.v_pool = None
+        if not keep_host:  # free the host copy, keep the (heads, block, dim) shape
+            w.k_pool = w.v_pool = np.empty((0,) + w.k_pool.shape[1:], dtype=np.uint16)
         self.table, self.lens, self.q = dev(w.block_table), dev(w.seq_lens), dev(w.q)
         self.kv = kt.paged_kv(self.k, self.v, self.table, self.lens)
         self.variants = {}
