@@ -137,17 +137,17 @@ def graph_time(fn_list, count, warmup, stream, chunk=1000, sampler=None):
                 fn_list[i % len(fn_list)]()
         graphs.append((g, n))
     plan = [graphs[0][0]] * reps + ([graphs[-1][0]] if rem else [])
-    # one untimed replay of each graph
-    for g, _ in graphs:
-        g.replay()
-    stream.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if sampler:
-        sampler.mark_start()
-    start.record(stream)
-    for g in plan:
-        g.replay()
-    end.record(stream)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        for g, _ in graphs:  # one untimed replay of each graph
+            g.replay()
+        stream.synchronize()
+        if sampler:
+            sampler.mark_start()
+        start.record(stream)
+        for g in plan:
+            g.replay()
+        end.record(stream)
     end.synchronize()
     if sampler:
         sampler.mark_end()
@@ -385,6 +385,8 @@ def main():
     barrier(world)
     t_step = max_over_ranks(t_step, world)
     per_step = t_step / args.steps
+    if per_step < 5e-7:
+        raise RuntimeError("timed region recorded no work")
     value = world * bytes_step["total"] * args.steps / t_step / 1e9
 
     # ---- per-kernel device time (roofline of the dominant kernel: attention)
