@@ -362,10 +362,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
           l += sc[1] * f;
         }
       }
-      dst[2 * p.G + gg * D + c] = o;
+      dst[gg * D + c] = o;  // slot: O[G][128], then m[G], then l[G]
       if (c == 0) {
-        dst[gg] = M;
-        dst[p.G + gg] = l;
+        dst[p.G * D + gg] = M;
+        dst[p.G * D + p.G + gg] = l;
       }
     }
     __threadfence();
@@ -379,37 +379,50 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     return n;
   };
 
-  // Final merge of all partials of `seg` (CTA order, phase A then B).
+  // Final merge of all partials of `seg` (CTA order, phase A then B).  Thread
+  // 0 lists the partial slots (arithmetic only), then every consumer thread
+  // owns float4 chunks of the G x 128 outputs and streams the partials with
+  // independent loads (online max-rescaling, base 2).
   auto merge = [&](int seg, long long UB) {
     __threadfence();
-    const int b = seg / p.H_kv, h = seg % p.H_kv, c = ctid;
-    for (int gg = 0; gg < p.G; ++gg) {
-      float M = -INFINITY;
-      auto visit_max = [&](long long slot) {
-        M = fmaxf(M, __ldcg(p.parts + slot * slot_stride + gg));
-      };
+    int* slots = reinterpret_cast<int*>(scratch);  // up to 2 * MAX_ATTN_CTAS entries
+    if (ctid == 0) {
+      int np = 0;
       for_overlapping_ctas(prefA[seg], prefA[seg + 1], UA, NC,
-                           [&](int cc) { visit_max((long long)cc + seg); });
+                           [&](int cc) { slots[np++] = cc + seg; });
       for_overlapping_ctas(prefB[seg], prefB[seg + 1], UB, NC,
-                           [&](int cc) { visit_max(half_slots + cc + seg); });
-      float o = 0.0f, l = 0.0f;
-      auto visit = [&](long long slot) {
-        const float* src = p.parts + slot * slot_stride;
-        const float m = __ldcg(src + gg);
-        if (m == -INFINITY) return;
-        const float f = exp2f(m - M);
-        l += __ldcg(src + p.G + gg) * f;
-        o += __ldcg(src + 2 * p.G + gg * D + c) * f;
-      };
-      if (M != -INFINITY) {
-        for_overlapping_ctas(prefA[seg], prefA[seg + 1], UA, NC,
-                             [&](int cc) { visit((long long)cc + seg); });
-        for_overlapping_ctas(prefB[seg], prefB[seg + 1], UB, NC,
-                             [&](int cc) { visit(half_slots + cc + seg); });
+                           [&](int cc) { slots[np++] = (int)half_slots + cc + seg; });
+      bcast[1] = np;
+    }
+    named_bar_sync(1, CONSUMERS * 32);
+    const int np = bcast[1];
+    const int b = seg / p.H_kv, h = seg % p.H_kv;
+    for (int f = 4 * ctid; f < p.G * D; f += 4 * CONSUMERS * 32) {
+      const int gg = f / D, c = f % D;
+      float M = -INFINITY, L = 0.0f;
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+      for (int i = 0; i < np; ++i) {
+        const float* src = p.parts + (size_t)slots[i] * slot_stride;
+        const float m = __ldcg(src + p.G * D + gg);
+        const float l = __ldcg(src + p.G * D + p.G + gg);
+        const float4 o = __ldcg(reinterpret_cast<const float4*>(src + f));
+        if (m == -INFINITY) continue;
+        const float Mn = fmaxf(M, m);
+        const float a = exp2f(M - Mn), w = exp2f(m - Mn);
+        L = L * a + l * w;
+        O.x = O.x * a + o.x * w;
+        O.y = O.y * a + o.y * w;
+        O.z = O.z * a + o.z * w;
+        O.w = O.w * a + o.w * w;
+        M = Mn;
       }
-      p.out[((size_t)b * H_q + h * p.G + gg) * D + c] = l > 0.0f ? o / l : 0.0f;
+      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+      float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)b * H_q + h * p.G + gg) * D + c);
+      *dst = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
     }
     if (ctid == 0) p.counters[seg] = 0;
+    named_bar_sync(1, CONSUMERS * 32);
   };
 
   // Ticket for `seg`; the CTA that completes the count merges.

@@ -80,11 +80,10 @@ int reps_rows(const kt_sparse_params* p) {
   }
 }
 
-bool op_selects(kt_op op) { return op == KT_OP_SCORE_SELECT || op == KT_OP_SPARSE_STEP; }
-bool op_attends(kt_op op) {
-  return op == KT_OP_SPARSE_ATTN || op == KT_OP_DENSE_ATTN || op == KT_OP_SPARSE_STEP;
-}
-
+// One layout for every op: [status header][attention][selection][dynamic].
+// Region offsets depend only on the shapes, so a workspace sized for a larger
+// op serves every smaller one; kt_workspace_bytes(op) is the end of the last
+// region that `op` uses.
 WsLayout layout(kt_op op, const kt_paged_kv* kv, const kt_sparse_params* p, int T) {
   WsLayout L;
   std::memset(&L, 0, sizeof(L));
@@ -92,31 +91,25 @@ WsLayout layout(kt_op op, const kt_paged_kv* kv, const kt_sparse_params* p, int 
   const int G = p->num_q_heads / H_kv;
   size_t off = 256;  // status header
   L.status = 0;
-  if (op_selects(op)) {
-    L.sel = make_sel_plan(B, H_kv, kv->max_blocks_per_seq, p->initial_blocks, p->local_blocks,
-                          p->top_k, p->head_mode);
-    const size_t units = (size_t)B * L.sel.SEL;
-    L.sel_counters = off;
-    off = align256(off + units * 4);
-    L.sel_ncand = off;
-    off = align256(off + units * L.sel.nchunks * 4);
-    L.sel_cand = off;
-    off = align256(off + units * L.sel.nchunks * L.sel.kk * 8);
-  }
-  if (op_attends(op)) {
-    L.slot_floats = ((2 * G + G * D) + 3) & ~3;
-    L.attn_counters = off;
-    off = align256(off + (size_t)S * 4);
-    L.attn_parts = off;
-    off = align256(off + (size_t)2 * (MAX_ATTN_CTAS + S) * L.slot_floats * 4);
-  }
-  if (op == KT_OP_DYNAMIC_REPS) {
-    (void)T;
-    L.dyn = off;
-    L.dyn_bytes = 0;
-    off = align256(off + L.dyn_bytes);
-  }
-  L.total = off;
+  L.slot_floats = ((2 * G + G * D) + 3) & ~3;
+  L.attn_counters = off;
+  off = align256(off + (size_t)S * 4);
+  L.attn_parts = off;
+  off = align256(off + (size_t)2 * (MAX_ATTN_CTAS + S) * L.slot_floats * 4);
+  const size_t attn_end = off;
+  L.sel = make_sel_plan(B, H_kv, kv->max_blocks_per_seq, p->initial_blocks, p->local_blocks,
+                        p->top_k > 0 ? p->top_k : 1, p->head_mode);
+  const size_t units = (size_t)B * L.sel.SEL;
+  L.sel_counters = off;
+  off = align256(off + units * 4);
+  L.sel_cand = off;
+  off = align256(off + units * L.sel.nchunks * L.sel.kk * 8);
+  const size_t sel_end = off;
+  (void)T;
+  L.dyn = off;
+  L.dyn_bytes = 0;
+  off = align256(off + L.dyn_bytes);
+  L.total = op == KT_OP_DENSE_ATTN ? attn_end : (op == KT_OP_DYNAMIC_REPS ? off : sel_end);
   return L;
 }
 
@@ -177,7 +170,6 @@ kt_status select_impl(const void* q, const kt_paged_kv* kv, const void* reps,
   a.sel_scores = sel_scores;
   a.status = at<int>(ws, L.status);
   a.counters = at<int>(ws, L.sel_counters);
-  a.ncand = at<int>(ws, L.sel_ncand);
   a.cand = at<unsigned long long>(ws, L.sel_cand);
   a.B = kv->batch;
   a.H_kv = kv->num_kv_heads;

@@ -38,7 +38,6 @@ struct SelPlan {
 struct WsLayout {
   size_t status;         // int32 status word, 256 B header
   size_t sel_counters;   // int32 [B*SEL]
-  size_t sel_ncand;      // int32 [B*SEL*nchunks]
   size_t sel_cand;       // uint64 [B*SEL*nchunks*kk]
   size_t attn_counters;  // int32 [S]
   size_t attn_parts;     // float [2*(MAX_ATTN_CTAS+S)][slot_floats]
@@ -252,7 +251,6 @@ struct SelectLaunch {
   float* sel_scores;
   int* status;
   int* counters;
-  int* ncand;
   unsigned long long* cand;
   int B, H_kv, G, max_blocks, P, I_b, L_b, top_k, rep, R, head_mode;
   SelPlan plan;

@@ -40,7 +40,6 @@ struct Params {
   float* sel_scores;
   int* status;
   int* counters;
-  int* ncand;
   unsigned long long* cand;
   int B, H_kv, G, max_blocks, P, I_b, L_b, top_k, rep, R, head_mode;
   int SEL, chunk, nchunks, kk;
@@ -294,9 +293,10 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
     }
     __syncthreads();
 
-    // ---- this chunk's top-kk candidates
+    // ---- this chunk's top-kk candidates; unused slots hold key 0, which is
+    // below every real key
     if (nloc <= p.kk) {
-      for (int i = tid; i < nloc; i += THREADS) my_cand[i] = keys[i];
+      for (int i = tid; i < p.kk; i += THREADS) my_cand[i] = i < nloc ? keys[i] : 0ull;
     } else {
       unsigned long long prefix, mask;
       radix_select(keys, nloc, p.kk, hist, sh_u64, sh_int, &prefix, &mask);
@@ -311,7 +311,8 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
       }
     }
   }
-  if (tid == 0) p.ncand[unit_base * p.nchunks + chunk] = min(nloc, p.kk);
+  if (nloc <= 0)
+    for (int i = tid; i < p.kk; i += THREADS) my_cand[i] = 0ull;
 
   // ---- ticket: the last chunk CTA of this unit merges
   __threadfence();
@@ -324,32 +325,32 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
   if (!sh_int[3]) return;
   __threadfence();
 
-  // gather every candidate of the unit (chunk order) into shared memory
+  // gather every candidate slot of the unit into shared memory (independent,
+  // coalesced loads); empty slots are key 0
   unsigned long long* all = keys;
-  if (tid == 0) {
-    int tot = 0;
-    for (int c = 0; c < p.nchunks; ++c) tot += __ldcg(p.ncand + unit_base * p.nchunks + c);
-    sh_int[0] = tot;
+  const int nslots = p.nchunks * p.kk;
+  const unsigned long long* src = p.cand + unit_base * (size_t)nslots;
+  int real = 0;
+  for (int i = tid; i < nslots; i += THREADS) {
+    const unsigned long long key = __ldcg(src + i);
+    all[i] = key;
+    real += key != 0ull ? 1 : 0;
   }
+  real = warp_sum_int(real);
+  if (tid == 0) sh_int[0] = 0;
   __syncthreads();
-  const int total = sh_int[0];
+  if (lane == 0) atomicAdd(&sh_int[0], real);
   __syncthreads();
-  for (int c = warp; c < p.nchunks; c += WARPS) {
-    const int nc = __ldcg(p.ncand + unit_base * p.nchunks + c);
-    int off = 0;
-    for (int c2 = lane; c2 < c; c2 += 32) off += __ldcg(p.ncand + unit_base * p.nchunks + c2);
-    off = warp_sum_int(off);
-    for (int i = lane; i < nc; i += 32)
-      all[off + i] = __ldcg(p.cand + (unit_base * p.nchunks + c) * p.kk + i);
-  }
+  const int total_real = sh_int[0];
+  const int total = nslots;
   __syncthreads();
 
-  const int keff = min(p.top_k, total);
+  const int keff = min(p.top_k, total_real);
   unsigned long long* chosen = all + total;  // keff entries
   if (keff > 0) {
     if (keff == total) {
       for (int i = tid; i < total; i += THREADS) chosen[i] = all[i];
-    } else {
+    } else {  // keff <= total_real: the zero slots are never chosen
       unsigned long long prefix, mask;
       radix_select(all, total, keff, hist, sh_u64, sh_int, &prefix, &mask);
       if (tid == 0) sh_int[2] = 0;
@@ -410,7 +411,6 @@ cudaError_t launch_select(const SelectLaunch& a, cudaStream_t stream) {
   p.sel_scores = a.sel_scores;
   p.status = a.status;
   p.counters = a.counters;
-  p.ncand = a.ncand;
   p.cand = a.cand;
   p.B = a.B;
   p.H_kv = a.H_kv;

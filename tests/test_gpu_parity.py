@@ -202,3 +202,21 @@ def test_workspace_reuse_is_stable():
     s2, c2, o2, _ = dw.step(ws)
     assert (s1 == s2).all() and (c1 == c2).all()
     assert (o1 == o2).all()  # deterministic merge order
+
+
+def test_one_workspace_serves_every_call():
+    # select, attend and step share one workspace (sized for the step) in any order
+    import block_sparse_long_quest_gb300 as kt
+    w = synth.custom(31, RAGGED, num_q_heads=8, num_kv_heads=2, top_k=4,
+                     head_mode=synth.HEAD_SEPARATE)
+    dw = DevWorkload(w)
+    dw.build_reps()
+    ws = kt.workspace(kt.KT_OP_SPARSE_STEP, dw.kv, dw.params)
+    s0, c0, o0, _ = dw.step(ws)
+    out_a, _ = dw.attend(s0, c0, ws)
+    s1, c1, _, _ = dw.select(ws)
+    dense, _ = dw.dense(ws)
+    s2, c2, o2, _ = dw.step(ws)
+    assert (s0 == s1).all() and (c0 == c1).all() and (s0 == s2).all()
+    assert (o0 == o2).all() and (o0 == out_a).all()
+    assert kt.kt_read_device_status(ws) == kt.KT_OK
