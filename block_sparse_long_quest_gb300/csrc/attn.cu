@@ -130,18 +130,33 @@ __device__ __forceinline__ long long range_start(int c, long long U, int NC) {
   return (long long)c * U / NC;
 }
 
-// Calls f(c) for every CTA c (ascending) whose non-empty range of a phase
-// with U units overlaps units [x, y).
+// CTA whose range holds unit u (0 <= u < U) when U units are split into NC
+// ranges [floor(c U / NC), floor((c+1) U / NC)).
+__device__ __forceinline__ int cta_of_unit(long long u, long long U, int NC) {
+  return (int)(((u + 1) * NC + U - 1) / U - 1);
+}
+
+// Calls f(c) for every CTA c (ascending) whose non-empty range of a phase with
+// U units overlaps units [x, y).  With U >= NC every range is non-empty, so the
+// overlapping CTAs are the interval [cta(x), cta(y-1)]; with U < NC every
+// non-empty range holds exactly one unit.
 template <class F>
 __device__ __forceinline__ void for_overlapping_ctas(long long x, long long y, long long U, int NC,
                                                      F f) {
   if (y <= x || U <= 0) return;
-  long long clo = ((x + 1) * NC + U - 1) / U - 1;
-  long long chi = (y * NC + U - 1) / U - 1;
-  if (clo < 0) clo = 0;
-  if (chi > NC - 1) chi = NC - 1;
-  for (long long c = clo; c <= chi; ++c)
-    if (range_start((int)c, U, NC) < range_start((int)c + 1, U, NC)) f((int)c);
+  if (U >= NC) {
+    const int chi = cta_of_unit(y - 1, U, NC);
+    for (int c = cta_of_unit(x, U, NC); c <= chi; ++c) f(c);
+  } else {
+    for (long long u = x; u < y; ++u) f(cta_of_unit(u, U, NC));
+  }
+}
+
+__device__ __forceinline__ int count_overlapping_ctas(long long x, long long y, long long U,
+                                                      int NC) {
+  if (y <= x || U <= 0) return 0;
+  if (U < NC) return (int)(y - x);
+  return cta_of_unit(y - 1, U, NC) - cta_of_unit(x, U, NC) + 1;
 }
 
 __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant__ Params p) {
@@ -373,10 +388,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   };
 
   auto expected_parts = [&](int seg, long long UB) {
-    int n = 0;
-    for_overlapping_ctas(prefA[seg], prefA[seg + 1], UA, NC, [&](int) { ++n; });
-    for_overlapping_ctas(prefB[seg], prefB[seg + 1], UB, NC, [&](int) { ++n; });
-    return n;
+    return count_overlapping_ctas(prefA[seg], prefA[seg + 1], UA, NC) +
+           count_overlapping_ctas(prefB[seg], prefB[seg + 1], UB, NC);
   };
 
   // Final merge of all partials of `seg` (CTA order, phase A then B).  Thread

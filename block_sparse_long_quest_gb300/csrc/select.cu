@@ -179,14 +179,22 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
   unsigned long long* my_cand = p.cand + (unit_base * p.nchunks + chunk) * p.kk;
 
   if (nloc > 0) {
-    // ---- weights (query heads summed in ascending order)
+    // ---- the unit's query rows -> shared memory (one coalesced pass), then
+    // weights (query heads summed in ascending order)
+    const int nq = nkv * p.G;  // query heads of the unit, contiguous from g0*G
+    __half* qs = reinterpret_cast<__half*>(keys + ((p.chunk + 1) & ~1));  // 16-B aligned
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)b * H_q + g0 * p.G) * D);
+      uint4* dst = reinterpret_cast<uint4*>(qs);
+      for (int i = tid; i < nq * D / 8; i += THREADS) dst[i] = __ldg(src + i);
+    }
+    __syncthreads();
     for (int i = tid; i < wfloats; i += THREADS) {
       if (linear) {
         const int gi = i / (Rw * D), r = (i / D) % Rw, c = i % D;
-        const int g = g0 + gi;
         float acc = 0.0f;
         for (int hh = 0; hh < p.G; ++hh) {
-          const float qv = __half2float(p.q[((size_t)b * H_q + g * p.G + hh) * D + c]);
+          const float qv = __half2float(qs[(gi * p.G + hh) * D + c]);
           if (p.rep == KT_REP_QUEST)
             acc += (r == 0) ? fminf(qv, 0.0f) : fmaxf(qv, 0.0f);
           else
@@ -194,8 +202,7 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
         }
         wts[i] = acc;
       } else {
-        const int hq = (p.head_mode == KT_HEAD_SHARED ? 0 : g0 * p.G) + i / D;
-        wts[i] = __half2float(p.q[((size_t)b * H_q + hq) * D + i % D]);
+        wts[i] = __half2float(qs[i]);
       }
     }
     __syncthreads();
@@ -393,10 +400,12 @@ size_t select_smem_bytes(const SelectLaunch& a) {
   const int Rw = a.rep == KT_REP_QUEST ? 2 : 1;
   const int wfloats =
       linear ? nkv * Rw * D : (a.head_mode == KT_HEAD_SHARED ? a.H_kv * a.G : a.G) * D;
-  const int chunk_keys = a.plan.chunk;
+  const int chunk_keys = (a.plan.chunk + 1) & ~1;
   const int merged = a.plan.nchunks * a.plan.kk;
   const int merge_keys = merged + (a.top_k < merged ? a.top_k : merged);
-  const int nkeys = chunk_keys > merge_keys ? chunk_keys : merge_keys;
+  const int nq = nkv * a.G;
+  const int score_keys = chunk_keys + (nq * D * 2 + 7) / 8;  // keys + staged q rows
+  const int nkeys = score_keys > merge_keys ? score_keys : merge_keys;
   return (size_t)((wfloats * 4 + 15) & ~15) + (size_t)nkeys * 8;
 }
 
