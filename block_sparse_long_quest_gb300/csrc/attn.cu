@@ -18,21 +18,24 @@
 //     ring, plus a bulk copy of the segment's G query rows.  Phase-B work waits
 //     on griddepcontrol.wait, so when this kernel is a programmatic dependent
 //     of the selection kernel, Initial/Local streaming overlaps selection.
-//   - Four consumer warps each take 16 tokens of a unit: S = q K^T and
-//     O += P V on mma.sync m16n8k16 (fp16 in, fp32 accumulate).  Query heads
-//     are rows 0..G-1 of the A operand; in P V the fp16 split P = P_hi + P_lo
-//     puts P_hi in rows 0..7 and P_lo in rows 8..15 of the same fragment, so P
-//     keeps ~22 bits.  Online softmax (base 2) per warp, merged at segment end.
-//   - Each CTA writes one (m, l, acc) partial per segment it touched; the CTA
-//     that takes a segment's last ticket merges the partials in CTA order
+//   - Eight consumer warps each take 8 tokens of a unit (two warps per SM
+//     sub-partition, so one hides the other's latency): S = q K^T on mma.sync
+//     m16n8k16 and O += P V on m16n8k8 (fp16 in, fp32 accumulate).  Query
+//     heads are rows 0..G-1 of the A operand; in P V the fp16 split
+//     P = P_hi + P_lo puts P_hi in rows 0..7 and P_lo in rows 8..15 of the same
+//     fragment, so P keeps ~22 bits.  Online softmax (base 2) per warp, merged
+//     through shared memory when the CTA moves to another segment or phase.
+//   - Each CTA writes one (m, l, acc) partial per segment and phase it touched
+//     and, after its last unit, takes one ticket per partial; the CTA that
+//     completes a segment's count merges its partials in CTA order
 //     (deterministic) and writes out[b][h].
 #include "kt_internal.cuh"
 
 namespace kt {
 namespace {
 
-constexpr int STAGES = 5;
-constexpr int CONSUMERS = 4;
+constexpr int STAGES = 4;
+constexpr int CONSUMERS = 8;
 constexpr int THREADS = (CONSUMERS + 1) * 32;
 constexpr int UNIT = 64;
 constexpr int BOX_BYTES = UNIT * 64 * 2;       // 64 tokens x 64 channels fp16
@@ -51,10 +54,11 @@ struct SmemLayout {
   static constexpr int prefA = scratch + SCRATCH_FLOATS * 4;
   static constexpr int prefB = prefA + (MAX_SEGS + 1) * 4;
   static constexpr int sl = prefB + (MAX_SEGS + 1) * 4;
-  static constexpr int info = sl + MAX_SEGS * 4;
+  static constexpr int touched = sl + MAX_SEGS * 4;
+  static constexpr int info = touched + 64 * 4;
   static constexpr int bars = (info + STAGES * (int)sizeof(StageInfo) + 15) & ~15;
   static constexpr int bcast = bars + 2 * STAGES * 8;
-  static constexpr int total = bcast + 64;
+  static constexpr int total = bcast + 64 * 4;
 };
 constexpr int SMEM_BYTES = SmemLayout::total + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "attention shared memory exceeds the per-CTA limit");
@@ -211,6 +215,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
 
   if (warp == CONSUMERS) {
     // =========================== producer warp ===============================
+    if (lane == 0) {
+      prefetch_tensormap(&p.kmap);
+      prefetch_tensormap(&p.vmap);
+    }
     const uint64_t policy = l2_evict_first_policy();
     uint32_t it = 0;
     bool ok = true;
@@ -327,13 +335,15 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
 
   // ============================ consumer warps ===============================
   const int g = lane >> 2, t = lane & 3;
-  const int ctid = tid;  // 0..127
+  const int ctid = tid;  // 0 .. CONSUMERS*32-1
+  constexpr int NCT = CONSUMERS * 32;
   float acc[16][4];
   float m_run = -INFINITY, l_part = 0.0f;
   uint32_t qa[8][2];
   int cur_seg = -1, cur_phase = 0;
-  bool a_tickets_done = false;
   bool q_loaded = false;
+  int* touched = reinterpret_cast<int*>(smem + SmemLayout::touched);  // (seg << 1 | phase)
+  int ntouched = 0;  // maintained identically by every consumer thread
   const int slot_stride = p.slot_floats;
   const long long half_slots = (long long)NC + S;
 
@@ -344,7 +354,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     l_part = 0.0f;
   };
 
-  // Merge the four warps' states and write this CTA's partial for `seg`.
+  // Merge the eight warps' states and write this CTA's partial for (seg, phase).
+  // Slot layout: O[G][128], then m[G], then l[G] (base-2 log domain).
   auto flush = [&](int seg, int phase) {
     float l_row = l_part;
     l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
@@ -361,11 +372,11 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         sc[2 + nt * 8 + 2 * t + 1] = acc[nt][1] + acc[nt][3];
       }
     }
-    named_bar_sync(1, CONSUMERS * 32);
+    named_bar_sync(1, NCT);
     const long long slot = (phase == 0 ? 0 : half_slots) + cta + seg;
     float* dst = p.parts + slot * slot_stride;
-    const int c = ctid;
-    for (int gg = 0; gg < p.G; ++gg) {
+    for (int idx = ctid; idx < p.G * D; idx += NCT) {
+      const int gg = idx / D, c = idx % D;
       float M = -INFINITY;
       for (int w = 0; w < CONSUMERS; ++w) M = fmaxf(M, scratch[(w * MAX_G + gg) * (D + 2)]);
       float o = 0.0f, l = 0.0f;
@@ -377,14 +388,18 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
           l += sc[1] * f;
         }
       }
-      dst[gg * D + c] = o;  // slot: O[G][128], then m[G], then l[G]
+      dst[gg * D + c] = o;
       if (c == 0) {
         dst[p.G * D + gg] = M;
         dst[p.G * D + p.G + gg] = l;
       }
     }
-    __threadfence();
-    named_bar_sync(1, CONSUMERS * 32);
+    if (ctid == 0) {
+      if (ntouched < 64) touched[ntouched] = (seg << 1) | phase;
+      else set_status(p.status, KT_ERR_DEVICE_CHECK);  // more partials than the list holds
+    }
+    ++ntouched;
+    named_bar_sync(1, NCT);
   };
 
   auto expected_parts = [&](int seg, long long UB) {
@@ -392,13 +407,13 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
            count_overlapping_ctas(prefB[seg], prefB[seg + 1], UB, NC);
   };
 
-  // Final merge of all partials of `seg` (CTA order, phase A then B).  Thread
-  // 0 lists the partial slots (arithmetic only), then every consumer thread
-  // owns float4 chunks of the G x 128 outputs and streams the partials with
-  // independent loads (online max-rescaling, base 2).
+  // Final merge of all partials of `seg` (CTA order, phase A then B): the slot
+  // list and the per-part weights are staged in shared memory, then each
+  // thread streams float4 chunks of the partial outputs with independent loads.
   auto merge = [&](int seg, long long UB) {
-    __threadfence();
-    int* slots = reinterpret_cast<int*>(scratch);  // up to 2 * MAX_ATTN_CTAS entries
+    int* slots = reinterpret_cast<int*>(scratch);
+    float* wts = scratch + 2 * MAX_ATTN_CTAS;  // [part][G] weights, then per-head L
+    const int cap = (SCRATCH_FLOATS - 2 * MAX_ATTN_CTAS) / p.G - 1;  // parts per batch
     if (ctid == 0) {
       int np = 0;
       for_overlapping_ctas(prefA[seg], prefA[seg + 1], UA, NC,
@@ -407,48 +422,85 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
                            [&](int cc) { slots[np++] = (int)half_slots + cc + seg; });
       bcast[1] = np;
     }
-    named_bar_sync(1, CONSUMERS * 32);
+    named_bar_sync(1, NCT);
     const int np = bcast[1];
     const int b = seg / p.H_kv, h = seg % p.H_kv;
-    for (int f = 4 * ctid; f < p.G * D; f += 4 * CONSUMERS * 32) {
-      const int gg = f / D, c = f % D;
-      float M = -INFINITY, L = 0.0f;
-      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-      for (int i = 0; i < np; ++i) {
-        const float* src = p.parts + (size_t)slots[i] * slot_stride;
-        const float m = __ldcg(src + p.G * D + gg);
-        const float l = __ldcg(src + p.G * D + p.G + gg);
-        const float4 o = __ldcg(reinterpret_cast<const float4*>(src + f));
-        if (m == -INFINITY) continue;
-        const float Mn = fmaxf(M, m);
-        const float a = exp2f(M - Mn), w = exp2f(m - Mn);
-        L = L * a + l * w;
-        O.x = O.x * a + o.x * w;
-        O.y = O.y * a + o.y * w;
-        O.z = O.z * a + o.z * w;
-        O.w = O.w * a + o.w * w;
-        M = Mn;
+    float* Ms = reinterpret_cast<float*>(bcast + 8);        // [G] running max
+    float* Ls = reinterpret_cast<float*>(bcast + 8 + MAX_G);  // [G] running sum
+    float* As = reinterpret_cast<float*>(bcast + 8 + 2 * MAX_G);  // [G] rescale of old sums
+    if (ctid < p.G) {
+      Ms[ctid] = -INFINITY;
+      Ls[ctid] = 0.0f;
+    }
+    // each thread owns float4 chunks f of the G x 128 outputs
+    float4 O[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int p0 = 0; p0 < np; p0 += cap) {
+      const int nb = min(cap, np - p0);
+      named_bar_sync(1, NCT);
+      // weights of this batch: w[i][g] = exp2(m_i - M_g), M_g the running max
+      for (int e = ctid; e < nb * p.G; e += NCT) {
+        const int i = e / p.G, gg = e % p.G;
+        wts[e] = __ldcg(p.parts + (size_t)slots[p0 + i] * slot_stride + p.G * D + gg);
       }
+      named_bar_sync(1, NCT);
+      if (warp < p.G) {  // warp gg reduces head gg
+        const int gg = warp;
+        float mx = -INFINITY;
+        for (int i = lane; i < nb; i += 32) mx = fmaxf(mx, wts[i * p.G + gg]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float Mold = Ms[gg];
+        const float Mn = fmaxf(Mold, mx);
+        float lsum = 0.0f;
+        for (int i = lane; i < nb; i += 32) {
+          const float m = wts[i * p.G + gg];
+          const float w = (m == -INFINITY) ? 0.0f : exp2f(m - Mn);
+          lsum += w * __ldcg(p.parts + (size_t)slots[p0 + i] * slot_stride + p.G * D + p.G + gg);
+          wts[i * p.G + gg] = w;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+        if (lane == 0) {
+          const float a = (Mold == -INFINITY) ? 0.0f : exp2f(Mold - Mn);
+          As[gg] = a;
+          Ls[gg] = Ls[gg] * a + lsum;
+          Ms[gg] = Mn;
+        }
+      }
+      named_bar_sync(1, NCT);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int f = 4 * (ctid + k * NCT);
+        if (f >= p.G * D) continue;
+        const int gg = f / D;
+        const float a = As[gg];
+        float4 o = make_float4(O[k].x * a, O[k].y * a, O[k].z * a, O[k].w * a);
+#pragma unroll 8
+        for (int i = 0; i < nb; ++i) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(
+              p.parts + (size_t)slots[p0 + i] * slot_stride + f));
+          const float w = wts[i * p.G + gg];
+          o.x = fmaf(v.x, w, o.x);
+          o.y = fmaf(v.y, w, o.y);
+          o.z = fmaf(v.z, w, o.z);
+          o.w = fmaf(v.w, w, o.w);
+        }
+        O[k] = o;
+      }
+    }
+    named_bar_sync(1, NCT);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int f = 4 * (ctid + k * NCT);
+      if (f >= p.G * D) continue;
+      const int gg = f / D, c = f % D;
+      const float L = Ls[gg];
       const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-      float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)b * H_q + h * p.G + gg) * D + c);
-      *dst = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+      *reinterpret_cast<float4*>(p.out + ((size_t)b * H_q + h * p.G + gg) * D + c) =
+          make_float4(O[k].x * inv, O[k].y * inv, O[k].z * inv, O[k].w * inv);
     }
     if (ctid == 0) p.counters[seg] = 0;
-    named_bar_sync(1, CONSUMERS * 32);
-  };
-
-  // Ticket for `seg`; the CTA that completes the count merges.
-  auto ticket = [&](int seg, long long UB) {
-    if (ctid == 0) {
-      const int expect = expected_parts(seg, UB);
-      const int old = atomicAdd(p.counters + seg, 1);
-      bcast[0] = (old + 1 == expect) ? 1 : 0;
-    }
-    named_bar_sync(1, CONSUMERS * 32);
-    const bool last = bcast[0] != 0;
-    named_bar_sync(1, CONSUMERS * 32);
-    if (last) merge(seg, UB);
+    named_bar_sync(1, NCT);
   };
 
   reset_state();
@@ -457,19 +509,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     if (!mbar_wait(bar_full + 8 * st, (it / STAGES) & 1, p.status)) break;
     const StageInfo in = info[st];
     if (in.end || in.seg != cur_seg || in.phase != cur_phase) {
-      const long long UB = prefB[S];  // valid once phase B or the end marker is visible
-      if (cur_seg >= 0) {
-        flush(cur_seg, cur_phase);
-        if (cur_phase == 1) ticket(cur_seg, UB);
-      }
-      if (!a_tickets_done && (in.end || in.phase == 1)) {
-        a_tickets_done = true;
-        if (a1 > a0) {
-          const int s_first = find_seg(prefA, S, (int)a0);
-          const int s_last = find_seg(prefA, S, (int)(a1 - 1));
-          for (int s = s_first; s <= s_last; ++s) ticket(s, UB);
-        }
-      }
+      if (cur_seg >= 0) flush(cur_seg, cur_phase);
       if (in.end) break;
       cur_seg = in.seg;
       cur_phase = in.phase;
@@ -492,38 +532,34 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       }
       q_loaded = true;
     }
-    if (in.ntok > 0) {
+    if (in.ntok > 0 && warp * 8 < in.ntok) {
       const uint32_t kb = kv_base + st * KV_STAGE_BYTES;
       const uint32_t vb = kb + 2 * BOX_BYTES;
       const int mi = lane >> 3, r = lane & 7;
-      // ---- S = q K^T for this warp's 16 tokens
-      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const int tok = warp * 8 + r;  // this warp's 8 tokens
+      // ---- S = q K^T: one n-tile of 8 tokens, k = 128 channels as two
+      // independent accumulation chains
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int tok = warp * 16 + (mi >> 1) * 8 + r;
-        const int chunk = kk * 2 + (mi & 1);
+      for (int j = 0; j < 4; ++j) {
+        const int chunk = 4 * j + mi;  // 8-channel chunks 4j .. 4j+3
         const uint32_t addr = kb + (chunk >> 3) * BOX_BYTES + tok * 128 +
                               (((chunk & 7) ^ (tok & 7)) << 4);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(b0, b1, b2, b3, addr);
-        mma_16816(s[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
-        mma_16816(s[1], qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+        mma_16816(sa, qa[2 * j][0], 0u, qa[2 * j][1], 0u, b0, b1);
+        mma_16816(sb, qa[2 * j + 1][0], 0u, qa[2 * j + 1][1], 0u, b2, b3);
       }
       // ---- online softmax (base 2), rows = query heads
-      float x[4];
-      const int tok0 = warp * 16 + 2 * t;
-      x[0] = (tok0 < in.ntok) ? s[0][0] * p.scale_log2 : -INFINITY;
-      x[1] = (tok0 + 1 < in.ntok) ? s[0][1] * p.scale_log2 : -INFINITY;
-      x[2] = (tok0 + 8 < in.ntok) ? s[1][0] * p.scale_log2 : -INFINITY;
-      x[3] = (tok0 + 9 < in.ntok) ? s[1][1] * p.scale_log2 : -INFINITY;
-      float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+      const int tk = warp * 8 + 2 * t;
+      const float x0 = (tk < in.ntok) ? (sa[0] + sb[0]) * p.scale_log2 : -INFINITY;
+      const float x1 = (tk + 1 < in.ntok) ? (sa[1] + sb[1]) * p.scale_log2 : -INFINITY;
+      float mx = fmaxf(x0, x1);
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const float m_new = fmaxf(m_run, mx);
       const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-      float pr[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) pr[i] = exp2f(x[i] - m_use);
+      const float p0 = exp2f(x0 - m_use), p1 = exp2f(x1 - m_use);
       if (__any_sync(0xffffffffu, m_new != m_run)) {
         const float alpha = exp2f(m_run - m_use);
         l_part *= alpha;
@@ -536,33 +572,53 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         }
       }
       m_run = m_new;
-      l_part += (pr[0] + pr[1]) + (pr[2] + pr[3]);
-      // ---- P = P_hi + P_lo (rows 0..7 hi, rows 8..15 lo)
-      __half hi[4], lo[4];
+      l_part += p0 + p1;
+      // ---- P = P_hi (row g) + P_lo (row g+8)
+      const __half h0 = __float2half_rn(p0), h1 = __float2half_rn(p1);
+      const __half l0 = __float2half_rn(p0 - __half2float(h0));
+      const __half l1 = __float2half_rn(p1 - __half2float(h1));
+      const uint32_t pa0 = pack_half2(h0, h1), pa1 = pack_half2(l0, l1);
+      // ---- O += P V over this warp's 8 tokens (k = 8), 16 channel tiles
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        hi[i] = __float2half_rn(pr[i]);
-        lo[i] = __float2half_rn(pr[i] - __half2float(hi[i]));
-      }
-      const uint32_t pa0 = pack_half2(hi[0], hi[1]);
-      const uint32_t pa1 = pack_half2(lo[0], lo[1]);
-      const uint32_t pa2 = pack_half2(hi[2], hi[3]);
-      const uint32_t pa3 = pack_half2(lo[2], lo[3]);
-      // ---- O += P V
-#pragma unroll
-      for (int cp = 0; cp < 8; ++cp) {
-        const int tok = warp * 16 + (mi & 1) * 8 + r;
-        const int chunk = cp * 2 + (mi >> 1);
+      for (int j = 0; j < 4; ++j) {
+        const int chunk = 4 * j + mi;
         const uint32_t addr = vb + (chunk >> 3) * BOX_BYTES + tok * 128 +
                               (((chunk & 7) ^ (tok & 7)) << 4);
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(b0, b1, b2, b3, addr);
-        mma_16816(acc[2 * cp], pa0, pa1, pa2, pa3, b0, b1);
-        mma_16816(acc[2 * cp + 1], pa0, pa1, pa2, pa3, b2, b3);
+        mma_1688(acc[4 * j + 0], pa0, pa1, b0);
+        mma_1688(acc[4 * j + 1], pa0, pa1, b1);
+        mma_1688(acc[4 * j + 2], pa0, pa1, b2);
+        mma_1688(acc[4 * j + 3], pa0, pa1, b3);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+  }
+
+  // ---- tickets: one per partial this CTA wrote; the completing CTA merges
+  const long long UB = prefB[S];  // the producer wrote it before the end marker
+  __threadfence();
+  named_bar_sync(1, NCT);
+  int* lastflag = bcast + 32;  // up to 32 flags, then chunks of 32
+  if (ntouched > 64) ntouched = 64;
+  for (int base = 0; base < ntouched; base += 32) {
+    const int n_here = min(32, ntouched - base);
+    if (ctid < n_here) {
+      const int code = touched[base + ctid];
+      const int seg = code >> 1;
+      const int old = atomicAdd(p.counters + seg, 1);
+      lastflag[ctid] = (old + 1 == expected_parts(seg, UB)) ? (seg + 1) : 0;
+    }
+    named_bar_sync(1, NCT);
+    for (int i = 0; i < n_here; ++i) {
+      const int seg1 = lastflag[i];
+      if (seg1) {
+        __threadfence();
+        merge(seg1 - 1, UB);
+      }
+    }
+    named_bar_sync(1, NCT);
   }
 }
 
