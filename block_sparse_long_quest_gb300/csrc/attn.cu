@@ -58,7 +58,7 @@ struct SmemLayout {
   static constexpr int info = touched + 64 * 4;
   static constexpr int bars = (info + STAGES * (int)sizeof(StageInfo) + 15) & ~15;
   static constexpr int bcast = bars + 2 * STAGES * 8;
-  static constexpr int total = bcast + 64 * 4;
+  static constexpr int total = bcast + 128 * 4;
 };
 constexpr int SMEM_BYTES = SmemLayout::total + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "attention shared memory exceeds the per-CTA limit");
@@ -373,25 +373,36 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       }
     }
     named_bar_sync(1, NCT);
+    // per head: M = max over warps, weights exp2(m_w - M), L = sum l_w w
+    float* fw = reinterpret_cast<float*>(bcast + 32);  // [G][CONSUMERS] weights
+    float* fm = reinterpret_cast<float*>(bcast + 8);   // [G] M, then [G] L at +MAX_G
+    if (ctid < p.G) {
+      const int gg = ctid;
+      float M = -INFINITY;
+      for (int w = 0; w < CONSUMERS; ++w) M = fmaxf(M, scratch[(w * MAX_G + gg) * (D + 2)]);
+      float L = 0.0f;
+      for (int w = 0; w < CONSUMERS; ++w) {
+        const float* sc = scratch + (w * MAX_G + gg) * (D + 2);
+        const float wt = (M == -INFINITY) ? 0.0f : exp2f(sc[0] - M);
+        fw[gg * CONSUMERS + w] = wt;
+        L += sc[1] * wt;
+      }
+      fm[gg] = M;
+      fm[MAX_G + gg] = L;
+    }
+    named_bar_sync(1, NCT);
     const long long slot = (phase == 0 ? 0 : half_slots) + cta + seg;
     float* dst = p.parts + slot * slot_stride;
     for (int idx = ctid; idx < p.G * D; idx += NCT) {
       const int gg = idx / D, c = idx % D;
-      float M = -INFINITY;
-      for (int w = 0; w < CONSUMERS; ++w) M = fmaxf(M, scratch[(w * MAX_G + gg) * (D + 2)]);
-      float o = 0.0f, l = 0.0f;
-      if (M != -INFINITY) {
-        for (int w = 0; w < CONSUMERS; ++w) {
-          const float* sc = scratch + (w * MAX_G + gg) * (D + 2);
-          const float f = exp2f(sc[0] - M);
-          o += sc[2 + c] * f;
-          l += sc[1] * f;
-        }
-      }
+      float o = 0.0f;
+#pragma unroll
+      for (int w = 0; w < CONSUMERS; ++w)
+        o = fmaf(scratch[(w * MAX_G + gg) * (D + 2) + 2 + c], fw[gg * CONSUMERS + w], o);
       dst[gg * D + c] = o;
       if (c == 0) {
-        dst[p.G * D + gg] = M;
-        dst[p.G * D + p.G + gg] = l;
+        dst[p.G * D + gg] = fm[gg];
+        dst[p.G * D + p.G + gg] = fm[MAX_G + gg];
       }
     }
     if (ctid == 0) {
@@ -407,13 +418,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
            count_overlapping_ctas(prefB[seg], prefB[seg + 1], UB, NC);
   };
 
-  // Final merge of all partials of `seg` (CTA order, phase A then B): the slot
-  // list and the per-part weights are staged in shared memory, then each
-  // thread streams float4 chunks of the partial outputs with independent loads.
+  // Final merge of all partials of `seg` (CTA order, phase A then B).  Thread
+  // 0 lists the partial slots (arithmetic only).  Each thread then owns one
+  // float4 chunk of the G x 128 outputs and a share of the partials, loads
+  // them in batches of 16 with independent loads, and merges online (base 2);
+  // the shares are combined through shared memory in a fixed order.
   auto merge = [&](int seg, long long UB) {
     int* slots = reinterpret_cast<int*>(scratch);
-    float* wts = scratch + 2 * MAX_ATTN_CTAS;  // [part][G] weights, then per-head L
-    const int cap = (SCRATCH_FLOATS - 2 * MAX_ATTN_CTAS) / p.G - 1;  // parts per batch
+    float* red = scratch + 2 * MAX_ATTN_CTAS;  // per thread: M, L, O.xyzw
     if (ctid == 0) {
       int np = 0;
       for_overlapping_ctas(prefA[seg], prefA[seg + 1], UA, NC,
@@ -425,79 +437,71 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     named_bar_sync(1, NCT);
     const int np = bcast[1];
     const int b = seg / p.H_kv, h = seg % p.H_kv;
-    float* Ms = reinterpret_cast<float*>(bcast + 8);        // [G] running max
-    float* Ls = reinterpret_cast<float*>(bcast + 8 + MAX_G);  // [G] running sum
-    float* As = reinterpret_cast<float*>(bcast + 8 + 2 * MAX_G);  // [G] rescale of old sums
-    if (ctid < p.G) {
-      Ms[ctid] = -INFINITY;
-      Ls[ctid] = 0.0f;
+    const int nchunk = p.G * D / 4;             // float4 chunks of the output
+    const int nsplit = NCT / nchunk;            // 1 (G=8), 2 (G=4), 4, 8
+    const int ch = ctid % nchunk, sp = ctid / nchunk;
+    const int f = 4 * ch, gg = f / D;
+    const int i0 = sp * np / nsplit, i1 = (sp + 1) * np / nsplit;
+    float M = -INFINITY, L = 0.0f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int base = i0; base < i1; base += 16) {
+      const int nb = min(16, i1 - base);
+      float m[16], l[16];
+      float4 o[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        if (k < nb) {
+          const float* src = p.parts + (size_t)slots[base + k] * slot_stride;
+          m[k] = __ldcg(src + p.G * D + gg);
+          l[k] = __ldcg(src + p.G * D + p.G + gg);
+          o[k] = __ldcg(reinterpret_cast<const float4*>(src + f));
+        } else {
+          m[k] = -INFINITY;
+          l[k] = 0.0f;
+          o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      float Mn = M;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) Mn = fmaxf(Mn, m[k]);
+      if (Mn == -INFINITY) continue;
+      const float a = exp2f(M - Mn);  // 0 when M is -inf
+      L *= a;
+      O.x *= a; O.y *= a; O.z *= a; O.w *= a;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float w = exp2f(m[k] - Mn);  // 0 for empty partials
+        L = fmaf(l[k], w, L);
+        O.x = fmaf(o[k].x, w, O.x);
+        O.y = fmaf(o[k].y, w, O.y);
+        O.z = fmaf(o[k].z, w, O.z);
+        O.w = fmaf(o[k].w, w, O.w);
+      }
+      M = Mn;
     }
-    // each thread owns float4 chunks f of the G x 128 outputs
-    float4 O[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-    for (int p0 = 0; p0 < np; p0 += cap) {
-      const int nb = min(cap, np - p0);
+    if (nsplit > 1) {
+      float* r = red + 6 * ctid;
+      r[0] = M; r[1] = L; r[2] = O.x; r[3] = O.y; r[4] = O.z; r[5] = O.w;
       named_bar_sync(1, NCT);
-      // weights of this batch: w[i][g] = exp2(m_i - M_g), M_g the running max
-      for (int e = ctid; e < nb * p.G; e += NCT) {
-        const int i = e / p.G, gg = e % p.G;
-        wts[e] = __ldcg(p.parts + (size_t)slots[p0 + i] * slot_stride + p.G * D + gg);
-      }
-      named_bar_sync(1, NCT);
-      if (warp < p.G) {  // warp gg reduces head gg
-        const int gg = warp;
-        float mx = -INFINITY;
-        for (int i = lane; i < nb; i += 32) mx = fmaxf(mx, wts[i * p.G + gg]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float Mold = Ms[gg];
-        const float Mn = fmaxf(Mold, mx);
-        float lsum = 0.0f;
-        for (int i = lane; i < nb; i += 32) {
-          const float m = wts[i * p.G + gg];
-          const float w = (m == -INFINITY) ? 0.0f : exp2f(m - Mn);
-          lsum += w * __ldcg(p.parts + (size_t)slots[p0 + i] * slot_stride + p.G * D + p.G + gg);
-          wts[i * p.G + gg] = w;
+      if (sp == 0) {
+        for (int q = 1; q < nsplit; ++q) {
+          const float* o2 = red + 6 * (ctid + q * nchunk);
+          const float Mn = fmaxf(M, o2[0]);
+          if (Mn == -INFINITY) continue;
+          const float a = exp2f(M - Mn), w = exp2f(o2[0] - Mn);
+          L = L * a + o2[1] * w;
+          O.x = O.x * a + o2[2] * w;
+          O.y = O.y * a + o2[3] * w;
+          O.z = O.z * a + o2[4] * w;
+          O.w = O.w * a + o2[5] * w;
+          M = Mn;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-        if (lane == 0) {
-          const float a = (Mold == -INFINITY) ? 0.0f : exp2f(Mold - Mn);
-          As[gg] = a;
-          Ls[gg] = Ls[gg] * a + lsum;
-          Ms[gg] = Mn;
-        }
-      }
-      named_bar_sync(1, NCT);
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int f = 4 * (ctid + k * NCT);
-        if (f >= p.G * D) continue;
-        const int gg = f / D;
-        const float a = As[gg];
-        float4 o = make_float4(O[k].x * a, O[k].y * a, O[k].z * a, O[k].w * a);
-#pragma unroll 8
-        for (int i = 0; i < nb; ++i) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(
-              p.parts + (size_t)slots[p0 + i] * slot_stride + f));
-          const float w = wts[i * p.G + gg];
-          o.x = fmaf(v.x, w, o.x);
-          o.y = fmaf(v.y, w, o.y);
-          o.z = fmaf(v.z, w, o.z);
-          o.w = fmaf(v.w, w, o.w);
-        }
-        O[k] = o;
       }
     }
-    named_bar_sync(1, NCT);
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int f = 4 * (ctid + k * NCT);
-      if (f >= p.G * D) continue;
-      const int gg = f / D, c = f % D;
-      const float L = Ls[gg];
+    if (sp == 0) {
       const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-      *reinterpret_cast<float4*>(p.out + ((size_t)b * H_q + h * p.G + gg) * D + c) =
-          make_float4(O[k].x * inv, O[k].y * inv, O[k].z * inv, O[k].w * inv);
+      *reinterpret_cast<float4*>(p.out + ((size_t)b * H_q + h * p.G + gg) * D + (f % D)) =
+          make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
     }
     if (ctid == 0) p.counters[seg] = 0;
     named_bar_sync(1, NCT);
@@ -600,7 +604,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   const long long UB = prefB[S];  // the producer wrote it before the end marker
   __threadfence();
   named_bar_sync(1, NCT);
-  int* lastflag = bcast + 32;  // up to 32 flags, then chunks of 32
+  int* lastflag = bcast + 96;  // 32 flags per round
   if (ntouched > 64) ntouched = 64;
   for (int base = 0; base < ntouched; base += 32) {
     const int n_here = min(32, ntouched - base);

@@ -77,19 +77,53 @@ __device__ __forceinline__ unsigned long long make_key(float score, int block) {
 
 // k-th largest of N distinct keys in shared memory (1 <= k <= N), all threads
 // of the CTA.  On return, a key is among the k largest iff
-// (key & *mask_out) >= *prefix_out.
+// (key & *mask_out) >= *prefix_out.  MSB-first radix select on 8-bit digits;
+// the leading bits common to every key are skipped, and histogram updates are
+// aggregated per warp (__match_any_sync) so that equal digits do not
+// serialise on one shared-memory address.
 __device__ void radix_select(const unsigned long long* keys, int N, int k, unsigned int* hist,
                              unsigned long long* sh_u64, int* sh_int,
                              unsigned long long* prefix_out, unsigned long long* mask_out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  unsigned long long prefix = 0ull, mask = 0ull;
+  // common leading bits: AND and OR over all keys
+  unsigned long long a = ~0ull, o = 0ull;
+  for (int i = tid; i < N; i += THREADS) {
+    a &= keys[i];
+    o |= keys[i];
+  }
+  unsigned int alo = __reduce_and_sync(0xffffffffu, (unsigned)a);
+  unsigned int ahi = __reduce_and_sync(0xffffffffu, (unsigned)(a >> 32));
+  unsigned int olo = __reduce_or_sync(0xffffffffu, (unsigned)o);
+  unsigned int ohi = __reduce_or_sync(0xffffffffu, (unsigned)(o >> 32));
+  if (tid == 0) {
+    sh_u64[0] = ~0ull;
+    sh_u64[1] = 0ull;
+  }
+  __syncthreads();
+  if (lane == 0) {
+    atomicAnd(&sh_u64[0], ((unsigned long long)ahi << 32) | alo);
+    atomicOr(&sh_u64[1], ((unsigned long long)ohi << 32) | olo);
+  }
+  __syncthreads();
+  const unsigned long long all_and = sh_u64[0], diff = all_and ^ sh_u64[1];
+  __syncthreads();
+  int top = diff ? 63 - __clzll((long long)diff) : 0;  // highest differing bit
+  int shift = (top / 8) * 8;
+  unsigned long long mask = (shift + 8 >= 64) ? 0ull : ~((1ull << (shift + 8)) - 1);
+  unsigned long long prefix = all_and & mask;
   int need = k;
-  for (int shift = 56; shift >= 0; shift -= 8) {
+  for (; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += THREADS) hist[i] = 0u;
     __syncthreads();
-    for (int i = tid; i < N; i += THREADS) {
-      const unsigned long long key = keys[i];
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    for (int base = 0; base < N; base += THREADS) {
+      const int i = base + tid;
+      unsigned int bin = 256u;
+      if (i < N) {
+        const unsigned long long key = keys[i];
+        if ((key & mask) == prefix) bin = (unsigned)((key >> shift) & 255u);
+      }
+      const unsigned int peers = __match_any_sync(0xffffffffu, bin);
+      if (bin < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
     }
     __syncthreads();
     if (warp == 0) {
@@ -103,9 +137,9 @@ __device__ void radix_select(const unsigned long long* keys, int N, int k, unsig
       }
       unsigned int incl = local;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+      for (int d = 1; d < 32; d <<= 1) {
+        const unsigned int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
       }
       const unsigned int excl = incl - local;
       const bool hit = excl < (unsigned)need && (unsigned)need <= incl;
