@@ -220,7 +220,10 @@ kt_status attn_impl(const void* q, const kt_paged_kv* kv, int num_q_heads, float
   a.dense = dense ? 1 : 0;
   a.slot_floats = L.slot_floats;
   a.scale_log2 = (float)((double)scale * 1.4426950408889634);
-  a.grid = sms < MAX_ATTN_CTAS ? sms : MAX_ATTN_CTAS;
+  // at least one CTA per (sequence, KV head) segment, at least one per SM
+  const int nseg = kv->batch * kv->num_kv_heads;
+  const int base = sms < MAX_ATTN_CTAS ? sms : MAX_ATTN_CTAS;
+  a.grid = base > nseg ? base : nseg;
   a.pdl = pdl;
   return cuda_status(launch_attention(a, stream));
 }
