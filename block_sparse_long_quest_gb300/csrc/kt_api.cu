@@ -128,14 +128,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [rows = pages*heads*128][128 channels] fp16, boxes of 64 channels x 64 rows,
-// 128-byte swizzle (the attention kernel's ldmatrix addressing assumes it).
+// [rows = pages*heads*128][128 channels] fp16, boxes of 64 channels x 128 rows
+// (one block of one head, half its channels), 128-byte swizzle; the attention
+// kernel's stage size and ldmatrix addressing assume exactly this box.
 bool make_pool_map(CUtensorMap* map, const void* pool, const kt_paged_kv* kv) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)kv->num_pages * kv->num_kv_heads * BS};
   cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {64, (cuuint32_t)BS};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(pool), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -21,7 +21,7 @@ constexpr int SEL_TARGET_CTAS = 1024;
 constexpr int SEL_MAX_CAND = 8192;  // candidates merged by the last selection CTA
 constexpr int SEL_MAX_CHUNK = 4096; // context blocks scored by one selection CTA
 constexpr int MAX_DYN_REPS = 32;
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s bound on any device-side wait
+constexpr uint64_t WAIT_LIMIT_NS = 100000000ull;  // 100 ms bound on any device-side wait
 
 // ---------------------------------------------------------------------------
 // Selection chunking and workspace layout.  Host sizing and device addressing

@@ -220,3 +220,27 @@ def test_one_workspace_serves_every_call():
     assert (s0 == s1).all() and (c0 == c1).all() and (s0 == s2).all()
     assert (o0 == o2).all() and (o0 == out_a).all()
     assert kt.kt_read_device_status(ws) == kt.KT_OK
+
+
+def test_more_segments_than_sms_and_empty_sequence():
+    # 45 sequences x 4 KV heads = 180 segments (more than the SM count), one empty
+    lens = [0] + [128 * (3 + (i * 7) % 11) + (i * 37) % 128 for i in range(44)]
+    w = synth.custom(32, lens, num_q_heads=8, num_kv_heads=4, top_k=3,
+                     head_mode=synth.HEAD_SEPARATE)
+    dw = DevWorkload(w)
+    dw.build_reps()
+    sel, cnt, out, ws = dw.step()
+    dense, _ = dw.dense()
+    ref = _oracle(w)
+    out, sel, cnt = out.cpu().numpy(), sel.cpu().numpy(), cnt.cpu().numpy()
+    assert np.all(out[0] == 0.0) and np.all(dense.cpu().numpy()[0] == 0.0)
+    d_ref = oracle.dense(oracle.KV.of(w), w.q, 8, w.params.softmax_scale)
+    assert row_rel_err(dense.cpu().numpy()[1:], d_ref[1:]).max() <= TOL
+    for b in range(1, w.batch):
+        for u in range(4):
+            ok, exact = selection_agrees(sel, cnt, ref, b, u)
+            assert ok
+            if exact:
+                assert row_rel_err(out[b, 2 * u:2 * u + 2], ref["out"][b, 2 * u:2 * u + 2]).max() <= TOL
+    import block_sparse_long_quest_gb300 as kt
+    assert kt.kt_read_device_status(ws) == kt.KT_OK
