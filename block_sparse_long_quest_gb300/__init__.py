@@ -31,7 +31,7 @@ EXPORTS = (
     "kt_workspace_init", "kt_build_block_reps", "kt_build_dynamic_reps",
     "kt_score_select_blocks", "kt_sparse_decode_attn", "kt_sparse_decode_step",
     "kt_sparse_decode_step_host", "kt_dense_decode_attn", "kt_read_device_status",
-    "kt_selftest_bounded_wait",
+    "kt_selftest_bounded_wait", "kt_sparse_decode_attn_noalloc",
 )
 
 
@@ -87,6 +87,8 @@ def _load():
                                                 vp]),
         "kt_read_device_status": (ctypes.c_int, [vp, sz, vp, P(i32)]),
         "kt_selftest_bounded_wait": (ctypes.c_int, [vp, sz, i32, vp]),
+        "kt_sparse_decode_attn_noalloc": (ctypes.c_int, [vp, P(PagedKV), P(SparseParams), vp,
+                                                         vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -224,3 +226,11 @@ def kt_read_device_status(ws, stream=None) -> int:
 def kt_selftest_bounded_wait(ws, spin_limit, stream=None):
     _check(lib.kt_selftest_bounded_wait(_ptr(ws), ws.numel(), spin_limit, _stream(stream)),
            "kt_selftest_bounded_wait")
+
+
+def kt_sparse_decode_attn_noalloc(q, kv, params, sel, cnt, out, stream=None):
+    """kt_sparse_decode_attn without a workspace (scratch in a fixed 1 MiB
+    device array of the library); for callers that cannot allocate."""
+    _check(lib.kt_sparse_decode_attn_noalloc(_ptr(q), ctypes.byref(kv), ctypes.byref(params),
+                                             _ptr(sel), _ptr(cnt), _ptr(out), _stream(stream)),
+           "kt_sparse_decode_attn_noalloc")

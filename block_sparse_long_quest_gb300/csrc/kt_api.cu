@@ -441,3 +441,98 @@ kt_status kt_selftest_bounded_wait(void* ws, size_t ws_bytes, int32_t spin_limit
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of kt_sparse_decode_attn: the scratch memory lives in
+// a fixed-size array of this library's device image instead of a caller
+// workspace.
+// ---------------------------------------------------------------------------
+namespace kt {
+namespace {
+
+constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(1) << 20;  // 1 MiB on every device
+static __device__ __align__(256) unsigned char noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex noalloc_mu;
+void* noalloc_dev_ptr[NOALLOC_MAX_DEVICES];  // device address of the array, per device
+
+// Device address of the scratch array on the current device.  The name
+// `noalloc_scratch` is only a host-side stand-in; the address has to come from
+// cudaGetSymbolAddress with the device current.  Done once per device.
+kt_status noalloc_scratch_ptr(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NOALLOC_MAX_DEVICES)
+    return KT_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(noalloc_mu);
+  if (!noalloc_dev_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, noalloc_scratch) != cudaSuccess || !p) return KT_ERR_CUDA;
+    noalloc_dev_ptr[dev] = p;
+  }
+  *out = noalloc_dev_ptr[dev];
+  return KT_OK;
+}
+
+}  // namespace
+}  // namespace kt
+
+extern "C" kt_status kt_sparse_decode_attn_noalloc(const void* q, const kt_paged_kv* kv,
+                                                   const kt_sparse_params* p, const int32_t* sel,
+                                                   const int32_t* cnt, float* out,
+                                                   kt_stream_t stream) {
+  kt_status s = check_kv(kv);
+  if (s != KT_OK) return s;
+  s = check_params(kv, p);
+  if (s != KT_OK) return s;
+  if (!q || !sel || !cnt || !out || !aligned16(q) || !aligned16(out)) return KT_ERR_INVALID_ARG;
+  const int sms = num_sms();
+  if (sms <= 0) return KT_ERR_CUDA;
+  const int S = kv->batch * kv->num_kv_heads;
+  const int G = p->num_q_heads / kv->num_kv_heads;
+  const int slot_floats = ((2 * G + G * D) + 3) & ~3;
+  const int base = sms < MAX_ATTN_CTAS ? sms : MAX_ATTN_CTAS;
+  const int grid = base > S ? base : S;
+  // status word, one ticket counter per segment, one partial per CTA
+  const size_t counters_off = 256;
+  const size_t parts_off = align256(counters_off + (size_t)S * 4);
+  const size_t need = parts_off + (size_t)grid * slot_floats * 4;
+  if (need > NOALLOC_SCRATCH_BYTES) return KT_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = nullptr;
+  s = noalloc_scratch_ptr(&scratch);
+  if (s != KT_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  // the array keeps the previous call's contents: the status word and the
+  // tickets must start at zero
+  if (cudaMemsetAsync(scratch, 0, parts_off, st) != cudaSuccess) return KT_ERR_CUDA;
+  CUtensorMap kmap, vmap;
+  if (!make_pool_map(&kmap, kv->k_pool, kv) || !make_pool_map(&vmap, kv->v_pool, kv))
+    return KT_ERR_CUDA;
+  AttnLaunch a;
+  a.kmap = &kmap;
+  a.vmap = &vmap;
+  a.q = static_cast<const __half*>(q);
+  a.table = kv->block_table;
+  a.seq_lens = kv->seq_lens;
+  a.sel = sel;
+  a.cnt = cnt;
+  a.out = out;
+  a.status = at<int>(scratch, 0);
+  a.counters = at<int>(scratch, counters_off);
+  a.parts = at<float>(scratch, parts_off);
+  a.B = kv->batch;
+  a.H_kv = kv->num_kv_heads;
+  a.G = G;
+  a.max_blocks = kv->max_blocks_per_seq;
+  a.P = kv->num_pages;
+  a.I_b = p->initial_blocks;
+  a.L_b = p->local_blocks;
+  a.top_k = p->top_k;
+  a.SEL = p->head_mode == KT_HEAD_SHARED ? 1 : kv->num_kv_heads;
+  a.dense = 0;
+  a.slot_floats = slot_floats;
+  a.scale_log2 = (float)((double)p->softmax_scale * 1.4426950408889634);
+  a.grid = grid;
+  a.pdl = false;
+  return cuda_status(launch_attention(a, st));
+}

@@ -257,6 +257,37 @@ kt_status kt_dense_decode_attn(const void* q, const kt_paged_kv* kv, int32_t num
                                kt_stream_t stream);
 
 /*
+ * kt_sparse_decode_attn without a workspace, for callers that cannot allocate
+ * device memory: for example a kernel plugged into an engine or framework
+ * that hands it only its input and output buffers and owns every other byte
+ * of device memory, or a latency-critical path where a cudaMalloc (which can
+ * synchronise the device) is not allowed.  The article has no counterpart:
+ * this is an interface variant, not part of the method.
+ *
+ * Same arguments, results and errors as kt_sparse_decode_attn, minus the
+ * workspace.  Its scratch memory (status word, tickets, split-K partials) is a
+ * fixed 1 MiB array inside this library's device image, which every GPU that
+ * loads the library keeps until the process exits.  It holds one partial of
+ * about G x 520 bytes per attention CTA (max(#SMs, batch*num_kv_heads) CTAs),
+ * so shapes up to roughly batch*num_kv_heads = 500 at G = 4 (250 at G = 8)
+ * fit; larger ones return KT_ERR_WORKSPACE_TOO_SMALL before any launch.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents; each call clears the status word and tickets on
+ *     `stream` before its kernel.  Calls that overlap on the GPU (different
+ *     streams, or host threads without ordering) race on it.
+ *   - Device-side check failures are recorded in the shared array and are not
+ *     reported by this call.
+ *   - It calls no allocator (no cudaMalloc, cudaFree or allocating library
+ *     routine).
+ */
+kt_status kt_sparse_decode_attn_noalloc(const void* q, const kt_paged_kv* kv,
+                                        const kt_sparse_params* p, const int32_t* sel,
+                                        const int32_t* cnt, float* out, kt_stream_t stream);
+
+/*
  * Synchronises `stream`, stores the workspace status word (a kt_status value,
  * KT_OK if no device-side anomaly was recorded since the last read) in
  * *device_status and clears it.
