@@ -78,23 +78,23 @@ __device__ __forceinline__ unsigned long long make_key(float score, int block) {
 // k-th largest of N distinct keys in shared memory (1 <= k <= N), all threads
 // of the CTA.  On return, a key is among the k largest iff
 // (key & *mask_out) >= *prefix_out.  MSB-first radix select on 8-bit digits;
-// the leading bits common to every key are skipped, and histogram updates are
-// aggregated per warp (__match_any_sync) so that equal digits do not
-// serialise on one shared-memory address.
+// the leading bits common to every key are skipped.  hist holds two 256-bin
+// histograms used alternately, so each pass needs two barriers.
 __device__ void radix_select(const unsigned long long* keys, int N, int k, unsigned int* hist,
                              unsigned long long* sh_u64, int* sh_int,
                              unsigned long long* prefix_out, unsigned long long* mask_out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // common leading bits: AND and OR over all keys
+  // common leading bits: AND and OR over all keys; clear both histograms
   unsigned long long a = ~0ull, o = 0ull;
   for (int i = tid; i < N; i += THREADS) {
     a &= keys[i];
     o |= keys[i];
   }
-  unsigned int alo = __reduce_and_sync(0xffffffffu, (unsigned)a);
-  unsigned int ahi = __reduce_and_sync(0xffffffffu, (unsigned)(a >> 32));
-  unsigned int olo = __reduce_or_sync(0xffffffffu, (unsigned)o);
-  unsigned int ohi = __reduce_or_sync(0xffffffffu, (unsigned)(o >> 32));
+  for (int i = tid; i < 512; i += THREADS) hist[i] = 0u;
+  const unsigned int alo = __reduce_and_sync(0xffffffffu, (unsigned)a);
+  const unsigned int ahi = __reduce_and_sync(0xffffffffu, (unsigned)(a >> 32));
+  const unsigned int olo = __reduce_or_sync(0xffffffffu, (unsigned)o);
+  const unsigned int ohi = __reduce_or_sync(0xffffffffu, (unsigned)(o >> 32));
   if (tid == 0) {
     sh_u64[0] = ~0ull;
     sh_u64[1] = 0ull;
@@ -106,24 +106,17 @@ __device__ void radix_select(const unsigned long long* keys, int N, int k, unsig
   }
   __syncthreads();
   const unsigned long long all_and = sh_u64[0], diff = all_and ^ sh_u64[1];
-  __syncthreads();
-  int top = diff ? 63 - __clzll((long long)diff) : 0;  // highest differing bit
+  const int top = diff ? 63 - __clzll((long long)diff) : 0;  // highest differing bit
   int shift = (top / 8) * 8;
   unsigned long long mask = (shift + 8 >= 64) ? 0ull : ~((1ull << (shift + 8)) - 1);
   unsigned long long prefix = all_and & mask;
   int need = k;
-  for (; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += THREADS) hist[i] = 0u;
-    __syncthreads();
-    for (int base = 0; base < N; base += THREADS) {
-      const int i = base + tid;
-      unsigned int bin = 256u;
-      if (i < N) {
-        const unsigned long long key = keys[i];
-        if ((key & mask) == prefix) bin = (unsigned)((key >> shift) & 255u);
-      }
-      const unsigned int peers = __match_any_sync(0xffffffffu, bin);
-      if (bin < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+  for (int pass = 0; shift >= 0; ++pass, shift -= 8) {
+    unsigned int* H = hist + 256 * (pass & 1);
+    unsigned int* Hn = hist + 256 * ((pass + 1) & 1);
+    for (int i = tid; i < N; i += THREADS) {
+      const unsigned long long key = keys[i];
+      if ((key & mask) == prefix) atomicAdd(&H[(key >> shift) & 255u], 1u);
     }
     __syncthreads();
     if (warp == 0) {
@@ -132,7 +125,7 @@ __device__ void radix_select(const unsigned long long* keys, int N, int k, unsig
       unsigned int local = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        c[i] = hist[255 - 8 * lane - i];
+        c[i] = H[255 - 8 * lane - i];
         local += c[i];
       }
       unsigned int incl = local;
@@ -164,22 +157,83 @@ __device__ void radix_select(const unsigned long long* keys, int N, int k, unsig
         sh_int[0] = need2;
         sh_int[1] = (bin == (unsigned)need2) ? 1 : 0;
       }
+    } else {
+      for (int i = tid - 32; i < 256; i += THREADS - 32) Hn[i] = 0u;  // next pass's bins
     }
     __syncthreads();
     prefix = sh_u64[0];
     mask = sh_u64[1];
     need = sh_int[0];
-    const int done = sh_int[1];
-    __syncthreads();
-    if (done) break;
+    if (sh_int[1]) break;
   }
+  __syncthreads();  // sh_* are rewritten by the caller
   *prefix_out = prefix;
   *mask_out = mask;
 }
 
+// Linear scoring (Max, Mean, Quest): each warp scores 8/NV blocks at a time;
+// a lane holds NV 16-byte vectors of each block, and every load of the group is
+// issued before any arithmetic.  V = 16-byte vectors per block and unit.
+template <int NV, bool F32>
+__device__ __forceinline__ void score_linear(const Params& p, int g0, int js, int je,
+                                             const int* pg, const float* wts, int V,
+                                             unsigned long long* keys, int warp, int lane) {
+  constexpr int GB = 8 / NV;
+  constexpr int VE = F32 ? 4 : 8;
+  float w[NV][VE];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int vec = lane + 32 * v;
+#pragma unroll
+    for (int e = 0; e < VE; ++e) w[v][e] = (vec < V) ? wts[vec * VE + e] : 0.0f;
+  }
+  const size_t head_bytes = (size_t)p.R * D * (F32 ? 4 : 2);
+  for (int j0 = js + warp * GB; j0 < je; j0 += WARPS * GB) {
+    uint4 x[GB][NV];
+    int page[GB];
+#pragma unroll
+    for (int bi = 0; bi < GB; ++bi) {
+      const int j = j0 + bi;
+      page[bi] = (j < je) ? pg[j - js] : -1;
+      const bool ok = page[bi] >= 0 && page[bi] < p.P;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const uint8_t*>(p.reps) +
+          ((size_t)(ok ? page[bi] : 0) * p.H_kv + g0) * head_bytes);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int vec = lane + 32 * v;
+        x[bi][v] = (ok && vec < V) ? __ldg(src + vec) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int bi = 0; bi < GB; ++bi) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        if (F32) {
+          const float4 f = *reinterpret_cast<const float4*>(&x[bi][v]);
+          acc = fmaf(w[v][0], f.x, acc);
+          acc = fmaf(w[v][1], f.y, acc);
+          acc = fmaf(w[v][2], f.z, acc);
+          acc = fmaf(w[v][3], f.w, acc);
+        } else {
+          acc += dot8(w[v], x[bi][v]);
+        }
+      }
+      acc = warp_sum(acc);
+      const int j = j0 + bi;
+      if (j < je) {
+        const bool ok = page[bi] >= 0 && page[bi] < p.P;
+        if (lane == 0) keys[j - js] = make_key(ok ? acc : -INFINITY, j);
+        if (!ok && lane == 0) set_status(p.status, KT_ERR_DEVICE_CHECK);
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ unsigned int hist[256];
+  __shared__ unsigned int hist[512];
   __shared__ unsigned long long sh_u64[2];
   __shared__ int sh_int[4];
 
@@ -192,115 +246,86 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
   const int g0 = p.head_mode == KT_HEAD_SHARED ? 0 : u;
   const bool linear = p.rep == KT_REP_MAX || p.rep == KT_REP_MEAN || p.rep == KT_REP_QUEST;
   const int Rw = p.rep == KT_REP_QUEST ? 2 : 1;  // weight rows for linear methods
+  // shared memory: weights (fp32), keys (u64), query rows (fp16), pages (int)
+  float* wts = reinterpret_cast<float*>(smem);
+  const int wfloats = linear ? nkv * Rw * D : (p.head_mode == KT_HEAD_SHARED ? H_q : p.G) * D;
+  unsigned long long* keys =
+      reinterpret_cast<unsigned long long*>(smem + ((wfloats * 4 + 15) & ~15));
+  const int nq = nkv * p.G;  // query heads of the unit, contiguous from g0*G
+  __half* qs = reinterpret_cast<__half*>(keys + ((p.chunk + 1) & ~1));  // 16-B aligned
+  int* pg = reinterpret_cast<int*>(qs + nq * D);
 
+  // ---- independent loads first: sequence length, the chunk's block-table
+  // entries (when the sequence has Context blocks the chunk starts at block
+  // I_b + chunk*CH) and the unit's query rows
   int n = p.seq_lens[b];
+  const int js_nom = p.I_b + chunk * p.chunk;
+  for (int t = tid; t < p.chunk; t += THREADS) {
+    const int j = js_nom + t;
+    pg[t] = (j < p.max_blocks) ? __ldg(p.table + (size_t)b * p.max_blocks + j) : -1;
+  }
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)b * H_q + g0 * p.G) * D);
+    uint4* dst = reinterpret_cast<uint4*>(qs);
+    for (int i = tid; i < nq * D / 8; i += THREADS) dst[i] = __ldg(src + i);
+  }
   if (n < 0 || n > p.max_blocks * BS) {
     set_status(p.status, KT_ERR_DEVICE_CHECK);
     n = n < 0 ? 0 : p.max_blocks * BS;
   }
   const int nb = (n + BS - 1) / BS;
   const int c0 = min(p.I_b, nb), c1 = max(c0, nb - p.L_b);
-  const int js = c0 + chunk * p.chunk, je = min(js + p.chunk, c1);
+  const int js = c0 + chunk * p.chunk, je = min(js + p.chunk, c1);  // js == js_nom if nloc > 0
   const int nloc = max(0, je - js);
-
-  // shared memory: weights (fp32) then keys (u64)
-  float* wts = reinterpret_cast<float*>(smem);
-  const int wfloats = linear ? nkv * Rw * D : (p.head_mode == KT_HEAD_SHARED ? H_q : p.G) * D;
-  unsigned long long* keys =
-      reinterpret_cast<unsigned long long*>(smem + ((wfloats * 4 + 15) & ~15));
 
   const size_t unit_base = (size_t)b * p.SEL + u;
   unsigned long long* my_cand = p.cand + (unit_base * p.nchunks + chunk) * p.kk;
+  __syncthreads();
 
   if (nloc > 0) {
-    // ---- the unit's query rows -> shared memory (one coalesced pass), then
-    // weights (query heads summed in ascending order)
-    const int nq = nkv * p.G;  // query heads of the unit, contiguous from g0*G
-    __half* qs = reinterpret_cast<__half*>(keys + ((p.chunk + 1) & ~1));  // 16-B aligned
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)b * H_q + g0 * p.G) * D);
-      uint4* dst = reinterpret_cast<uint4*>(qs);
-      for (int i = tid; i < nq * D / 8; i += THREADS) dst[i] = __ldg(src + i);
-    }
-    __syncthreads();
-    for (int i = tid; i < wfloats; i += THREADS) {
-      if (linear) {
-        const int gi = i / (Rw * D), r = (i / D) % Rw, c = i % D;
-        float acc = 0.0f;
+    // ---- weights (query heads summed in ascending order)
+    if (linear) {
+      for (int i = tid; i < nkv * D; i += THREADS) {
+        const int gi = i / D, c = i % D;
+        float sum = 0.0f, neg = 0.0f, pos = 0.0f;
         for (int hh = 0; hh < p.G; ++hh) {
           const float qv = __half2float(qs[(gi * p.G + hh) * D + c]);
-          if (p.rep == KT_REP_QUEST)
-            acc += (r == 0) ? fminf(qv, 0.0f) : fmaxf(qv, 0.0f);
-          else
-            acc += qv;
+          sum += qv;
+          neg += fminf(qv, 0.0f);
+          pos += fmaxf(qv, 0.0f);
         }
-        wts[i] = acc;
-      } else {
-        wts[i] = __half2float(qs[i]);
+        if (p.rep == KT_REP_QUEST) {
+          wts[(gi * 2 + 0) * D + c] = neg;  // pairs with the kmin row
+          wts[(gi * 2 + 1) * D + c] = pos;  // pairs with the kmax row
+        } else {
+          wts[gi * D + c] = sum;
+        }
       }
+    } else {
+      for (int i = tid; i < wfloats; i += THREADS) wts[i] = __half2float(qs[i]);
     }
     __syncthreads();
 
     // ---- scores
     if (linear) {
-      // the rep bytes of the unit's KV heads for one block are contiguous
-      const int elems = nkv * p.R * D;  // R == Rw here
       const bool f32 = p.rep == KT_REP_MEAN;
-      const int vec_elems = f32 ? 4 : 8;
-      const int V = elems / vec_elems;  // 16-byte vectors per block
-      for (int j0 = js + warp * 4; j0 < je; j0 += WARPS * 4) {
-        int page[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int j = j0 + k;
-          page[k] = (j < je) ? p.table[(size_t)b * p.max_blocks + j] : -1;
-          if (j < je && (page[k] < 0 || page[k] >= p.P)) {
-            set_status(p.status, KT_ERR_DEVICE_CHECK);
-            page[k] = -2;
-          }
-        }
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int v0 = 0; v0 < V; v0 += 32) {
-          const int v = v0 + lane;
-          uint4 x[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            x[k] = make_uint4(0u, 0u, 0u, 0u);
-            if (page[k] >= 0 && v < V) {
-              const uint4* src = reinterpret_cast<const uint4*>(
-                  static_cast<const uint8_t*>(p.reps) +
-                  ((size_t)page[k] * p.H_kv + g0) * p.R * D * (f32 ? 4 : 2));
-              x[k] = __ldg(src + v);
-            }
-          }
-          if (v < V) {
-            const float* w = wts + v * vec_elems;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              if (f32) {
-                const float4 f = *reinterpret_cast<const float4*>(&x[k]);
-                acc[k] = fmaf(w[0], f.x, acc[k]);
-                acc[k] = fmaf(w[1], f.y, acc[k]);
-                acc[k] = fmaf(w[2], f.z, acc[k]);
-                acc[k] = fmaf(w[3], f.w, acc[k]);
-              } else {
-                acc[k] += dot8(w, x[k]);
-              }
-            }
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float s = warp_sum(acc[k]);
-          const int j = j0 + k;
-          if (lane == 0 && j < je) keys[j - js] = make_key(page[k] == -2 ? -INFINITY : s, j);
-        }
+      const int V = nkv * p.R * D / (f32 ? 4 : 8);  // 16-byte vectors per block
+      if (f32) {
+        if (V <= 32) score_linear<1, true>(p, g0, js, je, pg, wts, V, keys, warp, lane);
+        else if (V <= 64) score_linear<2, true>(p, g0, js, je, pg, wts, V, keys, warp, lane);
+        else if (V <= 128) score_linear<4, true>(p, g0, js, je, pg, wts, V, keys, warp, lane);
+        else score_linear<8, true>(p, g0, js, je, pg, wts, V, keys, warp, lane);
+      } else {
+        if (V <= 32) score_linear<1, false>(p, g0, js, je, pg, wts, V, keys, warp, lane);
+        else if (V <= 64) score_linear<2, false>(p, g0, js, je, pg, wts, V, keys, warp, lane);
+        else if (V <= 128) score_linear<4, false>(p, g0, js, je, pg, wts, V, keys, warp, lane);
+        else score_linear<8, false>(p, g0, js, je, pg, wts, V, keys, warp, lane);
       }
     } else {
       // Fix / Dynamic: per KV head, per query head, max over reps of q.rep;
       // lane owns channels 4*lane .. 4*lane+3.
       for (int j = js + warp; j < je; j += WARPS) {
-        const int page = p.table[(size_t)b * p.max_blocks + j];
+        const int page = pg[j - js];
         float total = 0.0f;
         if (page < 0 || page >= p.P) {
           set_status(p.status, KT_ERR_DEVICE_CHECK);
@@ -318,12 +343,12 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
                 const uint2 raw = __ldg(reinterpret_cast<const uint2*>(rp + r * D) + lane);
                 const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
                 const float2 f0 = __half22float2(h2[0]), f1 = __half22float2(h2[1]);
-                float s = w[0] * f0.x;
-                s = fmaf(w[1], f0.y, s);
-                s = fmaf(w[2], f1.x, s);
-                s = fmaf(w[3], f1.y, s);
-                s = warp_sum(s);
-                best = fmaxf(best, s);
+                float sc = w[0] * f0.x;
+                sc = fmaf(w[1], f0.y, sc);
+                sc = fmaf(w[2], f1.x, sc);
+                sc = fmaf(w[3], f1.y, sc);
+                sc = warp_sum(sc);
+                best = fmaxf(best, sc);
               }
               total += best;
             }
@@ -438,7 +463,8 @@ size_t select_smem_bytes(const SelectLaunch& a) {
   const int merged = a.plan.nchunks * a.plan.kk;
   const int merge_keys = merged + (a.top_k < merged ? a.top_k : merged);
   const int nq = nkv * a.G;
-  const int score_keys = chunk_keys + (nq * D * 2 + 7) / 8;  // keys + staged q rows
+  // keys + staged q rows + the chunk's page ids
+  const int score_keys = chunk_keys + (nq * D * 2 + 7) / 8 + (a.plan.chunk * 4 + 7) / 8;
   const int nkeys = score_keys > merge_keys ? score_keys : merge_keys;
   return (size_t)((wfloats * 4 + 15) & ~15) + (size_t)nkeys * 8;
 }
