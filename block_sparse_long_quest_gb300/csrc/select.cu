@@ -91,32 +91,45 @@ __device__ void radix_select(const unsigned long long* keys, int N, int k, unsig
     o |= keys[i];
   }
   for (int i = tid; i < 512; i += THREADS) hist[i] = 0u;
-  const unsigned int alo = __reduce_and_sync(0xffffffffu, (unsigned)a);
-  const unsigned int ahi = __reduce_and_sync(0xffffffffu, (unsigned)(a >> 32));
-  const unsigned int olo = __reduce_or_sync(0xffffffffu, (unsigned)o);
-  const unsigned int ohi = __reduce_or_sync(0xffffffffu, (unsigned)(o >> 32));
-  if (tid == 0) {
-    sh_u64[0] = ~0ull;
-    sh_u64[1] = 0ull;
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    a &= __shfl_xor_sync(0xffffffffu, a, d);
+    o |= __shfl_xor_sync(0xffffffffu, o, d);
   }
-  __syncthreads();
+  unsigned long long* red = sh_u64 + 2;  // [WARPS] ANDs, then [WARPS] ORs
   if (lane == 0) {
-    atomicAnd(&sh_u64[0], ((unsigned long long)ahi << 32) | alo);
-    atomicOr(&sh_u64[1], ((unsigned long long)ohi << 32) | olo);
+    red[warp] = a;
+    red[WARPS + warp] = o;
   }
   __syncthreads();
-  const unsigned long long all_and = sh_u64[0], diff = all_and ^ sh_u64[1];
+  unsigned long long all_and = ~0ull, all_or = 0ull;
+#pragma unroll
+  for (int w = 0; w < WARPS; ++w) {
+    all_and &= red[w];
+    all_or |= red[WARPS + w];
+  }
+  const unsigned long long diff = all_and ^ all_or;
   const int top = diff ? 63 - __clzll((long long)diff) : 0;  // highest differing bit
-  int shift = (top / 8) * 8;
-  unsigned long long mask = (shift + 8 >= 64) ? 0ull : ~((1ull << (shift + 8)) - 1);
+  // digit windows [lo, hi) of up to 8 bits, starting at the top differing bit
+  int hi = top + 1;
+  unsigned long long mask = (hi >= 64) ? 0ull : ~((1ull << hi) - 1);
   unsigned long long prefix = all_and & mask;
   int need = k;
-  for (int pass = 0; shift >= 0; ++pass, shift -= 8) {
+  for (int pass = 0; hi > 0; ++pass) {
+    const int shift = hi > 8 ? hi - 8 : 0;
+    const unsigned long long dmask = (1ull << (hi - shift)) - 1;
     unsigned int* H = hist + 256 * (pass & 1);
     unsigned int* Hn = hist + 256 * ((pass + 1) & 1);
-    for (int i = tid; i < N; i += THREADS) {
-      const unsigned long long key = keys[i];
-      if ((key & mask) == prefix) atomicAdd(&H[(key >> shift) & 255u], 1u);
+    for (int base = 0; base < N; base += THREADS) {
+      // equal digits are counted once per warp: keys are often clustered
+      const int i = base + tid;
+      unsigned int bin = 256u;
+      if (i < N) {
+        const unsigned long long key = keys[i];
+        if ((key & mask) == prefix) bin = (unsigned)((key >> shift) & dmask);
+      }
+      const unsigned int peers = __match_any_sync(0xffffffffu, bin);
+      if (bin < 256u && lane == __ffs(peers) - 1) atomicAdd(&H[bin], (unsigned)__popc(peers));
     }
     __syncthreads();
     if (warp == 0) {
@@ -153,7 +166,7 @@ __device__ void radix_select(const unsigned long long* keys, int N, int k, unsig
         }
         const int need2 = need - (int)above;
         sh_u64[0] = prefix | (static_cast<unsigned long long>(digit) << shift);
-        sh_u64[1] = mask | (0xFFull << shift);
+        sh_u64[1] = mask | (dmask << shift);
         sh_int[0] = need2;
         sh_int[1] = (bin == (unsigned)need2) ? 1 : 0;
       }
@@ -165,6 +178,7 @@ __device__ void radix_select(const unsigned long long* keys, int N, int k, unsig
     mask = sh_u64[1];
     need = sh_int[0];
     if (sh_int[1]) break;
+    hi = shift;
   }
   __syncthreads();  // sh_* are rewritten by the caller
   *prefix_out = prefix;
@@ -185,7 +199,14 @@ __device__ __forceinline__ void score_linear(const Params& p, int g0, int js, in
   for (int v = 0; v < NV; ++v) {
     const int vec = lane + 32 * v;
 #pragma unroll
-    for (int e = 0; e < VE; ++e) w[v][e] = (vec < V) ? wts[vec * VE + e] : 0.0f;
+    for (int e = 0; e < VE; e += 4) {
+      const float4 f = (vec < V) ? *reinterpret_cast<const float4*>(wts + vec * VE + e)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+      w[v][e] = f.x;
+      w[v][e + 1] = f.y;
+      w[v][e + 2] = f.z;
+      w[v][e + 3] = f.w;
+    }
   }
   const size_t head_bytes = (size_t)p.R * D * (F32 ? 4 : 2);
   for (int j0 = js + warp * GB; j0 < je; j0 += WARPS * GB) {
@@ -234,7 +255,7 @@ __device__ __forceinline__ void score_linear(const Params& p, int g0, int js, in
 __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ unsigned int hist[512];
-  __shared__ unsigned long long sh_u64[2];
+  __shared__ unsigned long long sh_u64[2 + 2 * WARPS];
   __shared__ int sh_int[4];
 
   if (p.trigger) griddep_launch_dependents();
