@@ -71,6 +71,7 @@ struct Params {
   const int32_t* seq_lens;
   const int32_t* sel;
   const int32_t* cnt;
+  const int32_t* sel_pages;
   float* out;
   int* status;
   int* counters;
@@ -158,6 +159,11 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       const Part pt = partition(seq_len(p, s / p.H_kv), p.I_b, p.L_b);
       return blocks_a(pt, p.dense) + blocks_b_max(pt, p.dense, p.top_k) + 1;
     }, lane);
+    // in place: cum[s] -> first CTA of segment s = s + floor(extra * cum[s] / W)
+    const long long extra = grid - S, W = cum[S];
+    __syncwarp();
+    for (int s = lane; s <= S; s += 32) cum[s] = s + (int)(extra * cum[s] / W);
+    __syncwarp();
   }
   if (tid == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -168,19 +174,17 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     fence_mbar_init();
   }
   __syncthreads();
-  // CTAs of segment s: [first(s), first(s+1)), first(s) = s + floor(extra*cum[s]/W)
-  const long long extra = grid - S, W = cum[S];
-  auto first_cta = [&](int s) { return s + (int)(extra * cum[s] / W); };
+  // CTAs of segment s: [cum[s], cum[s+1])
   int seg;
   {
     int lo = 0, hi = S - 1;  // largest s with first(s) <= cta
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (first_cta(mid) <= cta) lo = mid; else hi = mid - 1;
+      if (cum[mid] <= cta) lo = mid; else hi = mid - 1;
     }
     seg = lo;
   }
-  const int f0 = first_cta(seg), ncta = first_cta(seg + 1) - f0, ci = cta - f0;
+  const int f0 = cum[seg], ncta = cum[seg + 1] - f0, ci = cta - f0;
   const int b = seg / p.H_kv, h = seg % p.H_kv;
   const Part pt = partition(seq_len(p, b), p.I_b, p.L_b);
   const int nA = blocks_a(pt, p.dense);
@@ -206,16 +210,21 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
           int j;
           if (phase == 0) {
             j = (p.dense || i < pt.c0) ? i : pt.c1 + (i - pt.c0);
-          } else {
+          } else if (p.sel_pages == nullptr) {
             const int unit = p.SEL == 1 ? 0 : h;
             j = p.sel[((size_t)b * p.SEL + unit) * p.top_k + i];
             if (j < pt.c0 || j >= pt.c1) {
               set_status(p.status, KT_ERR_DEVICE_CHECK);
               j = -1;
             }
+          } else {
+            j = pt.c0;  // a selected Context block: full; its page comes with the selection
           }
           if (j >= 0) {
-            const int page = p.table[(size_t)b * p.max_blocks + j];
+            const int page =
+                (phase == 1 && p.sel_pages != nullptr)
+                    ? p.sel_pages[((size_t)b * p.SEL + (p.SEL == 1 ? 0 : h)) * p.top_k + i]
+                    : p.table[(size_t)b * p.max_blocks + j];
             if (page < 0 || page >= p.P) {
               set_status(p.status, KT_ERR_DEVICE_CHECK);
             } else {
@@ -262,7 +271,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     int nB = 0;
     if (!p.dense) {
       const int cmax = blocks_b_max(pt, 0, p.top_k);
-      nB = p.cnt[b * p.SEL + (p.SEL == 1 ? 0 : h)];
+      nB = p.cnt ? p.cnt[b * p.SEL + (p.SEL == 1 ? 0 : h)] : cmax;
       if (nB < 0 || nB > cmax) {
         set_status(p.status, KT_ERR_DEVICE_CHECK);
         nB = nB < 0 ? 0 : cmax;
@@ -596,6 +605,7 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   p.seq_lens = a.seq_lens;
   p.sel = a.sel;
   p.cnt = a.cnt;
+  p.sel_pages = a.sel_pages;
   p.out = a.out;
   p.status = a.status;
   p.counters = a.counters;

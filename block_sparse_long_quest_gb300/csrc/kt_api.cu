@@ -104,6 +104,10 @@ WsLayout layout(kt_op op, const kt_paged_kv* kv, const kt_sparse_params* p, int 
   off = align256(off + units * 4);
   L.sel_cand = off;
   off = align256(off + units * L.sel.nchunks * L.sel.kk * 8);
+  L.sel_cand_pages = off;
+  off = align256(off + units * L.sel.nchunks * L.sel.kk * 4);
+  L.sel_pages = off;
+  off = align256(off + units * (size_t)(p->top_k > 0 ? p->top_k : 1) * 4);
   const size_t sel_end = off;
   (void)T;
   L.dyn = off;
@@ -172,6 +176,8 @@ kt_status select_impl(const void* q, const kt_paged_kv* kv, const void* reps,
   a.status = at<int>(ws, L.status);
   a.counters = at<int>(ws, L.sel_counters);
   a.cand = at<unsigned long long>(ws, L.sel_cand);
+  a.cand_pages = at<int>(ws, L.sel_cand_pages);
+  a.sel_pages = at<int32_t>(ws, L.sel_pages);
   a.B = kv->batch;
   a.H_kv = kv->num_kv_heads;
   a.G = p->num_q_heads / kv->num_kv_heads;
@@ -189,9 +195,12 @@ kt_status select_impl(const void* q, const kt_paged_kv* kv, const void* reps,
   return cuda_status(launch_select(a, stream));
 }
 
+// step_path: the selection ran in this call on this workspace, so its page ids
+// (sel_pages) and counts (min(top_k, C)) are used directly.
 kt_status attn_impl(const void* q, const kt_paged_kv* kv, int num_q_heads, float scale,
                     const kt_sparse_params* p, const int32_t* sel, const int32_t* cnt, float* out,
-                    void* ws, const WsLayout& L, bool dense, bool pdl, cudaStream_t stream) {
+                    void* ws, const WsLayout& L, bool dense, bool pdl, cudaStream_t stream,
+                    bool step_path = false) {
   CUtensorMap kmap, vmap;
   if (!make_pool_map(&kmap, kv->k_pool, kv) || !make_pool_map(&vmap, kv->v_pool, kv))
     return KT_ERR_CUDA;
@@ -204,7 +213,8 @@ kt_status attn_impl(const void* q, const kt_paged_kv* kv, int num_q_heads, float
   a.table = kv->block_table;
   a.seq_lens = kv->seq_lens;
   a.sel = sel;
-  a.cnt = cnt;
+  a.cnt = step_path ? nullptr : cnt;
+  a.sel_pages = step_path ? at<int32_t>(ws, L.sel_pages) : nullptr;
   a.out = out;
   a.status = at<int>(ws, L.status);
   a.counters = at<int>(ws, L.attn_counters);
@@ -373,7 +383,7 @@ kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void
   s = select_impl(q, kv, reps_pool, p, sel, cnt, nullptr, ws, L, true, (cudaStream_t)stream);
   if (s != KT_OK) return s;
   return attn_impl(q, kv, p->num_q_heads, p->softmax_scale, p, sel, cnt, out, ws, L, false, true,
-                   (cudaStream_t)stream);
+                   (cudaStream_t)stream, true);
 }
 
 kt_status kt_sparse_decode_step_host(const void* q_host, void* q_dev, const kt_paged_kv* kv,
@@ -516,6 +526,7 @@ extern "C" kt_status kt_sparse_decode_attn_noalloc(const void* q, const kt_paged
   a.seq_lens = kv->seq_lens;
   a.sel = sel;
   a.cnt = cnt;
+  a.sel_pages = nullptr;
   a.out = out;
   a.status = at<int>(scratch, 0);
   a.counters = at<int>(scratch, counters_off);

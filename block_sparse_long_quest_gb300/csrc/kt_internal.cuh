@@ -39,6 +39,8 @@ struct WsLayout {
   size_t status;         // int32 status word, 256 B header
   size_t sel_counters;   // int32 [B*SEL]
   size_t sel_cand;       // uint64 [B*SEL*nchunks*kk]
+  size_t sel_cand_pages; // int32 [B*SEL*nchunks*kk], page id of each candidate
+  size_t sel_pages;      // int32 [B*SEL*top_k], page ids of the selection (step path)
   size_t attn_counters;  // int32 [S]
   size_t attn_parts;     // float [2*(MAX_ATTN_CTAS+S)][slot_floats]
   size_t dyn;            // dynamic-rep scratch
@@ -242,7 +244,8 @@ struct AttnLaunch {
   const int32_t* table;
   const int32_t* seq_lens;
   const int32_t* sel;
-  const int32_t* cnt;
+  const int32_t* cnt;        // nullable: then min(top_k, C) blocks were selected
+  const int32_t* sel_pages;  // nullable: page ids of sel (skips the table lookup)
   float* out;
   int* status;
   int* counters;
@@ -265,6 +268,8 @@ struct SelectLaunch {
   int* status;
   int* counters;
   unsigned long long* cand;
+  int* cand_pages;
+  int32_t* sel_pages;  // nullable
   int B, H_kv, G, max_blocks, P, I_b, L_b, top_k, rep, R, head_mode;
   SelPlan plan;
   bool trigger_dependents;

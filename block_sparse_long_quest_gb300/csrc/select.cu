@@ -41,6 +41,8 @@ struct Params {
   int* status;
   int* counters;
   unsigned long long* cand;
+  int* cand_pages;
+  int32_t* sel_pages;
   int B, H_kv, G, max_blocks, P, I_b, L_b, top_k, rep, R, head_mode;
   int SEL, chunk, nchunks, kk;
   int trigger;
@@ -301,6 +303,7 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
 
   const size_t unit_base = (size_t)b * p.SEL + u;
   unsigned long long* my_cand = p.cand + (unit_base * p.nchunks + chunk) * p.kk;
+  int* my_pages = p.cand_pages + (unit_base * p.nchunks + chunk) * p.kk;
   __syncthreads();
 
   if (nloc > 0) {
@@ -383,7 +386,10 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
     // ---- this chunk's top-kk candidates; unused slots hold key 0, which is
     // below every real key
     if (nloc <= p.kk) {
-      for (int i = tid; i < p.kk; i += THREADS) my_cand[i] = i < nloc ? keys[i] : 0ull;
+      for (int i = tid; i < p.kk; i += THREADS) {
+        my_cand[i] = i < nloc ? keys[i] : 0ull;
+        my_pages[i] = i < nloc ? pg[i] : -1;
+      }
     } else {
       unsigned long long prefix, mask;
       radix_select(keys, nloc, p.kk, hist, sh_u64, sh_int, &prefix, &mask);
@@ -393,13 +399,21 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
         const unsigned long long key = keys[i];
         if ((key & mask) >= prefix) {
           const int pos = atomicAdd(&sh_int[2], 1);
-          if (pos < p.kk) my_cand[pos] = key; else set_status(p.status, KT_ERR_DEVICE_CHECK);
+          if (pos < p.kk) {
+            my_cand[pos] = key;
+            my_pages[pos] = pg[i];
+          } else {
+            set_status(p.status, KT_ERR_DEVICE_CHECK);
+          }
         }
       }
     }
   }
   if (nloc <= 0)
-    for (int i = tid; i < p.kk; i += THREADS) my_cand[i] = 0ull;
+    for (int i = tid; i < p.kk; i += THREADS) {
+      my_cand[i] = 0ull;
+      my_pages[i] = -1;
+    }
 
   // ---- ticket: the last chunk CTA of this unit merges
   __threadfence();
@@ -416,11 +430,16 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
   // coalesced loads); empty slots are key 0
   unsigned long long* all = keys;
   const int nslots = p.nchunks * p.kk;
+  const int max_keff = min(p.top_k, nslots);
+  int* allp = reinterpret_cast<int*>(all + nslots + max_keff);  // pages of `all`
+  int* chosenp = allp + nslots;                                  // pages of `chosen`
   const unsigned long long* src = p.cand + unit_base * (size_t)nslots;
+  const int* srcp = p.cand_pages + unit_base * (size_t)nslots;
   int real = 0;
   for (int i = tid; i < nslots; i += THREADS) {
     const unsigned long long key = __ldcg(src + i);
     all[i] = key;
+    allp[i] = __ldcg(srcp + i);
     real += key != 0ull ? 1 : 0;
   }
   real = warp_sum_int(real);
@@ -436,7 +455,10 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
   unsigned long long* chosen = all + total;  // keff entries
   if (keff > 0) {
     if (keff == total) {
-      for (int i = tid; i < total; i += THREADS) chosen[i] = all[i];
+      for (int i = tid; i < total; i += THREADS) {
+        chosen[i] = all[i];
+        chosenp[i] = allp[i];
+      }
     } else {  // keff <= total_real: the zero slots are never chosen
       unsigned long long prefix, mask;
       radix_select(all, total, keff, hist, sh_u64, sh_int, &prefix, &mask);
@@ -446,7 +468,12 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
         const unsigned long long key = all[i];
         if ((key & mask) >= prefix) {
           const int pos = atomicAdd(&sh_int[2], 1);
-          if (pos < keff) chosen[pos] = key; else set_status(p.status, KT_ERR_DEVICE_CHECK);
+          if (pos < keff) {
+            chosen[pos] = key;
+            chosenp[pos] = allp[i];
+          } else {
+            set_status(p.status, KT_ERR_DEVICE_CHECK);
+          }
         }
       }
     }
@@ -464,6 +491,7 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
       }
       sel_out[rank] = static_cast<int32_t>(id);
       if (sc_out) sc_out[rank] = key_float(static_cast<uint32_t>(ki >> 32));
+      if (p.sel_pages) p.sel_pages[unit_base * p.top_k + rank] = chosenp[i];
     }
   }
   if (tid == 0) {
@@ -482,7 +510,9 @@ size_t select_smem_bytes(const SelectLaunch& a) {
       linear ? nkv * Rw * D : (a.head_mode == KT_HEAD_SHARED ? a.H_kv * a.G : a.G) * D;
   const int chunk_keys = (a.plan.chunk + 1) & ~1;
   const int merged = a.plan.nchunks * a.plan.kk;
-  const int merge_keys = merged + (a.top_k < merged ? a.top_k : merged);
+  // keys of all slots and of the chosen ones, plus their page ids (as ints)
+  const int merge_keys = merged + (a.top_k < merged ? a.top_k : merged) +
+                         (merged + (a.top_k < merged ? a.top_k : merged) + 1) / 2;
   const int nq = nkv * a.G;
   // keys + staged q rows + the chunk's page ids
   const int score_keys = chunk_keys + (nq * D * 2 + 7) / 8 + (a.plan.chunk * 4 + 7) / 8;
@@ -502,6 +532,8 @@ cudaError_t launch_select(const SelectLaunch& a, cudaStream_t stream) {
   p.status = a.status;
   p.counters = a.counters;
   p.cand = a.cand;
+  p.cand_pages = a.cand_pages;
+  p.sel_pages = a.sel_pages;
   p.B = a.B;
   p.H_kv = a.H_kv;
   p.G = a.G;
