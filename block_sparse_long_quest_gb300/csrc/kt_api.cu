@@ -111,7 +111,7 @@ WsLayout layout(kt_op op, const kt_paged_kv* kv, const kt_sparse_params* p, int 
   const size_t sel_end = off;
   (void)T;
   L.dyn = off;
-  L.dyn_bytes = 0;
+  L.dyn_bytes = op == KT_OP_DYNAMIC_REPS ? dynamic_ws_bytes(B, H_kv, kv->max_blocks_per_seq) : 0;
   off = align256(off + L.dyn_bytes);
   L.total = op == KT_OP_DENSE_ATTN ? attn_end : (op == KT_OP_DYNAMIC_REPS ? off : sel_end);
   return L;
@@ -327,13 +327,49 @@ kt_status kt_build_dynamic_reps(const kt_paged_kv* kv, const kt_sparse_params* p
                                 const void* q_local, int32_t T, int32_t first_block,
                                 int32_t num_blocks, void* reps_pool, float* token_scores,
                                 void* ws, size_t ws_bytes, kt_stream_t stream) {
-  (void)q_local; (void)T; (void)first_block; (void)num_blocks; (void)reps_pool;
-  (void)token_scores; (void)ws; (void)ws_bytes; (void)stream;
   kt_status s = check_kv(kv);
   if (s != KT_OK) return s;
   s = check_params(kv, p);
   if (s != KT_OK) return s;
-  return KT_ERR_UNSUPPORTED;
+  if (p->rep != KT_REP_DYNAMIC) return KT_ERR_INVALID_ARG;
+  if (!q_local || !reps_pool || !ws || !aligned16(q_local) || !aligned16(reps_pool) ||
+      !aligned16(ws) || (token_scores && !aligned16(token_scores)))
+    return KT_ERR_INVALID_ARG;
+  if (T < 1 || first_block < 0 || num_blocks < 0) return KT_ERR_INVALID_ARG;
+  const int G = p->num_q_heads / kv->num_kv_heads;
+  if ((long long)T * G > MAX_DYN_ROWS) return KT_ERR_UNSUPPORTED;
+  const WsLayout L = layout(KT_OP_DYNAMIC_REPS, kv, p, T);
+  if (ws_bytes < L.total) return KT_ERR_WORKSPACE_TOO_SMALL;
+  CUtensorMap kmap;
+  if (!make_pool_map(&kmap, kv->k_pool, kv)) return KT_ERR_CUDA;
+  const int sms = num_sms();
+  if (sms <= 0) return KT_ERR_CUDA;
+  DynLaunch a;
+  a.kmap = &kmap;
+  a.k_pool = static_cast<const __half*>(kv->k_pool);
+  a.q_local = static_cast<const __half*>(q_local);
+  a.table = kv->block_table;
+  a.seq_lens = kv->seq_lens;
+  a.ws = at<uint8_t>(ws, L.dyn);
+  a.reps = reps_pool;
+  a.token_scores = token_scores;
+  a.status = at<int>(ws, L.status);
+  a.B = kv->batch;
+  a.H_kv = kv->num_kv_heads;
+  a.G = G;
+  a.T = T;
+  a.max_blocks = kv->max_blocks_per_seq;
+  a.P = kv->num_pages;
+  a.R = p->num_reps;
+  a.first_block = first_block;
+  const long long last = (long long)first_block + num_blocks;
+  a.num_blocks = (int)((last > kv->max_blocks_per_seq ? kv->max_blocks_per_seq : last) -
+                       (first_block < kv->max_blocks_per_seq ? first_block
+                                                             : kv->max_blocks_per_seq));
+  if (a.num_blocks < 0) a.num_blocks = 0;
+  a.num_sms = sms;
+  a.scale_log2 = (float)((double)p->softmax_scale * 1.4426950408889634);
+  return cuda_status(launch_dynamic(a, (cudaStream_t)stream));
 }
 
 kt_status kt_score_select_blocks(const void* q, const kt_paged_kv* kv, const void* reps_pool,

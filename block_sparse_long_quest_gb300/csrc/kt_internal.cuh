@@ -286,6 +286,23 @@ struct RepsLaunch {
 };
 cudaError_t launch_reps(const RepsLaunch& a, cudaStream_t stream);
 
+struct DynLaunch {
+  const CUtensorMap* kmap;
+  const __half* k_pool;
+  const __half* q_local;
+  const int32_t* table;
+  const int32_t* seq_lens;
+  void* ws;  // dynamic_ws_bytes(B, H_kv, max_blocks) bytes
+  void* reps;
+  float* token_scores;
+  int* status;
+  int B, H_kv, G, T, max_blocks, P, R, first_block, num_blocks, num_sms;
+  float scale_log2;
+};
+cudaError_t launch_dynamic(const DynLaunch& a, cudaStream_t stream);
+size_t dynamic_ws_bytes(int B, int H_kv, int max_blocks);
+constexpr int MAX_DYN_ROWS = 256;  // local queries x query heads per KV head
+
 cudaError_t launch_selftest_wait(int* status, int spin_limit, cudaStream_t stream);
 
 }  // namespace kt

@@ -153,3 +153,61 @@ def selection_agrees(gpu_sel, gpu_cnt, oracle_res, b, u):
         if not zone[j]:
             return False, False
     return True, False
+
+
+def build_dynamic(dw):
+    """Dynamic reps on the GPU; returns the accumulated token scores (numpy)."""
+    import torch
+    import block_sparse_long_quest_gb300 as kt
+    w = dw.w
+    T = w.q_local.shape[1]
+    n = kt.kt_reps_pool_bytes(dw.kv, dw.params)
+    dw.reps = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    scores = torch.full((w.batch, w.num_kv_heads, w.max_blocks * 128), -1.0,
+                        dtype=torch.float32, device="cuda")
+    ws = kt.workspace(kt.KT_OP_DYNAMIC_REPS, dw.kv, dw.params, T)
+    kt.kt_build_dynamic_reps(dw.kv, dw.params, dw.q_local, T, 0, w.max_blocks, dw.reps, scores, ws)
+    assert kt.kt_read_device_status(ws) == kt.KT_OK
+    return scores.cpu().numpy()
+
+
+def dynamic_rep_tokens(w, reps_view, b, j, h):
+    """Token offsets (within block j) whose key rows form the GPU reps."""
+    page = w.block_table[b, j]
+    rows = w.k_pool[page, h]            # [128][128]
+    out = []
+    for r in reps_view[page, h]:
+        hit = np.nonzero((rows == r).all(axis=1))[0]
+        out.append(int(hit[0]) if hit.size else -1)
+    return out
+
+
+def check_dynamic_reps(dw, ref_scores, zone=ZONE):
+    """GPU reps equal the oracle's choice of tokens, except where the tokens'
+    oracle scores sit within `zone` (relative) of the R-th best score.
+    Returns (#blocks checked, #blocks that differ inside the zone, bad list)."""
+    w = dw.w
+    R = w.params.num_reps
+    got = dw.reps_view()
+    checked = differ = 0
+    bad = []
+    for b in range(w.batch):
+        n = int(w.seq_lens[b])
+        for h in range(w.num_kv_heads):
+            sc = ref_scores[b, h]
+            for j in range(n // 128):
+                blk = sc[j * 128:(j + 1) * 128]
+                order = sorted(range(128), key=lambda t: (-blk[t], t))
+                want = sorted(order[:R])
+                toks = dynamic_rep_tokens(w, got, b, j, h)
+                checked += 1
+                if toks == want:
+                    continue
+                rth = blk[order[R - 1]]
+                tol = zone * max(abs(rth), 1e-30)
+                if -1 in toks or any(abs(blk[t] - rth) > tol
+                                     for t in set(toks).symmetric_difference(want)):
+                    bad.append((b, h, j, toks, want))
+                else:
+                    differ += 1
+    return checked, differ, bad
