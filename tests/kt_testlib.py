@@ -182,7 +182,7 @@ def dynamic_rep_tokens(w, reps_view, b, j, h):
     return out
 
 
-def check_dynamic_reps(dw, ref_scores, zone=ZONE):
+def check_dynamic_reps(dw, ref_scores, zone=ZONE, heads=None):
     """GPU reps equal the oracle's choice of tokens, except where the tokens'
     oracle scores sit within `zone` (relative) of the R-th best score.
     Returns (#blocks checked, #blocks that differ inside the zone, bad list)."""
@@ -193,7 +193,7 @@ def check_dynamic_reps(dw, ref_scores, zone=ZONE):
     bad = []
     for b in range(w.batch):
         n = int(w.seq_lens[b])
-        for h in range(w.num_kv_heads):
+        for h in (range(w.num_kv_heads) if heads is None else heads):
             sc = ref_scores[b, h]
             for j in range(n // 128):
                 blk = sc[j * 128:(j + 1) * 128]
