@@ -91,7 +91,8 @@ class Layer:
                                       fix_stride=p.fix_stride, softmax_scale=p.softmax_scale)
             reps = torch.zeros(kt.kt_reps_pool_bytes(self.kv, params), dtype=torch.uint8,
                                device="cuda")
-            kt.kt_build_block_reps(self.kv, params, 0, w.max_blocks, reps)
+            if rep != synth.REP_DYNAMIC:  # Dynamic reps need the local queries
+                kt.kt_build_block_reps(self.kv, params, 0, w.max_blocks, reps)
             SEL = 1 if p.head_mode == synth.HEAD_SHARED else w.num_kv_heads
             self.variants[rep] = dict(
                 params=params, reps=reps,
@@ -341,6 +342,7 @@ def main():
     ap.add_argument("--seq-len", type=int, default=131072)
     ap.add_argument("--no-1m", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dynamic", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -363,6 +365,7 @@ def main():
         layers.append(Layer(w, keep_host=(l == 0)))
     w0 = layers[0].w
     rep = w0.params.rep
+    l2_bytes = torch.cuda.get_device_properties(local).L2_cache_size
     bytes_step = step_bytes(w0)
     torch.cuda.synchronize()
 
@@ -422,6 +425,18 @@ def main():
     e2e_value = world * bytes_step["total"] * n_e2e / t_e2e / 1e9
 
     extra = {}
+    # ---- representative build (amortised, outside the step): Quest reps of one
+    # 128K layer; algorithmic bytes = K read once + reps written
+    L0 = layers[0]
+    v0q = L0.variants[rep]
+    n_rb = 20
+    t_rb = graph_time([lambda: kt.kt_build_block_reps(L0.kv, v0q["params"], 0, w0.max_blocks,
+                                                      v0q["reps"])], n_rb, args.warmup, stream)
+    rb_bytes = int(L0.k.numel() * 2 + v0q["reps"].numel())
+    extra["rep_build_128k_quest"] = {"us": t_rb / n_rb * 1e6,
+                                     "gbs": rb_bytes / (t_rb / n_rb) / 1e9,
+                                     "bytes": rb_bytes}
+
     # ---- 1M-token leg: 4 layers back to back, Quest and Max reps
     if world == 1 and not args.no_1m:
         del layers, steps_fns, q_dev
@@ -450,6 +465,10 @@ def main():
             wq.params.rep = synth.REP_QUEST
         extra["at_1m"] = {"workload": "1m-gqa4-separate-k32 (4 layers, 1048576 tokens each)",
                           **res}
+        del big
+        torch.cuda.empty_cache()
+    if world == 1 and not args.no_dynamic:
+        extra["at_dynamic_128k"] = dynamic_leg(args, stream)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -461,7 +480,8 @@ def main():
                    "local_tokens": 4096, "top_k": 32, "rep": "quest", "head_mode": "shared",
                    "bytes_per_step": bytes_step,
                    "l2": f"{n_layers} layers rotated, touched set "
-                         f"{n_layers * bytes_step['total'] / 1e6:.0f} MB > 2x L2",
+                         f"{n_layers * bytes_step['total'] / 1e6:.0f} MB vs L2 "
+                         f"{l2_bytes / 1e6:.0f} MB",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": "attn_kernel", "achieved": attn_gbs,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
@@ -485,6 +505,35 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def dynamic_leg(args, stream):
+    """Dynamic reps at 128K: the rep build (two passes over K, tensor-core
+    contraction of the 64 local queries x 4 heads against every key) and the
+    decode step that scores blocks by max q.rep over 4 reps."""
+    import torch
+
+    import block_sparse_long_quest_gb300 as kt
+    w = synth.dynamic128k()
+    L = Layer(w)  # builds no reps for Dynamic (kt_build_block_reps rejects it)
+    v = L.variants[synth.REP_DYNAMIC]
+    q_local = torch.from_numpy(w.q_local.view(np.int16)).view(torch.float16).cuda()
+    T = w.q_local.shape[1]
+    ws_dyn = kt.workspace(kt.KT_OP_DYNAMIC_REPS, L.kv, v["params"], T)
+    build = lambda: kt.kt_build_dynamic_reps(L.kv, v["params"], q_local, T, 0, w.max_blocks,
+                                             v["reps"], None, ws_dyn)
+    n_b = 10
+    t_b = graph_time([build], n_b, 3, stream)
+    rows = T * w.params.num_q_heads
+    flops = 2 * 2 * rows * int(w.seq_lens[0]) * D  # two passes of Q K^T
+    n_s = 2000
+    t_s = graph_time([lambda: L.step(synth.REP_DYNAMIC)], n_s, args.warmup, stream)
+    b = step_bytes(w)
+    return {"workload": w.name,
+            "rep_build_us": t_b / n_b * 1e6, "rep_build_tflops": flops / (t_b / n_b) / 1e12,
+            "rep_build_k_bytes_read": 2 * int(L.k.numel()) * 2,
+            "step_us": t_s / n_s * 1e6, "step_gbs": b["total"] / (t_s / n_s) / 1e9,
+            "step_bytes": b["total"], "l2_note": "one layer repeated (touched set fits L2)"}
 
 
 def layers_q_bytes(w):
