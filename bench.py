@@ -218,6 +218,23 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+# DRAM traffic per attn_kernel launch (dram__bytes_read.sum + dram__bytes_write.sum)
+# from one ncu capture of the 128K workload, valid only for the source it was
+# taken from (profiles/attn_kernel_128k.md).
+ATTN_TRAFFIC = {"bytes": 34159104 + 23552,
+                "source_sha256": "f105066e291adda668e8a619f9a009be2c1269ba78aefdf0d01ec386c9253950"}
+
+
+def attn_traffic():
+    import hashlib
+    path = os.path.join(ROOT, "block_sparse_long_quest_gb300", "csrc", "attn.cu")
+    try:
+        sha = hashlib.sha256(open(path, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return ATTN_TRAFFIC["bytes"] if sha == ATTN_TRAFFIC["source_sha256"] else None
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -485,7 +502,7 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": "attn_kernel", "achieved": attn_gbs,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": attn_gbs / peak, "traffic": None,
+                     "frac": attn_gbs / peak, "traffic": attn_traffic(),
                      "algorithmic_bytes_per_launch": bytes_step["kv"],
                      "us_per_launch": attn_us},
         "kernels_us": {"select_kernel": sel_us, "attn_kernel": attn_us},
