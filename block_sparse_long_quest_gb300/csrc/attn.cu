@@ -31,7 +31,7 @@
 //     segment served by one CTA is written to out directly; otherwise each CTA
 //     writes an (m, l, acc) partial, takes a ticket, and the CTA completing the
 //     count merges the segment's partials in CTA order (deterministic).
-#include "kt_internal.cuh"
+#include "select_common.cuh"
 
 namespace kt {
 namespace {
@@ -46,6 +46,7 @@ constexpr int KV_STAGE_BYTES = 4 * BOX_BYTES;  // K lo, K hi, V lo, V hi
 constexpr int Q_BYTES = MAX_G * D * 2;
 constexpr int HALF_WARPS = CONSUMERS / 2;
 constexpr int SCRATCH_FLOATS = HALF_WARPS * MAX_G * (D + 2);
+static_assert(SCRATCH_FLOATS * 4 == ATTN_SCRATCH_BYTES, "scratch size shared with the host");
 
 struct StageInfo {
   int ntok, end, pad0, pad1;
@@ -78,6 +79,17 @@ struct Params {
   float* parts;
   int B, H_kv, G, max_blocks, P, I_b, L_b, top_k, SEL, dense, slot_floats;
   float scale_log2;
+  // fused step only: in-kernel selection (see fused_select)
+  const void* reps;
+  int rep, R, ncpu, kk_f;
+  unsigned long long* f_cand;
+  int* f_cand_pages;
+  int* f_counters;
+  int32_t* sel_out;
+  int32_t* cnt_out;
+  int32_t* sel_pages_out;
+  int* f_flags;
+  int* f_epoch;
 };
 
 struct Part {
@@ -132,8 +144,12 @@ __device__ void warp_prefix(int* pref, int S, F count, int lane) {
   __syncwarp();
 }
 
+template <bool FUSED>
 __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ unsigned int f_hist[FUSED ? 512 : 1];
+  __shared__ unsigned long long f_sh_u64[FUSED ? 2 + 2 * CONSUMERS : 1];
+  __shared__ int f_sh_int[FUSED ? 8 : 1];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -166,6 +182,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     __syncwarp();
   }
   if (tid == 0) {
+    if (FUSED) bcast[62] = __ldcg(p.f_epoch);  // this launch's epoch
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(bar_full + 8 * i, 1);
       mbar_init(bar_empty + 8 * i, CONSUMERS);
@@ -266,15 +283,39 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       }
     };
     produce(0, a0, a1);
-    // Phase B needs the selection: wait for the grid this launch depends on.
-    griddep_wait();
     int nB = 0;
-    if (!p.dense) {
-      const int cmax = blocks_b_max(pt, 0, p.top_k);
-      nB = p.cnt ? p.cnt[b * p.SEL + (p.SEL == 1 ? 0 : h)] : cmax;
-      if (nB < 0 || nB > cmax) {
-        set_status(p.status, KT_ERR_DEVICE_CHECK);
-        nB = nB < 0 ? 0 : cmax;
+    if (FUSED) {
+      // Phase B needs this segment's selection unit: wait (bounded) until its
+      // last scoring CTA publishes it for this launch's epoch.
+      const int unit = b * p.SEL + (p.SEL == 1 ? 0 : h);
+      const int want = bcast[62] + 1;
+      int ready = 0;
+      if (lane == 0) {
+        const uint64_t t0 = globaltimer();
+        for (uint32_t i = 0;; ++i) {
+          if (ld_acquire_gpu(p.f_flags + unit) == want) {
+            ready = 1;
+            break;
+          }
+          if ((i & 63u) == 63u && globaltimer() - t0 > WAIT_LIMIT_NS) {
+            set_status(p.status, KT_ERR_TIMEOUT);
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      ready = __shfl_sync(0xffffffffu, ready, 0);
+      nB = ready ? blocks_b_max(pt, 0, p.top_k) : 0;
+    } else {
+      // Phase B needs the selection: wait for the grid this launch depends on.
+      griddep_wait();
+      if (!p.dense) {
+        const int cmax = blocks_b_max(pt, 0, p.top_k);
+        nB = p.cnt ? p.cnt[b * p.SEL + (p.SEL == 1 ? 0 : h)] : cmax;
+        if (nB < 0 || nB > cmax) {
+          set_status(p.status, KT_ERR_DEVICE_CHECK);
+          nB = nB < 0 ? 0 : cmax;
+        }
       }
     }
     if (ok) produce(1, (int)((long long)ci * nB / ncta), (int)((long long)(ci + 1) * nB / ncta));
@@ -292,6 +333,184 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   // ============================ consumer warps ===============================
   const int g = lane >> 2, t = lane & 3;
   const int ctid = tid;
+  auto bar_c = [] { named_bar_sync(1, NCT); };
+
+  // Fused step: count this CTA done; the last CTA of the launch advances the
+  // epoch that tags the selection flags.
+  auto finish = [&]() {
+    if (FUSED && ctid == 0) {
+      __threadfence();
+      const int old = atomicAdd(p.f_epoch + 1, 1);
+      if (old == grid - 1) {
+        p.f_epoch[1] = 0;
+        __threadfence();
+        atomicAdd(p.f_epoch, 1);
+      }
+    }
+  };
+
+  if constexpr (FUSED) {
+    // ---- in-kernel selection: CTA c scores slice c % ncpu of the Context
+    // blocks of selection unit c / ncpu (same scoring and keys as
+    // select_kernel), keeps its top kk_f, and the unit's last CTA merges,
+    // writes sel / cnt / page ids and publishes the unit for this epoch.
+    const int U = p.B * p.SEL;
+    const int u = cta / p.ncpu;
+    if (u < U) {
+      const int cs = cta % p.ncpu;
+      const int bu = u / p.SEL, g0 = p.SEL == 1 ? 0 : u % p.SEL;
+      const int nkv = p.SEL == 1 ? p.H_kv : 1;
+      const int Rw = p.rep == KT_REP_QUEST ? 2 : 1;
+      const bool f32 = p.rep == KT_REP_MEAN;
+      const Part pu = partition(seq_len(p, bu), p.I_b, p.L_b);
+      const int C = pu.c1 - pu.c0;
+      const int js = pu.c0 + (int)((long long)cs * C / p.ncpu);
+      const int je = pu.c0 + (int)((long long)(cs + 1) * C / p.ncpu);
+      const int nloc = je - js;
+      const int wfl = nkv * Rw * D;
+      float* wts = scratch;
+      unsigned long long* keys = reinterpret_cast<unsigned long long*>(scratch + ((wfl + 3) & ~3));
+      int* pgs = reinterpret_cast<int*>(keys + ((nloc + 1) & ~1));
+      unsigned long long* cand = p.f_cand + ((size_t)u * p.ncpu + cs) * p.kk_f;
+      int* cpage = p.f_cand_pages + ((size_t)u * p.ncpu + cs) * p.kk_f;
+      if (nloc > 0) {
+        for (int i = ctid; i < nloc; i += NCT) pgs[i] = __ldg(p.table + (size_t)bu * p.max_blocks + js + i);
+        for (int i = ctid; i < nkv * D; i += NCT) {
+          const int gi = i / D, c = i % D;
+          float sum = 0.0f, neg = 0.0f, pos = 0.0f;
+          for (int hh = 0; hh < p.G; ++hh) {
+            const float qv = __half2float(p.q[((size_t)bu * H_q + (g0 + gi) * p.G + hh) * D + c]);
+            sum += qv;
+            neg += fminf(qv, 0.0f);
+            pos += fmaxf(qv, 0.0f);
+          }
+          if (p.rep == KT_REP_QUEST) {
+            wts[(gi * 2 + 0) * D + c] = neg;  // pairs with the kmin row
+            wts[(gi * 2 + 1) * D + c] = pos;  // pairs with the kmax row
+          } else {
+            wts[gi * D + c] = sum;
+          }
+        }
+        bar_c();
+        const int V = nkv * p.R * D / (f32 ? 4 : 8);
+        if (f32) {
+          if (V <= 32) selc::score_linear<1, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+          else if (V <= 64) selc::score_linear<2, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+          else if (V <= 128) selc::score_linear<4, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+          else selc::score_linear<8, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+        } else {
+          if (V <= 32) selc::score_linear<1, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+          else if (V <= 64) selc::score_linear<2, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+          else if (V <= 128) selc::score_linear<4, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+          else selc::score_linear<8, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+        }
+        bar_c();
+        if (nloc <= p.kk_f) {
+          for (int i = ctid; i < p.kk_f; i += NCT) {
+            cand[i] = i < nloc ? keys[i] : 0ull;
+            cpage[i] = i < nloc ? pgs[i] : -1;
+          }
+        } else {
+          unsigned long long prefix, mask;
+          selc::radix_select<NCT>(keys, nloc, p.kk_f, f_hist, f_sh_u64, f_sh_int, &prefix, &mask,
+                                  ctid, bar_c);
+          if (ctid == 0) f_sh_int[2] = 0;
+          bar_c();
+          for (int i = ctid; i < nloc; i += NCT) {
+            const unsigned long long key = keys[i];
+            if ((key & mask) >= prefix) {
+              const int pos = atomicAdd(&f_sh_int[2], 1);
+              if (pos < p.kk_f) {
+                cand[pos] = key;
+                cpage[pos] = pgs[i];
+              } else {
+                set_status(p.status, KT_ERR_DEVICE_CHECK);
+              }
+            }
+          }
+        }
+      } else {
+        for (int i = ctid; i < p.kk_f; i += NCT) {
+          cand[i] = 0ull;
+          cpage[i] = -1;
+        }
+      }
+      __threadfence();
+      bar_c();
+      if (ctid == 0) {
+        const int old = atomicAdd(p.f_counters + u, 1);
+        f_sh_int[3] = (old == p.ncpu - 1) ? 1 : 0;
+        f_sh_int[4] = 0;
+      }
+      bar_c();
+      if (f_sh_int[3]) {
+        __threadfence();
+        // gather every candidate slot of the unit (key 0 = empty slot)
+        const int nslots = p.ncpu * p.kk_f;
+        const int kmax = min(p.top_k, nslots);
+        unsigned long long* all = reinterpret_cast<unsigned long long*>(scratch);
+        unsigned long long* chosen = all + nslots;
+        int* allp = reinterpret_cast<int*>(chosen + kmax);
+        int* chosenp = allp + nslots;
+        const unsigned long long* src = p.f_cand + (size_t)u * nslots;
+        const int* srcp = p.f_cand_pages + (size_t)u * nslots;
+        int real = 0;
+        for (int i = ctid; i < nslots; i += NCT) {
+          const unsigned long long key = __ldcg(src + i);
+          all[i] = key;
+          allp[i] = __ldcg(srcp + i);
+          real += key != 0ull ? 1 : 0;
+        }
+        real = selc::warp_sum_int(real);
+        if (lane == 0) atomicAdd(&f_sh_int[4], real);
+        bar_c();
+        const int keff = min(p.top_k, f_sh_int[4]);
+        if (keff > 0) {
+          if (keff == nslots) {
+            for (int i = ctid; i < nslots; i += NCT) {
+              chosen[i] = all[i];
+              chosenp[i] = allp[i];
+            }
+          } else {
+            unsigned long long prefix, mask;
+            selc::radix_select<NCT>(all, nslots, keff, f_hist, f_sh_u64, f_sh_int, &prefix,
+                                    &mask, ctid, bar_c);
+            if (ctid == 0) f_sh_int[2] = 0;
+            bar_c();
+            for (int i = ctid; i < nslots; i += NCT) {
+              const unsigned long long key = all[i];
+              if ((key & mask) >= prefix) {
+                const int pos = atomicAdd(&f_sh_int[2], 1);
+                if (pos < keff) {
+                  chosen[pos] = key;
+                  chosenp[pos] = allp[i];
+                } else {
+                  set_status(p.status, KT_ERR_DEVICE_CHECK);
+                }
+              }
+            }
+          }
+          bar_c();
+          for (int i = ctid; i < keff; i += NCT) {
+            const uint32_t id = 0xFFFFFFFFu - static_cast<uint32_t>(chosen[i] & 0xFFFFFFFFull);
+            int rank = 0;
+            for (int m = 0; m < keff; ++m)
+              rank += (0xFFFFFFFFu - static_cast<uint32_t>(chosen[m] & 0xFFFFFFFFull)) < id ? 1 : 0;
+            p.sel_out[(size_t)u * p.top_k + rank] = static_cast<int32_t>(id);
+            p.sel_pages_out[(size_t)u * p.top_k + rank] = chosenp[i];
+          }
+        }
+        if (ctid == 0) {
+          p.cnt_out[u] = keff;
+          p.f_counters[u] = 0;
+        }
+        __threadfence();
+        bar_c();
+        if (ctid == 0) st_release_gpu(p.f_flags + u, bcast[62] + 1);
+      }
+      bar_c();  // scratch is reused below
+    }
+  }
   float acc[16][4];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
@@ -480,6 +699,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       const float L = fm[MAX_G + gg];
       p.out[((size_t)b * H_q + h * p.G + gg) * D + c] = L > 0.0f ? v / L : 0.0f;
     }
+    finish();
     return;
   }
 
@@ -505,7 +725,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     bcast[60] = (old + 1 == ncta) ? 1 : 0;
   }
   named_bar_sync(1, NCT);
-  if (!bcast[60]) return;
+  if (!bcast[60]) {
+    finish();
+    return;
+  }
   __threadfence();
 
   // ---- last CTA of the segment: merge partials of CTAs f0 .. f0+ncta-1.
@@ -589,13 +812,26 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
   }
   if (ctid == 0) p.counters[seg] = 0;
+  finish();
 }
 
 }  // namespace
 
+int attn_fused_max_ctas_per_sm() {
+  if (cudaFuncSetAttribute(attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SMEM_BYTES) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<true>, THREADS, SMEM_BYTES) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
 cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SMEM_BYTES);
+  cudaError_t e =
+      cudaFuncSetAttribute(a.fused ? attn_kernel<true> : attn_kernel<false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   Params p;
   p.kmap = *a.kmap;
@@ -605,7 +841,7 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   p.seq_lens = a.seq_lens;
   p.sel = a.sel;
   p.cnt = a.cnt;
-  p.sel_pages = a.sel_pages;
+  p.sel_pages = a.fused ? a.sel_pages_out : a.sel_pages;
   p.out = a.out;
   p.status = a.status;
   p.counters = a.counters;
@@ -622,6 +858,19 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   p.dense = a.dense;
   p.slot_floats = a.slot_floats;
   p.scale_log2 = a.scale_log2;
+  p.reps = a.reps;
+  p.rep = a.rep;
+  p.R = a.R;
+  p.ncpu = a.ncpu;
+  p.kk_f = a.kk_f;
+  p.f_cand = a.f_cand;
+  p.f_cand_pages = a.f_cand_pages;
+  p.f_counters = a.f_counters;
+  p.sel_out = a.sel_out;
+  p.cnt_out = a.cnt_out;
+  p.sel_pages_out = a.sel_pages_out;
+  p.f_flags = a.f_flags;
+  p.f_epoch = a.f_epoch;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);
@@ -629,11 +878,19 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = a.pdl ? 1 : 0;
+  if (a.fused) {
+    // every CTA must be resident: the producers wait for selection flags set
+    // by other CTAs of the same grid
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = a.pdl ? 1 : 0;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_kernel, p);
+  if (a.fused) return cudaLaunchKernelEx(&cfg, attn_kernel<true>, p);
+  return cudaLaunchKernelEx(&cfg, attn_kernel<false>, p);
 }
 
 }  // namespace kt

@@ -108,6 +108,20 @@ WsLayout layout(kt_op op, const kt_paged_kv* kv, const kt_sparse_params* p, int 
   off = align256(off + units * L.sel.nchunks * L.sel.kk * 4);
   L.sel_pages = off;
   off = align256(off + units * (size_t)(p->top_k > 0 ? p->top_k : 1) * 4);
+  // fused step (selection inside the attention launch)
+  const size_t fcap = (size_t)MAX_ATTN_CTAS *
+                      (size_t)(p->top_k < FUSED_KK_CAP ? (p->top_k > 0 ? p->top_k : 1)
+                                                       : FUSED_KK_CAP);
+  L.f_counters = off;
+  off = align256(off + units * 4);
+  L.f_flags = off;
+  off = align256(off + units * 4);
+  L.f_epoch = off;
+  off = align256(off + 8);
+  L.f_cand = off;
+  off = align256(off + fcap * 8);
+  L.f_cand_pages = off;
+  off = align256(off + fcap * 4);
   const size_t sel_end = off;
   (void)T;
   L.dyn = off;
@@ -207,6 +221,7 @@ kt_status attn_impl(const void* q, const kt_paged_kv* kv, int num_q_heads, float
   const int sms = num_sms();
   if (sms <= 0) return KT_ERR_CUDA;
   AttnLaunch a;
+  std::memset(&a, 0, sizeof(a));
   a.kmap = &kmap;
   a.vmap = &vmap;
   a.q = static_cast<const __half*>(q);
@@ -404,6 +419,46 @@ kt_status kt_sparse_decode_attn(const void* q, const kt_paged_kv* kv, const kt_s
                    (cudaStream_t)stream);
 }
 
+namespace kt {
+namespace {
+
+// Whether the one-launch step applies: linear reps, at most one attention CTA
+// per SM per segment and per selection unit, and the in-kernel selection
+// buffers fit the attention kernel's scratch.  Sets CTAs per unit and
+// candidates per CTA.
+bool fused_plan(const kt_paged_kv* kv, const kt_sparse_params* p, int sms, int* ncpu, int* kk) {
+  if (p->rep != KT_REP_MAX && p->rep != KT_REP_MEAN && p->rep != KT_REP_QUEST) return false;
+  if (sms < 1 || sms > MAX_ATTN_CTAS) return false;
+  const long long S = (long long)kv->batch * kv->num_kv_heads;
+  const int SEL = p->head_mode == KT_HEAD_SHARED ? 1 : kv->num_kv_heads;
+  const long long U = (long long)kv->batch * SEL;
+  if (S > sms || U > sms) return false;
+  const int nc = (int)(sms / U);
+  const int cmax = kv->max_blocks_per_seq - p->initial_blocks - p->local_blocks;
+  const int chunk = cmax > 0 ? (cmax + nc - 1) / nc : 1;
+  const int k = p->top_k < chunk ? p->top_k : chunk;
+  if (k > FUSED_KK_CAP) return false;
+  const int nkv = SEL == 1 ? kv->num_kv_heads : 1;
+  const int Rw = p->rep == KT_REP_QUEST ? 2 : 1;
+  const bool f32 = p->rep == KT_REP_MEAN;
+  const int V = nkv * reps_rows(p) * D / (f32 ? 4 : 8);
+  if (V > 256) return false;
+  const size_t scratch = ATTN_SCRATCH_BYTES;
+  const size_t chunk_bytes = (size_t)((nkv * Rw * D + 3) & ~3) * 4 +
+                             (size_t)((chunk + 1) & ~1) * 8 + (size_t)chunk * 4;
+  const size_t nslots = (size_t)nc * k;
+  const size_t kmax = (size_t)p->top_k < nslots ? (size_t)p->top_k : nslots;
+  const size_t merge_bytes = (nslots + kmax) * 12;
+  if (chunk_bytes > scratch || merge_bytes > scratch) return false;
+  if (attn_fused_max_ctas_per_sm() < 1) return false;
+  *ncpu = nc;
+  *kk = k;
+  return true;
+}
+
+}  // namespace
+}  // namespace kt
+
 kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void* reps_pool,
                                 const kt_sparse_params* p, int32_t* sel, int32_t* cnt,
                                 float* out, void* ws, size_t ws_bytes, kt_stream_t stream) {
@@ -416,6 +471,53 @@ kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void
     return KT_ERR_INVALID_ARG;
   const WsLayout L = layout(KT_OP_SPARSE_STEP, kv, p, 0);
   if (ws_bytes < L.total) return KT_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = num_sms();
+  int ncpu = 0, kk = 0;
+  if (sms > 0 && fused_plan(kv, p, sms, &ncpu, &kk)) {
+    // one launch: selection inside the attention kernel
+    CUtensorMap kmap, vmap;
+    if (!make_pool_map(&kmap, kv->k_pool, kv) || !make_pool_map(&vmap, kv->v_pool, kv))
+      return KT_ERR_CUDA;
+    AttnLaunch a;
+    std::memset(&a, 0, sizeof(a));
+    a.kmap = &kmap;
+    a.vmap = &vmap;
+    a.q = static_cast<const __half*>(q);
+    a.table = kv->block_table;
+    a.seq_lens = kv->seq_lens;
+    a.out = out;
+    a.status = at<int>(ws, L.status);
+    a.counters = at<int>(ws, L.attn_counters);
+    a.parts = at<float>(ws, L.attn_parts);
+    a.B = kv->batch;
+    a.H_kv = kv->num_kv_heads;
+    a.G = p->num_q_heads / kv->num_kv_heads;
+    a.max_blocks = kv->max_blocks_per_seq;
+    a.P = kv->num_pages;
+    a.I_b = p->initial_blocks;
+    a.L_b = p->local_blocks;
+    a.top_k = p->top_k;
+    a.SEL = p->head_mode == KT_HEAD_SHARED ? 1 : kv->num_kv_heads;
+    a.dense = 0;
+    a.slot_floats = L.slot_floats;
+    a.scale_log2 = (float)((double)p->softmax_scale * 1.4426950408889634);
+    a.grid = sms;
+    a.fused = true;
+    a.reps = reps_pool;
+    a.rep = p->rep;
+    a.R = reps_rows(p);
+    a.ncpu = ncpu;
+    a.kk_f = kk;
+    a.f_cand = at<unsigned long long>(ws, L.f_cand);
+    a.f_cand_pages = at<int>(ws, L.f_cand_pages);
+    a.f_counters = at<int>(ws, L.f_counters);
+    a.sel_out = sel;
+    a.cnt_out = cnt;
+    a.sel_pages_out = at<int32_t>(ws, L.sel_pages);
+    a.f_flags = at<int>(ws, L.f_flags);
+    a.f_epoch = at<int>(ws, L.f_epoch);
+    return cuda_status(launch_attention(a, (cudaStream_t)stream));
+  }
   s = select_impl(q, kv, reps_pool, p, sel, cnt, nullptr, ws, L, true, (cudaStream_t)stream);
   if (s != KT_OK) return s;
   return attn_impl(q, kv, p->num_q_heads, p->softmax_scale, p, sel, cnt, out, ws, L, false, true,
@@ -555,6 +657,7 @@ extern "C" kt_status kt_sparse_decode_attn_noalloc(const void* q, const kt_paged
   if (!make_pool_map(&kmap, kv->k_pool, kv) || !make_pool_map(&vmap, kv->v_pool, kv))
     return KT_ERR_CUDA;
   AttnLaunch a;
+  std::memset(&a, 0, sizeof(a));
   a.kmap = &kmap;
   a.vmap = &vmap;
   a.q = static_cast<const __half*>(q);

@@ -21,6 +21,8 @@ constexpr int SEL_TARGET_CTAS = 1024;
 constexpr int SEL_MAX_CAND = 8192;  // candidates merged by the last selection CTA
 constexpr int SEL_MAX_CHUNK = 4096; // context blocks scored by one selection CTA
 constexpr int MAX_DYN_REPS = 32;
+constexpr int ATTN_SCRATCH_BYTES = 4 * MAX_G * (D + 2) * 4;  // attention kernel scratch (smem)
+constexpr int FUSED_KK_CAP = 256;  // per-CTA candidates of the fused step
 constexpr uint64_t WAIT_LIMIT_NS = 100000000ull;  // 100 ms bound on any device-side wait
 
 // ---------------------------------------------------------------------------
@@ -41,6 +43,11 @@ struct WsLayout {
   size_t sel_cand;       // uint64 [B*SEL*nchunks*kk]
   size_t sel_cand_pages; // int32 [B*SEL*nchunks*kk], page id of each candidate
   size_t sel_pages;      // int32 [B*SEL*top_k], page ids of the selection (step path)
+  size_t f_counters;     // int32 [B*SEL] fused step: scoring tickets per unit
+  size_t f_flags;        // int32 [B*SEL] fused step: unit published for epoch + 1
+  size_t f_epoch;        // int32 [2]: epoch, CTAs done in this launch
+  size_t f_cand;         // uint64 [MAX_ATTN_CTAS * min(top_k, FUSED_KK_CAP)]
+  size_t f_cand_pages;   // int32, same count
   size_t attn_counters;  // int32 [S]
   size_t attn_parts;     // float [2*(MAX_ATTN_CTAS+S)][slot_floats]
   size_t dyn;            // dynamic-rep scratch
@@ -203,6 +210,16 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void griddep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -254,7 +271,20 @@ struct AttnLaunch {
   float scale_log2;
   int grid;
   bool pdl;  // launched as a programmatic dependent of the previous kernel
+  // fused step (selection inside the attention kernel, cooperative launch)
+  bool fused;
+  const void* reps;
+  int rep, R, ncpu, kk_f;
+  unsigned long long* f_cand;
+  int* f_cand_pages;
+  int* f_counters;
+  int32_t* sel_out;
+  int32_t* cnt_out;
+  int32_t* sel_pages_out;
+  int* f_flags;
+  int* f_epoch;  // [0] epoch, [1] CTAs done
 };
+int attn_fused_max_ctas_per_sm();
 cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream);
 
 struct SelectLaunch {

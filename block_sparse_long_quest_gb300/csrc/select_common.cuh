@@ -1,0 +1,226 @@
+// select_common.cuh — block scoring and radix top-k helpers shared by the
+// selection kernel and the fused decode-step kernel.
+#pragma once
+
+#include "kt_internal.cuh"
+
+namespace kt {
+namespace selc {
+
+__device__ __forceinline__ float dot8(const float* w, uint4 v) {
+  const __half2* h = reinterpret_cast<const __half2*>(&v);
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(h[i]);
+    s = fmaf(w[2 * i], f.x, s);
+    s = fmaf(w[2 * i + 1], f.y, s);
+  }
+  return s;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long make_key(float score, int block) {
+  return (static_cast<unsigned long long>(float_key(score)) << 32) |
+         static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(block));
+}
+
+// k-th largest of N distinct keys in shared memory (1 <= k <= N), all threads
+// of the CTA.  On return, a key is among the k largest iff
+// (key & *mask_out) >= *prefix_out.  MSB-first radix select on 8-bit digits;
+// the leading bits common to every key are skipped.  hist holds two 256-bin
+// histograms used alternately, so each pass needs two barriers.
+//
+// NT threads take part (thread index `tid` in [0, NT)); `bar` synchronises
+// exactly those threads.  sh_u64 holds 2 + 2*NT/32 entries, sh_int 2.
+template <int NT, class Bar>
+__device__ void radix_select(const unsigned long long* keys, int N, int k, unsigned int* hist,
+                             unsigned long long* sh_u64, int* sh_int,
+                             unsigned long long* prefix_out, unsigned long long* mask_out,
+                             int tid, Bar bar) {
+  constexpr int WARPS = NT / 32;
+  const int lane = tid & 31, warp = tid >> 5;
+  // common leading bits: AND and OR over all keys; clear both histograms
+  unsigned long long a = ~0ull, o = 0ull;
+  for (int i = tid; i < N; i += NT) {
+    a &= keys[i];
+    o |= keys[i];
+  }
+  for (int i = tid; i < 512; i += NT) hist[i] = 0u;
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    a &= __shfl_xor_sync(0xffffffffu, a, d);
+    o |= __shfl_xor_sync(0xffffffffu, o, d);
+  }
+  unsigned long long* red = sh_u64 + 2;  // [WARPS] ANDs, then [WARPS] ORs
+  if (lane == 0) {
+    red[warp] = a;
+    red[WARPS + warp] = o;
+  }
+  bar();
+  unsigned long long all_and = ~0ull, all_or = 0ull;
+#pragma unroll
+  for (int w = 0; w < WARPS; ++w) {
+    all_and &= red[w];
+    all_or |= red[WARPS + w];
+  }
+  const unsigned long long diff = all_and ^ all_or;
+  const int top = diff ? 63 - __clzll((long long)diff) : 0;  // highest differing bit
+  // digit windows [lo, hi) of up to 8 bits, starting at the top differing bit
+  int hi = top + 1;
+  unsigned long long mask = (hi >= 64) ? 0ull : ~((1ull << hi) - 1);
+  unsigned long long prefix = all_and & mask;
+  int need = k;
+  for (int pass = 0; hi > 0; ++pass) {
+    const int shift = hi > 8 ? hi - 8 : 0;
+    const unsigned long long dmask = (1ull << (hi - shift)) - 1;
+    unsigned int* H = hist + 256 * (pass & 1);
+    unsigned int* Hn = hist + 256 * ((pass + 1) & 1);
+    for (int base = 0; base < N; base += NT) {
+      // equal digits are counted once per warp: keys are often clustered
+      const int i = base + tid;
+      unsigned int bin = 256u;
+      if (i < N) {
+        const unsigned long long key = keys[i];
+        if ((key & mask) == prefix) bin = (unsigned)((key >> shift) & dmask);
+      }
+      const unsigned int peers = __match_any_sync(0xffffffffu, bin);
+      if (bin < 256u && lane == __ffs(peers) - 1) atomicAdd(&H[bin], (unsigned)__popc(peers));
+    }
+    bar();
+    if (warp == 0) {
+      // lane l holds digits 255-8l .. 248-8l (descending)
+      unsigned int c[8];
+      unsigned int local = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = H[255 - 8 * lane - i];
+        local += c[i];
+      }
+      unsigned int incl = local;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const unsigned int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+      }
+      const unsigned int excl = incl - local;
+      const bool hit = excl < (unsigned)need && (unsigned)need <= incl;
+      const unsigned int ball = __ballot_sync(0xffffffffu, hit);
+      const int src = __ffs(ball) - 1;
+      if (lane == src) {
+        unsigned int above = excl;
+        int digit = 0;
+        unsigned int bin = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (above + c[i] >= (unsigned)need) {
+            digit = 255 - 8 * lane - i;
+            bin = c[i];
+            break;
+          }
+          above += c[i];
+        }
+        const int need2 = need - (int)above;
+        sh_u64[0] = prefix | (static_cast<unsigned long long>(digit) << shift);
+        sh_u64[1] = mask | (dmask << shift);
+        sh_int[0] = need2;
+        sh_int[1] = (bin == (unsigned)need2) ? 1 : 0;
+      }
+    } else {
+      for (int i = tid - 32; i < 256; i += NT - 32) Hn[i] = 0u;  // next pass's bins
+    }
+    bar();
+    prefix = sh_u64[0];
+    mask = sh_u64[1];
+    need = sh_int[0];
+    if (sh_int[1]) break;
+    hi = shift;
+  }
+  bar();  // sh_* are rewritten by the caller
+  *prefix_out = prefix;
+  *mask_out = mask;
+}
+
+// Linear scoring (Max, Mean, Quest): each warp scores 8/NV blocks at a time;
+// a lane holds NV 16-byte vectors of each block, and every load of the group is
+// issued before any arithmetic.  V = 16-byte vectors per block and unit.
+//
+// reps: the representative pool; R rows of 128 per (page, KV head); P pages.
+template <int NV, bool F32, int WARPS>
+__device__ __forceinline__ void score_linear(const void* reps, int P, int H_kv, int R, int g0,
+                                             int js, int je, const int* pg, const float* wts,
+                                             int V, unsigned long long* keys, int warp, int lane,
+                                             int* status) {
+  constexpr int GB = 8 / NV;
+  constexpr int VE = F32 ? 4 : 8;
+  float w[NV][VE];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int vec = lane + 32 * v;
+#pragma unroll
+    for (int e = 0; e < VE; e += 4) {
+      const float4 f = (vec < V) ? *reinterpret_cast<const float4*>(wts + vec * VE + e)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+      w[v][e] = f.x;
+      w[v][e + 1] = f.y;
+      w[v][e + 2] = f.z;
+      w[v][e + 3] = f.w;
+    }
+  }
+  const size_t head_bytes = (size_t)R * D * (F32 ? 4 : 2);
+  for (int j0 = js + warp * GB; j0 < je; j0 += WARPS * GB) {
+    uint4 x[GB][NV];
+    int page[GB];
+#pragma unroll
+    for (int bi = 0; bi < GB; ++bi) {
+      const int j = j0 + bi;
+      page[bi] = (j < je) ? pg[j - js] : -1;
+      const bool ok = page[bi] >= 0 && page[bi] < P;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const uint8_t*>(reps) +
+          ((size_t)(ok ? page[bi] : 0) * H_kv + g0) * head_bytes);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int vec = lane + 32 * v;
+        x[bi][v] = (ok && vec < V) ? __ldg(src + vec) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int bi = 0; bi < GB; ++bi) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        if (F32) {
+          const float4 f = *reinterpret_cast<const float4*>(&x[bi][v]);
+          acc = fmaf(w[v][0], f.x, acc);
+          acc = fmaf(w[v][1], f.y, acc);
+          acc = fmaf(w[v][2], f.z, acc);
+          acc = fmaf(w[v][3], f.w, acc);
+        } else {
+          acc += dot8(w[v], x[bi][v]);
+        }
+      }
+      acc = warp_sum(acc);
+      const int j = j0 + bi;
+      if (j < je) {
+        const bool ok = page[bi] >= 0 && page[bi] < P;
+        if (lane == 0) keys[j - js] = make_key(ok ? acc : -INFINITY, j);
+        if (!ok && lane == 0) set_status(status, KT_ERR_DEVICE_CHECK);
+      }
+    }
+  }
+}
+
+}  // namespace selc
+}  // namespace kt

@@ -244,3 +244,32 @@ def test_more_segments_than_sms_and_empty_sequence():
                 assert row_rel_err(out[b, 2 * u:2 * u + 2], ref["out"][b, 2 * u:2 * u + 2]).max() <= TOL
     import block_sparse_long_quest_gb300 as kt
     assert kt.kt_read_device_status(ws) == kt.KT_OK
+
+
+def test_step_after_query_change_uses_the_new_selection():
+    # The one-launch step tags each unit's published selection with a launch
+    # counter; a step with new queries must never attend the previous one.
+    import block_sparse_long_quest_gb300 as kt
+    from kt_testlib import to_dev
+    w = synth.custom(33, RAGGED, num_q_heads=16, num_kv_heads=4, rep=synth.REP_QUEST,
+                     head_mode=synth.HEAD_SEPARATE, top_k=4, num_needles=3)
+    dw = DevWorkload(w)
+    dw.build_reps()
+    ws = kt.workspace(kt.KT_OP_SPARSE_STEP, dw.kv, dw.params)
+    q_first = w.q.copy()
+    for it in range(6):
+        q = q_first.copy() if it % 2 else synth.normal_f16(w.q.shape, 33, 900 + it, sigma=2.0)
+        dw.q.copy_(to_dev(q))
+        w.q = q
+        sel, cnt, out, _ = dw.step(ws)
+        ref = _oracle(w)
+        sel, cnt, out = sel.cpu().numpy(), cnt.cpu().numpy(), out.cpu().numpy()
+        for b in range(w.batch):
+            for u in range(dw.SEL):
+                ok, exact = selection_agrees(sel, cnt, ref, b, u)
+                assert ok, (it, b, u)
+                if exact:
+                    hs = list(range(4 * u, 4 * u + 4))
+                    assert row_rel_err(out[b, hs], ref["out"][b, hs]).max() <= TOL
+        assert kt.kt_read_device_status(ws) == kt.KT_OK
+
