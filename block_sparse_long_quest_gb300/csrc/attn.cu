@@ -47,6 +47,7 @@ constexpr int Q_BYTES = MAX_G * D * 2;
 constexpr int HALF_WARPS = CONSUMERS / 2;
 constexpr int SCRATCH_FLOATS = HALF_WARPS * MAX_G * (D + 2);
 static_assert(SCRATCH_FLOATS * 4 == ATTN_SCRATCH_BYTES, "scratch size shared with the host");
+static_assert(NCT == ATTN_CONSUMER_THREADS, "consumer threads shared with the host");
 
 struct StageInfo {
   int ntok, end, pad0, pad1;
@@ -59,7 +60,7 @@ struct SmemLayout {
   static constexpr int cum = scratch + SCRATCH_FLOATS * 4;  // [MAX_SEGS+1] work prefix
   static constexpr int info = cum + (MAX_SEGS + 1) * 4;
   static constexpr int bars = (info + STAGES * (int)sizeof(StageInfo) + 15) & ~15;
-  static constexpr int bcast = bars + (2 * STAGES + 1) * 8;
+  static constexpr int bcast = bars + (2 * STAGES + 2) * 8;
   static constexpr int total = bcast + 64 * 4;
 };
 constexpr int SMEM_BYTES = SmemLayout::total + 1024;  // + alignment slack
@@ -79,17 +80,15 @@ struct Params {
   float* parts;
   int B, H_kv, G, max_blocks, P, I_b, L_b, top_k, SEL, dense, slot_floats;
   float scale_log2;
-  // fused step only: in-kernel selection (see fused_select)
+  // fused step only: in-kernel selection (fused_score, fused_merge)
   const void* reps;
-  int rep, R, ncpu, kk_f;
+  int rep, R, ncpu, f_chunk, kk_f;
   unsigned long long* f_cand;
   int* f_cand_pages;
   int* f_counters;
+  int* f_done;
   int32_t* sel_out;
   int32_t* cnt_out;
-  int32_t* sel_pages_out;
-  int* f_flags;
-  int* f_epoch;
 };
 
 struct Part {
@@ -144,12 +143,205 @@ __device__ void warp_prefix(int* pref, int S, F count, int lane) {
   __syncwarp();
 }
 
+// Fused step, consumer warps of CTA c < U*ncpu: score slice c % ncpu (nominal
+// Context blocks I_b + s*f_chunk ...) of selection unit c / ncpu with the same
+// weights, dot products and keys as the selection kernel, keep the slice's best
+// kk_f (key 0 = empty slot) in the unit's candidate table and take a ticket.
+// The block-table entries do not depend on the sequence length, so they load
+// together with the length and the query rows.
+template <class Bar>
+__device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
+                            unsigned long long* sh_u64, int* sh_int, int ctid, int warp, int lane,
+                            Bar bar_c) {
+  const int U = p.B * p.SEL;
+  const int u = blockIdx.x / p.ncpu;
+  if (u >= U) return;
+  const int cs = blockIdx.x % p.ncpu;
+  const int bu = u / p.SEL, g0 = p.SEL == 1 ? 0 : u % p.SEL;
+  const int nkv = p.SEL == 1 ? p.H_kv : 1;
+  const int Rw = p.rep == KT_REP_QUEST ? 2 : 1;
+  const bool f32 = p.rep == KT_REP_MEAN;
+  const int H_q = p.H_kv * p.G;
+  const FusedScoreLayout Ls = fused_score_layout(nkv * Rw * D, p.f_chunk, p.kk_f);
+  float* wts = reinterpret_cast<float*>(scr);
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(scr + Ls.keys);
+  int* pgs = reinterpret_cast<int*>(scr + Ls.pgs);
+
+  const int js = p.I_b + cs * p.f_chunk;
+  for (int i = ctid; i < p.f_chunk; i += NCT) {
+    const int j = js + i;
+    pgs[i] = j < p.max_blocks ? __ldg(p.table + (size_t)bu * p.max_blocks + j) : -1;
+  }
+  const Part pu = partition(seq_len(p, bu), p.I_b, p.L_b);
+  // weights: query heads of each KV head summed in ascending order per channel
+  const __half* qu = p.q + ((size_t)bu * H_q + (size_t)g0 * p.G) * D;
+  for (int it = ctid; it < nkv * (D / 8); it += NCT) {
+    const int gi = it / (D / 8), c8 = it % (D / 8);
+    uint4 v[MAX_G];
+#pragma unroll
+    for (int hh = 0; hh < MAX_G; ++hh)
+      v[hh] = hh < p.G ? __ldg(reinterpret_cast<const uint4*>(qu + (size_t)(gi * p.G + hh) * D) + c8)
+                       : make_uint4(0u, 0u, 0u, 0u);
+    float sum[8], neg[8], pos[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sum[e] = neg[e] = pos[e] = 0.0f;
+#pragma unroll
+    for (int hh = 0; hh < MAX_G; ++hh) {
+      if (hh < p.G) {
+        const __half2* h2 = reinterpret_cast<const __half2*>(&v[hh]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(h2[e]);
+          sum[2 * e] += f.x;
+          neg[2 * e] += fminf(f.x, 0.0f);
+          pos[2 * e] += fmaxf(f.x, 0.0f);
+          sum[2 * e + 1] += f.y;
+          neg[2 * e + 1] += fminf(f.y, 0.0f);
+          pos[2 * e + 1] += fmaxf(f.y, 0.0f);
+        }
+      }
+    }
+    if (p.rep == KT_REP_QUEST) {
+      float4* wn = reinterpret_cast<float4*>(wts + (gi * 2 + 0) * D + c8 * 8);  // kmin row
+      float4* wp = reinterpret_cast<float4*>(wts + (gi * 2 + 1) * D + c8 * 8);  // kmax row
+      wn[0] = make_float4(neg[0], neg[1], neg[2], neg[3]);
+      wn[1] = make_float4(neg[4], neg[5], neg[6], neg[7]);
+      wp[0] = make_float4(pos[0], pos[1], pos[2], pos[3]);
+      wp[1] = make_float4(pos[4], pos[5], pos[6], pos[7]);
+    } else {
+      float4* w = reinterpret_cast<float4*>(wts + gi * D + c8 * 8);
+      w[0] = make_float4(sum[0], sum[1], sum[2], sum[3]);
+      w[1] = make_float4(sum[4], sum[5], sum[6], sum[7]);
+    }
+  }
+  const int je = min(js + p.f_chunk, pu.c1);
+  const int nloc = max(0, je - js);  // js >= c0 whenever the slice is not empty
+  bar_c();
+  if (nloc > 0) {
+    const int V = nkv * p.R * D / (f32 ? 4 : 8);
+    if (f32) {
+      if (V <= 32) selc::score_linear<1, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+      else if (V <= 64) selc::score_linear<2, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+      else if (V <= 128) selc::score_linear<4, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+      else selc::score_linear<8, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+    } else {
+      if (V <= 32) selc::score_linear<1, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+      else if (V <= 64) selc::score_linear<2, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+      else if (V <= 128) selc::score_linear<4, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+      else selc::score_linear<8, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+    }
+    bar_c();
+  }
+  unsigned long long* cand = p.f_cand + ((size_t)u * p.ncpu + cs) * p.kk_f;
+  int* cpage = p.f_cand_pages + ((size_t)u * p.ncpu + cs) * p.kk_f;
+  if (nloc <= p.kk_f) {
+    for (int i = ctid; i < p.kk_f; i += NCT) {
+      cand[i] = i < nloc ? keys[i] : 0ull;
+      cpage[i] = i < nloc ? pgs[i] : -1;
+    }
+  } else {
+    int* idx = reinterpret_cast<int*>(scr + Ls.idx);
+    selc::select_top<NCT>(keys, nloc, p.kk_f, idx,
+                          reinterpret_cast<unsigned long long*>(scr + Ls.bkey),
+                          reinterpret_cast<int*>(scr + Ls.bidx), hist, sh_u64, sh_int, ctid, bar_c);
+    for (int i = ctid; i < p.kk_f; i += NCT) {
+      cand[i] = keys[idx[i]];
+      cpage[i] = pgs[idx[i]];
+    }
+  }
+  __threadfence();
+  bar_c();
+  if (ctid == 0) atomicAdd(p.f_counters + u, 1);
+}
+
+// Fused step, consumer warps of every CTA: wait (bounded) for every scoring
+// slice of this segment's selection unit, pick the unit's top-k from the
+// candidate table (the same keys as the selection kernel, so the same blocks),
+// order them by block id and keep this CTA's share [i0, i1) of their page ids
+// in `slice`.  One CTA per unit writes sel / cnt.  Returns i1 - i0.
+template <class Bar>
+__device__ int fused_merge(const Params& p, uint8_t* scr, int* slice, unsigned int* hist,
+                           unsigned long long* sh_u64, int* sh_int, int b, int h, int ci,
+                           int ncta, int ctid, Bar bar_c) {
+  const int unit = b * p.SEL + (p.SEL == 1 ? 0 : h);
+  const Part pt = partition(seq_len(p, b), p.I_b, p.L_b);
+  const int keff = min(p.top_k, pt.c1 - pt.c0);
+  if (ctid == 0) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 0;; ++i) {
+      if (ld_acquire_gpu(p.f_counters + unit) >= p.ncpu) break;
+      if ((i & 63u) == 63u && globaltimer() - t0 > WAIT_LIMIT_NS) {
+        set_status(p.status, KT_ERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(32);
+    }
+  }
+  bar_c();
+  const int nslots = p.ncpu * p.kk_f;
+  const int kmax = min(p.top_k, nslots);
+  const FusedMergeLayout Lm = fused_merge_layout(nslots, kmax);
+  unsigned long long* all = reinterpret_cast<unsigned long long*>(scr + Lm.all);
+  int* allp = reinterpret_cast<int*>(scr + Lm.allp);
+  int* idx = reinterpret_cast<int*>(scr + Lm.idx);
+  uint32_t* cid = reinterpret_cast<uint32_t*>(scr + Lm.cid);
+  const bool writer = ci == 0 && (p.SEL != 1 || h == 0);
+  if (keff <= 0) {
+    if (writer && ctid == 0) p.cnt_out[unit] = 0;
+    return 0;
+  }
+  // gather the unit's candidates, four loads in flight per thread
+  const unsigned long long* src = p.f_cand + (size_t)unit * nslots;
+  const int* srcp = p.f_cand_pages + (size_t)unit * nslots;
+  for (int i0 = ctid; i0 < nslots; i0 += 4 * NCT) {
+    unsigned long long kx[4];
+    int px[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = i0 + r * NCT;
+      kx[r] = i < nslots ? __ldcg(src + i) : 0ull;
+      px[r] = i < nslots ? __ldcg(srcp + i) : -1;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = i0 + r * NCT;
+      if (i < nslots) {
+        all[i] = kx[r];
+        allp[i] = px[r];
+      }
+    }
+  }
+  bar_c();
+  selc::select_top<NCT>(all, nslots, keff, idx, reinterpret_cast<unsigned long long*>(scr + Lm.bkey),
+                        reinterpret_cast<int*>(scr + Lm.bidx), hist, sh_u64, sh_int, ctid, bar_c);
+  const int kpad = (keff + 3) & ~3;
+  for (int i = ctid; i < kpad; i += NCT)
+    cid[i] = i < keff ? 0xFFFFFFFFu - static_cast<uint32_t>(all[idx[i]] & 0xFFFFFFFFull)
+                      : 0xFFFFFFFFu;
+  bar_c();
+  // position of a chosen block = chosen blocks with a smaller id
+  const int i0 = (int)((long long)ci * keff / ncta), i1 = (int)((long long)(ci + 1) * keff / ncta);
+  for (int i = ctid; i < keff; i += NCT) {
+    const uint32_t id = cid[i];
+    int r = 0;
+    for (int m = 0; m < kpad; m += 4) {
+      const uint4 c4 = *reinterpret_cast<const uint4*>(cid + m);
+      r += (c4.x < id ? 1 : 0) + (c4.y < id ? 1 : 0) + (c4.z < id ? 1 : 0) + (c4.w < id ? 1 : 0);
+    }
+    if (writer) p.sel_out[(size_t)unit * p.top_k + r] = static_cast<int32_t>(id);
+    if (r >= i0 && r < i1) slice[r - i0] = allp[idx[i]];
+  }
+  if (writer && ctid == 0) p.cnt_out[unit] = keff;
+  bar_c();
+  return i1 - i0;
+}
+
 template <bool FUSED>
 __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ unsigned int f_hist[FUSED ? 512 : 1];
   __shared__ unsigned long long f_sh_u64[FUSED ? 2 + 2 * CONSUMERS : 1];
-  __shared__ int f_sh_int[FUSED ? 8 : 1];
+  __shared__ int f_sh_int[FUSED ? 4 : 1];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -162,9 +354,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   const uint32_t bar_full = smem_u32(smem + SmemLayout::bars);
   const uint32_t bar_empty = bar_full + STAGES * 8;
   const uint32_t bar_q = bar_empty + STAGES * 8;
+  const uint32_t bar_sel = bar_q + 8;  // fused: this CTA's selected pages are in `cum`
   const uint32_t kv_base = smem_u32(smem + SmemLayout::kv);
+  auto bar_c = [] { named_bar_sync(1, NCT); };
 
-  // ---- set-up: segment work prefix -> this CTA's segment and slice ----------
+  // ---- set-up: segment work prefix -> this CTA's segment and slice.  In the
+  // fused step the consumer warps score their selection slice meanwhile.
   if (warp == CONSUMERS) {
     if (lane == 0) {
       prefetch_tensormap(&p.kmap);
@@ -179,18 +374,22 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     const long long extra = grid - S, W = cum[S];
     __syncwarp();
     for (int s = lane; s <= S; s += 32) cum[s] = s + (int)(extra * cum[s] / W);
-    __syncwarp();
-  }
-  if (tid == 0) {
-    if (FUSED) bcast[62] = __ldcg(p.f_epoch);  // this launch's epoch
-    for (int i = 0; i < STAGES; ++i) {
-      mbar_init(bar_full + 8 * i, 1);
-      mbar_init(bar_empty + 8 * i, CONSUMERS);
+    if (lane == 0) {
+      for (int i = 0; i < STAGES; ++i) {
+        mbar_init(bar_full + 8 * i, 1);
+        mbar_init(bar_empty + 8 * i, CONSUMERS);
+      }
+      mbar_init(bar_q, 1);
+      mbar_init(bar_sel, 1);
+      fence_mbar_init();
     }
-    mbar_init(bar_q, 1);
-    fence_mbar_init();
+    __syncwarp();
+  } else if (FUSED) {
+    fused_score(p, reinterpret_cast<uint8_t*>(scratch), f_hist, f_sh_u64, f_sh_int, tid, warp,
+                lane, bar_c);
   }
-  __syncthreads();
+  if (!FUSED) __syncthreads();
+  else if (warp != CONSUMERS) named_bar_sync(2, THREADS);
   // CTAs of segment s: [cum[s], cum[s+1])
   int seg;
   {
@@ -202,6 +401,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     seg = lo;
   }
   const int f0 = cum[seg], ncta = cum[seg + 1] - f0, ci = cta - f0;
+  // fused: the consumers may overwrite `cum` once the producer has read it
+  if (FUSED && warp == CONSUMERS) named_bar_arrive(2, THREADS);
   const int b = seg / p.H_kv, h = seg % p.H_kv;
   const Part pt = partition(seq_len(p, b), p.I_b, p.L_b);
   const int nA = blocks_a(pt, p.dense);
@@ -224,24 +425,27 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         const int i = base + lane;
         int ntok = 0, row = 0;
         if (i < u1) {
-          int j;
+          int j, page = -1;
           if (phase == 0) {
             j = (p.dense || i < pt.c0) ? i : pt.c1 + (i - pt.c0);
+            page = p.table[(size_t)b * p.max_blocks + j];
+          } else if (FUSED) {
+            j = pt.c0;  // a selected Context block: full
+            page = cum[i];
           } else if (p.sel_pages == nullptr) {
             const int unit = p.SEL == 1 ? 0 : h;
             j = p.sel[((size_t)b * p.SEL + unit) * p.top_k + i];
             if (j < pt.c0 || j >= pt.c1) {
               set_status(p.status, KT_ERR_DEVICE_CHECK);
               j = -1;
+            } else {
+              page = p.table[(size_t)b * p.max_blocks + j];
             }
           } else {
             j = pt.c0;  // a selected Context block: full; its page comes with the selection
+            page = p.sel_pages[((size_t)b * p.SEL + (p.SEL == 1 ? 0 : h)) * p.top_k + i];
           }
           if (j >= 0) {
-            const int page =
-                (phase == 1 && p.sel_pages != nullptr)
-                    ? p.sel_pages[((size_t)b * p.SEL + (p.SEL == 1 ? 0 : h)) * p.top_k + i]
-                    : p.table[(size_t)b * p.max_blocks + j];
             if (page < 0 || page >= p.P) {
               set_status(p.status, KT_ERR_DEVICE_CHECK);
             } else {
@@ -283,32 +487,17 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       }
     };
     produce(0, a0, a1);
-    int nB = 0;
     if (FUSED) {
-      // Phase B needs this segment's selection unit: wait (bounded) until its
-      // last scoring CTA publishes it for this launch's epoch.
-      const int unit = b * p.SEL + (p.SEL == 1 ? 0 : h);
-      const int want = bcast[62] + 1;
-      int ready = 0;
-      if (lane == 0) {
-        const uint64_t t0 = globaltimer();
-        for (uint32_t i = 0;; ++i) {
-          if (ld_acquire_gpu(p.f_flags + unit) == want) {
-            ready = 1;
-            break;
-          }
-          if ((i & 63u) == 63u && globaltimer() - t0 > WAIT_LIMIT_NS) {
-            set_status(p.status, KT_ERR_TIMEOUT);
-            break;
-          }
-          __nanosleep(64);
-        }
-      }
-      ready = __shfl_sync(0xffffffffu, ready, 0);
-      nB = ready ? blocks_b_max(pt, 0, p.top_k) : 0;
+      // phase B: this CTA's share of the selected blocks, handed over by the
+      // consumer warps once the unit's selection is complete
+      int n1 = 0;
+      if (lane == 0 && mbar_wait(bar_sel, 0, p.status)) n1 = bcast[61];
+      n1 = __shfl_sync(0xffffffffu, n1, 0);
+      if (ok) produce(1, 0, n1);
     } else {
       // Phase B needs the selection: wait for the grid this launch depends on.
       griddep_wait();
+      int nB = 0;
       if (!p.dense) {
         const int cmax = blocks_b_max(pt, 0, p.top_k);
         nB = p.cnt ? p.cnt[b * p.SEL + (p.SEL == 1 ? 0 : h)] : cmax;
@@ -317,8 +506,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
           nB = nB < 0 ? 0 : cmax;
         }
       }
+      if (ok)
+        produce(1, (int)((long long)ci * nB / ncta), (int)((long long)(ci + 1) * nB / ncta));
     }
-    if (ok) produce(1, (int)((long long)ci * nB / ncta), (int)((long long)(ci + 1) * nB / ncta));
     if (ok && lane == 0) {
       const uint32_t st = it % STAGES;
       if (it < STAGES || mbar_wait(bar_empty + 8 * st, ((it / STAGES) - 1) & 1, p.status)) {
@@ -333,182 +523,26 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   // ============================ consumer warps ===============================
   const int g = lane >> 2, t = lane & 3;
   const int ctid = tid;
-  auto bar_c = [] { named_bar_sync(1, NCT); };
 
-  // Fused step: count this CTA done; the last CTA of the launch advances the
-  // epoch that tags the selection flags.
+  // Fused step: count this CTA done; the last CTA of the launch zeroes the
+  // scoring tickets and the count for the next launch.
   auto finish = [&]() {
     if (FUSED && ctid == 0) {
       __threadfence();
-      const int old = atomicAdd(p.f_epoch + 1, 1);
+      const int old = atomicAdd(p.f_done, 1);
       if (old == grid - 1) {
-        p.f_epoch[1] = 0;
-        __threadfence();
-        atomicAdd(p.f_epoch, 1);
+        for (int i = 0; i < p.B * p.SEL; ++i) p.f_counters[i] = 0;
+        p.f_done[0] = 0;
       }
     }
   };
 
   if constexpr (FUSED) {
-    // ---- in-kernel selection: CTA c scores slice c % ncpu of the Context
-    // blocks of selection unit c / ncpu (same scoring and keys as
-    // select_kernel), keeps its top kk_f, and the unit's last CTA merges,
-    // writes sel / cnt / page ids and publishes the unit for this epoch.
-    const int U = p.B * p.SEL;
-    const int u = cta / p.ncpu;
-    if (u < U) {
-      const int cs = cta % p.ncpu;
-      const int bu = u / p.SEL, g0 = p.SEL == 1 ? 0 : u % p.SEL;
-      const int nkv = p.SEL == 1 ? p.H_kv : 1;
-      const int Rw = p.rep == KT_REP_QUEST ? 2 : 1;
-      const bool f32 = p.rep == KT_REP_MEAN;
-      const Part pu = partition(seq_len(p, bu), p.I_b, p.L_b);
-      const int C = pu.c1 - pu.c0;
-      const int js = pu.c0 + (int)((long long)cs * C / p.ncpu);
-      const int je = pu.c0 + (int)((long long)(cs + 1) * C / p.ncpu);
-      const int nloc = je - js;
-      const int wfl = nkv * Rw * D;
-      float* wts = scratch;
-      unsigned long long* keys = reinterpret_cast<unsigned long long*>(scratch + ((wfl + 3) & ~3));
-      int* pgs = reinterpret_cast<int*>(keys + ((nloc + 1) & ~1));
-      unsigned long long* cand = p.f_cand + ((size_t)u * p.ncpu + cs) * p.kk_f;
-      int* cpage = p.f_cand_pages + ((size_t)u * p.ncpu + cs) * p.kk_f;
-      if (nloc > 0) {
-        for (int i = ctid; i < nloc; i += NCT) pgs[i] = __ldg(p.table + (size_t)bu * p.max_blocks + js + i);
-        for (int i = ctid; i < nkv * D; i += NCT) {
-          const int gi = i / D, c = i % D;
-          float sum = 0.0f, neg = 0.0f, pos = 0.0f;
-          for (int hh = 0; hh < p.G; ++hh) {
-            const float qv = __half2float(p.q[((size_t)bu * H_q + (g0 + gi) * p.G + hh) * D + c]);
-            sum += qv;
-            neg += fminf(qv, 0.0f);
-            pos += fmaxf(qv, 0.0f);
-          }
-          if (p.rep == KT_REP_QUEST) {
-            wts[(gi * 2 + 0) * D + c] = neg;  // pairs with the kmin row
-            wts[(gi * 2 + 1) * D + c] = pos;  // pairs with the kmax row
-          } else {
-            wts[gi * D + c] = sum;
-          }
-        }
-        bar_c();
-        const int V = nkv * p.R * D / (f32 ? 4 : 8);
-        if (f32) {
-          if (V <= 32) selc::score_linear<1, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
-          else if (V <= 64) selc::score_linear<2, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
-          else if (V <= 128) selc::score_linear<4, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
-          else selc::score_linear<8, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
-        } else {
-          if (V <= 32) selc::score_linear<1, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
-          else if (V <= 64) selc::score_linear<2, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
-          else if (V <= 128) selc::score_linear<4, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
-          else selc::score_linear<8, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
-        }
-        bar_c();
-        if (nloc <= p.kk_f) {
-          for (int i = ctid; i < p.kk_f; i += NCT) {
-            cand[i] = i < nloc ? keys[i] : 0ull;
-            cpage[i] = i < nloc ? pgs[i] : -1;
-          }
-        } else {
-          unsigned long long prefix, mask;
-          selc::radix_select<NCT>(keys, nloc, p.kk_f, f_hist, f_sh_u64, f_sh_int, &prefix, &mask,
-                                  ctid, bar_c);
-          if (ctid == 0) f_sh_int[2] = 0;
-          bar_c();
-          for (int i = ctid; i < nloc; i += NCT) {
-            const unsigned long long key = keys[i];
-            if ((key & mask) >= prefix) {
-              const int pos = atomicAdd(&f_sh_int[2], 1);
-              if (pos < p.kk_f) {
-                cand[pos] = key;
-                cpage[pos] = pgs[i];
-              } else {
-                set_status(p.status, KT_ERR_DEVICE_CHECK);
-              }
-            }
-          }
-        }
-      } else {
-        for (int i = ctid; i < p.kk_f; i += NCT) {
-          cand[i] = 0ull;
-          cpage[i] = -1;
-        }
-      }
-      __threadfence();
-      bar_c();
-      if (ctid == 0) {
-        const int old = atomicAdd(p.f_counters + u, 1);
-        f_sh_int[3] = (old == p.ncpu - 1) ? 1 : 0;
-        f_sh_int[4] = 0;
-      }
-      bar_c();
-      if (f_sh_int[3]) {
-        __threadfence();
-        // gather every candidate slot of the unit (key 0 = empty slot)
-        const int nslots = p.ncpu * p.kk_f;
-        const int kmax = min(p.top_k, nslots);
-        unsigned long long* all = reinterpret_cast<unsigned long long*>(scratch);
-        unsigned long long* chosen = all + nslots;
-        int* allp = reinterpret_cast<int*>(chosen + kmax);
-        int* chosenp = allp + nslots;
-        const unsigned long long* src = p.f_cand + (size_t)u * nslots;
-        const int* srcp = p.f_cand_pages + (size_t)u * nslots;
-        int real = 0;
-        for (int i = ctid; i < nslots; i += NCT) {
-          const unsigned long long key = __ldcg(src + i);
-          all[i] = key;
-          allp[i] = __ldcg(srcp + i);
-          real += key != 0ull ? 1 : 0;
-        }
-        real = selc::warp_sum_int(real);
-        if (lane == 0) atomicAdd(&f_sh_int[4], real);
-        bar_c();
-        const int keff = min(p.top_k, f_sh_int[4]);
-        if (keff > 0) {
-          if (keff == nslots) {
-            for (int i = ctid; i < nslots; i += NCT) {
-              chosen[i] = all[i];
-              chosenp[i] = allp[i];
-            }
-          } else {
-            unsigned long long prefix, mask;
-            selc::radix_select<NCT>(all, nslots, keff, f_hist, f_sh_u64, f_sh_int, &prefix,
-                                    &mask, ctid, bar_c);
-            if (ctid == 0) f_sh_int[2] = 0;
-            bar_c();
-            for (int i = ctid; i < nslots; i += NCT) {
-              const unsigned long long key = all[i];
-              if ((key & mask) >= prefix) {
-                const int pos = atomicAdd(&f_sh_int[2], 1);
-                if (pos < keff) {
-                  chosen[pos] = key;
-                  chosenp[pos] = allp[i];
-                } else {
-                  set_status(p.status, KT_ERR_DEVICE_CHECK);
-                }
-              }
-            }
-          }
-          bar_c();
-          for (int i = ctid; i < keff; i += NCT) {
-            const uint32_t id = 0xFFFFFFFFu - static_cast<uint32_t>(chosen[i] & 0xFFFFFFFFull);
-            int rank = 0;
-            for (int m = 0; m < keff; ++m)
-              rank += (0xFFFFFFFFu - static_cast<uint32_t>(chosen[m] & 0xFFFFFFFFull)) < id ? 1 : 0;
-            p.sel_out[(size_t)u * p.top_k + rank] = static_cast<int32_t>(id);
-            p.sel_pages_out[(size_t)u * p.top_k + rank] = chosenp[i];
-          }
-        }
-        if (ctid == 0) {
-          p.cnt_out[u] = keff;
-          p.f_counters[u] = 0;
-        }
-        __threadfence();
-        bar_c();
-        if (ctid == 0) st_release_gpu(p.f_flags + u, bcast[62] + 1);
-      }
-      bar_c();  // scratch is reused below
+    const int n1 = fused_merge(p, reinterpret_cast<uint8_t*>(scratch), cum, f_hist, f_sh_u64,
+                               f_sh_int, b, h, ci, ncta, ctid, bar_c);
+    if (ctid == 0) {
+      bcast[61] = n1;
+      mbar_arrive(bar_sel);
     }
   }
   float acc[16][4];
@@ -841,7 +875,7 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   p.seq_lens = a.seq_lens;
   p.sel = a.sel;
   p.cnt = a.cnt;
-  p.sel_pages = a.fused ? a.sel_pages_out : a.sel_pages;
+  p.sel_pages = a.sel_pages;
   p.out = a.out;
   p.status = a.status;
   p.counters = a.counters;
@@ -862,15 +896,14 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   p.rep = a.rep;
   p.R = a.R;
   p.ncpu = a.ncpu;
+  p.f_chunk = a.f_chunk;
   p.kk_f = a.kk_f;
   p.f_cand = a.f_cand;
   p.f_cand_pages = a.f_cand_pages;
   p.f_counters = a.f_counters;
+  p.f_done = a.f_done;
   p.sel_out = a.sel_out;
   p.cnt_out = a.cnt_out;
-  p.sel_pages_out = a.sel_pages_out;
-  p.f_flags = a.f_flags;
-  p.f_epoch = a.f_epoch;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);

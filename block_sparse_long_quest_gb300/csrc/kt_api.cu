@@ -114,10 +114,8 @@ WsLayout layout(kt_op op, const kt_paged_kv* kv, const kt_sparse_params* p, int 
                                                        : FUSED_KK_CAP);
   L.f_counters = off;
   off = align256(off + units * 4);
-  L.f_flags = off;
-  off = align256(off + units * 4);
-  L.f_epoch = off;
-  off = align256(off + 8);
+  L.f_done = off;
+  off = align256(off + 4);
   L.f_cand = off;
   off = align256(off + fcap * 8);
   L.f_cand_pages = off;
@@ -426,7 +424,8 @@ namespace {
 // per SM per segment and per selection unit, and the in-kernel selection
 // buffers fit the attention kernel's scratch.  Sets CTAs per unit and
 // candidates per CTA.
-bool fused_plan(const kt_paged_kv* kv, const kt_sparse_params* p, int sms, int* ncpu, int* kk) {
+bool fused_plan(const kt_paged_kv* kv, const kt_sparse_params* p, int sms, int* ncpu,
+                int* chunk_out, int* kk) {
   if (p->rep != KT_REP_MAX && p->rep != KT_REP_MEAN && p->rep != KT_REP_QUEST) return false;
   if (sms < 1 || sms > MAX_ATTN_CTAS) return false;
   const long long S = (long long)kv->batch * kv->num_kv_heads;
@@ -443,15 +442,15 @@ bool fused_plan(const kt_paged_kv* kv, const kt_sparse_params* p, int sms, int* 
   const bool f32 = p->rep == KT_REP_MEAN;
   const int V = nkv * reps_rows(p) * D / (f32 ? 4 : 8);
   if (V > 256) return false;
-  const size_t scratch = ATTN_SCRATCH_BYTES;
-  const size_t chunk_bytes = (size_t)((nkv * Rw * D + 3) & ~3) * 4 +
-                             (size_t)((chunk + 1) & ~1) * 8 + (size_t)chunk * 4;
-  const size_t nslots = (size_t)nc * k;
-  const size_t kmax = (size_t)p->top_k < nslots ? (size_t)p->top_k : nslots;
-  const size_t merge_bytes = (nslots + kmax) * 12;
-  if (chunk_bytes > scratch || merge_bytes > scratch) return false;
+  const long long nslots = (long long)nc * k;
+  if (nslots > (1 << 20)) return false;
+  const int kmax = (int)(p->top_k < nslots ? p->top_k : nslots);
+  if (fused_score_layout(nkv * Rw * D, chunk, k).total > ATTN_SCRATCH_BYTES) return false;
+  if (fused_merge_layout((int)nslots, kmax).total > ATTN_SCRATCH_BYTES) return false;
+  if (kmax > MAX_SEGS + 1) return false;  // the CTA's slice of page ids
   if (attn_fused_max_ctas_per_sm() < 1) return false;
   *ncpu = nc;
+  *chunk_out = chunk;
   *kk = k;
   return true;
 }
@@ -472,8 +471,8 @@ kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void
   const WsLayout L = layout(KT_OP_SPARSE_STEP, kv, p, 0);
   if (ws_bytes < L.total) return KT_ERR_WORKSPACE_TOO_SMALL;
   const int sms = num_sms();
-  int ncpu = 0, kk = 0;
-  if (sms > 0 && fused_plan(kv, p, sms, &ncpu, &kk)) {
+  int ncpu = 0, chunk = 0, kk = 0;
+  if (sms > 0 && fused_plan(kv, p, sms, &ncpu, &chunk, &kk)) {
     // one launch: selection inside the attention kernel
     CUtensorMap kmap, vmap;
     if (!make_pool_map(&kmap, kv->k_pool, kv) || !make_pool_map(&vmap, kv->v_pool, kv))
@@ -507,15 +506,14 @@ kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void
     a.rep = p->rep;
     a.R = reps_rows(p);
     a.ncpu = ncpu;
+    a.f_chunk = chunk;
     a.kk_f = kk;
     a.f_cand = at<unsigned long long>(ws, L.f_cand);
     a.f_cand_pages = at<int>(ws, L.f_cand_pages);
     a.f_counters = at<int>(ws, L.f_counters);
+    a.f_done = at<int>(ws, L.f_done);
     a.sel_out = sel;
     a.cnt_out = cnt;
-    a.sel_pages_out = at<int32_t>(ws, L.sel_pages);
-    a.f_flags = at<int>(ws, L.f_flags);
-    a.f_epoch = at<int>(ws, L.f_epoch);
     return cuda_status(launch_attention(a, (cudaStream_t)stream));
   }
   s = select_impl(q, kv, reps_pool, p, sel, cnt, nullptr, ws, L, true, (cudaStream_t)stream);

@@ -23,6 +23,41 @@ constexpr int SEL_MAX_CHUNK = 4096; // context blocks scored by one selection CT
 constexpr int MAX_DYN_REPS = 32;
 constexpr int ATTN_SCRATCH_BYTES = 4 * MAX_G * (D + 2) * 4;  // attention kernel scratch (smem)
 constexpr int FUSED_KK_CAP = 256;  // per-CTA candidates of the fused step
+constexpr int ATTN_CONSUMER_THREADS = 256;  // consumer threads of the attention kernel
+
+// Byte offsets inside the attention kernel's scratch for the in-kernel
+// selection of the fused step.  Scoring: weights (fp32), keys and page ids of
+// the CTA's Context slice, and the top-k temporaries when the slice holds more
+// than kk blocks.  Merge: every candidate key and page of the unit, the chosen
+// indices, their block ids (padded to a multiple of 4) and the top-k
+// temporaries.
+struct FusedScoreLayout {
+  int keys, pgs, idx, bkey, bidx, total;
+};
+__host__ __device__ inline FusedScoreLayout fused_score_layout(int wfl, int chunk, int kk) {
+  FusedScoreLayout L;
+  L.keys = (wfl * 4 + 15) & ~15;
+  L.pgs = L.keys + chunk * 8;
+  L.idx = L.pgs + chunk * 4;
+  L.bkey = (L.idx + kk * 4 + 15) & ~15;
+  L.bidx = L.bkey + ATTN_CONSUMER_THREADS * 8;
+  L.total = chunk > kk ? L.bidx + ATTN_CONSUMER_THREADS * 4 : L.idx;
+  return L;
+}
+struct FusedMergeLayout {
+  int all, allp, idx, cid, bkey, bidx, total;
+};
+__host__ __device__ inline FusedMergeLayout fused_merge_layout(int nslots, int kmax) {
+  FusedMergeLayout L;
+  L.all = 0;
+  L.allp = nslots * 8;
+  L.idx = L.allp + nslots * 4;
+  L.cid = (L.idx + kmax * 4 + 15) & ~15;
+  L.bkey = (L.cid + ((kmax + 3) & ~3) * 4 + 15) & ~15;
+  L.bidx = L.bkey + ATTN_CONSUMER_THREADS * 8;
+  L.total = L.bidx + ATTN_CONSUMER_THREADS * 4;
+  return L;
+}
 constexpr uint64_t WAIT_LIMIT_NS = 100000000ull;  // 100 ms bound on any device-side wait
 
 // ---------------------------------------------------------------------------
@@ -44,8 +79,7 @@ struct WsLayout {
   size_t sel_cand_pages; // int32 [B*SEL*nchunks*kk], page id of each candidate
   size_t sel_pages;      // int32 [B*SEL*top_k], page ids of the selection (step path)
   size_t f_counters;     // int32 [B*SEL] fused step: scoring tickets per unit
-  size_t f_flags;        // int32 [B*SEL] fused step: unit published for epoch + 1
-  size_t f_epoch;        // int32 [2]: epoch, CTAs done in this launch
+  size_t f_done;         // int32: fused step CTAs finished in this launch
   size_t f_cand;         // uint64 [MAX_ATTN_CTAS * min(top_k, FUSED_KK_CAP)]
   size_t f_cand_pages;   // int32, same count
   size_t attn_counters;  // int32 [S]
@@ -232,6 +266,10 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
   return static_cast<uint32_t>(__half_as_ushort(lo)) |
          (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
@@ -274,15 +312,16 @@ struct AttnLaunch {
   // fused step (selection inside the attention kernel, cooperative launch)
   bool fused;
   const void* reps;
-  int rep, R, ncpu, kk_f;
+  int rep, R;
+  int ncpu;     // CTAs scoring one selection unit
+  int f_chunk;  // Context blocks per scoring CTA (nominal, from max_blocks)
+  int kk_f;     // candidates kept per scoring CTA
   unsigned long long* f_cand;
   int* f_cand_pages;
-  int* f_counters;
+  int* f_counters;  // [B*SEL] scoring tickets, zero between launches
+  int* f_done;      // CTAs finished in this launch, zero between launches
   int32_t* sel_out;
   int32_t* cnt_out;
-  int32_t* sel_pages_out;
-  int* f_flags;
-  int* f_epoch;  // [0] epoch, [1] CTAs done
 };
 int attn_fused_max_ctas_per_sm();
 cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream);

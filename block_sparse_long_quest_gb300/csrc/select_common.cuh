@@ -152,6 +152,157 @@ __device__ void radix_select(const unsigned long long* keys, int N, int k, unsig
   *mask_out = mask;
 }
 
+// Indices of the k largest of N distinct keys in shared memory (1 <= k <= N),
+// written unordered to idx_out[0, k).  MSB-first 8-bit digit histograms over
+// the keys sharing the running prefix narrow the search until the bin holding
+// the k-th key has at most NT keys (usually after one pass); keys in higher
+// bins are taken outright and the bin's keys are ranked exactly among
+// themselves.  Scratch: hist 512 bins, bkey/bidx NT entries, sh_u64
+// 2 + 2*NT/32, sh_int 4.  All NT threads call it; `bar` synchronises them.
+template <int NT, class Bar>
+__device__ void select_top(const unsigned long long* keys, int N, int k, int* idx_out,
+                           unsigned long long* bkey, int* bidx, unsigned int* hist,
+                           unsigned long long* sh_u64, int* sh_int, int tid, Bar bar) {
+  constexpr int WARPS = NT / 32;
+  const int lane = tid & 31, warp = tid >> 5;
+  if (k >= N) {
+    for (int i = tid; i < N; i += NT) idx_out[i] = i;
+    bar();
+    return;
+  }
+  unsigned long long a = ~0ull, o = 0ull;
+  for (int i = tid; i < N; i += NT) {
+    a &= keys[i];
+    o |= keys[i];
+  }
+  for (int i = tid; i < 512; i += NT) hist[i] = 0u;
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    a &= __shfl_xor_sync(0xffffffffu, a, d);
+    o |= __shfl_xor_sync(0xffffffffu, o, d);
+  }
+  unsigned long long* red = sh_u64 + 2;
+  if (lane == 0) {
+    red[warp] = a;
+    red[WARPS + warp] = o;
+  }
+  if (tid == 0) {
+    sh_int[2] = 0;
+    sh_int[3] = 0;
+  }
+  bar();
+  unsigned long long all_and = ~0ull, all_or = 0ull;
+#pragma unroll
+  for (int w = 0; w < WARPS; ++w) {
+    all_and &= red[w];
+    all_or |= red[WARPS + w];
+  }
+  const unsigned long long diff = all_and ^ all_or;
+  int hi = diff ? 64 - __clzll((long long)diff) : 0;  // one past the top differing bit
+  unsigned long long mask = (hi >= 64) ? 0ull : ~((1ull << hi) - 1);
+  unsigned long long prefix = all_and & mask;
+  int need = k;
+  for (int pass = 0; hi > 0; ++pass) {
+    const int shift = hi > 8 ? hi - 8 : 0;
+    const unsigned long long dmask = (1ull << (hi - shift)) - 1;
+    unsigned int* H = hist + 256 * (pass & 1);
+    unsigned int* Hn = hist + 256 * ((pass + 1) & 1);
+    for (int base = 0; base < N; base += NT) {
+      const int i = base + tid;
+      unsigned int bin = 256u;
+      if (i < N) {
+        const unsigned long long key = keys[i];
+        if ((key & mask) == prefix) bin = (unsigned)((key >> shift) & dmask);
+      }
+      const unsigned int peers = __match_any_sync(0xffffffffu, bin);
+      if (bin < 256u && lane == __ffs(peers) - 1) atomicAdd(&H[bin], (unsigned)__popc(peers));
+    }
+    bar();
+    if (warp == 0) {
+      // lane l holds digits 255-8l .. 248-8l (descending)
+      unsigned int c[8];
+      unsigned int local = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = H[255 - 8 * lane - i];
+        local += c[i];
+      }
+      unsigned int incl = local;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const unsigned int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+      }
+      const unsigned int excl = incl - local;
+      const bool hit = excl < (unsigned)need && (unsigned)need <= incl;
+      const unsigned int ball = __ballot_sync(0xffffffffu, hit);
+      if (lane == __ffs(ball) - 1) {
+        unsigned int above = excl;
+        int digit = 0;
+        unsigned int inbin = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (above + c[i] >= (unsigned)need) {
+            digit = 255 - 8 * lane - i;
+            inbin = c[i];
+            break;
+          }
+          above += c[i];
+        }
+        sh_u64[0] = prefix | (static_cast<unsigned long long>(digit) << shift);
+        sh_u64[1] = mask | (dmask << shift);
+        sh_int[0] = need - (int)above;
+        sh_int[1] = (inbin <= (unsigned)NT || shift == 0) ? 1 : 0;
+      }
+    } else {
+      for (int i = tid - 32; i < 256; i += NT - 32) Hn[i] = 0u;
+    }
+    bar();
+    prefix = sh_u64[0];
+    mask = sh_u64[1];
+    need = sh_int[0];
+    if (sh_int[1]) break;
+    hi = shift;
+  }
+  // keys above the boundary bin are chosen; the bin's keys go to bkey/bidx
+  const unsigned int lt = (1u << lane) - 1u;
+  for (int base = 0; base < N; base += NT) {
+    const int i = base + tid;
+    unsigned long long key = 0ull, m = 0ull;
+    if (i < N) {
+      key = keys[i];
+      m = key & mask;
+    }
+    const bool up = i < N && m > prefix, eq = i < N && m == prefix;
+    const unsigned int bu = __ballot_sync(0xffffffffu, up);
+    const unsigned int be = __ballot_sync(0xffffffffu, eq);
+    int ou = 0, oe = 0;
+    if (lane == 0) {
+      if (bu) ou = atomicAdd(&sh_int[2], __popc(bu));
+      if (be) oe = atomicAdd(&sh_int[3], __popc(be));
+    }
+    ou = __shfl_sync(0xffffffffu, ou, 0);
+    oe = __shfl_sync(0xffffffffu, oe, 0);
+    if (up) idx_out[ou + __popc(bu & lt)] = i;
+    if (eq) {
+      const int pos = oe + __popc(be & lt);
+      if (pos < NT) {
+        bkey[pos] = key;
+        bidx[pos] = i;
+      }
+    }
+  }
+  bar();
+  const int taken = sh_int[2], nb = min(sh_int[3], NT);
+  if (tid < nb) {
+    const unsigned long long key = bkey[tid];
+    int r = 0;
+    for (int s = 0; s < nb; ++s) r += bkey[s] > key ? 1 : 0;
+    if (r < need && taken + r < k) idx_out[taken + r] = bidx[tid];
+  }
+  bar();
+}
+
 // Linear scoring (Max, Mean, Quest): each warp scores 8/NV blocks at a time;
 // a lane holds NV 16-byte vectors of each block, and every load of the group is
 // issued before any arithmetic.  V = 16-byte vectors per block and unit.
