@@ -65,6 +65,9 @@ struct SmemLayout {
 };
 constexpr int SMEM_BYTES = SmemLayout::total + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "attention shared memory exceeds the per-CTA limit");
+static_assert(SmemLayout::cum == SmemLayout::scratch + ATTN_SCRATCH_BYTES &&
+                  ATTN_MERGE_BYTES == ATTN_SCRATCH_BYTES + (MAX_SEGS + 1) * 4,
+              "the fused merge area is scratch + block prefix, contiguous");
 
 struct Params {
   CUtensorMap kmap, vmap;
@@ -143,38 +146,61 @@ __device__ void warp_prefix(int* pref, int S, F count, int lane) {
   __syncwarp();
 }
 
-// Fused step, consumer warps of CTA c < U*ncpu: score slice c % ncpu (nominal
-// Context blocks I_b + s*f_chunk ...) of selection unit c / ncpu with the same
-// weights, dot products and keys as the selection kernel, keep the slice's best
-// kk_f (key 0 = empty slot) in the unit's candidate table and take a ticket.
-// The block-table entries do not depend on the sequence length, so they load
-// together with the length and the query rows.
-template <class Bar>
-__device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
-                            unsigned long long* sh_u64, int* sh_int, int ctid, int warp, int lane,
-                            Bar bar_c) {
-  const int U = p.B * p.SEL;
-  const int u = blockIdx.x / p.ncpu;
-  if (u >= U) return;
-  const int cs = blockIdx.x % p.ncpu;
-  const int bu = u / p.SEL, g0 = p.SEL == 1 ? 0 : u % p.SEL;
-  const int nkv = p.SEL == 1 ? p.H_kv : 1;
-  const int Rw = p.rep == KT_REP_QUEST ? 2 : 1;
-  const bool f32 = p.rep == KT_REP_MEAN;
-  const int H_q = p.H_kv * p.G;
-  const FusedScoreLayout Ls = fused_score_layout(nkv * Rw * D, p.f_chunk, p.kk_f);
-  float* wts = reinterpret_cast<float*>(scr);
-  unsigned long long* keys = reinterpret_cast<unsigned long long*>(scr + Ls.keys);
-  int* pgs = reinterpret_cast<int*>(scr + Ls.pgs);
-
-  const int js = p.I_b + cs * p.f_chunk;
-  for (int i = ctid; i < p.f_chunk; i += NCT) {
-    const int j = js + i;
-    pgs[i] = j < p.max_blocks ? __ldg(p.table + (size_t)bu * p.max_blocks + j) : -1;
+// Number of keys in a[0, n) greater than key; a is 16-byte aligned and n even.
+// Eight loads in flight per iteration.
+__device__ __forceinline__ int count_greater(const unsigned long long* a, int n,
+                                             unsigned long long key) {
+  int r0 = 0, r1 = 0;
+  int m = 0;
+#pragma unroll 1
+  for (; m + 8 <= n; m += 8) {
+    const ulonglong2 v0 = *reinterpret_cast<const ulonglong2*>(a + m);
+    const ulonglong2 v1 = *reinterpret_cast<const ulonglong2*>(a + m + 2);
+    const ulonglong2 v2 = *reinterpret_cast<const ulonglong2*>(a + m + 4);
+    const ulonglong2 v3 = *reinterpret_cast<const ulonglong2*>(a + m + 6);
+    r0 += (v0.x > key ? 1 : 0) + (v0.y > key ? 1 : 0) + (v1.x > key ? 1 : 0) + (v1.y > key ? 1 : 0);
+    r1 += (v2.x > key ? 1 : 0) + (v2.y > key ? 1 : 0) + (v3.x > key ? 1 : 0) + (v3.y > key ? 1 : 0);
   }
-  const Part pu = partition(seq_len(p, bu), p.I_b, p.L_b);
-  // weights: query heads of each KV head summed in ascending order per channel
+#pragma unroll 1
+  for (; m < n; m += 2) {
+    const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(a + m);
+    r0 += (v.x > key ? 1 : 0) + (v.y > key ? 1 : 0);
+  }
+  return r0 + r1;
+}
+
+// Number of ids in a[0, n) smaller than id; a is 16-byte aligned, n a multiple of 4.
+__device__ __forceinline__ int count_less_u32(const uint32_t* a, int n, uint32_t id) {
+  int r0 = 0, r1 = 0;
+  int m = 0;
+#pragma unroll 1
+  for (; m + 16 <= n; m += 16) {
+    const uint4 v0 = *reinterpret_cast<const uint4*>(a + m);
+    const uint4 v1 = *reinterpret_cast<const uint4*>(a + m + 4);
+    const uint4 v2 = *reinterpret_cast<const uint4*>(a + m + 8);
+    const uint4 v3 = *reinterpret_cast<const uint4*>(a + m + 12);
+    r0 += (v0.x < id ? 1 : 0) + (v0.y < id ? 1 : 0) + (v0.z < id ? 1 : 0) + (v0.w < id ? 1 : 0) +
+          (v1.x < id ? 1 : 0) + (v1.y < id ? 1 : 0) + (v1.z < id ? 1 : 0) + (v1.w < id ? 1 : 0);
+    r1 += (v2.x < id ? 1 : 0) + (v2.y < id ? 1 : 0) + (v2.z < id ? 1 : 0) + (v2.w < id ? 1 : 0) +
+          (v3.x < id ? 1 : 0) + (v3.y < id ? 1 : 0) + (v3.z < id ? 1 : 0) + (v3.w < id ? 1 : 0);
+  }
+#pragma unroll 1
+  for (; m < n; m += 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(a + m);
+    r0 += (v.x < id ? 1 : 0) + (v.y < id ? 1 : 0) + (v.z < id ? 1 : 0) + (v.w < id ? 1 : 0);
+  }
+  return r0 + r1;
+}
+
+// Fused step: the linear weight rows of KV heads g0 .. g0+nkv-1 of sequence bu
+// (query heads summed in ascending order per channel; Quest: the negative and
+// positive parts, paired with the kmin and kmax rows).  Same values as the
+// selection kernel.
+__device__ __forceinline__ void fused_weights(const Params& p, float* wts, int bu, int g0, int nkv,
+                                           int ctid) {
+  const int H_q = p.H_kv * p.G;
   const __half* qu = p.q + ((size_t)bu * H_q + (size_t)g0 * p.G) * D;
+#pragma unroll 1
   for (int it = ctid; it < nkv * (D / 8); it += NCT) {
     const int gi = it / (D / 8), c8 = it % (D / 8);
     uint4 v[MAX_G];
@@ -214,53 +240,111 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
       w[1] = make_float4(sum[4], sum[5], sum[6], sum[7]);
     }
   }
+}
+
+// Fused step, consumer warps of CTA c < U*ncpu: score slice c % ncpu (nominal
+// Context blocks I_b + s*f_chunk ...) of selection unit c / ncpu with the same
+// weights, dot products and keys as the selection kernel, keep the slice's best
+// kk_f (key 0 = empty slot) in the unit's candidate table and take a ticket.
+// The block-table entries of the nominal slice do not depend on the sequence
+// length, so they load together with the length and the query rows.
+template <class Bar>
+__device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
+                            unsigned long long* sh_u64, int* sh_int, int ctid, int warp, int lane,
+                            Bar bar_c) {
+  const int U = p.B * p.SEL;
+  const int u = blockIdx.x / p.ncpu;
+  if (u >= U) return;
+  const int cs = blockIdx.x % p.ncpu;
+  const int bu = u / p.SEL, g0 = p.SEL == 1 ? 0 : u % p.SEL;
+  const int nkv = p.SEL == 1 ? p.H_kv : 1;
+  const int Rw = p.rep == KT_REP_QUEST ? 2 : 1;
+  const bool f32 = p.rep == KT_REP_MEAN;
+  const FusedScoreLayout Ls = fused_score_layout(nkv * Rw * D, p.f_chunk, p.kk_f);
+  float* wts = reinterpret_cast<float*>(scr);
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(scr + Ls.keys);
+  int* pgs = reinterpret_cast<int*>(scr + Ls.pgs);
+
+  const int js = p.I_b + cs * p.f_chunk;
+#pragma unroll 1
+  for (int i = ctid; i < p.f_chunk; i += NCT) {
+    const int j = js + i;
+    pgs[i] = j < p.max_blocks ? __ldg(p.table + (size_t)bu * p.max_blocks + j) : -1;
+  }
+  const Part pu = partition(seq_len(p, bu), p.I_b, p.L_b);
+  fused_weights(p, wts, bu, g0, nkv, ctid);
   const int je = min(js + p.f_chunk, pu.c1);
   const int nloc = max(0, je - js);  // js >= c0 whenever the slice is not empty
   bar_c();
   if (nloc > 0) {
     const int V = nkv * p.R * D / (f32 ? 4 : 8);
+#define KT_SCORE(NV, F) selc::score_linear<NV, F, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status)
     if (f32) {
-      if (V <= 32) selc::score_linear<1, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
-      else if (V <= 64) selc::score_linear<2, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
-      else if (V <= 128) selc::score_linear<4, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
-      else selc::score_linear<8, true, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+      if (V <= 32) KT_SCORE(1, true);
+      else if (V <= 64) KT_SCORE(2, true);
+      else if (V <= 128) KT_SCORE(4, true);
+      else KT_SCORE(8, true);
     } else {
-      if (V <= 32) selc::score_linear<1, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
-      else if (V <= 64) selc::score_linear<2, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
-      else if (V <= 128) selc::score_linear<4, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
-      else selc::score_linear<8, false, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status);
+      if (V <= 32) KT_SCORE(1, false);
+      else if (V <= 64) KT_SCORE(2, false);
+      else if (V <= 128) KT_SCORE(4, false);
+      else KT_SCORE(8, false);
     }
+#undef KT_SCORE
     bar_c();
   }
+  // the slice's best min(nloc, kk_f) keys, written in descending key order
+  // (empty slots: key 0, page -1), then the ticket
+  const int nk = min(nloc, p.kk_f);
+  const unsigned long long* ck = keys;
+  const int* cp = pgs;
+  if (nloc > p.kk_f) {
+    int* idx = reinterpret_cast<int*>(scr + Ls.idx);
+    unsigned long long* bkey = reinterpret_cast<unsigned long long*>(scr + Ls.bkey);
+    int* bidx = reinterpret_cast<int*>(scr + Ls.bidx);
+    selc::select_top<NCT>(keys, nloc, p.kk_f, idx, bkey, bidx, hist, sh_u64, sh_int, ctid, bar_c);
+#pragma unroll 1
+    for (int i = ctid; i < p.kk_f; i += NCT) {  // chosen keys, contiguous
+      bkey[i] = keys[idx[i]];
+      bidx[i] = pgs[idx[i]];
+    }
+    ck = bkey;
+    cp = bidx;
+  }
+  if (ctid == 0 && (nk & 1)) const_cast<unsigned long long*>(ck)[nk] = 0ull;
+  bar_c();
   unsigned long long* cand = p.f_cand + ((size_t)u * p.ncpu + cs) * p.kk_f;
   int* cpage = p.f_cand_pages + ((size_t)u * p.ncpu + cs) * p.kk_f;
-  if (nloc <= p.kk_f) {
-    for (int i = ctid; i < p.kk_f; i += NCT) {
-      cand[i] = i < nloc ? keys[i] : 0ull;
-      cpage[i] = i < nloc ? pgs[i] : -1;
-    }
-  } else {
-    int* idx = reinterpret_cast<int*>(scr + Ls.idx);
-    selc::select_top<NCT>(keys, nloc, p.kk_f, idx,
-                          reinterpret_cast<unsigned long long*>(scr + Ls.bkey),
-                          reinterpret_cast<int*>(scr + Ls.bidx), hist, sh_u64, sh_int, ctid, bar_c);
-    for (int i = ctid; i < p.kk_f; i += NCT) {
-      cand[i] = keys[idx[i]];
-      cpage[i] = pgs[idx[i]];
+#pragma unroll 1
+  for (int i = ctid; i < p.kk_f; i += NCT) {
+    if (i < nk) {
+      const unsigned long long key = ck[i];
+      const int r = count_greater(ck, (nk + 1) & ~1, key);
+      cand[r] = key;
+      cpage[r] = cp[i];
+    } else {
+      cand[i] = 0ull;
+      cpage[i] = -1;
     }
   }
-  __threadfence();
   bar_c();
-  if (ctid == 0) atomicAdd(p.f_counters + u, 1);
+  if (ctid == 0) red_release_gpu_add(p.f_counters + u, 1);
 }
 
 // Fused step, consumer warps of every CTA: wait (bounded) for every scoring
 // slice of this segment's selection unit, pick the unit's top-k from the
-// candidate table (the same keys as the selection kernel, so the same blocks),
-// order them by block id and keep this CTA's share [i0, i1) of their page ids
-// in `slice`.  One CTA per unit writes sel / cnt.  Returns i1 - i0.
+// candidate table, order the chosen blocks by id and keep this CTA's share
+// [i0, i1) of their page ids in the merge area's slice.  One CTA per unit
+// writes sel / cnt.  Returns i1 - i0.
+//
+// The per-slice lists are sorted, so the keff-th largest of their first J
+// keys (J lists' heads, ncpu * J >= keff) is a lower bound T0 for the unit's
+// keff-th largest key: only keys >= T0 can be chosen, and they are few
+// (at most keff / J lists reach T0 at their J-th key).  Those are ranked
+// exactly by counting; the same keys as the selection kernel give the same
+// blocks.
 template <class Bar>
-__device__ int fused_merge(const Params& p, uint8_t* scr, int* slice, unsigned int* hist,
+__device__ int fused_merge(const Params& p, uint8_t* scr, unsigned int* hist,
                            unsigned long long* sh_u64, int* sh_int, int b, int h, int ci,
                            int ncta, int ctid, Bar bar_c) {
   const int unit = b * p.SEL + (p.SEL == 1 ? 0 : h);
@@ -278,58 +362,199 @@ __device__ int fused_merge(const Params& p, uint8_t* scr, int* slice, unsigned i
     }
   }
   bar_c();
-  const int nslots = p.ncpu * p.kk_f;
-  const int kmax = min(p.top_k, nslots);
-  const FusedMergeLayout Lm = fused_merge_layout(nslots, kmax);
+  const int kk = p.kk_f, nslots = p.ncpu * kk;
+  const FusedMergeLayout Lm = fused_merge_layout(p.ncpu, kk, min(p.top_k, nslots));
   unsigned long long* all = reinterpret_cast<unsigned long long*>(scr + Lm.all);
   int* allp = reinterpret_cast<int*>(scr + Lm.allp);
+  unsigned long long* heads = reinterpret_cast<unsigned long long*>(scr + Lm.heads);
+  unsigned long long* ckey = reinterpret_cast<unsigned long long*>(scr + Lm.ck);
+  int* cslot = reinterpret_cast<int*>(scr + Lm.cs);
   int* idx = reinterpret_cast<int*>(scr + Lm.idx);
   uint32_t* cid = reinterpret_cast<uint32_t*>(scr + Lm.cid);
+  int* slice = reinterpret_cast<int*>(scr + Lm.slice);
   const bool writer = ci == 0 && (p.SEL != 1 || h == 0);
   if (keff <= 0) {
     if (writer && ctid == 0) p.cnt_out[unit] = 0;
     return 0;
   }
-  // gather the unit's candidates, four loads in flight per thread
+  // gather: slots ctid + r*NCT of the unit's table into registers (one round
+  // trip), their pages and keys into shared memory, and the head sample
+  constexpr int GP = FUSED_GATHER_PER_THREAD;
   const unsigned long long* src = p.f_cand + (size_t)unit * nslots;
   const int* srcp = p.f_cand_pages + (size_t)unit * nslots;
-  for (int i0 = ctid; i0 < nslots; i0 += 4 * NCT) {
-    unsigned long long kx[4];
-    int px[4];
+  const int J = Lm.J, H = Lm.nheads, Hpad = (H + 1) & ~1;
+  unsigned long long kx[GP];
+  int px[GP];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = i0 + r * NCT;
-      kx[r] = i < nslots ? __ldcg(src + i) : 0ull;
-      px[r] = i < nslots ? __ldcg(srcp + i) : -1;
+  for (int r = 0; r < GP; ++r) {
+    const int s = ctid + r * NCT;
+    kx[r] = s < nslots ? __ldcg(src + s) : 0ull;
+    px[r] = s < nslots ? __ldcg(srcp + s) : -1;
+  }
+  // head sample with its common leading bits (AND / OR) and nonzero count
+  unsigned long long h_and = ~0ull, h_or = 0ull;
+  int h_nz = 0;
+#pragma unroll 1
+  for (int hh = ctid; hh < Hpad; hh += NCT) {
+    const unsigned long long key = hh < H ? __ldcg(src + (hh / J) * kk + (hh % J)) : 0ull;
+    heads[hh] = key;
+    if (key != 0ull) {
+      h_and &= key;
+      h_or |= key;
+      ++h_nz;
     }
+  }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = i0 + r * NCT;
-      if (i < nslots) {
-        all[i] = kx[r];
-        allp[i] = px[r];
+  for (int r = 0; r < GP; ++r) {
+    const int s = ctid + r * NCT;
+    if (s < nslots) {
+      all[s] = kx[r];
+      allp[s] = px[r];
+    }
+  }
+  const int kpad = (keff + 3) & ~3;
+#pragma unroll 1
+  for (int i = ctid; i < kpad; i += NCT) {
+    idx[i] = -1;
+    cid[i] = 0xFFFFFFFFu;
+  }
+#pragma unroll 1
+  for (int i = ctid; i < Lm.mcap; i += NCT) ckey[i] = 0ull;
+  hist[ctid] = 0u;  // NCT == 256 bins
+  {
+    const int lane = ctid & 31, w = ctid >> 5;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+      h_and &= __shfl_xor_sync(0xffffffffu, h_and, d);
+      h_or |= __shfl_xor_sync(0xffffffffu, h_or, d);
+      h_nz += __shfl_xor_sync(0xffffffffu, h_nz, d);
+    }
+    if (lane == 0) {
+      sh_u64[2 + w] = h_and;
+      sh_u64[2 + CONSUMERS + w] = h_or;
+      hist[256 + w] = (unsigned)h_nz;
+    }
+  }
+  if (ctid == 0) {
+    sh_u64[0] = 1ull;
+    sh_int[0] = 0;
+  }
+  bar_c();
+  // T0: lower edge of the 8-bit digit bin (just below the heads' common
+  // leading bits) that holds the keff-th largest head.  At least keff heads,
+  // hence keys, are >= T0, so T0 bounds the keff-th largest key from below;
+  // with fewer than keff nonzero heads every nonzero key stays (T0 = 1).
+  {
+    unsigned long long a = ~0ull, o = 0ull;
+    int nz = 0;
+#pragma unroll
+    for (int w = 0; w < CONSUMERS; ++w) {
+      a &= sh_u64[2 + w];
+      o |= sh_u64[2 + CONSUMERS + w];
+      nz += (int)hist[256 + w];
+    }
+    if (nz >= keff) {
+      const unsigned long long diff = a ^ o;
+      const int hi = diff ? 64 - __clzll((long long)diff) : 0;
+      const int shift = hi > 8 ? hi - 8 : 0;
+      const unsigned long long pmask = hi >= 64 ? 0ull : ~((1ull << hi) - 1);
+      const unsigned long long prefix = a & pmask;
+#pragma unroll 1
+      for (int hh = ctid; hh < H; hh += NCT) {
+        const unsigned long long key = heads[hh];
+        if (key != 0ull) atomicAdd(&hist[(unsigned)((key >> shift) & 255ull)], 1u);
+      }
+      bar_c();
+      if (ctid < 32) {
+        // lane l holds digits 255-8l .. 248-8l (descending)
+        const int lane = ctid;
+        unsigned int c[8], local = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          c[i] = hist[255 - 8 * lane - i];
+          local += c[i];
+        }
+        unsigned int incl = local;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const unsigned int v = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += v;
+        }
+        const unsigned int excl = incl - local;
+        const bool hit = excl < (unsigned)keff && (unsigned)keff <= incl;
+        if (hit) {
+          unsigned int above = excl;
+          int digit = 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            above += c[i];
+            if (above >= (unsigned)keff) {
+              digit = 255 - 8 * lane - i;
+              break;
+            }
+          }
+          sh_u64[0] = prefix | (static_cast<unsigned long long>(digit) << shift);
+        }
       }
     }
   }
   bar_c();
-  selc::select_top<NCT>(all, nslots, keff, idx, reinterpret_cast<unsigned long long*>(scr + Lm.bkey),
-                        reinterpret_cast<int*>(scr + Lm.bidx), hist, sh_u64, sh_int, ctid, bar_c);
-  const int kpad = (keff + 3) & ~3;
-  for (int i = ctid; i < kpad; i += NCT)
-    cid[i] = i < keff ? 0xFFFFFFFFu - static_cast<uint32_t>(all[idx[i]] & 0xFFFFFFFFull)
-                      : 0xFFFFFFFFu;
+  const unsigned long long T0 = sh_u64[0] > 0ull ? sh_u64[0] : 1ull;
+  // keys >= T0 with their slots: one shared atomic per warp
+  {
+    const int lane = ctid & 31;
+    const unsigned int lt = (1u << lane) - 1u;
+    unsigned int bal[GP];
+    int tot = 0;
+#pragma unroll
+    for (int r = 0; r < GP; ++r) {
+      bal[r] = __ballot_sync(0xffffffffu, kx[r] >= T0);
+      tot += __popc(bal[r]);
+    }
+    int o = 0;
+    if (lane == 0 && tot) o = atomicAdd(&sh_int[0], tot);
+    o = __shfl_sync(0xffffffffu, o, 0);
+#pragma unroll
+    for (int r = 0; r < GP; ++r) {
+      const int pos = o + __popc(bal[r] & lt);
+      if (kx[r] >= T0 && pos < Lm.mcap) {
+        ckey[pos] = kx[r];
+        cslot[pos] = ctid + r * NCT;
+      }
+      o += __popc(bal[r]);
+    }
+  }
   bar_c();
+  const int M = sh_int[0];
+  if (M <= Lm.mcap) {
+    // exact rank among them; the chosen keep their block ids for the ordering
+#pragma unroll 1
+    for (int i = ctid; i < M; i += NCT) {
+      const unsigned long long key = ckey[i];
+      const int r = count_greater(ckey, (M + 1) & ~1, key);
+      if (r < keff) {
+        idx[r] = cslot[i];
+        cid[r] = 0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFull);
+      }
+    }
+  } else {
+    // many keys near the bound: radix selection over the whole table
+    selc::select_top<NCT>(all, nslots, keff, idx, ckey, cslot, hist, sh_u64, sh_int, ctid, bar_c);
+#pragma unroll 1
+    for (int i = ctid; i < keff; i += NCT)
+      cid[i] = 0xFFFFFFFFu - static_cast<uint32_t>(all[idx[i]] & 0xFFFFFFFFull);
+  }
+  bar_c();
+  if (ctid == 0 && M < keff) set_status(p.status, KT_ERR_DEVICE_CHECK);
   // position of a chosen block = chosen blocks with a smaller id
   const int i0 = (int)((long long)ci * keff / ncta), i1 = (int)((long long)(ci + 1) * keff / ncta);
+#pragma unroll 1
   for (int i = ctid; i < keff; i += NCT) {
     const uint32_t id = cid[i];
-    int r = 0;
-    for (int m = 0; m < kpad; m += 4) {
-      const uint4 c4 = *reinterpret_cast<const uint4*>(cid + m);
-      r += (c4.x < id ? 1 : 0) + (c4.y < id ? 1 : 0) + (c4.z < id ? 1 : 0) + (c4.w < id ? 1 : 0);
-    }
-    if (writer) p.sel_out[(size_t)unit * p.top_k + r] = static_cast<int32_t>(id);
-    if (r >= i0 && r < i1) slice[r - i0] = allp[idx[i]];
+    const int r = min(count_less_u32(cid, kpad, id), keff - 1);
+    const int x = idx[i];
+    if (writer) p.sel_out[(size_t)unit * p.top_k + r] = x >= 0 ? static_cast<int32_t>(id) : -1;
+    if (r >= i0 && r < i1) slice[r - i0] = x >= 0 ? allp[x] : -1;
   }
   if (writer && ctid == 0) p.cnt_out[unit] = keff;
   bar_c();
@@ -342,8 +567,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   __shared__ unsigned int f_hist[FUSED ? 512 : 1];
   __shared__ unsigned long long f_sh_u64[FUSED ? 2 + 2 * CONSUMERS : 1];
   __shared__ int f_sh_int[FUSED ? 4 : 1];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-byte aligned (128-byte swizzled TMA boxes); offsetting the array
+  // itself keeps the accesses below in the shared address space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grid = gridDim.x, cta = blockIdx.x;
   const int S = p.B * p.H_kv, H_q = p.H_kv * p.G;
@@ -354,7 +580,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   const uint32_t bar_full = smem_u32(smem + SmemLayout::bars);
   const uint32_t bar_empty = bar_full + STAGES * 8;
   const uint32_t bar_q = bar_empty + STAGES * 8;
-  const uint32_t bar_sel = bar_q + 8;  // fused: this CTA's selected pages are in `cum`
+  const uint32_t bar_sel = bar_q + 8;  // fused: this CTA's selected pages are ready
   const uint32_t kv_base = smem_u32(smem + SmemLayout::kv);
   auto bar_c = [] { named_bar_sync(1, NCT); };
 
@@ -417,6 +643,13 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       bulk_load(smem_u32(smem + SmemLayout::q), p.q + ((size_t)b * H_q + h * p.G) * D, qbytes,
                 bar_q);
     }
+    // fused: this CTA's selected page ids, written by the consumer warps
+    const int* fslice = nullptr;
+    if (FUSED) {
+      const FusedMergeLayout Lm =
+          fused_merge_layout(p.ncpu, p.kk_f, min(p.top_k, p.ncpu * p.kk_f));
+      fslice = reinterpret_cast<const int*>(smem + SmemLayout::scratch + Lm.slice);
+    }
     uint32_t it = 0;
     bool ok = true;
     // phase 0: list index i -> Initial/Local block; phase 1: i -> selected block
@@ -431,7 +664,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
             page = p.table[(size_t)b * p.max_blocks + j];
           } else if (FUSED) {
             j = pt.c0;  // a selected Context block: full
-            page = cum[i];
+            page = fslice[i];
           } else if (p.sel_pages == nullptr) {
             const int unit = p.SEL == 1 ? 0 : h;
             j = p.sel[((size_t)b * p.SEL + unit) * p.top_k + i];
@@ -491,7 +724,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       // phase B: this CTA's share of the selected blocks, handed over by the
       // consumer warps once the unit's selection is complete
       int n1 = 0;
-      if (lane == 0 && mbar_wait(bar_sel, 0, p.status)) n1 = bcast[61];
+      if (lane == 0 && mbar_wait_sleep(bar_sel, 0, p.status, 128)) n1 = bcast[61];
       n1 = __shfl_sync(0xffffffffu, n1, 0);
       if (ok) produce(1, 0, n1);
     } else {
@@ -528,8 +761,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   // scoring tickets and the count for the next launch.
   auto finish = [&]() {
     if (FUSED && ctid == 0) {
-      __threadfence();
-      const int old = atomicAdd(p.f_done, 1);
+      const int old = atom_acq_rel_gpu_add(p.f_done, 1);
       if (old == grid - 1) {
         for (int i = 0; i < p.B * p.SEL; ++i) p.f_counters[i] = 0;
         p.f_done[0] = 0;
@@ -538,7 +770,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   };
 
   if constexpr (FUSED) {
-    const int n1 = fused_merge(p, reinterpret_cast<uint8_t*>(scratch), cum, f_hist, f_sh_u64,
+    const int n1 = fused_merge(p, reinterpret_cast<uint8_t*>(scratch), f_hist, f_sh_u64,
                                f_sh_int, b, h, ci, ncta, ctid, bar_c);
     if (ctid == 0) {
       bcast[61] = n1;
@@ -752,10 +984,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       dst[p.G * D + p.G + gg] = fm[MAX_G + gg];
     }
   }
-  __threadfence();
   named_bar_sync(1, NCT);
   if (ctid == 0) {
-    const int old = atomicAdd(p.counters + seg, 1);
+    const int old = atom_acq_rel_gpu_add(p.counters + seg, 1);
     bcast[60] = (old + 1 == ncta) ? 1 : 0;
   }
   named_bar_sync(1, NCT);
@@ -763,7 +994,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     finish();
     return;
   }
-  __threadfence();
 
   // ---- last CTA of the segment: merge partials of CTAs f0 .. f0+ncta-1.
   // Each thread owns one float4 chunk of the G x 128 outputs and a share of

@@ -58,8 +58,9 @@ __device__ __forceinline__ int seq_len_checked(const DynParams& p, int b) {
 // One CTA: KV head h of sequence b, blocks j = j_begin, j_begin + stride, ...
 __global__ void __launch_bounds__(THREADS, 1) dyn_pass_kernel(const __grid_constant__ DynParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-byte aligned (128-byte swizzled TMA boxes); offsetting the array
+  // itself keeps the accesses below in the shared address space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(8) uint64_t bars[2];
   __shared__ float colsum[8][BS];
   __shared__ float tscore[BS];

@@ -443,11 +443,10 @@ bool fused_plan(const kt_paged_kv* kv, const kt_sparse_params* p, int sms, int* 
   const int V = nkv * reps_rows(p) * D / (f32 ? 4 : 8);
   if (V > 256) return false;
   const long long nslots = (long long)nc * k;
-  if (nslots > (1 << 20)) return false;
+  if (nslots > FUSED_MAX_SLOTS) return false;
   const int kmax = (int)(p->top_k < nslots ? p->top_k : nslots);
   if (fused_score_layout(nkv * Rw * D, chunk, k).total > ATTN_SCRATCH_BYTES) return false;
-  if (fused_merge_layout((int)nslots, kmax).total > ATTN_SCRATCH_BYTES) return false;
-  if (kmax > MAX_SEGS + 1) return false;  // the CTA's slice of page ids
+  if (fused_merge_layout(nc, k, kmax).total > ATTN_MERGE_BYTES) return false;
   if (attn_fused_max_ctas_per_sm() < 1) return false;
   *ncpu = nc;
   *chunk_out = chunk;

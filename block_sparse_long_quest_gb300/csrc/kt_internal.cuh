@@ -24,6 +24,8 @@ constexpr int MAX_DYN_REPS = 32;
 constexpr int ATTN_SCRATCH_BYTES = 4 * MAX_G * (D + 2) * 4;  // attention kernel scratch (smem)
 constexpr int FUSED_KK_CAP = 256;  // per-CTA candidates of the fused step
 constexpr int ATTN_CONSUMER_THREADS = 256;  // consumer threads of the attention kernel
+constexpr int FUSED_GATHER_PER_THREAD = 8;  // candidate slots a merging thread holds
+constexpr int FUSED_MAX_SLOTS = FUSED_GATHER_PER_THREAD * ATTN_CONSUMER_THREADS;
 
 // Byte offsets inside the attention kernel's scratch for the in-kernel
 // selection of the fused step.  Scoring: weights (fp32), keys and page ids of
@@ -37,25 +39,42 @@ struct FusedScoreLayout {
 __host__ __device__ inline FusedScoreLayout fused_score_layout(int wfl, int chunk, int kk) {
   FusedScoreLayout L;
   L.keys = (wfl * 4 + 15) & ~15;
-  L.pgs = L.keys + chunk * 8;
+  L.pgs = L.keys + ((chunk + 1) & ~1) * 8;  // keys padded to an even count
   L.idx = L.pgs + chunk * 4;
   L.bkey = (L.idx + kk * 4 + 15) & ~15;
   L.bidx = L.bkey + ATTN_CONSUMER_THREADS * 8;
   L.total = chunk > kk ? L.bidx + ATTN_CONSUMER_THREADS * 4 : L.idx;
   return L;
 }
+// Merge: the unit's candidate table (keys, pages), the head sample (the first
+// J keys of every sorted per-CTA list), the keys at or above the sample's k-th
+// largest (at most mcap of them, with their slots), the chosen slots, their
+// block ids and this CTA's share of their page ids.  Lives in the attention
+// kernel's scratch and block-prefix areas, which are contiguous.
 struct FusedMergeLayout {
-  int all, allp, idx, cid, bkey, bidx, total;
+  int all, allp, heads, ck, cs, idx, cid, slice, total, mcap, J, nheads;
 };
-__host__ __device__ inline FusedMergeLayout fused_merge_layout(int nslots, int kmax) {
+constexpr int ATTN_MERGE_BYTES = ATTN_SCRATCH_BYTES + (MAX_SEGS + 1) * 4;
+// ncpu lists of kk candidates each; kmax = min(top_k, ncpu * kk).
+__host__ __device__ inline FusedMergeLayout fused_merge_layout(int ncpu, int kk, int kmax) {
   FusedMergeLayout L;
+  const int nslots = ncpu * kk;
+  L.J = (kmax + ncpu - 1) / ncpu;  // head keys per list: ncpu * J >= kmax
+  if (L.J > kk) L.J = kk;
+  const int nheads = ncpu * L.J;
+  L.nheads = nheads;
+  L.mcap = nslots < 512 ? nslots : 512;
+  if (L.mcap < ATTN_CONSUMER_THREADS) L.mcap = ATTN_CONSUMER_THREADS;  // select_top temporaries
+  L.mcap = (L.mcap + 1) & ~1;
   L.all = 0;
   L.allp = nslots * 8;
-  L.idx = L.allp + nslots * 4;
+  L.heads = (L.allp + nslots * 4 + 15) & ~15;
+  L.ck = (L.heads + ((nheads + 1) & ~1) * 8 + 15) & ~15;
+  L.cs = L.ck + L.mcap * 8;
+  L.idx = (L.cs + L.mcap * 4 + 15) & ~15;
   L.cid = (L.idx + kmax * 4 + 15) & ~15;
-  L.bkey = (L.cid + ((kmax + 3) & ~3) * 4 + 15) & ~15;
-  L.bidx = L.bkey + ATTN_CONSUMER_THREADS * 8;
-  L.total = L.bidx + ATTN_CONSUMER_THREADS * 4;
+  L.slice = (L.cid + ((kmax + 3) & ~3) * 4 + 15) & ~15;
+  L.total = L.slice + kmax * 4;
   return L;
 }
 constexpr uint64_t WAIT_LIMIT_NS = 100000000ull;  // 100 ms bound on any device-side wait
@@ -181,6 +200,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
   }
 }
 
+// mbar_wait for long waits: sleeps between polls so the waiting warp leaves
+// the shared-memory pipe to the warps doing the work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, int* status,
+                                                unsigned int sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0 && globaltimer() - t0 > WAIT_LIMIT_NS) {
+      set_status(status, KT_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -252,6 +287,21 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// Ticket counters.  The CTA's writes are ordered before a ticket by a CTA
+// barrier followed by one thread's release (release is cumulative over what
+// the barrier made visible to that thread); the thread that takes the last
+// ticket acquires, and a CTA barrier then orders the other threads' reads.
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int atom_acq_rel_gpu_add(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
 }
 
 __device__ __forceinline__ void griddep_wait() {

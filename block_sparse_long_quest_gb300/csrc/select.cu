@@ -217,15 +217,13 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
     }
 
   // ---- ticket: the last chunk CTA of this unit merges
-  __threadfence();
   __syncthreads();
   if (tid == 0) {
-    const int old = atomicAdd(p.counters + unit_base, 1);
+    const int old = atom_acq_rel_gpu_add(p.counters + unit_base, 1);
     sh_int[3] = (old == p.nchunks - 1) ? 1 : 0;
   }
   __syncthreads();
   if (!sh_int[3]) return;
-  __threadfence();
 
   // gather every candidate slot of the unit into shared memory (independent,
   // coalesced loads); empty slots are key 0

@@ -53,10 +53,12 @@ __device__ void radix_select(const unsigned long long* keys, int N, int k, unsig
   const int lane = tid & 31, warp = tid >> 5;
   // common leading bits: AND and OR over all keys; clear both histograms
   unsigned long long a = ~0ull, o = 0ull;
+#pragma unroll 1
   for (int i = tid; i < N; i += NT) {
     a &= keys[i];
     o |= keys[i];
   }
+#pragma unroll 1
   for (int i = tid; i < 512; i += NT) hist[i] = 0u;
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) {
@@ -82,11 +84,13 @@ __device__ void radix_select(const unsigned long long* keys, int N, int k, unsig
   unsigned long long mask = (hi >= 64) ? 0ull : ~((1ull << hi) - 1);
   unsigned long long prefix = all_and & mask;
   int need = k;
+#pragma unroll 1
   for (int pass = 0; hi > 0; ++pass) {
     const int shift = hi > 8 ? hi - 8 : 0;
     const unsigned long long dmask = (1ull << (hi - shift)) - 1;
     unsigned int* H = hist + 256 * (pass & 1);
     unsigned int* Hn = hist + 256 * ((pass + 1) & 1);
+#pragma unroll 1
     for (int base = 0; base < N; base += NT) {
       // equal digits are counted once per warp: keys are often clustered
       const int i = base + tid;
@@ -138,6 +142,7 @@ __device__ void radix_select(const unsigned long long* keys, int N, int k, unsig
         sh_int[1] = (bin == (unsigned)need2) ? 1 : 0;
       }
     } else {
+#pragma unroll 1
       for (int i = tid - 32; i < 256; i += NT - 32) Hn[i] = 0u;  // next pass's bins
     }
     bar();
@@ -171,10 +176,12 @@ __device__ void select_top(const unsigned long long* keys, int N, int k, int* id
     return;
   }
   unsigned long long a = ~0ull, o = 0ull;
+#pragma unroll 1
   for (int i = tid; i < N; i += NT) {
     a &= keys[i];
     o |= keys[i];
   }
+#pragma unroll 1
   for (int i = tid; i < 512; i += NT) hist[i] = 0u;
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) {
@@ -202,11 +209,13 @@ __device__ void select_top(const unsigned long long* keys, int N, int k, int* id
   unsigned long long mask = (hi >= 64) ? 0ull : ~((1ull << hi) - 1);
   unsigned long long prefix = all_and & mask;
   int need = k;
+#pragma unroll 1
   for (int pass = 0; hi > 0; ++pass) {
     const int shift = hi > 8 ? hi - 8 : 0;
     const unsigned long long dmask = (1ull << (hi - shift)) - 1;
     unsigned int* H = hist + 256 * (pass & 1);
     unsigned int* Hn = hist + 256 * ((pass + 1) & 1);
+#pragma unroll 1
     for (int base = 0; base < N; base += NT) {
       const int i = base + tid;
       unsigned int bin = 256u;
@@ -255,6 +264,7 @@ __device__ void select_top(const unsigned long long* keys, int N, int k, int* id
         sh_int[1] = (inbin <= (unsigned)NT || shift == 0) ? 1 : 0;
       }
     } else {
+#pragma unroll 1
       for (int i = tid - 32; i < 256; i += NT - 32) Hn[i] = 0u;
     }
     bar();
@@ -266,6 +276,7 @@ __device__ void select_top(const unsigned long long* keys, int N, int k, int* id
   }
   // keys above the boundary bin are chosen; the bin's keys go to bkey/bidx
   const unsigned int lt = (1u << lane) - 1u;
+#pragma unroll 1
   for (int base = 0; base < N; base += NT) {
     const int i = base + tid;
     unsigned long long key = 0ull, m = 0ull;
@@ -297,6 +308,7 @@ __device__ void select_top(const unsigned long long* keys, int N, int k, int* id
   if (tid < nb) {
     const unsigned long long key = bkey[tid];
     int r = 0;
+#pragma unroll 4
     for (int s = 0; s < nb; ++s) r += bkey[s] > key ? 1 : 0;
     if (r < need && taken + r < k) idx_out[taken + r] = bidx[tid];
   }
@@ -330,6 +342,7 @@ __device__ __forceinline__ void score_linear(const void* reps, int P, int H_kv, 
     }
   }
   const size_t head_bytes = (size_t)R * D * (F32 ? 4 : 2);
+#pragma unroll 1
   for (int j0 = js + warp * GB; j0 < je; j0 += WARPS * GB) {
     uint4 x[GB][NV];
     int page[GB];
