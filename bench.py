@@ -3,8 +3,10 @@
 
 One step = kt_sparse_decode_step on one layer: score every Context block
 against its representatives, select the top-k, and attend over Initial +
-selected + Local blocks (selection and attention kernels, the attention launched
-as a programmatic dependent of the selection).
+selected + Local blocks.  For the benchmarked shapes this is one cooperative
+launch of the attention kernel with the selection inside it
+(kt_sparse_decode_step_kernels reports the launches per step); the two-kernel
+path (selection, then attention) is timed beside it.
 
 Default workload: the InternLM2.5-7B-1M-shaped 128K layer (32 query heads, 8 KV
 heads, head_dim 128, 131072 fp16 tokens in 128-token blocks, Initial 128,
@@ -218,21 +220,34 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-# DRAM traffic per attn_kernel launch (dram__bytes_read.sum + dram__bytes_write.sum)
-# from one ncu capture of the 128K workload, valid only for the source it was
-# taken from (profiles/attn_kernel_128k.md).
-ATTN_TRAFFIC = {"bytes": 34159104 + 23552,
-                "source_sha256": "f105066e291adda668e8a619f9a009be2c1269ba78aefdf0d01ec386c9253950"}
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# one ncu capture of the 128K workload, per kernel, valid only for the kernel
+# sources it was taken from (sha256 over KERNEL_SOURCES); null otherwise.
+KERNEL_SOURCES = ("attn.cu", "select_common.cuh", "kt_internal.cuh")
+KERNEL_TRAFFIC = {
+    "attn_kernel<fused step>": {
+        "bytes": 38291712 + 35584,
+        "sources_sha256": "f1e4dc221d0ef574eadcf83e2282b420ea7fba210f363d46a75be494c770f7a7"},
+}
 
 
-def attn_traffic():
+def kernel_sources_sha():
     import hashlib
-    path = os.path.join(ROOT, "block_sparse_long_quest_gb300", "csrc", "attn.cu")
-    try:
-        sha = hashlib.sha256(open(path, "rb").read()).hexdigest()
-    except OSError:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        path = os.path.join(ROOT, "block_sparse_long_quest_gb300", "csrc", name)
+        try:
+            h.update(open(path, "rb").read())
+        except OSError:
+            return None
+    return h.hexdigest()
+
+
+def kernel_traffic(kernel):
+    rec = KERNEL_TRAFFIC.get(kernel)
+    if rec is None:
         return None
-    return ATTN_TRAFFIC["bytes"] if sha == ATTN_TRAFFIC["source_sha256"] else None
+    return rec["bytes"] if kernel_sources_sha() == rec["sources_sha256"] else None
 
 
 def measured_peak():
@@ -409,16 +424,24 @@ def main():
         raise RuntimeError("timed region recorded no work")
     value = world * bytes_step["total"] * args.steps / t_step / 1e9
 
-    # ---- per-kernel device time (roofline of the dominant kernel: attention)
+    # ---- per-kernel device time.  With one launch per step the step kernel is
+    # the dominant (only) kernel: its algorithmic bytes are the reps it scores
+    # plus the KV it attends, its duration the event-timed step above.  The
+    # two-kernel path (selection, then attention) is timed beside it.
+    v0 = layers[0].variants[rep]
+    launches = kt.kt_sparse_decode_step_kernels(layers[0].kv, v0["params"])
     n_k = min(args.steps, 20000)
     t_attn = graph_time([lambda L=L: L.attend(rep) for L in layers], n_k, args.warmup, stream)
     t_sel = graph_time([lambda L=L: L.select(rep) for L in layers], n_k, args.warmup, stream)
     attn_us, sel_us = t_attn / n_k * 1e6, t_sel / n_k * 1e6
     peak, peak_kind = measured_peak()
-    attn_gbs = bytes_step["kv"] / (t_attn / n_k) / 1e9
+    if launches == 1:
+        roof_kernel, roof_bytes, roof_us = "attn_kernel<fused step>", bytes_step["total"], per_step * 1e6
+    else:
+        roof_kernel, roof_bytes, roof_us = "attn_kernel", bytes_step["kv"], attn_us
+    roof_gbs = roof_bytes / (roof_us * 1e-6) / 1e9
 
     # ---- end to end through the host-buffer entry point
-    v0 = layers[0].variants[rep]
     q_host = torch.empty_like(layers[0].q, device="cpu").pin_memory()
     out_host = torch.empty_like(v0["out"], device="cpu").pin_memory()
     q_host.copy_(layers[0].q.cpu())
@@ -500,16 +523,18 @@ def main():
                          f"{n_layers * bytes_step['total'] / 1e6:.0f} MB vs L2 "
                          f"{l2_bytes / 1e6:.0f} MB",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "attn_kernel", "achieved": attn_gbs,
+        "roofline": {"bound": "hbm", "kernel": roof_kernel, "achieved": roof_gbs,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": attn_gbs / peak, "traffic": attn_traffic(),
-                     "algorithmic_bytes_per_launch": bytes_step["kv"],
-                     "us_per_launch": attn_us},
-        "kernels_us": {"select_kernel": sel_us, "attn_kernel": attn_us},
+                     "frac": roof_gbs / peak, "traffic": kernel_traffic(roof_kernel),
+                     "algorithmic_bytes_per_launch": roof_bytes,
+                     "us_per_launch": roof_us},
+        "kernels_us": {roof_kernel: roof_us,
+                       "two_kernel_path": {"select_kernel": sel_us, "attn_kernel": attn_us}},
+        "launches_per_step": launches,
         "e2e": {"value": e2e_value, "unit": "GB/s", "us_per_step": t_e2e / n_e2e * 1e6,
                 "steps": n_e2e, "h2d_bytes_per_step": int(layers_q_bytes(w0)),
                 "d2h_bytes_per_step": int(w0.batch * w0.params.num_q_heads * D * 4)},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clocks.summary(),
         **extra,
     }

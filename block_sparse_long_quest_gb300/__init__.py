@@ -31,7 +31,7 @@ EXPORTS = (
     "kt_workspace_init", "kt_build_block_reps", "kt_build_dynamic_reps",
     "kt_score_select_blocks", "kt_sparse_decode_attn", "kt_sparse_decode_step",
     "kt_sparse_decode_step_host", "kt_dense_decode_attn", "kt_read_device_status",
-    "kt_selftest_bounded_wait", "kt_sparse_decode_attn_noalloc",
+    "kt_selftest_bounded_wait", "kt_sparse_decode_attn_noalloc", "kt_sparse_decode_step_kernels",
 )
 
 
@@ -81,6 +81,7 @@ def _load():
                                                  vp, sz, vp]),
         "kt_sparse_decode_step": (ctypes.c_int, [vp, P(PagedKV), vp, P(SparseParams), vp, vp,
                                                  vp, vp, sz, vp]),
+        "kt_sparse_decode_step_kernels": (i32, [P(PagedKV), P(SparseParams)]),
         "kt_sparse_decode_step_host": (ctypes.c_int, [vp, vp, P(PagedKV), vp, P(SparseParams),
                                                       vp, vp, vp, vp, vp, sz, vp]),
         "kt_dense_decode_attn": (ctypes.c_int, [vp, P(PagedKV), i32, ctypes.c_float, vp, vp, sz,
@@ -199,6 +200,15 @@ def kt_sparse_decode_step(q, kv, reps_pool, params, sel, cnt, out, ws, stream=No
                                      ctypes.byref(params), _ptr(sel), _ptr(cnt), _ptr(out),
                                      _ptr(ws), ws.numel(), _stream(stream)),
            "kt_sparse_decode_step")
+
+
+def kt_sparse_decode_step_kernels(kv, params):
+    """Launches per kt_sparse_decode_step for this shape: 1 (one cooperative
+    launch) or 2 (selection + attention)."""
+    n = lib.kt_sparse_decode_step_kernels(ctypes.byref(kv), ctypes.byref(params))
+    if n < 0:
+        raise KtError(-n, "kt_sparse_decode_step_kernels")
+    return n
 
 
 def kt_sparse_decode_step_host(q_host, q_dev, kv, reps_pool, params, sel, cnt, out_dev,

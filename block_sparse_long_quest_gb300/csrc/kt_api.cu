@@ -457,6 +457,16 @@ bool fused_plan(const kt_paged_kv* kv, const kt_sparse_params* p, int sms, int* 
 }  // namespace
 }  // namespace kt
 
+int32_t kt_sparse_decode_step_kernels(const kt_paged_kv* kv, const kt_sparse_params* p) {
+  kt_status s = check_kv(kv);
+  if (s != KT_OK) return -(int32_t)s;
+  s = check_params(kv, p);
+  if (s != KT_OK) return -(int32_t)s;
+  const int sms = num_sms();
+  int ncpu = 0, chunk = 0, kk = 0;
+  return (sms > 0 && fused_plan(kv, p, sms, &ncpu, &chunk, &kk)) ? 1 : 2;
+}
+
 kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void* reps_pool,
                                 const kt_sparse_params* p, int32_t* sel, int32_t* cnt,
                                 float* out, void* ws, size_t ws_bytes, kt_stream_t stream) {

@@ -228,13 +228,28 @@ kt_status kt_sparse_decode_attn(const void* q, const kt_paged_kv* kv, const kt_s
                                 size_t ws_bytes, kt_stream_t stream);
 
 /*
- * One decode step: kt_score_select_blocks then kt_sparse_decode_attn, the
- * attention launched as a programmatic dependent of the selection so that the
- * Initial/Local blocks stream while selection runs.  Workspace: KT_OP_SPARSE_STEP.
+ * One decode step: the selection of kt_score_select_blocks and the attention
+ * of kt_sparse_decode_attn, with the same sel / cnt / out.
+ * When the shape allows it (linear reps Max/Mean/Quest; at most one
+ * (sequence, KV head) segment and one selection unit per SM; the per-CTA
+ * selection buffers fit shared memory) the step is ONE cooperative launch:
+ * every CTA streams its Initial/Local blocks while its consumer warps score a
+ * slice of one unit's Context blocks, and each CTA merges its unit's
+ * candidates itself before loading its share of the selected blocks.
+ * Otherwise two launches: selection, then the attention as its programmatic
+ * dependent.  kt_sparse_decode_step_kernels tells which.  Concurrent steps
+ * need separate workspaces.  Workspace: KT_OP_SPARSE_STEP.
  */
 kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void* reps_pool,
                                 const kt_sparse_params* p, int32_t* sel, int32_t* cnt,
                                 float* out, void* ws, size_t ws_bytes, kt_stream_t stream);
+
+/*
+ * Kernel launches one kt_sparse_decode_step makes for this shape on the
+ * current device: 1 (one cooperative launch) or 2 (selection + attention);
+ * a negative kt_status value for invalid arguments.  Host only, no launch.
+ */
+int32_t kt_sparse_decode_step_kernels(const kt_paged_kv* kv, const kt_sparse_params* p);
 
 /*
  * The same step for callers whose query and output live in HOST memory:

@@ -95,6 +95,15 @@ def test_invalid_arguments(k, p, status):
     st = kt.lib.kt_sparse_decode_step(FAKE, ctypes.byref(k), FAKE, ctypes.byref(p), FAKE, FAKE,
                                       FAKE, FAKE, 1 << 30, None)
     assert st == status
+    assert kt.lib.kt_sparse_decode_step_kernels(ctypes.byref(k), ctypes.byref(p)) == -status
+
+
+def test_step_kernel_count_is_one_or_two():
+    # 1 needs a device with enough SMs; without one the two-kernel plan stands
+    n = kt.kt_sparse_decode_step_kernels(kv(), params())
+    assert n in (1, 2)
+    with pytest.raises(kt.KtError):
+        kt.kt_sparse_decode_step_kernels(kv(batch=0), params())
 
 
 def test_calls_reject_null_and_small_workspace_without_a_device():

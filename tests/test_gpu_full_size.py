@@ -65,9 +65,11 @@ def _check_step(w, dw, units):
 
 
 def test_128k_shared_quest_full_size():
+    import block_sparse_long_quest_gb300 as kt
     w = synth.long128k()
     dw = DevWorkload(w)
     dw.build_reps()
+    assert kt.kt_sparse_decode_step_kernels(dw.kv, dw.params) == 1
     _check_step(w, dw, (0, 1))
 
 

@@ -224,11 +224,13 @@ def test_one_workspace_serves_every_call():
 
 def test_more_segments_than_sms_and_empty_sequence():
     # 45 sequences x 4 KV heads = 180 segments (more than the SM count), one empty
+    import block_sparse_long_quest_gb300 as kt
     lens = [0] + [128 * (3 + (i * 7) % 11) + (i * 37) % 128 for i in range(44)]
     w = synth.custom(32, lens, num_q_heads=8, num_kv_heads=4, top_k=3,
                      head_mode=synth.HEAD_SEPARATE)
     dw = DevWorkload(w)
     dw.build_reps()
+    assert kt.kt_sparse_decode_step_kernels(dw.kv, dw.params) == 2  # two-kernel path
     sel, cnt, out, ws = dw.step()
     dense, _ = dw.dense()
     ref = _oracle(w)
@@ -255,6 +257,7 @@ def test_step_after_query_change_uses_the_new_selection():
                      head_mode=synth.HEAD_SEPARATE, top_k=4, num_needles=3)
     dw = DevWorkload(w)
     dw.build_reps()
+    assert kt.kt_sparse_decode_step_kernels(dw.kv, dw.params) == 1  # one-launch path
     ws = kt.workspace(kt.KT_OP_SPARSE_STEP, dw.kv, dw.params)
     q_first = w.q.copy()
     for it in range(6):
