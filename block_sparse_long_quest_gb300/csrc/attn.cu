@@ -60,7 +60,7 @@ struct SmemLayout {
   static constexpr int cum = scratch + SCRATCH_FLOATS * 4;  // [MAX_SEGS+1] work prefix
   static constexpr int info = cum + (MAX_SEGS + 1) * 4;
   static constexpr int bars = (info + STAGES * (int)sizeof(StageInfo) + 15) & ~15;
-  static constexpr int bcast = bars + (2 * STAGES + 2) * 8;
+  static constexpr int bcast = bars + (2 * STAGES + 3) * 8;
   static constexpr int total = bcast + 64 * 4;
 };
 constexpr int SMEM_BYTES = SmemLayout::total + 1024;  // + alignment slack
@@ -146,29 +146,6 @@ __device__ void warp_prefix(int* pref, int S, F count, int lane) {
   __syncwarp();
 }
 
-// Number of keys in a[0, n) greater than key; a is 16-byte aligned and n even.
-// Eight loads in flight per iteration.
-__device__ __forceinline__ int count_greater(const unsigned long long* a, int n,
-                                             unsigned long long key) {
-  int r0 = 0, r1 = 0;
-  int m = 0;
-#pragma unroll 1
-  for (; m + 8 <= n; m += 8) {
-    const ulonglong2 v0 = *reinterpret_cast<const ulonglong2*>(a + m);
-    const ulonglong2 v1 = *reinterpret_cast<const ulonglong2*>(a + m + 2);
-    const ulonglong2 v2 = *reinterpret_cast<const ulonglong2*>(a + m + 4);
-    const ulonglong2 v3 = *reinterpret_cast<const ulonglong2*>(a + m + 6);
-    r0 += (v0.x > key ? 1 : 0) + (v0.y > key ? 1 : 0) + (v1.x > key ? 1 : 0) + (v1.y > key ? 1 : 0);
-    r1 += (v2.x > key ? 1 : 0) + (v2.y > key ? 1 : 0) + (v3.x > key ? 1 : 0) + (v3.y > key ? 1 : 0);
-  }
-#pragma unroll 1
-  for (; m < n; m += 2) {
-    const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(a + m);
-    r0 += (v.x > key ? 1 : 0) + (v.y > key ? 1 : 0);
-  }
-  return r0 + r1;
-}
-
 // Number of ids in a[0, n) smaller than id; a is 16-byte aligned, n a multiple of 4.
 __device__ __forceinline__ int count_less_u32(const uint32_t* a, int n, uint32_t id) {
   int r0 = 0, r1 = 0;
@@ -246,15 +223,19 @@ __device__ __forceinline__ void fused_weights(const Params& p, float* wts, int b
 // Context blocks I_b + s*f_chunk ...) of selection unit c / ncpu with the same
 // weights, dot products and keys as the selection kernel, keep the slice's best
 // kk_f (key 0 = empty slot) in the unit's candidate table and take a ticket.
+// Arrives on bar_scored once its representative loads are done (every CTA).
 // The block-table entries of the nominal slice do not depend on the sequence
 // length, so they load together with the length and the query rows.
 template <class Bar>
 __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
                             unsigned long long* sh_u64, int* sh_int, int ctid, int warp, int lane,
-                            Bar bar_c) {
+                            Bar bar_c, uint32_t bar_scored) {
   const int U = p.B * p.SEL;
   const int u = blockIdx.x / p.ncpu;
-  if (u >= U) return;
+  if (u >= U) {
+    if (ctid == 0) mbar_arrive(bar_scored);
+    return;
+  }
   const int cs = blockIdx.x % p.ncpu;
   const int bu = u / p.SEL, g0 = p.SEL == 1 ? 0 : u % p.SEL;
   const int nkv = p.SEL == 1 ? p.H_kv : 1;
@@ -278,7 +259,7 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
   bar_c();
   if (nloc > 0) {
     const int V = nkv * p.R * D / (f32 ? 4 : 8);
-#define KT_SCORE(NV, F) selc::score_linear<NV, F, CONSUMERS>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status)
+#define KT_SCORE(NV, F) selc::score_linear<NV, F, CONSUMERS, true>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status)
     if (f32) {
       if (V <= 32) KT_SCORE(1, true);
       else if (V <= 64) KT_SCORE(2, true);
@@ -293,38 +274,35 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
 #undef KT_SCORE
     bar_c();
   }
+  if (ctid == 0) mbar_arrive(bar_scored);  // the producer may start its own loads
   // the slice's best min(nloc, kk_f) keys, written in descending key order
   // (empty slots: key 0, page -1), then the ticket
   const int nk = min(nloc, p.kk_f);
-  const unsigned long long* ck = keys;
-  const int* cp = pgs;
-  if (nloc > p.kk_f) {
-    int* idx = reinterpret_cast<int*>(scr + Ls.idx);
-    unsigned long long* bkey = reinterpret_cast<unsigned long long*>(scr + Ls.bkey);
-    int* bidx = reinterpret_cast<int*>(scr + Ls.bidx);
-    selc::select_top<NCT>(keys, nloc, p.kk_f, idx, bkey, bidx, hist, sh_u64, sh_int, ctid, bar_c);
-#pragma unroll 1
-    for (int i = ctid; i < p.kk_f; i += NCT) {  // chosen keys, contiguous
-      bkey[i] = keys[idx[i]];
-      bidx[i] = pgs[idx[i]];
-    }
-    ck = bkey;
-    cp = bidx;
-  }
-  if (ctid == 0 && (nk & 1)) const_cast<unsigned long long*>(ck)[nk] = 0ull;
-  bar_c();
   unsigned long long* cand = p.f_cand + ((size_t)u * p.ncpu + cs) * p.kk_f;
   int* cpage = p.f_cand_pages + ((size_t)u * p.ncpu + cs) * p.kk_f;
+  if (nloc > p.kk_f) {
+    selc::topk_sorted<NCT>(keys, nloc, p.kk_f,
+                           reinterpret_cast<unsigned long long*>(scr + Ls.bkey),
+                           reinterpret_cast<int*>(scr + Ls.bidx),
+                           reinterpret_cast<int*>(scr + Ls.idx), hist, sh_u64, sh_int, ctid,
+                           bar_c, [&](int r, int i) {
+                             cand[r] = keys[i];
+                             cpage[r] = pgs[i];
+                           });
+  } else {
+    if (ctid == 0 && (nk & 1)) keys[nk] = 0ull;
+    bar_c();
 #pragma unroll 1
-  for (int i = ctid; i < p.kk_f; i += NCT) {
-    if (i < nk) {
-      const unsigned long long key = ck[i];
-      const int r = count_greater(ck, (nk + 1) & ~1, key);
-      cand[r] = key;
-      cpage[r] = cp[i];
-    } else {
-      cand[i] = 0ull;
-      cpage[i] = -1;
+    for (int i = ctid; i < p.kk_f; i += NCT) {
+      if (i < nk) {
+        const unsigned long long key = keys[i];
+        const int r = selc::count_greater(keys, (nk + 1) & ~1, key);
+        cand[r] = key;
+        cpage[r] = pgs[i];
+      } else {
+        cand[i] = 0ull;
+        cpage[i] = -1;
+      }
     }
   }
   bar_c();
@@ -531,7 +509,7 @@ __device__ int fused_merge(const Params& p, uint8_t* scr, unsigned int* hist,
 #pragma unroll 1
     for (int i = ctid; i < M; i += NCT) {
       const unsigned long long key = ckey[i];
-      const int r = count_greater(ckey, (M + 1) & ~1, key);
+      const int r = selc::count_greater(ckey, (M + 1) & ~1, key);
       if (r < keff) {
         idx[r] = cslot[i];
         cid[r] = 0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFull);
@@ -580,9 +558,21 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   const uint32_t bar_full = smem_u32(smem + SmemLayout::bars);
   const uint32_t bar_empty = bar_full + STAGES * 8;
   const uint32_t bar_q = bar_empty + STAGES * 8;
-  const uint32_t bar_sel = bar_q + 8;  // fused: this CTA's selected pages are ready
+  const uint32_t bar_sel = bar_q + 8;      // fused: this CTA's selected pages are ready
+  const uint32_t bar_scored = bar_sel + 8;  // fused: this CTA's scoring loads are done
   const uint32_t kv_base = smem_u32(smem + SmemLayout::kv);
   auto bar_c = [] { named_bar_sync(1, NCT); };
+  if (tid == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(bar_full + 8 * i, 1);
+      mbar_init(bar_empty + 8 * i, CONSUMERS);
+    }
+    mbar_init(bar_q, 1);
+    mbar_init(bar_sel, 1);
+    mbar_init(bar_scored, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
 
   // ---- set-up: segment work prefix -> this CTA's segment and slice.  In the
   // fused step the consumer warps score their selection slice meanwhile.
@@ -600,19 +590,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     const long long extra = grid - S, W = cum[S];
     __syncwarp();
     for (int s = lane; s <= S; s += 32) cum[s] = s + (int)(extra * cum[s] / W);
-    if (lane == 0) {
-      for (int i = 0; i < STAGES; ++i) {
-        mbar_init(bar_full + 8 * i, 1);
-        mbar_init(bar_empty + 8 * i, CONSUMERS);
-      }
-      mbar_init(bar_q, 1);
-      mbar_init(bar_sel, 1);
-      fence_mbar_init();
-    }
     __syncwarp();
   } else if (FUSED) {
     fused_score(p, reinterpret_cast<uint8_t*>(scratch), f_hist, f_sh_u64, f_sh_int, tid, warp,
-                lane, bar_c);
+                lane, bar_c, bar_scored);
   }
   if (!FUSED) __syncthreads();
   else if (warp != CONSUMERS) named_bar_sync(2, THREADS);
@@ -719,6 +700,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         }
       }
     };
+    // fused: the scoring loads go first; the Initial/Local blocks are needed
+    // only after the selection
+    if (FUSED && lane == 0) mbar_wait_sleep(bar_scored, 0, p.status, 64);
+    __syncwarp();
     produce(0, a0, a1);
     if (FUSED) {
       // phase B: this CTA's share of the selected blocks, handed over by the

@@ -36,6 +36,29 @@ __device__ __forceinline__ unsigned long long make_key(float score, int block) {
          static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(block));
 }
 
+// Number of keys in a[0, n) greater than key; a is 16-byte aligned and n even.
+// Eight loads in flight per iteration.
+__device__ __forceinline__ int count_greater(const unsigned long long* a, int n,
+                                             unsigned long long key) {
+  int r0 = 0, r1 = 0;
+  int m = 0;
+#pragma unroll 1
+  for (; m + 8 <= n; m += 8) {
+    const ulonglong2 v0 = *reinterpret_cast<const ulonglong2*>(a + m);
+    const ulonglong2 v1 = *reinterpret_cast<const ulonglong2*>(a + m + 2);
+    const ulonglong2 v2 = *reinterpret_cast<const ulonglong2*>(a + m + 4);
+    const ulonglong2 v3 = *reinterpret_cast<const ulonglong2*>(a + m + 6);
+    r0 += (v0.x > key ? 1 : 0) + (v0.y > key ? 1 : 0) + (v1.x > key ? 1 : 0) + (v1.y > key ? 1 : 0);
+    r1 += (v2.x > key ? 1 : 0) + (v2.y > key ? 1 : 0) + (v3.x > key ? 1 : 0) + (v3.y > key ? 1 : 0);
+  }
+#pragma unroll 1
+  for (; m < n; m += 2) {
+    const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(a + m);
+    r0 += (v.x > key ? 1 : 0) + (v.y > key ? 1 : 0);
+  }
+  return r0 + r1;
+}
+
 // k-th largest of N distinct keys in shared memory (1 <= k <= N), all threads
 // of the CTA.  On return, a key is among the k largest iff
 // (key & *mask_out) >= *prefix_out.  MSB-first radix select on 8-bit digits;
@@ -315,12 +338,132 @@ __device__ void select_top(const unsigned long long* keys, int N, int k, int* id
   bar();
 }
 
+// The k largest of N distinct keys in shared memory (1 <= k < N, k <= NT),
+// emitted in descending order as emit(rank, index).  One 8-bit digit
+// histogram (just below the keys' common leading bits) finds the bin of the
+// k-th largest key; the keys from that bin up are ranked exactly by counting.
+// When more than NT keys reach that bin, select_top narrows first (k <= NT).
+// Scratch: hist 256 bins; ck (16-byte aligned) / ci NT entries; idx k
+// entries; sh_u64 2 + 2*NT/32; sh_int 4.  All NT threads call it.
+template <int NT, class Bar, class Emit>
+__device__ void topk_sorted(const unsigned long long* keys, int N, int k,
+                            unsigned long long* ck, int* ci, int* idx, unsigned int* hist,
+                            unsigned long long* sh_u64, int* sh_int, int tid, Bar bar,
+                            Emit emit) {
+  constexpr int WARPS = NT / 32;
+  const int lane = tid & 31, warp = tid >> 5;
+  unsigned long long a = ~0ull, o = 0ull;
+#pragma unroll 1
+  for (int i = tid; i < N; i += NT) {
+    a &= keys[i];
+    o |= keys[i];
+  }
+#pragma unroll 1
+  for (int i = tid; i < 256; i += NT) hist[i] = 0u;
+#pragma unroll 1
+  for (int i = tid; i < NT; i += NT) ck[i] = 0ull;
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    a &= __shfl_xor_sync(0xffffffffu, a, d);
+    o |= __shfl_xor_sync(0xffffffffu, o, d);
+  }
+  if (lane == 0) {
+    sh_u64[2 + warp] = a;
+    sh_u64[2 + WARPS + warp] = o;
+  }
+  if (tid == 0) sh_int[0] = 0;
+  bar();
+  unsigned long long all_and = ~0ull, all_or = 0ull;
+#pragma unroll
+  for (int w = 0; w < WARPS; ++w) {
+    all_and &= sh_u64[2 + w];
+    all_or |= sh_u64[2 + WARPS + w];
+  }
+  const unsigned long long diff = all_and ^ all_or;
+  const int hi = diff ? 64 - __clzll((long long)diff) : 0;
+  const int shift = hi > 8 ? hi - 8 : 0;
+  const unsigned long long pmask = hi >= 64 ? 0ull : ~((1ull << hi) - 1);
+  const unsigned long long prefix = all_and & pmask;
+#pragma unroll 1
+  for (int base = 0; base < N; base += NT) {
+    const int i = base + tid;
+    unsigned int bin = 256u;
+    if (i < N) bin = (unsigned)((keys[i] >> shift) & 255ull);
+    const unsigned int peers = __match_any_sync(0xffffffffu, bin);
+    if (bin < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (unsigned)__popc(peers));
+  }
+  bar();
+  if (warp == 0) {
+    unsigned int c[8], local = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      c[i] = hist[255 - 8 * lane - i];
+      local += c[i];
+    }
+    unsigned int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const unsigned int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    const unsigned int excl = incl - local;
+    if (excl < (unsigned)k && (unsigned)k <= incl) {
+      unsigned int above = excl;
+      int digit = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        above += c[i];
+        if (above >= (unsigned)k) {
+          digit = 255 - 8 * lane - i;
+          break;
+        }
+      }
+      sh_u64[0] = prefix | (static_cast<unsigned long long>(digit) << shift);
+    }
+  }
+  bar();
+  const unsigned long long T = sh_u64[0];
+  {
+    const unsigned int lt = (1u << lane) - 1u;
+#pragma unroll 1
+    for (int base = 0; base < N; base += NT) {
+      const int i = base + tid;
+      const bool take = i < N && keys[i] >= T;
+      const unsigned int bal = __ballot_sync(0xffffffffu, take);
+      int off = 0;
+      if (lane == 0 && bal) off = atomicAdd(&sh_int[0], __popc(bal));
+      off = __shfl_sync(0xffffffffu, off, 0) + __popc(bal & lt);
+      if (take && off < NT) {
+        ck[off] = keys[i];
+        ci[off] = i;
+      }
+    }
+  }
+  bar();
+  const int M = sh_int[0];
+  if (M <= NT) {
+#pragma unroll 1
+    for (int i = tid; i < M; i += NT) {
+      const int r = count_greater(ck, (M + 1) & ~1, ck[i]);
+      if (r < k) emit(r, ci[i]);
+    }
+  } else {
+    select_top<NT>(keys, N, k, idx, ck, ci, hist, sh_u64, sh_int, tid, bar);
+#pragma unroll 1
+    for (int i = tid; i < NT; i += NT) ck[i] = i < k ? keys[idx[i]] : 0ull;
+    bar();
+#pragma unroll 1
+    for (int i = tid; i < k; i += NT) emit(count_greater(ck, (k + 1) & ~1, ck[i]), idx[i]);
+  }
+  bar();
+}
+
 // Linear scoring (Max, Mean, Quest): each warp scores 8/NV blocks at a time;
 // a lane holds NV 16-byte vectors of each block, and every load of the group is
 // issued before any arithmetic.  V = 16-byte vectors per block and unit.
 //
 // reps: the representative pool; R rows of 128 per (page, KV head); P pages.
-template <int NV, bool F32, int WARPS>
+template <int NV, bool F32, int WARPS, bool PIPE = false>
 __device__ __forceinline__ void score_linear(const void* reps, int P, int H_kv, int R, int g0,
                                              int js, int je, const int* pg, const float* wts,
                                              int V, unsigned long long* keys, int warp, int lane,
@@ -342,10 +485,9 @@ __device__ __forceinline__ void score_linear(const void* reps, int P, int H_kv, 
     }
   }
   const size_t head_bytes = (size_t)R * D * (F32 ? 4 : 2);
-#pragma unroll 1
-  for (int j0 = js + warp * GB; j0 < je; j0 += WARPS * GB) {
-    uint4 x[GB][NV];
-    int page[GB];
+  // PIPE: the next group's loads are in flight while the current group is
+  // reduced (twice the registers)
+  auto load = [&](int j0, uint4 (&x)[GB][NV], int (&page)[GB]) {
 #pragma unroll
     for (int bi = 0; bi < GB; ++bi) {
       const int j = j0 + bi;
@@ -360,6 +502,8 @@ __device__ __forceinline__ void score_linear(const void* reps, int P, int H_kv, 
         x[bi][v] = (ok && vec < V) ? __ldg(src + vec) : make_uint4(0u, 0u, 0u, 0u);
       }
     }
+  };
+  auto reduce = [&](int j0, const uint4 (&x)[GB][NV], const int (&page)[GB]) {
 #pragma unroll
     for (int bi = 0; bi < GB; ++bi) {
       float acc = 0.0f;
@@ -382,6 +526,37 @@ __device__ __forceinline__ void score_linear(const void* reps, int P, int H_kv, 
         if (lane == 0) keys[j - js] = make_key(ok ? acc : -INFINITY, j);
         if (!ok && lane == 0) set_status(status, KT_ERR_DEVICE_CHECK);
       }
+    }
+  };
+  if constexpr (PIPE) {
+    int j0 = js + warp * GB;
+    if (j0 >= je) return;
+    uint4 x[GB][NV];
+    int page[GB];
+    load(j0, x, page);
+#pragma unroll 1
+    for (; j0 < je; j0 += WARPS * GB) {
+      uint4 xn[GB][NV];
+      int pn[GB];
+      const int jn = j0 + WARPS * GB;
+      if (jn < je) load(jn, xn, pn);
+      reduce(j0, x, page);
+      if (jn < je) {
+#pragma unroll
+        for (int bi = 0; bi < GB; ++bi) {
+          page[bi] = pn[bi];
+#pragma unroll
+          for (int v = 0; v < NV; ++v) x[bi][v] = xn[bi][v];
+        }
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int j0 = js + warp * GB; j0 < je; j0 += WARPS * GB) {
+      uint4 x[GB][NV];
+      int page[GB];
+      load(j0, x, page);
+      reduce(j0, x, page);
     }
   }
 }
