@@ -60,7 +60,7 @@ struct SmemLayout {
   static constexpr int cum = scratch + SCRATCH_FLOATS * 4;  // [MAX_SEGS+1] work prefix
   static constexpr int info = cum + (MAX_SEGS + 1) * 4;
   static constexpr int bars = (info + STAGES * (int)sizeof(StageInfo) + 15) & ~15;
-  static constexpr int bcast = bars + (2 * STAGES + 3) * 8;
+  static constexpr int bcast = bars + (2 * STAGES + 5) * 8;
   static constexpr int total = bcast + 64 * 4;
 };
 constexpr int SMEM_BYTES = SmemLayout::total + 1024;  // + alignment slack
@@ -89,7 +89,7 @@ struct Params {
   unsigned long long* f_cand;
   int* f_cand_pages;
   int* f_counters;
-  int* f_done;
+  int* f_polled;
   int32_t* sel_out;
   int32_t* cnt_out;
 };
@@ -169,6 +169,24 @@ __device__ __forceinline__ int count_less_u32(const uint32_t* a, int n, uint32_t
   return r0 + r1;
 }
 
+// Fused step: where the scoring CTA stages its slice's representative rows in
+// the KV ring.  When a whole nominal slice fits, it sits at the top of the
+// ring and the stages below it stay free for the Initial/Local blocks;
+// otherwise rounds use the two halves from offset 0.  Also returns the row
+// stride (fp16 rows are padded by 16 bytes for conflict-free ldmatrix).
+__device__ __forceinline__ uint32_t fused_stage_off(const Params& p, uint32_t* stride = nullptr,
+                                                    bool* single = nullptr) {
+  constexpr uint32_t RING = STAGES * KV_STAGE_BYTES;
+  const int nkv = p.SEL == 1 ? p.H_kv : 1;
+  const bool f32 = p.rep == KT_REP_MEAN;
+  const uint32_t bbytes = (uint32_t)(nkv * p.R * D * (f32 ? 4 : 2));
+  const uint32_t sb = f32 ? bbytes : bbytes + 16;
+  const uint64_t need = (uint64_t)p.f_chunk * sb;
+  if (stride) *stride = sb;
+  if (single) *single = need <= RING;
+  return need <= RING ? (uint32_t)(RING - need) : 0u;
+}
+
 // Fused step: the linear weight rows of KV heads g0 .. g0+nkv-1 of sequence bu
 // (query heads summed in ascending order per channel; Quest: the negative and
 // positive parts, paired with the kmin and kmax rows).  Same values as the
@@ -229,7 +247,8 @@ __device__ __forceinline__ void fused_weights(const Params& p, float* wts, int b
 template <class Bar>
 __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
                             unsigned long long* sh_u64, int* sh_int, int ctid, int warp, int lane,
-                            Bar bar_c, uint32_t bar_scored) {
+                            Bar bar_c, uint32_t bar_scored, const uint8_t* ring,
+                            uint32_t ring_u32, uint32_t bar_reps) {
   const int U = p.B * p.SEL;
   const int u = blockIdx.x / p.ncpu;
   if (u >= U) {
@@ -258,21 +277,69 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
   const int nloc = max(0, je - js);  // js >= c0 whenever the slice is not empty
   bar_c();
   if (nloc > 0) {
+    // the slice's representative rows, staged into the (still idle) KV ring by
+    // bulk copies in rounds of up to ring-size bytes, then scored from there
+    // fp16 reps (Max, Quest) are scored on the tensor cores from rows padded
+    // by 16 bytes (conflict-free ldmatrix); fp32 reps (Mean) on the CUDA cores
     const int V = nkv * p.R * D / (f32 ? 4 : 8);
-#define KT_SCORE(NV, F) selc::score_linear<NV, F, CONSUMERS, true>(p.reps, p.P, p.H_kv, p.R, g0, js, je, pgs, wts, V, keys, warp, lane, p.status)
-    if (f32) {
-      if (V <= 32) KT_SCORE(1, true);
-      else if (V <= 64) KT_SCORE(2, true);
-      else if (V <= 128) KT_SCORE(4, true);
-      else KT_SCORE(8, true);
-    } else {
-      if (V <= 32) KT_SCORE(1, false);
-      else if (V <= 64) KT_SCORE(2, false);
-      else if (V <= 128) KT_SCORE(4, false);
-      else KT_SCORE(8, false);
-    }
+    const uint32_t bbytes = (uint32_t)V * 16;  // one block's rows for the unit's heads
+    const uint32_t sb = f32 ? bbytes : bbytes + 16;
+    const size_t head_bytes = (size_t)p.R * D * (f32 ? 4 : 2);
+    // one round when the slice fits the ring, else rounds alternating between
+    // its two halves so that the next round's copies fly while one is scored;
+    // each warp issues its share of a round (its expect-tx, then its copies)
+    constexpr uint32_t RING = STAGES * KV_STAGE_BYTES, HALF = RING / 2;
+    bool single = false;
+    const uint32_t off = fused_stage_off(p, nullptr, &single);
+    const int rcap = single ? nloc : (int)(HALF / sb);
+    const int nrounds = (nloc + rcap - 1) / rcap;
+    auto buf_off = [&](int r) { return single ? off : (uint32_t)(r & 1) * HALF; };
+    auto issue = [&](int r) {
+      const int r0 = r * rcap, nr = min(rcap, nloc - r0);
+      const uint32_t base = ring_u32 + buf_off(r);
+      const uint32_t bar = (r & 1) ? bar_reps + 8 : bar_reps;
+      const int i0 = warp * nr / CONSUMERS, i1 = (warp + 1) * nr / CONSUMERS;
+      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(i1 - i0) * bbytes);
+      __syncwarp();
+#pragma unroll 1
+      for (int i = i0 + lane; i < i1; i += 32) {
+        const int page = pgs[r0 + i];
+        const bool ok = page >= 0 && page < p.P;  // out of range: scored -inf, flagged
+        bulk_load(base + (uint32_t)i * sb,
+                  static_cast<const uint8_t*>(p.reps) +
+                      ((size_t)(ok ? page : 0) * p.H_kv + g0) * head_bytes,
+                  bbytes, bar);
+      }
+    };
+    issue(0);
+    if (nrounds > 1) issue(1);
+#pragma unroll 1
+    for (int r = 0; r < nrounds; ++r) {
+      const int r0 = r * rcap, nr = min(rcap, nloc - r0);
+      mbar_wait((r & 1) ? bar_reps + 8 : bar_reps, (uint32_t)(r >> 1) & 1u, p.status);
+      const uint32_t base = ring_u32 + buf_off(r);
+      const uint4* sbuf = reinterpret_cast<const uint4*>(ring + buf_off(r));
+#define KT_SCORE(NV, F) selc::score_linear_smem<NV, F, CONSUMERS>(sbuf, (int)(sb / 16), nr, js + r0, p.P, pgs + r0, wts, V, keys + r0, warp, lane, p.status)
+      if (f32) {
+        if (V <= 32) KT_SCORE(1, true);
+        else if (V <= 64) KT_SCORE(2, true);
+        else if (V <= 128) KT_SCORE(4, true);
+        else KT_SCORE(8, true);
+      } else if (nr <= 8 * CONSUMERS / (V <= 32 ? 1 : V <= 64 ? 2 : V <= 128 ? 4 : 8)) {
+        // one pass of the CUDA-core path: each warp reduces its few blocks
+        if (V <= 32) KT_SCORE(1, false);
+        else if (V <= 64) KT_SCORE(2, false);
+        else if (V <= 128) KT_SCORE(4, false);
+        else KT_SCORE(8, false);
+      } else {
+        selc::score_mma_smem<CONSUMERS>(base, (int)sb, nr, js + r0, p.P, pgs + r0, wts, V * 8,
+                                        keys + r0, reinterpret_cast<float*>(hist), warp, lane,
+                                        p.status, bar_c);
+      }
 #undef KT_SCORE
-    bar_c();
+      bar_c();  // this half is refilled by round r + 2, the ring by the producer
+      if (r + 2 < nrounds) issue(r + 2);
+    }
   }
   if (ctid == 0) mbar_arrive(bar_scored);  // the producer may start its own loads
   // the slice's best min(nloc, kk_f) keys, written in descending key order
@@ -560,6 +627,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   const uint32_t bar_q = bar_empty + STAGES * 8;
   const uint32_t bar_sel = bar_q + 8;      // fused: this CTA's selected pages are ready
   const uint32_t bar_scored = bar_sel + 8;  // fused: this CTA's scoring loads are done
+  const uint32_t bar_reps = bar_scored + 8;  // fused: staged reps landed (two, one per ring half)
   const uint32_t kv_base = smem_u32(smem + SmemLayout::kv);
   auto bar_c = [] { named_bar_sync(1, NCT); };
   if (tid == 0) {
@@ -570,6 +638,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     mbar_init(bar_q, 1);
     mbar_init(bar_sel, 1);
     mbar_init(bar_scored, 1);
+    mbar_init(bar_reps, CONSUMERS);
+    mbar_init(bar_reps + 8, CONSUMERS);
     fence_mbar_init();
   }
   __syncthreads();
@@ -593,7 +663,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     __syncwarp();
   } else if (FUSED) {
     fused_score(p, reinterpret_cast<uint8_t*>(scratch), f_hist, f_sh_u64, f_sh_int, tid, warp,
-                lane, bar_c, bar_scored);
+                lane, bar_c, bar_scored, smem + SmemLayout::kv, kv_base, bar_reps);
   }
   if (!FUSED) __syncthreads();
   else if (warp != CONSUMERS) named_bar_sync(2, THREADS);
@@ -608,6 +678,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     seg = lo;
   }
   const int f0 = cum[seg], ncta = cum[seg + 1] - f0, ci = cta - f0;
+  // fused: CTAs that wait on this segment's selection unit (SHARED: every
+  // segment of the sequence)
+  const int npoll = (p.SEL == 1) ? cum[(seg / p.H_kv + 1) * p.H_kv] - cum[(seg / p.H_kv) * p.H_kv]
+                                 : ncta;
   // fused: the consumers may overwrite `cum` once the producer has read it
   if (FUSED && warp == CONSUMERS) named_bar_arrive(2, THREADS);
   const int b = seg / p.H_kv, h = seg % p.H_kv;
@@ -633,6 +707,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     }
     uint32_t it = 0;
     bool ok = true;
+    bool scored = !FUSED;
+    const uint32_t blocked = FUSED ? fused_stage_off(p) / KV_STAGE_BYTES : STAGES;
     // phase 0: list index i -> Initial/Local block; phase 1: i -> selected block
     auto produce = [&](int phase, int u0, int u1) {
       for (int base = u0; base < u1 && ok; base += 32) {
@@ -678,6 +754,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
             if (it >= STAGES &&
                 !mbar_wait(bar_empty + 8 * st, ((it / STAGES) - 1) & 1, p.status))
               okl = 0;
+            // fused: stages holding the staged representatives are refilled
+            // only once this CTA's scoring is done
+            if (okl && !scored && st >= blocked && ntok_k > 0) {
+              mbar_wait_sleep(bar_scored, 0, p.status, 64);
+              scored = true;
+            }
             if (okl) {
               info[st].ntok = ntok_k;
               info[st].end = 0;
@@ -700,10 +782,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         }
       }
     };
-    // fused: the scoring loads go first; the Initial/Local blocks are needed
-    // only after the selection
-    if (FUSED && lane == 0) mbar_wait_sleep(bar_scored, 0, p.status, 64);
-    __syncwarp();
     produce(0, a0, a1);
     if (FUSED) {
       // phase B: this CTA's share of the selected blocks, handed over by the
@@ -742,24 +820,19 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   const int g = lane >> 2, t = lane & 3;
   const int ctid = tid;
 
-  // Fused step: count this CTA done; the last CTA of the launch zeroes the
-  // scoring tickets and the count for the next launch.
-  auto finish = [&]() {
-    if (FUSED && ctid == 0) {
-      const int old = atom_acq_rel_gpu_add(p.f_done, 1);
-      if (old == grid - 1) {
-        for (int i = 0; i < p.B * p.SEL; ++i) p.f_counters[i] = 0;
-        p.f_done[0] = 0;
-      }
-    }
-  };
-
   if constexpr (FUSED) {
     const int n1 = fused_merge(p, reinterpret_cast<uint8_t*>(scratch), f_hist, f_sh_u64,
                                f_sh_int, b, h, ci, ncta, ctid, bar_c);
     if (ctid == 0) {
       bcast[61] = n1;
       mbar_arrive(bar_sel);
+      // the last of the unit's npoll waiting CTAs zeroes its tickets for the
+      // next launch (every other waiter has read them by then)
+      const int unit = b * p.SEL + (p.SEL == 1 ? 0 : h);
+      if (atomicAdd(p.f_polled + unit, 1) == npoll - 1) {
+        p.f_counters[unit] = 0;
+        p.f_polled[unit] = 0;
+      }
     }
   }
   float acc[16][4];
@@ -950,7 +1023,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       const float L = fm[MAX_G + gg];
       p.out[((size_t)b * H_q + h * p.G + gg) * D + c] = L > 0.0f ? v / L : 0.0f;
     }
-    finish();
     return;
   }
 
@@ -970,14 +1042,33 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     }
   }
   named_bar_sync(1, NCT);
-  if (ctid == 0) {
-    const int old = atom_acq_rel_gpu_add(p.counters + seg, 1);
-    bcast[60] = (old + 1 == ncta) ? 1 : 0;
-  }
-  named_bar_sync(1, NCT);
-  if (!bcast[60]) {
-    finish();
-    return;
+  if constexpr (FUSED) {
+    // every CTA is resident: the segment's first CTA merges once the others'
+    // partials are in; the others leave as soon as theirs is released
+    if (ci != 0) {
+      if (ctid == 0) red_release_gpu_add(p.counters + seg, 1);
+      return;
+    }
+    if (ctid == 0) {
+      const uint64_t t0 = globaltimer();
+      for (uint32_t i = 0;; ++i) {
+        if (ld_acquire_gpu(p.counters + seg) >= ncta - 1) break;
+        if ((i & 63u) == 63u && globaltimer() - t0 > WAIT_LIMIT_NS) {
+          set_status(p.status, KT_ERR_TIMEOUT);
+          break;
+        }
+        __nanosleep(32);
+      }
+      p.counters[seg] = 0;  // all ncta - 1 tickets are in
+    }
+    named_bar_sync(1, NCT);
+  } else {
+    if (ctid == 0) {
+      const int old = atom_acq_rel_gpu_add(p.counters + seg, 1);
+      bcast[60] = (old + 1 == ncta) ? 1 : 0;
+    }
+    named_bar_sync(1, NCT);
+    if (!bcast[60]) return;
   }
 
   // ---- last CTA of the segment: merge partials of CTAs f0 .. f0+ncta-1.
@@ -1060,8 +1151,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     *reinterpret_cast<float4*>(p.out + ((size_t)b * H_q + h * p.G + gg) * D + (f % D)) =
         make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
   }
-  if (ctid == 0) p.counters[seg] = 0;
-  finish();
+  if (!FUSED && ctid == 0) p.counters[seg] = 0;
 }
 
 }  // namespace
@@ -1116,7 +1206,7 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   p.f_cand = a.f_cand;
   p.f_cand_pages = a.f_cand_pages;
   p.f_counters = a.f_counters;
-  p.f_done = a.f_done;
+  p.f_polled = a.f_polled;
   p.sel_out = a.sel_out;
   p.cnt_out = a.cnt_out;
 

@@ -114,8 +114,8 @@ WsLayout layout(kt_op op, const kt_paged_kv* kv, const kt_sparse_params* p, int 
                                                        : FUSED_KK_CAP);
   L.f_counters = off;
   off = align256(off + units * 4);
-  L.f_done = off;
-  off = align256(off + 4);
+  L.f_polled = off;
+  off = align256(off + units * 4);
   L.f_cand = off;
   off = align256(off + fcap * 8);
   L.f_cand_pages = off;
@@ -520,7 +520,7 @@ kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void
     a.f_cand = at<unsigned long long>(ws, L.f_cand);
     a.f_cand_pages = at<int>(ws, L.f_cand_pages);
     a.f_counters = at<int>(ws, L.f_counters);
-    a.f_done = at<int>(ws, L.f_done);
+    a.f_polled = at<int>(ws, L.f_polled);
     a.sel_out = sel;
     a.cnt_out = cnt;
     return cuda_status(launch_attention(a, (cudaStream_t)stream));

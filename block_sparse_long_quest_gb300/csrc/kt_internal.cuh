@@ -98,7 +98,7 @@ struct WsLayout {
   size_t sel_cand_pages; // int32 [B*SEL*nchunks*kk], page id of each candidate
   size_t sel_pages;      // int32 [B*SEL*top_k], page ids of the selection (step path)
   size_t f_counters;     // int32 [B*SEL] fused step: scoring tickets per unit
-  size_t f_done;         // int32: fused step CTAs finished in this launch
+  size_t f_polled;       // int32 [B*SEL]: fused step CTAs done polling each unit
   size_t f_cand;         // uint64 [MAX_ATTN_CTAS * min(top_k, FUSED_KK_CAP)]
   size_t f_cand_pages;   // int32, same count
   size_t attn_counters;  // int32 [S]
@@ -369,7 +369,7 @@ struct AttnLaunch {
   unsigned long long* f_cand;
   int* f_cand_pages;
   int* f_counters;  // [B*SEL] scoring tickets, zero between launches
-  int* f_done;      // CTAs finished in this launch, zero between launches
+  int* f_polled;    // [B*SEL] CTAs past each unit's ticket wait, zero between launches
   int32_t* sel_out;
   int32_t* cnt_out;
 };

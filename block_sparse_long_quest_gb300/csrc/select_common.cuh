@@ -25,6 +25,17 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// warp_sum of N independent values, the butterfly steps interleaved so that
+// the N shuffle chains overlap; each value is summed in warp_sum's order.
+template <int N>
+__device__ __forceinline__ void warp_sum_n(float (&v)[N]) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+  }
+}
+
 __device__ __forceinline__ int warp_sum_int(int v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -57,6 +68,26 @@ __device__ __forceinline__ int count_greater(const unsigned long long* a, int n,
     r0 += (v.x > key ? 1 : 0) + (v.y > key ? 1 : 0);
   }
   return r0 + r1;
+}
+
+// This lane's share of a block's dot product with the weights: NV 16-byte
+// vectors, fp16 (8 values each) or fp32 (4 values each), in a fixed order.
+template <int NV, bool F32>
+__device__ __forceinline__ float lane_dot(const float (&w)[NV][F32 ? 4 : 8], const uint4 (&x)[NV]) {
+  float acc = 0.0f;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    if constexpr (F32) {
+      const float4 f = *reinterpret_cast<const float4*>(&x[v]);
+      acc = fmaf(w[v][0], f.x, acc);
+      acc = fmaf(w[v][1], f.y, acc);
+      acc = fmaf(w[v][2], f.z, acc);
+      acc = fmaf(w[v][3], f.w, acc);
+    } else {
+      acc += dot8(w[v], x[v]);
+    }
+  }
+  return acc;
 }
 
 // k-th largest of N distinct keys in shared memory (1 <= k <= N), all threads
@@ -504,27 +535,19 @@ __device__ __forceinline__ void score_linear(const void* reps, int P, int H_kv, 
     }
   };
   auto reduce = [&](int j0, const uint4 (&x)[GB][NV], const int (&page)[GB]) {
+    float acc[GB];
 #pragma unroll
-    for (int bi = 0; bi < GB; ++bi) {
-      float acc = 0.0f;
+    for (int bi = 0; bi < GB; ++bi) acc[bi] = lane_dot<NV, F32>(w, x[bi]);
+    warp_sum_n(acc);
+    if (lane == 0) {
 #pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        if (F32) {
-          const float4 f = *reinterpret_cast<const float4*>(&x[bi][v]);
-          acc = fmaf(w[v][0], f.x, acc);
-          acc = fmaf(w[v][1], f.y, acc);
-          acc = fmaf(w[v][2], f.z, acc);
-          acc = fmaf(w[v][3], f.w, acc);
-        } else {
-          acc += dot8(w[v], x[bi][v]);
+      for (int bi = 0; bi < GB; ++bi) {
+        const int j = j0 + bi;
+        if (j < je) {
+          const bool ok = page[bi] >= 0 && page[bi] < P;
+          keys[j - js] = make_key(ok ? acc[bi] : -INFINITY, j);
+          if (!ok) set_status(status, KT_ERR_DEVICE_CHECK);
         }
-      }
-      acc = warp_sum(acc);
-      const int j = j0 + bi;
-      if (j < je) {
-        const bool ok = page[bi] >= 0 && page[bi] < P;
-        if (lane == 0) keys[j - js] = make_key(ok ? acc : -INFINITY, j);
-        if (!ok && lane == 0) set_status(status, KT_ERR_DEVICE_CHECK);
       }
     }
   };
@@ -557,6 +580,188 @@ __device__ __forceinline__ void score_linear(const void* reps, int P, int H_kv, 
       int page[GB];
       load(j0, x, page);
       reduce(j0, x, page);
+    }
+  }
+}
+
+// score_linear over representatives already in shared memory: block i of
+// the group (i < nblk) has its V 16-byte vectors at sbuf + i*sstride; its key goes to
+// keys[i] with block id j0 + i, its page (for the range check) is pg[i].
+// Same lane-to-vector mapping and summation order as score_linear, so the
+// keys are identical.
+template <int NV, bool F32, int WARPS>
+__device__ __forceinline__ void score_linear_smem(const uint4* sbuf, int sstride, int nblk, int j0, int P,
+                                                  const int* pg, const float* wts, int V,
+                                                  unsigned long long* keys, int warp, int lane,
+                                                  int* status) {
+  constexpr int GB = 8 / NV;
+  constexpr int VE = F32 ? 4 : 8;
+  float w[NV][VE];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int vec = lane + 32 * v;
+#pragma unroll
+    for (int e = 0; e < VE; e += 4) {
+      const float4 f = (vec < V) ? *reinterpret_cast<const float4*>(wts + vec * VE + e)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+      w[v][e] = f.x;
+      w[v][e + 1] = f.y;
+      w[v][e + 2] = f.z;
+      w[v][e + 3] = f.w;
+    }
+  }
+#pragma unroll 1
+  for (int i0 = warp * GB; i0 < nblk; i0 += WARPS * GB) {
+    uint4 x[GB][NV];
+#pragma unroll
+    for (int bi = 0; bi < GB; ++bi) {
+      const int i = i0 + bi;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int vec = lane + 32 * v;
+        x[bi][v] = (i < nblk && vec < V) ? sbuf[(size_t)i * sstride + vec] : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    float acc[GB];
+#pragma unroll
+    for (int bi = 0; bi < GB; ++bi) acc[bi] = lane_dot<NV, F32>(w, x[bi]);
+    warp_sum_n(acc);
+    if (lane == 0) {
+#pragma unroll
+      for (int bi = 0; bi < GB; ++bi) {
+        const int i = i0 + bi;
+        if (i < nblk) {
+          const bool ok = pg[i] >= 0 && pg[i] < P;
+          keys[i] = make_key(ok ? acc[bi] : -INFINITY, j0 + i);
+          if (!ok) set_status(status, KT_ERR_DEVICE_CHECK);
+        }
+      }
+    }
+  }
+}
+
+// Linear scoring of fp16 representatives on the tensor cores.  Blocks are
+// staged in shared memory at a row stride of sb bytes (sbase, a shared-space
+// address), K fp16 values each in the order of the fp32 weights wts[K].  The
+// weights are split into fp16 hi + lo parts, which form columns 0 and 1 of the
+// B operand (the other columns are zero), so one mma.sync m16n8k16 step
+// reduces 16 blocks x 16 values into two fp32 partial sums per block; the
+// score is their sum.  Products of fp16 values are exact in fp32, and hi + lo
+// carries the weight to about 2^-22.  With many 16-block groups each warp
+// takes whole groups (w, w + WARPS, ...); with few, each group's K range is
+// split over WARPS / groups warps and the partial sums are added through
+// red[WARPS * 16] in warp order.  All WARPS warps call it (bar syncs them).
+// keys[i] receives block i's key with block id j0 + i.
+template <int WARPS, class Bar>
+__device__ __forceinline__ void score_mma_smem(uint32_t sbase, int sb, int nblk, int j0, int P,
+                                               const int* pg, const float* wts, int K,
+                                               unsigned long long* keys, float* red, int warp,
+                                               int lane, int* status, Bar bar) {
+  constexpr int MAXG = 4;  // groups per warp per pass
+  constexpr int KC = 16;   // k-steps whose weight fragments are held in registers
+  const int ngrp = (nblk + 15) >> 4;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t koff = (uint32_t)((lane >> 4) * 16);  // bytes: k offset 0 or 8
+  const int nks = K / 16;
+  // weight fragments of k-steps ks0 .. ks0+kn-1 (kn <= KC): column 0 hi, 1 lo
+  auto build = [&](int ks0, int kn, uint32_t (&bf)[KC][2]) {
+#pragma unroll
+    for (int kk = 0; kk < KC; ++kk) {
+      bf[kk][0] = bf[kk][1] = 0u;
+      if (kk < kn && g < 2) {
+        const int ks = ks0 + kk;
+        const float2 wa = *reinterpret_cast<const float2*>(wts + ks * 16 + 2 * t);
+        const float2 wb = *reinterpret_cast<const float2*>(wts + ks * 16 + 2 * t + 8);
+        __half2 ha = __floats2half2_rn(wa.x, wa.y), hb = __floats2half2_rn(wb.x, wb.y);
+        if (g == 1) {
+          ha = __floats2half2_rn(wa.x - __low2float(ha), wa.y - __high2float(ha));
+          hb = __floats2half2_rn(wb.x - __low2float(hb), wb.y - __high2float(hb));
+        }
+        bf[kk][0] = *reinterpret_cast<uint32_t*>(&ha);
+        bf[kk][1] = *reinterpret_cast<uint32_t*>(&hb);
+      }
+    }
+  };
+  // acc += rows of ra (16 blocks) x weights over k-steps ks0 .. ks0+kn-1,
+  // eight A fragments in flight at a time
+  auto run = [&](uint32_t ra, int ks0, int kn, const uint32_t (&bf)[KC][2], float (&acc)[4]) {
+#pragma unroll
+    for (int h = 0; h < KC; h += 8) {
+      uint32_t a[8][4];
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        if (h + kk < kn) ldsm_x4(a[kk][0], a[kk][1], a[kk][2], a[kk][3], ra + (uint32_t)(ks0 + h + kk) * 32u);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        if (h + kk < kn)
+          mma_16816(acc, a[kk][0], a[kk][1], a[kk][2], a[kk][3], bf[h + kk][0], bf[h + kk][1]);
+    }
+  };
+  auto emit = [&](int i, float score) {
+    const bool ok = pg[i] >= 0 && pg[i] < P;
+    keys[i] = make_key(ok ? score : -INFINITY, j0 + i);
+    if (!ok) set_status(status, KT_ERR_DEVICE_CHECK);
+  };
+  if (ngrp * 2 <= WARPS) {
+    // split K: warp w -> group w / ns, k-steps part w % ns of ns
+    const int ns = WARPS / ngrp;
+    const int grp = warp / ns, part = warp % ns;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (grp < ngrp) {
+      const int row = min(grp * 16 + (lane & 15), nblk - 1);
+      const uint32_t ra = sbase + (uint32_t)row * (uint32_t)sb + koff;
+      const int k0 = part * nks / ns, k1 = (part + 1) * nks / ns;
+#pragma unroll 1
+      for (int ks0 = k0; ks0 < k1; ks0 += KC) {
+        uint32_t bf[KC][2];
+        const int kn = min(KC, k1 - ks0);
+        build(ks0, kn, bf);
+        run(ra, ks0, kn, bf, acc);
+      }
+    }
+    if (t == 0) {
+      red[warp * 16 + g] = acc[0] + acc[1];
+      red[warp * 16 + g + 8] = acc[2] + acc[3];
+    }
+    bar();
+    const int tid = warp * 32 + lane;
+    if (tid < nblk) {
+      const int gi = tid >> 4, r = tid & 15;
+      float sc = 0.0f;
+      for (int q = 0; q < ns; ++q) sc += red[(gi * ns + q) * 16 + r];
+      emit(tid, sc);
+    }
+    return;
+  }
+#pragma unroll 1
+  for (int gb = warp; gb < ngrp; gb += WARPS * MAXG) {
+    float acc[MAXG][4];
+    uint32_t rowaddr[MAXG];
+#pragma unroll
+    for (int m = 0; m < MAXG; ++m) {
+      acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.0f;
+      const int row = min((gb + m * WARPS) * 16 + (lane & 15), nblk - 1);  // past the end: ignored
+      rowaddr[m] = sbase + (uint32_t)row * (uint32_t)sb + koff;
+    }
+#pragma unroll 1
+    for (int ks0 = 0; ks0 < nks; ks0 += KC) {
+      uint32_t bf[KC][2];
+      const int kn = min(KC, nks - ks0);
+      build(ks0, kn, bf);
+#pragma unroll
+      for (int m = 0; m < MAXG; ++m)
+        if (gb + m * WARPS < ngrp) run(rowaddr[m], ks0, kn, bf, acc[m]);
+    }
+    if (t == 0) {
+#pragma unroll
+      for (int m = 0; m < MAXG; ++m) {
+        const int grp = gb + m * WARPS;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = grp * 16 + g + 8 * h;
+          if (grp < ngrp && i < nblk) emit(i, acc[m][2 * h] + acc[m][2 * h + 1]);
+        }
+      }
     }
   }
 }
