@@ -48,6 +48,7 @@ constexpr int HALF_WARPS = CONSUMERS / 2;
 constexpr int SCRATCH_FLOATS = HALF_WARPS * MAX_G * (D + 2);
 static_assert(SCRATCH_FLOATS * 4 == ATTN_SCRATCH_BYTES, "scratch size shared with the host");
 static_assert(NCT == ATTN_CONSUMER_THREADS, "consumer threads shared with the host");
+static_assert(STAGES * KV_STAGE_BYTES == ATTN_RING_BYTES, "ring size shared with the host");
 
 struct StageInfo {
   int ntok, end, pad0, pad1;
@@ -260,7 +261,8 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
   const int nkv = p.SEL == 1 ? p.H_kv : 1;
   const int Rw = p.rep == KT_REP_QUEST ? 2 : 1;
   const bool f32 = p.rep == KT_REP_MEAN;
-  const FusedScoreLayout Ls = fused_score_layout(nkv * Rw * D, p.f_chunk, p.kk_f);
+  const bool multi = p.rep == KT_REP_FIX || p.rep == KT_REP_DYNAMIC;  // max over reps per head
+  const FusedScoreLayout Ls = fused_score_layout(multi ? 0 : nkv * Rw * D, p.f_chunk, p.kk_f);
   float* wts = reinterpret_cast<float*>(scr);
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(scr + Ls.keys);
   int* pgs = reinterpret_cast<int*>(scr + Ls.pgs);
@@ -272,7 +274,7 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     pgs[i] = j < p.max_blocks ? __ldg(p.table + (size_t)bu * p.max_blocks + j) : -1;
   }
   const Part pu = partition(seq_len(p, bu), p.I_b, p.L_b);
-  fused_weights(p, wts, bu, g0, nkv, ctid);
+  if (!multi) fused_weights(p, wts, bu, g0, nkv, ctid);
   const int je = min(js + p.f_chunk, pu.c1);
   const int nloc = max(0, je - js);  // js >= c0 whenever the slice is not empty
   bar_c();
@@ -320,7 +322,12 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
       const uint32_t base = ring_u32 + buf_off(r);
       const uint4* sbuf = reinterpret_cast<const uint4*>(ring + buf_off(r));
 #define KT_SCORE(NV, F) selc::score_linear_smem<NV, F, CONSUMERS>(sbuf, (int)(sb / 16), nr, js + r0, p.P, pgs + r0, wts, V, keys + r0, warp, lane, p.status)
-      if (f32) {
+      if (multi) {
+        selc::score_multi_mma_smem<CONSUMERS>(
+            base, (int)sb, nr, js + r0, p.P, pgs + r0,
+            p.q + ((size_t)bu * p.H_kv * p.G + (size_t)g0 * p.G) * D, p.G, nkv, p.R, keys + r0,
+            reinterpret_cast<float*>(hist), warp, lane, p.status, bar_c);
+      } else if (f32) {
         if (V <= 32) KT_SCORE(1, true);
         else if (V <= 64) KT_SCORE(2, true);
         else if (V <= 128) KT_SCORE(4, true);

@@ -426,7 +426,7 @@ namespace {
 // candidates per CTA.
 bool fused_plan(const kt_paged_kv* kv, const kt_sparse_params* p, int sms, int* ncpu,
                 int* chunk_out, int* kk) {
-  if (p->rep != KT_REP_MAX && p->rep != KT_REP_MEAN && p->rep != KT_REP_QUEST) return false;
+  const bool multi = p->rep == KT_REP_FIX || p->rep == KT_REP_DYNAMIC;
   if (sms < 1 || sms > MAX_ATTN_CTAS) return false;
   const long long S = (long long)kv->batch * kv->num_kv_heads;
   const int SEL = p->head_mode == KT_HEAD_SHARED ? 1 : kv->num_kv_heads;
@@ -441,11 +441,13 @@ bool fused_plan(const kt_paged_kv* kv, const kt_sparse_params* p, int sms, int* 
   const int Rw = p->rep == KT_REP_QUEST ? 2 : 1;
   const bool f32 = p->rep == KT_REP_MEAN;
   const int V = nkv * reps_rows(p) * D / (f32 ? 4 : 8);
-  if (V > 256) return false;
+  if (!multi && V > 256) return false;  // linear CUDA-core scoring: 8 vectors a lane
+  if ((long long)V * 16 + 16 > ATTN_RING_BYTES / 2) return false;  // a block per staging round
   const long long nslots = (long long)nc * k;
   if (nslots > FUSED_MAX_SLOTS) return false;
   const int kmax = (int)(p->top_k < nslots ? p->top_k : nslots);
-  if (fused_score_layout(nkv * Rw * D, chunk, k).total > ATTN_SCRATCH_BYTES) return false;
+  if (fused_score_layout(multi ? 0 : nkv * Rw * D, chunk, k).total > ATTN_SCRATCH_BYTES)
+    return false;
   if (fused_merge_layout(nc, k, kmax).total > ATTN_MERGE_BYTES) return false;
   if (attn_fused_max_ctas_per_sm() < 1) return false;
   *ncpu = nc;

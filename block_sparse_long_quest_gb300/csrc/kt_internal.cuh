@@ -24,6 +24,7 @@ constexpr int MAX_DYN_REPS = 32;
 constexpr int ATTN_SCRATCH_BYTES = 4 * MAX_G * (D + 2) * 4;  // attention kernel scratch (smem)
 constexpr int FUSED_KK_CAP = 256;  // per-CTA candidates of the fused step
 constexpr int ATTN_CONSUMER_THREADS = 256;  // consumer threads of the attention kernel
+constexpr int ATTN_RING_BYTES = 3 * 4 * 128 * 64 * 2;  // attention KV ring (3 stages x 64 KB)
 constexpr int FUSED_GATHER_PER_THREAD = 8;  // candidate slots a merging thread holds
 constexpr int FUSED_MAX_SLOTS = FUSED_GATHER_PER_THREAD * ATTN_CONSUMER_THREADS;
 

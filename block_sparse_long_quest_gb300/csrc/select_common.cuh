@@ -766,5 +766,101 @@ __device__ __forceinline__ void score_mma_smem(uint32_t sbase, int sb, int nblk,
   }
 }
 
+// Multi-representative scoring (Fix, Dynamic) on the tensor cores: the head
+// score of query head h is max_r q_h . rep_r of its KV head, the unit score
+// the sum over the unit's heads.  Blocks are staged at a row stride of sb
+// bytes as [KV head gi][rep r][128] fp16 (nkv KV heads from q_unit's heads,
+// G query heads each).  One mma.sync tile holds 16 blocks x one (gi, r) x the
+// G query heads (columns; the fp16 queries are exact), so the max over r is
+// elementwise and the sum over a KV head's queries a 4-lane reduction.  With
+// many tiles each warp takes whole tiles; with few, the KV heads of a tile are
+// split over WARPS / tiles warps and the partial sums are added through
+// red[WARPS * 16] in warp order.  All WARPS warps call it (bar syncs them).
+template <int WARPS, class Bar>
+__device__ __forceinline__ void score_multi_mma_smem(uint32_t sbase, int sb, int nblk, int j0,
+                                                     int P, const int* pg, const __half* q_unit,
+                                                     int G, int nkv, int R,
+                                                     unsigned long long* keys, float* red,
+                                                     int warp, int lane, int* status, Bar bar) {
+  const int ntile = (nblk + 15) >> 4;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t koff = (uint32_t)((lane >> 4) * 16);
+  // sum over KV heads gi = gi0, gi0 + gstep, ... of the head scores of the
+  // tile's rows g and g + 8 (every lane of a quad returns the same sums)
+  auto tile_sum = [&](int tile, int gi0, int gstep, float& s_lo, float& s_hi) {
+    s_lo = s_hi = 0.0f;
+    const int row = min(tile * 16 + (lane & 15), nblk - 1);
+    const uint32_t ra = sbase + (uint32_t)row * (uint32_t)sb + koff;
+#pragma unroll 1
+    for (int gi = gi0; gi < nkv; gi += gstep) {
+      uint32_t bf[8][2];
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        bf[ks][0] = bf[ks][1] = 0u;
+        if (g < G) {
+          const __half* qr = q_unit + (size_t)(gi * G + g) * D + ks * 16 + 2 * t;
+          bf[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qr));
+          bf[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qr + 8));
+        }
+      }
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+      for (int r = 0; r < R; ++r) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t rr = ra + (uint32_t)((gi * R + r) * D * 2);
+        uint32_t a[8][4];
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) ldsm_x4(a[ks][0], a[ks][1], a[ks][2], a[ks][3], rr + ks * 32);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_16816(c, a[ks][0], a[ks][1], a[ks][2], a[ks][3], bf[ks][0], bf[ks][1]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mx[e] = fmaxf(mx[e], c[e]);
+      }
+      // columns >= G are zero; sum the 8 columns of rows g and g + 8
+      float lo = mx[0] + mx[1], hi = mx[2] + mx[3];
+      lo += __shfl_xor_sync(0xffffffffu, lo, 1);
+      hi += __shfl_xor_sync(0xffffffffu, hi, 1);
+      lo += __shfl_xor_sync(0xffffffffu, lo, 2);
+      hi += __shfl_xor_sync(0xffffffffu, hi, 2);
+      s_lo += lo;
+      s_hi += hi;
+    }
+  };
+  auto emit = [&](int i, float score) {
+    const bool ok = pg[i] >= 0 && pg[i] < P;
+    keys[i] = make_key(ok ? score : -INFINITY, j0 + i);
+    if (!ok) set_status(status, KT_ERR_DEVICE_CHECK);
+  };
+  if (ntile * 2 <= WARPS && nkv > 1) {
+    const int ns = min(WARPS / ntile, nkv);
+    const int tile = warp / ns, part = warp % ns;
+    float lo = 0.f, hi = 0.f;
+    if (tile < ntile) tile_sum(tile, part, ns, lo, hi);
+    if (t == 0) {
+      red[warp * 16 + g] = lo;
+      red[warp * 16 + g + 8] = hi;
+    }
+    bar();
+    const int tid = warp * 32 + lane;
+    if (tid < nblk) {
+      const int ti = tid >> 4, rw = tid & 15;
+      float sc = 0.0f;
+      for (int q = 0; q < ns; ++q) sc += red[(ti * ns + q) * 16 + rw];
+      emit(tid, sc);
+    }
+    return;
+  }
+#pragma unroll 1
+  for (int tile = warp; tile < ntile; tile += WARPS) {
+    float lo, hi;
+    tile_sum(tile, 0, 1, lo, hi);
+    if (t == 0) {
+      if (tile * 16 + g < nblk) emit(tile * 16 + g, lo);
+      if (tile * 16 + g + 8 < nblk) emit(tile * 16 + g + 8, hi);
+    }
+  }
+}
+
 }  // namespace selc
 }  // namespace kt

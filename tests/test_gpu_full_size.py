@@ -73,7 +73,7 @@ def test_128k_shared_quest_full_size():
     _check_step(w, dw, (0, 1))
 
 
-@pytest.mark.parametrize("rep", [synth.REP_QUEST, synth.REP_MAX])
+@pytest.mark.parametrize("rep", [synth.REP_QUEST, synth.REP_MAX, synth.REP_FIX])
 def test_1m_separate_full_size_sampled_heads(rep):
     w = synth.long1m(rep=rep)
     dw = DevWorkload(w)
