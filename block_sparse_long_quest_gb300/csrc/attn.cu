@@ -188,6 +188,18 @@ __device__ __forceinline__ uint32_t fused_stage_off(const Params& p, uint32_t* s
   return need <= RING ? (uint32_t)(RING - need) : 0u;
 }
 
+// Mean reps (fp32) scored on the CUDA cores; kept out of line, away from the
+// common fp16 path.
+__device__ __noinline__ void fused_score_f32(const uint4* sbuf, int sstride, int nblk, int j0,
+                                             int P, const int* pg, const float* wts, int V,
+                                             unsigned long long* keys, int warp, int lane,
+                                             int* status) {
+  if (V <= 32) selc::score_linear_smem<1, true, CONSUMERS>(sbuf, sstride, nblk, j0, P, pg, wts, V, keys, warp, lane, status);
+  else if (V <= 64) selc::score_linear_smem<2, true, CONSUMERS>(sbuf, sstride, nblk, j0, P, pg, wts, V, keys, warp, lane, status);
+  else if (V <= 128) selc::score_linear_smem<4, true, CONSUMERS>(sbuf, sstride, nblk, j0, P, pg, wts, V, keys, warp, lane, status);
+  else selc::score_linear_smem<8, true, CONSUMERS>(sbuf, sstride, nblk, j0, P, pg, wts, V, keys, warp, lane, status);
+}
+
 // Fused step: the linear weight rows of KV heads g0 .. g0+nkv-1 of sequence bu
 // (query heads summed in ascending order per channel; Quest: the negative and
 // positive parts, paired with the kmin and kmax rows).  Same values as the
@@ -328,10 +340,8 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
             p.q + ((size_t)bu * p.H_kv * p.G + (size_t)g0 * p.G) * D, p.G, nkv, p.R, keys + r0,
             reinterpret_cast<float*>(hist), warp, lane, p.status, bar_c);
       } else if (f32) {
-        if (V <= 32) KT_SCORE(1, true);
-        else if (V <= 64) KT_SCORE(2, true);
-        else if (V <= 128) KT_SCORE(4, true);
-        else KT_SCORE(8, true);
+        fused_score_f32(sbuf, (int)(sb / 16), nr, js + r0, p.P, pgs + r0, wts, V, keys + r0, warp,
+                        lane, p.status);
       } else if (nr <= 8 * CONSUMERS / (V <= 32 ? 1 : V <= 64 ? 2 : V <= 128 ? 4 : 8)) {
         // one pass of the CUDA-core path: each warp reduces its few blocks
         if (V <= 32) KT_SCORE(1, false);

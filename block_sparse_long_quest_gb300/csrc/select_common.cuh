@@ -219,7 +219,7 @@ __device__ void radix_select(const unsigned long long* keys, int N, int k, unsig
 // themselves.  Scratch: hist 512 bins, bkey/bidx NT entries, sh_u64
 // 2 + 2*NT/32, sh_int 4.  All NT threads call it; `bar` synchronises them.
 template <int NT, class Bar>
-__device__ void select_top(const unsigned long long* keys, int N, int k, int* idx_out,
+__device__ __noinline__ void select_top(const unsigned long long* keys, int N, int k, int* idx_out,
                            unsigned long long* bkey, int* bidx, unsigned int* hist,
                            unsigned long long* sh_u64, int* sh_int, int tid, Bar bar) {
   constexpr int WARPS = NT / 32;
@@ -777,7 +777,7 @@ __device__ __forceinline__ void score_mma_smem(uint32_t sbase, int sb, int nblk,
 // split over WARPS / tiles warps and the partial sums are added through
 // red[WARPS * 16] in warp order.  All WARPS warps call it (bar syncs them).
 template <int WARPS, class Bar>
-__device__ __forceinline__ void score_multi_mma_smem(uint32_t sbase, int sb, int nblk, int j0,
+__device__ __noinline__ void score_multi_mma_smem(uint32_t sbase, int sb, int nblk, int j0,
                                                      int P, const int* pg, const __half* q_unit,
                                                      int G, int nkv, int R,
                                                      unsigned long long* keys, float* red,
