@@ -195,18 +195,30 @@ __global__ void __launch_bounds__(THREADS, 1) dyn_pass_kernel(const __grid_const
           }
         }
       }
-      // ---- mask, scale; pass 1: row max / sum; pass 2: normalised column sums
+      // ---- mask, scale; pass 1: row max / sum; pass 2: normalised column sums.
+      // A block that ends before the first query position is seen whole by
+      // every present row: only absent rows are masked there.
+      if (page_ok && (j + 1) * BS - 1 <= n - p.T) {
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+          for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int hr = e >> 1;
-            const int tok = j * BS + half * 64 + nt * 8 + 2 * t + (e & 1);
-            const bool vis = page_ok && tok < n && tok <= pos[mt][hr];
-            s[mt][nt][e] = vis ? s[mt][nt][e] * p.scale_log2 : -INFINITY;
-          }
+            for (int e = 0; e < 4; ++e)
+              s[mt][nt][e] = pos[mt][e >> 1] >= 0 ? s[mt][nt][e] * p.scale_log2 : -INFINITY;
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int hr = e >> 1;
+              const int tok = j * BS + half * 64 + nt * 8 + 2 * t + (e & 1);
+              const bool vis = page_ok && tok < n && tok <= pos[mt][hr];
+              s[mt][nt][e] = vis ? s[mt][nt][e] * p.scale_log2 : -INFINITY;
+            }
+      }
       if (p.pass == 1) {
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
@@ -290,14 +302,38 @@ __global__ void __launch_bounds__(THREADS, 1) dyn_pass_kernel(const __grid_const
     // reps exist for full blocks only: the num_reps best tokens (ties: lower
     // index), emitted in token order
     if ((j + 1) * BS <= n && page_ok) {
-      if (tid < BS) {
-        const float v = tscore[tid];
-        int rank = 0;
-        for (int u = 0; u < BS; ++u) {
-          const float w = tscore[u];
-          rank += (w > v || (w == v && u < tid)) ? 1 : 0;
+      // warp 0 takes the best token R times (score descending, then index
+      // ascending): lane l holds tokens l, l+32, l+64, l+96
+      if (warp == 0) {
+        float v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = tscore[lane + 32 * k];
+        unsigned int taken = 0u;
+#pragma unroll 1
+        for (int rr = 0; rr < p.R; ++rr) {
+          float bv = -INFINITY;
+          int bi = 0x7fffffff;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int idx = lane + 32 * k;
+            if (!((taken >> k) & 1u) && (v[k] > bv || (v[k] == bv && idx < bi))) {
+              bv = v[k];
+              bi = idx;
+            }
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) {
+              bv = ov;
+              bi = oi;
+            }
+          }
+          if (bi < BS && (bi & 31) == lane) taken |= 1u << (bi >> 5);
         }
-        pick[tid] = rank < p.R ? 1 : 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) pick[lane + 32 * k] = (taken >> k) & 1u;
       }
       __syncthreads();
       if (tid < BS && pick[tid]) {
