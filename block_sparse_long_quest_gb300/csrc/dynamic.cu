@@ -10,14 +10,15 @@
 // where s_rt = q_r . k_t * scale, m_r = max_t s_rt and l_r = sum_t exp(s_rt - m_r)
 // over the tokens row r sees.  Three launches:
 //   pass 1   one CTA per (block slice, KV head, sequence): S = Q K^T for every
-//            block of its slice (mma.sync m16n8k16, Q fragments held in
-//            registers, K blocks by 2-D TMA into a double buffer); per block and
-//            row, the partial max and sum (base 2) go to the workspace.
+//            block of its slice on the 5th-generation tensor cores (tcgen05,
+//            accumulators in tensor memory, K blocks by 2-D TMA into a double
+//            buffer); per block and row, the partial max and sum (base 2) go to
+//            the workspace.
 //   combine  per (split, KV head, sequence): merge the partials of a range of
 //            blocks per row.
-//   pass 2   the same S for the requested blocks; p = exp2(s - M_r) / L_r summed
-//            over rows per token; the num_reps best tokens of each full block
-//            (ties: lower index) are copied, in token order, as its reps.
+//   pass 2   S^T for the requested blocks; p = exp2(s - M_r) / L_r summed over
+//            rows per token; the num_reps best tokens of each full block (ties:
+//            lower index) are copied, in token order, as its reps.
 // The path is a dense contraction (M = T*G rows per KV head) plus one exp per
 // logit per pass; K is read twice (once per pass).
 #include "kt_internal.cuh"
@@ -25,7 +26,6 @@
 namespace kt {
 namespace {
 
-constexpr int THREADS = 256;  // 8 warps; warp w owns rows 32w .. 32w+31
 constexpr int MAX_ROWS = 256;
 constexpr int BOX_BYTES = BS * 64 * 2;  // 128 tokens x 64 channels
 constexpr int KBUF_BYTES = 2 * BOX_BYTES;
@@ -55,40 +55,70 @@ __device__ __forceinline__ int seq_len_checked(const DynParams& p, int b) {
   return n;
 }
 
-// One CTA: KV head h of sequence b, blocks j = j_begin, j_begin + stride, ...
-__global__ void __launch_bounds__(THREADS, 1) dyn_pass_kernel(const __grid_constant__ DynParams p) {
+// ---- tcgen05 version of the two passes ---------------------------------------
+// One CTA (8 epilogue warps + 1 control warp) per (block slice, KV head,
+// sequence).  The T*G query rows live in shared memory as two K-major
+// 128-byte-swizzled boxes (64 channels x 256 rows each); each K block arrives
+// by TMA as two boxes (64 channels x 128 tokens) into a double buffer.  One
+// thread issues the tcgen05.mma chains into one of two 256-column TMEM
+// accumulators:
+//   pass 1  S = Q K^T, two M = 128 tiles (rows 0-127, 128-255) x N = 128
+//           tokens: a thread of the epilogue owns one row (its TMEM lane) and
+//           reduces the row's max and sum over the block's tokens itself;
+//   pass 2  S^T = K Q^T, M = 128 tokens x N = 256 rows: a thread owns one
+//           token and sums exp2(s - M_r) / L_r over its 128 rows; the two row
+//           halves meet in shared memory.
+// The epilogue of block q overlaps the MMAs of block q + 1.
+constexpr int TC_EPI_WARPS = 8;
+constexpr int TC_THREADS = (TC_EPI_WARPS + 1) * 32;
+constexpr int Q_BOX = MAX_ROWS * 128;  // 256 rows x 64 channels fp16
+constexpr int TC_SMEM = 2 * Q_BOX + 2 * KBUF_BYTES + 1024;
+constexpr uint32_t TMEM_COLS = 512;    // two 256-column accumulators
+static_assert(TC_SMEM > 233472 / 2, "one CTA per SM: it holds all of TMEM");
+
+__global__ void __launch_bounds__(TC_THREADS, 1) dyn_pass_tc_kernel(const __grid_constant__ DynParams p) {
   extern __shared__ uint8_t smem_raw[];
-  // 1024-byte aligned (128-byte swizzled TMA boxes); offsetting the array
-  // itself keeps the accesses below in the shared address space
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ __align__(8) uint64_t bars[2];
-  __shared__ float colsum[8][BS];
+  __shared__ __align__(8) uint64_t bars[6];  // K full x2, MMA done x2, TMEM free x2
+  __shared__ uint32_t tmem_base;
+  __shared__ __align__(16) float rowC[MAX_ROWS];  // pass 2: M_r + log2 L_r
+  __shared__ int rowPos[MAX_ROWS];
+  __shared__ float part[2][BS];
   __shared__ float tscore[BS];
-  __shared__ float rowM[MAX_ROWS], rowInvL[MAX_ROWS];
   __shared__ int pick[BS];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t = lane & 3;
   const int slice = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int n = seq_len_checked(p, b);
   const int nb = (n + BS - 1) / BS;
   const int rows = p.T * p.G;
   const int H_q = p.H_kv * p.G;
-  // blocks handled: pass 1 all blocks, pass 2 the requested range
   const int jb = p.pass == 1 ? 0 : min(p.first_block, nb);
   const int je = p.pass == 1 ? nb : min(nb, p.first_block + p.num_blocks);
-  const uint32_t bar0 = smem_u32(&bars[0]);
-  const uint32_t kbase = smem_u32(smem);
+  const int stride = p.nslices;
+  const int nmine = (jb + slice < je) ? (je - jb - slice + stride - 1) / stride : 0;
+  const uint32_t sQ = smem_u32(smem), sK = sQ + 2 * Q_BOX;
+  const uint32_t kfull = smem_u32(&bars[0]), mdone = kfull + 16, tfree = kfull + 32;
 
   if (tid == 0) {
-    mbar_init(bar0, 1);
-    mbar_init(bar0 + 8, 1);
+    mbar_init(kfull, 1);
+    mbar_init(kfull + 8, 1);
+    mbar_init(mdone, 1);
+    mbar_init(mdone + 8, 1);
+    mbar_init(tfree, TC_EPI_WARPS);
+    mbar_init(tfree + 8, TC_EPI_WARPS);
     fence_mbar_init();
     prefetch_tensormap(&p.kmap);
   }
-  // final row statistics for pass 2: combine the NSPLIT split partials
-  if (p.pass == 2) {
-    for (int r = tid; r < MAX_ROWS; r += THREADS) {
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_base)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  // rows: final statistics (pass 2) and query positions
+  for (int r = tid; r < MAX_ROWS; r += TC_THREADS) {
+    if (p.pass == 2) {
       float M = -INFINITY, L = 0.0f;
       if (r < rows) {
         const float2* sp = p.split + ((size_t)(b * p.H_kv + h) * NSPLIT) * MAX_ROWS + r;
@@ -100,261 +130,229 @@ __global__ void __launch_bounds__(THREADS, 1) dyn_pass_kernel(const __grid_const
           M = Mn;
         }
       }
-      rowM[r] = M;
-      rowInvL[r] = L > 0.0f ? 1.0f / L : 0.0f;
+      rowC[r] = (L > 0.0f && M != -INFINITY) ? M + log2f(L) : INFINITY;
     }
+    rowPos[r] = r < rows ? n - p.T + r / p.G : -1;  // -1: row absent, sees nothing
   }
-  // query fragments of this warp's two m-tiles (rows 32w .. 32w+31), all 8 k-steps
-  uint32_t qa[2][8][4];
-#pragma unroll
-  for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int r = warp * 32 + mt * 16 + g + 8 * hr;
-      const __half* qrow = nullptr;
-      if (r < rows) {
-        const int i = r / p.G, gg = r % p.G;
-        qrow = p.q_local + (((size_t)b * p.T + i) * H_q + h * p.G + gg) * D;
-      }
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        qa[mt][kk][hr] = qrow ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * t)) : 0u;
-        qa[mt][kk][2 + hr] =
-            qrow ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * t)) : 0u;
-      }
+  // query rows into the two swizzled boxes (16-byte chunk c of row r goes to
+  // box c / 8, chunk slot (c % 8) ^ (r % 8))
+  for (int idx = tid; idx < MAX_ROWS * 16; idx += TC_THREADS) {
+    const int r = idx >> 4, c = idx & 15;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r < rows) {
+      const __half* src = p.q_local + (((size_t)b * p.T + r / p.G) * H_q + h * p.G + r % p.G) * D;
+      v = __ldg(reinterpret_cast<const uint4*>(src) + c);
     }
+    *reinterpret_cast<uint4*>(smem + (c >> 3) * Q_BOX + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
   }
-  // positions of the four rows this thread holds: [mt][hr]
-  int pos[2][2];
-#pragma unroll
-  for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int r = warp * 32 + mt * 16 + g + 8 * hr;
-      pos[mt][hr] = r < rows ? n - p.T + r / p.G : -1;  // -1: row absent, sees nothing
-    }
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
 
-  auto issue = [&](int j, int buf) {
-    const int page = p.table[(size_t)b * p.max_blocks + j];
-    const uint32_t bar = bar0 + 8 * buf;
-    if (page < 0 || page >= p.P) {
-      set_status(p.status, KT_ERR_DEVICE_CHECK);
-      mbar_arrive(bar);
-      return false;
-    }
-    const int row = (page * p.H_kv + h) * BS;
-    mbar_arrive_expect_tx(bar, KBUF_BYTES);
-    const uint64_t pol = l2_evict_first_policy();
-    tma_load_2d(kbase + buf * KBUF_BYTES, &p.kmap, 0, row, bar, pol);
-    tma_load_2d(kbase + buf * KBUF_BYTES + BOX_BYTES, &p.kmap, 64, row, bar, pol);
-    return true;
-  };
-
-  const int stride = p.nslices;
-  int it = 0;
-  if (tid == 0 && jb + slice < je) issue(jb + slice, 0);
-  for (int j = jb + slice; j < je; j += stride, ++it) {
-    const int buf = it & 1;
-    if (tid == 0 && j + stride < je) issue(j + stride, buf ^ 1);
-    if (!mbar_wait(bar0 + 8 * buf, (it >> 1) & 1, p.status)) break;
-    const int page = p.table[(size_t)b * p.max_blocks + j];
-    const bool page_ok = page >= 0 && page < p.P;
-    const uint32_t kb = kbase + buf * KBUF_BYTES;
-    const int mi = lane >> 3, r8 = lane & 7;
-
-    // ---- S for this warp's 32 rows x 128 tokens, in two halves of 64 tokens
-    float rm[2][2] = {{-INFINITY, -INFINITY}, {-INFINITY, -INFINITY}};
-    float rl[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-    float cs[16][2];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) cs[i][0] = cs[i][1] = 0.0f;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float s[2][8][4];
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) s[mt][nt][0] = s[mt][nt][1] = s[mt][nt][2] = s[mt][nt][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {  // pairs of 8-token n-tiles
-          const int tok = half * 64 + np * 16 + (mi >> 1) * 8 + r8;
-          const int chunk = kk * 2 + (mi & 1);
-          const uint32_t addr = kb + (chunk >> 3) * BOX_BYTES + tok * 128 +
-                                (((chunk & 7) ^ (tok & 7)) << 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(b0, b1, b2, b3, addr);
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            mma_16816(s[mt][2 * np], qa[mt][kk][0], qa[mt][kk][1], qa[mt][kk][2], qa[mt][kk][3],
-                      b0, b1);
-            mma_16816(s[mt][2 * np + 1], qa[mt][kk][0], qa[mt][kk][1], qa[mt][kk][2],
-                      qa[mt][kk][3], b2, b3);
-          }
+  if (warp == TC_EPI_WARPS) {
+    // ============================ control thread ============================
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      auto load = [&](int q) {
+        const int j = jb + slice + q * stride, buf = q & 1;
+        const int page = p.table[(size_t)b * p.max_blocks + j];
+        if (page < 0 || page >= p.P) {  // the epilogue masks the whole block
+          set_status(p.status, KT_ERR_DEVICE_CHECK);
+          mbar_arrive(kfull + 8 * buf);
+          return;
         }
-      }
-      // ---- mask, scale; pass 1: row max / sum; pass 2: normalised column sums.
-      // A block that ends before the first query position is seen whole by
-      // every present row: only absent rows are masked there.
-      if (page_ok && (j + 1) * BS - 1 <= n - p.T) {
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              s[mt][nt][e] = pos[mt][e >> 1] >= 0 ? s[mt][nt][e] * p.scale_log2 : -INFINITY;
-      } else {
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int hr = e >> 1;
-              const int tok = j * BS + half * 64 + nt * 8 + 2 * t + (e & 1);
-              const bool vis = page_ok && tok < n && tok <= pos[mt][hr];
-              s[mt][nt][e] = vis ? s[mt][nt][e] * p.scale_log2 : -INFINITY;
-            }
-      }
-      if (p.pass == 1) {
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-              mx = fmaxf(mx, fmaxf(s[mt][nt][2 * hr], s[mt][nt][2 * hr + 1]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float Mn = fmaxf(rm[mt][hr], mx);
-            if (Mn == -INFINITY) continue;
-            float sum = 0.0f;
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-              sum += exp2f(s[mt][nt][2 * hr] - Mn) + exp2f(s[mt][nt][2 * hr + 1] - Mn);
-            rl[mt][hr] = rl[mt][hr] * exp2f(rm[mt][hr] - Mn) + sum;
-            rm[mt][hr] = Mn;
-          }
-      } else {
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const int r = warp * 32 + mt * 16 + g + 8 * hr;
-            const float M = rowM[r], iL = rowInvL[r];
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-              const float a0 = s[mt][nt][2 * hr], a1 = s[mt][nt][2 * hr + 1];
-              cs[half * 8 + nt][0] += (a0 == -INFINITY) ? 0.0f : exp2f(a0 - M) * iL;
-              cs[half * 8 + nt][1] += (a1 == -INFINITY) ? 0.0f : exp2f(a1 - M) * iL;
-            }
-          }
+        const int row = (page * p.H_kv + h) * BS;
+        mbar_arrive_expect_tx(kfull + 8 * buf, KBUF_BYTES);
+        tma_load_2d(sK + buf * KBUF_BYTES, &p.kmap, 0, row, kfull + 8 * buf, pol);
+        tma_load_2d(sK + buf * KBUF_BYTES + BOX_BYTES, &p.kmap, 64, row, kfull + 8 * buf, pol);
+      };
+      if (nmine > 0) load(0);
+      if (nmine > 1) load(1);
+      for (int q = 0; q < nmine; ++q) {
+        const int buf = q & 1;
+        if (!mbar_wait(kfull + 8 * buf, (q >> 1) & 1, p.status)) break;
+        if (q >= 2 && !mbar_wait(tfree + 8 * buf, ((q >> 1) - 1) & 1, p.status)) break;
+        tc_fence_after();
+        const uint32_t dt = tmem + (uint32_t)buf * 256u;
+        const uint32_t kb = sK + buf * KBUF_BYTES;
+        if (p.pass == 1) {
+          constexpr uint32_t id = umma_idesc_f16_f32(128, 128);
+          for (int mt = 0; mt < 2; ++mt)
+            for (int ks = 0; ks < 8; ++ks)
+              umma_f16(dt + mt * 128,
+                       umma_sdesc_sw128(sQ + (ks >> 2) * Q_BOX + mt * 128 * 128 + (ks & 3) * 32),
+                       umma_sdesc_sw128(kb + (ks >> 2) * BOX_BYTES + (ks & 3) * 32), id, ks > 0);
+        } else {
+          constexpr uint32_t id = umma_idesc_f16_f32(128, 256);
+          for (int ks = 0; ks < 8; ++ks)
+            umma_f16(dt, umma_sdesc_sw128(kb + (ks >> 2) * BOX_BYTES + (ks & 3) * 32),
+                     umma_sdesc_sw128(sQ + (ks >> 2) * Q_BOX + (ks & 3) * 32), id, ks > 0);
+        }
+        umma_commit(mdone + 8 * buf);
+        if (q + 2 < nmine) {
+          // the K buffer is free once these MMAs have read it
+          if (!mbar_wait(mdone + 8 * buf, (q >> 1) & 1, p.status)) break;
+          load(q + 2);
+        }
       }
     }
     __syncwarp();
-    // the K buffer is free once every warp is past its ldmatrix reads
-    __syncthreads();
-
-    if (p.pass == 1) {
-      // row sums over the four lanes of a row, then one write per row
+  } else {
+    // ============================ epilogue warps ============================
+    const int quarter = warp & 3, half = warp >> 2;
+    for (int q = 0; q < nmine; ++q) {
+      const int buf = q & 1, j = jb + slice + q * stride;
+      const bool live = mbar_wait(mdone + 8 * buf, (q >> 1) & 1, p.status);
+      tc_fence_after();
+      const int page = p.table[(size_t)b * p.max_blocks + j];
+      const bool page_ok = live && page >= 0 && page < p.P;
+      const bool whole = page_ok && (j + 1) * BS - 1 <= n - p.T;  // every present row sees it all
+      const uint32_t dt = tmem + (uint32_t)buf * 256u + ((uint32_t)(quarter * 32) << 16) +
+                          (uint32_t)(half * 128);
+      if (p.pass == 1) {
+        const int r = half * 128 + quarter * 32 + lane;  // this thread's row
+        const int pos = rowPos[r];
+        const bool row_ok = page_ok && pos >= 0;
+        const bool row_whole = whole && pos >= 0;  // no token of the block is masked
+        float m = -INFINITY, l = 0.0f;
+        // tcgen05.ld is warp-collective: every lane loads, masks apply after
+        for (int c0 = 0; c0 < BS; c0 += 32) {
+          float v[32];
+          tmem_ld32(dt + c0, v);
+          if (!row_whole) {
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          float l = rl[mt][hr];
-          l += __shfl_xor_sync(0xffffffffu, l, 1);
-          l += __shfl_xor_sync(0xffffffffu, l, 2);
-          const int r = warp * 32 + mt * 16 + g + 8 * hr;
-          if (t == 0)
-            p.stats[(((size_t)b * p.H_kv + h) * p.max_blocks + j) * MAX_ROWS + r] =
-                make_float2(rm[mt][hr], l);
-        }
-      continue;
-    }
-
-    // ---- pass 2: token scores of block j = column sums over all rows
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float v = cs[i][e];
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 16);
-        if (g == 0) colsum[warp][i * 8 + 2 * t + e] = v;
-      }
-    __syncthreads();
-    if (tid < BS) {
-      float v = 0.0f;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) v += colsum[w][tid];
-      tscore[tid] = v;
-      if (p.token_scores) {
-        const int tok = j * BS + tid;
-        p.token_scores[((size_t)b * p.H_kv + h) * p.max_blocks * BS + tok] = tok < n ? v : 0.0f;
-      }
-    }
-    __syncthreads();
-    // reps exist for full blocks only: the num_reps best tokens (ties: lower
-    // index), emitted in token order
-    if ((j + 1) * BS <= n && page_ok) {
-      // warp 0 takes the best token R times (score descending, then index
-      // ascending): lane l holds tokens l, l+32, l+64, l+96
-      if (warp == 0) {
-        float v[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = tscore[lane + 32 * k];
-        unsigned int taken = 0u;
-#pragma unroll 1
-        for (int rr = 0; rr < p.R; ++rr) {
-          float bv = -INFINITY;
-          int bi = 0x7fffffff;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int idx = lane + 32 * k;
-            if (!((taken >> k) & 1u) && (v[k] > bv || (v[k] == bv && idx < bi))) {
-              bv = v[k];
-              bi = idx;
+            for (int e = 0; e < 32; ++e) {
+              const int tok = j * BS + c0 + e;
+              v[e] = (row_ok && tok < n && tok <= pos) ? v[e] : -INFINITY;
             }
           }
+          float cm[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-              bv = ov;
-              bi = oi;
+          for (int e = 4; e < 32; ++e) cm[e & 3] = fmaxf(cm[e & 3], v[e]);
+          const float cmax = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3])) * p.scale_log2;
+          const float mn = fmaxf(m, cmax);
+          if (mn != -INFINITY) {
+            float sm4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sm4[e & 3] += exp2f(fmaf(v[e], p.scale_log2, -mn));
+            l = l * exp2f(m - mn) + ((sm4[0] + sm4[1]) + (sm4[2] + sm4[3]));
+            m = mn;
+          }
+        }
+        p.stats[(((size_t)b * p.H_kv + h) * p.max_blocks + j) * MAX_ROWS + r] = make_float2(m, l);
+      } else {
+        const int t = quarter * 32 + lane, tok = j * BS + t;  // this thread's token
+        const bool tok_ok = page_ok && tok < n;
+        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        // tcgen05.ld is warp-collective: every lane loads, masks apply after.
+        // exp2(s - M_r) / L_r = exp2(s - rowC[r]) with rowC = M + log2 L
+        // (+inf for rows without tokens)
+        for (int c0 = 0; c0 < BS; c0 += 32) {
+          float v[32];
+          tmem_ld32(dt + c0, v);
+          const float4* rc = reinterpret_cast<const float4*>(rowC + half * 128 + c0);
+          if (whole) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const float4 c = rc[e >> 2];
+              acc4[0] += exp2f(fmaf(v[e], p.scale_log2, -c.x));
+              acc4[1] += exp2f(fmaf(v[e + 1], p.scale_log2, -c.y));
+              acc4[2] += exp2f(fmaf(v[e + 2], p.scale_log2, -c.z));
+              acc4[3] += exp2f(fmaf(v[e + 3], p.scale_log2, -c.w));
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int r = half * 128 + c0 + e;
+              const int pos = rowPos[r];
+              if (tok_ok && pos >= 0 && tok <= pos)
+                acc4[e & 3] += exp2f(fmaf(v[e], p.scale_log2, -rowC[r]));
             }
           }
-          if (bi < BS && (bi & 31) == lane) taken |= 1u << (bi >> 5);
         }
+        const float acc = tok_ok ? (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]) : 0.0f;
+        part[half][t] = acc;
+      }
+      // this warp is done with the TMEM buffer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tfree + 8 * buf);
+      if (p.pass == 2) {
+        named_bar_sync(1, TC_EPI_WARPS * 32);
+        if (tid < BS) {
+          const float v = part[0][tid] + part[1][tid];
+          tscore[tid] = v;
+          if (p.token_scores)
+            p.token_scores[((size_t)b * p.H_kv + h) * p.max_blocks * BS + j * BS + tid] =
+                (j * BS + tid < n) ? v : 0.0f;
+        }
+        named_bar_sync(1, TC_EPI_WARPS * 32);
+        // reps exist for full blocks only: the num_reps best tokens (score
+        // descending, then index ascending), emitted in token order
+        if ((j + 1) * BS <= n && page_ok) {
+          if (warp == 0) {
+            float v[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) pick[lane + 32 * k] = (taken >> k) & 1u;
-      }
-      __syncthreads();
-      if (tid < BS && pick[tid]) {
-        int order = 0;
-        for (int u = 0; u < tid; ++u) order += pick[u];
-        pick[tid] = 1 + order;  // 1-based output slot
-      }
-      __syncthreads();
-      // copy the chosen rows: warp w copies tokens w, w+8, ... (16 lanes x 16 B)
-      for (int tk = warp; tk < BS; tk += 8) {
-        const int slot = pick[tk];
-        if (slot && lane < 16) {
-          const uint4* src =
-              reinterpret_cast<const uint4*>(p.k_pool + (((size_t)page * p.H_kv + h) * BS + tk) * D);
-          uint4* dst = reinterpret_cast<uint4*>(
-              p.reps + (((size_t)page * p.H_kv + h) * p.R + (slot - 1)) * D);
-          dst[lane] = __ldg(src + lane);
+            for (int k = 0; k < 4; ++k) v[k] = tscore[lane + 32 * k];
+            unsigned int taken = 0u;
+            for (int rr = 0; rr < p.R; ++rr) {
+              float bv = -INFINITY;
+              int bi = 0x7fffffff;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int idx = lane + 32 * k;
+                if (!((taken >> k) & 1u) && (v[k] > bv || (v[k] == bv && idx < bi))) {
+                  bv = v[k];
+                  bi = idx;
+                }
+              }
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                  bv = ov;
+                  bi = oi;
+                }
+              }
+              if (bi < BS && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+            }
+            // output slot = chosen tokens before this one (token order)
+            unsigned int before = 0u;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const unsigned int bal = __ballot_sync(0xffffffffu, (taken >> k) & 1u);
+              const int slot = (int)before + __popc(bal & ((1u << lane) - 1u));
+              pick[lane + 32 * k] = ((taken >> k) & 1u) ? slot + 1 : 0;
+              before += __popc(bal);
+            }
+          }
+          named_bar_sync(1, TC_EPI_WARPS * 32);
+          // copy the chosen rows: warp w copies tokens w, w+8, ... (16 lanes x 16 B)
+          for (int tk = warp; tk < BS; tk += TC_EPI_WARPS) {
+            const int slot = pick[tk];
+            if (slot && lane < 16) {
+              const uint4* src = reinterpret_cast<const uint4*>(
+                  p.k_pool + (((size_t)page * p.H_kv + h) * BS + tk) * D);
+              uint4* dst = reinterpret_cast<uint4*>(
+                  p.reps + (((size_t)page * p.H_kv + h) * p.R + (slot - 1)) * D);
+              dst[lane] = __ldg(src + lane);
+            }
+          }
+          named_bar_sync(1, TC_EPI_WARPS * 32);
         }
       }
-      __syncthreads();
     }
+  }
+  // all tcgen05 work of this CTA has completed once every epilogue warp has
+  // seen its last commit; then the accumulators are released
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
   }
 }
 
@@ -413,9 +411,8 @@ cudaError_t launch_dynamic(const DynLaunch& a, cudaStream_t stream) {
   p.first_block = a.first_block;
   p.num_blocks = a.num_blocks;
   p.scale_log2 = a.scale_log2;
-  const int smem = KBUF_BYTES * 2 + 1024;
-  cudaError_t e = cudaFuncSetAttribute(dyn_pass_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(dyn_pass_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
   if (e != cudaSuccess) return e;
   // slices per (KV head, sequence) so that the grid covers the SMs a few times
   int slices = (2 * a.num_sms + a.B * a.H_kv - 1) / (a.B * a.H_kv);
@@ -424,12 +421,12 @@ cudaError_t launch_dynamic(const DynLaunch& a, cudaStream_t stream) {
   p.nslices = slices;
   const dim3 grid(slices, a.H_kv, a.B);
   p.pass = 1;
-  dyn_pass_kernel<<<grid, THREADS, smem, stream>>>(p);
+  dyn_pass_tc_kernel<<<grid, TC_THREADS, TC_SMEM, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   dyn_combine_kernel<<<dim3(NSPLIT, a.H_kv, a.B), MAX_ROWS, 0, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   p.pass = 2;
-  dyn_pass_kernel<<<grid, THREADS, smem, stream>>>(p);
+  dyn_pass_tc_kernel<<<grid, TC_THREADS, TC_SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -777,7 +777,7 @@ __device__ __forceinline__ void score_mma_smem(uint32_t sbase, int sb, int nblk,
 // split over WARPS / tiles warps and the partial sums are added through
 // red[WARPS * 16] in warp order.  All WARPS warps call it (bar syncs them).
 template <int WARPS, class Bar>
-__device__ __noinline__ void score_multi_mma_smem(uint32_t sbase, int sb, int nblk, int j0,
+__device__ __forceinline__ void score_multi_mma_smem(uint32_t sbase, int sb, int nblk, int j0,
                                                      int P, const int* pg, const __half* q_unit,
                                                      int G, int nkv, int R,
                                                      unsigned long long* keys, float* red,
