@@ -226,8 +226,8 @@ class ClockSampler:
 KERNEL_SOURCES = ("attn.cu", "select_common.cuh", "kt_internal.cuh")
 KERNEL_TRAFFIC = {
     "attn_kernel<fused step>": {
-        "bytes": 38291712 + 35584,
-        "sources_sha256": "f1e4dc221d0ef574eadcf83e2282b420ea7fba210f363d46a75be494c770f7a7"},
+        "bytes": 38288384 + 28672,
+        "sources_sha256": "1a4309cc3482a93882ecdfdf11ea80345171ddf3032527c763b73c1546edfdfb"},
 }
 
 
