@@ -1173,21 +1173,34 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
 
 }  // namespace
 
+// Per device: the shared-memory opt-in of both variants (0 = done, else the
+// error), and the resident CTAs of the fused variant per SM.
+int attn_smem_optin() {
+  static std::atomic<int> slot[KT_MAX_DEVICES];
+  return per_device_cached(slot, [] {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_BYTES);
+    return (int)e;
+  });
+}
+
 int attn_fused_max_ctas_per_sm() {
-  if (cudaFuncSetAttribute(attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           SMEM_BYTES) != cudaSuccess)
-    return 0;
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<true>, THREADS, SMEM_BYTES) !=
-      cudaSuccess)
-    return 0;
-  return n;
+  static std::atomic<int> slot[KT_MAX_DEVICES];
+  return per_device_cached(slot, [] {
+    if (attn_smem_optin() != 0) return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<true>, THREADS,
+                                                      SMEM_BYTES) != cudaSuccess)
+      return 0;
+    return n;
+  });
 }
 
 cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
-  cudaError_t e =
-      cudaFuncSetAttribute(a.fused ? attn_kernel<true> : attn_kernel<false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  const cudaError_t e = (cudaError_t)attn_smem_optin();
   if (e != cudaSuccess) return e;
   Params p;
   p.kmap = *a.kmap;

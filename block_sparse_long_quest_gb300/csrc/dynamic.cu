@@ -411,8 +411,11 @@ cudaError_t launch_dynamic(const DynLaunch& a, cudaStream_t stream) {
   p.first_block = a.first_block;
   p.num_blocks = a.num_blocks;
   p.scale_log2 = a.scale_log2;
-  cudaError_t e = cudaFuncSetAttribute(dyn_pass_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+  static std::atomic<int> optin[KT_MAX_DEVICES];
+  cudaError_t e = (cudaError_t)per_device_cached(optin, [] {
+    return (int)cudaFuncSetAttribute(dyn_pass_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     TC_SMEM);
+  });
   if (e != cudaSuccess) return e;
   // slices per (KV head, sequence) so that the grid covers the SMs a few times
   int slices = (2 * a.num_sms + a.B * a.H_kv - 1) / (a.B * a.H_kv);

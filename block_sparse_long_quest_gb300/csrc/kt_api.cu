@@ -147,7 +147,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // [rows = pages*heads*128][128 channels] fp16, boxes of 64 channels x 128 rows
 // (one block of one head, half its channels), 128-byte swizzle; the attention
 // kernel's stage size and ldmatrix addressing assume exactly this box.
-bool make_pool_map(CUtensorMap* map, const void* pool, const kt_paged_kv* kv) {
+bool encode_pool_map(CUtensorMap* map, const void* pool, const kt_paged_kv* kv) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)kv->num_pages * kv->num_kv_heads * BS};
@@ -160,11 +160,45 @@ bool make_pool_map(CUtensorMap* map, const void* pool, const kt_paged_kv* kv) {
   return r == CUDA_SUCCESS;
 }
 
+// The map depends only on the pool address and its extent: the last few are
+// kept per thread, so a decode loop encodes each pool once.
+bool make_pool_map(CUtensorMap* map, const void* pool, const kt_paged_kv* kv) {
+  struct Entry {
+    const void* pool;
+    long long rows;
+    int dev;
+    CUtensorMap map;
+  };
+  constexpr int N = 8;
+  thread_local Entry cache[N];
+  thread_local int used = 0, next = 0;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const long long rows = (long long)kv->num_pages * kv->num_kv_heads * BS;
+  for (int i = 0; i < used; ++i)
+    if (cache[i].pool == pool && cache[i].rows == rows && cache[i].dev == dev) {
+      *map = cache[i].map;
+      return true;
+    }
+  if (!encode_pool_map(map, pool, kv)) return false;
+  Entry& e = cache[next];
+  e.pool = pool;
+  e.rows = rows;
+  e.dev = dev;
+  e.map = *map;
+  next = (next + 1) % N;
+  if (used < N) ++used;
+  return true;
+}
+
 int num_sms() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return n;
+  static std::atomic<int> slot[KT_MAX_DEVICES];
+  return per_device_cached(slot, [] {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+  });
 }
 
 kt_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KT_OK : KT_ERR_CUDA; }

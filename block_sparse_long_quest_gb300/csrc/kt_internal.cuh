@@ -2,6 +2,8 @@
 // shared by the libkt translation units (not part of the public ABI).
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -407,6 +409,22 @@ __device__ __forceinline__ float key_float(uint32_t k) {
 }
 
 #endif  // __CUDACC__
+
+// ---------------------------------------------------------------------------
+// Host: a value computed once per device (the current one) and cached; the
+// launch path calls these on every step.
+// ---------------------------------------------------------------------------
+constexpr int KT_MAX_DEVICES = 64;
+template <class F>
+inline int per_device_cached(std::atomic<int> (&slot)[KT_MAX_DEVICES], F compute) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= KT_MAX_DEVICES) return compute();
+  const int v = slot[dev].load(std::memory_order_relaxed);
+  if (v != 0) return v - 1;
+  const int r = compute();
+  slot[dev].store(r + 1, std::memory_order_relaxed);
+  return r;
+}
 
 // ---------------------------------------------------------------------------
 // Launch entry points implemented in the kernel translation units.

@@ -351,9 +351,21 @@ cudaError_t launch_select(const SelectLaunch& a, cudaStream_t stream) {
   p.kk = a.plan.kk;
   p.trigger = a.trigger_dependents ? 1 : 0;
   const size_t smem = select_smem_bytes(a);
-  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)(smem > 48 * 1024 ? smem : 48 * 1024));
+  // the shared-memory opt-in only grows; it is raised when a call needs more
+  static std::atomic<int> optin[KT_MAX_DEVICES];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const int want = (int)(smem > 48 * 1024 ? smem : 48 * 1024);
+  if (dev < 0 || dev >= KT_MAX_DEVICES || optin[dev].load(std::memory_order_relaxed) < want) {
+    e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < KT_MAX_DEVICES) {
+      int cur = optin[dev].load(std::memory_order_relaxed);
+      while (cur < want && !optin[dev].compare_exchange_weak(cur, want)) {
+      }
+    }
+  }
   const dim3 grid(a.plan.nchunks, a.plan.SEL, a.B);
   select_kernel<<<grid, THREADS, smem, stream>>>(p);
   return cudaGetLastError();
