@@ -476,6 +476,20 @@ def main():
     extra["rep_build_128k_quest"] = {"us": t_rb / n_rb * 1e6,
                                      "gbs": rb_bytes / (t_rb / n_rb) / 1e9,
                                      "bytes": rb_bytes}
+    # ---- dense decode over all 131072 tokens (the full scan the method avoids):
+    # the attention kernel alone on K/V of every token, layers rotated
+    n_d = 200
+    dense_fns = []
+    for L in layers:
+        vL = L.variants[rep]
+        ws_d = kt.workspace(kt.KT_OP_DENSE_ATTN, L.kv, vL["params"])
+        dense_fns.append(lambda L=L, vL=vL, ws_d=ws_d: kt.kt_dense_decode_attn(
+            L.q, L.kv, w0.params.num_q_heads, w0.params.softmax_scale, vL["out"], ws_d))
+    t_d = graph_time(dense_fns, n_d, args.warmup, stream)
+    d_bytes = int(w0.seq_lens.sum()) * w0.num_kv_heads * D * 2 * 2
+    extra["dense_128k"] = {"us": t_d / n_d * 1e6, "gbs": d_bytes / (t_d / n_d) / 1e9,
+                           "frac_of_hbm_peak": d_bytes / (t_d / n_d) / 1e9 / peak,
+                           "bytes": d_bytes, "l2_note": f"{n_layers} layers rotated"}
 
     # ---- 1M-token leg: 4 layers back to back, Quest and Max reps
     if world == 1 and not args.no_1m:

@@ -83,6 +83,13 @@ def lib():
         L.orc_score_select_attend.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64]
         L.orc_sparse_step.restype = ctypes.c_int
         L.orc_sparse_step.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, i64, i64]
+        L.orc_sparse_step_presel.restype = ctypes.c_int
+        L.orc_sparse_step_presel.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, i64, i64, vp,
+                                             vp, i64]
+        L.orc_avg_pool1d.restype = None
+        L.orc_avg_pool1d.argtypes = [vp, i64, i64, vp]
+        L.orc_preselect.restype = ctypes.c_int
+        L.orc_preselect.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp]
         _lib = L
     return _lib
 
@@ -222,6 +229,54 @@ def sparse_step(kv: KV, q, p, q_local=None, *, units=None, want_reps=True,
         raise ValueError("oracle rejected the parameters")
     return dict(reps=reps_f32 if p.rep == REP_MEAN else reps_h16, unit_scores=us, sel=sel,
                 cnt=cnt, out=out, dyn_scores=dyn)
+
+
+def avg_pool1d(x, kernel: int) -> np.ndarray:
+    """Zero-padded average pooling, window kernel (odd), stride 1 [LC §4.6]."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty_like(x)
+    lib().orc_avg_pool1d(x.ctypes.data, x.size, kernel, out.ctypes.data)
+    return out
+
+
+def preselect(kv: KV, p, q_local, kernel: int, count: int):
+    """Preselected context blocks per unit [LC §4.4, §4.6 preselect_block()]:
+    (presel [B][SEL][count] ascending, -1 padded; presel_cnt [B][SEL])."""
+    pp = params(p)
+    SEL = 1 if p.head_mode == HEAD_SHARED else kv.H_kv
+    ql = np.ascontiguousarray(q_local, dtype=np.uint16)
+    presel = np.full((kv.B, SEL, count), -1, dtype=np.int32)
+    pcnt = np.zeros((kv.B, SEL), dtype=np.int32)
+    rc = lib().orc_preselect(ctypes.byref(kv.s), ctypes.byref(pp), ql.ctypes.data, ql.shape[1],
+                             kernel, count, presel.ctypes.data, pcnt.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle rejected the preselection parameters")
+    return presel, pcnt
+
+
+def sparse_step_presel(kv: KV, q, p, presel, presel_cnt, q_local=None, *, units=None):
+    """sparse_step with each unit's selection restricted to its preselected
+    blocks; returns sel, cnt, out, unit_scores."""
+    pp = params(p)
+    B, d, MB = kv.B, kv.d, kv.max_blocks
+    SEL = 1 if p.head_mode == HEAD_SHARED else kv.H_kv
+    lo, hi = (0, SEL) if units is None else units
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    ql = None if q_local is None else np.ascontiguousarray(q_local, dtype=np.uint16)
+    T = 0 if ql is None else ql.shape[1]
+    presel = np.ascontiguousarray(presel, dtype=np.int32)
+    pcnt = np.ascontiguousarray(presel_cnt, dtype=np.int32)
+    us = np.full((B, SEL, MB), np.nan, dtype=np.float64)
+    sel = np.full((B, SEL, max(p.top_k, 1)), -1, dtype=np.int32)
+    cnt = np.zeros((B, SEL), dtype=np.int32)
+    out = np.zeros((B, p.num_q_heads, d), dtype=np.float64)
+    rc = lib().orc_sparse_step_presel(ctypes.byref(kv.s), q.ctypes.data, ctypes.byref(pp),
+                                      _ptr(ql), T, us.ctypes.data, sel.ctypes.data,
+                                      cnt.ctypes.data, out.ctypes.data, lo, hi,
+                                      presel.ctypes.data, pcnt.ctypes.data, presel.shape[-1])
+    if rc != 0:
+        raise ValueError("oracle rejected the parameters")
+    return dict(unit_scores=us, sel=sel, cnt=cnt, out=out)
 
 
 class StepTimer:

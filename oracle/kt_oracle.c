@@ -28,6 +28,13 @@
  *     partial, block; with nb <= I + L every block is attended.
  *   - SHARED sums per-head block scores over all query heads; SEPARATE sums over
  *     the query heads of one KV head (GQA group).
+ *   - Preselection [LC §4.4, §4.6]: the vote of a context token is its
+ *     accumulated softmax probability over the unit's local query rows (the
+ *     Dynamic token scores, summed over the unit's KV heads); "pool1d" is an
+ *     average pool with zero padding (odd kernel, padding kernel/2, stride 1)
+ *     over the context tokens; a block is preselected when its tokens come
+ *     first in descending pooled vote, i.e. the top `count` blocks by their
+ *     largest pooled vote.
  *   - Fix and Dynamic score a block by the max over its reps of q.rep.
  *   - Fix takes tokens 0, s, 2s, ... of the block.
  *   - Mean is the exact mean rounded once to binary32.
@@ -420,9 +427,14 @@ int orc_build_all_reps(const orc_kv* kv, const orc_params* p, const uint16_t* q_
   return 0;
 }
 
-int orc_score_select_attend(const orc_kv* kv, const uint16_t* q, const orc_params* p,
-                            const double* rv, double* unit_scores, int32_t* sel, int32_t* cnt,
-                            double* out, int64_t unit_lo, int64_t unit_hi) {
+/* Score, select and attend; with presel (non-NULL) the selection of unit u
+ * of sequence b only considers the presel_cnt[b*SEL+u] blocks listed at
+ * presel[(b*SEL+u)*presel_stride ...] (the preselection of [LC §4.4]). */
+int orc_score_select_attend_presel(const orc_kv* kv, const uint16_t* q, const orc_params* p,
+                                   const double* rv, double* unit_scores, int32_t* sel,
+                                   int32_t* cnt, double* out, int64_t unit_lo, int64_t unit_hi,
+                                   const int32_t* presel, const int32_t* presel_cnt,
+                                   int64_t presel_stride) {
   const int64_t B = kv->B, H_kv = kv->H_kv, d = kv->d, bs = kv->bs, MB = kv->max_blocks;
   const int64_t H_q = p->H_q, G = H_q / H_kv, R = orc_reps_per_block(p, bs);
   const int64_t SEL = p->head_mode == ORC_SHARED ? 1 : H_kv;
@@ -452,7 +464,27 @@ int orc_score_select_attend(const orc_kv* kv, const uint16_t* q, const orc_param
         for (int64_t j = 0; j < MB; ++j)
           unit_scores[(b * SEL + u) * MB + j] = (j >= c0 && j < c1) ? score[j - c0] : NAN;
       int32_t* su = sel + (b * SEL + u) * p->top_k;
-      int64_t cu = orc_select(score, c0, c1 - c0, p->top_k, su);
+      int64_t cu;
+      if (presel) {
+        /* only the preselected context blocks compete */
+        const int32_t* ps = presel + (b * SEL + u) * presel_stride;
+        const int64_t np = presel_cnt[b * SEL + u];
+        scored* v = (scored*)malloc(sizeof(scored) * (size_t)(np > 0 ? np : 1));
+        int64_t m2 = 0;
+        for (int64_t i = 0; i < np; ++i)
+          if (ps[i] >= c0 && ps[i] < c1) {
+            v[m2].s = score[ps[i] - c0];
+            v[m2].j = ps[i];
+            ++m2;
+          }
+        qsort(v, (size_t)m2, sizeof(scored), by_score_then_block);
+        cu = p->top_k < m2 ? p->top_k : m2;
+        for (int64_t i = 0; i < cu; ++i) su[i] = (int32_t)v[i].j;
+        qsort(su, (size_t)cu, sizeof(int32_t), ascending_i32);
+        free(v);
+      } else {
+        cu = orc_select(score, c0, c1 - c0, p->top_k, su);
+      }
       cnt[b * SEL + u] = (int32_t)cu;
       /* token set = Initial + selected Context + Local [LC §4.2] */
       int64_t m = 0;
@@ -470,6 +502,76 @@ int orc_score_select_attend(const orc_kv* kv, const uint16_t* q, const orc_param
   return 0;
 }
 
+int orc_score_select_attend(const orc_kv* kv, const uint16_t* q, const orc_params* p,
+                            const double* rv, double* unit_scores, int32_t* sel, int32_t* cnt,
+                            double* out, int64_t unit_lo, int64_t unit_hi) {
+  return orc_score_select_attend_presel(kv, q, p, rv, unit_scores, sel, cnt, out, unit_lo,
+                                        unit_hi, NULL, NULL, 0);
+}
+
+/* ---- preselection [LC §4.4; §4.6 preselect_block()] ----------------------------
+ * Average pooling along a vector with zero padding: out[t] = (sum of in[u] for
+ * u in [t - kernel/2, t + kernel/2] inside [0, n)) / kernel, kernel odd. */
+void orc_avg_pool1d(const double* in, int64_t n, int64_t kernel, double* out) {
+  const int64_t half = kernel / 2;
+  for (int64_t t = 0; t < n; ++t) {
+    double s = 0.0;
+    for (int64_t u = t - half; u <= t + half; ++u)
+      if (u >= 0 && u < n) s += in[u];
+    out[t] = s / (double)kernel;
+  }
+}
+
+/* The vote of each context token of a unit is its accumulated softmax
+ * probability over the unit's local query rows (the Dynamic token scores of
+ * each of the unit's KV heads, summed over those heads); votes are
+ * average-pooled along the context tokens; tokens are taken in descending
+ * pooled vote and their blocks collected until `count` distinct context blocks
+ * are preselected.  Taking tokens in that order reaches each block at its
+ * largest pooled vote, so this equals the top `count` blocks by (largest
+ * pooled vote of its tokens desc, block asc).  Writes presel[(b*SEL+u)*count ..]
+ * ascending and presel_cnt[b*SEL+u] = min(count, C). */
+int orc_preselect(const orc_kv* kv, const orc_params* p, const uint16_t* q_local, int64_t T,
+                  int64_t kernel, int64_t count, int32_t* presel, int32_t* presel_cnt) {
+  const int64_t B = kv->B, H_kv = kv->H_kv, bs = kv->bs, H_q = p->H_q, d = kv->d;
+  const int64_t SEL = p->head_mode == ORC_SHARED ? 1 : H_kv;
+  if (kernel < 1 || (kernel % 2) == 0 || count < 1 || T < 1 || H_q % H_kv != 0) return -1;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t n = kv->seq_lens[b];
+    int64_t nb, c0, c1;
+    orc_partition(n, bs, p->initial_blocks, p->local_blocks, &nb, &c0, &c1);
+    const int64_t C = c1 - c0, ntok = C * bs;
+    double* acc = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    double* vote = (double*)calloc((size_t)(ntok > 0 ? ntok : 1), sizeof(double));
+    double* pooled = (double*)malloc(sizeof(double) * (size_t)(ntok > 0 ? ntok : 1));
+    double* bscore = (double*)malloc(sizeof(double) * (size_t)(C > 0 ? C : 1));
+    const uint16_t* qb = q_local + b * T * H_q * d;
+    for (int64_t u = 0; u < SEL; ++u) {
+      for (int64_t t = 0; t < ntok; ++t) vote[t] = 0.0;
+      const int64_t h0 = p->head_mode == ORC_SHARED ? 0 : u;
+      const int64_t h1 = p->head_mode == ORC_SHARED ? H_kv : u + 1;
+      for (int64_t h = h0; h < h1; ++h) {
+        orc_dynamic_token_scores(kv, b, h, p, qb, T, acc);
+        for (int64_t t = 0; t < ntok; ++t) vote[t] += acc[c0 * bs + t];
+      }
+      orc_avg_pool1d(vote, ntok, kernel, pooled);
+      for (int64_t j = 0; j < C; ++j) {
+        double m = -INFINITY;
+        for (int64_t t = 0; t < bs; ++t)
+          if (pooled[j * bs + t] > m) m = pooled[j * bs + t];
+        bscore[j] = m;
+      }
+      presel_cnt[b * SEL + u] =
+          (int32_t)orc_select(bscore, c0, C, count, presel + (b * SEL + u) * count);
+    }
+    free(acc);
+    free(vote);
+    free(pooled);
+    free(bscore);
+  }
+  return 0;
+}
+
 int orc_sparse_step(const orc_kv* kv, const uint16_t* q, const orc_params* p,
                     const uint16_t* q_local, int64_t T, uint16_t* reps_h16, float* reps_f32,
                     double* dyn_scores, double* unit_scores, int32_t* sel, int32_t* cnt,
@@ -479,6 +581,23 @@ int orc_sparse_step(const orc_kv* kv, const uint16_t* q, const orc_params* p,
   double* rv = (double*)calloc((size_t)(kv->B * kv->max_blocks * kv->H_kv * R * kv->d), sizeof(double));
   int rc = orc_build_all_reps(kv, p, q_local, T, rv, reps_h16, reps_f32, dyn_scores, unit_lo, unit_hi);
   if (rc == 0) rc = orc_score_select_attend(kv, q, p, rv, unit_scores, sel, cnt, out, unit_lo, unit_hi);
+  free(rv);
+  return rc;
+}
+
+/* orc_sparse_step with the selection restricted to a preselection. */
+int orc_sparse_step_presel(const orc_kv* kv, const uint16_t* q, const orc_params* p,
+                           const uint16_t* q_local, int64_t T, double* unit_scores, int32_t* sel,
+                           int32_t* cnt, double* out, int64_t unit_lo, int64_t unit_hi,
+                           const int32_t* presel, const int32_t* presel_cnt,
+                           int64_t presel_stride) {
+  const int64_t R = orc_reps_per_block(p, kv->bs);
+  if (check_args(kv, p, q_local, T)) return -1;
+  double* rv = (double*)calloc((size_t)(kv->B * kv->max_blocks * kv->H_kv * R * kv->d), sizeof(double));
+  int rc = orc_build_all_reps(kv, p, q_local, T, rv, NULL, NULL, NULL, unit_lo, unit_hi);
+  if (rc == 0)
+    rc = orc_score_select_attend_presel(kv, q, p, rv, unit_scores, sel, cnt, out, unit_lo,
+                                        unit_hi, presel, presel_cnt, presel_stride);
   free(rv);
   return rc;
 }

@@ -425,3 +425,78 @@ def test_dynamic_scores_zero_queries_closed_form():
     want = np.array([G * sum(1.0 / (p + 1) for p in pos if p >= t) for t in range(n)])
     assert np.allclose(acc, want, rtol=1e-12)
     assert acc.sum() == pytest.approx(T * G, rel=1e-12)
+
+
+# --------------------------------------------------------------------------- preselection
+
+@pytest.mark.parametrize("k", [1, 3, 5])
+def test_avg_pool_closed_forms(k):
+    # a unit impulse spreads 1/k over the k positions around it; a constant c
+    # stays c where the window fits and loses the padded part at the ends
+    n, c = 23, 2.5
+    x = np.zeros(n)
+    x[10] = 1.0
+    got = oracle.avg_pool1d(x, k)
+    want = np.zeros(n)
+    want[10 - k // 2:10 + k // 2 + 1] = 1.0 / k
+    assert np.allclose(got, want, rtol=0, atol=1e-15)
+    got = oracle.avg_pool1d(np.full(n, c), k)
+    inside = [min(k, t + k // 2 + 1, n - t + k // 2) for t in range(n)]
+    assert np.allclose(got, c * np.array(inside) / k, rtol=1e-15)
+
+
+def test_preselect_one_query_no_pooling_is_top_blocks_by_max_logit():
+    # T = 1, G = 1, kernel 1: the vote is one softmax row over the tokens the
+    # last query sees, monotone in the logit, so the preselected blocks are the
+    # context blocks with the largest maximum logit (ties: lower block)
+    n = 128 * 12 + 40
+    w = synth.custom(41, [n], num_q_heads=1, num_kv_heads=1, rep=synth.REP_QUEST,
+                     local_queries=1, initial_blocks=1, local_blocks=2)
+    kv = oracle.KV.of(w)
+    presel, pcnt = oracle.preselect(kv, w.params, w.q_local, kernel=1, count=4)
+    K = logical_keys(kv, 0, 0)
+    logits = K @ decode(w.q_local[0, 0, 0])
+    nb = (n + 127) // 128
+    c0, c1 = 1, nb - 2
+    best = {j: logits[j * 128:(j + 1) * 128].max() for j in range(c0, c1)}
+    want = sorted(sorted(best, key=lambda j: (-best[j], j))[:4])
+    assert pcnt[0, 0] == 4 and list(presel[0, 0]) == want
+
+
+def test_preselect_count_covers_all_context_blocks():
+    w = synth.custom(42, [128 * 9 + 5, 128 * 6], num_q_heads=4, num_kv_heads=2,
+                     rep=synth.REP_QUEST, head_mode=synth.HEAD_SEPARATE, local_queries=8,
+                     initial_blocks=1, local_blocks=2)
+    kv = oracle.KV.of(w)
+    presel, pcnt = oracle.preselect(kv, w.params, w.q_local, kernel=5, count=64)
+    for b, n in enumerate(w.seq_lens):
+        nb = (int(n) + 127) // 128
+        ctx = list(range(1, nb - 2))
+        for u in range(2):
+            assert pcnt[b, u] == len(ctx)
+            assert list(presel[b, u, :len(ctx)]) == ctx
+
+
+def test_step_restricted_to_everything_equals_unrestricted_step():
+    w = synth.custom(43, [128 * 20 + 7, 128 * 11], num_q_heads=8, num_kv_heads=2,
+                     rep=synth.REP_QUEST, head_mode=synth.HEAD_SHARED, top_k=3,
+                     local_queries=4)
+    kv = oracle.KV.of(w)
+    ref = oracle.sparse_step(kv, w.q, w.params, w.q_local)
+    presel, pcnt = oracle.preselect(kv, w.params, w.q_local, kernel=3, count=1000)
+    got = oracle.sparse_step_presel(kv, w.q, w.params, presel, pcnt, w.q_local)
+    assert np.array_equal(got["sel"], ref["sel"]) and np.array_equal(got["cnt"], ref["cnt"])
+    assert np.array_equal(got["out"], ref["out"])
+
+
+def test_step_restricted_selection_is_top_k_of_the_preselection():
+    w = synth.custom(44, [128 * 30 + 3], num_q_heads=8, num_kv_heads=2, rep=synth.REP_MAX,
+                     head_mode=synth.HEAD_SEPARATE, top_k=3, local_queries=4)
+    kv = oracle.KV.of(w)
+    presel, pcnt = oracle.preselect(kv, w.params, w.q_local, kernel=5, count=6)
+    got = oracle.sparse_step_presel(kv, w.q, w.params, presel, pcnt, w.q_local)
+    for u in range(2):
+        cand = presel[0, u, :pcnt[0, u]]
+        sc = got["unit_scores"][0, u]
+        want = sorted(sorted(cand, key=lambda j: (-sc[j], j))[:3])
+        assert got["cnt"][0, u] == 3 and list(got["sel"][0, u, :3]) == want
