@@ -23,7 +23,7 @@ KT_ERR_TIMEOUT = 6
 KT_REP_MAX, KT_REP_MEAN, KT_REP_QUEST, KT_REP_FIX, KT_REP_DYNAMIC = 0, 1, 2, 3, 4
 KT_HEAD_SHARED, KT_HEAD_SEPARATE = 0, 1
 (KT_OP_SCORE_SELECT, KT_OP_SPARSE_ATTN, KT_OP_DENSE_ATTN, KT_OP_SPARSE_STEP,
- KT_OP_DYNAMIC_REPS) = 0, 1, 2, 3, 4
+ KT_OP_DYNAMIC_REPS, KT_OP_PRESELECT) = 0, 1, 2, 3, 4, 5
 
 # Every symbol declared in include/kt.h.
 EXPORTS = (
@@ -32,6 +32,8 @@ EXPORTS = (
     "kt_score_select_blocks", "kt_sparse_decode_attn", "kt_sparse_decode_step",
     "kt_sparse_decode_step_host", "kt_dense_decode_attn", "kt_read_device_status",
     "kt_selftest_bounded_wait", "kt_sparse_decode_attn_noalloc", "kt_sparse_decode_step_kernels",
+    "kt_preselect_mask_words", "kt_preselect_blocks", "kt_score_select_blocks_presel",
+    "kt_sparse_decode_step_presel",
 )
 
 
@@ -82,6 +84,13 @@ def _load():
         "kt_sparse_decode_step": (ctypes.c_int, [vp, P(PagedKV), vp, P(SparseParams), vp, vp,
                                                  vp, vp, sz, vp]),
         "kt_sparse_decode_step_kernels": (i32, [P(PagedKV), P(SparseParams)]),
+        "kt_preselect_mask_words": (i32, [P(PagedKV)]),
+        "kt_preselect_blocks": (ctypes.c_int, [P(PagedKV), P(SparseParams), vp, i32, i32, i32,
+                                               vp, vp, vp, sz, vp]),
+        "kt_score_select_blocks_presel": (ctypes.c_int, [vp, P(PagedKV), vp, P(SparseParams),
+                                                         vp, vp, vp, vp, vp, sz, vp]),
+        "kt_sparse_decode_step_presel": (ctypes.c_int, [vp, P(PagedKV), vp, P(SparseParams),
+                                                        vp, vp, vp, vp, vp, vp, sz, vp]),
         "kt_sparse_decode_step_host": (ctypes.c_int, [vp, vp, P(PagedKV), vp, P(SparseParams),
                                                       vp, vp, vp, vp, vp, sz, vp]),
         "kt_dense_decode_attn": (ctypes.c_int, [vp, P(PagedKV), i32, ctypes.c_float, vp, vp, sz,
@@ -179,6 +188,39 @@ def kt_build_dynamic_reps(kv, params, q_local, T, first_block, num_blocks, reps_
                                      first_block, num_blocks, _ptr(reps_pool),
                                      _ptr(token_scores), _ptr(ws), ws.numel(), _stream(stream)),
            "kt_build_dynamic_reps")
+
+
+def kt_preselect_mask_words(kv):
+    n = lib.kt_preselect_mask_words(ctypes.byref(kv))
+    if n < 0:
+        raise KtError(-n, "kt_preselect_mask_words")
+    return n
+
+
+def kt_preselect_blocks(kv, params, q_local, T, kernel_size, count, presel_mask, presel_cnt, ws,
+                        stream=None):
+    _check(lib.kt_preselect_blocks(ctypes.byref(kv), ctypes.byref(params), _ptr(q_local), T,
+                                   kernel_size, count, _ptr(presel_mask), _ptr(presel_cnt),
+                                   _ptr(ws), ws.numel(), _stream(stream)),
+           "kt_preselect_blocks")
+
+
+def kt_score_select_blocks_presel(q, kv, reps_pool, params, presel_mask, sel, cnt, sel_scores,
+                                  ws, stream=None):
+    _check(lib.kt_score_select_blocks_presel(_ptr(q), ctypes.byref(kv), _ptr(reps_pool),
+                                             ctypes.byref(params), _ptr(presel_mask), _ptr(sel),
+                                             _ptr(cnt), _ptr(sel_scores), _ptr(ws), ws.numel(),
+                                             _stream(stream)),
+           "kt_score_select_blocks_presel")
+
+
+def kt_sparse_decode_step_presel(q, kv, reps_pool, params, presel_mask, presel_cnt, sel, cnt,
+                                 out, ws, stream=None):
+    _check(lib.kt_sparse_decode_step_presel(_ptr(q), ctypes.byref(kv), _ptr(reps_pool),
+                                            ctypes.byref(params), _ptr(presel_mask),
+                                            _ptr(presel_cnt), _ptr(sel), _ptr(cnt), _ptr(out),
+                                            _ptr(ws), ws.numel(), _stream(stream)),
+           "kt_sparse_decode_step_presel")
 
 
 def kt_score_select_blocks(q, kv, reps_pool, params, sel, cnt, sel_scores, ws, stream=None):

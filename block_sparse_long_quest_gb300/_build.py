@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkt.so")
-SOURCES = ["kt_api.cu", "attn.cu", "select.cu", "reps.cu", "dynamic.cu"]
+SOURCES = ["kt_api.cu", "attn.cu", "select.cu", "reps.cu", "dynamic.cu", "preselect.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

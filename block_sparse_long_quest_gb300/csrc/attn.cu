@@ -93,6 +93,9 @@ struct Params {
   int* f_polled;
   int32_t* sel_out;
   int32_t* cnt_out;
+  const uint32_t* presel_mask;
+  const int32_t* presel_cnt;
+  int mask_words;
 };
 
 struct Part {
@@ -361,10 +364,36 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
   if (ctid == 0) mbar_arrive(bar_scored);  // the producer may start its own loads
   // the slice's best min(nloc, kk_f) keys, written in descending key order
   // (empty slots: key 0, page -1), then the ticket
-  const int nk = min(nloc, p.kk_f);
   unsigned long long* cand = p.f_cand + ((size_t)u * p.ncpu + cs) * p.kk_f;
   int* cpage = p.f_cand_pages + ((size_t)u * p.ncpu + cs) * p.kk_f;
-  if (nloc > p.kk_f) {
+  bool few = nloc <= p.kk_f;  // every key of the slice is a candidate
+  if (p.presel_mask) {
+    // preselection: blocks outside it get key 0, the empty slot; with at most
+    // kk_f real keys left they are all candidates
+    const uint32_t* mk = p.presel_mask + (size_t)u * p.mask_words;
+    int real = 0;
+#pragma unroll 1
+    for (int i = ctid; i < nloc; i += NCT) {
+      const int j = js + i;
+      if (!((__ldg(mk + (j >> 5)) >> (j & 31)) & 1u)) keys[i] = 0ull;
+      else ++real;
+    }
+    real = selc::warp_sum_int(real);
+    if (ctid == 0) sh_int[3] = 0;
+    bar_c();
+    if (lane == 0) atomicAdd(&sh_int[3], real);
+    bar_c();
+    few = few || sh_int[3] <= p.kk_f;
+  }
+  // slots not written below stay empty (keys of equal value share a rank, and
+  // empty keys are never written)
+#pragma unroll 1
+  for (int i = ctid; i < p.kk_f; i += NCT) {
+    cand[i] = 0ull;
+    cpage[i] = -1;
+  }
+  bar_c();
+  if (!few) {
     selc::topk_sorted<NCT>(keys, nloc, p.kk_f,
                            reinterpret_cast<unsigned long long*>(scr + Ls.bkey),
                            reinterpret_cast<int*>(scr + Ls.bidx),
@@ -374,18 +403,18 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
                              cpage[r] = pgs[i];
                            });
   } else {
-    if (ctid == 0 && (nk & 1)) keys[nk] = 0ull;
+    const int npad = (nloc + 1) & ~1;
+    if (ctid == 0 && (nloc & 1)) keys[nloc] = 0ull;
     bar_c();
 #pragma unroll 1
-    for (int i = ctid; i < p.kk_f; i += NCT) {
-      if (i < nk) {
-        const unsigned long long key = keys[i];
-        const int r = selc::count_greater(keys, (nk + 1) & ~1, key);
-        cand[r] = key;
-        cpage[r] = pgs[i];
-      } else {
-        cand[i] = 0ull;
-        cpage[i] = -1;
+    for (int i = ctid; i < nloc; i += NCT) {
+      const unsigned long long key = keys[i];
+      if (key != 0ull) {
+        const int r = selc::count_greater(keys, npad, key);
+        if (r < p.kk_f) {
+          cand[r] = key;
+          cpage[r] = pgs[i];
+        }
       }
     }
   }
@@ -411,7 +440,8 @@ __device__ int fused_merge(const Params& p, uint8_t* scr, unsigned int* hist,
                            int ncta, int ctid, Bar bar_c) {
   const int unit = b * p.SEL + (p.SEL == 1 ? 0 : h);
   const Part pt = partition(seq_len(p, b), p.I_b, p.L_b);
-  const int keff = min(p.top_k, pt.c1 - pt.c0);
+  int keff = min(p.top_k, pt.c1 - pt.c0);
+  if (p.presel_mask) keff = min(keff, max(0, __ldg(p.presel_cnt + unit)));
   if (ctid == 0) {
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 0;; ++i) {
@@ -1239,6 +1269,9 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   p.f_polled = a.f_polled;
   p.sel_out = a.sel_out;
   p.cnt_out = a.cnt_out;
+  p.presel_mask = a.presel_mask;
+  p.presel_cnt = a.presel_cnt;
+  p.mask_words = a.mask_words;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);

@@ -123,9 +123,17 @@ WsLayout layout(kt_op op, const kt_paged_kv* kv, const kt_sparse_params* p, int 
   const size_t sel_end = off;
   (void)T;
   L.dyn = off;
-  L.dyn_bytes = op == KT_OP_DYNAMIC_REPS ? dynamic_ws_bytes(B, H_kv, kv->max_blocks_per_seq) : 0;
+  L.dyn_bytes = (op == KT_OP_DYNAMIC_REPS || op == KT_OP_PRESELECT)
+                    ? dynamic_ws_bytes(B, H_kv, kv->max_blocks_per_seq)
+                    : 0;
   off = align256(off + L.dyn_bytes);
-  L.total = op == KT_OP_DENSE_ATTN ? attn_end : (op == KT_OP_DYNAMIC_REPS ? off : sel_end);
+  const int SELp = p->head_mode == KT_HEAD_SHARED ? 1 : H_kv;
+  L.presel_votes = off;
+  L.presel_bscore = off + align256((size_t)B * H_kv * kv->max_blocks_per_seq * BS * 4);
+  if (op == KT_OP_PRESELECT) off += preselect_ws_bytes(B, H_kv, SELp, kv->max_blocks_per_seq);
+  L.total = op == KT_OP_DENSE_ATTN ? attn_end
+            : (op == KT_OP_DYNAMIC_REPS || op == KT_OP_PRESELECT) ? off
+                                                                   : sel_end;
   return L;
 }
 
@@ -208,10 +216,15 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
+int mask_words_of(const kt_paged_kv* kv) { return (kv->max_blocks_per_seq + 31) / 32; }
+
 kt_status select_impl(const void* q, const kt_paged_kv* kv, const void* reps,
                       const kt_sparse_params* p, int32_t* sel, int32_t* cnt, float* sel_scores,
-                      void* ws, const WsLayout& L, bool trigger, cudaStream_t stream) {
+                      void* ws, const WsLayout& L, bool trigger, cudaStream_t stream,
+                      const uint32_t* presel_mask = nullptr) {
   SelectLaunch a;
+  a.presel_mask = presel_mask;
+  a.mask_words = mask_words_of(kv);
   a.q = static_cast<const __half*>(q);
   a.reps = reps;
   a.table = kv->block_table;
@@ -242,11 +255,12 @@ kt_status select_impl(const void* q, const kt_paged_kv* kv, const void* reps,
 }
 
 // step_path: the selection ran in this call on this workspace, so its page ids
-// (sel_pages) and counts (min(top_k, C)) are used directly.
+// (sel_pages) are used directly, and its counts are min(top_k, C) unless
+// counts_vary (a preselection can leave fewer candidates; cnt is then read).
 kt_status attn_impl(const void* q, const kt_paged_kv* kv, int num_q_heads, float scale,
                     const kt_sparse_params* p, const int32_t* sel, const int32_t* cnt, float* out,
                     void* ws, const WsLayout& L, bool dense, bool pdl, cudaStream_t stream,
-                    bool step_path = false) {
+                    bool step_path = false, bool counts_vary = false) {
   CUtensorMap kmap, vmap;
   if (!make_pool_map(&kmap, kv->k_pool, kv) || !make_pool_map(&vmap, kv->v_pool, kv))
     return KT_ERR_CUDA;
@@ -260,7 +274,7 @@ kt_status attn_impl(const void* q, const kt_paged_kv* kv, int num_q_heads, float
   a.table = kv->block_table;
   a.seq_lens = kv->seq_lens;
   a.sel = sel;
-  a.cnt = step_path ? nullptr : cnt;
+  a.cnt = (step_path && !counts_vary) ? nullptr : cnt;
   a.sel_pages = step_path ? at<int32_t>(ws, L.sel_pages) : nullptr;
   a.out = out;
   a.status = at<int>(ws, L.status);
@@ -319,7 +333,7 @@ size_t kt_reps_pool_bytes(const kt_paged_kv* kv, const kt_sparse_params* p) {
 kt_status kt_workspace_bytes(kt_op op, const kt_paged_kv* kv, const kt_sparse_params* p,
                              int32_t T, size_t* bytes) {
   if (!bytes) return KT_ERR_INVALID_ARG;
-  if (op < KT_OP_SCORE_SELECT || op > KT_OP_DYNAMIC_REPS) return KT_ERR_INVALID_ARG;
+  if (op < KT_OP_SCORE_SELECT || op > KT_OP_PRESELECT) return KT_ERR_INVALID_ARG;
   kt_status s = check_kv(kv);
   if (s != KT_OK) return s;
   if (op == KT_OP_DENSE_ATTN) {
@@ -436,6 +450,96 @@ kt_status kt_score_select_blocks(const void* q, const kt_paged_kv* kv, const voi
                      (cudaStream_t)stream);
 }
 
+kt_status kt_score_select_blocks_presel(const void* q, const kt_paged_kv* kv,
+                                        const void* reps_pool, const kt_sparse_params* p,
+                                        const uint32_t* presel_mask, int32_t* sel, int32_t* cnt,
+                                        float* sel_scores, void* ws, size_t ws_bytes,
+                                        kt_stream_t stream) {
+  kt_status s = check_kv(kv);
+  if (s != KT_OK) return s;
+  s = check_params(kv, p);
+  if (s != KT_OK) return s;
+  if (!q || !reps_pool || !sel || !cnt || !ws || !presel_mask || !aligned16(q) ||
+      !aligned16(reps_pool) || !aligned16(ws))
+    return KT_ERR_INVALID_ARG;
+  const WsLayout L = layout(KT_OP_SCORE_SELECT, kv, p, 0);
+  if (ws_bytes < L.total) return KT_ERR_WORKSPACE_TOO_SMALL;
+  return select_impl(q, kv, reps_pool, p, sel, cnt, sel_scores, ws, L, false,
+                     (cudaStream_t)stream, presel_mask);
+}
+
+int32_t kt_preselect_mask_words(const kt_paged_kv* kv) {
+  if (!kv || kv->max_blocks_per_seq < 1) return -(int32_t)KT_ERR_INVALID_ARG;
+  return mask_words_of(kv);
+}
+
+kt_status kt_preselect_blocks(const kt_paged_kv* kv, const kt_sparse_params* p,
+                              const void* q_local, int32_t T, int32_t kernel_size, int32_t count,
+                              uint32_t* presel_mask, int32_t* presel_cnt, void* ws,
+                              size_t ws_bytes, kt_stream_t stream) {
+  kt_status s = check_kv(kv);
+  if (s != KT_OK) return s;
+  s = check_params(kv, p);
+  if (s != KT_OK) return s;
+  if (!q_local || !presel_mask || !presel_cnt || !ws || !aligned16(q_local) || !aligned16(ws))
+    return KT_ERR_INVALID_ARG;
+  if (T < 1 || count < 1 || kernel_size < 1 || (kernel_size % 2) == 0)
+    return KT_ERR_INVALID_ARG;
+  if (kernel_size > PRESEL_MAX_KERNEL) return KT_ERR_UNSUPPORTED;
+  const int G = p->num_q_heads / kv->num_kv_heads;
+  if ((long long)T * G > MAX_DYN_ROWS) return KT_ERR_UNSUPPORTED;
+  const int mw = mask_words_of(kv);
+  if (preselect_smem_bytes(kv->max_blocks_per_seq, mw) > 200 * 1024) return KT_ERR_UNSUPPORTED;
+  const WsLayout L = layout(KT_OP_PRESELECT, kv, p, T);
+  if (ws_bytes < L.total) return KT_ERR_WORKSPACE_TOO_SMALL;
+  CUtensorMap kmap;
+  if (!make_pool_map(&kmap, kv->k_pool, kv)) return KT_ERR_CUDA;
+  const int sms = num_sms();
+  if (sms <= 0) return KT_ERR_CUDA;
+  // token votes: the Dynamic passes without representatives
+  float* votes = at<float>(ws, L.presel_votes);
+  DynLaunch d;
+  d.kmap = &kmap;
+  d.k_pool = static_cast<const __half*>(kv->k_pool);
+  d.q_local = static_cast<const __half*>(q_local);
+  d.table = kv->block_table;
+  d.seq_lens = kv->seq_lens;
+  d.ws = at<uint8_t>(ws, L.dyn);
+  d.reps = nullptr;
+  d.token_scores = votes;
+  d.status = at<int>(ws, L.status);
+  d.B = kv->batch;
+  d.H_kv = kv->num_kv_heads;
+  d.G = G;
+  d.T = T;
+  d.max_blocks = kv->max_blocks_per_seq;
+  d.P = kv->num_pages;
+  d.R = 0;
+  d.first_block = 0;
+  d.num_blocks = kv->max_blocks_per_seq;
+  d.num_sms = sms;
+  d.scale_log2 = (float)((double)p->softmax_scale * 1.4426950408889634);
+  cudaError_t e = launch_dynamic(d, (cudaStream_t)stream);
+  if (e != cudaSuccess) return KT_ERR_CUDA;
+  PreselLaunch a;
+  a.votes = votes;
+  a.seq_lens = kv->seq_lens;
+  a.bscore = at<float>(ws, L.presel_bscore);
+  a.mask = presel_mask;
+  a.cnt = presel_cnt;
+  a.status = at<int>(ws, L.status);
+  a.B = kv->batch;
+  a.H_kv = kv->num_kv_heads;
+  a.SEL = p->head_mode == KT_HEAD_SHARED ? 1 : kv->num_kv_heads;
+  a.max_blocks = kv->max_blocks_per_seq;
+  a.I_b = p->initial_blocks;
+  a.L_b = p->local_blocks;
+  a.kernel = kernel_size;
+  a.count = count;
+  a.mask_words = mw;
+  return cuda_status(launch_preselect(a, (cudaStream_t)stream));
+}
+
 kt_status kt_sparse_decode_attn(const void* q, const kt_paged_kv* kv, const kt_sparse_params* p,
                                 const int32_t* sel, const int32_t* cnt, float* out, void* ws,
                                 size_t ws_bytes, kt_stream_t stream) {
@@ -503,9 +607,13 @@ int32_t kt_sparse_decode_step_kernels(const kt_paged_kv* kv, const kt_sparse_par
   return (sms > 0 && fused_plan(kv, p, sms, &ncpu, &chunk, &kk)) ? 1 : 2;
 }
 
-kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void* reps_pool,
-                                const kt_sparse_params* p, int32_t* sel, int32_t* cnt,
-                                float* out, void* ws, size_t ws_bytes, kt_stream_t stream) {
+namespace kt {
+namespace {
+
+kt_status step_impl(const void* q, const kt_paged_kv* kv, const void* reps_pool,
+                    const kt_sparse_params* p, const uint32_t* presel_mask,
+                    const int32_t* presel_cnt, int32_t* sel, int32_t* cnt, float* out, void* ws,
+                    size_t ws_bytes, kt_stream_t stream) {
   kt_status s = check_kv(kv);
   if (s != KT_OK) return s;
   s = check_params(kv, p);
@@ -559,12 +667,35 @@ kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void
     a.f_polled = at<int>(ws, L.f_polled);
     a.sel_out = sel;
     a.cnt_out = cnt;
+    a.presel_mask = presel_mask;
+    a.presel_cnt = presel_cnt;
+    a.mask_words = mask_words_of(kv);
     return cuda_status(launch_attention(a, (cudaStream_t)stream));
   }
-  s = select_impl(q, kv, reps_pool, p, sel, cnt, nullptr, ws, L, true, (cudaStream_t)stream);
+  s = select_impl(q, kv, reps_pool, p, sel, cnt, nullptr, ws, L, true, (cudaStream_t)stream,
+                  presel_mask);
   if (s != KT_OK) return s;
   return attn_impl(q, kv, p->num_q_heads, p->softmax_scale, p, sel, cnt, out, ws, L, false, true,
-                   (cudaStream_t)stream, true);
+                   (cudaStream_t)stream, true, presel_mask != nullptr);
+}
+
+}  // namespace
+}  // namespace kt
+
+kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void* reps_pool,
+                                const kt_sparse_params* p, int32_t* sel, int32_t* cnt,
+                                float* out, void* ws, size_t ws_bytes, kt_stream_t stream) {
+  return step_impl(q, kv, reps_pool, p, nullptr, nullptr, sel, cnt, out, ws, ws_bytes, stream);
+}
+
+kt_status kt_sparse_decode_step_presel(const void* q, const kt_paged_kv* kv,
+                                       const void* reps_pool, const kt_sparse_params* p,
+                                       const uint32_t* presel_mask, const int32_t* presel_cnt,
+                                       int32_t* sel, int32_t* cnt, float* out, void* ws,
+                                       size_t ws_bytes, kt_stream_t stream) {
+  if (!presel_mask || !presel_cnt) return KT_ERR_INVALID_ARG;
+  return step_impl(q, kv, reps_pool, p, presel_mask, presel_cnt, sel, cnt, out, ws, ws_bytes,
+                   stream);
 }
 
 kt_status kt_sparse_decode_step_host(const void* q_host, void* q_dev, const kt_paged_kv* kv,

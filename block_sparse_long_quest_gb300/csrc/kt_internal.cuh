@@ -108,6 +108,8 @@ struct WsLayout {
   size_t attn_parts;     // float [2*(MAX_ATTN_CTAS+S)][slot_floats]
   size_t dyn;            // dynamic-rep scratch
   size_t dyn_bytes;
+  size_t presel_votes;   // preselection: token votes [B][H_kv][max_blocks*128] fp32
+  size_t presel_bscore;  // preselection: block scores [B][SEL][max_blocks] fp32
   size_t total;
   int slot_floats;
   SelPlan sel;
@@ -459,6 +461,9 @@ struct AttnLaunch {
   int* f_polled;    // [B*SEL] CTAs past each unit's ticket wait, zero between launches
   int32_t* sel_out;
   int32_t* cnt_out;
+  const uint32_t* presel_mask;  // nullable [B][SEL][mask_words]
+  const int32_t* presel_cnt;    // with presel_mask: blocks preselected per unit
+  int mask_words;
 };
 int attn_fused_max_ctas_per_sm();
 cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream);
@@ -479,6 +484,8 @@ struct SelectLaunch {
   int B, H_kv, G, max_blocks, P, I_b, L_b, top_k, rep, R, head_mode;
   SelPlan plan;
   bool trigger_dependents;
+  const uint32_t* presel_mask;  // nullable: only these Context blocks compete
+  int mask_words;
 };
 cudaError_t launch_select(const SelectLaunch& a, cudaStream_t stream);
 size_t select_smem_bytes(const SelectLaunch& a);
@@ -508,6 +515,20 @@ struct DynLaunch {
 cudaError_t launch_dynamic(const DynLaunch& a, cudaStream_t stream);
 size_t dynamic_ws_bytes(int B, int H_kv, int max_blocks);
 constexpr int MAX_DYN_ROWS = 256;  // local queries x query heads per KV head
+
+struct PreselLaunch {
+  const float* votes;  // [B][H_kv][max_blocks*128] token scores (Dynamic passes)
+  const int32_t* seq_lens;
+  float* bscore;       // workspace [B][SEL][max_blocks]
+  uint32_t* mask;      // [B][SEL][mask_words]
+  int32_t* cnt;        // [B][SEL]
+  int* status;
+  int B, H_kv, SEL, max_blocks, I_b, L_b, kernel, count, mask_words;
+};
+cudaError_t launch_preselect(const PreselLaunch& a, cudaStream_t stream);
+size_t preselect_ws_bytes(int B, int H_kv, int SEL, int max_blocks);
+size_t preselect_smem_bytes(int max_blocks, int mask_words);
+constexpr int PRESEL_MAX_KERNEL = 65;
 
 cudaError_t launch_selftest_wait(int* status, int spin_limit, cudaStream_t stream);
 

@@ -52,6 +52,8 @@ struct Params {
   int B, H_kv, G, max_blocks, P, I_b, L_b, top_k, rep, R, head_mode;
   int SEL, chunk, nchunks, kk;
   int trigger;
+  const uint32_t* presel_mask;  // nullable [B][SEL][mask_words]
+  int mask_words;
 };
 
 __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__ Params p) {
@@ -182,6 +184,15 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
       }
     }
     __syncthreads();
+    // preselection: blocks outside it get key 0, the empty slot
+    if (p.presel_mask) {
+      const uint32_t* mk = p.presel_mask + unit_base * p.mask_words;
+      for (int i = tid; i < nloc; i += THREADS) {
+        const int j = js + i;
+        if (!((__ldg(mk + (j >> 5)) >> (j & 31)) & 1u)) keys[i] = 0ull;
+      }
+      __syncthreads();
+    }
 
     // ---- this chunk's top-kk candidates; unused slots hold key 0, which is
     // below every real key
@@ -195,10 +206,14 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const __grid_constant__
       selc::radix_select<THREADS>(keys, nloc, p.kk, hist, sh_u64, sh_int, &prefix, &mask, tid,
                                     [] { __syncthreads(); });
       if (tid == 0) sh_int[2] = 0;
+      for (int i = tid; i < p.kk; i += THREADS) {  // slots left empty stay key 0
+        my_cand[i] = 0ull;
+        my_pages[i] = -1;
+      }
       __syncthreads();
       for (int i = tid; i < nloc; i += THREADS) {
         const unsigned long long key = keys[i];
-        if ((key & mask) >= prefix) {
+        if (key != 0ull && (key & mask) >= prefix) {
           const int pos = atomicAdd(&sh_int[2], 1);
           if (pos < p.kk) {
             my_cand[pos] = key;
@@ -350,6 +365,8 @@ cudaError_t launch_select(const SelectLaunch& a, cudaStream_t stream) {
   p.nchunks = a.plan.nchunks;
   p.kk = a.plan.kk;
   p.trigger = a.trigger_dependents ? 1 : 0;
+  p.presel_mask = a.presel_mask;
+  p.mask_words = a.mask_words;
   const size_t smem = select_smem_bytes(a);
   // the shared-memory opt-in only grows; it is raised when a call needs more
   static std::atomic<int> optin[KT_MAX_DEVICES];

@@ -78,7 +78,8 @@ typedef enum {
   KT_OP_SPARSE_ATTN = 1,
   KT_OP_DENSE_ATTN = 2,
   KT_OP_SPARSE_STEP = 3,   /* score/select + sparse attention in one call */
-  KT_OP_DYNAMIC_REPS = 4
+  KT_OP_DYNAMIC_REPS = 4,
+  KT_OP_PRESELECT = 5      /* kt_preselect_blocks (needs T like KT_OP_DYNAMIC_REPS) */
 } kt_op;
 
 /*
@@ -150,7 +151,7 @@ size_t kt_reps_pool_bytes(const kt_paged_kv* kv, const kt_sparse_params* p);
 /*
  * Workspace bytes needed by `op` for these shapes (host-only computation; no
  * device is touched).  T is the number of local queries for
- * KT_OP_DYNAMIC_REPS and is ignored otherwise.  The workspace holds the device
+ * KT_OP_DYNAMIC_REPS and KT_OP_PRESELECT and is ignored otherwise.  The workspace holds the device
  * status word, cross-CTA candidate lists, tickets and split-K partials.  It must
  * be zero-filled before its first use (kt_workspace_init); every call leaves it
  * ready for the next.  Calls that share one workspace must not overlap on the
@@ -250,6 +251,47 @@ kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void
  * a negative kt_status value for invalid arguments.  Host only, no launch.
  */
 int32_t kt_sparse_decode_step_kernels(const kt_paged_kv* kv, const kt_sparse_params* p);
+
+/*
+ * Preselection [LC §4.4 "预选择 Preselect", §4.6 preselect_block()]: before
+ * decoding, pick per selection unit a fixed set of Context blocks from the
+ * attention of the last T prompt positions; later selections choose only
+ * among them (the preselect_block / preselect_block_count keys of [HOWTO]
+ * Step 1).  The vote of a Context token is its accumulated softmax probability
+ * over the unit's local query rows (T positions x the query heads of each of
+ * the unit's KV heads, causal), votes are average-pooled along the Context
+ * tokens (window kernel_size, odd, <= 65, zero padding kernel_size/2, stride
+ * 1), and the `count` blocks whose tokens rank first by pooled vote are
+ * preselected, i.e. the top `count` blocks by their largest pooled vote
+ * (ties: lower block).
+ *   q_local     : fp16 [batch][T][num_q_heads][128] (as kt_build_dynamic_reps)
+ *   presel_mask : uint32 [batch][SEL][kt_preselect_mask_words(kv)], bit j%32 of
+ *                 word j/32 set when logical block j is preselected
+ *   presel_cnt  : int32 [batch][SEL], min(count, C)
+ * Workspace: KT_OP_PRESELECT with the same T.  T*G <= 256.
+ */
+int32_t kt_preselect_mask_words(const kt_paged_kv* kv);
+kt_status kt_preselect_blocks(const kt_paged_kv* kv, const kt_sparse_params* p,
+                              const void* q_local, int32_t T, int32_t kernel_size, int32_t count,
+                              uint32_t* presel_mask, int32_t* presel_cnt, void* ws,
+                              size_t ws_bytes, kt_stream_t stream);
+
+/*
+ * kt_score_select_blocks and kt_sparse_decode_step with each unit's choice
+ * restricted to its preselected blocks (presel_mask / presel_cnt as written by
+ * kt_preselect_blocks): the top min(top_k, presel_cnt) preselected blocks by
+ * unit score.  Same workspaces as the unrestricted calls.
+ */
+kt_status kt_score_select_blocks_presel(const void* q, const kt_paged_kv* kv,
+                                        const void* reps_pool, const kt_sparse_params* p,
+                                        const uint32_t* presel_mask, int32_t* sel, int32_t* cnt,
+                                        float* sel_scores, void* ws, size_t ws_bytes,
+                                        kt_stream_t stream);
+kt_status kt_sparse_decode_step_presel(const void* q, const kt_paged_kv* kv,
+                                       const void* reps_pool, const kt_sparse_params* p,
+                                       const uint32_t* presel_mask, const int32_t* presel_cnt,
+                                       int32_t* sel, int32_t* cnt, float* out, void* ws,
+                                       size_t ws_bytes, kt_stream_t stream);
 
 /*
  * The same step for callers whose query and output live in HOST memory:
