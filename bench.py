@@ -523,6 +523,7 @@ def main():
         torch.cuda.empty_cache()
     if world == 1 and not args.no_dynamic:
         extra["at_dynamic_128k"] = dynamic_leg(args, stream)
+        extra["preselect_128k"] = preselect_leg(args, stream)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -590,6 +591,45 @@ def dynamic_leg(args, stream):
             "rep_build_k_bytes_read": 2 * int(L.k.numel()) * 2,
             "step_us": t_s / n_s * 1e6, "step_gbs": b["total"] / (t_s / n_s) / 1e9,
             "step_bytes": b["total"], "l2_note": "one layer repeated (touched set fits L2)"}
+
+
+def preselect_leg(args, stream):
+    """Preselection at 128K (the 96 blocks of the pages' YAML, pool window 5,
+    64 local queries): its one-off cost, and the Quest SHARED top-32 step
+    restricted to it."""
+    import torch
+
+    import block_sparse_long_quest_gb300 as kt
+    w = synth.dynamic128k()
+    w.params.rep = synth.REP_QUEST
+    L = Layer(w)
+    v = L.variants[synth.REP_QUEST]
+    q_local = torch.from_numpy(w.q_local.view(np.int16)).view(torch.float16).cuda()
+    T = w.q_local.shape[1]
+    SEL = 1 if w.params.head_mode == synth.HEAD_SHARED else w.num_kv_heads
+    mw = kt.kt_preselect_mask_words(L.kv)
+    mask = torch.zeros((w.batch, SEL, mw), dtype=torch.int32, device="cuda")
+    pcnt = torch.zeros((w.batch, SEL), dtype=torch.int32, device="cuda")
+    ws_p = kt.workspace(kt.KT_OP_PRESELECT, L.kv, v["params"], T)
+    run_p = lambda: kt.kt_preselect_blocks(L.kv, v["params"], q_local, T, 5, 96, mask, pcnt, ws_p)
+    n_p = 10
+    t_p = graph_time([run_p], n_p, 3, stream)
+    if kt.kt_read_device_status(ws_p) != kt.KT_OK:
+        raise RuntimeError("device status after preselection")
+    step = lambda: kt.kt_sparse_decode_step_presel(L.q, L.kv, v["reps"], v["params"], mask, pcnt,
+                                                   v["sel"], v["cnt"], v["out"], v["ws"])
+    n_s = 2000
+    t_s = graph_time([step], n_s, args.warmup, stream)
+    # algorithmic bytes: reps of the 96 candidates + K/V of the attended tokens
+    b = step_bytes(w)
+    R = w.params.reps_per_block()
+    cand = int(pcnt.sum().item())
+    reps_b = cand * w.num_kv_heads * R * D * 2
+    total = b["kv"] + reps_b
+    return {"workload": "128k-gqa4-quest-shared-k32, preselect 96 blocks (pool 5, 64 local queries)",
+            "preselect_us": t_p / n_p * 1e6, "step_us": t_s / n_s * 1e6,
+            "step_gbs": total / (t_s / n_s) / 1e9, "step_bytes": total,
+            "note": "the restricted step still scores every Context block; only the 96 compete"}
 
 
 def layers_q_bytes(w):
