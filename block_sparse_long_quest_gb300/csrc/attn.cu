@@ -330,6 +330,11 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     };
     issue(0);
     if (nrounds > 1) issue(1);
+    // fp16 reps: a few blocks on the CUDA cores (whole columns per thread),
+    // many on the tensor cores, whose B fragments replace the weights in place
+    const int lin_max = 8 * CONSUMERS / (V <= 32 ? 1 : V <= 64 ? 2 : V <= 128 ? 4 : 8);
+    const bool use_mma = !multi && !f32 && nloc > lin_max;
+    if (use_mma) selc::weights_to_frags<NCT>(wts, V * 8, ctid, bar_c);
 #pragma unroll 1
     for (int r = 0; r < nrounds; ++r) {
       const int r0 = r * rcap, nr = min(rcap, nloc - r0);
@@ -337,6 +342,7 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
       const uint32_t base = ring_u32 + buf_off(r);
       const uint4* sbuf = reinterpret_cast<const uint4*>(ring + buf_off(r));
 #define KT_SCORE(NV, F) selc::score_linear_smem<NV, F, CONSUMERS>(sbuf, (int)(sb / 16), nr, js + r0, p.P, pgs + r0, wts, V, keys + r0, warp, lane, p.status)
+#define KT_COLS(VC) selc::score_linear_cols<VC, CONSUMERS>(sbuf, (int)(sb / 16), nr, js + r0, p.P, pgs + r0, wts, keys + r0, red, warp, lane, p.status, bar_c)
       if (multi) {
         selc::score_multi_mma_smem<CONSUMERS>(
             base, (int)sb, nr, js + r0, p.P, pgs + r0,
@@ -345,18 +351,26 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
       } else if (f32) {
         fused_score_f32(sbuf, (int)(sb / 16), nr, js + r0, p.P, pgs + r0, wts, V, keys + r0, warp,
                         lane, p.status);
-      } else if (nr <= 8 * CONSUMERS / (V <= 32 ? 1 : V <= 64 ? 2 : V <= 128 ? 4 : 8)) {
+      } else if (use_mma) {
+        selc::score_mma_smem<CONSUMERS>(base, (int)sb, nr, js + r0, p.P, pgs + r0,
+                                        reinterpret_cast<const uint2*>(wts), V * 8, keys + r0,
+                                        reinterpret_cast<float*>(hist), warp, lane, p.status,
+                                        bar_c);
+      } else if (V == 256 || V == 128 || V == 64) {
+        // one pass: every thread owns one 16-byte column of the few blocks
+        float* red = reinterpret_cast<float*>(hist);
+        if (V == 256) KT_COLS(256);
+        else if (V == 128) KT_COLS(128);
+        else KT_COLS(64);
+      } else {
         // one pass of the CUDA-core path: each warp reduces its few blocks
         if (V <= 32) KT_SCORE(1, false);
         else if (V <= 64) KT_SCORE(2, false);
         else if (V <= 128) KT_SCORE(4, false);
         else KT_SCORE(8, false);
-      } else {
-        selc::score_mma_smem<CONSUMERS>(base, (int)sb, nr, js + r0, p.P, pgs + r0, wts, V * 8,
-                                        keys + r0, reinterpret_cast<float*>(hist), warp, lane,
-                                        p.status, bar_c);
       }
 #undef KT_SCORE
+#undef KT_COLS
       bar_c();  // this half is refilled by round r + 2, the ring by the producer
       if (r + 2 < nrounds) issue(r + 2);
     }

@@ -640,88 +640,188 @@ __device__ __forceinline__ void score_linear_smem(const uint4* sbuf, int sstride
   }
 }
 
+// Linear scoring of a few staged fp16 blocks on the CUDA cores, one 16-byte
+// column of the blocks' rows per thread, so the weights are read once per CTA
+// rather than once per warp.  V (64, 128 or 256) columns per block; phase
+// s = tid / V of S = 32 WARPS / V takes blocks s, s + S, ... (nblk <= 8 S).
+// Each thread forms its (up to) 8 block partials, a halving butterfly over
+// lane bits 4, 3, 2 leaves block slot (lane >> 2) in every lane, then lanes 2
+// and 1 are folded and the phase's warps added in warp order through
+// red[WARPS * 8].  All WARPS warps call it (bar syncs them).  keys[i] receives
+// block i's key with block id j0 + i.
+template <int V, int WARPS, class Bar>
+__device__ __forceinline__ void score_linear_cols(const uint4* sbuf, int sstride, int nblk, int j0,
+                                                  int P, const int* pg, const float* wts,
+                                                  unsigned long long* keys, float* red, int warp,
+                                                  int lane, int* status, Bar bar) {
+  static_assert(V == 64 || V == 128 || V == 256, "columns per block");
+  constexpr int S = WARPS * 32 / V, WP = V / 32;
+  const int tid = warp * 32 + lane;
+  const int s = tid / V, c = tid % V;
+  float w[8];
+  {
+    const float4 f0 = *reinterpret_cast<const float4*>(wts + c * 8);
+    const float4 f1 = *reinterpret_cast<const float4*>(wts + c * 8 + 4);
+    w[0] = f0.x; w[1] = f0.y; w[2] = f0.z; w[3] = f0.w;
+    w[4] = f1.x; w[5] = f1.y; w[6] = f1.z; w[7] = f1.w;
+  }
+  uint4 x[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int i = s + S * k;
+    x[k] = i < nblk ? sbuf[(size_t)i * sstride + c] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float a[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const __half2* h = reinterpret_cast<const __half2*>(&x[k]);
+    float e = 0.0f, o = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; q += 2) {
+      const float2 f = __half22float2(h[q]), g = __half22float2(h[q + 1]);
+      e = fmaf(w[2 * q], f.x, e);
+      o = fmaf(w[2 * q + 1], f.y, o);
+      e = fmaf(w[2 * q + 2], g.x, e);
+      o = fmaf(w[2 * q + 3], g.y, o);
+    }
+    a[k] = e + o;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const bool up = lane & 16;
+    const float send = up ? a[k] : a[k + 4], keep = up ? a[k + 4] : a[k];
+    a[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const bool up = lane & 8;
+    const float send = up ? a[k] : a[k + 2], keep = up ? a[k + 2] : a[k];
+    a[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  {
+    const bool up = lane & 4;
+    const float send = up ? a[0] : a[1], keep = up ? a[1] : a[0];
+    a[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  a[0] += __shfl_xor_sync(0xffffffffu, a[0], 2);
+  a[0] += __shfl_xor_sync(0xffffffffu, a[0], 1);
+  if ((lane & 3) == 0) red[warp * 8 + (lane >> 2)] = a[0];
+  bar();
+  if (tid < nblk) {
+    const int ss = tid % S, k = tid / S;
+    float v[WP];
+#pragma unroll
+    for (int q = 0; q < WP; ++q) v[q] = red[(ss * WP + q) * 8 + k];
+    float sc = v[0];
+#pragma unroll
+    for (int q = 1; q < WP; ++q) sc += v[q];
+    const int pgi = pg[tid];
+    const bool ok = pgi >= 0 && pgi < P;
+    keys[tid] = make_key(ok ? sc : -INFINITY, j0 + tid);
+    if (!ok) set_status(status, KT_ERR_DEVICE_CHECK);
+  }
+}
+
+// In place, the fp32 weights wts[K] (K a multiple of 16, at most 2048) become
+// the B fragments of score_mma_smem: the weights split into fp16 hi + lo parts
+// as B columns 0 (hi) and 1 (lo).  Fragment j of k-step ks, j = g * 4 + t
+// (g = 0 hi, 1 lo), holds the fp16 pairs of k rows (2t, 2t + 1) and
+// (2t + 8, 2t + 9) at ((uint2*)wts)[ks * 8 + j], i.e. in the same 64 bytes as
+// the k-step's 16 weights: every thread reads before the barrier and writes
+// after it.  All NT threads call it; on return the fragments are visible.
+template <int NT, class Bar>
+__device__ __forceinline__ void weights_to_frags(float* wts, int K, int tid, Bar bar) {
+  constexpr int PER = 2048 / 2 / NT;  // fragments per thread at K = 2048
+  uint2 v[PER];
+#pragma unroll
+  for (int r = 0; r < PER; ++r) {
+    const int e = tid + r * NT;
+    const int ks = e >> 3, lo = (e >> 2) & 1, t = e & 3;
+    v[r] = make_uint2(0u, 0u);
+    if (e < K / 2) {
+      const float2 wa = *reinterpret_cast<const float2*>(wts + ks * 16 + 2 * t);
+      const float2 wb = *reinterpret_cast<const float2*>(wts + ks * 16 + 2 * t + 8);
+      __half2 ha = __floats2half2_rn(wa.x, wa.y), hb = __floats2half2_rn(wb.x, wb.y);
+      const __half2 la = __floats2half2_rn(wa.x - __low2float(ha), wa.y - __high2float(ha));
+      const __half2 lb = __floats2half2_rn(wb.x - __low2float(hb), wb.y - __high2float(hb));
+      if (lo) {
+        ha = la;
+        hb = lb;
+      }
+      v[r] = make_uint2(*reinterpret_cast<const uint32_t*>(&ha), *reinterpret_cast<const uint32_t*>(&hb));
+    }
+  }
+  bar();
+#pragma unroll
+  for (int r = 0; r < PER; ++r) {
+    const int e = tid + r * NT;
+    if (e < K / 2) reinterpret_cast<uint2*>(wts)[e] = v[r];
+  }
+  bar();
+}
+
 // Linear scoring of fp16 representatives on the tensor cores.  Blocks are
 // staged in shared memory at a row stride of sb bytes (sbase, a shared-space
-// address), K fp16 values each in the order of the fp32 weights wts[K].  The
-// weights are split into fp16 hi + lo parts, which form columns 0 and 1 of the
-// B operand (the other columns are zero), so one mma.sync m16n8k16 step
-// reduces 16 blocks x 16 values into two fp32 partial sums per block; the
-// score is their sum.  Products of fp16 values are exact in fp32, and hi + lo
-// carries the weight to about 2^-22.  With many 16-block groups each warp
-// takes whole groups (w, w + WARPS, ...); with few, each group's K range is
-// split over WARPS / groups warps and the partial sums are added through
-// red[WARPS * 16] in warp order.  All WARPS warps call it (bar syncs them).
-// keys[i] receives block i's key with block id j0 + i.
+// address), K fp16 values each in the order of the weights.  The weights come
+// as the B fragments of weights_to_frags (hi + lo fp16 parts as columns 0 and
+// 1, the other columns zero), so one mma.sync m16n8k16 step reduces 16 blocks
+// x 16 values into two fp32 partial sums per block; the score is their sum.
+// Products of fp16 values are exact in fp32, and hi + lo carries the weight
+// to about 2^-22.  Each 16-row group accumulates its k-steps in two chains
+// (even, odd); every operand load is unconditional (k-steps clamped, masked
+// after), so a warp keeps eight A and B fragments in flight.  With many groups
+// each warp takes whole groups (w, w + WARPS, ...); with few, each group's K
+// range is split over WARPS / groups warps and the partial sums are added
+// through red[WARPS * 16] in warp order.  All WARPS warps call it (bar syncs
+// them).  keys[i] receives block i's key with block id j0 + i.
 template <int WARPS, class Bar>
 __device__ __forceinline__ void score_mma_smem(uint32_t sbase, int sb, int nblk, int j0, int P,
-                                               const int* pg, const float* wts, int K,
+                                               const int* pg, const uint2* wf, int K,
                                                unsigned long long* keys, float* red, int warp,
                                                int lane, int* status, Bar bar) {
-  constexpr int MAXG = 4;  // groups per warp per pass
-  constexpr int KC = 16;   // k-steps whose weight fragments are held in registers
   const int ngrp = (nblk + 15) >> 4;
   const int g = lane >> 2, t = lane & 3;
+  const bool bcol = g < 2;  // lanes holding B columns 0 and 1
   const uint32_t koff = (uint32_t)((lane >> 4) * 16);  // bytes: k offset 0 or 8
   const int nks = K / 16;
-  // weight fragments of k-steps ks0 .. ks0+kn-1 (kn <= KC): column 0 hi, 1 lo
-  auto build = [&](int ks0, int kn, uint32_t (&bf)[KC][2]) {
-#pragma unroll
-    for (int kk = 0; kk < KC; ++kk) {
-      bf[kk][0] = bf[kk][1] = 0u;
-      if (kk < kn && g < 2) {
-        const int ks = ks0 + kk;
-        const float2 wa = *reinterpret_cast<const float2*>(wts + ks * 16 + 2 * t);
-        const float2 wb = *reinterpret_cast<const float2*>(wts + ks * 16 + 2 * t + 8);
-        __half2 ha = __floats2half2_rn(wa.x, wa.y), hb = __floats2half2_rn(wb.x, wb.y);
-        if (g == 1) {
-          ha = __floats2half2_rn(wa.x - __low2float(ha), wa.y - __high2float(ha));
-          hb = __floats2half2_rn(wb.x - __low2float(hb), wb.y - __high2float(hb));
-        }
-        bf[kk][0] = *reinterpret_cast<uint32_t*>(&ha);
-        bf[kk][1] = *reinterpret_cast<uint32_t*>(&hb);
-      }
-    }
-  };
-  // acc += rows of ra (16 blocks) x weights over k-steps ks0 .. ks0+kn-1,
-  // eight A fragments in flight at a time
-  auto run = [&](uint32_t ra, int ks0, int kn, const uint32_t (&bf)[KC][2], float (&acc)[4]) {
-#pragma unroll
-    for (int h = 0; h < KC; h += 8) {
-      uint32_t a[8][4];
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        if (h + kk < kn) ldsm_x4(a[kk][0], a[kk][1], a[kk][2], a[kk][3], ra + (uint32_t)(ks0 + h + kk) * 32u);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        if (h + kk < kn)
-          mma_16816(acc, a[kk][0], a[kk][1], a[kk][2], a[kk][3], bf[h + kk][0], bf[h + kk][1]);
-    }
-  };
+  bool bad = false;
   auto emit = [&](int i, float score) {
-    const bool ok = pg[i] >= 0 && pg[i] < P;
+    const int pgi = pg[i];
+    const bool ok = pgi >= 0 && pgi < P;
     keys[i] = make_key(ok ? score : -INFINITY, j0 + i);
-    if (!ok) set_status(status, KT_ERR_DEVICE_CHECK);
+    bad |= !ok;
+  };
+  // acc (chains 0 and 1) += the 16 rows at ra x k-steps [k0, k1)
+  auto run = [&](uint32_t ra, int k0, int k1, float (&acc)[2][4]) {
+#pragma unroll 1
+    for (int ks0 = k0; ks0 < k1; ks0 += 8) {
+      uint32_t a[8][4];
+      uint2 b[8];
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int ks = min(ks0 + kk, k1 - 1);
+        ldsm_x4(a[kk][0], a[kk][1], a[kk][2], a[kk][3], ra + (uint32_t)ks * 32u);
+        const uint2 f = wf[ks * 8 + (lane & 7)];
+        const bool on = bcol && ks0 + kk < k1;
+        b[kk] = on ? f : make_uint2(0u, 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_16816_sched(acc[kk & 1], a[kk][0], a[kk][1], a[kk][2], a[kk][3], b[kk].x, b[kk].y);
+    }
   };
   if (ngrp * 2 <= WARPS) {
     // split K: warp w -> group w / ns, k-steps part w % ns of ns
     const int ns = WARPS / ngrp;
     const int grp = warp / ns, part = warp % ns;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     if (grp < ngrp) {
       const int row = min(grp * 16 + (lane & 15), nblk - 1);
-      const uint32_t ra = sbase + (uint32_t)row * (uint32_t)sb + koff;
-      const int k0 = part * nks / ns, k1 = (part + 1) * nks / ns;
-#pragma unroll 1
-      for (int ks0 = k0; ks0 < k1; ks0 += KC) {
-        uint32_t bf[KC][2];
-        const int kn = min(KC, k1 - ks0);
-        build(ks0, kn, bf);
-        run(ra, ks0, kn, bf, acc);
-      }
+      run(sbase + (uint32_t)row * (uint32_t)sb + koff, part * nks / ns, (part + 1) * nks / ns, acc);
     }
     if (t == 0) {
-      red[warp * 16 + g] = acc[0] + acc[1];
-      red[warp * 16 + g + 8] = acc[2] + acc[3];
+      red[warp * 16 + g] = (acc[0][0] + acc[0][1]) + (acc[1][0] + acc[1][1]);
+      red[warp * 16 + g + 8] = (acc[0][2] + acc[0][3]) + (acc[1][2] + acc[1][3]);
     }
     bar();
     const int tid = warp * 32 + lane;
@@ -731,39 +831,22 @@ __device__ __forceinline__ void score_mma_smem(uint32_t sbase, int sb, int nblk,
       for (int q = 0; q < ns; ++q) sc += red[(gi * ns + q) * 16 + r];
       emit(tid, sc);
     }
-    return;
-  }
+  } else {
 #pragma unroll 1
-  for (int gb = warp; gb < ngrp; gb += WARPS * MAXG) {
-    float acc[MAXG][4];
-    uint32_t rowaddr[MAXG];
-#pragma unroll
-    for (int m = 0; m < MAXG; ++m) {
-      acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.0f;
-      const int row = min((gb + m * WARPS) * 16 + (lane & 15), nblk - 1);  // past the end: ignored
-      rowaddr[m] = sbase + (uint32_t)row * (uint32_t)sb + koff;
-    }
-#pragma unroll 1
-    for (int ks0 = 0; ks0 < nks; ks0 += KC) {
-      uint32_t bf[KC][2];
-      const int kn = min(KC, nks - ks0);
-      build(ks0, kn, bf);
-#pragma unroll
-      for (int m = 0; m < MAXG; ++m)
-        if (gb + m * WARPS < ngrp) run(rowaddr[m], ks0, kn, bf, acc[m]);
-    }
-    if (t == 0) {
-#pragma unroll
-      for (int m = 0; m < MAXG; ++m) {
-        const int grp = gb + m * WARPS;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int i = grp * 16 + g + 8 * h;
-          if (grp < ngrp && i < nblk) emit(i, acc[m][2 * h] + acc[m][2 * h + 1]);
-        }
+    for (int gb = warp; gb < ngrp; gb += WARPS) {
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const int row = min(gb * 16 + (lane & 15), nblk - 1);  // past the end: ignored
+      run(sbase + (uint32_t)row * (uint32_t)sb + koff, 0, nks, acc);
+      if (t == 0) {
+        const int i0 = gb * 16 + g, i1 = i0 + 8;
+        const float s0 = (acc[0][0] + acc[0][1]) + (acc[1][0] + acc[1][1]);
+        const float s1 = (acc[0][2] + acc[0][3]) + (acc[1][2] + acc[1][3]);
+        if (i0 < nblk) emit(i0, s0);
+        if (i1 < nblk) emit(i1, s1);
       }
     }
   }
+  if (bad) set_status(status, KT_ERR_DEVICE_CHECK);
 }
 
 // Multi-representative scoring (Fix, Dynamic) on the tensor cores: the head
