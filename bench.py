@@ -226,8 +226,8 @@ class ClockSampler:
 KERNEL_SOURCES = ("attn.cu", "select_common.cuh", "kt_internal.cuh")
 KERNEL_TRAFFIC = {
     "attn_kernel<fused step>": {
-        "bytes": 38288384 + 28672,
-        "sources_sha256": "1a4309cc3482a93882ecdfdf11ea80345171ddf3032527c763b73c1546edfdfb"},
+        "bytes": 38288640 + 33280,
+        "sources_sha256": "0a76d10a89ec5c37fb012ea62c198ca27ceb225be50045f082c3e091c8c4c6d8"},
 }
 
 

@@ -288,10 +288,20 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     const int j = js + i;
     pgs[i] = j < p.max_blocks ? __ldg(p.table + (size_t)bu * p.max_blocks + j) : -1;
   }
+  // the slice's candidate slots start empty (key 0, page -1): keys of equal
+  // value share a rank and empty keys are never written, so some may stay so
+  unsigned long long* cand = p.f_cand + ((size_t)u * p.ncpu + cs) * p.kk_f;
+  int* cpage = p.f_cand_pages + ((size_t)u * p.ncpu + cs) * p.kk_f;
+#pragma unroll 1
+  for (int i = ctid; i < p.kk_f; i += NCT) {
+    cand[i] = 0ull;
+    cpage[i] = -1;
+  }
   const Part pu = partition(seq_len(p, bu), p.I_b, p.L_b);
   if (!multi) fused_weights(p, wts, bu, g0, nkv, ctid);
   const int je = min(js + p.f_chunk, pu.c1);
   const int nloc = max(0, je - js);  // js >= c0 whenever the slice is not empty
+  if (ctid == 0 && (nloc & 1)) keys[nloc] = 0ull;  // the ranking's zero padding
   bar_c();
   if (nloc > 0) {
     // the slice's representative rows, staged into the (still idle) KV ring by
@@ -378,8 +388,6 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
   if (ctid == 0) mbar_arrive(bar_scored);  // the producer may start its own loads
   // the slice's best min(nloc, kk_f) keys, written in descending key order
   // (empty slots: key 0, page -1), then the ticket
-  unsigned long long* cand = p.f_cand + ((size_t)u * p.ncpu + cs) * p.kk_f;
-  int* cpage = p.f_cand_pages + ((size_t)u * p.ncpu + cs) * p.kk_f;
   bool few = nloc <= p.kk_f;  // every key of the slice is a candidate
   if (p.presel_mask) {
     // preselection: blocks outside it get key 0, the empty slot; with at most
@@ -399,27 +407,23 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     bar_c();
     few = few || sh_int[3] <= p.kk_f;
   }
-  // slots not written below stay empty (keys of equal value share a rank, and
-  // empty keys are never written)
-#pragma unroll 1
-  for (int i = ctid; i < p.kk_f; i += NCT) {
-    cand[i] = 0ull;
-    cpage[i] = -1;
-  }
-  bar_c();
   if (!few) {
-    selc::topk_sorted<NCT>(keys, nloc, p.kk_f,
-                           reinterpret_cast<unsigned long long*>(scr + Ls.bkey),
-                           reinterpret_cast<int*>(scr + Ls.bidx),
-                           reinterpret_cast<int*>(scr + Ls.idx), hist, sh_u64, sh_int, ctid,
-                           bar_c, [&](int r, int i) {
-                             cand[r] = keys[i];
-                             cpage[r] = pgs[i];
-                           });
+    auto emit = [&](int r, int i) {
+      cand[r] = keys[i];
+      cpage[r] = pgs[i];
+    };
+    unsigned long long* ck = reinterpret_cast<unsigned long long*>(scr + Ls.bkey);
+    int* ci = reinterpret_cast<int*>(scr + Ls.bidx);
+    int* ix = reinterpret_cast<int*>(scr + Ls.idx);
+    if (nloc <= 8 * NCT)
+      selc::topk_sorted_reg<NCT>(keys, nloc, p.kk_f, ck, ci, ix, hist, sh_u64, sh_int, ctid,
+                                 bar_c, emit);
+    else
+      selc::topk_sorted<NCT>(keys, nloc, p.kk_f, ck, ci, ix, hist, sh_u64, sh_int, ctid, bar_c,
+                             emit);
   } else {
+    // with nloc odd, keys[nloc] is the zero padding
     const int npad = (nloc + 1) & ~1;
-    if (ctid == 0 && (nloc & 1)) keys[nloc] = 0ull;
-    bar_c();
 #pragma unroll 1
     for (int i = ctid; i < nloc; i += NCT) {
       const unsigned long long key = keys[i];

@@ -489,6 +489,127 @@ __device__ void topk_sorted(const unsigned long long* keys, int N, int k,
   bar();
 }
 
+// The same selection as topk_sorted for N <= 8 NT keys, with each thread's
+// keys (i = tid + r NT) held in registers: the common leading bits come from
+// warp AND / OR reductions, the digit histogram takes one shared atomic per
+// key, and every warp scans the histogram itself, so the bound needs no extra
+// barrier.  Same scratch and the same emitted ranks and indices.
+template <int NT, class Bar, class Emit>
+__device__ void topk_sorted_reg(const unsigned long long* keys, int N, int k,
+                                unsigned long long* ck, int* ci, int* idx, unsigned int* hist,
+                                unsigned long long* sh_u64, int* sh_int, int tid, Bar bar,
+                                Emit emit) {
+  constexpr int WARPS = NT / 32, PER = 8;
+  const int lane = tid & 31, warp = tid >> 5;
+  unsigned long long kx[PER];
+  uint32_t a_lo = ~0u, a_hi = ~0u, o_lo = 0u, o_hi = 0u;
+#pragma unroll
+  for (int r = 0; r < PER; ++r) {
+    const int i = tid + r * NT;
+    kx[r] = i < N ? keys[i] : 0ull;
+    if (i < N) {
+      a_lo &= (uint32_t)kx[r];
+      a_hi &= (uint32_t)(kx[r] >> 32);
+      o_lo |= (uint32_t)kx[r];
+      o_hi |= (uint32_t)(kx[r] >> 32);
+    }
+  }
+  a_lo = __reduce_and_sync(0xffffffffu, a_lo);
+  a_hi = __reduce_and_sync(0xffffffffu, a_hi);
+  o_lo = __reduce_or_sync(0xffffffffu, o_lo);
+  o_hi = __reduce_or_sync(0xffffffffu, o_hi);
+  if (lane == 0) {
+    sh_u64[2 + warp] = ((unsigned long long)a_hi << 32) | a_lo;
+    sh_u64[2 + WARPS + warp] = ((unsigned long long)o_hi << 32) | o_lo;
+  }
+#pragma unroll 1
+  for (int i = tid; i < 256; i += NT) hist[i] = 0u;
+  ck[tid] = 0ull;  // NT entries: the padding slot of the ranking
+  if (tid == 0) sh_int[0] = 0;
+  bar();
+  unsigned long long all_and = ~0ull, all_or = 0ull;
+#pragma unroll
+  for (int w = 0; w < WARPS; ++w) {
+    all_and &= sh_u64[2 + w];
+    all_or |= sh_u64[2 + WARPS + w];
+  }
+  const unsigned long long diff = all_and ^ all_or;
+  const int hi = diff ? 64 - __clzll((long long)diff) : 0;
+  const int shift = hi > 8 ? hi - 8 : 0;
+  const unsigned long long pmask = hi >= 64 ? 0ull : ~((1ull << hi) - 1);
+  const unsigned long long prefix = all_and & pmask;
+#pragma unroll
+  for (int r = 0; r < PER; ++r)
+    if (tid + r * NT < N) atomicAdd(&hist[(unsigned)((kx[r] >> shift) & 255ull)], 1u);
+  bar();
+  unsigned long long T;
+  {
+    // lane l holds digits 255-8l .. 248-8l (descending)
+    unsigned int c[8], local = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      c[i] = hist[255 - 8 * lane - i];
+      local += c[i];
+    }
+    unsigned int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const unsigned int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    const unsigned int excl = incl - local;
+    const bool hit = excl < (unsigned)k && (unsigned)k <= incl;
+    int digit = 0;
+    unsigned int above = excl;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      above += c[i];
+      if (hit && digit == 0 && above >= (unsigned)k) digit = 256 + 255 - 8 * lane - i;
+    }
+    const int src = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;
+    digit = __shfl_sync(0xffffffffu, digit, src < 0 ? 0 : src) - 256;
+    T = prefix | (static_cast<unsigned long long>(digit < 0 ? 0 : digit) << shift);
+  }
+  {
+    const unsigned int lt = (1u << lane) - 1u;
+    unsigned int bal[PER];
+    int tot = 0;
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+      bal[r] = __ballot_sync(0xffffffffu, tid + r * NT < N && kx[r] >= T);
+      tot += __popc(bal[r]);
+    }
+    int off = 0;
+    if (lane == 0 && tot) off = atomicAdd(&sh_int[0], tot);
+    off = __shfl_sync(0xffffffffu, off, 0);
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+      const int pos = off + __popc(bal[r] & lt);
+      if (((bal[r] >> lane) & 1u) && pos < NT) {
+        ck[pos] = kx[r];
+        ci[pos] = tid + r * NT;
+      }
+      off += __popc(bal[r]);
+    }
+  }
+  bar();
+  const int M = sh_int[0];
+  if (M <= NT) {
+    if (tid < M) {
+      const int r = count_greater(ck, (M + 1) & ~1, ck[tid]);
+      if (r < k) emit(r, ci[tid]);
+    }
+  } else {
+    select_top<NT>(keys, N, k, idx, ck, ci, hist, sh_u64, sh_int, tid, bar);
+#pragma unroll 1
+    for (int i = tid; i < NT; i += NT) ck[i] = i < k ? keys[idx[i]] : 0ull;
+    bar();
+#pragma unroll 1
+    for (int i = tid; i < k; i += NT) emit(count_greater(ck, (k + 1) & ~1, ck[i]), idx[i]);
+  }
+  bar();
+}
+
 // Linear scoring (Max, Mean, Quest): each warp scores 8/NV blocks at a time;
 // a lane holds NV 16-byte vectors of each block, and every load of the group is
 // issued before any arithmetic.  V = 16-byte vectors per block and unit.
