@@ -8,7 +8,7 @@
 // position pos sees tokens 0..pos.  The accumulated score of token t is
 //   acc[t] = sum over rows r with t <= pos_r of exp(s_rt - m_r) / l_r,
 // where s_rt = q_r . k_t * scale, m_r = max_t s_rt and l_r = sum_t exp(s_rt - m_r)
-// over the tokens row r sees.  Three launches:
+// over the tokens row r sees.  Four launches:
 //   pass 1   one CTA per (block slice, KV head, sequence): S = Q K^T for every
 //            block of its slice on the 5th-generation tensor cores (tcgen05,
 //            accumulators in tensor memory, K blocks by 2-D TMA into a double
@@ -17,8 +17,10 @@
 //   combine  per (split, KV head, sequence): merge the partials of a range of
 //            blocks per row.
 //   pass 2   S^T for the requested blocks; p = exp2(s - M_r) / L_r summed over
-//            rows per token; the num_reps best tokens of each full block (ties:
-//            lower index) are copied, in token order, as its reps.
+//            rows per token, written per token.
+//   pick     per (block, KV head, sequence): the num_reps best tokens of each
+//            full block (ties: lower index) are copied, in token order, as its
+//            reps.
 // The path is a dense contraction (M = T*G rows per KV head) plus one exp per
 // logit per pass; K is read twice (once per pass).
 #include "kt_internal.cuh"
@@ -40,11 +42,19 @@ struct DynParams {
   float2* stats;    // [B][H_kv][max_blocks][MAX_ROWS] (m, l) per block, base 2
   float2* split;    // [B][H_kv][NSPLIT][MAX_ROWS] combined over a block range
   __half* reps;     // [P][H_kv][R][128]
-  float* token_scores;  // nullable [B][H_kv][max_blocks*128]
+  float* token_scores;  // [B][H_kv][max_blocks*128] (the caller's or the workspace's)
   int* status;
   int B, H_kv, G, T, max_blocks, P, R, first_block, num_blocks, pass, nslices;
   float scale_log2;
 };
+
+// 2^x on the MUFU unit (PTX ex2.approx.ftz: relative error about 2^-22,
+// results below 2^-126 flushed to zero; 2^-inf = 0)
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ int seq_len_checked(const DynParams& p, int b) {
   int n = __ldg(p.seq_lens + b);
@@ -56,20 +66,22 @@ __device__ __forceinline__ int seq_len_checked(const DynParams& p, int b) {
 }
 
 // ---- tcgen05 version of the two passes ---------------------------------------
-// One CTA (8 epilogue warps + 1 control warp) per (block slice, KV head,
+// One CTA (16 epilogue warps + 1 control warp) per (block slice, KV head,
 // sequence).  The T*G query rows live in shared memory as two K-major
 // 128-byte-swizzled boxes (64 channels x 256 rows each); each K block arrives
 // by TMA as two boxes (64 channels x 128 tokens) into a double buffer.  One
 // thread issues the tcgen05.mma chains into one of two 256-column TMEM
-// accumulators:
+// accumulators.  An epilogue warp reads the TMEM lanes of its quarter
+// (warp % 4) and a quarter of the columns:
 //   pass 1  S = Q K^T, two M = 128 tiles (rows 0-127, 128-255) x N = 128
-//           tokens: a thread of the epilogue owns one row (its TMEM lane) and
-//           reduces the row's max and sum over the block's tokens itself;
+//           tokens: a thread owns one row (its TMEM lane) and half of the
+//           block's tokens; the two halves' (max, sum) meet in shared memory;
 //   pass 2  S^T = K Q^T, M = 128 tokens x N = 256 rows: a thread owns one
-//           token and sums exp2(s - M_r) / L_r over its 128 rows; the two row
-//           halves meet in shared memory.
-// The epilogue of block q overlaps the MMAs of block q + 1.
-constexpr int TC_EPI_WARPS = 8;
+//           token and sums exp2(s - M_r) / L_r over 64 of the rows; the four
+//           row quarters meet in shared memory.
+// Two or four warps meet on their own named barrier, so no warp waits for
+// the whole CTA; the epilogue of block q overlaps the MMAs of block q + 1.
+constexpr int TC_EPI_WARPS = 16;
 constexpr int TC_THREADS = (TC_EPI_WARPS + 1) * 32;
 constexpr int Q_BOX = MAX_ROWS * 128;  // 256 rows x 64 channels fp16
 constexpr int TC_SMEM = 2 * Q_BOX + 2 * KBUF_BYTES + 1024;
@@ -83,9 +95,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) dyn_pass_tc_kernel(const __grid
   __shared__ uint32_t tmem_base;
   __shared__ __align__(16) float rowC[MAX_ROWS];  // pass 2: M_r + log2 L_r
   __shared__ int rowPos[MAX_ROWS];
-  __shared__ float part[2][BS];
-  __shared__ float tscore[BS];
-  __shared__ int pick[BS];
+  __shared__ float2 pslot[2][MAX_ROWS];  // pass 1: second token half's (max, sum)
+  __shared__ float part4[2][4][BS];      // pass 2: row quarters' sums
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int slice = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -201,7 +212,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) dyn_pass_tc_kernel(const __grid
     __syncwarp();
   } else {
     // ============================ epilogue warps ============================
-    const int quarter = warp & 3, half = warp >> 2;
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     for (int q = 0; q < nmine; ++q) {
       const int buf = q & 1, j = jb + slice + q * stride;
       const bool live = mbar_wait(mdone + 8 * buf, (q >> 1) & 1, p.status);
@@ -209,22 +220,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) dyn_pass_tc_kernel(const __grid
       const int page = p.table[(size_t)b * p.max_blocks + j];
       const bool page_ok = live && page >= 0 && page < p.P;
       const bool whole = page_ok && (j + 1) * BS - 1 <= n - p.T;  // every present row sees it all
-      const uint32_t dt = tmem + (uint32_t)buf * 256u + ((uint32_t)(quarter * 32) << 16) +
-                          (uint32_t)(half * 128);
       if (p.pass == 1) {
+        const int half = (warp >> 2) & 1, cpart = warp >> 3;  // M tile, token half
+        const uint32_t dt = tmem + (uint32_t)buf * 256u + ((uint32_t)(quarter * 32) << 16) +
+                            (uint32_t)(half * 128 + cpart * 64);
         const int r = half * 128 + quarter * 32 + lane;  // this thread's row
         const int pos = rowPos[r];
         const bool row_ok = page_ok && pos >= 0;
         const bool row_whole = whole && pos >= 0;  // no token of the block is masked
         float m = -INFINITY, l = 0.0f;
         // tcgen05.ld is warp-collective: every lane loads, masks apply after
-        for (int c0 = 0; c0 < BS; c0 += 32) {
+        for (int c0 = 0; c0 < 64; c0 += 32) {
           float v[32];
           tmem_ld32(dt + c0, v);
           if (!row_whole) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              const int tok = j * BS + c0 + e;
+              const int tok = j * BS + cpart * 64 + c0 + e;
               v[e] = (row_ok && tok < n && tok <= pos) ? v[e] : -INFINITY;
             }
           }
@@ -236,112 +248,67 @@ __global__ void __launch_bounds__(TC_THREADS, 1) dyn_pass_tc_kernel(const __grid
           if (mn != -INFINITY) {
             float sm4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < 32; ++e) sm4[e & 3] += exp2f(fmaf(v[e], p.scale_log2, -mn));
-            l = l * exp2f(m - mn) + ((sm4[0] + sm4[1]) + (sm4[2] + sm4[3]));
+            for (int e = 0; e < 32; ++e) sm4[e & 3] += ex2_fast(fmaf(v[e], p.scale_log2, -mn));
+            l = l * ex2_fast(m - mn) + ((sm4[0] + sm4[1]) + (sm4[2] + sm4[3]));
             m = mn;
           }
         }
-        p.stats[(((size_t)b * p.H_kv + h) * p.max_blocks + j) * MAX_ROWS + r] = make_float2(m, l);
+        // this warp is done with the TMEM buffer
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tfree + 8 * buf);
+        // the row's two token halves meet: warps w and w + 8 share barrier 1 + w % 8
+        if (cpart == 1) pslot[buf][r] = make_float2(m, l);
+        named_bar_sync(1 + (warp & 7), 64);
+        if (cpart == 0) {
+          const float2 o = pslot[buf][r];
+          const float M = fmaxf(m, o.x);
+          const float L = M == -INFINITY ? 0.0f : l * ex2_fast(m - M) + o.y * ex2_fast(o.x - M);
+          p.stats[(((size_t)b * p.H_kv + h) * p.max_blocks + j) * MAX_ROWS + r] = make_float2(M, L);
+        }
       } else {
+        const int rq = warp >> 2;  // rows 64*rq .. +63
+        const uint32_t dt = tmem + (uint32_t)buf * 256u + ((uint32_t)(quarter * 32) << 16) +
+                            (uint32_t)(rq * 64);
         const int t = quarter * 32 + lane, tok = j * BS + t;  // this thread's token
         const bool tok_ok = page_ok && tok < n;
         float acc4[4] = {0.f, 0.f, 0.f, 0.f};
         // tcgen05.ld is warp-collective: every lane loads, masks apply after.
         // exp2(s - M_r) / L_r = exp2(s - rowC[r]) with rowC = M + log2 L
         // (+inf for rows without tokens)
-        for (int c0 = 0; c0 < BS; c0 += 32) {
+        for (int c0 = 0; c0 < 64; c0 += 32) {
           float v[32];
           tmem_ld32(dt + c0, v);
-          const float4* rc = reinterpret_cast<const float4*>(rowC + half * 128 + c0);
+          const float4* rc = reinterpret_cast<const float4*>(rowC + rq * 64 + c0);
           if (whole) {
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
               const float4 c = rc[e >> 2];
-              acc4[0] += exp2f(fmaf(v[e], p.scale_log2, -c.x));
-              acc4[1] += exp2f(fmaf(v[e + 1], p.scale_log2, -c.y));
-              acc4[2] += exp2f(fmaf(v[e + 2], p.scale_log2, -c.z));
-              acc4[3] += exp2f(fmaf(v[e + 3], p.scale_log2, -c.w));
+              acc4[0] += ex2_fast(fmaf(v[e], p.scale_log2, -c.x));
+              acc4[1] += ex2_fast(fmaf(v[e + 1], p.scale_log2, -c.y));
+              acc4[2] += ex2_fast(fmaf(v[e + 2], p.scale_log2, -c.z));
+              acc4[3] += ex2_fast(fmaf(v[e + 3], p.scale_log2, -c.w));
             }
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              const int r = half * 128 + c0 + e;
+              const int r = rq * 64 + c0 + e;
               const int pos = rowPos[r];
               if (tok_ok && pos >= 0 && tok <= pos)
-                acc4[e & 3] += exp2f(fmaf(v[e], p.scale_log2, -rowC[r]));
+                acc4[e & 3] += ex2_fast(fmaf(v[e], p.scale_log2, -rowC[r]));
             }
           }
         }
-        const float acc = tok_ok ? (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]) : 0.0f;
-        part[half][t] = acc;
-      }
-      // this warp is done with the TMEM buffer
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tfree + 8 * buf);
-      if (p.pass == 2) {
-        named_bar_sync(1, TC_EPI_WARPS * 32);
-        if (tid < BS) {
-          const float v = part[0][tid] + part[1][tid];
-          tscore[tid] = v;
-          if (p.token_scores)
-            p.token_scores[((size_t)b * p.H_kv + h) * p.max_blocks * BS + j * BS + tid] =
-                (j * BS + tid < n) ? v : 0.0f;
-        }
-        named_bar_sync(1, TC_EPI_WARPS * 32);
-        // reps exist for full blocks only: the num_reps best tokens (score
-        // descending, then index ascending), emitted in token order
-        if ((j + 1) * BS <= n && page_ok) {
-          if (warp == 0) {
-            float v[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) v[k] = tscore[lane + 32 * k];
-            unsigned int taken = 0u;
-            for (int rr = 0; rr < p.R; ++rr) {
-              float bv = -INFINITY;
-              int bi = 0x7fffffff;
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const int idx = lane + 32 * k;
-                if (!((taken >> k) & 1u) && (v[k] > bv || (v[k] == bv && idx < bi))) {
-                  bv = v[k];
-                  bi = idx;
-                }
-              }
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (ov > bv || (ov == bv && oi < bi)) {
-                  bv = ov;
-                  bi = oi;
-                }
-              }
-              if (bi < BS && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-            }
-            // output slot = chosen tokens before this one (token order)
-            unsigned int before = 0u;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const unsigned int bal = __ballot_sync(0xffffffffu, (taken >> k) & 1u);
-              const int slot = (int)before + __popc(bal & ((1u << lane) - 1u));
-              pick[lane + 32 * k] = ((taken >> k) & 1u) ? slot + 1 : 0;
-              before += __popc(bal);
-            }
-          }
-          named_bar_sync(1, TC_EPI_WARPS * 32);
-          // copy the chosen rows: warp w copies tokens w, w+8, ... (16 lanes x 16 B)
-          for (int tk = warp; tk < BS; tk += TC_EPI_WARPS) {
-            const int slot = pick[tk];
-            if (slot && lane < 16) {
-              const uint4* src = reinterpret_cast<const uint4*>(
-                  p.k_pool + (((size_t)page * p.H_kv + h) * BS + tk) * D);
-              uint4* dst = reinterpret_cast<uint4*>(
-                  p.reps + (((size_t)page * p.H_kv + h) * p.R + (slot - 1)) * D);
-              dst[lane] = __ldg(src + lane);
-            }
-          }
-          named_bar_sync(1, TC_EPI_WARPS * 32);
+        // this warp is done with the TMEM buffer
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tfree + 8 * buf);
+        // the token's four row quarters meet: warps quarter + 4i share barrier 1 + quarter
+        part4[buf][rq][t] = tok_ok ? (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]) : 0.0f;
+        named_bar_sync(1 + quarter, 128);
+        if (rq == 0) {
+          const float v = (part4[buf][0][t] + part4[buf][1][t]) + (part4[buf][2][t] + part4[buf][3][t]);
+          p.token_scores[((size_t)b * p.H_kv + h) * p.max_blocks * BS + (size_t)j * BS + t] = v;
         }
       }
     }
@@ -380,11 +347,76 @@ __global__ void __launch_bounds__(MAX_ROWS) dyn_combine_kernel(const __grid_cons
   p.split[(((size_t)b * p.H_kv + h) * NSPLIT + sp) * MAX_ROWS + r] = make_float2(M, L);
 }
 
+// Reps of the requested full blocks: one warp per (block, KV head,
+// sequence) takes the num_reps best tokens by accumulated score (descending,
+// then index ascending) and copies their key rows, in token order.
+constexpr int PICK_WARPS = 8;
+__global__ void __launch_bounds__(PICK_WARPS * 32) dyn_pick_kernel(const __grid_constant__ DynParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int jj = blockIdx.x * PICK_WARPS + warp;
+  const int n = seq_len_checked(p, b);
+  const int j = p.first_block + jj;
+  if (jj >= p.num_blocks || (j + 1) * BS > n) return;  // reps exist for full blocks only
+  const int page = p.table[(size_t)b * p.max_blocks + j];
+  if (page < 0 || page >= p.P) {
+    if (lane == 0) set_status(p.status, KT_ERR_DEVICE_CHECK);
+    return;
+  }
+  const float* sc = p.token_scores + ((size_t)b * p.H_kv + h) * p.max_blocks * BS + (size_t)j * BS;
+  float v[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) v[k] = sc[lane + 32 * k];
+  unsigned int taken = 0u;
+  for (int rr = 0; rr < p.R; ++rr) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int idx = lane + 32 * k;
+      if (!((taken >> k) & 1u) && (v[k] > bv || (v[k] == bv && idx < bi))) {
+        bv = v[k];
+        bi = idx;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (bi < BS && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+  }
+  // output slot = chosen tokens before this one (token order); a half warp
+  // copies each chosen 256-byte row
+  const uint4* src = reinterpret_cast<const uint4*>(p.k_pool + ((size_t)page * p.H_kv + h) * BS * D);
+  uint4* dst = reinterpret_cast<uint4*>(p.reps + ((size_t)page * p.H_kv + h) * p.R * D);
+  int before = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    unsigned int bal = __ballot_sync(0xffffffffu, (taken >> k) & 1u);
+    while (bal) {
+      const int l0 = __ffs(bal) - 1;
+      bal &= bal - 1u;
+      const int l1 = bal ? __ffs(bal) - 1 : -1;  // a second row for the upper half warp
+      if (l1 >= 0) bal &= bal - 1u;
+      const int mine = lane < 16 ? l0 : l1;
+      const int slot = lane < 16 ? before : before + 1;
+      if (mine >= 0) dst[(size_t)slot * (D / 8) + (lane & 15)] = __ldg(src + (size_t)(mine + 32 * k) * (D / 8) + (lane & 15));
+      before += l1 >= 0 ? 2 : 1;
+    }
+  }
+}
+
 }  // namespace
 
 size_t dynamic_ws_bytes(int B, int H_kv, int max_blocks) {
   return align256((size_t)B * H_kv * max_blocks * MAX_ROWS * sizeof(float2)) +
-         align256((size_t)B * H_kv * NSPLIT * MAX_ROWS * sizeof(float2));
+         align256((size_t)B * H_kv * NSPLIT * MAX_ROWS * sizeof(float2)) +
+         align256((size_t)B * H_kv * max_blocks * BS * sizeof(float));
 }
 
 cudaError_t launch_dynamic(const DynLaunch& a, cudaStream_t stream) {
@@ -399,7 +431,13 @@ cudaError_t launch_dynamic(const DynLaunch& a, cudaStream_t stream) {
                                       align256((size_t)a.B * a.H_kv * a.max_blocks * MAX_ROWS *
                                                sizeof(float2)));
   p.reps = static_cast<__half*>(a.reps);
-  p.token_scores = a.token_scores;
+  // token scores: the caller's array, else the workspace's
+  p.token_scores = a.token_scores
+                       ? a.token_scores
+                       : reinterpret_cast<float*>(
+                             static_cast<uint8_t*>(a.ws) +
+                             align256((size_t)a.B * a.H_kv * a.max_blocks * MAX_ROWS * sizeof(float2)) +
+                             align256((size_t)a.B * a.H_kv * NSPLIT * MAX_ROWS * sizeof(float2)));
   p.status = a.status;
   p.B = a.B;
   p.H_kv = a.H_kv;
@@ -430,7 +468,13 @@ cudaError_t launch_dynamic(const DynLaunch& a, cudaStream_t stream) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   p.pass = 2;
   dyn_pass_tc_kernel<<<grid, TC_THREADS, TC_SMEM, stream>>>(p);
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (p.R > 0 && p.reps && p.num_blocks > 0) {
+    const dim3 pg((p.num_blocks + PICK_WARPS - 1) / PICK_WARPS, a.H_kv, a.B);
+    dyn_pick_kernel<<<pg, PICK_WARPS * 32, 0, stream>>>(p);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 }  // namespace kt
