@@ -213,11 +213,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) dyn_pass_tc_kernel(const __grid
   } else {
     // ============================ epilogue warps ============================
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int* trow = p.table + (size_t)b * p.max_blocks;
+    int page_next = nmine > 0 ? trow[jb + slice] : -1;  // loaded a block ahead
     for (int q = 0; q < nmine; ++q) {
       const int buf = q & 1, j = jb + slice + q * stride;
+      const int page = page_next;
+      if (q + 1 < nmine) page_next = trow[j + stride];
       const bool live = mbar_wait(mdone + 8 * buf, (q >> 1) & 1, p.status);
       tc_fence_after();
-      const int page = p.table[(size_t)b * p.max_blocks + j];
       const bool page_ok = live && page >= 0 && page < p.P;
       const bool whole = page_ok && (j + 1) * BS - 1 <= n - p.T;  // every present row sees it all
       if (p.pass == 1) {
