@@ -226,8 +226,8 @@ class ClockSampler:
 KERNEL_SOURCES = ("attn.cu", "select_common.cuh", "kt_internal.cuh")
 KERNEL_TRAFFIC = {
     "attn_kernel<fused step>": {
-        "bytes": 38288640 + 33280,
-        "sources_sha256": "0a76d10a89ec5c37fb012ea62c198ca27ceb225be50045f082c3e091c8c4c6d8"},
+        "bytes": 38287616 + 25600,
+        "sources_sha256": "7a0c3607261c926625500148c3ce67ff816bbd3087491a437b13f511036e95a0"},
 }
 
 
