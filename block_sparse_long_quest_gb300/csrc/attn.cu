@@ -298,7 +298,6 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     cpage[i] = -1;
   }
   const Part pu = partition(seq_len(p, bu), p.I_b, p.L_b);
-  if (!multi) fused_weights(p, wts, bu, g0, nkv, ctid);
   const int je = min(js + p.f_chunk, pu.c1);
   const int nloc = max(0, je - js);  // js >= c0 whenever the slice is not empty
   if (ctid == 0 && (nloc & 1)) keys[nloc] = 0ull;  // the ranking's zero padding
@@ -340,6 +339,11 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     };
     issue(0);
     if (nrounds > 1) issue(1);
+    // the query-dependent weights are folded while the copies fly
+    if (!multi) {
+      fused_weights(p, wts, bu, g0, nkv, ctid);
+      bar_c();
+    }
     // fp16 reps: a few blocks on the CUDA cores (whole columns per thread),
     // many on the tensor cores, whose B fragments replace the weights in place
     const int lin_max = 8 * CONSUMERS / (V <= 32 ? 1 : V <= 64 ? 2 : V <= 128 ? 4 : 8);
@@ -533,27 +537,25 @@ __device__ int fused_merge(const Params& p, uint8_t* scr, unsigned int* hist,
   hist[ctid] = 0u;  // NCT == 256 bins
   {
     const int lane = ctid & 31, w = ctid >> 5;
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-      h_and &= __shfl_xor_sync(0xffffffffu, h_and, d);
-      h_or |= __shfl_xor_sync(0xffffffffu, h_or, d);
-      h_nz += __shfl_xor_sync(0xffffffffu, h_nz, d);
-    }
+    const uint32_t a_lo = __reduce_and_sync(0xffffffffu, (uint32_t)h_and);
+    const uint32_t a_hi = __reduce_and_sync(0xffffffffu, (uint32_t)(h_and >> 32));
+    const uint32_t o_lo = __reduce_or_sync(0xffffffffu, (uint32_t)h_or);
+    const uint32_t o_hi = __reduce_or_sync(0xffffffffu, (uint32_t)(h_or >> 32));
+    const unsigned nz = __reduce_add_sync(0xffffffffu, (unsigned)h_nz);
     if (lane == 0) {
-      sh_u64[2 + w] = h_and;
-      sh_u64[2 + CONSUMERS + w] = h_or;
-      hist[256 + w] = (unsigned)h_nz;
+      sh_u64[2 + w] = ((unsigned long long)a_hi << 32) | a_lo;
+      sh_u64[2 + CONSUMERS + w] = ((unsigned long long)o_hi << 32) | o_lo;
+      hist[256 + w] = nz;
     }
   }
-  if (ctid == 0) {
-    sh_u64[0] = 1ull;
-    sh_int[0] = 0;
-  }
+  if (ctid == 0) sh_int[0] = 0;
   bar_c();
   // T0: lower edge of the 8-bit digit bin (just below the heads' common
   // leading bits) that holds the keff-th largest head.  At least keff heads,
   // hence keys, are >= T0, so T0 bounds the keff-th largest key from below;
   // with fewer than keff nonzero heads every nonzero key stays (T0 = 1).
+  // Every warp scans the histogram itself.
+  unsigned long long T0 = 1ull;
   {
     unsigned long long a = ~0ull, o = 0ull;
     int nz = 0;
@@ -575,41 +577,35 @@ __device__ int fused_merge(const Params& p, uint8_t* scr, unsigned int* hist,
         if (key != 0ull) atomicAdd(&hist[(unsigned)((key >> shift) & 255ull)], 1u);
       }
       bar_c();
-      if (ctid < 32) {
-        // lane l holds digits 255-8l .. 248-8l (descending)
-        const int lane = ctid;
-        unsigned int c[8], local = 0;
+      // lane l holds digits 255-8l .. 248-8l (descending)
+      const int lane = ctid & 31;
+      unsigned int c[8], local = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          c[i] = hist[255 - 8 * lane - i];
-          local += c[i];
-        }
-        unsigned int incl = local;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-          const unsigned int v = __shfl_up_sync(0xffffffffu, incl, d);
-          if (lane >= d) incl += v;
-        }
-        const unsigned int excl = incl - local;
-        const bool hit = excl < (unsigned)keff && (unsigned)keff <= incl;
-        if (hit) {
-          unsigned int above = excl;
-          int digit = 0;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            above += c[i];
-            if (above >= (unsigned)keff) {
-              digit = 255 - 8 * lane - i;
-              break;
-            }
-          }
-          sh_u64[0] = prefix | (static_cast<unsigned long long>(digit) << shift);
-        }
+      for (int i = 0; i < 8; ++i) {
+        c[i] = hist[255 - 8 * lane - i];
+        local += c[i];
       }
+      unsigned int incl = local;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const unsigned int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+      }
+      const unsigned int excl = incl - local;
+      const bool hit = excl < (unsigned)keff && (unsigned)keff <= incl;
+      int digit = 0;  // 256 + digit once found
+      unsigned int above = excl;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        above += c[i];
+        if (hit && digit == 0 && above >= (unsigned)keff) digit = 256 + 255 - 8 * lane - i;
+      }
+      const int src = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;
+      digit = __shfl_sync(0xffffffffu, digit, src < 0 ? 0 : src) - 256;
+      if (digit >= 0) T0 = prefix | (static_cast<unsigned long long>(digit) << shift);
+      if (T0 == 0ull) T0 = 1ull;
     }
   }
-  bar_c();
-  const unsigned long long T0 = sh_u64[0] > 0ull ? sh_u64[0] : 1ull;
   // keys >= T0 with their slots: one shared atomic per warp
   {
     const int lane = ctid & 31;
@@ -773,7 +769,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     uint32_t it = 0;
     bool ok = true;
     bool scored = !FUSED;
-    const uint32_t blocked = FUSED ? fused_stage_off(p) / KV_STAGE_BYTES : STAGES;
     // phase 0: list index i -> Initial/Local block; phase 1: i -> selected block
     auto produce = [&](int phase, int u0, int u1) {
       for (int base = u0; base < u1 && ok; base += 32) {
@@ -819,9 +814,11 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
             if (it >= STAGES &&
                 !mbar_wait(bar_empty + 8 * st, ((it / STAGES) - 1) & 1, p.status))
               okl = 0;
-            // fused: stages holding the staged representatives are refilled
-            // only once this CTA's scoring is done
-            if (okl && !scored && st >= blocked && ntok_k > 0) {
+            // fused: the Initial/Local loads start once this CTA's slice is
+            // scored, so the representative rows (the selection's critical
+            // path) do not queue behind them in HBM; by then the stages that
+            // held those rows are free as well
+            if (okl && !scored && ntok_k > 0) {
               mbar_wait_sleep(bar_scored, 0, p.status, 64);
               scored = true;
             }
