@@ -491,6 +491,9 @@ def main():
                            "frac_of_hbm_peak": d_bytes / (t_d / n_d) / 1e9 / peak,
                            "bytes": d_bytes, "l2_note": f"{n_layers} layers rotated"}
 
+    # ---- decoding over the rotated layers with selection reuse
+    extra["decode_reuse_128k"] = decode_reuse_leg(stream, layers, rep)
+
     # ---- 1M-token leg: 4 layers back to back, Quest and Max reps
     if world == 1 and not args.no_1m:
         del layers, steps_fns, q_dev
@@ -591,6 +594,44 @@ def dynamic_leg(args, stream):
             "rep_build_k_bytes_read": 2 * int(L.k.numel()) * 2,
             "step_us": t_s / n_s * 1e6, "step_gbs": b["total"] / (t_s / n_s) / 1e9,
             "step_bytes": b["total"], "l2_note": "one layer repeated (touched set fits L2)"}
+
+
+def decode_reuse_leg(stream, layers, rep):
+    """Decoding over the rotated 128K layers under selection-reuse policies
+    (dense layers, layer_step, token_step of the pages' parameter list): one
+    kt_decode_layer call per (token, layer) over one token_step window,
+    captured in graphs; the KV cache is not appended to, so every window
+    repeats the same work."""
+    import torch
+
+    import block_sparse_long_quest_gb300 as kt
+    nl = len(layers)
+    p = layers[0].w.params
+    res = {}
+    for name, (dense, lstep, tstep) in (("select_every_layer_and_token", (0, 1, 1)),
+                                        ("layer_step2_token_step4", (0, 2, 4)),
+                                        ("dense2_layer_step1_token_step100", (2, 1, 100))):
+        pol = kt.reuse_policy(nl, dense, lstep, tstep)
+        slots = max(1, kt.kt_decode_history_slots(pol))
+        SEL = layers[0].variants[rep]["sel"].shape[1]
+        hs = torch.zeros((slots, 1, SEL, p.top_k), dtype=torch.int32, device="cuda")
+        hc = torch.zeros((slots, 1, SEL), dtype=torch.int32, device="cuda")
+        fns, actions = [], []
+        for t in range(tstep):
+            for l, Ly in enumerate(layers):
+                v = Ly.variants[rep]
+                actions.append(kt.kt_decode_layer_action(pol, t, l)[0])
+                fns.append(lambda t=t, l=l, Ly=Ly, v=v, pol=pol, hs=hs, hc=hc: kt.kt_decode_layer(
+                    pol, t, l, Ly.q, Ly.kv, v["reps"], v["params"], hs, hc, v["out"], v["ws"]))
+        per = len(fns)
+        count = per * max(1, 800 // per)
+        sec = graph_time(fns, count, per, stream, chunk=per * max(1, 1000 // per))
+        tokens = count // nl
+        res[name] = {"dense_layer_num": dense, "layer_step": lstep, "token_step": tstep,
+                     "us_per_token_all_layers": sec / tokens * 1e6,
+                     "selections_per_token": actions.count(kt.KT_LAYER_SELECT) / tstep,
+                     "dense_layers_per_token": actions.count(kt.KT_LAYER_DENSE) / tstep}
+    return {"workload": f"128k-gqa4-quest-shared-k32, {nl} layers", **res}
 
 
 def preselect_leg(args, stream):

@@ -24,6 +24,7 @@ KT_REP_MAX, KT_REP_MEAN, KT_REP_QUEST, KT_REP_FIX, KT_REP_DYNAMIC = 0, 1, 2, 3, 
 KT_HEAD_SHARED, KT_HEAD_SEPARATE = 0, 1
 (KT_OP_SCORE_SELECT, KT_OP_SPARSE_ATTN, KT_OP_DENSE_ATTN, KT_OP_SPARSE_STEP,
  KT_OP_DYNAMIC_REPS, KT_OP_PRESELECT) = 0, 1, 2, 3, 4, 5
+KT_LAYER_DENSE, KT_LAYER_SELECT, KT_LAYER_REUSE = 0, 1, 2
 
 # Every symbol declared in include/kt.h.
 EXPORTS = (
@@ -33,7 +34,8 @@ EXPORTS = (
     "kt_sparse_decode_step_host", "kt_dense_decode_attn", "kt_read_device_status",
     "kt_selftest_bounded_wait", "kt_sparse_decode_attn_noalloc", "kt_sparse_decode_step_kernels",
     "kt_preselect_mask_words", "kt_preselect_blocks", "kt_score_select_blocks_presel",
-    "kt_sparse_decode_step_presel",
+    "kt_sparse_decode_step_presel", "kt_decode_history_slots", "kt_decode_layer_action",
+    "kt_decode_layer", "kt_append_kv",
 )
 
 
@@ -59,6 +61,12 @@ class SparseParams(ctypes.Structure):
                 ("num_reps", ctypes.c_int32), ("fix_stride", ctypes.c_int32),
                 ("rep", ctypes.c_int32), ("head_mode", ctypes.c_int32),
                 ("softmax_scale", ctypes.c_float)]
+
+
+class ReusePolicy(ctypes.Structure):
+    """kt_reuse_policy: dense layers and the selection reuse strides."""
+    _fields_ = [("num_layers", ctypes.c_int32), ("dense_layer_num", ctypes.c_int32),
+                ("layer_step", ctypes.c_int32), ("token_step", ctypes.c_int32)]
 
 
 def _load():
@@ -99,6 +107,11 @@ def _load():
         "kt_selftest_bounded_wait": (ctypes.c_int, [vp, sz, i32, vp]),
         "kt_sparse_decode_attn_noalloc": (ctypes.c_int, [vp, P(PagedKV), P(SparseParams), vp,
                                                          vp, vp, vp]),
+        "kt_decode_history_slots": (i32, [P(ReusePolicy)]),
+        "kt_decode_layer_action": (ctypes.c_int, [P(ReusePolicy), i32, i32, P(i32), P(i32)]),
+        "kt_decode_layer": (ctypes.c_int, [P(ReusePolicy), i32, i32, vp, P(PagedKV), vp,
+                                           P(SparseParams), vp, vp, vp, vp, sz, vp]),
+        "kt_append_kv": (ctypes.c_int, [P(PagedKV), P(SparseParams), vp, vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -188,6 +201,39 @@ def kt_build_dynamic_reps(kv, params, q_local, T, first_block, num_blocks, reps_
                                      first_block, num_blocks, _ptr(reps_pool),
                                      _ptr(token_scores), _ptr(ws), ws.numel(), _stream(stream)),
            "kt_build_dynamic_reps")
+
+
+def reuse_policy(num_layers, dense_layer_num=0, layer_step=1, token_step=1) -> ReusePolicy:
+    return ReusePolicy(num_layers, dense_layer_num, layer_step, token_step)
+
+
+def kt_decode_history_slots(pol) -> int:
+    n = lib.kt_decode_history_slots(ctypes.byref(pol))
+    if n < 0:
+        raise KtError(-n, "kt_decode_history_slots")
+    return n
+
+
+def kt_decode_layer_action(pol, token_idx, layer_idx):
+    """(action, slot) of decode step token_idx at layer layer_idx."""
+    a, sl = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib.kt_decode_layer_action(ctypes.byref(pol), token_idx, layer_idx, ctypes.byref(a),
+                                      ctypes.byref(sl)), "kt_decode_layer_action")
+    return a.value, sl.value
+
+
+def kt_decode_layer(pol, token_idx, layer_idx, q, kv, reps_pool, params, hist_sel, hist_cnt, out,
+                    ws, stream=None):
+    _check(lib.kt_decode_layer(ctypes.byref(pol), token_idx, layer_idx, _ptr(q), ctypes.byref(kv),
+                               _ptr(reps_pool), ctypes.byref(params), _ptr(hist_sel),
+                               _ptr(hist_cnt), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+           "kt_decode_layer")
+
+
+def kt_append_kv(kv, params, k_new, v_new, reps_pool, ws, stream=None):
+    _check(lib.kt_append_kv(ctypes.byref(kv), ctypes.byref(params), _ptr(k_new), _ptr(v_new),
+                            _ptr(reps_pool), _ptr(ws), ws.numel(), _stream(stream)),
+           "kt_append_kv")
 
 
 def kt_preselect_mask_words(kv):

@@ -742,6 +742,102 @@ kt_status kt_dense_decode_attn(const void* q, const kt_paged_kv* kv, int32_t num
                    false, (cudaStream_t)stream);
 }
 
+// ---- decoding with selection reuse [LC §4.5, §4.6 decode loop] --------------
+
+namespace {
+bool policy_ok(const kt_reuse_policy* pol) {
+  return pol && pol->num_layers >= 1 && pol->dense_layer_num >= 0 &&
+         pol->dense_layer_num <= pol->num_layers && pol->layer_step >= 1 && pol->token_step >= 1;
+}
+}  // namespace
+
+int32_t kt_decode_history_slots(const kt_reuse_policy* pol) {
+  if (!policy_ok(pol)) return -(int32_t)KT_ERR_INVALID_ARG;
+  const int sparse = pol->num_layers - pol->dense_layer_num;
+  return (sparse + pol->layer_step - 1) / pol->layer_step;
+}
+
+kt_status kt_decode_layer_action(const kt_reuse_policy* pol, int32_t token_idx,
+                                 int32_t layer_idx, int32_t* action, int32_t* slot) {
+  if (!policy_ok(pol) || !action || !slot || token_idx < 0 || layer_idx < 0 ||
+      layer_idx >= pol->num_layers)
+    return KT_ERR_INVALID_ARG;
+  if (layer_idx < pol->dense_layer_num) {
+    *action = KT_LAYER_DENSE;
+    *slot = -1;
+    return KT_OK;
+  }
+  const int l = layer_idx - pol->dense_layer_num;  // index among the sparse layers
+  *slot = l / pol->layer_step;
+  *action = (token_idx % pol->token_step == 0 && l % pol->layer_step == 0) ? KT_LAYER_SELECT
+                                                                            : KT_LAYER_REUSE;
+  return KT_OK;
+}
+
+kt_status kt_decode_layer(const kt_reuse_policy* pol, int32_t token_idx, int32_t layer_idx,
+                          const void* q, const kt_paged_kv* kv, const void* reps_pool,
+                          const kt_sparse_params* p, int32_t* hist_sel, int32_t* hist_cnt,
+                          float* out, void* ws, size_t ws_bytes, kt_stream_t stream) {
+  int32_t action = 0, slot = 0;
+  kt_status s = kt_decode_layer_action(pol, token_idx, layer_idx, &action, &slot);
+  if (s != KT_OK) return s;
+  if (!kv || !p) return KT_ERR_INVALID_ARG;
+  if (action == KT_LAYER_DENSE)
+    return kt_dense_decode_attn(q, kv, p->num_q_heads, p->softmax_scale, out, ws, ws_bytes,
+                                stream);
+  if (!hist_sel || !hist_cnt || p->top_k < 1 || p->top_k > MAX_TOPK) return KT_ERR_INVALID_ARG;
+  const int SEL = p->head_mode == KT_HEAD_SHARED ? 1 : kv->num_kv_heads;
+  const size_t units = (size_t)kv->batch * SEL;
+  int32_t* sel = hist_sel + (size_t)slot * units * p->top_k;
+  int32_t* cnt = hist_cnt + (size_t)slot * units;
+  if (action == KT_LAYER_SELECT)
+    return kt_sparse_decode_step(q, kv, reps_pool, p, sel, cnt, out, ws, ws_bytes, stream);
+  return kt_sparse_decode_attn(q, kv, p, sel, cnt, out, ws, ws_bytes, stream);
+}
+
+kt_status kt_append_kv(const kt_paged_kv* kv, const kt_sparse_params* p, const void* k_new,
+                       const void* v_new, void* reps_pool, void* ws, size_t ws_bytes,
+                       kt_stream_t stream) {
+  kt_status s = check_kv(kv);
+  if (s != KT_OK) return s;
+  s = check_params(kv, p);
+  if (s != KT_OK) return s;
+  if (!k_new || !v_new || !ws || ws_bytes < 256 || !aligned16(k_new) || !aligned16(v_new) ||
+      !aligned16(ws) || (reps_pool && !aligned16(reps_pool)))
+    return KT_ERR_INVALID_ARG;
+  AppendLaunch a;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_pool = const_cast<void*>(kv->k_pool);
+  a.v_pool = const_cast<void*>(kv->v_pool);
+  a.table = kv->block_table;
+  a.seq_lens = const_cast<int32_t*>(kv->seq_lens);
+  a.status = at<int>(ws, 0);
+  a.B = kv->batch;
+  a.H_kv = kv->num_kv_heads;
+  a.max_blocks = kv->max_blocks_per_seq;
+  a.P = kv->num_pages;
+  cudaError_t e = launch_append(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return KT_ERR_CUDA;
+  if (!reps_pool || p->rep == KT_REP_DYNAMIC) return KT_OK;
+  // the reps of the blocks this token completed
+  RepsLaunch r;
+  r.k_pool = static_cast<const __half*>(kv->k_pool);
+  r.table = kv->block_table;
+  r.seq_lens = kv->seq_lens;
+  r.reps = reps_pool;
+  r.B = kv->batch;
+  r.H_kv = kv->num_kv_heads;
+  r.max_blocks = kv->max_blocks_per_seq;
+  r.P = kv->num_pages;
+  r.rep = p->rep;
+  r.R = reps_rows(p);
+  r.fix_stride = p->fix_stride;
+  r.first_block = -1;
+  r.num_blocks = 1;
+  return cuda_status(launch_reps(r, (cudaStream_t)stream));
+}
+
 kt_status kt_read_device_status(void* ws, size_t ws_bytes, kt_stream_t stream,
                                 int32_t* device_status) {
   if (!ws || ws_bytes < 256 || !device_status) return KT_ERR_INVALID_ARG;

@@ -507,7 +507,19 @@ struct RepsLaunch {
   void* reps;
   int B, H_kv, max_blocks, P, rep, R, fix_stride, first_block, num_blocks;
 };
-cudaError_t launch_reps(const RepsLaunch& a, cudaStream_t stream);
+cudaError_t launch_reps(const RepsLaunch& a, cudaStream_t stream);  // first_block < 0: completed tail blocks
+
+struct AppendLaunch {
+  const void* k_new;
+  const void* v_new;
+  void* k_pool;
+  void* v_pool;
+  const int32_t* table;
+  int32_t* seq_lens;
+  int* status;
+  int B, H_kv, max_blocks, P;
+};
+cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream);
 
 struct DynLaunch {
   const CUtensorMap* kmap;

@@ -45,11 +45,14 @@ __device__ __forceinline__ long long f16_fixed(uint32_t h) {
   return (h & 0x8000u) ? -mag : mag;
 }
 
+// first_block < 0: per sequence, the block that ends at its current length
+// (the block the last appended token completed), if any.
 __global__ void __launch_bounds__(THREADS) reps_kernel(const __grid_constant__ Params p) {
   const int b = blockIdx.y;
-  const int j = p.first_block + blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = p.seq_lens[b];
+  const int j = p.first_block >= 0 ? p.first_block + (int)blockIdx.x
+                                   : (n > 0 && n % BS == 0 ? n / BS - 1 : -1);
   if (j < 0 || j >= p.max_blocks || (long long)(j + 1) * BS > n) return;  // full blocks only
   const int page = p.table[(size_t)b * p.max_blocks + j];
   if (page < 0 || page >= p.P) return;
@@ -133,6 +136,41 @@ __global__ void __launch_bounds__(THREADS) reps_kernel(const __grid_constant__ P
   }
 }
 
+struct AppendParams {
+  const uint4* k_new;  // [B][H_kv][16] (128 fp16 per head)
+  const uint4* v_new;
+  uint4* k_pool;       // [P][H_kv][128][16]
+  uint4* v_pool;
+  const int32_t* table;
+  int32_t* seq_lens;
+  int* status;
+  int H_kv, max_blocks, P;
+};
+
+// One decoded token per sequence (CTA b): the K and V rows of every KV head
+// go to row n % 128 of the page of block n / 128, then n becomes n + 1.
+__global__ void __launch_bounds__(THREADS) append_kernel(const __grid_constant__ AppendParams p) {
+  const int b = blockIdx.x;
+  const int n = p.seq_lens[b];
+  const int j = n / BS;
+  int page = -1;
+  if (n >= 0 && j < p.max_blocks) page = p.table[(size_t)b * p.max_blocks + j];
+  if (page < 0 || page >= p.P) {  // no room in the table, or a page outside the pool
+    if (threadIdx.x == 0) set_status(p.status, KT_ERR_DEVICE_CHECK);
+    return;
+  }
+  const int per = p.H_kv * (D / 8);  // 16-byte chunks of one token's rows
+  for (int i = threadIdx.x; i < 2 * per; i += THREADS) {
+    const int r = i % per, h = r / (D / 8), c = r % (D / 8);
+    const uint4* src = (i < per ? p.k_new : p.v_new) + ((size_t)b * p.H_kv + h) * (D / 8) + c;
+    uint4* dst = (i < per ? p.k_pool : p.v_pool) +
+                 (((size_t)page * p.H_kv + h) * BS + n % BS) * (D / 8) + c;
+    *dst = *src;
+  }
+  __syncthreads();  // every thread has read seq_lens[b]
+  if (threadIdx.x == 0) p.seq_lens[b] = n + 1;
+}
+
 __global__ void selftest_wait_kernel(int* status, int spin_limit) {
   __shared__ __align__(8) uint64_t bar;
   const uint32_t a = smem_u32(&bar);
@@ -168,6 +206,23 @@ cudaError_t launch_reps(const RepsLaunch& a, cudaStream_t stream) {
   if (a.num_blocks <= 0) return cudaSuccess;
   const dim3 grid(a.num_blocks, a.B);
   reps_kernel<<<grid, THREADS, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
+  AppendParams p;
+  p.k_new = static_cast<const uint4*>(a.k_new);
+  p.v_new = static_cast<const uint4*>(a.v_new);
+  p.k_pool = static_cast<uint4*>(a.k_pool);
+  p.v_pool = static_cast<uint4*>(a.v_pool);
+  p.table = a.table;
+  p.seq_lens = a.seq_lens;
+  p.status = a.status;
+  p.H_kv = a.H_kv;
+  p.max_blocks = a.max_blocks;
+  p.P = a.P;
+  if (a.B <= 0) return cudaSuccess;
+  append_kernel<<<a.B, THREADS, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -314,6 +314,75 @@ kt_status kt_dense_decode_attn(const void* q, const kt_paged_kv* kv, int32_t num
                                kt_stream_t stream);
 
 /*
+ * Decoding over many layers and tokens with selection reuse [LC §4.5
+ * token_step / layer_step / dense_layer_num; §4.6, the decode loop of the
+ * framework pseudocode].  The first dense_layer_num layers attend every
+ * block.  For the other layers, with l = layer_idx - dense_layer_num (the
+ * index among sparse layers), the layers l = s*layer_step .. s*layer_step +
+ * layer_step - 1 share history slot s; decode step token_idx (counted from 0
+ * after prefill) selects afresh at layer l, and stores that selection in slot
+ * s, when token_idx % token_step == 0 and l % layer_step == 0; every other
+ * sparse (token, layer) attends with the selection stored in slot s, whose
+ * blocks are still Context blocks because Context only grows while decoding.
+ * Counting l among the sparse layers makes the first sparse layer of every
+ * slot select before the others read it.
+ */
+typedef struct {
+  int32_t num_layers;       /* >= 1 */
+  int32_t dense_layer_num;  /* 0 .. num_layers */
+  int32_t layer_step;       /* >= 1 */
+  int32_t token_step;       /* >= 1 */
+} kt_reuse_policy;
+
+typedef enum {
+  KT_LAYER_DENSE = 0,   /* kt_dense_decode_attn */
+  KT_LAYER_SELECT = 1,  /* kt_sparse_decode_step into the history slot */
+  KT_LAYER_REUSE = 2    /* kt_sparse_decode_attn with the history slot */
+} kt_layer_action;
+
+/* History slots the policy needs: ceil((num_layers - dense_layer_num) /
+ * layer_step); negative (a kt_status value negated) for an invalid policy. */
+int32_t kt_decode_history_slots(const kt_reuse_policy* pol);
+
+/* The action of decode step token_idx at layer layer_idx and its history
+ * slot (-1 for dense layers).  Host only; no device work. */
+kt_status kt_decode_layer_action(const kt_reuse_policy* pol, int32_t token_idx,
+                                 int32_t layer_idx, int32_t* action, int32_t* slot);
+
+/*
+ * One layer of one decode step under the policy: the action of
+ * kt_decode_layer_action on this layer's q / kv / reps.
+ *   hist_sel : int32 [slots][batch][SEL][top_k], hist_cnt : int32
+ *              [slots][batch][SEL], caller-owned device memory that persists
+ *              across calls (slots = kt_decode_history_slots); a SELECT call
+ *              writes slot s, a REUSE call reads it.
+ *   ws       : a workspace of kt_workspace_bytes(KT_OP_SPARSE_STEP) bytes,
+ *              which serves all three actions.
+ * Errors as the call the action maps to; KT_ERR_INVALID_ARG for an invalid
+ * policy or index.
+ */
+kt_status kt_decode_layer(const kt_reuse_policy* pol, int32_t token_idx, int32_t layer_idx,
+                          const void* q, const kt_paged_kv* kv, const void* reps_pool,
+                          const kt_sparse_params* p, int32_t* hist_sel, int32_t* hist_cnt,
+                          float* out, void* ws, size_t ws_bytes, kt_stream_t stream);
+
+/*
+ * Appends one decoded token to every sequence: writes k_new / v_new (fp16
+ * [batch][num_kv_heads][128]) as token n_b = seq_lens[b] of sequence b, into
+ * row n_b % 128 of page block_table[b][n_b / 128], and increments seq_lens[b]
+ * on the device (kv->seq_lens is written through).  With Max, Mean, Quest or
+ * Fix reps, the reps of a block that this token completes are built in the
+ * same call (Dynamic reps are built by kt_build_dynamic_reps when the caller
+ * chooses).  The caller allocates the page of a new block before the call.
+ * A sequence whose table has no room, or whose page is outside the pool,
+ * records KT_ERR_DEVICE_CHECK and is left unchanged.  ws: any workspace
+ * (its status word is used).
+ */
+kt_status kt_append_kv(const kt_paged_kv* kv, const kt_sparse_params* p, const void* k_new,
+                       const void* v_new, void* reps_pool, void* ws, size_t ws_bytes,
+                       kt_stream_t stream);
+
+/*
  * kt_sparse_decode_attn without a workspace, for callers that cannot allocate
  * device memory: for example a kernel plugged into an engine or framework
  * that hands it only its input and output buffers and owns every other byte

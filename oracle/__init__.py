@@ -279,6 +279,50 @@ def sparse_step_presel(kv: KV, q, p, presel, presel_cnt, q_local=None, *, units=
     return dict(unit_scores=us, sel=sel, cnt=cnt, out=out)
 
 
+# ---- decoding with selection reuse [LC §4.5 token_step / layer_step /
+# dense_layer_num; §4.6 decode loop] -------------------------------------------
+LAYER_DENSE, LAYER_SELECT, LAYER_REUSE = 0, 1, 2
+
+
+def decode_layer_action(num_layers: int, dense_layer_num: int, layer_step: int,
+                        token_step: int, token_idx: int, layer_idx: int):
+    """(action, slot) of decode step token_idx at layer layer_idx.
+
+    The first dense_layer_num layers attend every block ([LC §4.5]).  The
+    decode loop of [LC §4.6] reselects at (token, layer) when token % token_step
+    == 0 and layer % layer_step == 0 and otherwise reuses the selection kept
+    for layer // layer_step; here the layer index is counted among the sparse
+    layers (layer - dense_layer_num), so every slot is written before it is
+    read."""
+    if not (num_layers >= 1 and 0 <= dense_layer_num <= num_layers and layer_step >= 1
+            and token_step >= 1 and token_idx >= 0 and 0 <= layer_idx < num_layers):
+        raise ValueError("invalid policy or index")
+    if layer_idx < dense_layer_num:
+        return LAYER_DENSE, -1
+    l = layer_idx - dense_layer_num
+    if token_idx % token_step == 0 and l % layer_step == 0:
+        return LAYER_SELECT, l // layer_step
+    return LAYER_REUSE, l // layer_step
+
+
+def attend_selection(kv: KV, q, p, sel, cnt) -> np.ndarray:
+    """Attention of every query head over Initial + the given selection of
+    its unit + Local at the current lengths ([LC §4.6] attn over
+    kvcache_after_retrieval), as [B][H_q][d]."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    H_q = p.num_q_heads
+    G = H_q // kv.H_kv
+    out = np.zeros((kv.B, H_q, kv.d), dtype=np.float64)
+    for b in range(kv.B):
+        nb, c0, c1 = partition(int(kv.seq_lens[b]), p.initial_blocks, p.local_blocks, kv.bs)
+        for hq in range(H_q):
+            u = 0 if p.head_mode == HEAD_SHARED else hq // G
+            blocks = list(range(c0)) + [int(j) for j in sel[b, u, :int(cnt[b, u])]] + \
+                list(range(c1, nb))
+            out[b, hq] = attend(kv, b, hq, H_q, q[b, hq], blocks, p.softmax_scale)
+    return out
+
+
 class StepTimer:
     """The per-step part of the oracle (score, select, attend) over reps built
     once up front; used to time the CPU baseline on the same work as one GPU
