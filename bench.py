@@ -12,8 +12,11 @@ Default workload: the InternLM2.5-7B-1M-shaped 128K layer (32 query heads, 8 KV
 heads, head_dim 128, 131072 fp16 tokens in 128-token blocks, Initial 128,
 Local 4096, Quest reps, SHARED top-32), seeded synthetic data, eight distinct
 layers rotated so that the touched working set (8 x 38 MB) is larger than twice
-the L2 cache.  A second leg runs the 1M-token, 4-layer workload (SEPARATE
-top-32 per KV head, Quest and Max reps).
+the L2 cache.  Further legs: the Quest rep build and the dense decode over the
+same layers; decoding over the eight layers under selection-reuse policies
+(kt_decode_layer: dense layers, layer_step, token_step); the 1M-token, 4-layer
+workload (SEPARATE top-32 per KV head, Quest and Max reps); the Dynamic rep
+build and step at 128K; the preselection and the step restricted to it.
 
 value = algorithmic bytes per step (reps of every Context block + K/V of the
 attended tokens) / device time per step, in GB/s; us_per_step and
@@ -226,8 +229,8 @@ class ClockSampler:
 KERNEL_SOURCES = ("attn.cu", "select_common.cuh", "kt_internal.cuh")
 KERNEL_TRAFFIC = {
     "attn_kernel<fused step>": {
-        "bytes": 38287616 + 25600,
-        "sources_sha256": "7a0c3607261c926625500148c3ce67ff816bbd3087491a437b13f511036e95a0"},
+        "bytes": 38289152 + 33024,
+        "sources_sha256": "c8a6c277ec76004316ff6f3439d6f1632b5ddcb2287d90b8cbd5c14fa7072a02"},
 }
 
 
