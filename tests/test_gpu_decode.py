@@ -33,7 +33,8 @@ def _gpu():
 
 def _layer(l, rep, head_mode):
     p = synth.Params(num_q_heads=8, initial_blocks=1, local_blocks=2, top_k=3, rep=rep,
-                     head_mode=head_mode)
+                     head_mode=head_mode, num_reps=4 if rep == synth.REP_FIX else 1,
+                     fix_stride=32)
     w = synth.make_workload(f"decode-l{l}", seed=61, seq_lens=CAP, num_q_heads=8,
                             num_kv_heads=2, params=p, layer=l, permute_pages=True)
     w.seq_lens = np.asarray(START, dtype=np.int32)
@@ -41,7 +42,9 @@ def _layer(l, rep, head_mode):
 
 
 @pytest.mark.parametrize("rep,head_mode", [(synth.REP_QUEST, synth.HEAD_SEPARATE),
-                                           (synth.REP_MAX, synth.HEAD_SHARED)])
+                                           (synth.REP_MAX, synth.HEAD_SHARED),
+                                           (synth.REP_MEAN, synth.HEAD_SEPARATE),
+                                           (synth.REP_FIX, synth.HEAD_SHARED)])
 def test_decode_loop_with_reuse_and_append(rep, head_mode):
     import torch
     import block_sparse_long_quest_gb300 as kt
