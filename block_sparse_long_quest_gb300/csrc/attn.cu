@@ -260,7 +260,7 @@ __device__ __forceinline__ void fused_weights(const Params& p, float* wts, int b
 // Arrives on bar_scored once its representative loads are done (every CTA).
 // The block-table entries of the nominal slice do not depend on the sequence
 // length, so they load together with the length and the query rows.
-template <class Bar>
+template <int SK, class Bar>
 __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
                             unsigned long long* sh_u64, int* sh_int, int ctid, int warp, int lane,
                             Bar bar_c, uint32_t bar_scored, const uint8_t* ring,
@@ -344,11 +344,10 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
       fused_weights(p, wts, bu, g0, nkv, ctid);
       bar_c();
     }
-    // fp16 reps: a few blocks on the CUDA cores (whole columns per thread),
-    // many on the tensor cores, whose B fragments replace the weights in place
-    const int lin_max = 8 * CONSUMERS / (V <= 32 ? 1 : V <= 64 ? 2 : V <= 128 ? 4 : 8);
-    const bool use_mma = !multi && !f32 && nloc > lin_max;
-    if (use_mma) selc::weights_to_frags<NCT>(wts, V * 8, ctid, bar_c);
+    // fp16 reps: a few blocks per CTA on the CUDA cores, many on the tensor
+    // cores, whose B fragments replace the weights in place (the launch's
+    // path SK follows from the largest slice, fused_score_kind)
+    if constexpr (SK == SK_MMA) selc::weights_to_frags<NCT>(wts, V * 8, ctid, bar_c);
 #pragma unroll 1
     for (int r = 0; r < nrounds; ++r) {
       const int r0 = r * rcap, nr = min(rcap, nloc - r0);
@@ -357,20 +356,20 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
       const uint4* sbuf = reinterpret_cast<const uint4*>(ring + buf_off(r));
 #define KT_SCORE(NV, F) selc::score_linear_smem<NV, F, CONSUMERS>(sbuf, (int)(sb / 16), nr, js + r0, p.P, pgs + r0, wts, V, keys + r0, warp, lane, p.status)
 #define KT_COLS(VC) selc::score_linear_cols<VC, CONSUMERS>(sbuf, (int)(sb / 16), nr, js + r0, p.P, pgs + r0, wts, keys + r0, red, warp, lane, p.status, bar_c)
-      if (multi) {
+      if constexpr (SK == SK_MULTI) {
         selc::score_multi_mma_smem<CONSUMERS>(
             base, (int)sb, nr, js + r0, p.P, pgs + r0,
             p.q + ((size_t)bu * p.H_kv * p.G + (size_t)g0 * p.G) * D, p.G, nkv, p.R, keys + r0,
             reinterpret_cast<float*>(hist), warp, lane, p.status, bar_c);
-      } else if (f32) {
+      } else if constexpr (SK == SK_F32) {
         fused_score_f32(sbuf, (int)(sb / 16), nr, js + r0, p.P, pgs + r0, wts, V, keys + r0, warp,
                         lane, p.status);
-      } else if (use_mma) {
+      } else if constexpr (SK == SK_MMA) {
         selc::score_mma_smem<CONSUMERS>(base, (int)sb, nr, js + r0, p.P, pgs + r0,
                                         reinterpret_cast<const uint2*>(wts), V * 8, keys + r0,
                                         reinterpret_cast<float*>(hist), warp, lane, p.status,
                                         bar_c);
-      } else if (V == 256 || V == 128 || V == 64) {
+      } else if constexpr (SK == SK_COLS) {
         // one pass: every thread owns one 16-byte column of the few blocks
         float* red = reinterpret_cast<float*>(hist);
         if (V == 256) KT_COLS(256);
@@ -411,7 +410,8 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     bar_c();
     few = few || sh_int[3] <= p.kk_f;
   }
-  if (!few) {
+  // SK_COLS launches have slices of at most top_k blocks: always `few`
+  if (SK != SK_COLS && !few) {
     auto emit = [&](int r, int i) {
       cand[r] = keys[i];
       cpage[r] = pgs[i];
@@ -419,12 +419,14 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     unsigned long long* ck = reinterpret_cast<unsigned long long*>(scr + Ls.bkey);
     int* ci = reinterpret_cast<int*>(scr + Ls.bidx);
     int* ix = reinterpret_cast<int*>(scr + Ls.idx);
-    if (nloc <= 8 * NCT)
-      selc::topk_sorted_reg<NCT>(keys, nloc, p.kk_f, ck, ci, ix, hist, sh_u64, sh_int, ctid,
-                                 bar_c, emit);
-    else
-      selc::topk_sorted<NCT>(keys, nloc, p.kk_f, ck, ci, ix, hist, sh_u64, sh_int, ctid, bar_c,
-                             emit);
+    if constexpr (SK != SK_COLS) {
+      if (nloc <= 8 * NCT)
+        selc::topk_sorted_reg<NCT>(keys, nloc, p.kk_f, ck, ci, ix, hist, sh_u64, sh_int, ctid,
+                                   bar_c, emit);
+      else
+        selc::topk_sorted<NCT>(keys, nloc, p.kk_f, ck, ci, ix, hist, sh_u64, sh_int, ctid, bar_c,
+                               emit);
+    }
   } else {
     // with nloc odd, keys[nloc] is the zero padding
     const int npad = (nloc + 1) & ~1;
@@ -667,8 +669,9 @@ __device__ int fused_merge(const Params& p, uint8_t* scr, unsigned int* hist,
   return i1 - i0;
 }
 
-template <bool FUSED>
+template <int SK>
 __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant__ Params p) {
+  constexpr bool FUSED = SK != SK_NONE;
   extern __shared__ uint8_t smem_raw[];
   __shared__ unsigned int f_hist[FUSED ? 512 : 1];
   __shared__ unsigned long long f_sh_u64[FUSED ? 2 + 2 * CONSUMERS : 1];
@@ -723,7 +726,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     for (int s = lane; s <= S; s += 32) cum[s] = s + (int)(extra * cum[s] / W);
     __syncwarp();
   } else if (FUSED) {
-    fused_score(p, reinterpret_cast<uint8_t*>(scratch), f_hist, f_sh_u64, f_sh_int, tid, warp,
+    fused_score<SK>(p, reinterpret_cast<uint8_t*>(scratch), f_hist, f_sh_u64, f_sh_int, tid, warp,
                 lane, bar_c, bar_scored, smem + SmemLayout::kv, kv_base, bar_reps);
   }
   if (!FUSED) __syncthreads();
@@ -1223,11 +1226,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
 int attn_smem_optin() {
   static std::atomic<int> slot[KT_MAX_DEVICES];
   return per_device_cached(slot, [] {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SMEM_BYTES);
+    cudaError_t e = cudaSuccess;
+    for (const void* f : {(const void*)attn_kernel<SK_NONE>, (const void*)attn_kernel<SK_COLS>,
+                          (const void*)attn_kernel<SK_LINEAR>, (const void*)attn_kernel<SK_MMA>,
+                          (const void*)attn_kernel<SK_F32>, (const void*)attn_kernel<SK_MULTI>})
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     return (int)e;
   });
 }
@@ -1237,10 +1241,18 @@ int attn_fused_max_ctas_per_sm() {
   return per_device_cached(slot, [] {
     if (attn_smem_optin() != 0) return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<true>, THREADS,
-                                                      SMEM_BYTES) != cudaSuccess)
-      return 0;
-    return n;
+    // every instantiation needs the same resources; the largest register
+    // count decides
+    int m = 1 << 30;
+    for (const void* f : {(const void*)attn_kernel<SK_COLS>, (const void*)attn_kernel<SK_LINEAR>,
+                          (const void*)attn_kernel<SK_MMA>, (const void*)attn_kernel<SK_F32>,
+                          (const void*)attn_kernel<SK_MULTI>}) {
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, THREADS, SMEM_BYTES) !=
+          cudaSuccess)
+        return 0;
+      m = n < m ? n : m;
+    }
+    return m;
   });
 }
 
@@ -1305,8 +1317,15 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (a.fused) return cudaLaunchKernelEx(&cfg, attn_kernel<true>, p);
-  return cudaLaunchKernelEx(&cfg, attn_kernel<false>, p);
+  if (!a.fused) return cudaLaunchKernelEx(&cfg, attn_kernel<SK_NONE>, p);
+  switch (a.sk) {
+    case SK_COLS: return cudaLaunchKernelEx(&cfg, attn_kernel<SK_COLS>, p);
+    case SK_LINEAR: return cudaLaunchKernelEx(&cfg, attn_kernel<SK_LINEAR>, p);
+    case SK_MMA: return cudaLaunchKernelEx(&cfg, attn_kernel<SK_MMA>, p);
+    case SK_F32: return cudaLaunchKernelEx(&cfg, attn_kernel<SK_F32>, p);
+    case SK_MULTI: return cudaLaunchKernelEx(&cfg, attn_kernel<SK_MULTI>, p);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace kt

@@ -655,6 +655,11 @@ kt_status step_impl(const void* q, const kt_paged_kv* kv, const void* reps_pool,
     a.scale_log2 = (float)((double)p->softmax_scale * 1.4426950408889634);
     a.grid = sms;
     a.fused = true;
+    {
+      const int nkv = a.SEL == 1 ? kv->num_kv_heads : 1;
+      const int V = nkv * reps_rows(p) * D / (p->rep == KT_REP_MEAN ? 4 : 8);
+      a.sk = fused_score_kind(p->rep, V, chunk, p->top_k);
+    }
     a.reps = reps_pool;
     a.rep = p->rep;
     a.R = reps_rows(p);

@@ -36,6 +36,25 @@ constexpr int FUSED_MAX_SLOTS = FUSED_GATHER_PER_THREAD * ATTN_CONSUMER_THREADS;
 // than kk blocks.  Merge: every candidate key and page of the unit, the chosen
 // indices, their block ids (padded to a multiple of 4) and the top-k
 // temporaries.
+// Scoring paths of the one-launch step, one kernel instantiation each (the
+// kernel runs most of its code once per launch, so it carries only the path
+// it uses): few fp16 blocks per CTA with 64/128/256 16-byte columns on the CUDA
+// cores (COLS), few fp16 blocks otherwise (LINEAR), many fp16 blocks on the
+// tensor cores (MMA), fp32 reps (F32), several reps per block (MULTI).
+enum : int { SK_NONE = 0, SK_COLS = 1, SK_LINEAR = 2, SK_MMA = 3, SK_F32 = 4, SK_MULTI = 5 };
+// the most fp16 blocks a CTA scores on the CUDA cores in one pass
+__host__ __device__ inline int fused_lin_max(int V) {
+  return 8 * (ATTN_CONSUMER_THREADS / 32) / (V <= 32 ? 1 : V <= 64 ? 2 : V <= 128 ? 4 : 8);
+}
+// COLS also needs every slice to be its own candidate list (chunk <= top_k),
+// so it carries no per-slice top-k
+__host__ __device__ inline int fused_score_kind(int rep, int V, int chunk, int top_k) {
+  if (rep == KT_REP_FIX || rep == KT_REP_DYNAMIC) return SK_MULTI;
+  if (rep == KT_REP_MEAN) return SK_F32;
+  if (chunk > fused_lin_max(V)) return SK_MMA;
+  return ((V == 64 || V == 128 || V == 256) && chunk <= top_k) ? SK_COLS : SK_LINEAR;
+}
+
 struct FusedScoreLayout {
   int keys, pgs, idx, bkey, bidx, total;
 };
@@ -460,6 +479,7 @@ struct AttnLaunch {
   bool pdl;  // launched as a programmatic dependent of the previous kernel
   // fused step (selection inside the attention kernel, cooperative launch)
   bool fused;
+  int sk;  // fused: the scoring path (SK_*)
   const void* reps;
   int rep, R;
   int ncpu;     // CTAs scoring one selection unit
