@@ -229,8 +229,8 @@ class ClockSampler:
 KERNEL_SOURCES = ("attn.cu", "select_common.cuh", "kt_internal.cuh")
 KERNEL_TRAFFIC = {
     "attn_kernel<fused step>": {
-        "bytes": 38289152 + 33024,
-        "sources_sha256": "c8a6c277ec76004316ff6f3439d6f1632b5ddcb2287d90b8cbd5c14fa7072a02"},
+        "bytes": 38259712 + 25344,
+        "sources_sha256": "24642bf58d65c4a14b7b0595c822e8a9b1f049b63404c849000a4996defd2f35"},
 }
 
 
@@ -614,6 +614,8 @@ def decode_reuse_leg(stream, layers, rep):
     for name, (dense, lstep, tstep) in (("select_every_layer_and_token", (0, 1, 1)),
                                         ("layer_step2_token_step4", (0, 2, 4)),
                                         ("dense2_layer_step1_token_step100", (2, 1, 100))):
+        if dense >= nl:  # needs more layers than are rotated
+            continue
         pol = kt.reuse_policy(nl, dense, lstep, tstep)
         slots = max(1, kt.kt_decode_history_slots(pol))
         SEL = layers[0].variants[rep]["sel"].shape[1]
