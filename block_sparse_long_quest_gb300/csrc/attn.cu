@@ -419,14 +419,10 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     unsigned long long* ck = reinterpret_cast<unsigned long long*>(scr + Ls.bkey);
     int* ci = reinterpret_cast<int*>(scr + Ls.bidx);
     int* ix = reinterpret_cast<int*>(scr + Ls.idx);
-    if constexpr (SK != SK_COLS) {
-      if (nloc <= 8 * NCT)
-        selc::topk_sorted_reg<NCT>(keys, nloc, p.kk_f, ck, ci, ix, hist, sh_u64, sh_int, ctid,
-                                   bar_c, emit);
-      else
-        selc::topk_sorted<NCT>(keys, nloc, p.kk_f, ck, ci, ix, hist, sh_u64, sh_int, ctid, bar_c,
-                               emit);
-    }
+    // slices hold at most FUSED_MAX_CHUNK = 8 NCT blocks (the host's plan)
+    if constexpr (SK != SK_COLS)
+      selc::topk_sorted_reg<NCT>(keys, nloc, p.kk_f, ck, ci, ix, hist, sh_u64, sh_int, ctid,
+                                 bar_c, emit);
   } else {
     // with nloc odd, keys[nloc] is the zero padding
     const int npad = (nloc + 1) & ~1;

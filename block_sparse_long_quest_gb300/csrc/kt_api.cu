@@ -574,7 +574,7 @@ bool fused_plan(const kt_paged_kv* kv, const kt_sparse_params* p, int sms, int* 
   const int cmax = kv->max_blocks_per_seq - p->initial_blocks - p->local_blocks;
   const int chunk = cmax > 0 ? (cmax + nc - 1) / nc : 1;
   const int k = p->top_k < chunk ? p->top_k : chunk;
-  if (k > FUSED_KK_CAP) return false;
+  if (k > FUSED_KK_CAP || chunk > FUSED_MAX_CHUNK) return false;
   const int nkv = SEL == 1 ? kv->num_kv_heads : 1;
   const int Rw = p->rep == KT_REP_QUEST ? 2 : 1;
   const bool f32 = p->rep == KT_REP_MEAN;

@@ -29,6 +29,7 @@ constexpr int ATTN_CONSUMER_THREADS = 256;  // consumer threads of the attention
 constexpr int ATTN_RING_BYTES = 3 * 4 * 128 * 64 * 2;  // attention KV ring (3 stages x 64 KB)
 constexpr int FUSED_GATHER_PER_THREAD = 8;  // candidate slots a merging thread holds
 constexpr int FUSED_MAX_SLOTS = FUSED_GATHER_PER_THREAD * ATTN_CONSUMER_THREADS;
+constexpr int FUSED_MAX_CHUNK = 8 * ATTN_CONSUMER_THREADS;  // blocks one CTA scores (keys held in registers)
 
 // Byte offsets inside the attention kernel's scratch for the in-kernel
 // selection of the fused step.  Scoring: weights (fp32), keys and page ids of
