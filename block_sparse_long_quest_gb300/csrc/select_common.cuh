@@ -369,131 +369,16 @@ __device__ __noinline__ void select_top(const unsigned long long* keys, int N, i
   bar();
 }
 
-// The k largest of N distinct keys in shared memory (1 <= k < N, k <= NT),
-// emitted in descending order as emit(rank, index).  One 8-bit digit
-// histogram (just below the keys' common leading bits) finds the bin of the
-// k-th largest key; the keys from that bin up are ranked exactly by counting.
-// When more than NT keys reach that bin, select_top narrows first (k <= NT).
-// Scratch: hist 256 bins; ck (16-byte aligned) / ci NT entries; idx k
-// entries; sh_u64 2 + 2*NT/32; sh_int 4.  All NT threads call it.
-template <int NT, class Bar, class Emit>
-__device__ void topk_sorted(const unsigned long long* keys, int N, int k,
-                            unsigned long long* ck, int* ci, int* idx, unsigned int* hist,
-                            unsigned long long* sh_u64, int* sh_int, int tid, Bar bar,
-                            Emit emit) {
-  constexpr int WARPS = NT / 32;
-  const int lane = tid & 31, warp = tid >> 5;
-  unsigned long long a = ~0ull, o = 0ull;
-#pragma unroll 1
-  for (int i = tid; i < N; i += NT) {
-    a &= keys[i];
-    o |= keys[i];
-  }
-#pragma unroll 1
-  for (int i = tid; i < 256; i += NT) hist[i] = 0u;
-#pragma unroll 1
-  for (int i = tid; i < NT; i += NT) ck[i] = 0ull;
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) {
-    a &= __shfl_xor_sync(0xffffffffu, a, d);
-    o |= __shfl_xor_sync(0xffffffffu, o, d);
-  }
-  if (lane == 0) {
-    sh_u64[2 + warp] = a;
-    sh_u64[2 + WARPS + warp] = o;
-  }
-  if (tid == 0) sh_int[0] = 0;
-  bar();
-  unsigned long long all_and = ~0ull, all_or = 0ull;
-#pragma unroll
-  for (int w = 0; w < WARPS; ++w) {
-    all_and &= sh_u64[2 + w];
-    all_or |= sh_u64[2 + WARPS + w];
-  }
-  const unsigned long long diff = all_and ^ all_or;
-  const int hi = diff ? 64 - __clzll((long long)diff) : 0;
-  const int shift = hi > 8 ? hi - 8 : 0;
-  const unsigned long long pmask = hi >= 64 ? 0ull : ~((1ull << hi) - 1);
-  const unsigned long long prefix = all_and & pmask;
-#pragma unroll 1
-  for (int base = 0; base < N; base += NT) {
-    const int i = base + tid;
-    unsigned int bin = 256u;
-    if (i < N) bin = (unsigned)((keys[i] >> shift) & 255ull);
-    const unsigned int peers = __match_any_sync(0xffffffffu, bin);
-    if (bin < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (unsigned)__popc(peers));
-  }
-  bar();
-  if (warp == 0) {
-    unsigned int c[8], local = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      c[i] = hist[255 - 8 * lane - i];
-      local += c[i];
-    }
-    unsigned int incl = local;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const unsigned int v = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += v;
-    }
-    const unsigned int excl = incl - local;
-    if (excl < (unsigned)k && (unsigned)k <= incl) {
-      unsigned int above = excl;
-      int digit = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        above += c[i];
-        if (above >= (unsigned)k) {
-          digit = 255 - 8 * lane - i;
-          break;
-        }
-      }
-      sh_u64[0] = prefix | (static_cast<unsigned long long>(digit) << shift);
-    }
-  }
-  bar();
-  const unsigned long long T = sh_u64[0];
-  {
-    const unsigned int lt = (1u << lane) - 1u;
-#pragma unroll 1
-    for (int base = 0; base < N; base += NT) {
-      const int i = base + tid;
-      const bool take = i < N && keys[i] >= T;
-      const unsigned int bal = __ballot_sync(0xffffffffu, take);
-      int off = 0;
-      if (lane == 0 && bal) off = atomicAdd(&sh_int[0], __popc(bal));
-      off = __shfl_sync(0xffffffffu, off, 0) + __popc(bal & lt);
-      if (take && off < NT) {
-        ck[off] = keys[i];
-        ci[off] = i;
-      }
-    }
-  }
-  bar();
-  const int M = sh_int[0];
-  if (M <= NT) {
-#pragma unroll 1
-    for (int i = tid; i < M; i += NT) {
-      const int r = count_greater(ck, (M + 1) & ~1, ck[i]);
-      if (r < k) emit(r, ci[i]);
-    }
-  } else {
-    select_top<NT>(keys, N, k, idx, ck, ci, hist, sh_u64, sh_int, tid, bar);
-#pragma unroll 1
-    for (int i = tid; i < NT; i += NT) ck[i] = i < k ? keys[idx[i]] : 0ull;
-    bar();
-#pragma unroll 1
-    for (int i = tid; i < k; i += NT) emit(count_greater(ck, (k + 1) & ~1, ck[i]), idx[i]);
-  }
-  bar();
-}
-
-// The same selection as topk_sorted for N <= 8 NT keys, with each thread's
-// keys (i = tid + r NT) held in registers: the common leading bits come from
-// warp AND / OR reductions, the digit histogram takes one shared atomic per
-// key, and every warp scans the histogram itself, so the bound needs no extra
-// barrier.  Same scratch and the same emitted ranks and indices.
+// The k largest of N distinct keys in shared memory (1 <= k < N <= 8 NT,
+// k <= NT), emitted in descending order as emit(rank, index).  Each thread
+// holds its keys (i = tid + r NT) in registers.  Warp AND / OR reductions give
+// the keys' common leading bits; one 8-bit digit histogram just below them
+// (one shared atomic per key, every warp scanning it itself) finds the bin of
+// the k-th largest key; the keys from that bin up are compacted and ranked
+// exactly by counting.  When more than NT keys reach that bin, select_top
+// narrows first.  Scratch: hist 256 bins (512 for select_top); ck (16-byte
+// aligned) / ci NT entries; idx k entries; sh_u64 2 + 2*NT/32; sh_int 4.  All
+// NT threads call it.
 template <int NT, class Bar, class Emit>
 __device__ void topk_sorted_reg(const unsigned long long* keys, int N, int k,
                                 unsigned long long* ck, int* ci, int* idx, unsigned int* hist,
