@@ -229,8 +229,8 @@ class ClockSampler:
 KERNEL_SOURCES = ("attn.cu", "select_common.cuh", "kt_internal.cuh")
 KERNEL_TRAFFIC = {
     "attn_kernel<fused step>": {
-        "bytes": 38259712 + 25344,
-        "sources_sha256": "24642bf58d65c4a14b7b0595c822e8a9b1f049b63404c849000a4996defd2f35"},
+        "bytes": 38259712 + 29952,
+        "sources_sha256": "13095cd3f979da214cd102b22f79234e05e30c9b3d4376cac7bc22d8365c73bb"},
 }
 
 
