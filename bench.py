@@ -225,13 +225,22 @@ class ClockSampler:
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
 # one ncu capture of the 128K workload, per kernel, valid only for the kernel
-# sources it was taken from (sha256 over KERNEL_SOURCES); null otherwise.
+# code it was taken from (sha256 over KERNEL_SOURCES without comments); null
+# otherwise.
 KERNEL_SOURCES = ("attn.cu", "select_common.cuh", "kt_internal.cuh")
 KERNEL_TRAFFIC = {
     "attn_kernel<fused step>": {
         "bytes": 38259712 + 29952,
-        "sources_sha256": "13095cd3f979da214cd102b22f79234e05e30c9b3d4376cac7bc22d8365c73bb"},
+        "sources_sha256": "0901bdbd81e4e26bf96948a21fedec4de37ad802c6b34d919bf94eeeb8f863c3"},
 }
+
+
+def _code_only(text: str) -> str:
+    """The source without comments and blank lines: the record follows the code."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
 
 
 def kernel_sources_sha():
@@ -240,7 +249,7 @@ def kernel_sources_sha():
     for name in KERNEL_SOURCES:
         path = os.path.join(ROOT, "block_sparse_long_quest_gb300", "csrc", name)
         try:
-            h.update(open(path, "rb").read())
+            h.update(_code_only(open(path, encoding="utf-8").read()).encode())
         except OSError:
             return None
     return h.hexdigest()

@@ -31,6 +31,16 @@
 //     segment served by one CTA is written to out directly; otherwise each CTA
 //     writes an (m, l, acc) partial, takes a ticket, and the CTA completing the
 //     count merges the segment's partials in CTA order (deterministic).
+//
+// The one-launch decode step (attn_kernel<SK>, SK != SK_NONE; a cooperative
+// launch of one CTA per SM) also makes the selection (§3.1, §4.3, §4.5): while
+// the producer waits, the consumer warps stage and score one slice of a
+// selection unit's Context blocks (fused_score), publish the slice's best keys
+// with a ticket, then wait for the unit's tickets and pick the unit's top-k
+// (fused_merge) and hand this CTA's share of the chosen pages to the producer.
+// Each segment's first CTA merges the partials (every CTA is resident).  SK
+// selects the scoring path at compile time, so a launch carries only the code
+// it runs.
 #include "select_common.cuh"
 
 namespace kt {
