@@ -368,15 +368,17 @@ kt_status kt_decode_layer(const kt_reuse_policy* pol, int32_t token_idx, int32_t
 
 /*
  * Appends one decoded token to every sequence: writes k_new / v_new (fp16
- * [batch][num_kv_heads][128]) as token n_b = seq_lens[b] of sequence b, into
- * row n_b % 128 of page block_table[b][n_b / 128], and increments seq_lens[b]
- * on the device (kv->seq_lens is written through).  With Max, Mean, Quest or
- * Fix reps, the reps of a block that this token completes are built in the
- * same call (Dynamic reps are built by kt_build_dynamic_reps when the caller
- * chooses).  The caller allocates the page of a new block before the call.
- * A sequence whose table has no room, or whose page is outside the pool,
- * records KT_ERR_DEVICE_CHECK and is left unchanged.  ws: any workspace
- * (its status word is used).
+ * [batch][num_kv_heads][128], 16-byte aligned) as token n_b = seq_lens[b] of
+ * sequence b, into row n_b % 128 of page block_table[b][n_b / 128], and
+ * increments seq_lens[b] on the device.  The pools and seq_lens that kv points
+ * to are written through its const pointers.  With Max, Mean, Quest or Fix
+ * reps and a non-NULL reps_pool, the reps of a block that this token completes
+ * are built in the same call (Dynamic reps are built by kt_build_dynamic_reps
+ * when the caller chooses; reps_pool NULL skips the reps).  The caller
+ * allocates the page of a new block before the call.  A sequence whose table
+ * has no room, or whose page is outside the pool, records KT_ERR_DEVICE_CHECK
+ * and is left unchanged.  ws: any workspace of at least 256 bytes (its status
+ * word is used).  Asynchronous on `stream`.
  */
 kt_status kt_append_kv(const kt_paged_kv* kv, const kt_sparse_params* p, const void* k_new,
                        const void* v_new, void* reps_pool, void* ws, size_t ws_bytes,
