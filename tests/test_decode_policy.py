@@ -1,7 +1,7 @@
 """Selection reuse while decoding ([LC §4.5] token_step / layer_step /
 dense_layer_num, [LC §4.6] decode loop): the oracle's action function pinned
-to the pseudocode's loop, and the library's host-side policy checked against
-it (no GPU work)."""
+to the decode loop's reuse rule, and the library's host-side policy checked
+against it (no GPU work)."""
 import itertools
 
 import pytest
@@ -11,31 +11,33 @@ import oracle
 DENSE, SELECT, REUSE = oracle.LAYER_DENSE, oracle.LAYER_SELECT, oracle.LAYER_REUSE
 
 
-def pseudocode_loop(num_tokens, num_layers, layer_steps, token_steps):
-    """The decode loop of [LC §4.6] written out literally (no dense layers):
-    per (token, layer), reuse history[layer // layer_steps] unless both
-    indices are on their strides, in which case reselect and store it there.
-    Returns the (action, slot) sequence and checks that nothing is read before
-    it was written."""
-    history = {}
+def decode_loop_rule(num_tokens, num_layers, lstride, tstride):
+    """The reuse rule of the decode loop of [LC §4.6] (no dense layers),
+    restated: every layer group g = layer // lstride keeps one stored
+    selection; a (token, layer) pair makes a new one, and stores it for its
+    group, exactly when the token is a multiple of tstride and the layer a
+    multiple of lstride; every other pair reuses its group's.  Returns the
+    (action, slot) sequence in decode order and checks that no group is read
+    before it was stored."""
+    stored = set()
     seq = []
-    for token_idx in range(num_tokens):
-        for layer_idx in range(num_layers):
-            slot = layer_idx // layer_steps
-            if token_idx % token_steps != 0 or layer_idx % layer_steps != 0:
-                assert slot in history
-                seq.append((REUSE, slot))
+    for tok in range(num_tokens):
+        for lay in range(num_layers):
+            group = lay // lstride
+            fresh = tok % tstride == 0 and lay % lstride == 0
+            if fresh:
+                stored.add(group)
             else:
-                history[slot] = (token_idx, layer_idx)
-                seq.append((SELECT, slot))
+                assert group in stored
+            seq.append((SELECT if fresh else REUSE, group))
     return seq
 
 
 @pytest.mark.parametrize("layers,lstep,tstep", [(1, 1, 1), (4, 1, 1), (4, 2, 1), (5, 2, 3),
                                                (32, 1, 100), (7, 7, 2), (6, 4, 1)])
-def test_action_matches_the_pseudocode_loop(layers, lstep, tstep):
+def test_action_matches_the_decode_loop_rule(layers, lstep, tstep):
     tokens = 2 * tstep + 1
-    want = pseudocode_loop(tokens, layers, lstep, tstep)
+    want = decode_loop_rule(tokens, layers, lstep, tstep)
     got = [oracle.decode_layer_action(layers, 0, lstep, tstep, t, l)
            for t in range(tokens) for l in range(layers)]
     assert got == want
