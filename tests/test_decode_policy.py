@@ -119,3 +119,24 @@ def test_library_rejects_invalid_policies():
     for t, l in [(-1, 0), (0, -1), (0, 4)]:
         with pytest.raises(kt.KtError):
             kt.kt_decode_layer_action(pol, t, l)
+
+
+# ---- the oracle's attention over a stored selection --------------------------
+
+@pytest.mark.parametrize("head_mode", [oracle.HEAD_SEPARATE, oracle.HEAD_SHARED])
+def test_attention_over_a_stored_selection_is_the_step_on_its_own_selection(head_mode):
+    import numpy as np
+
+    import synth
+    w = synth.custom(71, [128 * 9 + 40, 128 * 6], num_q_heads=4, num_kv_heads=2, top_k=3,
+                     head_mode=head_mode)
+    kv = oracle.KV.of(w)
+    ref = oracle.sparse_step(kv, w.q, w.params)
+    got = oracle.attend_selection(kv, w.q, w.params, ref["sel"], ref["cnt"])
+    assert np.allclose(got, ref["out"], rtol=1e-12, atol=1e-15)
+    # a different selection gives a different result (the ids are used)
+    sel2 = ref["sel"].copy()
+    sel2[0, 0, 0] = next(j for j in range(1, 9) if j not in set(ref["sel"][0, 0].tolist()))
+    sel2[0, 0].sort()
+    other = oracle.attend_selection(kv, w.q, w.params, sel2, ref["cnt"])
+    assert not np.allclose(other[0], got[0])
