@@ -35,7 +35,7 @@ EXPORTS = (
     "kt_selftest_bounded_wait", "kt_sparse_decode_attn_noalloc", "kt_sparse_decode_step_kernels",
     "kt_preselect_mask_words", "kt_preselect_blocks", "kt_score_select_blocks_presel",
     "kt_sparse_decode_step_presel", "kt_decode_history_slots", "kt_decode_layer_action",
-    "kt_decode_layer", "kt_append_kv",
+    "kt_decode_layer", "kt_append_kv", "kt_set_max_ctas",
 )
 
 
@@ -112,6 +112,7 @@ def _load():
         "kt_decode_layer": (ctypes.c_int, [P(ReusePolicy), i32, i32, vp, P(PagedKV), vp,
                                            P(SparseParams), vp, vp, vp, vp, sz, vp]),
         "kt_append_kv": (ctypes.c_int, [P(PagedKV), P(SparseParams), vp, vp, vp, vp, sz, vp]),
+        "kt_set_max_ctas": (ctypes.c_int, [i32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -297,6 +298,11 @@ def kt_sparse_decode_step_kernels(kv, params):
     if n < 0:
         raise KtError(-n, "kt_sparse_decode_step_kernels")
     return n
+
+
+def kt_set_max_ctas(max_ctas: int):
+    """Cap the CTAs of this thread's attention launches (0: one per SM)."""
+    _check(lib.kt_set_max_ctas(int(max_ctas)), "kt_set_max_ctas")
 
 
 def kt_sparse_decode_step_host(q_host, q_dev, kv, reps_pool, params, sel, cnt, out_dev,

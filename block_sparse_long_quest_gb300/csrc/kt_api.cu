@@ -209,6 +209,14 @@ int num_sms() {
   });
 }
 
+// CTAs an attention launch may use from this host thread: one per SM, or
+// fewer when the caller has set a cap (kt_set_max_ctas).
+thread_local int max_ctas_cap = 0;
+int cta_budget() {
+  const int sms = num_sms();
+  return (max_ctas_cap > 0 && max_ctas_cap < sms) ? max_ctas_cap : sms;
+}
+
 kt_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KT_OK : KT_ERR_CUDA; }
 
 template <class T>
@@ -264,7 +272,7 @@ kt_status attn_impl(const void* q, const kt_paged_kv* kv, int num_q_heads, float
   CUtensorMap kmap, vmap;
   if (!make_pool_map(&kmap, kv->k_pool, kv) || !make_pool_map(&vmap, kv->v_pool, kv))
     return KT_ERR_CUDA;
-  const int sms = num_sms();
+  const int sms = cta_budget();
   if (sms <= 0) return KT_ERR_CUDA;
   AttnLaunch a;
   std::memset(&a, 0, sizeof(a));
@@ -602,7 +610,7 @@ int32_t kt_sparse_decode_step_kernels(const kt_paged_kv* kv, const kt_sparse_par
   if (s != KT_OK) return -(int32_t)s;
   s = check_params(kv, p);
   if (s != KT_OK) return -(int32_t)s;
-  const int sms = num_sms();
+  const int sms = cta_budget();
   int ncpu = 0, chunk = 0, kk = 0;
   return (sms > 0 && fused_plan(kv, p, sms, &ncpu, &chunk, &kk)) ? 1 : 2;
 }
@@ -623,7 +631,7 @@ kt_status step_impl(const void* q, const kt_paged_kv* kv, const void* reps_pool,
     return KT_ERR_INVALID_ARG;
   const WsLayout L = layout(KT_OP_SPARSE_STEP, kv, p, 0);
   if (ws_bytes < L.total) return KT_ERR_WORKSPACE_TOO_SMALL;
-  const int sms = num_sms();
+  const int sms = cta_budget();
   int ncpu = 0, chunk = 0, kk = 0;
   if (sms > 0 && fused_plan(kv, p, sms, &ncpu, &chunk, &kk)) {
     // one launch: selection inside the attention kernel
@@ -853,6 +861,12 @@ kt_status kt_read_device_status(void* ws, size_t ws_bytes, kt_stream_t stream,
   if (cudaMemsetAsync(ws, 0, sizeof(v), st) != cudaSuccess) return KT_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return KT_ERR_CUDA;
   *device_status = v;
+  return KT_OK;
+}
+
+kt_status kt_set_max_ctas(int32_t max_ctas) {
+  if (max_ctas < 0) return KT_ERR_INVALID_ARG;
+  max_ctas_cap = max_ctas;
   return KT_OK;
 }
 

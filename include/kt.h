@@ -253,6 +253,20 @@ kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void
 int32_t kt_sparse_decode_step_kernels(const kt_paged_kv* kv, const kt_sparse_params* p);
 
 /*
+ * Caps the CTAs that the attention calls (kt_sparse_decode_attn,
+ * kt_sparse_decode_step, kt_decode_layer, kt_dense_decode_attn) launch from
+ * the calling host thread: at most max_ctas, and never fewer than one per
+ * (sequence, KV head) segment; 0 restores the default of one per SM.  A
+ * caller that runs other work beside the decode step can leave SMs to it.
+ * The split-K partition of each segment, and in the one-launch step the
+ * scoring slices, follow from the CTA count; outputs agree within rounding
+ * and selections outside the near-tie zone whatever the cap.  Host only,
+ * thread-local, takes effect at the next launch.  INVALID_ARG if max_ctas < 0.
+ * No counterpart in the article (a launch-shape setting of this library).
+ */
+kt_status kt_set_max_ctas(int32_t max_ctas);
+
+/*
  * Preselection [LC §4.4 "预选择 Preselect", §4.6 preselect_block()]: before
  * decoding, pick per selection unit a fixed set of Context blocks from the
  * attention of the last T prompt positions; later selections choose only

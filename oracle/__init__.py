@@ -231,6 +231,31 @@ def sparse_step(kv: KV, q, p, q_local=None, *, units=None, want_reps=True,
                 cnt=cnt, out=out, dyn_scores=dyn)
 
 
+def score_select_attend(kv: KV, q, p, rv, *, units=None):
+    """Score, select and attend ([LC §3.1, §4.3, §4.5, §4.6]) over given
+    representative values rv [B][max_blocks][H_kv][R][d] (double, by logical
+    block); returns unit_scores, sel, cnt, out as sparse_step does."""
+    pp = params(p)
+    B, H_kv, d, MB = kv.B, kv.H_kv, kv.d, kv.max_blocks
+    R = reps_per_block(p, kv.bs)
+    rv = np.ascontiguousarray(rv, dtype=np.float64)
+    if rv.shape != (B, MB, H_kv, R, d):
+        raise ValueError(f"rv must be [B][max_blocks][H_kv][R][d] = {(B, MB, H_kv, R, d)}")
+    SEL = 1 if p.head_mode == HEAD_SHARED else H_kv
+    lo, hi = (0, SEL) if units is None else units
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    us = np.full((B, SEL, MB), np.nan, dtype=np.float64)
+    sel = np.full((B, SEL, max(p.top_k, 1)), -1, dtype=np.int32)
+    cnt = np.zeros((B, SEL), dtype=np.int32)
+    out = np.zeros((B, p.num_q_heads, d), dtype=np.float64)
+    rc = lib().orc_score_select_attend(ctypes.byref(kv.s), q.ctypes.data, ctypes.byref(pp),
+                                       rv.ctypes.data, us.ctypes.data, sel.ctypes.data,
+                                       cnt.ctypes.data, out.ctypes.data, lo, hi)
+    if rc != 0:
+        raise ValueError("oracle rejected the parameters")
+    return dict(unit_scores=us, sel=sel, cnt=cnt, out=out)
+
+
 def avg_pool1d(x, kernel: int) -> np.ndarray:
     """Zero-padded average pooling, window kernel (odd), stride 1 [LC §4.6]."""
     x = np.ascontiguousarray(x, dtype=np.float64)

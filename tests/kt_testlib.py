@@ -211,3 +211,98 @@ def check_dynamic_reps(dw, ref_scores, zone=ZONE, heads=None):
                 else:
                     differ += 1
     return checked, differ, bad
+
+
+def unit_heads(w, u):
+    """Query heads whose selection unit is u."""
+    G = w.params.num_q_heads // w.num_kv_heads
+    if w.params.head_mode == synth.HEAD_SHARED:
+        return list(range(w.params.num_q_heads))
+    return list(range(u * G, (u + 1) * G))
+
+
+def check_units(w, kv, sel, cnt, out, ref, units, batches=None):
+    """Selection and output of units [units[0], units[1]) of every sequence.
+
+    The selected set must equal the oracle's outside the near-tie zone
+    (selection_agrees).  The output of the unit's query heads is compared with
+    the oracle's output when the sets are equal; when they differ only inside
+    the zone the GPU made another valid selection, and its output is compared
+    with the oracle's attention over that (just validated) set, so no unit's
+    output goes unchecked.  Returns (#units with equal sets, #units with a
+    valid zone difference)."""
+    p = w.params
+    n_exact = n_zone = 0
+    for b in (range(w.batch) if batches is None else batches):
+        nb, c0, c1 = oracle.partition(int(w.seq_lens[b]), p.initial_blocks, p.local_blocks)
+        for u in range(units[0], units[1]):
+            ok, exact = selection_agrees(sel, cnt, ref, b, u)
+            assert ok, (b, u, sel[b, u], ref["sel"][b, u])
+            heads = unit_heads(w, u)
+            if exact:
+                want = ref["out"][b, heads]
+                n_exact += 1
+            else:
+                blocks = list(range(c0)) + [int(j) for j in sel[b, u, :int(cnt[b, u])]] + \
+                    list(range(c1, nb))
+                want = np.stack([oracle.attend(kv, b, hq, p.num_q_heads, w.q[b, hq], blocks,
+                                               p.softmax_scale) for hq in heads])
+                n_zone += 1
+            err = row_rel_err(out[b, heads], want)
+            assert err.max() <= TOL, (b, u, err.max())
+    return n_exact, n_zone
+
+
+def parallel(fn, jobs, threads=16):
+    """fn over jobs in host threads (the oracle's C calls release the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=min(threads, max(1, len(jobs)))) as ex:
+        return list(ex.map(fn, jobs))
+
+
+def dynamic_oracle_scores(w, kv, heads=None):
+    """Oracle token scores [B][H_kv][max_blocks*128] of the given KV heads (all
+    by default), one host thread per (sequence, KV head)."""
+    B, H_kv = w.batch, w.num_kv_heads
+    heads = range(H_kv) if heads is None else heads
+    out = np.zeros((B, H_kv, w.max_blocks * 128))
+    jobs = [(b, h) for b in range(B) for h in heads]
+    res = parallel(lambda bh: oracle.dynamic_token_scores(kv, w.params, bh[0], bh[1],
+                                                          w.q_local[bh[0]]), jobs)
+    for (b, h), r in zip(jobs, res):
+        out[b, h, :r.size] = r
+    return out
+
+
+def rep_values_of_gpu_tokens(w, dw):
+    """[B][max_blocks][H_kv][R][128] (double): the key rows, taken from the
+    input K, of the tokens whose rows the GPU chose as Dynamic reps.  Call it
+    after check_dynamic_reps has shown every choice to be valid."""
+    R = w.params.num_reps
+    got = dw.reps_view()
+    rv = np.zeros((w.batch, w.max_blocks, w.num_kv_heads, R, 128))
+    for b in range(w.batch):
+        for j in range(int(w.seq_lens[b]) // 128):
+            page = w.block_table[b, j]
+            for h in range(w.num_kv_heads):
+                toks = dynamic_rep_tokens(w, got, b, j, h)
+                assert -1 not in toks, (b, j, h)
+                rows = w.k_pool[page, h, toks]
+                rv[b, j, h] = rows.view(np.float16).astype(np.float64)
+    return rv
+
+
+def oracle_step_by_unit(w, kv, units, **kw):
+    """oracle.sparse_step of each unit in `units` (SEPARATE) in parallel host
+    threads, merged into one result (reps, unit_scores, sel, cnt, out)."""
+    res = parallel(lambda u: oracle.sparse_step(kv, w.q, w.params, w.q_local, units=(u, u + 1),
+                                                **kw), list(units))
+    ref = res[0]
+    G = w.params.num_q_heads // w.num_kv_heads
+    for u, r in zip(units, res):
+        for key in ("unit_scores", "sel", "cnt"):
+            ref[key][:, u] = r[key][:, u]
+        ref["out"][:, u * G:(u + 1) * G] = r["out"][:, u * G:(u + 1) * G]
+        if ref.get("reps") is not None:
+            ref["reps"][:, :, u] = r["reps"][:, :, u]
+    return ref

@@ -1,12 +1,13 @@
 """GPU parity of the Dynamic representative build (accumulated softmax scores of
-the last T queries; the best tokens of each block) against the oracle."""
+the last T queries; the best tokens of each block) against the oracle, and of
+the decode step over Dynamic reps."""
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from kt_testlib import (TOL, DevWorkload, build_dynamic, check_dynamic_reps, row_rel_err,
-                        selection_agrees)
+from kt_testlib import (DevWorkload, build_dynamic, check_dynamic_reps, check_units,
+                        rep_values_of_gpu_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -36,19 +37,26 @@ def test_dynamic_token_scores_and_reps(G, T, R):
     assert checked > 0 and not bad, bad[:3]
 
 
-def test_dynamic_full_step_selection_and_output():
+@pytest.mark.parametrize("mode", [synth.HEAD_SHARED, synth.HEAD_SEPARATE])
+def test_dynamic_full_step_selection_and_output(mode):
+    """Every block's reps are checked against the oracle's token scores (a
+    token inside the 1e-5 zone of the block's cut may stand in for another);
+    the oracle then scores the blocks with the reps the GPU chose, and every
+    unit's selection and output is compared (check_units).  When no rep
+    differs, that is exactly the oracle's own step."""
     w = synth.custom(52, [128 * 40 + 17, 128 * 25], num_q_heads=8, num_kv_heads=2,
                      rep=synth.REP_DYNAMIC, num_reps=4, local_queries=16, top_k=5,
-                     head_mode=synth.HEAD_SHARED, num_needles=2)
+                     head_mode=mode, num_needles=2)
     dw = DevWorkload(w)
     build_dynamic(dw)
-    ref = oracle.sparse_step(oracle.KV.of(w), w.q, w.params, w.q_local, want_dyn_scores=True)
-    checked, differ, bad = check_dynamic_reps(dw, ref["dyn_scores"])
-    assert not bad
+    kv = oracle.KV.of(w)
+    own = oracle.sparse_step(kv, w.q, w.params, w.q_local, want_dyn_scores=True)
+    checked, differ, bad = check_dynamic_reps(dw, own["dyn_scores"])
+    assert checked > 0 and not bad, bad[:3]
+    ref = oracle.score_select_attend(kv, w.q, w.params, rep_values_of_gpu_tokens(w, dw))
+    if differ == 0:
+        assert np.array_equal(ref["sel"], own["sel"]) and np.array_equal(ref["cnt"], own["cnt"])
     sel, cnt, out, ws = dw.step()
-    sel, cnt, out = sel.cpu().numpy(), cnt.cpu().numpy(), out.cpu().numpy()
-    for b in range(2):
-        ok, exact = selection_agrees(sel, cnt, ref, b, 0)
-        assert ok or differ, (sel[b, 0], ref["sel"][b, 0])
-        if exact:
-            assert row_rel_err(out[b], ref["out"][b]).max() <= TOL
+    exact, zone = check_units(w, kv, sel.cpu().numpy(), cnt.cpu().numpy(), out.cpu().numpy(),
+                              ref, (0, dw.SEL))
+    assert exact + zone == w.batch * dw.SEL

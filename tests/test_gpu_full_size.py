@@ -1,18 +1,20 @@
 """Parity at the workloads' full sizes, through kt_sparse_decode_step (the call
-bench.py times), against the oracle on sampled outputs: all reps, and the
-selection and attention output of the sampled selection units.
+bench.py times), against the oracle: reps bit for bit, and the selection and
+attention output of every selection unit (check_units).
 
-Sizes: 128K tokens (32/8 heads, SHARED), 1M tokens (SEPARATE; KV heads 0-1
-checked), 16 paged sequences of 8K-64K tokens (every rep method and head mode),
-and the Dynamic 128K layer (KV head 0's token scores and reps).
+Sizes: 128K tokens (32/8 heads, SHARED), 1M tokens (SEPARATE, all 8 KV heads,
+the oracle run per head in parallel host threads), 16 paged sequences of
+8K-64K tokens (every rep method and head mode), and the Dynamic 128K layer
+(token scores and reps of every KV head, then the step).
 """
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from kt_testlib import (TOL, DevWorkload, build_dynamic, check_dynamic_reps, check_reps,
-                        row_rel_err, selection_agrees)
+from kt_testlib import (TOL, DevWorkload, build_dynamic, check_dynamic_reps, check_units,
+                        dynamic_oracle_scores, oracle_step_by_unit, rep_values_of_gpu_tokens,
+                        row_rel_err)
 
 pytestmark = pytest.mark.gpu
 
@@ -25,43 +27,31 @@ def _gpu():
     import block_sparse_long_quest_gb300  # noqa: F401
 
 
-def _check_step(w, dw, units):
-    """Selection + output of the given units against the oracle."""
+def _check_reps(w, dw, ref, heads):
+    got = dw.reps_view()
+    R = w.params.reps_per_block()
+    for b in range(w.batch):
+        for j in range(int(w.seq_lens[b]) // 128):
+            for h in heads:
+                a = got[w.block_table[b, j], h]
+                r = ref["reps"][b, j, h]
+                if w.params.rep == synth.REP_MEAN:
+                    assert np.array_equal(a.reshape(-1).view(np.uint32),
+                                          r.reshape(-1).view(np.uint32)), (b, j, h)
+                else:
+                    assert np.array_equal(a, r.reshape(R, 128)), (b, j, h)
+
+
+def _check_step(w, dw, ref):
+    """Every unit's selection and output; the reps of every KV head."""
     import block_sparse_long_quest_gb300 as kt
     sel, cnt, out, ws = dw.step()
     assert kt.kt_read_device_status(ws) == kt.KT_OK
-    ref = oracle.sparse_step(oracle.KV.of(w), w.q, w.params, w.q_local, units=units)
-    if w.params.rep != synth.REP_DYNAMIC:
-        # reps of the sampled units' KV heads, bit for bit
-        got = dw.reps_view()
-        R = w.params.reps_per_block()
-        heads = range(w.num_kv_heads) if w.params.head_mode == synth.HEAD_SHARED \
-            else range(units[0], units[1])
-        for b in range(w.batch):
-            for j in range(int(w.seq_lens[b]) // 128):
-                for h in heads:
-                    a = got[w.block_table[b, j], h]
-                    r = ref["reps"][b, j, h]
-                    if w.params.rep == synth.REP_MEAN:
-                        assert np.array_equal(a.reshape(-1).view(np.uint32),
-                                              r.reshape(-1).view(np.uint32))
-                    else:
-                        assert np.array_equal(a, r.reshape(R, 128)), (b, j, h)
-    sel, cnt, out = sel.cpu().numpy(), cnt.cpu().numpy(), out.cpu().numpy()
-    G = w.params.num_q_heads // w.num_kv_heads
-    compared = 0
-    for b in range(w.batch):
-        for u in range(units[0], units[1]):
-            ok, exact = selection_agrees(sel, cnt, ref, b, u)
-            assert ok, (b, u, sel[b, u], ref["sel"][b, u])
-            if exact:
-                heads = range(w.params.num_q_heads) if w.params.head_mode == synth.HEAD_SHARED \
-                    else range(u * G, (u + 1) * G)
-                err = row_rel_err(out[b, list(heads)], ref["out"][b, list(heads)])
-                assert err.max() <= TOL, err.max()
-                compared += 1
-    assert compared > 0
-    return ref
+    _check_reps(w, dw, ref, range(w.num_kv_heads))
+    kv = oracle.KV.of(w)
+    exact, zone = check_units(w, kv, sel.cpu().numpy(), cnt.cpu().numpy(), out.cpu().numpy(),
+                              ref, (0, dw.SEL))
+    assert exact + zone == w.batch * dw.SEL
 
 
 def test_128k_shared_quest_full_size():
@@ -70,15 +60,15 @@ def test_128k_shared_quest_full_size():
     dw = DevWorkload(w)
     dw.build_reps()
     assert kt.kt_sparse_decode_step_kernels(dw.kv, dw.params) == 1
-    _check_step(w, dw, (0, 1))
+    _check_step(w, dw, oracle.sparse_step(oracle.KV.of(w), w.q, w.params))
 
 
 @pytest.mark.parametrize("rep", [synth.REP_QUEST, synth.REP_MAX, synth.REP_FIX])
-def test_1m_separate_full_size_sampled_heads(rep):
+def test_1m_separate_full_size_every_head(rep):
     w = synth.long1m(rep=rep)
     dw = DevWorkload(w)
     dw.build_reps()
-    _check_step(w, dw, (0, 2))
+    _check_step(w, dw, oracle_step_by_unit(w, oracle.KV.of(w), range(w.num_kv_heads)))
 
 
 @pytest.mark.parametrize("rep", [synth.REP_MAX, synth.REP_MEAN, synth.REP_QUEST, synth.REP_FIX])
@@ -87,19 +77,38 @@ def test_batched_paged_full_size(rep, mode):
     w = synth.batched(rep=rep, head_mode=mode)
     dw = DevWorkload(w)
     dw.build_reps()
-    units = (0, 1) if mode == synth.HEAD_SHARED else (0, 8)
-    _check_step(w, dw, units)
+    _check_step(w, dw, oracle.sparse_step(oracle.KV.of(w), w.q, w.params))
 
 
-def test_dynamic_128k_full_size_head0():
+def test_dynamic_128k_full_size_step():
+    """The Dynamic 128K layer end to end: token scores and reps of every KV
+    head against the oracle, then the one-launch step's selection and output.
+    Reps whose token scores sit within the 1e-5 zone of a block's cut may be
+    either token; the oracle scores the blocks with the tokens the GPU chose
+    once each choice has been shown valid, so the step is compared on the reps
+    it used.  The gap to dense attention over the same KV is printed (a
+    reported figure, not a bound)."""
+    import block_sparse_long_quest_gb300 as kt
     w = synth.dynamic128k()
     dw = DevWorkload(w)
     got = build_dynamic(dw)
     kv = oracle.KV.of(w)
-    ref0 = oracle.dynamic_token_scores(kv, w.params, 0, 0, w.q_local[0])
-    assert np.abs(got[0, 0, :ref0.size] - ref0).max() <= 1e-4 * ref0.max()
-    # reps of KV head 0 for every full block, against the oracle's choice
-    scores = np.zeros((1, w.num_kv_heads, w.max_blocks * 128))
-    scores[0, 0, :ref0.size] = ref0
-    checked, differ, bad = check_dynamic_reps(dw, scores, heads=[0])
-    assert checked == 1024 and not bad, bad[:3]
+    ref_scores = dynamic_oracle_scores(w, kv)
+    n = int(w.seq_lens[0])
+    for h in range(w.num_kv_heads):
+        r = ref_scores[0, h, :n]
+        assert np.abs(got[0, h, :n] - r).max() <= 1e-4 * r.max(), h
+    checked, differ, bad = check_dynamic_reps(dw, ref_scores)
+    assert checked == 1024 * w.num_kv_heads and not bad, bad[:3]
+    ref = oracle.score_select_attend(kv, w.q, w.params, rep_values_of_gpu_tokens(w, dw))
+    assert kt.kt_sparse_decode_step_kernels(dw.kv, dw.params) == 1
+    sel, cnt, out, ws = dw.step()
+    assert kt.kt_read_device_status(ws) == kt.KT_OK
+    out = out.cpu().numpy()
+    exact, zone = check_units(w, kv, sel.cpu().numpy(), cnt.cpu().numpy(), out, ref, (0, 1))
+    assert exact + zone == 1
+    dense, ws_d = dw.dense()
+    assert kt.kt_read_device_status(ws_d) == kt.KT_OK
+    gap = row_rel_err(out[0], dense.cpu().numpy()[0])
+    print(f"dynamic 128K: {differ} of {checked} blocks' reps differ inside the zone; "
+          f"sparse vs dense max row rel err {gap.max():.3e}, median {np.median(gap):.3e}")

@@ -502,3 +502,20 @@ def test_step_restricted_selection_is_top_k_of_the_preselection():
         sc = got["unit_scores"][0, u]
         want = sorted(sorted(cand, key=lambda j: (-sc[j], j))[:3])
         assert got["cnt"][0, u] == 3 and list(got["sel"][0, u, :3]) == want
+
+
+def test_score_select_attend_over_own_reps_is_the_step():
+    # the entry that takes representative values reproduces the step when
+    # given the oracle's own reps (Quest, SEPARATE, ragged batch)
+    w = synth.custom(45, [128 * 14 + 9, 128 * 8], num_q_heads=8, num_kv_heads=2,
+                     rep=synth.REP_QUEST, head_mode=synth.HEAD_SEPARATE, top_k=3)
+    kv = oracle.KV.of(w)
+    ref = oracle.sparse_step(kv, w.q, w.params)
+    R = w.params.reps_per_block()
+    rv = np.zeros((w.batch, w.max_blocks, 2, R, 128))
+    for b in range(w.batch):
+        for j in range(int(w.seq_lens[b]) // 128):
+            rv[b, j] = decode(ref["reps"][b, j])
+    got = oracle.score_select_attend(kv, w.q, w.params, rv)
+    assert np.array_equal(got["sel"], ref["sel"]) and np.array_equal(got["cnt"], ref["cnt"])
+    assert np.array_equal(got["out"], ref["out"])
