@@ -387,6 +387,8 @@ def main():
     ap.add_argument("--no-1m", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dynamic", action="store_true")
+    ap.add_argument("--phase-stamps", action="store_true",
+                    help="add per-phase timings of single step launches (phase_us)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -477,6 +479,9 @@ def main():
     e2e_value = world * bytes_step["total"] * n_e2e / t_e2e / 1e9
 
     extra = {}
+    if args.phase_stamps:
+        extra["phase_us"] = {"128k": phase_stamps_leg(steps_fns)}
+
     # ---- representative build (amortised, outside the step): Quest reps of one
     # 128K layer; algorithmic bytes = K read once + reps written
     L0 = layers[0]
@@ -532,6 +537,9 @@ def main():
                          "gbs": b1["total"] / per_layer / 1e9,
                          "bytes_per_layer_step": b1["total"]}
             wq.params.rep = synth.REP_QUEST
+            if args.phase_stamps:
+                extra.setdefault("phase_us", {})[f"1m_{name}"] = phase_stamps_leg(
+                    [lambda L=L, r=r: L.step(r) for L in big])
         extra["at_1m"] = {"workload": "1m-gqa4-separate-k32 (4 layers, 1048576 tokens each)",
                           **res}
         del big
@@ -685,6 +693,45 @@ def preselect_leg(args, stream):
             "preselect_us": t_p / n_p * 1e6, "step_us": t_s / n_s * 1e6,
             "step_gbs": total / (t_s / n_s) / 1e9, "step_bytes": total,
             "note": "the restricted step still scores every Context block; only the 96 compete"}
+
+
+PHASES = ("entry", "slice_pages", "slice_reps_landed", "slice_scored", "slice_published",
+          "unit_slices_seen", "selection_picked", "first_kv_load", "first_selected_load",
+          "last_block_attended", "partial_published", "partials_seen", "output_written")
+
+
+def phase_stamps_leg(step_fns, launches=40):
+    """Per-CTA phase stamps (kt_set_phase_stamps) of single step launches, in
+    us after the launch's first CTA entry: for each phase the median over CTAs
+    (and the latest CTA), each the median over `launches` launches."""
+    import torch
+
+    import block_sparse_long_quest_gb300 as kt
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    buf = torch.zeros(sms * 16, dtype=torch.int64, device="cuda")
+    med = {ph: [] for ph in PHASES}
+    last = {ph: [] for ph in PHASES}
+    kt.kt_set_phase_stamps(buf, sms)
+    try:
+        for i in range(launches + 5):
+            buf.zero_()
+            step_fns[i % len(step_fns)]()
+            torch.cuda.synchronize()
+            if i < 5:
+                continue
+            st = buf.view(sms, 16).cpu().numpy().astype(np.float64)
+            t0 = st[:, 0][st[:, 0] > 0].min()
+            for k, ph in enumerate(PHASES):
+                col = st[:, k]
+                col = col[col > 0]
+                if col.size:
+                    med[ph].append(float(np.median(col - t0)) / 1e3)
+                    last[ph].append(float((col - t0).max()) / 1e3)
+    finally:
+        kt.kt_set_phase_stamps(None)
+    return {ph: {"median_cta_us": round(float(np.median(med[ph])), 3),
+                 "last_cta_us": round(float(np.median(last[ph])), 3)}
+            for ph in PHASES if med[ph]}
 
 
 def layers_q_bytes(w):

@@ -35,7 +35,7 @@ EXPORTS = (
     "kt_selftest_bounded_wait", "kt_sparse_decode_attn_noalloc", "kt_sparse_decode_step_kernels",
     "kt_preselect_mask_words", "kt_preselect_blocks", "kt_score_select_blocks_presel",
     "kt_sparse_decode_step_presel", "kt_decode_history_slots", "kt_decode_layer_action",
-    "kt_decode_layer", "kt_append_kv", "kt_set_max_ctas",
+    "kt_decode_layer", "kt_append_kv", "kt_set_max_ctas", "kt_set_phase_stamps",
 )
 
 
@@ -113,6 +113,7 @@ def _load():
                                            P(SparseParams), vp, vp, vp, vp, sz, vp]),
         "kt_append_kv": (ctypes.c_int, [P(PagedKV), P(SparseParams), vp, vp, vp, vp, sz, vp]),
         "kt_set_max_ctas": (ctypes.c_int, [i32]),
+        "kt_set_phase_stamps": (ctypes.c_int, [vp, i32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -298,6 +299,16 @@ def kt_sparse_decode_step_kernels(kv, params):
     if n < 0:
         raise KtError(-n, "kt_sparse_decode_step_kernels")
     return n
+
+
+def kt_set_phase_stamps(stamps, max_ctas: int = 0):
+    """Record per-CTA phase stamps of this thread's attention launches into a
+    uint64 device tensor of >= max_ctas * 16 entries (None: off)."""
+    if stamps is None:
+        _check(lib.kt_set_phase_stamps(None, 0), "kt_set_phase_stamps")
+    else:
+        _check(lib.kt_set_phase_stamps(_ptr(stamps), int(max_ctas or stamps.numel() // 16)),
+               "kt_set_phase_stamps")
 
 
 def kt_set_max_ctas(max_ctas: int):

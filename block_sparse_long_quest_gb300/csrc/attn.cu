@@ -71,7 +71,7 @@ struct SmemLayout {
   static constexpr int cum = scratch + SCRATCH_FLOATS * 4;  // [MAX_SEGS+1] work prefix
   static constexpr int info = cum + (MAX_SEGS + 1) * 4;
   static constexpr int bars = (info + STAGES * (int)sizeof(StageInfo) + 15) & ~15;
-  static constexpr int bcast = bars + (2 * STAGES + 5) * 8;
+  static constexpr int bcast = bars + (2 * STAGES + 6) * 8;
   static constexpr int total = bcast + 64 * 4;
 };
 constexpr int SMEM_BYTES = SmemLayout::total + 1024;  // + alignment slack
@@ -98,15 +98,22 @@ struct Params {
   const void* reps;
   int rep, R, ncpu, f_chunk, kk_f;
   unsigned long long* f_cand;
-  int* f_cand_pages;
-  int* f_counters;
-  int* f_polled;
+  int f_cand_len;
+  uint32_t* f_cpage;
+  int* f_sync;
   int32_t* sel_out;
   int32_t* cnt_out;
   const uint32_t* presel_mask;
   const int32_t* presel_cnt;
   int mask_words;
+  unsigned long long* stamps;
 };
+
+// Phase stamp i of this CTA (global timer, ns) when stamps are requested.
+#define KT_STAMP(p, i)                                                                  \
+  do {                                                                                  \
+    if ((p).stamps) (p).stamps[(size_t)blockIdx.x * KT_PHASE_STAMPS + (i)] = globaltimer(); \
+  } while (0)
 
 struct Part {
   int n, nb, c0, c1;
@@ -277,8 +284,14 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
                             uint32_t ring_u32, uint32_t bar_reps) {
   const int U = p.B * p.SEL;
   const int u = blockIdx.x / p.ncpu;
+  // this launch's slot tag, which every CTA needs for the pick
+  const uint32_t epoch = ctid == 0 ? ld_relaxed_gpu_u32(p.f_sync) : 0u;
   if (u >= U) {
-    if (ctid == 0) mbar_arrive(bar_scored);
+    if (ctid == 0) {
+      sh_int[12] = (int)(1u + epoch % FUSED_TAG_CYCLE);
+      sh_int[15] = (int)(1u + epoch % 0xFFFFFFFEu);  // partial tag (never 0)
+      mbar_arrive(bar_scored);
+    }
     return;
   }
   const int cs = blockIdx.x % p.ncpu;
@@ -298,20 +311,20 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     const int j = js + i;
     pgs[i] = j < p.max_blocks ? __ldg(p.table + (size_t)bu * p.max_blocks + j) : -1;
   }
-  // the slice's candidate slots start empty (key 0, page -1): keys of equal
-  // value share a rank and empty keys are never written, so some may stay so
+  // the slice's candidate and page slots, each written once below with this
+  // launch's tag
   unsigned long long* cand = p.f_cand + ((size_t)u * p.ncpu + cs) * p.kk_f;
-  int* cpage = p.f_cand_pages + ((size_t)u * p.ncpu + cs) * p.kk_f;
-#pragma unroll 1
-  for (int i = ctid; i < p.kk_f; i += NCT) {
-    cand[i] = 0ull;
-    cpage[i] = -1;
-  }
+  uint32_t* cpage = p.f_cpage + ((size_t)u * p.ncpu + cs) * p.kk_f;
   const Part pu = partition(seq_len(p, bu), p.I_b, p.L_b);
   const int je = min(js + p.f_chunk, pu.c1);
   const int nloc = max(0, je - js);  // js >= c0 whenever the slice is not empty
-  if (ctid == 0 && (nloc & 1)) keys[nloc] = 0ull;  // the ranking's zero padding
+  if (ctid == 0) {
+    if (nloc & 1) keys[nloc] = 0ull;  // the ranking's zero padding
+    sh_int[12] = (int)(1u + epoch % FUSED_TAG_CYCLE);
+    sh_int[15] = (int)(1u + epoch % 0xFFFFFFFEu);  // partial tag (never 0)
+  }
   bar_c();
+  if (ctid == 0) KT_STAMP(p, 1);
   if (nloc > 0) {
     // the slice's representative rows, staged into the (still idle) KV ring by
     // bulk copies in rounds of up to ring-size bytes, then scored from there
@@ -362,6 +375,7 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     for (int r = 0; r < nrounds; ++r) {
       const int r0 = r * rcap, nr = min(rcap, nloc - r0);
       mbar_wait((r & 1) ? bar_reps + 8 : bar_reps, (uint32_t)(r >> 1) & 1u, p.status);
+      if (r == 0 && ctid == 0) KT_STAMP(p, 2);
       const uint32_t base = ring_u32 + buf_off(r);
       const uint4* sbuf = reinterpret_cast<const uint4*>(ring + buf_off(r));
 #define KT_SCORE(NV, F) selc::score_linear_smem<NV, F, CONSUMERS>(sbuf, (int)(sb / 16), nr, js + r0, p.P, pgs + r0, wts, V, keys + r0, warp, lane, p.status)
@@ -398,9 +412,14 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
       if (r + 2 < nrounds) issue(r + 2);
     }
   }
-  if (ctid == 0) mbar_arrive(bar_scored);  // the producer may start its own loads
-  // the slice's best min(nloc, kk_f) keys, written in descending key order
-  // (empty slots: key 0, page -1), then the ticket
+  if (ctid == 0) {
+    mbar_arrive(bar_scored);  // the producer may start its own loads
+    KT_STAMP(p, 3);
+  }
+  // the slice's best min(nloc, kk_f) keys as tagged slots, in descending key
+  // order, then its empty slots; no fence: readers check each slot's tag
+  const uint32_t tag = (uint32_t)sh_int[12];
+  int nreal = nloc;
   bool few = nloc <= p.kk_f;  // every key of the slice is a candidate
   if (p.presel_mask) {
     // preselection: blocks outside it get key 0, the empty slot; with at most
@@ -418,13 +437,14 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     bar_c();
     if (lane == 0) atomicAdd(&sh_int[3], real);
     bar_c();
-    few = few || sh_int[3] <= p.kk_f;
+    nreal = sh_int[3];
+    few = few || nreal <= p.kk_f;
   }
   // SK_COLS launches have slices of at most top_k blocks: always `few`
   if (SK != SK_COLS && !few) {
     auto emit = [&](int r, int i) {
-      cand[r] = keys[i];
-      cpage[r] = pgs[i];
+      st_relaxed_gpu_u64(cand + r, fused_slot(keys[i], tag));
+      st_relaxed_gpu_u32(cpage + r, ((uint32_t)pgs[i] & 0xFFFFFu) << FUSED_TAG_BITS | tag);
     };
     unsigned long long* ck = reinterpret_cast<unsigned long long*>(scr + Ls.bkey);
     int* ci = reinterpret_cast<int*>(scr + Ls.bidx);
@@ -442,179 +462,95 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
       if (key != 0ull) {
         const int r = selc::count_greater(keys, npad, key);
         if (r < p.kk_f) {
-          cand[r] = key;
-          cpage[r] = pgs[i];
+          st_relaxed_gpu_u64(cand + r, fused_slot(key, tag));
+          st_relaxed_gpu_u32(cpage + r, ((uint32_t)pgs[i] & 0xFFFFFu) << FUSED_TAG_BITS | tag);
         }
       }
     }
+#pragma unroll 1
+    for (int r = nreal + ctid; r < p.kk_f; r += NCT) {
+      st_relaxed_gpu_u64(cand + r, tag);
+      st_relaxed_gpu_u32(cpage + r, tag);
+    }
   }
-  bar_c();
-  if (ctid == 0) red_release_gpu_add(p.f_counters + u, 1);
+  // the slots carry their own validity; a fence after the CTA's stores only
+  // pushes them out to L2 now rather than whenever the SM drains them
+  if (ctid == 0) KT_STAMP(p, 4);
 }
 
-// Fused step, consumer warps of every CTA: wait (bounded) for every scoring
-// slice of this segment's selection unit, pick the unit's top-k from the
-// candidate table, order the chosen blocks by id and keep this CTA's share
-// [i0, i1) of their page ids in the merge area's slice.  One CTA per unit
-// writes sel / cnt.  Returns i1 - i0.
-//
-// The per-slice lists are sorted, so the keff-th largest of their first J
-// keys (J lists' heads, ncpu * J >= keff) is a lower bound T0 for the unit's
-// keff-th largest key: only keys >= T0 can be chosen, and they are few
-// (at most keff / J lists reach T0 at their J-th key).  Those are ranked
-// exactly by counting; the same keys as the selection kernel give the same
-// blocks.
+// Fused step, consumer warps of every CTA: read the candidate slots of this
+// segment's selection unit until each carries this launch's tag (one round of
+// loads once the unit's slices are published; no fence on either side), find
+// the threshold of the unit's top keff keys (kth_largest_reg: keys held in
+// registers, ties to the lower block as the keys order them), order the
+// chosen blocks by id and return this CTA's share [i0, i0 + n) of them: n,
+// with i0 in *i0_out.  The ascending ids stay in the pick layout's `sorted`
+// array, where the producer reads them.  One CTA per unit writes sel / cnt.
 template <class Bar>
-__device__ int fused_merge(const Params& p, uint8_t* scr, unsigned int* hist,
-                           unsigned long long* sh_u64, int* sh_int, int b, int h, int ci,
-                           int ncta, int ctid, Bar bar_c) {
+__device__ int fused_pick(const Params& p, uint8_t* scr, unsigned long long* sh_u64, int* sh_int,
+                          int b, int h, int ci, int ncta, int ctid, Bar bar_c, int* i0_out,
+                          uint32_t bar_seen) {
   const int unit = b * p.SEL + (p.SEL == 1 ? 0 : h);
   const Part pt = partition(seq_len(p, b), p.I_b, p.L_b);
   int keff = min(p.top_k, pt.c1 - pt.c0);
   if (p.presel_mask) keff = min(keff, max(0, __ldg(p.presel_cnt + unit)));
-  if (ctid == 0) {
-    const uint64_t t0 = globaltimer();
-    for (uint32_t i = 0;; ++i) {
-      if (ld_acquire_gpu(p.f_counters + unit) >= p.ncpu) break;
-      if ((i & 63u) == 63u && globaltimer() - t0 > WAIT_LIMIT_NS) {
-        set_status(p.status, KT_ERR_TIMEOUT);
-        break;
-      }
-      __nanosleep(32);
-    }
-  }
-  bar_c();
-  const int kk = p.kk_f, nslots = p.ncpu * kk;
-  const FusedMergeLayout Lm = fused_merge_layout(p.ncpu, kk, min(p.top_k, nslots));
-  unsigned long long* all = reinterpret_cast<unsigned long long*>(scr + Lm.all);
-  int* allp = reinterpret_cast<int*>(scr + Lm.allp);
-  unsigned long long* heads = reinterpret_cast<unsigned long long*>(scr + Lm.heads);
-  unsigned long long* ckey = reinterpret_cast<unsigned long long*>(scr + Lm.ck);
-  int* cslot = reinterpret_cast<int*>(scr + Lm.cs);
-  int* idx = reinterpret_cast<int*>(scr + Lm.idx);
-  uint32_t* cid = reinterpret_cast<uint32_t*>(scr + Lm.cid);
-  int* slice = reinterpret_cast<int*>(scr + Lm.slice);
+  const int nslots = p.ncpu * p.kk_f, kmax = min(p.top_k, nslots), kpad = (kmax + 3) & ~3;
+  const FusedPickLayout Lp = fused_pick_layout(nslots, kmax);
+  uint32_t* ids = reinterpret_cast<uint32_t*>(scr + Lp.ids);
+  int* pages = reinterpret_cast<int*>(scr + Lp.pages);
+  int* sorted = reinterpret_cast<int*>(scr + Lp.sorted);
+  int* sorted_pages = reinterpret_cast<int*>(scr + Lp.sorted_pages);
   const bool writer = ci == 0 && (p.SEL != 1 || h == 0);
+  const uint32_t tag = (uint32_t)sh_int[12];
+  if (ctid == 0) sh_int[13] = 0;
+#pragma unroll 1
+  for (int i = ctid; i < kpad; i += NCT) ids[i] = 0xFFFFFFFFu;
+  // every slot of the unit, read until all carry the tag (bounded)
+  constexpr int GP = FUSED_GATHER_PER_THREAD;
+  const unsigned long long* src = p.f_cand + (size_t)unit * nslots;
+  const uint32_t* srcp = p.f_cpage + (size_t)unit * nslots;
+  unsigned long long kx[GP];
+  uint32_t px[GP];
+  bool ok = false;
+  const uint64_t t0 = globaltimer();
+#pragma unroll 1
+  for (;;) {
+    ok = true;
+#pragma unroll
+    for (int r = 0; r < GP; ++r) {
+      const int s = ctid + r * NCT;
+      kx[r] = s < nslots ? ld_relaxed_gpu_u64(src + s) : static_cast<unsigned long long>(tag);
+      px[r] = s < nslots ? ld_relaxed_gpu_u32(srcp + s) : tag;
+      ok = ok && (static_cast<uint32_t>(kx[r]) & ((1u << FUSED_TAG_BITS) - 1u)) == tag &&
+           (px[r] & ((1u << FUSED_TAG_BITS) - 1u)) == tag;
+    }
+    if (named_bar_and(1, NCT, ok || globaltimer() - t0 > WAIT_LIMIT_NS)) break;
+  }
+  if (!ok) set_status(p.status, KT_ERR_TIMEOUT);
+  if (ctid == 0) {
+    mbar_arrive(bar_seen);  // the producer may start the Initial/Local loads
+    KT_STAMP(p, 5);
+  }
+  *i0_out = 0;
   if (keff <= 0) {
     if (writer && ctid == 0) p.cnt_out[unit] = 0;
     return 0;
   }
-  // gather: slots ctid + r*NCT of the unit's table into registers (one round
-  // trip), their pages and keys into shared memory, and the head sample
-  constexpr int GP = FUSED_GATHER_PER_THREAD;
-  const unsigned long long* src = p.f_cand + (size_t)unit * nslots;
-  const int* srcp = p.f_cand_pages + (size_t)unit * nslots;
-  const int J = Lm.J, H = Lm.nheads, Hpad = (H + 1) & ~1;
-  unsigned long long kx[GP];
-  int px[GP];
 #pragma unroll
-  for (int r = 0; r < GP; ++r) {
-    const int s = ctid + r * NCT;
-    kx[r] = s < nslots ? __ldcg(src + s) : 0ull;
-    px[r] = s < nslots ? __ldcg(srcp + s) : -1;
-  }
-  // head sample with its common leading bits (AND / OR) and nonzero count
-  unsigned long long h_and = ~0ull, h_or = 0ull;
-  int h_nz = 0;
-#pragma unroll 1
-  for (int hh = ctid; hh < Hpad; hh += NCT) {
-    const unsigned long long key = hh < H ? __ldcg(src + (hh / J) * kk + (hh % J)) : 0ull;
-    heads[hh] = key;
-    if (key != 0ull) {
-      h_and &= key;
-      h_or |= key;
-      ++h_nz;
+  for (int r = 0; r < GP; ++r) kx[r] &= ~((1ull << FUSED_TAG_BITS) - 1ull);  // empty: 0
+  int N = 0;
+  const unsigned long long T = selc::kth_largest_reg<NCT, GP>(
+      kx, keff, reinterpret_cast<unsigned int*>(scr + Lp.hist),
+      reinterpret_cast<unsigned long long*>(scr + Lp.bink), sh_u64, sh_int, &N, ctid, bar_c);
+  if (N < keff) {
+    if (ctid == 0) set_status(p.status, KT_ERR_DEVICE_CHECK);
+    keff = N;
+    if (keff <= 0) {
+      if (writer && ctid == 0) p.cnt_out[unit] = 0;
+      return 0;
     }
   }
-#pragma unroll
-  for (int r = 0; r < GP; ++r) {
-    const int s = ctid + r * NCT;
-    if (s < nslots) {
-      all[s] = kx[r];
-      allp[s] = px[r];
-    }
-  }
-  const int kpad = (keff + 3) & ~3;
-#pragma unroll 1
-  for (int i = ctid; i < kpad; i += NCT) {
-    idx[i] = -1;
-    cid[i] = 0xFFFFFFFFu;
-  }
-#pragma unroll 1
-  for (int i = ctid; i < Lm.mcap; i += NCT) ckey[i] = 0ull;
-  hist[ctid] = 0u;  // NCT == 256 bins
-  {
-    const int lane = ctid & 31, w = ctid >> 5;
-    const uint32_t a_lo = __reduce_and_sync(0xffffffffu, (uint32_t)h_and);
-    const uint32_t a_hi = __reduce_and_sync(0xffffffffu, (uint32_t)(h_and >> 32));
-    const uint32_t o_lo = __reduce_or_sync(0xffffffffu, (uint32_t)h_or);
-    const uint32_t o_hi = __reduce_or_sync(0xffffffffu, (uint32_t)(h_or >> 32));
-    const unsigned nz = __reduce_add_sync(0xffffffffu, (unsigned)h_nz);
-    if (lane == 0) {
-      sh_u64[2 + w] = ((unsigned long long)a_hi << 32) | a_lo;
-      sh_u64[2 + CONSUMERS + w] = ((unsigned long long)o_hi << 32) | o_lo;
-      hist[256 + w] = nz;
-    }
-  }
-  if (ctid == 0) sh_int[0] = 0;
-  bar_c();
-  // T0: lower edge of the 8-bit digit bin (just below the heads' common
-  // leading bits) that holds the keff-th largest head.  At least keff heads,
-  // hence keys, are >= T0, so T0 bounds the keff-th largest key from below;
-  // with fewer than keff nonzero heads every nonzero key stays (T0 = 1).
-  // Every warp scans the histogram itself.
-  unsigned long long T0 = 1ull;
-  {
-    unsigned long long a = ~0ull, o = 0ull;
-    int nz = 0;
-#pragma unroll
-    for (int w = 0; w < CONSUMERS; ++w) {
-      a &= sh_u64[2 + w];
-      o |= sh_u64[2 + CONSUMERS + w];
-      nz += (int)hist[256 + w];
-    }
-    if (nz >= keff) {
-      const unsigned long long diff = a ^ o;
-      const int hi = diff ? 64 - __clzll((long long)diff) : 0;
-      const int shift = hi > 8 ? hi - 8 : 0;
-      const unsigned long long pmask = hi >= 64 ? 0ull : ~((1ull << hi) - 1);
-      const unsigned long long prefix = a & pmask;
-#pragma unroll 1
-      for (int hh = ctid; hh < H; hh += NCT) {
-        const unsigned long long key = heads[hh];
-        if (key != 0ull) atomicAdd(&hist[(unsigned)((key >> shift) & 255ull)], 1u);
-      }
-      bar_c();
-      // lane l holds digits 255-8l .. 248-8l (descending)
-      const int lane = ctid & 31;
-      unsigned int c[8], local = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        c[i] = hist[255 - 8 * lane - i];
-        local += c[i];
-      }
-      unsigned int incl = local;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const unsigned int v = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += v;
-      }
-      const unsigned int excl = incl - local;
-      const bool hit = excl < (unsigned)keff && (unsigned)keff <= incl;
-      int digit = 0;  // 256 + digit once found
-      unsigned int above = excl;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        above += c[i];
-        if (hit && digit == 0 && above >= (unsigned)keff) digit = 256 + 255 - 8 * lane - i;
-      }
-      const int src = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;
-      digit = __shfl_sync(0xffffffffu, digit, src < 0 ? 0 : src) - 256;
-      if (digit >= 0) T0 = prefix | (static_cast<unsigned long long>(digit) << shift);
-      if (T0 == 0ull) T0 = 1ull;
-    }
-  }
-  // keys >= T0 with their slots: one shared atomic per warp
+  // the chosen blocks' ids, one shared atomic per warp
   {
     const int lane = ctid & 31;
     const unsigned int lt = (1u << lane) - 1u;
@@ -622,57 +558,59 @@ __device__ int fused_merge(const Params& p, uint8_t* scr, unsigned int* hist,
     int tot = 0;
 #pragma unroll
     for (int r = 0; r < GP; ++r) {
-      bal[r] = __ballot_sync(0xffffffffu, kx[r] >= T0);
+      bal[r] = __ballot_sync(0xffffffffu, kx[r] != 0ull && kx[r] >= T);
       tot += __popc(bal[r]);
     }
     int o = 0;
-    if (lane == 0 && tot) o = atomicAdd(&sh_int[0], tot);
+    if (lane == 0 && tot) o = atomicAdd(&sh_int[13], tot);
     o = __shfl_sync(0xffffffffu, o, 0);
 #pragma unroll
     for (int r = 0; r < GP; ++r) {
       const int pos = o + __popc(bal[r] & lt);
-      if (kx[r] >= T0 && pos < Lm.mcap) {
-        ckey[pos] = kx[r];
-        cslot[pos] = ctid + r * NCT;
+      if (((bal[r] >> lane) & 1u) && pos < kpad) {
+        ids[pos] = static_cast<uint32_t>(fused_slot_block(kx[r]));
+        pages[pos] = static_cast<int>(px[r] >> FUSED_TAG_BITS);
       }
       o += __popc(bal[r]);
     }
   }
   bar_c();
-  const int M = sh_int[0];
-  if (M <= Lm.mcap) {
-    // exact rank among them; the chosen keep their block ids for the ordering
-#pragma unroll 1
-    for (int i = ctid; i < M; i += NCT) {
-      const unsigned long long key = ckey[i];
-      const int r = selc::count_greater(ckey, (M + 1) & ~1, key);
-      if (r < keff) {
-        idx[r] = cslot[i];
-        cid[r] = 0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFull);
-      }
-    }
-  } else {
-    // many keys near the bound: radix selection over the whole table
-    selc::select_top<NCT>(all, nslots, keff, idx, ckey, cslot, hist, sh_u64, sh_int, ctid, bar_c);
-#pragma unroll 1
-    for (int i = ctid; i < keff; i += NCT)
-      cid[i] = 0xFFFFFFFFu - static_cast<uint32_t>(all[idx[i]] & 0xFFFFFFFFull);
-  }
-  bar_c();
-  if (ctid == 0 && M < keff) set_status(p.status, KT_ERR_DEVICE_CHECK);
   // position of a chosen block = chosen blocks with a smaller id
-  const int i0 = (int)((long long)ci * keff / ncta), i1 = (int)((long long)(ci + 1) * keff / ncta);
 #pragma unroll 1
   for (int i = ctid; i < keff; i += NCT) {
-    const uint32_t id = cid[i];
-    const int r = min(count_less_u32(cid, kpad, id), keff - 1);
-    const int x = idx[i];
-    if (writer) p.sel_out[(size_t)unit * p.top_k + r] = x >= 0 ? static_cast<int32_t>(id) : -1;
-    if (r >= i0 && r < i1) slice[r - i0] = x >= 0 ? allp[x] : -1;
+    const uint32_t id = ids[i];
+    const int r = min(count_less_u32(ids, kpad, id), keff - 1);
+    sorted[r] = static_cast<int>(id);
+    sorted_pages[r] = pages[i];
+    if (writer) p.sel_out[(size_t)unit * p.top_k + r] = static_cast<int32_t>(id);
   }
   if (writer && ctid == 0) p.cnt_out[unit] = keff;
   bar_c();
+  const int i0 = (int)((long long)ci * keff / ncta), i1 = (int)((long long)(ci + 1) * keff / ncta);
+  *i0_out = i0;
   return i1 - i0;
+}
+
+// Fused step, all consumer threads of a CTA as it leaves: the CTA counts
+// itself done, and the last CTA of the launch advances the launch epoch (every
+// CTA read it when it started) and, when the slot tags wrap, zeroes the slot
+// region so that no stale slot can carry a live tag.
+__device__ __forceinline__ void fused_exit(const Params& p, int ctid, int* sh_last) {
+  if (ctid == 0) *sh_last = atomicAdd(p.f_sync + 1, 1) == (int)gridDim.x - 1 ? 1 : 0;
+  named_bar_sync(1, NCT);
+  if (!*sh_last) return;
+  const uint32_t e = ld_relaxed_gpu_u32(p.f_sync);
+  if (1u + e % FUSED_TAG_CYCLE == FUSED_TAG_CYCLE) {
+#pragma unroll 1
+    for (int i = ctid; i < p.f_cand_len; i += NCT) {
+      p.f_cand[i] = 0ull;
+      p.f_cpage[i] = 0u;
+    }
+  }
+  if (ctid == 0) {
+    p.f_sync[1] = 0;
+    p.f_sync[0] = static_cast<int>(e + 1u);
+  }
 }
 
 template <int SK>
@@ -681,7 +619,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   extern __shared__ uint8_t smem_raw[];
   __shared__ unsigned int f_hist[FUSED ? 512 : 1];
   __shared__ unsigned long long f_sh_u64[FUSED ? 2 + 2 * CONSUMERS : 1];
-  __shared__ int f_sh_int[FUSED ? 4 : 1];
+  __shared__ int f_sh_int[FUSED ? 16 : 1];
   // 1024-byte aligned (128-byte swizzled TMA boxes); offsetting the array
   // itself keeps the accesses below in the shared address space
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -698,6 +636,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   const uint32_t bar_sel = bar_q + 8;      // fused: this CTA's selected pages are ready
   const uint32_t bar_scored = bar_sel + 8;  // fused: this CTA's scoring loads are done
   const uint32_t bar_reps = bar_scored + 8;  // fused: staged reps landed (two, one per ring half)
+  const uint32_t bar_seen = bar_reps + 16;   // fused: the unit's candidate slots are all seen
   const uint32_t kv_base = smem_u32(smem + SmemLayout::kv);
   auto bar_c = [] { named_bar_sync(1, NCT); };
   if (tid == 0) {
@@ -710,7 +649,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     mbar_init(bar_scored, 1);
     mbar_init(bar_reps, CONSUMERS);
     mbar_init(bar_reps + 8, CONSUMERS);
+    mbar_init(bar_seen, 1);
     fence_mbar_init();
+    KT_STAMP(p, 0);
   }
   __syncthreads();
 
@@ -748,10 +689,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     seg = lo;
   }
   const int f0 = cum[seg], ncta = cum[seg + 1] - f0, ci = cta - f0;
-  // fused: CTAs that wait on this segment's selection unit (SHARED: every
-  // segment of the sequence)
-  const int npoll = (p.SEL == 1) ? cum[(seg / p.H_kv + 1) * p.H_kv] - cum[(seg / p.H_kv) * p.H_kv]
-                                 : ncta;
   // fused: the consumers may overwrite `cum` once the producer has read it
   if (FUSED && warp == CONSUMERS) named_bar_arrive(2, THREADS);
   const int b = seg / p.H_kv, h = seg % p.H_kv;
@@ -768,16 +705,22 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       bulk_load(smem_u32(smem + SmemLayout::q), p.q + ((size_t)b * H_q + h * p.G) * D, qbytes,
                 bar_q);
     }
-    // fused: this CTA's selected page ids, written by the consumer warps
-    const int* fslice = nullptr;
+    // fused: the unit's chosen block ids in ascending order, written by the
+    // consumer warps (this CTA's share starts at fi0); the page of each of this
+    // CTA's first 32 Initial/Local blocks, looked up now
+    const int* fsorted = nullptr;
+    const int* fpages = nullptr;
+    int fi0 = 0, pgA = -1;
     if (FUSED) {
-      const FusedMergeLayout Lm =
-          fused_merge_layout(p.ncpu, p.kk_f, min(p.top_k, p.ncpu * p.kk_f));
-      fslice = reinterpret_cast<const int*>(smem + SmemLayout::scratch + Lm.slice);
+      const int nsl = p.ncpu * p.kk_f;
+      const FusedPickLayout Lp = fused_pick_layout(nsl, min(p.top_k, nsl));
+      fsorted = reinterpret_cast<const int*>(smem + SmemLayout::scratch + Lp.sorted);
+      fpages = reinterpret_cast<const int*>(smem + SmemLayout::scratch + Lp.sorted_pages);
+      const int i = a0 + lane;
+      if (i < a1) pgA = p.table[(size_t)b * p.max_blocks + (i < pt.c0 ? i : pt.c1 + (i - pt.c0))];
     }
     uint32_t it = 0;
     bool ok = true;
-    bool scored = !FUSED;
     // phase 0: list index i -> Initial/Local block; phase 1: i -> selected block
     auto produce = [&](int phase, int u0, int u1) {
       for (int base = u0; base < u1 && ok; base += 32) {
@@ -787,10 +730,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
           int j, page = -1;
           if (phase == 0) {
             j = (p.dense || i < pt.c0) ? i : pt.c1 + (i - pt.c0);
-            page = p.table[(size_t)b * p.max_blocks + j];
+            page = (FUSED && base == u0) ? pgA : p.table[(size_t)b * p.max_blocks + j];
           } else if (FUSED) {
-            j = pt.c0;  // a selected Context block: full
-            page = fslice[i];
+            j = fsorted[fi0 + i];  // a selected Context block (full), with its page
+            page = fpages[fi0 + i];
+            if (j < pt.c0 || j >= pt.c1) {
+              set_status(p.status, KT_ERR_DEVICE_CHECK);
+              j = -1;
+            }
           } else if (p.sel_pages == nullptr) {
             const int unit = p.SEL == 1 ? 0 : h;
             j = p.sel[((size_t)b * p.SEL + unit) * p.top_k + i];
@@ -823,19 +770,13 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
             if (it >= STAGES &&
                 !mbar_wait(bar_empty + 8 * st, ((it / STAGES) - 1) & 1, p.status))
               okl = 0;
-            // fused: the Initial/Local loads start once this CTA's slice is
-            // scored, so the representative rows (the selection's critical
-            // path) do not queue behind them in HBM; by then the stages that
-            // held those rows are free as well
-            if (okl && !scored && ntok_k > 0) {
-              mbar_wait_sleep(bar_scored, 0, p.status, 64);
-              scored = true;
-            }
             if (okl) {
               info[st].ntok = ntok_k;
               info[st].end = 0;
               const uint32_t bar = bar_full + 8 * st;
               if (ntok_k > 0) {
+                if (it == 0) KT_STAMP(p, 7);
+                if (phase == 1 && k == 0 && base == u0) KT_STAMP(p, 8);
                 mbar_arrive_expect_tx(bar, KV_STAGE_BYTES);
                 const uint32_t dst = kv_base + st * KV_STAGE_BYTES;
                 tma_load_2d(dst, &p.kmap, 0, row_k, bar, policy);
@@ -853,15 +794,25 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         }
       }
     };
-    produce(0, a0, a1);
     if (FUSED) {
-      // phase B: this CTA's share of the selected blocks, handed over by the
-      // consumer warps once the unit's selection is complete
-      int n1 = 0;
-      if (lane == 0 && mbar_wait_sleep(bar_sel, 0, p.status, 128)) n1 = bcast[61];
+      // The Initial/Local loads start once the unit's candidate slots have
+      // all been read: data arriving at this SM would queue the selection's
+      // own loads (the representative rows, the slot polls) behind it.  They
+      // land while the top-k is picked.  This CTA's share of the chosen
+      // blocks follows once the selection is made.
+      if (lane == 0) mbar_wait_sleep(bar_seen, 0, p.status, 64);
+      __syncwarp();
+      produce(0, a0, a1);
+      int n1 = 0, i0 = 0;
+      if (lane == 0 && mbar_wait_sleep(bar_sel, 0, p.status, 128)) {
+        n1 = bcast[61];
+        i0 = bcast[62];
+      }
       n1 = __shfl_sync(0xffffffffu, n1, 0);
+      fi0 = __shfl_sync(0xffffffffu, i0, 0);
       if (ok) produce(1, 0, n1);
     } else {
+      produce(0, a0, a1);
       // Phase B needs the selection: wait for the grid this launch depends on.
       griddep_wait();
       int nB = 0;
@@ -892,18 +843,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   const int ctid = tid;
 
   if constexpr (FUSED) {
-    const int n1 = fused_merge(p, reinterpret_cast<uint8_t*>(scratch), f_hist, f_sh_u64,
-                               f_sh_int, b, h, ci, ncta, ctid, bar_c);
+    int i0 = 0;
+    const int n1 = fused_pick(p, reinterpret_cast<uint8_t*>(scratch), f_sh_u64, f_sh_int, b, h,
+                              ci, ncta, ctid, bar_c, &i0, bar_seen);
     if (ctid == 0) {
       bcast[61] = n1;
+      bcast[62] = i0;
       mbar_arrive(bar_sel);
-      // the last of the unit's npoll waiting CTAs zeroes its tickets for the
-      // next launch (every other waiter has read them by then)
-      const int unit = b * p.SEL + (p.SEL == 1 ? 0 : h);
-      if (atomicAdd(p.f_polled + unit, 1) == npoll - 1) {
-        p.f_counters[unit] = 0;
-        p.f_polled[unit] = 0;
-      }
+      KT_STAMP(p, 6);
     }
   }
   float acc[16][4];
@@ -1013,127 +960,167 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
 
   // a CTA without units still owns the query copy it started: let it land
   if (!q_loaded && warp == 0) mbar_wait(bar_q, 0, p.status);
+  if (ctid == 0) KT_STAMP(p, 9);
 
-  // ---- merge the eight warp states: warps 4..7 into 0..3, then 0..3 --------
-  float l_row = l_part;
-  l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
-  l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
-  float o[32];  // this lane's 32 channels of head g: nt*8 + 2t (+1)
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    o[2 * nt] = acc[nt][0] + acc[nt][2];
-    o[2 * nt + 1] = acc[nt][1] + acc[nt][3];
+  // ---- combine the eight warp states in one barrier round: each warp stores
+  // (m, l, O[128]) per query head; then each thread combines two channels of a
+  // head over the eight states.  The scratch and block-prefix areas hold them
+  // for G <= 4; for larger G the (now idle) KV ring does, once every warp is
+  // past its last block.
+  constexpr int WST = D + 2;
+  float* wst = scratch;
+  if (p.G * CONSUMERS * WST * 4 > ATTN_MERGE_BYTES) {
+    wst = reinterpret_cast<float*>(smem + SmemLayout::kv);
+    named_bar_sync(1, NCT);
   }
-  const int wl = warp & (HALF_WARPS - 1);
-  float* sc = scratch + (wl * MAX_G + g) * (D + 2);
-  if (warp >= HALF_WARPS && g < p.G) {
-    if (t == 0) {
-      sc[0] = m_run;
-      sc[1] = l_row;
-    }
+  {
+    float l_row = l_part;
+    l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
+    l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+    if (g < p.G) {
+      float* sw = wst + (warp * p.G + g) * WST;
+      if (t == 0) {
+        sw[0] = m_run;
+        sw[1] = l_row;
+      }
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      sc[2 + nt * 8 + 2 * t] = o[2 * nt];
-      sc[2 + nt * 8 + 2 * t + 1] = o[2 * nt + 1];
-    }
-  }
-  named_bar_sync(1, NCT);
-  if (warp < HALF_WARPS && g < p.G) {
-    const float m2 = sc[0], l2 = sc[1];
-    const float M = fmaxf(m_run, m2);
-    const float wa = (M == -INFINITY) ? 0.0f : exp2f(m_run - M);
-    const float wb = (M == -INFINITY) ? 0.0f : exp2f(m2 - M);
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      o[2 * nt] = o[2 * nt] * wa + sc[2 + nt * 8 + 2 * t] * wb;
-      o[2 * nt + 1] = o[2 * nt + 1] * wa + sc[2 + nt * 8 + 2 * t + 1] * wb;
-    }
-    l_row = l_row * wa + l2 * wb;
-    m_run = M;
-  }
-  named_bar_sync(1, NCT);
-  if (warp < HALF_WARPS && g < p.G) {
-    if (t == 0) {
-      sc[0] = m_run;
-      sc[1] = l_row;
-    }
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      sc[2 + nt * 8 + 2 * t] = o[2 * nt];
-      sc[2 + nt * 8 + 2 * t + 1] = o[2 * nt + 1];
+      for (int nt = 0; nt < 16; ++nt)
+        *reinterpret_cast<float2*>(sw + 2 + nt * 8 + 2 * t) =
+            make_float2(acc[nt][0] + acc[nt][2], acc[nt][1] + acc[nt][3]);
     }
   }
   named_bar_sync(1, NCT);
-  // per head: M over the four states, weights, L
-  float* fw = reinterpret_cast<float*>(bcast + 16);  // [G][4] weights
-  float* fm = reinterpret_cast<float*>(bcast);       // [G] M, [G] L at +MAX_G
-  if (ctid < p.G) {
-    const int gg = ctid;
+  const int slot_stride = p.slot_floats;
+  float* dst = p.parts + (size_t)cta * slot_stride;  // partial: O[G][128], m[G], l[G] (base 2)
+  // fused: tagged partial words (value bits | launch tag << 32), two per float
+  // slot pair, so readers validate the data itself
+  unsigned long long* dstw = reinterpret_cast<unsigned long long*>(p.parts) + (size_t)cta * slot_stride;
+  const uint32_t ptag = FUSED ? (uint32_t)f_sh_int[15] : 0u;
+#pragma unroll 1
+  for (int idx = 2 * ctid; idx < p.G * D; idx += 2 * NCT) {
+    const int gg = idx / D, c = idx % D;
     float M = -INFINITY;
-    for (int w = 0; w < HALF_WARPS; ++w) M = fmaxf(M, scratch[(w * MAX_G + gg) * (D + 2)]);
-    float L = 0.0f;
-    for (int w = 0; w < HALF_WARPS; ++w) {
-      const float* s2 = scratch + (w * MAX_G + gg) * (D + 2);
-      const float wt = (M == -INFINITY) ? 0.0f : exp2f(s2[0] - M);
-      fw[gg * HALF_WARPS + w] = wt;
-      L += s2[1] * wt;
-    }
-    fm[gg] = M;
-    fm[MAX_G + gg] = L;
-  }
-  named_bar_sync(1, NCT);
-
-  if (ncta == 1) {
-    // the only CTA of its segment: normalise and write the output
-    for (int idx = ctid; idx < p.G * D; idx += NCT) {
-      const int gg = idx / D, c = idx % D;
-      float v = 0.0f;
 #pragma unroll
-      for (int w = 0; w < HALF_WARPS; ++w)
-        v = fmaf(scratch[(w * MAX_G + gg) * (D + 2) + 2 + c], fw[gg * HALF_WARPS + w], v);
-      const float L = fm[MAX_G + gg];
-      p.out[((size_t)b * H_q + h * p.G + gg) * D + c] = L > 0.0f ? v / L : 0.0f;
+    for (int w = 0; w < CONSUMERS; ++w) M = fmaxf(M, wst[(w * p.G + gg) * WST]);
+    float L = 0.0f, o0 = 0.0f, o1 = 0.0f;
+#pragma unroll
+    for (int w = 0; w < CONSUMERS; ++w) {
+      const float* sw = wst + (w * p.G + gg) * WST;
+      const float wt = (M == -INFINITY) ? 0.0f : exp2f(sw[0] - M);
+      const float2 ov = *reinterpret_cast<const float2*>(sw + 2 + c);
+      L = fmaf(sw[1], wt, L);
+      o0 = fmaf(ov.x, wt, o0);
+      o1 = fmaf(ov.y, wt, o1);
     }
+    if (ncta == 1) {
+      // the only CTA of its segment: normalise and write the output
+      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+      *reinterpret_cast<float2*>(p.out + ((size_t)b * H_q + h * p.G + gg) * D + c) =
+          make_float2(o0 * inv, o1 * inv);
+    } else if (FUSED) {
+      const unsigned long long hi = static_cast<unsigned long long>(ptag) << 32;
+      st_relaxed_gpu_u64(dstw + gg * D + c, hi | __float_as_uint(o0));
+      st_relaxed_gpu_u64(dstw + gg * D + c + 1, hi | __float_as_uint(o1));
+      if (c == 0) {
+        st_relaxed_gpu_u64(dstw + p.G * D + gg, hi | __float_as_uint(M));
+        st_relaxed_gpu_u64(dstw + p.G * D + p.G + gg, hi | __float_as_uint(L));
+      }
+    } else {
+      *reinterpret_cast<float2*>(dst + gg * D + c) = make_float2(o0, o1);
+      if (c == 0) {
+        dst[p.G * D + gg] = M;
+        dst[p.G * D + p.G + gg] = L;
+      }
+    }
+  }
+  if (ncta == 1) {
+    if (ctid == 0) KT_STAMP(p, 10);
+    if constexpr (FUSED) fused_exit(p, ctid, f_sh_int + 14);
     return;
   }
-
-  // ---- partial (slot = this CTA): O[G][128], then m[G], then l[G] (base 2)
-  const int slot_stride = p.slot_floats;
-  float* dst = p.parts + (size_t)cta * slot_stride;
-  for (int idx = ctid; idx < p.G * D; idx += NCT) {
-    const int gg = idx / D, c = idx % D;
-    float v = 0.0f;
-#pragma unroll
-    for (int w = 0; w < HALF_WARPS; ++w)
-      v = fmaf(scratch[(w * MAX_G + gg) * (D + 2) + 2 + c], fw[gg * HALF_WARPS + w], v);
-    dst[gg * D + c] = v;
-    if (c == 0) {
-      dst[p.G * D + gg] = fm[gg];
-      dst[p.G * D + p.G + gg] = fm[MAX_G + gg];
-    }
-  }
-  named_bar_sync(1, NCT);
   if constexpr (FUSED) {
-    // every CTA is resident: the segment's first CTA merges once the others'
-    // partials are in; the others leave as soon as theirs is released
-    if (ci != 0) {
-      if (ctid == 0) red_release_gpu_add(p.counters + seg, 1);
-      return;
-    }
-    if (ctid == 0) {
-      const uint64_t t0 = globaltimer();
-      for (uint32_t i = 0;; ++i) {
-        if (ld_acquire_gpu(p.counters + seg) >= ncta - 1) break;
-        if ((i & 63u) == 63u && globaltimer() - t0 > WAIT_LIMIT_NS) {
-          set_status(p.status, KT_ERR_TIMEOUT);
-          break;
+    // the tagged partial words are pushed out to L2 now (see the slots)
+  }
+  if constexpr (FUSED) {
+    // every CTA is resident: each CTA of the segment merges its share of the
+    // G x 128 output channels from every CTA's partial, reading the tagged
+    // words until all carry this launch's tag (no fence, no ticket)
+    if (ctid == 0) KT_STAMP(p, 10);
+    // shares are whole groups of 4 channels (a group never straddles a head)
+    const int GD = p.G * D, G4 = GD / 4;
+    const int q0 = 4 * (int)((long long)ci * G4 / ncta), q1 = 4 * (int)((long long)(ci + 1) * G4 / ncta);
+    const unsigned long long* base = reinterpret_cast<const unsigned long long*>(p.parts) +
+                                     (size_t)f0 * slot_stride;
+    const unsigned long long tagw = static_cast<unsigned long long>(ptag) << 32;
+    const int lane = ctid & 31, wp = ctid >> 5;
+    const uint64_t t0 = globaltimer();
+    // rounds over the share: warp wp takes the 4 channels cb .. cb+3; its lane
+    // k holds partial k0 + k (m, l and the 4 O words, one round of loads), and
+    // butterflies over the lanes merge the partials in a fixed order
+    const int rounds = (q1 - q0 + 4 * CONSUMERS - 1) / (4 * CONSUMERS);
+#pragma unroll 1
+    for (int rr = 0; rr < rounds; ++rr) {
+      const int cb = q0 + 4 * (rr * CONSUMERS + wp);
+      const bool has_ch = cb < q1;
+      const int gg = has_ch ? cb / D : 0;
+      float Mw = -INFINITY, Lw = 0.0f, Ow[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      bool ok = false;
+#pragma unroll 1
+      for (;;) {
+        ok = true;
+        Mw = -INFINITY;
+        Lw = 0.0f;
+        Ow[0] = Ow[1] = Ow[2] = Ow[3] = 0.0f;
+#pragma unroll 1
+        for (int k0 = 0; k0 < ncta; k0 += 32) {
+          const bool has = has_ch && k0 + lane < ncta;
+          const unsigned long long* src = base + (size_t)(k0 + lane) * slot_stride;
+          const unsigned long long wm = has ? ld_relaxed_gpu_u64(src + GD + gg)
+                                            : (tagw | __float_as_uint(-INFINITY));
+          const unsigned long long wl = has ? ld_relaxed_gpu_u64(src + GD + p.G + gg) : tagw;
+          unsigned long long wo[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) wo[i] = has ? ld_relaxed_gpu_u64(src + cb + i) : tagw;
+          const bool lane_ok = (wm >> 32) == ptag && (wl >> 32) == ptag &&
+                               (wo[0] >> 32) == ptag && (wo[1] >> 32) == ptag &&
+                               (wo[2] >> 32) == ptag && (wo[3] >> 32) == ptag;
+          ok = ok && lane_ok;
+          if (!__all_sync(0xffffffffu, lane_ok)) continue;  // not all in yet: poll again
+          const float mk = __uint_as_float((uint32_t)wm);
+          float M = mk;
+#pragma unroll
+          for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, d));
+          const float Mn = fmaxf(Mw, M);
+          if (Mn == -INFINITY) continue;  // warp-uniform
+          const float w = exp2f(mk - Mn);  // 0 for lanes without a partial
+          const float a0 = exp2f(Mw - Mn);  // 0 when Mw is -inf
+          float v[5] = {__uint_as_float((uint32_t)wl) * w, __uint_as_float((uint32_t)wo[0]) * w,
+                        __uint_as_float((uint32_t)wo[1]) * w, __uint_as_float((uint32_t)wo[2]) * w,
+                        __uint_as_float((uint32_t)wo[3]) * w};
+#pragma unroll
+          for (int d = 16; d > 0; d >>= 1)
+#pragma unroll
+            for (int i = 0; i < 5; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], d);
+          Lw = fmaf(Lw, a0, v[0]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) Ow[i] = fmaf(Ow[i], a0, v[1 + i]);
+          Mw = Mn;
         }
-        __nanosleep(32);
+        if (named_bar_and(1, NCT, ok || globaltimer() - t0 > WAIT_LIMIT_NS)) break;
       }
-      p.counters[seg] = 0;  // all ncta - 1 tickets are in
+      if (!ok) set_status(p.status, KT_ERR_TIMEOUT);
+      if (ctid == 0) KT_STAMP(p, 11);
+      const float inv = Lw > 0.0f ? 1.0f / Lw : 0.0f;
+      if (has_ch && lane < 4) {
+        const float ov = lane == 0 ? Ow[0] : lane == 1 ? Ow[1] : lane == 2 ? Ow[2] : Ow[3];
+        p.out[((size_t)b * H_q + h * p.G) * D + cb + lane] = ov * inv;
+      }
     }
-    named_bar_sync(1, NCT);
+    if (ctid == 0) KT_STAMP(p, 12);
+    fused_exit(p, ctid, f_sh_int + 14);
+    return;
   } else {
+    named_bar_sync(1, NCT);
     if (ctid == 0) {
       const int old = atom_acq_rel_gpu_add(p.counters + seg, 1);
       bcast[60] = (old + 1 == ncta) ? 1 : 0;
@@ -1142,87 +1129,55 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     if (!bcast[60]) return;
   }
 
-  // ---- last CTA of the segment: merge partials of CTAs f0 .. f0+ncta-1.
-  // Each thread owns one float4 chunk of the G x 128 outputs and a share of
-  // the partials, loaded 16 at a time with independent loads and merged
-  // online; the shares are combined through shared memory in a fixed order.
-  float* red = scratch;  // per thread: M, L, O.xyzw
-  const int nchunk = p.G * D / 4;
-  const int nsplit = NCT / nchunk;  // 1 (G=8), 2 (G=4), 4, 8
-  const int chn = ctid % nchunk, sp = ctid / nchunk;
-  const int f = 4 * chn, gg = f / D;
-  const int i0 = sp * ncta / nsplit, i1 = (sp + 1) * ncta / nsplit;
-  float M = -INFINITY, L = 0.0f;
-  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int base = i0; base < i1; base += 16) {
-    const int nb = min(16, i1 - base);
-    float m[16], l[16];
-    float4 ov[16];
+  // ---- the merging CTA: partials of CTAs f0 .. f0+ncta-1 in CTA order; each
+  // thread owns two channels of one head and takes 16 partials per round of
+  // independent loads, merged online
+#pragma unroll 1
+  for (int idx = 2 * ctid; idx < p.G * D; idx += 2 * NCT) {
+    const int gg = idx / D, c = idx % D;
+    float M = -INFINITY, L = 0.0f, o0 = 0.0f, o1 = 0.0f;
+#pragma unroll 1
+    for (int base = 0; base < ncta; base += 16) {
+      const int nb = min(16, ncta - base);
+      float m[16], l[16];
+      float2 ov[16];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      if (k < nb) {
-        const float* src = p.parts + (size_t)(f0 + base + k) * slot_stride;
-        m[k] = __ldcg(src + p.G * D + gg);
-        l[k] = __ldcg(src + p.G * D + p.G + gg);
-        ov[k] = __ldcg(reinterpret_cast<const float4*>(src + f));
-      } else {
-        m[k] = -INFINITY;
-        l[k] = 0.0f;
-        ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < 16; ++k) {
+        if (k < nb) {
+          const float* src = p.parts + (size_t)(f0 + base + k) * slot_stride;
+          m[k] = __ldcg(src + p.G * D + gg);
+          l[k] = __ldcg(src + p.G * D + p.G + gg);
+          ov[k] = __ldcg(reinterpret_cast<const float2*>(src + gg * D + c));
+        } else {
+          m[k] = -INFINITY;
+          l[k] = 0.0f;
+          ov[k] = make_float2(0.f, 0.f);
+        }
       }
-    }
-    float Mn = M;
+      float Mn = M;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) Mn = fmaxf(Mn, m[k]);
-    if (Mn == -INFINITY) continue;
-    const float a = exp2f(M - Mn);  // 0 when M is -inf
-    L *= a;
-    O.x *= a;
-    O.y *= a;
-    O.z *= a;
-    O.w *= a;
+      for (int k = 0; k < 16; ++k) Mn = fmaxf(Mn, m[k]);
+      if (Mn == -INFINITY) continue;
+      const float a0 = exp2f(M - Mn);  // 0 when M is -inf
+      L *= a0;
+      o0 *= a0;
+      o1 *= a0;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float w = exp2f(m[k] - Mn);  // 0 for empty partials
-      L = fmaf(l[k], w, L);
-      O.x = fmaf(ov[k].x, w, O.x);
-      O.y = fmaf(ov[k].y, w, O.y);
-      O.z = fmaf(ov[k].z, w, O.z);
-      O.w = fmaf(ov[k].w, w, O.w);
-    }
-    M = Mn;
-  }
-  if (nsplit > 1) {
-    named_bar_sync(1, NCT);  // scratch (red) was read above for the weights
-    float* r6 = red + 6 * ctid;
-    r6[0] = M;
-    r6[1] = L;
-    r6[2] = O.x;
-    r6[3] = O.y;
-    r6[4] = O.z;
-    r6[5] = O.w;
-    named_bar_sync(1, NCT);
-    if (sp == 0) {
-      for (int qd = 1; qd < nsplit; ++qd) {
-        const float* o2 = red + 6 * (ctid + qd * nchunk);
-        const float Mn = fmaxf(M, o2[0]);
-        if (Mn == -INFINITY) continue;
-        const float a = exp2f(M - Mn), w = exp2f(o2[0] - Mn);
-        L = L * a + o2[1] * w;
-        O.x = O.x * a + o2[2] * w;
-        O.y = O.y * a + o2[3] * w;
-        O.z = O.z * a + o2[4] * w;
-        O.w = O.w * a + o2[5] * w;
-        M = Mn;
+      for (int k = 0; k < 16; ++k) {
+        const float w = exp2f(m[k] - Mn);  // 0 for empty partials
+        L = fmaf(l[k], w, L);
+        o0 = fmaf(ov[k].x, w, o0);
+        o1 = fmaf(ov[k].y, w, o1);
       }
+      M = Mn;
     }
-  }
-  if (sp == 0) {
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    *reinterpret_cast<float4*>(p.out + ((size_t)b * H_q + h * p.G + gg) * D + (f % D)) =
-        make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+    *reinterpret_cast<float2*>(p.out + ((size_t)b * H_q + h * p.G + gg) * D + c) =
+        make_float2(o0 * inv, o1 * inv);
   }
   if (!FUSED && ctid == 0) p.counters[seg] = 0;
+  if (ctid == 0) KT_STAMP(p, 12);
+  if constexpr (FUSED) fused_exit(p, ctid, f_sh_int + 14);
 }
 
 }  // namespace
@@ -1297,14 +1252,15 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   p.f_chunk = a.f_chunk;
   p.kk_f = a.kk_f;
   p.f_cand = a.f_cand;
-  p.f_cand_pages = a.f_cand_pages;
-  p.f_counters = a.f_counters;
-  p.f_polled = a.f_polled;
+  p.f_cand_len = a.f_cand_len;
+  p.f_cpage = a.f_cpage;
+  p.f_sync = a.f_sync;
   p.sel_out = a.sel_out;
   p.cnt_out = a.cnt_out;
   p.presel_mask = a.presel_mask;
   p.presel_cnt = a.presel_cnt;
   p.mask_words = a.mask_words;
+  p.stamps = a.stamps;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);

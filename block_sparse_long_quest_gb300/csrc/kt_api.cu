@@ -112,13 +112,12 @@ WsLayout layout(kt_op op, const kt_paged_kv* kv, const kt_sparse_params* p, int 
   const size_t fcap = (size_t)MAX_ATTN_CTAS *
                       (size_t)(p->top_k < FUSED_KK_CAP ? (p->top_k > 0 ? p->top_k : 1)
                                                        : FUSED_KK_CAP);
-  L.f_counters = off;
-  off = align256(off + units * 4);
-  L.f_polled = off;
-  off = align256(off + units * 4);
+  L.f_sync = off;
+  off = align256(off + 2 * 4);
   L.f_cand = off;
+  L.f_cand_slots = fcap;
   off = align256(off + fcap * 8);
-  L.f_cand_pages = off;
+  L.f_cpage = off;
   off = align256(off + fcap * 4);
   const size_t sel_end = off;
   (void)T;
@@ -217,6 +216,11 @@ int cta_budget() {
   return (max_ctas_cap > 0 && max_ctas_cap < sms) ? max_ctas_cap : sms;
 }
 
+// Phase-stamp buffer of this host thread's attention launches (kt_set_phase_stamps).
+thread_local unsigned long long* stamps_buf = nullptr;
+thread_local int stamps_max_ctas = 0;
+unsigned long long* stamps_for(int grid) { return grid <= stamps_max_ctas ? stamps_buf : nullptr; }
+
 kt_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KT_OK : KT_ERR_CUDA; }
 
 template <class T>
@@ -305,6 +309,7 @@ kt_status attn_impl(const void* q, const kt_paged_kv* kv, int num_q_heads, float
   const int base = sms < MAX_ATTN_CTAS ? sms : MAX_ATTN_CTAS;
   a.grid = base > nseg ? base : nseg;
   a.pdl = pdl;
+  a.stamps = stamps_for(a.grid);
   return cuda_status(launch_attention(a, stream));
 }
 
@@ -594,7 +599,9 @@ bool fused_plan(const kt_paged_kv* kv, const kt_sparse_params* p, int sms, int* 
   const int kmax = (int)(p->top_k < nslots ? p->top_k : nslots);
   if (fused_score_layout(multi ? 0 : nkv * Rw * D, chunk, k).total > ATTN_SCRATCH_BYTES)
     return false;
-  if (fused_merge_layout(nc, k, kmax).total > ATTN_MERGE_BYTES) return false;
+  if (fused_pick_layout((int)nslots, kmax).total > ATTN_MERGE_BYTES) return false;
+  // block ids and pages in tagged slots
+  if (kv->max_blocks_per_seq > FUSED_MAX_BLOCKS || kv->num_pages > FUSED_MAX_PAGES) return false;
   if (attn_fused_max_ctas_per_sm() < 1) return false;
   *ncpu = nc;
   *chunk_out = chunk;
@@ -675,14 +682,15 @@ kt_status step_impl(const void* q, const kt_paged_kv* kv, const void* reps_pool,
     a.f_chunk = chunk;
     a.kk_f = kk;
     a.f_cand = at<unsigned long long>(ws, L.f_cand);
-    a.f_cand_pages = at<int>(ws, L.f_cand_pages);
-    a.f_counters = at<int>(ws, L.f_counters);
-    a.f_polled = at<int>(ws, L.f_polled);
+    a.f_cand_len = (int)L.f_cand_slots;
+    a.f_cpage = at<uint32_t>(ws, L.f_cpage);
+    a.f_sync = at<int>(ws, L.f_sync);
     a.sel_out = sel;
     a.cnt_out = cnt;
     a.presel_mask = presel_mask;
     a.presel_cnt = presel_cnt;
     a.mask_words = mask_words_of(kv);
+    a.stamps = stamps_for(a.grid);
     return cuda_status(launch_attention(a, (cudaStream_t)stream));
   }
   s = select_impl(q, kv, reps_pool, p, sel, cnt, nullptr, ws, L, true, (cudaStream_t)stream,
@@ -861,6 +869,14 @@ kt_status kt_read_device_status(void* ws, size_t ws_bytes, kt_stream_t stream,
   if (cudaMemsetAsync(ws, 0, sizeof(v), st) != cudaSuccess) return KT_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return KT_ERR_CUDA;
   *device_status = v;
+  return KT_OK;
+}
+
+kt_status kt_set_phase_stamps(void* stamps, int32_t max_ctas) {
+  if (stamps && ((reinterpret_cast<uintptr_t>(stamps) & 7u) != 0 || max_ctas < 1))
+    return KT_ERR_INVALID_ARG;
+  stamps_buf = static_cast<unsigned long long*>(stamps);
+  stamps_max_ctas = stamps ? max_ctas : 0;
   return KT_OK;
 }
 

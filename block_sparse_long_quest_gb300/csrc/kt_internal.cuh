@@ -69,38 +69,43 @@ __host__ __device__ inline FusedScoreLayout fused_score_layout(int wfl, int chun
   L.total = chunk > kk ? L.bidx + ATTN_CONSUMER_THREADS * 4 : L.idx;
   return L;
 }
-// Merge: the unit's candidate table (keys, pages), the head sample (the first
-// J keys of every sorted per-CTA list), the keys at or above the sample's k-th
-// largest (at most mcap of them, with their slots), the chosen slots, their
-// block ids and this CTA's share of their page ids.  Lives in the attention
-// kernel's scratch and block-prefix areas, which are contiguous.
-struct FusedMergeLayout {
-  int all, allp, heads, ck, cs, idx, cid, slice, total, mcap, J, nheads;
+// Pick: the 2048-bin histogram and the boundary-bin keys of the threshold
+// search (the unit's keys themselves stay in registers), the chosen block ids,
+// their pages, and both in ascending id order (this CTA's share is read from
+// there by the producer).  Lives in the attention kernel's scratch and block-prefix
+// areas, which are contiguous.
+struct FusedPickLayout {
+  int hist, bink, ids, pages, sorted, sorted_pages, total;
 };
-constexpr int ATTN_MERGE_BYTES = ATTN_SCRATCH_BYTES + (MAX_SEGS + 1) * 4;
-// ncpu lists of kk candidates each; kmax = min(top_k, ncpu * kk).
-__host__ __device__ inline FusedMergeLayout fused_merge_layout(int ncpu, int kk, int kmax) {
-  FusedMergeLayout L;
-  const int nslots = ncpu * kk;
-  L.J = (kmax + ncpu - 1) / ncpu;  // head keys per list: ncpu * J >= kmax
-  if (L.J > kk) L.J = kk;
-  const int nheads = ncpu * L.J;
-  L.nheads = nheads;
-  L.mcap = nslots < 512 ? nslots : 512;
-  if (L.mcap < ATTN_CONSUMER_THREADS) L.mcap = ATTN_CONSUMER_THREADS;  // select_top temporaries
-  L.mcap = (L.mcap + 1) & ~1;
-  L.all = 0;
-  L.allp = nslots * 8;
-  L.heads = (L.allp + nslots * 4 + 15) & ~15;
-  L.ck = (L.heads + ((nheads + 1) & ~1) * 8 + 15) & ~15;
-  L.cs = L.ck + L.mcap * 8;
-  L.idx = (L.cs + L.mcap * 4 + 15) & ~15;
-  L.cid = (L.idx + kmax * 4 + 15) & ~15;
-  L.slice = (L.cid + ((kmax + 3) & ~3) * 4 + 15) & ~15;
-  L.total = L.slice + kmax * 4;
+__host__ __device__ inline FusedPickLayout fused_pick_layout(int nslots, int kmax) {
+  FusedPickLayout L;
+  (void)nslots;
+  const int kpad = (kmax + 3) & ~3;
+  L.hist = 0;
+  L.bink = 2048 * 4;
+  L.ids = L.bink + ATTN_CONSUMER_THREADS * 8;
+  L.pages = L.ids + kpad * 4;
+  L.sorted = L.pages + kpad * 4;
+  L.sorted_pages = L.sorted + kpad * 4;
+  L.total = L.sorted_pages + kpad * 4;
   return L;
 }
+// Candidate slots of the one-launch step carry the launch's tag in their low
+// 12 bits, so a reader can tell a slot written by this launch from a stale one
+// without any fence: 8-byte words are written and read whole.  A slot holds
+// (score bits << 32) | ((2^20 - 1 - block) << 12) | tag, which orders as the
+// selection key (score, then lower block) for block ids below 2^20; an empty
+// slot is the tag alone.  Beside each key slot a 4-byte page slot holds
+// (page << 12) | tag, for pages below 2^20.  Tags cycle through 1..4095 (launch epoch modulo
+// 4095, plus one) and the slot region is zeroed when the cycle wraps, so a
+// stale slot never carries a live tag.
+constexpr int FUSED_MAX_BLOCKS = (1 << 20) - 1;
+constexpr int FUSED_MAX_PAGES = (1 << 20) - 1;
+constexpr uint32_t FUSED_TAG_BITS = 12;
+constexpr uint32_t FUSED_TAG_CYCLE = 4095;
+constexpr int ATTN_MERGE_BYTES = ATTN_SCRATCH_BYTES + (MAX_SEGS + 1) * 4;
 constexpr uint64_t WAIT_LIMIT_NS = 100000000ull;  // 100 ms bound on any device-side wait
+constexpr int KT_PHASE_STAMPS = 16;               // phase stamps per CTA (kt_set_phase_stamps)
 
 // ---------------------------------------------------------------------------
 // Selection chunking and workspace layout.  Host sizing and device addressing
@@ -120,10 +125,10 @@ struct WsLayout {
   size_t sel_cand;       // uint64 [B*SEL*nchunks*kk]
   size_t sel_cand_pages; // int32 [B*SEL*nchunks*kk], page id of each candidate
   size_t sel_pages;      // int32 [B*SEL*top_k], page ids of the selection (step path)
-  size_t f_counters;     // int32 [B*SEL] fused step: scoring tickets per unit
-  size_t f_polled;       // int32 [B*SEL]: fused step CTAs done polling each unit
-  size_t f_cand;         // uint64 [MAX_ATTN_CTAS * min(top_k, FUSED_KK_CAP)]
-  size_t f_cand_pages;   // int32, same count
+  size_t f_sync;         // int32 [2] fused step: launch epoch, CTAs done with the launch
+  size_t f_cand;         // uint64 [MAX_ATTN_CTAS * min(top_k, FUSED_KK_CAP)] tagged slots
+  size_t f_cand_slots;   // slots in that region
+  size_t f_cpage;        // uint32, one page slot per candidate slot
   size_t attn_counters;  // int32 [S]
   size_t attn_parts;     // float [2*(MAX_ATTN_CTAS+S)][slot_floats]
   size_t dyn;            // dynamic-rep scratch
@@ -167,6 +172,47 @@ inline SelPlan make_sel_plan(int B, int H_kv, int max_blocks, int I, int L, int 
 // Device helpers
 // ---------------------------------------------------------------------------
 #ifdef __CUDACC__
+
+__device__ __forceinline__ unsigned long long fused_slot(unsigned long long key, uint32_t tag) {
+  return (key & 0xFFFFFFFF00000000ull) |
+         (static_cast<unsigned long long>(static_cast<uint32_t>(key) & 0xFFFFFu) << FUSED_TAG_BITS) |
+         tag;
+}
+__device__ __forceinline__ int fused_slot_block(unsigned long long slot) {
+  return 0xFFFFF - static_cast<int>((slot >> FUSED_TAG_BITS) & 0xFFFFFull);
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_gpu_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_gpu_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_relaxed_gpu_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Named barrier `id` over `nthreads` threads that also returns, to every one
+// of them, whether `pred` held in all of them.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ void set_status(int* st, int code) {
   if (st) atomicCAS(st, 0, code);
@@ -308,6 +354,14 @@ __device__ __forceinline__ void mma_1688(float* d, uint32_t a0, uint32_t a1, uin
       "{%4, %5}, {%6}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(b0));
+}
+
+// Warms one 2-D box of a tensor map into L2 (no data comes back to the SM).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
@@ -486,15 +540,16 @@ struct AttnLaunch {
   int ncpu;     // CTAs scoring one selection unit
   int f_chunk;  // Context blocks per scoring CTA (nominal, from max_blocks)
   int kk_f;     // candidates kept per scoring CTA
-  unsigned long long* f_cand;
-  int* f_cand_pages;
-  int* f_counters;  // [B*SEL] scoring tickets, zero between launches
-  int* f_polled;    // [B*SEL] CTAs past each unit's ticket wait, zero between launches
+  unsigned long long* f_cand;  // tagged candidate slots [B*SEL][ncpu][kk_f]
+  int f_cand_len;              // slots in the workspace region (zeroed when tags wrap)
+  uint32_t* f_cpage;           // the page slot of each candidate slot
+  int* f_sync;                 // [0] launch epoch, [1] CTAs done with this launch
   int32_t* sel_out;
   int32_t* cnt_out;
   const uint32_t* presel_mask;  // nullable [B][SEL][mask_words]
   const int32_t* presel_cnt;    // with presel_mask: blocks preselected per unit
   int mask_words;
+  unsigned long long* stamps;   // nullable: [grid][KT_PHASE_STAMPS] global-timer stamps
 };
 int attn_fused_max_ctas_per_sm();
 cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream);

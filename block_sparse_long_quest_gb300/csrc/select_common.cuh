@@ -211,6 +211,153 @@ __device__ void radix_select(const unsigned long long* keys, int N, int k, unsig
   *mask_out = mask;
 }
 
+// Threshold of the k largest nonzero keys held in registers (GP per thread;
+// nonzero keys distinct): returns T > 0 such that exactly min(k, N) nonzero
+// keys are >= T, and the count N of nonzero keys in *n_out.  MSB-first passes
+// over 11-bit digits of the keys that share the running prefix, starting
+// below the bits every key has in common: a 2048-bin histogram, scanned by
+// all NT threads at once (PER bins each, warp shuffles, then the warp totals),
+// locates the bin of the k-th key; once that bin holds at most NT keys they
+// are ranked exactly by counting.  Every one of the NT threads calls it; bar
+// synchronises them.  Scratch: hist 2048 u32 (16-byte aligned), bink NT u64,
+// sh_u64 2 * NT / 32 + 1 entries, sh_int NT / 32 + 4 entries.
+template <int NT, int GP, class Bar>
+__device__ __forceinline__ unsigned long long kth_largest_reg(const unsigned long long (&kx)[GP], int k,
+                                                           unsigned int* hist, unsigned long long* bink,
+                                                           unsigned long long* sh_u64, int* sh_int,
+                                                           int* n_out, int tid, Bar bar) {
+  constexpr int WARPS = NT / 32, BINS = 2048, PER = BINS / NT;
+  static_assert(PER == 8, "two 16-byte vectors of bins per thread");
+  const int lane = tid & 31, warp = tid >> 5;
+  int* wsum = sh_int + 4;  // [WARPS]
+  // common leading bits and the count of the nonzero keys
+  unsigned long long a = ~0ull, o = 0ull;
+  int cnt = 0;
+#pragma unroll
+  for (int r = 0; r < GP; ++r)
+    if (kx[r]) {
+      a &= kx[r];
+      o |= kx[r];
+      ++cnt;
+    }
+  {
+    // warp reductions as independent redux instructions (no shuffle chain)
+    const uint32_t a_lo = __reduce_and_sync(0xffffffffu, static_cast<uint32_t>(a));
+    const uint32_t a_hi = __reduce_and_sync(0xffffffffu, static_cast<uint32_t>(a >> 32));
+    const uint32_t o_lo = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(o));
+    const uint32_t o_hi = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(o >> 32));
+    const int wc = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(cnt)));
+    if (lane == 0) {
+      sh_u64[warp] = (static_cast<unsigned long long>(a_hi) << 32) | a_lo;
+      sh_u64[WARPS + warp] = (static_cast<unsigned long long>(o_hi) << 32) | o_lo;
+      wsum[warp] = wc;
+    }
+  }
+  if (tid == 0) sh_int[3] = 0;
+  bar();
+  a = ~0ull;
+  o = 0ull;
+  int N = 0;
+#pragma unroll
+  for (int w = 0; w < WARPS; ++w) {
+    a &= sh_u64[w];
+    o |= sh_u64[WARPS + w];
+    N += wsum[w];
+  }
+  *n_out = N;
+  if (N <= k) return 1ull;  // every nonzero key (uniform: N is the same in every thread)
+  const unsigned long long diff = a ^ o;
+  int hi = diff ? 64 - __clzll((long long)diff) : 0;  // bits below the common prefix
+  unsigned long long mask = hi >= 64 ? 0ull : ~((1ull << hi) - 1);
+  unsigned long long prefix = a & mask;
+  int need = k, nb = N;
+#pragma unroll 1
+  while (nb > NT && hi > 0) {
+    const int shift = hi > 11 ? hi - 11 : 0;
+    const unsigned long long dmask = (1ull << (hi - shift)) - 1;
+    bar();  // the previous pass's scan has read the histogram and wsum
+    reinterpret_cast<uint4*>(hist)[2 * tid] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(hist)[2 * tid + 1] = make_uint4(0u, 0u, 0u, 0u);
+    bar();
+#pragma unroll
+    for (int r = 0; r < GP; ++r)
+      if (kx[r] && (kx[r] & mask) == prefix) atomicAdd(&hist[(unsigned)((kx[r] >> shift) & dmask)], 1u);
+    bar();
+    // thread t holds bins BINS-1-PER*t (first) .. BINS-PER-PER*t, descending
+    const uint4 lo4 = reinterpret_cast<const uint4*>(hist)[2 * (NT - 1 - tid)];
+    const uint4 hi4 = reinterpret_cast<const uint4*>(hist)[2 * (NT - 1 - tid) + 1];
+    const unsigned c[PER] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) local += (int)c[i];
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    bar();
+    int excl = incl - local;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) excl += w < warp ? wsum[w] : 0;
+    if (excl < need && need <= excl + local) {
+      int above = excl;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        if (above + (int)c[i] >= need) {
+          sh_int[0] = BINS - 1 - PER * tid - i;
+          sh_int[1] = need - above;
+          sh_int[2] = (int)c[i];
+          break;
+        }
+        above += (int)c[i];
+      }
+    }
+    bar();
+    prefix |= static_cast<unsigned long long>(sh_int[0]) << shift;
+    mask |= dmask << shift;
+    need = sh_int[1];
+    nb = sh_int[2];
+    hi = shift;
+  }
+  // the keys sharing the final prefix (at most NT of them), ranked exactly
+  {
+    // one shared atomic per warp (ballots give each key its place)
+    const unsigned int lt = (1u << lane) - 1u;
+    unsigned int bal[GP];
+    int tot = 0;
+#pragma unroll
+    for (int r = 0; r < GP; ++r) {
+      bal[r] = __ballot_sync(0xffffffffu, kx[r] != 0ull && (kx[r] & mask) == prefix);
+      tot += __popc(bal[r]);
+    }
+    int o0 = 0;
+    if (lane == 0 && tot) o0 = atomicAdd(&sh_int[3], tot);
+    o0 = __shfl_sync(0xffffffffu, o0, 0);
+#pragma unroll
+    for (int r = 0; r < GP; ++r) {
+      const int pos = o0 + __popc(bal[r] & lt);
+      // more than NT only if keys repeat (never for distinct keys)
+      if (((bal[r] >> lane) & 1u) && pos < NT) bink[pos] = kx[r];
+      o0 += __popc(bal[r]);
+    }
+  }
+  if (nb > NT) nb = NT;
+  bar();
+  for (int i = tid; i < nb; i += NT) {
+    const unsigned long long key = bink[i];
+    int g = 0;
+#pragma unroll 4
+    for (int j = 0; j < nb; ++j) g += bink[j] > key ? 1 : 0;
+    if (g == need - 1) sh_u64[2 * WARPS] = key;
+  }
+  bar();
+  const unsigned long long t = sh_u64[2 * WARPS];
+  bar();  // the caller may reuse the scratch
+  return t;
+}
+
 // Indices of the k largest of N distinct keys in shared memory (1 <= k <= N),
 // written unordered to idx_out[0, k).  MSB-first 8-bit digit histograms over
 // the keys sharing the running prefix narrow the search until the bin holding

@@ -267,6 +267,28 @@ int32_t kt_sparse_decode_step_kernels(const kt_paged_kv* kv, const kt_sparse_par
 kt_status kt_set_max_ctas(int32_t max_ctas);
 
 /*
+ * Phase timing of the attention launches made from the calling host thread
+ * (kt_sparse_decode_attn, kt_sparse_decode_step, kt_dense_decode_attn,
+ * kt_decode_layer): with a non-NULL buffer, each CTA of a launch with at most
+ * max_ctas CTAs writes the device global timer (ns) at the phases below into
+ * stamps[cta * 16 + phase] (uint64, device memory owned by the caller, at
+ * least max_ctas * 16 entries); a phase a CTA does not reach is left as it
+ * was, so clear the buffer between launches.  NULL turns it off (default).
+ * Thread-local; takes effect at the next launch.  INVALID_ARG if the buffer
+ * is non-NULL and misaligned or max_ctas < 1.  No counterpart in the article
+ * (a measurement aid of this library).
+ *   0 CTA entry                          7 first K/V block load issued
+ *   1 slice block-table entries loaded   8 first selected block load issued
+ *   2 slice representatives landed       9 last block attended
+ *   3 slice scored                      10 partial published / output written
+ *   4 slice candidates published        11 segment's partials all seen (merger)
+ *   5 unit's slices all seen            12 output written (merger)
+ *   6 unit's top-k picked, this CTA's pages handed to the loads
+ * Phases 1-6 and 11 exist only in the one-launch step.
+ */
+kt_status kt_set_phase_stamps(void* stamps, int32_t max_ctas);
+
+/*
  * Preselection [LC §4.4 "预选择 Preselect", §4.6 preselect_block()]: before
  * decoding, pick per selection unit a fixed set of Context blocks from the
  * attention of the last T prompt positions; later selections choose only

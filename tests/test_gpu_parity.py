@@ -226,7 +226,10 @@ def test_one_workspace_serves_every_call():
             for u in range(dw.SEL):
                 assert selection_agrees(sel, cnt, ref, b, u)[0]
     assert (s0 == s2).all() and (c0 == c2).all()
-    assert (o0 == o2).all() and (o0 == out_a).all()
+    # repeated steps agree bit for bit; the one-launch step and the
+    # attention-only call group the split-K merge differently (rounding only)
+    assert (o0 == o2).all()
+    assert row_rel_err(o0.cpu().numpy(), out_a.cpu().numpy()).max() <= 2.0 ** -18
     assert kt.kt_read_device_status(ws) == kt.KT_OK
 
 
