@@ -90,6 +90,12 @@ def lib():
         L.orc_avg_pool1d.argtypes = [vp, i64, i64, vp]
         L.orc_preselect.restype = ctypes.c_int
         L.orc_preselect.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp]
+        L.orc_f32_to_f16.restype = ctypes.c_uint16
+        L.orc_f32_to_f16.argtypes = [ctypes.c_float]
+        L.orc_quantize_q8_0.restype = None
+        L.orc_quantize_q8_0.argtypes = [vp, i64, vp, vp]
+        L.orc_attend_q8.restype = None
+        L.orc_attend_q8.argtypes = [vp, i64, i64, i64, vp, vp, i64, ctypes.c_double, vp]
         _lib = L
     return _lib
 
@@ -118,6 +124,69 @@ class KV:
     @classmethod
     def of(cls, w):
         return cls(w.k_pool, w.v_pool, w.block_table, w.seq_lens)
+
+
+class _KVQ(ctypes.Structure):
+    _fields_ = [("k_code", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_code", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("B", ctypes.c_int64), ("H_kv", ctypes.c_int64), ("d", ctypes.c_int64),
+                ("bs", ctypes.c_int64), ("max_blocks", ctypes.c_int64), ("P", ctypes.c_int64)]
+
+
+def f32_to_f16(x: float) -> int:
+    """binary32 -> binary16 bits, round to nearest even."""
+    return int(lib().orc_f32_to_f16(ctypes.c_float(x)))
+
+
+def quantize_q8_0(bits):
+    """[..., 128] binary16 bits -> (codes int8 [..., 128], scales binary16 bits [..., 4])
+    (the oracle's Q8_0 reading: 4 groups of 32 channels per row)."""
+    x = np.ascontiguousarray(bits, dtype=np.uint16)
+    rows = x.size // 128
+    code = np.zeros(x.shape, dtype=np.int8)
+    scale = np.zeros(x.shape[:-1] + (4,), dtype=np.uint16)
+    lib().orc_quantize_q8_0(x.ctypes.data, rows, code.ctypes.data, scale.ctypes.data)
+    return code, scale
+
+
+class KVQ:
+    """Q8_0 K/V pools (codes + binary16 scales) with the block table of a KV."""
+
+    def __init__(self, kv: "KV"):
+        self.kv = kv
+        self.k_code, self.k_scale = quantize_q8_0(kv.k_pool)
+        self.v_code, self.v_scale = quantize_q8_0(kv.v_pool)
+        self.s = _KVQ(self.k_code.ctypes.data, self.k_scale.ctypes.data,
+                      self.v_code.ctypes.data, self.v_scale.ctypes.data,
+                      kv.block_table.ctypes.data, kv.seq_lens.ctypes.data,
+                      kv.B, kv.H_kv, kv.d, kv.bs, kv.max_blocks, kv.P)
+
+
+def attend_q8(kvq: KVQ, b: int, hq: int, num_q_heads: int, q_bits, blocks, scale: float):
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    bl = np.ascontiguousarray(blocks, dtype=np.int32)
+    out = np.zeros(kvq.kv.d, dtype=np.float64)
+    lib().orc_attend_q8(ctypes.byref(kvq.s), b, hq, num_q_heads, q.ctypes.data, bl.ctypes.data,
+                        bl.size, scale, out.ctypes.data)
+    return out
+
+
+def attend_selection_q8(kvq: KVQ, q, p, sel, cnt) -> np.ndarray:
+    """attend_selection over the dequantised Q8_0 K and V: [B][H_q][d]."""
+    kv = kvq.kv
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    H_q = p.num_q_heads
+    G = H_q // kv.H_kv
+    out = np.zeros((kv.B, H_q, kv.d), dtype=np.float64)
+    for b in range(kv.B):
+        nb, c0, c1 = partition(int(kv.seq_lens[b]), p.initial_blocks, p.local_blocks, kv.bs)
+        for hq in range(H_q):
+            u = 0 if p.head_mode == HEAD_SHARED else hq // G
+            blocks = list(range(c0)) + [int(j) for j in sel[b, u, :int(cnt[b, u])]] + \
+                list(range(c1, nb))
+            out[b, hq] = attend_q8(kvq, b, hq, H_q, q[b, hq], blocks, p.softmax_scale)
+    return out
 
 
 def params(p) -> _Params:

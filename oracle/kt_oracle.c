@@ -606,3 +606,106 @@ int orc_sparse_step_presel(const orc_kv* kv, const uint16_t* q, const orc_params
 void orc_f16_array(const uint16_t* in, double* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = orc_f16_to_double(in[i]);
 }
+
+/* ---- quantised KV, Q8_0 (the kv_type choices FP16 / FP32 / Q4_0 / Q8_0 of
+ * [HOWTO] Step 1; Q8_0 is the 8-bit block format of the llama.cpp family that
+ * the key names) ---------------------------------------------------------------
+ * Reading taken (the pages name the type, not its arithmetic): a row of 128
+ * channels of K or V is cut into 4 groups of 32 channels; a group keeps one
+ * binary16 scale and 32 signed 8-bit codes.  With amax the largest |x| of the
+ * group in binary32, dd = amax / 127 and id = 1 / dd (0 when dd is 0) in
+ * binary32, the code of x is round-half-away-from-zero(x * id) (binary32
+ * product) and the stored scale is dd rounded to binary16; the dequantised
+ * value is dec(scale) * code.  The codes are decided in binary32 so that an
+ * implementation in that precision reproduces them exactly. */
+
+/* binary32 -> binary16, round to nearest even (IEEE 754-2008 §4.3.1, §3.4). */
+uint16_t orc_f32_to_f16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  const uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+  if (f != f) return (uint16_t)(sign | 0x7E00u);
+  const double a = fabs((double)f);
+  if (a >= 65520.0) return (uint16_t)(sign | 0x7C00u); /* past the midpoint above 65504 */
+  if (a < ldexp(1.0, -14)) {
+    /* subnormal (or zero): units of 2^-24; 1024 units become the smallest normal */
+    const double qq = rint(ldexp(a, 24));
+    return (uint16_t)(sign | (uint16_t)qq);
+  }
+  int e;
+  const double m = frexp(a, &e); /* a = m * 2^e, m in [0.5, 1) */
+  double q = rint(ldexp(m, 11));  /* 1024 .. 2048 */
+  int E = e - 1;                  /* a in [2^E, 2^(E+1)) */
+  if (q >= 2048.0) {
+    q = 1024.0;
+    E += 1;
+  }
+  if (E > 15) return (uint16_t)(sign | 0x7C00u);
+  return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(q - 1024.0));
+}
+
+/* rows x 128 binary16 values -> codes [rows][128] and scales [rows][4]. */
+void orc_quantize_q8_0(const uint16_t* x, int64_t rows, int8_t* code, uint16_t* scale) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t g = 0; g < 4; ++g) {
+      const uint16_t* xs = x + r * 128 + g * 32;
+      float amax = 0.0f;
+      for (int j = 0; j < 32; ++j) {
+        const float a = fabsf((float)dec(xs[j]));
+        if (a > amax) amax = a;
+      }
+      const float dd = amax / 127.0f;
+      const float id = dd != 0.0f ? 1.0f / dd : 0.0f;
+      scale[r * 4 + g] = orc_f32_to_f16(dd);
+      for (int j = 0; j < 32; ++j) {
+        const float t = (float)dec(xs[j]) * id;
+        code[r * 128 + g * 32 + j] = (int8_t)roundf(t);
+      }
+    }
+}
+
+typedef struct {
+  const int8_t* k_code;      /* [P][H_kv][bs][d] */
+  const uint16_t* k_scale;   /* [P][H_kv][bs][d/32] binary16 */
+  const int8_t* v_code;
+  const uint16_t* v_scale;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int64_t B, H_kv, d, bs, max_blocks, P;
+} orc_kvq;
+
+static double q8_val(const int8_t* code, const uint16_t* scale, const orc_kvq* kv, int64_t b,
+                     int64_t h, int64_t t, int64_t c) {
+  const int64_t page = kv->block_table[b * kv->max_blocks + t / kv->bs];
+  const int64_t row = (page * kv->H_kv + h) * kv->bs + t % kv->bs;
+  return dec(scale[row * (kv->d / 32) + c / 32]) * (double)code[row * kv->d + c];
+}
+
+/* orc_attend over the dequantised K and V of the listed blocks. */
+void orc_attend_q8(const orc_kvq* kv, int64_t b, int64_t hq, int64_t H_q, const uint16_t* q_bits,
+                   const int32_t* blocks, int64_t nblocks, double scale, double* out) {
+  const int64_t d = kv->d, bs = kv->bs, G = H_q / kv->H_kv, h = hq / G;
+  const int64_t n = kv->seq_lens[b];
+  double* q = (double*)malloc(sizeof(double) * (size_t)d);
+  for (int64_t c = 0; c < d; ++c) q[c] = dec(q_bits[c]);
+  double m = -INFINITY;
+  for (int64_t i = 0; i < nblocks; ++i)
+    for (int64_t t = blocks[i] * bs; t < (blocks[i] + 1) * bs && t < n; ++t) {
+      double s = 0.0;
+      for (int64_t c = 0; c < d; ++c) s += q[c] * q8_val(kv->k_code, kv->k_scale, kv, b, h, t, c);
+      s *= scale;
+      if (s > m) m = s;
+    }
+  double z = 0.0;
+  for (int64_t c = 0; c < d; ++c) out[c] = 0.0;
+  for (int64_t i = 0; i < nblocks; ++i)
+    for (int64_t t = blocks[i] * bs; t < (blocks[i] + 1) * bs && t < n; ++t) {
+      double s = 0.0;
+      for (int64_t c = 0; c < d; ++c) s += q[c] * q8_val(kv->k_code, kv->k_scale, kv, b, h, t, c);
+      const double w = exp(s * scale - m);
+      z += w;
+      for (int64_t c = 0; c < d; ++c) out[c] += w * q8_val(kv->v_code, kv->v_scale, kv, b, h, t, c);
+    }
+  for (int64_t c = 0; c < d; ++c) out[c] = z > 0.0 ? out[c] / z : 0.0;
+  free(q);
+}
