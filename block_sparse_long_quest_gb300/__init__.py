@@ -36,6 +36,7 @@ EXPORTS = (
     "kt_preselect_mask_words", "kt_preselect_blocks", "kt_score_select_blocks_presel",
     "kt_sparse_decode_step_presel", "kt_decode_history_slots", "kt_decode_layer_action",
     "kt_decode_layer", "kt_append_kv", "kt_set_max_ctas", "kt_set_phase_stamps",
+    "kt_sparse_decode_attn_hostkv", "kt_quantize_kv_q8_0", "kt_sparse_decode_attn_q8_0",
 )
 
 
@@ -61,6 +62,16 @@ class SparseParams(ctypes.Structure):
                 ("num_reps", ctypes.c_int32), ("fix_stride", ctypes.c_int32),
                 ("rep", ctypes.c_int32), ("head_mode", ctypes.c_int32),
                 ("softmax_scale", ctypes.c_float)]
+
+
+class PagedKVQ8(ctypes.Structure):
+    """kt_paged_kv_q8: Q8_0 code and scale pools + block table and lengths."""
+    _fields_ = [("k_code", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_code", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("batch", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("num_pages", ctypes.c_int32)]
 
 
 class ReusePolicy(ctypes.Structure):
@@ -114,6 +125,11 @@ def _load():
         "kt_append_kv": (ctypes.c_int, [P(PagedKV), P(SparseParams), vp, vp, vp, vp, sz, vp]),
         "kt_set_max_ctas": (ctypes.c_int, [i32]),
         "kt_set_phase_stamps": (ctypes.c_int, [vp, i32]),
+        "kt_sparse_decode_attn_hostkv": (ctypes.c_int, [vp, P(PagedKV), P(SparseParams), vp, vp,
+                                                        vp, vp, sz, vp]),
+        "kt_quantize_kv_q8_0": (ctypes.c_int, [P(PagedKV), vp, vp, vp, vp, i32, i32, vp]),
+        "kt_sparse_decode_attn_q8_0": (ctypes.c_int, [vp, P(PagedKVQ8), P(SparseParams), vp, vp,
+                                                      vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -299,6 +315,35 @@ def kt_sparse_decode_step_kernels(kv, params):
     if n < 0:
         raise KtError(-n, "kt_sparse_decode_step_kernels")
     return n
+
+
+def kt_sparse_decode_attn_hostkv(q, kv, params, sel, cnt, out, ws, stream=None):
+    """kt_sparse_decode_attn with kv's K/V pools in page-locked host memory."""
+    _check(lib.kt_sparse_decode_attn_hostkv(_ptr(q), ctypes.byref(kv), ctypes.byref(params),
+                                            _ptr(sel), _ptr(cnt), _ptr(out), _ptr(ws), ws.numel(),
+                                            _stream(stream)),
+           "kt_sparse_decode_attn_hostkv")
+
+
+def paged_kv_q8(k_code, k_scale, v_code, v_scale, block_table, seq_lens) -> PagedKVQ8:
+    P, H_kv, bs, d = k_code.shape
+    return PagedKVQ8(_ptr(k_code), _ptr(k_scale), _ptr(v_code), _ptr(v_scale), _ptr(block_table),
+                     _ptr(seq_lens), seq_lens.numel(), H_kv, d, bs, block_table.shape[1], P)
+
+
+def kt_quantize_kv_q8_0(kv, k_code, k_scale, v_code, v_scale, first_page=0, num_pages=None,
+                        stream=None):
+    n = kv.num_pages - first_page if num_pages is None else num_pages
+    _check(lib.kt_quantize_kv_q8_0(ctypes.byref(kv), _ptr(k_code), _ptr(k_scale), _ptr(v_code),
+                                   _ptr(v_scale), first_page, n, _stream(stream)),
+           "kt_quantize_kv_q8_0")
+
+
+def kt_sparse_decode_attn_q8_0(q, kvq, params, sel, cnt, out, ws, stream=None):
+    _check(lib.kt_sparse_decode_attn_q8_0(_ptr(q), ctypes.byref(kvq), ctypes.byref(params),
+                                          _ptr(sel), _ptr(cnt), _ptr(out), _ptr(ws), ws.numel(),
+                                          _stream(stream)),
+           "kt_sparse_decode_attn_q8_0")
 
 
 def kt_set_phase_stamps(stamps, max_ctas: int = 0):

@@ -17,7 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkt.so")
-SOURCES = ["kt_api.cu", "attn.cu", "select.cu", "reps.cu", "dynamic.cu", "preselect.cu"]
+SOURCES = ["kt_api.cu", "attn.cu", "select.cu", "reps.cu", "dynamic.cu", "preselect.cu",
+           "quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

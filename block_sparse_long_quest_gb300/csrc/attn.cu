@@ -60,6 +60,18 @@ static_assert(SCRATCH_FLOATS * 4 == ATTN_SCRATCH_BYTES, "scratch size shared wit
 static_assert(NCT == ATTN_CONSUMER_THREADS, "consumer threads shared with the host");
 static_assert(STAGES * KV_STAGE_BYTES == ATTN_RING_BYTES, "ring size shared with the host");
 
+// Q8_0 source: per stage the int8 codes of K and V (16 KB each, 128-byte
+// swizzled TMA boxes) and their binary16 scales (1 KB each); each consumer
+// warp dequantises its 16 token rows into one fp16 block in the layout the
+// fp16 stages have, at the start of the ring, and the int8 stages follow it.
+constexpr int Q8_CODE_BYTES = UNIT * D;
+constexpr int Q8_SCALE_BYTES = UNIT * (D / 32) * 2;
+constexpr int Q8_STAGE_BYTES = 2 * Q8_CODE_BYTES + 2 * Q8_SCALE_BYTES;
+constexpr int Q8_RING_OFF = KV_STAGE_BYTES;
+static_assert(Q8_RING_OFF + STAGES * Q8_STAGE_BYTES <= STAGES * KV_STAGE_BYTES,
+              "Q8_0 stages and the dequantised block fit the ring");
+static_assert(Q8_STAGE_BYTES % 1024 == 0, "128-byte swizzled boxes need 1024-byte alignment");
+
 struct StageInfo {
   int ntok, end, pad0, pad1;
 };
@@ -107,6 +119,10 @@ struct Params {
   const int32_t* presel_cnt;
   int mask_words;
   unsigned long long* stamps;
+  const __half* k_src;    // KVM_HOST: fp16 pools in device-accessible host memory
+  const __half* v_src;
+  const __half* k_scale;  // KVM_Q8: binary16 scales [P][H_kv][128][4]
+  const __half* v_scale;
 };
 
 // Phase stamp i of this CTA (global timer, ns) when stamps are requested.
@@ -613,9 +629,10 @@ __device__ __forceinline__ void fused_exit(const Params& p, int ctid, int* sh_la
   }
 }
 
-template <int SK>
+template <int SK, int KVM = KVM_F16>
 __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant__ Params p) {
   constexpr bool FUSED = SK != SK_NONE;
+  static_assert(!FUSED || KVM == KVM_F16, "the one-launch step reads fp16 pools");
   extern __shared__ uint8_t smem_raw[];
   __shared__ unsigned int f_hist[FUSED ? 512 : 1];
   __shared__ unsigned long long f_sh_u64[FUSED ? 2 + 2 * CONSUMERS : 1];
@@ -641,7 +658,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   auto bar_c = [] { named_bar_sync(1, NCT); };
   if (tid == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(bar_full + 8 * i, 1);
+      // host source: all 32 producer lanes arrive (each once its copies land)
+      mbar_init(bar_full + 8 * i, KVM == KVM_HOST ? 32 : 1);
       mbar_init(bar_empty + 8 * i, CONSUMERS);
     }
     mbar_init(bar_q, 1);
@@ -658,7 +676,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   // ---- set-up: segment work prefix -> this CTA's segment and slice.  In the
   // fused step the consumer warps score their selection slice meanwhile.
   if (warp == CONSUMERS) {
-    if (lane == 0) {
+    if (lane == 0 && KVM != KVM_HOST) {  // the host source uses no tensor maps
       prefetch_tensormap(&p.kmap);
       prefetch_tensormap(&p.vmap);
     }
@@ -777,19 +795,49 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
               if (ntok_k > 0) {
                 if (it == 0) KT_STAMP(p, 7);
                 if (phase == 1 && k == 0 && base == u0) KT_STAMP(p, 8);
-                mbar_arrive_expect_tx(bar, KV_STAGE_BYTES);
-                const uint32_t dst = kv_base + st * KV_STAGE_BYTES;
-                tma_load_2d(dst, &p.kmap, 0, row_k, bar, policy);
-                tma_load_2d(dst + BOX_BYTES, &p.kmap, 64, row_k, bar, policy);
-                tma_load_2d(dst + 2 * BOX_BYTES, &p.vmap, 0, row_k, bar, policy);
-                tma_load_2d(dst + 3 * BOX_BYTES, &p.vmap, 64, row_k, bar, policy);
-              } else {
+                if constexpr (KVM == KVM_F16) {
+                  mbar_arrive_expect_tx(bar, KV_STAGE_BYTES);
+                  const uint32_t dst = kv_base + st * KV_STAGE_BYTES;
+                  tma_load_2d(dst, &p.kmap, 0, row_k, bar, policy);
+                  tma_load_2d(dst + BOX_BYTES, &p.kmap, 64, row_k, bar, policy);
+                  tma_load_2d(dst + 2 * BOX_BYTES, &p.vmap, 0, row_k, bar, policy);
+                  tma_load_2d(dst + 3 * BOX_BYTES, &p.vmap, 64, row_k, bar, policy);
+                } else if constexpr (KVM == KVM_Q8) {
+                  mbar_arrive_expect_tx(bar, Q8_STAGE_BYTES);
+                  const uint32_t dst = kv_base + Q8_RING_OFF + st * Q8_STAGE_BYTES;
+                  tma_load_2d(dst, &p.kmap, 0, row_k, bar, policy);
+                  tma_load_2d(dst + Q8_CODE_BYTES, &p.vmap, 0, row_k, bar, policy);
+                  bulk_load(dst + 2 * Q8_CODE_BYTES, p.k_scale + (size_t)row_k * (D / 32),
+                            Q8_SCALE_BYTES, bar);
+                  bulk_load(dst + 2 * Q8_CODE_BYTES + Q8_SCALE_BYTES,
+                            p.v_scale + (size_t)row_k * (D / 32), Q8_SCALE_BYTES, bar);
+                }
+              } else if constexpr (KVM != KVM_HOST) {
                 mbar_arrive(bar);
               }
             }
           }
           ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
           if (!ok) break;
+          if constexpr (KVM == KVM_HOST) {
+            // every lane: its 128 of the block's 4096 16-byte pieces (K and V,
+            // each two 64-channel boxes in the 128-byte swizzled layout of the
+            // TMA stages), then an arrival that completes once they have landed
+            const uint32_t st = it % STAGES;
+            if (ntok_k > 0) {
+              const uint32_t dst = kv_base + st * KV_STAGE_BYTES;
+#pragma unroll 4
+              for (int idx = lane; idx < 4 * UNIT * 8; idx += 32) {
+                const int bx = idx >> 10, r = (idx >> 3) & (UNIT - 1), c = idx & 7;
+                const __half* src = (bx < 2 ? p.k_src : p.v_src) + ((size_t)row_k + r) * D +
+                                    (bx & 1) * 64 + c * 8;
+                cp_async_16(dst + bx * BOX_BYTES + r * 128 + ((c ^ (r & 7)) << 4), src);
+              }
+              cp_async_mbar_arrive_noinc(bar_full + 8 * st);
+            } else {
+              mbar_arrive(bar_full + 8 * st);
+            }
+          }
           ++it;
         }
       }
@@ -827,13 +875,18 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       if (ok)
         produce(1, (int)((long long)ci * nB / ncta), (int)((long long)(ci + 1) * nB / ncta));
     }
-    if (ok && lane == 0) {
+    if (ok) {
       const uint32_t st = it % STAGES;
-      if (it < STAGES || mbar_wait(bar_empty + 8 * st, ((it / STAGES) - 1) & 1, p.status)) {
+      int okl = 0;
+      if (lane == 0 &&
+          (it < STAGES || mbar_wait(bar_empty + 8 * st, ((it / STAGES) - 1) & 1, p.status))) {
         info[st].end = 1;
         info[st].ntok = 0;
-        mbar_arrive(bar_full + 8 * st);
+        okl = 1;
       }
+      okl = __shfl_sync(0xffffffffu, okl, 0);
+      // the end marker: one arrival, or one per lane for the host source
+      if (okl && (KVM == KVM_HOST || lane == 0)) mbar_arrive(bar_full + 8 * st);
     }
     return;
   }
@@ -881,7 +934,44 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       q_loaded = true;
     }
     if (in.ntok > warp * 16) {
-      const uint32_t kb = kv_base + st * KV_STAGE_BYTES;
+      if constexpr (KVM == KVM_Q8) {
+        // this warp's 16 token rows of K and V: int8 code * binary16 scale
+        // (exact in fp32), rounded once to fp16, into the fp16 block at the
+        // start of the ring in the layout of an fp16 stage (lane: one row,
+        // half its channels)
+        const uint8_t* qst = smem + SmemLayout::kv + Q8_RING_OFF + st * Q8_STAGE_BYTES;
+        const int rr = lane >> 1, hh = lane & 1, tok = warp * 16 + rr, sw = tok & 7;
+#pragma unroll
+        for (int kvs = 0; kvs < 2; ++kvs) {
+          const uint8_t* codes = qst + kvs * Q8_CODE_BYTES + tok * 128;
+          const __half* scl = reinterpret_cast<const __half*>(qst + 2 * Q8_CODE_BYTES +
+                                                              kvs * Q8_SCALE_BYTES) + tok * (D / 32);
+          uint8_t* row16 = smem + SmemLayout::kv + (2 * kvs + hh) * BOX_BYTES + tok * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c16 = 4 * hh + i;  // 16-channel piece of the int8 row
+            const uint4 v = *reinterpret_cast<const uint4*>(codes + ((c16 ^ sw) << 4));
+            const float dq = __half2float(scl[c16 >> 1]);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            uint32_t h2[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int b0 = (int)(int8_t)(wv[j] & 0xFFu), b1 = (int)(int8_t)((wv[j] >> 8) & 0xFFu);
+              const int b2 = (int)(int8_t)((wv[j] >> 16) & 0xFFu), b3 = (int)(int8_t)(wv[j] >> 24);
+              const __half2 lo2 = __floats2half2_rn((float)b0 * dq, (float)b1 * dq);
+              const __half2 hi2 = __floats2half2_rn((float)b2 * dq, (float)b3 * dq);
+              h2[2 * j] = *reinterpret_cast<const uint32_t*>(&lo2);
+              h2[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi2);
+            }
+            *reinterpret_cast<uint4*>(row16 + (((2 * i) ^ sw) << 4)) =
+                make_uint4(h2[0], h2[1], h2[2], h2[3]);
+            *reinterpret_cast<uint4*>(row16 + (((2 * i + 1) ^ sw) << 4)) =
+                make_uint4(h2[4], h2[5], h2[6], h2[7]);
+          }
+        }
+        __syncwarp();
+      }
+      const uint32_t kb = KVM == KVM_Q8 ? kv_base : kv_base + st * KV_STAGE_BYTES;
       const uint32_t vb = kb + 2 * BOX_BYTES;
       const int mi = lane >> 3, r = lane & 7;
       // ---- S = q K^T for this warp's 16 tokens: two n-tiles, each with two
@@ -1132,6 +1222,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   // ---- the merging CTA: partials of CTAs f0 .. f0+ncta-1 in CTA order; each
   // thread owns two channels of one head and takes 16 partials per round of
   // independent loads, merged online
+  if constexpr (!FUSED) {
 #pragma unroll 1
   for (int idx = 2 * ctid; idx < p.G * D; idx += 2 * NCT) {
     const int gg = idx / D, c = idx % D;
@@ -1175,9 +1266,11 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     *reinterpret_cast<float2*>(p.out + ((size_t)b * H_q + h * p.G + gg) * D + c) =
         make_float2(o0 * inv, o1 * inv);
   }
-  if (!FUSED && ctid == 0) p.counters[seg] = 0;
-  if (ctid == 0) KT_STAMP(p, 12);
-  if constexpr (FUSED) fused_exit(p, ctid, f_sh_int + 14);
+  if (ctid == 0) {
+    p.counters[seg] = 0;
+    KT_STAMP(p, 12);
+  }
+  }
 }
 
 }  // namespace
@@ -1190,7 +1283,9 @@ int attn_smem_optin() {
     cudaError_t e = cudaSuccess;
     for (const void* f : {(const void*)attn_kernel<SK_NONE>, (const void*)attn_kernel<SK_COLS>,
                           (const void*)attn_kernel<SK_LINEAR>, (const void*)attn_kernel<SK_MMA>,
-                          (const void*)attn_kernel<SK_F32>, (const void*)attn_kernel<SK_MULTI>})
+                          (const void*)attn_kernel<SK_F32>, (const void*)attn_kernel<SK_MULTI>,
+                          (const void*)attn_kernel<SK_NONE, KVM_HOST>,
+                          (const void*)attn_kernel<SK_NONE, KVM_Q8>})
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     return (int)e;
@@ -1261,6 +1356,10 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   p.presel_cnt = a.presel_cnt;
   p.mask_words = a.mask_words;
   p.stamps = a.stamps;
+  p.k_src = static_cast<const __half*>(a.k_src);
+  p.v_src = static_cast<const __half*>(a.v_src);
+  p.k_scale = static_cast<const __half*>(a.k_scale);
+  p.v_scale = static_cast<const __half*>(a.v_scale);
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);
@@ -1279,7 +1378,11 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!a.fused) return cudaLaunchKernelEx(&cfg, attn_kernel<SK_NONE>, p);
+  if (!a.fused) {
+    if (a.kvm == KVM_HOST) return cudaLaunchKernelEx(&cfg, attn_kernel<SK_NONE, KVM_HOST>, p);
+    if (a.kvm == KVM_Q8) return cudaLaunchKernelEx(&cfg, attn_kernel<SK_NONE, KVM_Q8>, p);
+    return cudaLaunchKernelEx(&cfg, attn_kernel<SK_NONE>, p);
+  }
   switch (a.sk) {
     case SK_COLS: return cudaLaunchKernelEx(&cfg, attn_kernel<SK_COLS>, p);
     case SK_LINEAR: return cudaLaunchKernelEx(&cfg, attn_kernel<SK_LINEAR>, p);

@@ -167,13 +167,30 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, const kt_paged_kv* kv) 
   return r == CUDA_SUCCESS;
 }
 
-// The map depends only on the pool address and its extent: the last few are
-// kept per thread, so a decode loop encodes each pool once.
-bool make_pool_map(CUtensorMap* map, const void* pool, const kt_paged_kv* kv) {
+// [rows][128] int8 Q8_0 codes, boxes of 128 bytes x 128 rows (one block of one
+// KV head), 128-byte swizzle.
+bool encode_code_map(CUtensorMap* map, const void* pool, long long rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D};
+  cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)BS};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The map depends only on the pool address, its extent and its element type:
+// the last few are kept per thread, so a decode loop encodes each pool once.
+bool make_pool_map(CUtensorMap* map, const void* pool, const kt_paged_kv* kv,
+                   bool codes = false) {
   struct Entry {
     const void* pool;
     long long rows;
     int dev;
+    bool codes;
     CUtensorMap map;
   };
   constexpr int N = 8;
@@ -183,15 +200,17 @@ bool make_pool_map(CUtensorMap* map, const void* pool, const kt_paged_kv* kv) {
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   const long long rows = (long long)kv->num_pages * kv->num_kv_heads * BS;
   for (int i = 0; i < used; ++i)
-    if (cache[i].pool == pool && cache[i].rows == rows && cache[i].dev == dev) {
+    if (cache[i].pool == pool && cache[i].rows == rows && cache[i].dev == dev &&
+        cache[i].codes == codes) {
       *map = cache[i].map;
       return true;
     }
-  if (!encode_pool_map(map, pool, kv)) return false;
+  if (!(codes ? encode_code_map(map, pool, rows) : encode_pool_map(map, pool, kv))) return false;
   Entry& e = cache[next];
   e.pool = pool;
   e.rows = rows;
   e.dev = dev;
+  e.codes = codes;
   e.map = *map;
   next = (next + 1) % N;
   if (used < N) ++used;
@@ -269,12 +288,29 @@ kt_status select_impl(const void* q, const kt_paged_kv* kv, const void* reps,
 // step_path: the selection ran in this call on this workspace, so its page ids
 // (sel_pages) are used directly, and its counts are min(top_k, C) unless
 // counts_vary (a preselection can leave fewer candidates; cnt is then read).
+// KV source of an attention-only launch (KVM_*): for KVM_HOST the device
+// addresses of the host pools; for KVM_Q8 the code and scale pools.
+struct KvSource {
+  int kvm = KVM_F16;
+  const void* k_src = nullptr;
+  const void* v_src = nullptr;
+  const void* k_scale = nullptr;
+  const void* v_scale = nullptr;
+};
+
 kt_status attn_impl(const void* q, const kt_paged_kv* kv, int num_q_heads, float scale,
                     const kt_sparse_params* p, const int32_t* sel, const int32_t* cnt, float* out,
                     void* ws, const WsLayout& L, bool dense, bool pdl, cudaStream_t stream,
-                    bool step_path = false, bool counts_vary = false) {
+                    bool step_path = false, bool counts_vary = false,
+                    const KvSource& src = KvSource()) {
   CUtensorMap kmap, vmap;
-  if (!make_pool_map(&kmap, kv->k_pool, kv) || !make_pool_map(&vmap, kv->v_pool, kv))
+  std::memset(&kmap, 0, sizeof(kmap));
+  std::memset(&vmap, 0, sizeof(vmap));
+  if (src.kvm == KVM_F16 &&
+      (!make_pool_map(&kmap, kv->k_pool, kv) || !make_pool_map(&vmap, kv->v_pool, kv)))
+    return KT_ERR_CUDA;
+  if (src.kvm == KVM_Q8 && (!make_pool_map(&kmap, src.k_src, kv, true) ||
+                            !make_pool_map(&vmap, src.v_src, kv, true)))
     return KT_ERR_CUDA;
   const int sms = cta_budget();
   if (sms <= 0) return KT_ERR_CUDA;
@@ -310,6 +346,11 @@ kt_status attn_impl(const void* q, const kt_paged_kv* kv, int num_q_heads, float
   a.grid = base > nseg ? base : nseg;
   a.pdl = pdl;
   a.stamps = stamps_for(a.grid);
+  a.kvm = src.kvm;
+  a.k_src = src.k_src;
+  a.v_src = src.v_src;
+  a.k_scale = src.k_scale;
+  a.v_scale = src.v_scale;
   return cuda_status(launch_attention(a, stream));
 }
 
@@ -566,6 +607,101 @@ kt_status kt_sparse_decode_attn(const void* q, const kt_paged_kv* kv, const kt_s
   if (ws_bytes < L.total) return KT_ERR_WORKSPACE_TOO_SMALL;
   return attn_impl(q, kv, p->num_q_heads, p->softmax_scale, p, sel, cnt, out, ws, L, false, false,
                    (cudaStream_t)stream);
+}
+
+// Device address of a host pool the GPU can read (page-locked, mapped), or
+// nullptr.
+static const void* host_pool_device_ptr(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
+  return at.devicePointer;
+}
+
+kt_status kt_sparse_decode_attn_hostkv(const void* q, const kt_paged_kv* kv,
+                                       const kt_sparse_params* p, const int32_t* sel,
+                                       const int32_t* cnt, float* out, void* ws, size_t ws_bytes,
+                                       kt_stream_t stream) {
+  kt_status s = check_kv(kv);
+  if (s != KT_OK) return s;
+  s = check_params(kv, p);
+  if (s != KT_OK) return s;
+  if (!q || !sel || !cnt || !out || !ws || !aligned16(q) || !aligned16(out) || !aligned16(ws))
+    return KT_ERR_INVALID_ARG;
+  KvSource src;
+  src.kvm = KVM_HOST;
+  src.k_src = host_pool_device_ptr(kv->k_pool);
+  src.v_src = host_pool_device_ptr(kv->v_pool);
+  if (!src.k_src || !src.v_src || !aligned16(src.k_src) || !aligned16(src.v_src))
+    return KT_ERR_INVALID_ARG;
+  const WsLayout L = layout(KT_OP_SPARSE_ATTN, kv, p, 0);
+  if (ws_bytes < L.total) return KT_ERR_WORKSPACE_TOO_SMALL;
+  return attn_impl(q, kv, p->num_q_heads, p->softmax_scale, p, sel, cnt, out, ws, L, false, false,
+                   (cudaStream_t)stream, false, false, src);
+}
+
+kt_status kt_quantize_kv_q8_0(const kt_paged_kv* kv, void* k_code, void* k_scale, void* v_code,
+                              void* v_scale, int32_t first_page, int32_t num_pages,
+                              kt_stream_t stream) {
+  kt_status s = check_kv(kv);
+  if (s != KT_OK) return s;
+  if (!k_code || !k_scale || !v_code || !v_scale || !aligned16(k_code) || !aligned16(k_scale) ||
+      !aligned16(v_code) || !aligned16(v_scale))
+    return KT_ERR_INVALID_ARG;
+  if (first_page < 0 || num_pages < 0 || (long long)first_page + num_pages > kv->num_pages)
+    return KT_ERR_INVALID_ARG;
+  QuantLaunch a;
+  a.k_pool = static_cast<const __half*>(kv->k_pool);
+  a.v_pool = static_cast<const __half*>(kv->v_pool);
+  a.k_code = static_cast<int8_t*>(k_code);
+  a.k_scale = static_cast<__half*>(k_scale);
+  a.v_code = static_cast<int8_t*>(v_code);
+  a.v_scale = static_cast<__half*>(v_scale);
+  a.first_page = first_page;
+  a.num_pages = num_pages;
+  a.H_kv = kv->num_kv_heads;
+  return cuda_status(launch_quant(a, (cudaStream_t)stream));
+}
+
+kt_status kt_sparse_decode_attn_q8_0(const void* q, const kt_paged_kv_q8* kvq,
+                                     const kt_sparse_params* p, const int32_t* sel,
+                                     const int32_t* cnt, float* out, void* ws, size_t ws_bytes,
+                                     kt_stream_t stream) {
+  if (!kvq) return KT_ERR_INVALID_ARG;
+  // the shapes and table as a kt_paged_kv (the code pools stand in for the
+  // fp16 pools in the checks; they are never read as fp16)
+  kt_paged_kv kv;
+  kv.k_pool = kvq->k_code;
+  kv.v_pool = kvq->v_code;
+  kv.block_table = kvq->block_table;
+  kv.seq_lens = kvq->seq_lens;
+  kv.batch = kvq->batch;
+  kv.num_kv_heads = kvq->num_kv_heads;
+  kv.head_dim = kvq->head_dim;
+  kv.block_size = kvq->block_size;
+  kv.max_blocks_per_seq = kvq->max_blocks_per_seq;
+  kv.num_pages = kvq->num_pages;
+  kt_status s = check_kv(&kv);
+  if (s != KT_OK) return s;
+  s = check_params(&kv, p);
+  if (s != KT_OK) return s;
+  if (!kvq->k_scale || !kvq->v_scale || !aligned16(kvq->k_scale) || !aligned16(kvq->v_scale))
+    return KT_ERR_INVALID_ARG;
+  if (!q || !sel || !cnt || !out || !ws || !aligned16(q) || !aligned16(out) || !aligned16(ws))
+    return KT_ERR_INVALID_ARG;
+  const WsLayout L = layout(KT_OP_SPARSE_ATTN, &kv, p, 0);
+  if (ws_bytes < L.total) return KT_ERR_WORKSPACE_TOO_SMALL;
+  KvSource src;
+  src.kvm = KVM_Q8;
+  src.k_src = kvq->k_code;
+  src.v_src = kvq->v_code;
+  src.k_scale = kvq->k_scale;
+  src.v_scale = kvq->v_scale;
+  return attn_impl(q, &kv, p->num_q_heads, p->softmax_scale, p, sel, cnt, out, ws, L, false,
+                   false, (cudaStream_t)stream, false, false, src);
 }
 
 namespace kt {

@@ -43,6 +43,11 @@ constexpr int FUSED_MAX_CHUNK = 8 * ATTN_CONSUMER_THREADS;  // blocks one CTA sc
 // cores (COLS), few fp16 blocks otherwise (LINEAR), many fp16 blocks on the
 // tensor cores (MMA), fp32 reps (F32), several reps per block (MULTI).
 enum : int { SK_NONE = 0, SK_COLS = 1, SK_LINEAR = 2, SK_MMA = 3, SK_F32 = 4, SK_MULTI = 5 };
+// Where the attention-only kernel reads K and V: fp16 pools in device memory
+// (2-D TMA), fp16 pools in host memory the GPU reads over NVLink-C2C (16-byte
+// cp.async by the producer warp), or Q8_0 pools in device memory (TMA of the
+// int8 codes and bulk copies of the binary16 scales, dequantised per warp).
+enum : int { KVM_F16 = 0, KVM_HOST = 1, KVM_Q8 = 2 };
 // the most fp16 blocks a CTA scores on the CUDA cores in one pass
 __host__ __device__ inline int fused_lin_max(int V) {
   return 8 * (ATTN_CONSUMER_THREADS / 32) / (V <= 32 ? 1 : V <= 64 ? 2 : V <= 128 ? 4 : 8);
@@ -356,6 +361,16 @@ __device__ __forceinline__ void mma_1688(float* d, uint32_t a0, uint32_t a1, uin
       : "r"(a0), "r"(a1), "r"(b0));
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), 16-byte aligned both.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// Arrival on `bar` once every cp.async this thread issued before it has
+// landed; counts as one of the barrier's expected arrivals.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Warms one 2-D box of a tensor map into L2 (no data comes back to the SM).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
@@ -550,6 +565,14 @@ struct AttnLaunch {
   const int32_t* presel_cnt;    // with presel_mask: blocks preselected per unit
   int mask_words;
   unsigned long long* stamps;   // nullable: [grid][KT_PHASE_STAMPS] global-timer stamps
+  // attention-only kernel, KV source (KVM_*): KVM_HOST reads k_src / v_src
+  // (device-accessible host pools, fp16); KVM_Q8 reads the int8 codes through
+  // kmap / vmap and the binary16 scales [pages][H_kv][128][4] at k_scale / v_scale
+  int kvm;
+  const void* k_src;
+  const void* v_src;
+  const void* k_scale;
+  const void* v_scale;
 };
 int attn_fused_max_ctas_per_sm();
 cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream);
@@ -575,6 +598,18 @@ struct SelectLaunch {
 };
 cudaError_t launch_select(const SelectLaunch& a, cudaStream_t stream);
 size_t select_smem_bytes(const SelectLaunch& a);
+
+// Q8_0 quantisation of pages [first_page, first_page + num_pages) of both pools.
+struct QuantLaunch {
+  const __half* k_pool;
+  const __half* v_pool;
+  int8_t* k_code;
+  __half* k_scale;
+  int8_t* v_code;
+  __half* v_scale;
+  int first_page, num_pages, H_kv;
+};
+cudaError_t launch_quant(const QuantLaunch& a, cudaStream_t stream);
 
 struct RepsLaunch {
   const __half* k_pool;

@@ -267,6 +267,72 @@ int32_t kt_sparse_decode_step_kernels(const kt_paged_kv* kv, const kt_sparse_par
 kt_status kt_set_max_ctas(int32_t max_ctas);
 
 /*
+ * ---- KV cache in host (Grace) memory, read over NVLink-C2C -------------------
+ * The article keeps the KV cache in CPU DRAM and moves only the retrieved
+ * blocks to the computation [LC §4.1; §1].  Here the K/V pools of `kv` live in
+ * page-locked host memory that the GPU can address (cudaHostAlloc /
+ * cudaHostRegister, mapped); the block table, lengths, queries, selection,
+ * output and workspace are in device memory, and so are the representatives
+ * that the selection scores (kt_score_select_blocks over the same kv reads only
+ * the reps pool, never the K/V pools).  This call attends exactly as
+ * kt_sparse_decode_attn (same arithmetic, same output) but fetches each
+ * attended (block, KV head) — Initial, the given selection, Local — straight
+ * from host memory into shared memory with 16-byte copies, so per step only
+ * the attended bytes cross the link.  INVALID_ARG if either pool is not host
+ * memory mapped for this device.  Workspace: KT_OP_SPARSE_ATTN.
+ */
+kt_status kt_sparse_decode_attn_hostkv(const void* q, const kt_paged_kv* kv,
+                                       const kt_sparse_params* p, const int32_t* sel,
+                                       const int32_t* cnt, float* out, void* ws, size_t ws_bytes,
+                                       kt_stream_t stream);
+
+/*
+ * ---- quantised KV, Q8_0 (the kv_type FP16 / FP32 / Q4_0 / Q8_0 choice of
+ * [HOWTO] Step 1) ---------------------------------------------------------------
+ * Each 128-channel row of K or V is stored as 4 groups of 32 channels: one
+ * binary16 scale and 32 signed 8-bit codes per group (34 bytes instead of 64).
+ * With amax the group's largest |x| (binary32), dd = amax / 127 and id = 1/dd
+ * (0 when dd is 0), a code is round-half-away-from-zero(x * id) in binary32
+ * and the scale is dd rounded to binary16; a value is read back as
+ * scale * code.
+ */
+typedef struct {
+  const void* k_code;   /* int8 [num_pages][num_kv_heads][128][128] */
+  const void* k_scale;  /* binary16 [num_pages][num_kv_heads][128][4] */
+  const void* v_code;   /* int8, as k_code */
+  const void* v_scale;  /* binary16, as k_scale */
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int32_t batch, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_pages;
+} kt_paged_kv_q8;
+
+/*
+ * Quantises pages [first_page, first_page + num_pages) of the fp16 pools of
+ * `kv` (every KV head and token row) into the Q8_0 pools.  Codes and scales
+ * are exact: they match any binary32 implementation of the definition above.
+ * All pointers are device memory, 16-byte aligned.  INVALID_ARG on a page
+ * range outside the pool.
+ */
+kt_status kt_quantize_kv_q8_0(const kt_paged_kv* kv, void* k_code, void* k_scale, void* v_code,
+                              void* v_scale, int32_t first_page, int32_t num_pages,
+                              kt_stream_t stream);
+
+/*
+ * kt_sparse_decode_attn over Q8_0 pools [LC §4.6 attn over the retrieved
+ * blocks]: per attended (block, KV head) 34 KB are read instead of 64 KB.
+ * Each consumer warp turns its token rows into fp16 (code * scale is exact in
+ * binary32 and is rounded once to binary16) and the attention proceeds as for
+ * fp16 pools (fp32 accumulation).  The selection is made beforehand from the
+ * fp16 representatives (kt_score_select_blocks: they are built from the keys
+ * as the blocks fill, before storage).  Workspace: KT_OP_SPARSE_ATTN of the
+ * same shapes.
+ */
+kt_status kt_sparse_decode_attn_q8_0(const void* q, const kt_paged_kv_q8* kv,
+                                     const kt_sparse_params* p, const int32_t* sel,
+                                     const int32_t* cnt, float* out, void* ws, size_t ws_bytes,
+                                     kt_stream_t stream);
+
+/*
  * Phase timing of the attention launches made from the calling host thread
  * (kt_sparse_decode_attn, kt_sparse_decode_step, kt_dense_decode_attn,
  * kt_decode_layer): with a non-NULL buffer, each CTA of a launch with at most
