@@ -15,8 +15,12 @@ layers rotated so that the touched working set (8 x 38 MB) is larger than twice
 the L2 cache.  Further legs: the Quest rep build and the dense decode over the
 same layers; decoding over the eight layers under selection-reuse policies
 (kt_decode_layer: dense layers, layer_step, token_step); the 1M-token, 4-layer
-workload (SEPARATE top-32 per KV head, Quest and Max reps); the Dynamic rep
-build and step at 128K; the preselection and the step restricted to it.
+workload (SEPARATE top-32 per KV head, Quest and Max reps); the batched paged
+workload (16 sequences, every rep method and head mode); the 128K layers with
+K/V stored as Q8_0 and with K/V in host memory read over NVLink-C2C; the
+Dynamic rep build and step at 128K (with its gap to dense attention); the
+preselection and the step restricted to it.  --phase-stamps adds per-phase
+timings of single step launches (kt_set_phase_stamps).
 
 value = algorithmic bytes per step (reps of every Context block + K/V of the
 attended tokens) / device time per step, in GB/s; us_per_step and
@@ -125,9 +129,11 @@ class Layer:
                                  v["ws"])
 
 
-def graph_time(fn_list, count, warmup, stream, chunk=1000, sampler=None):
+def graph_time(fn_list, count, warmup, stream, chunk=1000, sampler=None, replays=None):
     """Device seconds for `count` calls cycling through fn_list, captured in CUDA
-    graphs (chunks of `chunk` calls + a remainder graph), timed with events."""
+    graphs (chunks of `chunk` calls + a remainder graph), timed with events.
+    With `replays` (a list), the device seconds of each full-chunk replay are
+    appended to it as well (events between replays; no work is added)."""
     import torch
     with torch.cuda.stream(stream):
         for i in range(warmup):
@@ -144,6 +150,8 @@ def graph_time(fn_list, count, warmup, stream, chunk=1000, sampler=None):
         graphs.append((g, n))
     plan = [graphs[0][0]] * reps + ([graphs[-1][0]] if rem else [])
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(len(plan) + 1)] \
+        if replays is not None else []
     with torch.cuda.stream(stream):  # replay() launches on the current stream
         for g, _ in graphs:  # one untimed replay of each graph
             g.replay()
@@ -151,12 +159,19 @@ def graph_time(fn_list, count, warmup, stream, chunk=1000, sampler=None):
         if sampler:
             sampler.mark_start()
         start.record(stream)
-        for g in plan:
+        for i, g in enumerate(plan):
+            if marks:
+                marks[i].record(stream)
             g.replay()
+        if marks:
+            marks[-1].record(stream)
         end.record(stream)
     end.synchronize()
     if sampler:
         sampler.mark_end()
+    if marks:
+        for i in range(reps):  # the full chunks (the remainder graph is shorter)
+            replays.append(marks[i].elapsed_time(marks[i + 1]) / 1e3)
     return start.elapsed_time(end) / 1e3
 
 
@@ -271,6 +286,14 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
+def workload_config(w, seq_len: int) -> dict:
+    """The `config` both arms print for the 128K workload (identical dicts)."""
+    return {"workload": w.name, "batch": w.batch, "seq_len": seq_len, "q_heads": 32,
+            "kv_heads": 8, "head_dim": 128, "block_size": 128, "initial_tokens": 128,
+            "local_tokens": 4096, "top_k": 32, "rep": "quest", "head_mode": "shared",
+            "bytes_per_step": step_bytes(w)}
+
+
 # ----------------------------------------------------------------------------- CPU baseline
 
 def cpu_baseline(w: synth.Workload, budget_s: float = 12.0) -> dict:
@@ -364,8 +387,8 @@ def run_reference(args, world, rank):
         "n_gpus": world, "steps": steps, "steps_requested": args.steps, "warmup": args.warmup,
         "ms_per_step": per * 1e3, "us_per_step": per * 1e6, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "batch": 1, "seq_len": args.seq_len,
-                   "parallelism": "single-thread CPU"},
+        "config": workload_config(w, args.seq_len),
+        "parallelism": "single-thread CPU",
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"oracle score+select+attend on one {w.name} layer, reps "
                                    f"prebuilt, {steps} steps (capped to ~90 s)"},
@@ -387,6 +410,9 @@ def main():
     ap.add_argument("--no-1m", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dynamic", action="store_true")
+    ap.add_argument("--no-kv-sources", action="store_true",
+                    help="skip the Q8_0 and host-memory KV legs")
+    ap.add_argument("--no-batched", action="store_true", help="skip the batched paged leg")
     ap.add_argument("--phase-stamps", action="store_true",
                     help="add per-phase timings of single step launches (phase_us)")
     args = ap.parse_args()
@@ -428,8 +454,10 @@ def main():
     n_layers = len(layers)
     barrier(world)
     torch.cuda.synchronize()
+    replay_s, replay_steps = [], min(args.steps, 1000)
     with ClockSampler(local) as clocks:
-        t_step = graph_time(steps_fns, args.steps, args.warmup, stream, sampler=clocks)
+        t_step = graph_time(steps_fns, args.steps, args.warmup, stream, sampler=clocks,
+                            replays=replay_s)
     torch.cuda.synchronize()
     barrier(world)
     t_step = max_over_ranks(t_step, world)
@@ -477,6 +505,7 @@ def main():
                                       v["ws"], stream)
     t_e2e = max_over_ranks(time.perf_counter() - t0, world)
     e2e_value = world * bytes_step["total"] * n_e2e / t_e2e / 1e9
+    e2e_parts = e2e_breakdown(layers, rep, q_host, out_host, q_dev, stream, per_step)
 
     extra = {}
     if args.phase_stamps:
@@ -510,6 +539,11 @@ def main():
 
     # ---- decoding over the rotated layers with selection reuse
     extra["decode_reuse_128k"] = decode_reuse_leg(stream, layers, rep)
+    # ---- the other KV sources over the same rotated layers: Q8_0 pools in HBM,
+    # and fp16 pools in host memory read over NVLink-C2C
+    if not args.no_kv_sources:
+        extra["q8_0_128k"] = q8_leg(args, stream, layers, rep)
+        extra["host_kv_128k"] = hostkv_leg(args, stream, layers, rep)
 
     # ---- 1M-token leg: 4 layers back to back, Quest and Max reps
     if world == 1 and not args.no_1m:
@@ -544,6 +578,8 @@ def main():
                           **res}
         del big
         torch.cuda.empty_cache()
+    if world == 1 and not args.no_batched:
+        extra["batched_paged"] = batched_leg(args, stream)
     if world == 1 and not args.no_dynamic:
         extra["at_dynamic_128k"] = dynamic_leg(args, stream)
         extra["preselect_128k"] = preselect_leg(args, stream)
@@ -553,14 +589,15 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
         "us_per_step": per_step * 1e6, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": w0.name, "batch": 1, "seq_len": args.seq_len, "q_heads": 32,
-                   "kv_heads": 8, "head_dim": 128, "block_size": 128, "initial_tokens": 128,
-                   "local_tokens": 4096, "top_k": 32, "rep": "quest", "head_mode": "shared",
-                   "bytes_per_step": bytes_step,
-                   "l2": f"{n_layers} layers rotated, touched set "
-                         f"{n_layers * bytes_step['total'] / 1e6:.0f} MB vs L2 "
-                         f"{l2_bytes / 1e6:.0f} MB",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(w0, args.seq_len),
+        "l2": f"{n_layers} layers rotated, touched set {n_layers * bytes_step['total'] / 1e6:.0f} MB "
+              f"vs L2 {l2_bytes / 1e6:.0f} MB (inputs larger than L2 between steps)",
+        "parallelism": f"replicas x{world}",
+        "replays": {"steps_per_replay": replay_steps, "count": len(replay_s),
+                    "median_us_per_step": float(np.median(replay_s)) / replay_steps * 1e6
+                    if replay_s else None,
+                    "min_us_per_step": float(np.min(replay_s)) / replay_steps * 1e6
+                    if replay_s else None},
         "roofline": {"bound": "hbm", "kernel": roof_kernel, "achieved": roof_gbs,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": roof_gbs / peak, "traffic": kernel_traffic(roof_kernel),
@@ -571,7 +608,8 @@ def main():
         "launches_per_step": launches,
         "e2e": {"value": e2e_value, "unit": "GB/s", "us_per_step": t_e2e / n_e2e * 1e6,
                 "steps": n_e2e, "h2d_bytes_per_step": int(layers_q_bytes(w0)),
-                "d2h_bytes_per_step": int(w0.batch * w0.params.num_q_heads * D * 4)},
+                "d2h_bytes_per_step": int(w0.batch * w0.params.num_q_heads * D * 4),
+                "breakdown": e2e_parts},
         "gpu_launches": launches * args.steps,
         "clocks": clocks.summary(),
         **extra,
@@ -587,33 +625,92 @@ def main():
         dist.destroy_process_group()
 
 
-def dynamic_leg(args, stream):
+def dynamic_leg(args, stream, nl=8):
     """Dynamic reps at 128K: the rep build (two passes over K, tensor-core
-    contraction of the 64 local queries x 4 heads against every key) and the
-    decode step that scores blocks by max q.rep over 4 reps."""
+    contraction of the 64 local queries x 4 heads against every key, timed on
+    one layer) and the decode step that scores blocks by max q.rep over 4 reps,
+    over `nl` rotated layers.  The gap to dense attention over the same KV is
+    reported (max and median row relative error, and the share of each query
+    head's dense attention mass that the attended blocks hold)."""
     import torch
 
     import block_sparse_long_quest_gb300 as kt
-    w = synth.dynamic128k()
-    L = Layer(w)  # builds no reps for Dynamic (kt_build_block_reps rejects it)
-    v = L.variants[synth.REP_DYNAMIC]
-    q_local = torch.from_numpy(w.q_local.view(np.int16)).view(torch.float16).cuda()
-    T = w.q_local.shape[1]
-    ws_dyn = kt.workspace(kt.KT_OP_DYNAMIC_REPS, L.kv, v["params"], T)
-    build = lambda: kt.kt_build_dynamic_reps(L.kv, v["params"], q_local, T, 0, w.max_blocks,
-                                             v["reps"], None, ws_dyn)
+    layers = []
+    for l in range(nl):
+        w = synth.dynamic128k(layer=l)
+        L = Layer(w, keep_host=(l == 0))  # no reps yet: Dynamic reps need the local queries
+        v = L.variants[synth.REP_DYNAMIC]
+        L.q_local = torch.from_numpy(w.q_local.view(np.int16)).view(torch.float16).cuda()
+        L.ws_dyn = kt.workspace(kt.KT_OP_DYNAMIC_REPS, L.kv, v["params"], w.q_local.shape[1])
+        kt.kt_build_dynamic_reps(L.kv, v["params"], L.q_local, w.q_local.shape[1], 0,
+                                 w.max_blocks, v["reps"], None, L.ws_dyn)
+        layers.append(L)
+    L0 = layers[0]
+    w0 = L0.w
+    v0 = L0.variants[synth.REP_DYNAMIC]
+    T = w0.q_local.shape[1]
+    build = lambda: kt.kt_build_dynamic_reps(L0.kv, v0["params"], L0.q_local, T, 0, w0.max_blocks,
+                                             v0["reps"], None, L0.ws_dyn)
     n_b = 10
     t_b = graph_time([build], n_b, 3, stream)
-    rows = T * w.params.num_q_heads
-    flops = 2 * 2 * rows * int(w.seq_lens[0]) * D  # two passes of Q K^T
+    rows = T * w0.params.num_q_heads
+    flops = 2 * 2 * rows * int(w0.seq_lens[0]) * D  # two passes of Q K^T
     n_s = 2000
-    t_s = graph_time([lambda: L.step(synth.REP_DYNAMIC)], n_s, args.warmup, stream)
-    b = step_bytes(w)
-    return {"workload": w.name,
+    t_s = graph_time([lambda L=L: L.step(synth.REP_DYNAMIC) for L in layers], n_s, args.warmup,
+                     stream)
+    b = step_bytes(w0)
+    # sparse vs dense on layer 0
+    L0.step(synth.REP_DYNAMIC)
+    sparse = v0["out"].cpu().numpy().astype(np.float64)
+    sel, cnt = v0["sel"].cpu().numpy(), v0["cnt"].cpu().numpy()
+    ws_d = kt.workspace(kt.KT_OP_DENSE_ATTN, L0.kv, v0["params"])
+    dense_t = torch.zeros_like(v0["out"])
+    kt.kt_dense_decode_attn(L0.q, L0.kv, 32, w0.params.softmax_scale, dense_t, ws_d)
+    dense = dense_t.cpu().numpy().astype(np.float64)
+    gap = np.abs(sparse - dense).max(-1) / np.abs(dense).max(-1)
+    mass = attention_mass(w0, sel, cnt)
+    return {"workload": f"{w0.name}, {nl} layers rotated for the step",
             "rep_build_us": t_b / n_b * 1e6, "rep_build_tflops": flops / (t_b / n_b) / 1e12,
-            "rep_build_k_bytes_read": 2 * int(L.k.numel()) * 2,
+            "rep_build_k_bytes_read": 2 * int(L0.k.numel()) * 2,
             "step_us": t_s / n_s * 1e6, "step_gbs": b["total"] / (t_s / n_s) / 1e9,
-            "step_bytes": b["total"], "l2_note": "one layer repeated (touched set fits L2)"}
+            "step_bytes": b["total"],
+            "l2_note": f"{nl} layers rotated, touched set {nl * b['total'] / 1e6:.0f} MB",
+            "dynamic_vs_dense": {
+                "max_row_rel_err": float(gap.max()), "median_row_rel_err": float(np.median(gap)),
+                "attention_mass_of_attended_tokens": {"min": float(mass.min()),
+                                                      "median": float(np.median(mass))},
+                "note": "synthetic N(0,1) keys and queries: dense attention is spread over "
+                        "all 131072 tokens, so the 8320 attended tokens (Initial 128 + 32 "
+                        "blocks + Local 4096) hold about their share of it, 1/16"}}
+
+
+def attention_mass(w, sel, cnt):
+    """Per query head, the share of dense softmax(q K^T / sqrt(d)) mass on the
+    tokens a step attends (Initial + selected + Local), from the host K."""
+    n = int(w.seq_lens[0])
+    p = w.params
+    nb = (n + 127) // 128
+    c0 = min(p.initial_blocks, nb)
+    c1 = max(c0, nb - p.local_blocks)
+    G = p.num_q_heads // w.num_kv_heads
+    out = np.zeros(p.num_q_heads)
+    for h in range(w.num_kv_heads):
+        K = w.k_pool[w.block_table[0, :nb], h].reshape(-1, D)[:n].view(np.float16)
+        K = K.astype(np.float32)
+        keep = np.zeros(nb, dtype=bool)
+        keep[:c0] = True
+        keep[c1:] = True
+        for g in range(G):
+            hq = h * G + g
+            u = 0 if p.head_mode == synth.HEAD_SHARED else h
+            kk = keep.copy()
+            kk[sel[0, u, :int(cnt[0, u])]] = True
+            q = w.q[0, hq].view(np.float16).astype(np.float32)
+            lg = (K @ q).astype(np.float64) * p.softmax_scale
+            pr = np.exp(lg - lg.max())
+            pr /= pr.sum()
+            out[hq] = pr[np.repeat(kk, 128)[:n]].sum()
+    return out
 
 
 def decode_reuse_leg(stream, layers, rep):
@@ -656,43 +753,219 @@ def decode_reuse_leg(stream, layers, rep):
     return {"workload": f"128k-gqa4-quest-shared-k32, {nl} layers", **res}
 
 
-def preselect_leg(args, stream):
+def preselect_leg(args, stream, nl=8):
     """Preselection at 128K (the 96 blocks of the pages' YAML, pool window 5,
-    64 local queries): its one-off cost, and the Quest SHARED top-32 step
-    restricted to it."""
+    64 local queries): its one-off cost (it reads K twice: 2 x 268 MB, past
+    the L2), and the Quest SHARED top-32 step restricted to it over `nl`
+    rotated layers.  The restricted step scores every Context block (only the
+    preselected ones compete), so its bytes count every Context block's reps."""
     import torch
 
     import block_sparse_long_quest_gb300 as kt
-    w = synth.dynamic128k()
-    w.params.rep = synth.REP_QUEST
-    L = Layer(w)
-    v = L.variants[synth.REP_QUEST]
-    q_local = torch.from_numpy(w.q_local.view(np.int16)).view(torch.float16).cuda()
-    T = w.q_local.shape[1]
-    SEL = 1 if w.params.head_mode == synth.HEAD_SHARED else w.num_kv_heads
-    mw = kt.kt_preselect_mask_words(L.kv)
-    mask = torch.zeros((w.batch, SEL, mw), dtype=torch.int32, device="cuda")
-    pcnt = torch.zeros((w.batch, SEL), dtype=torch.int32, device="cuda")
-    ws_p = kt.workspace(kt.KT_OP_PRESELECT, L.kv, v["params"], T)
-    run_p = lambda: kt.kt_preselect_blocks(L.kv, v["params"], q_local, T, 5, 96, mask, pcnt, ws_p)
+    layers = []
+    for l in range(nl):
+        w = synth.dynamic128k(layer=l)
+        w.params.rep = synth.REP_QUEST
+        L = Layer(w)
+        v = L.variants[synth.REP_QUEST]
+        q_local = torch.from_numpy(w.q_local.view(np.int16)).view(torch.float16).cuda()
+        T = w.q_local.shape[1]
+        SEL = 1 if w.params.head_mode == synth.HEAD_SHARED else w.num_kv_heads
+        mw = kt.kt_preselect_mask_words(L.kv)
+        L.mask = torch.zeros((w.batch, SEL, mw), dtype=torch.int32, device="cuda")
+        L.pcnt = torch.zeros((w.batch, SEL), dtype=torch.int32, device="cuda")
+        L.ws_p = kt.workspace(kt.KT_OP_PRESELECT, L.kv, v["params"], T)
+        L.run_p = lambda L=L, v=v, q_local=q_local, T=T: kt.kt_preselect_blocks(
+            L.kv, v["params"], q_local, T, 5, 96, L.mask, L.pcnt, L.ws_p)
+        L.run_p()
+        if kt.kt_read_device_status(L.ws_p) != kt.KT_OK:
+            raise RuntimeError("device status after preselection")
+        layers.append(L)
     n_p = 10
-    t_p = graph_time([run_p], n_p, 3, stream)
-    if kt.kt_read_device_status(ws_p) != kt.KT_OK:
-        raise RuntimeError("device status after preselection")
-    step = lambda: kt.kt_sparse_decode_step_presel(L.q, L.kv, v["reps"], v["params"], mask, pcnt,
-                                                   v["sel"], v["cnt"], v["out"], v["ws"])
+    t_p = graph_time([layers[0].run_p], n_p, 3, stream)
+
+    def step(L):
+        v = L.variants[synth.REP_QUEST]
+        kt.kt_sparse_decode_step_presel(L.q, L.kv, v["reps"], v["params"], L.mask, L.pcnt,
+                                        v["sel"], v["cnt"], v["out"], v["ws"])
+
     n_s = 2000
-    t_s = graph_time([step], n_s, args.warmup, stream)
-    # algorithmic bytes: reps of the 96 candidates + K/V of the attended tokens
-    b = step_bytes(w)
-    R = w.params.reps_per_block()
-    cand = int(pcnt.sum().item())
-    reps_b = cand * w.num_kv_heads * R * D * 2
-    total = b["kv"] + reps_b
-    return {"workload": "128k-gqa4-quest-shared-k32, preselect 96 blocks (pool 5, 64 local queries)",
+    t_s = graph_time([lambda L=L: step(L) for L in layers], n_s, args.warmup, stream)
+    b = step_bytes(layers[0].w)
+    return {"workload": "128k-gqa4-quest-shared-k32, preselect 96 blocks (pool 5, 64 local "
+                        f"queries), {nl} layers rotated",
             "preselect_us": t_p / n_p * 1e6, "step_us": t_s / n_s * 1e6,
-            "step_gbs": total / (t_s / n_s) / 1e9, "step_bytes": total,
-            "note": "the restricted step still scores every Context block; only the 96 compete"}
+            "step_gbs": b["total"] / (t_s / n_s) / 1e9, "step_bytes": b["total"],
+            "note": "the restricted step reads the reps of every Context block and attends "
+                    "the top-32 of the 96 preselected"}
+
+
+def e2e_breakdown(layers, rep, q_host, out_host, q_dev, stream, device_s, n=500):
+    """Host wall time per step of each part of the host-buffer call, each timed
+    alone: the query upload (pinned -> device, then a stream sync), the output
+    download, one step launched and synchronised, and the host time to launch
+    a step (enqueue only); device_us is the event-timed step."""
+    import torch
+
+    import block_sparse_long_quest_gb300 as kt
+    L = layers[0]
+    v = L.variants[rep]
+
+    def per_call(fn):
+        fn()
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        return (time.perf_counter() - t0) / n * 1e6
+
+    with torch.cuda.stream(stream):
+        h2d = per_call(lambda: (q_dev[0].copy_(q_host, non_blocking=True), stream.synchronize()))
+        d2h = per_call(lambda: (out_host.copy_(v["out"], non_blocking=True), stream.synchronize()))
+        step = per_call(lambda: (kt.kt_sparse_decode_step(L.q, L.kv, v["reps"], v["params"],
+                                                          v["sel"], v["cnt"], v["out"], v["ws"],
+                                                          stream), stream.synchronize()))
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(200):
+            kt.kt_sparse_decode_step(L.q, L.kv, v["reps"], v["params"], v["sel"], v["cnt"],
+                                     v["out"], v["ws"], stream)
+        launch = (time.perf_counter() - t0) / 200 * 1e6
+        stream.synchronize()
+    return {"h2d_and_sync_us": h2d, "d2h_and_sync_us": d2h, "step_and_sync_us": step,
+            "launch_host_us": launch, "device_us": device_s * 1e6}
+
+
+def batched_leg(args, stream):
+    """The batched paged workload: 16 sequences of 8K-64K tokens whose pages are
+    permuted in one pool, GQA 32/8, Local 2048, top-16; one step per rep method
+    (Max, Mean, Quest, Fix stride 32) and head mode (SHARED, SEPARATE) on the
+    same KV.  The touched set of one step (~300 MB) exceeds twice the L2."""
+    import torch
+
+    import block_sparse_long_quest_gb300 as kt
+    w = synth.batched(rep=synth.REP_QUEST, head_mode=synth.HEAD_SHARED)
+    L = Layer(w, extra_reps=(synth.REP_MAX, synth.REP_MEAN, synth.REP_FIX))
+    p = w.params
+    res = {}
+    for mode, mname in ((synth.HEAD_SHARED, "shared"), (synth.HEAD_SEPARATE, "separate")):
+        SEL = 1 if mode == synth.HEAD_SHARED else w.num_kv_heads
+        for r, rname in ((synth.REP_MAX, "max"), (synth.REP_MEAN, "mean"),
+                         (synth.REP_QUEST, "quest"), (synth.REP_FIX, "fix32")):
+            params = kt.sparse_params(p.num_q_heads, p.initial_blocks, p.local_blocks, p.top_k, r,
+                                      mode, num_reps=p.num_reps, fix_stride=p.fix_stride,
+                                      softmax_scale=p.softmax_scale)
+            reps = L.variants[r]["reps"]
+            sel = torch.zeros((w.batch, SEL, p.top_k), dtype=torch.int32, device="cuda")
+            cnt = torch.zeros((w.batch, SEL), dtype=torch.int32, device="cuda")
+            out = torch.zeros((w.batch, p.num_q_heads, D), dtype=torch.float32, device="cuda")
+            ws = kt.workspace(kt.KT_OP_SPARSE_STEP, L.kv, params)
+            fn = lambda params=params, reps=reps, sel=sel, cnt=cnt, out=out, ws=ws: \
+                kt.kt_sparse_decode_step(L.q, L.kv, reps, params, sel, cnt, out, ws)
+            fn()
+            if kt.kt_read_device_status(ws) != kt.KT_OK:
+                raise RuntimeError("device status after a batched step")
+            n = 1000
+            t = graph_time([fn], n, args.warmup, stream) / n
+            w.params.rep, w.params.head_mode = r, mode
+            b = step_bytes(w)
+            res[f"{rname}_{mname}"] = {"us_per_step": t * 1e6, "gbs": b["total"] / t / 1e9,
+                                       "bytes_per_step": b["total"],
+                                       "launches": kt.kt_sparse_decode_step_kernels(L.kv, params)}
+    w.params.rep, w.params.head_mode = synth.REP_QUEST, synth.HEAD_SHARED
+    peak, _ = measured_peak()
+    best = max(v["gbs"] for v in res.values())
+    return {"workload": "batched16-paged-k16 (16 sequences, 8K-64K tokens, pages permuted)",
+            "sequence_lengths": [int(x) for x in w.seq_lens], **res,
+            "best_frac_of_hbm_peak": best / peak,
+            "l2_note": "one step touches ~300 MB, more than twice the L2"}
+
+
+def q8_leg(args, stream, layers, rep):
+    """Q8_0 K/V for the rotated 128K layers: each layer's fp16 pools quantised
+    once (timed on one layer), then per step the selection from the fp16 reps
+    and the attention over the codes; bytes per attended (block, KV head) are
+    2 x (16 KiB codes + 1 KiB scales) instead of 64 KiB."""
+    import torch
+
+    import block_sparse_long_quest_gb300 as kt
+    pools = []
+    for L in layers:
+        P, H, bs, d = L.k.shape
+        kc = torch.empty((P, H, bs, d), dtype=torch.int8, device="cuda")
+        vc = torch.empty_like(kc)
+        ks = torch.empty((P, H, bs, d // 32), dtype=torch.float16, device="cuda")
+        vs = torch.empty_like(ks)
+        kt.kt_quantize_kv_q8_0(L.kv, kc, ks, vc, vs)
+        pools.append(dict(kc=kc, vc=vc, ks=ks, vs=vs,
+                          kvq=kt.paged_kv_q8(kc, ks, vc, vs, L.table, L.lens)))
+    L0, p0 = layers[0], pools[0]
+    n_q = 10
+    t_q = graph_time([lambda: kt.kt_quantize_kv_q8_0(L0.kv, p0["kc"], p0["ks"], p0["vc"],
+                                                     p0["vs"])], n_q, 3, stream) / n_q
+    q_bytes = 2 * L0.k.numel() * 2 + 2 * (p0["kc"].numel() + p0["ks"].numel() * 2)
+
+    def attend(L, pq):
+        v = L.variants[rep]
+        kt.kt_sparse_decode_attn_q8_0(L.q, pq["kvq"], v["params"], v["sel"], v["cnt"], v["out"],
+                                      v["ws"])
+
+    for L in layers:  # a selection for every layer first
+        L.select(rep)
+    n = 2000
+    t_att = graph_time([lambda L=L, pq=pq: attend(L, pq) for L, pq in zip(layers, pools)], n,
+                       args.warmup, stream) / n
+    t_step = graph_time([lambda L=L, pq=pq: (L.select(rep), attend(L, pq))
+                         for L, pq in zip(layers, pools)], n, args.warmup, stream) / n
+    w = layers[0].w
+    b = step_bytes(w)
+    kv_q8 = b["kv"] * (2 * (16384 + 1024)) // (2 * 32768)
+    peak, _ = measured_peak()
+    return {"workload": f"{w.name}, {len(layers)} layers rotated, K/V stored as Q8_0",
+            "quantise_us_per_layer": t_q * 1e6, "quantise_gbs": q_bytes / t_q / 1e9,
+            "attention_us": t_att * 1e6, "attention_kv_bytes": int(kv_q8),
+            "attention_gbs": kv_q8 / t_att / 1e9,
+            "attention_frac_of_hbm_peak": kv_q8 / t_att / 1e9 / peak,
+            "fp16_attention_kv_bytes": int(b["kv"]),
+            "step_us (select + attention)": t_step * 1e6,
+            "step_bytes": int(b["reps"] + kv_q8),
+            "step_gbs": (b["reps"] + kv_q8) / t_step / 1e9}
+
+
+def hostkv_leg(args, stream, layers, rep):
+    """The rotated 128K layers with their K/V pools copied into page-locked host
+    memory: per step the selection (reps stay on the GPU) and the attention,
+    which reads the attended (block, KV head) pairs over NVLink-C2C."""
+    import torch
+
+    import block_sparse_long_quest_gb300 as kt
+    host = []
+    for L in layers:
+        hk = torch.empty(L.k.shape, dtype=L.k.dtype, device="cpu", pin_memory=True)
+        hv = torch.empty(L.v.shape, dtype=L.v.dtype, device="cpu", pin_memory=True)
+        hk.copy_(L.k)
+        hv.copy_(L.v)
+        host.append((hk, hv, kt.paged_kv(hk, hv, L.table, L.lens)))
+
+    def attend(L, kvh):
+        v = L.variants[rep]
+        kt.kt_sparse_decode_attn_hostkv(L.q, kvh, v["params"], v["sel"], v["cnt"], v["out"],
+                                        v["ws"])
+
+    for L in layers:
+        L.select(rep)
+    n = 400
+    t_att = graph_time([lambda L=L, h=h: attend(L, h[2]) for L, h in zip(layers, host)], n,
+                       args.warmup, stream) / n
+    t_step = graph_time([lambda L=L, h=h: (L.select(rep), attend(L, h[2]))
+                         for L, h in zip(layers, host)], n, args.warmup, stream) / n
+    b = step_bytes(layers[0].w)
+    del host
+    return {"workload": f"{layers[0].w.name}, {len(layers)} layers rotated, K/V in host memory",
+            "attention_us": t_att * 1e6, "attended_kv_bytes_over_c2c": int(b["kv"]),
+            "c2c_gbs": b["kv"] / t_att / 1e9,
+            "step_us (select + attention)": t_step * 1e6,
+            "note": "reps and the selection stay in HBM; only attended K/V cross NVLink-C2C"}
 
 
 PHASES = ("entry", "slice_pages", "slice_reps_landed", "slice_scored", "slice_published",

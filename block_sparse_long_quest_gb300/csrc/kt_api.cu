@@ -610,14 +610,30 @@ kt_status kt_sparse_decode_attn(const void* q, const kt_paged_kv* kv, const kt_s
 }
 
 // Device address of a host pool the GPU can read (page-locked, mapped), or
-// nullptr.
+// nullptr.  The last few answers are kept per host thread and device, so a
+// decode loop (or a CUDA graph capture of one) queries each pool once.
 static const void* host_pool_device_ptr(const void* p) {
+  struct Entry {
+    const void* host;
+    const void* dev_ptr;
+    int dev;
+  };
+  constexpr int N = 16;
+  thread_local Entry cache[N];
+  thread_local int used = 0, next = 0;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  for (int i = 0; i < used; ++i)
+    if (cache[i].host == p && cache[i].dev == dev) return cache[i].dev_ptr;
   cudaPointerAttributes at;
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
     cudaGetLastError();
     return nullptr;
   }
   if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
+  cache[next] = Entry{p, at.devicePointer, dev};
+  next = (next + 1) % N;
+  if (used < N) ++used;
   return at.devicePointer;
 }
 

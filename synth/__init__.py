@@ -326,13 +326,13 @@ def batched(seed: int = 3, *, rep: int = REP_QUEST, head_mode: int = HEAD_SHARED
 
 
 def dynamic128k(seed: int = 4, *, seq_len: int = 131072, head_mode: int = HEAD_SHARED,
-                local_queries: int = 64) -> Workload:
+                local_queries: int = 64, layer: int = 0) -> Workload:
     """128K, GQA 32/8, Dynamic reps (4 per block) from the last 64 local-window
     queries, top-32, Local 4096."""
     p = Params(num_q_heads=32, initial_blocks=1, local_blocks=32, top_k=32, rep=REP_DYNAMIC,
                head_mode=head_mode, num_reps=4)
     return make_workload("128k-gqa4-dynamic4-k32", seed=seed, seq_lens=[seq_len],
-                         num_q_heads=32, num_kv_heads=8, params=p,
+                         num_q_heads=32, num_kv_heads=8, params=p, layer=layer,
                          local_queries=local_queries)
 
 
