@@ -245,8 +245,8 @@ class ClockSampler:
 KERNEL_SOURCES = ("attn.cu", "select_common.cuh", "kt_internal.cuh")
 KERNEL_TRAFFIC = {
     "attn_kernel<fused step>": {
-        "bytes": 38259712 + 29952,
-        "sources_sha256": "0901bdbd81e4e26bf96948a21fedec4de37ad802c6b34d919bf94eeeb8f863c3"},
+        "bytes": 38265600 + 204800,
+        "sources_sha256": "650f6790f74f1c55f13303dbc08f87551129753381fe9b9e888cdfaf61adcd05"},
 }
 
 
@@ -408,6 +408,9 @@ def main():
     ap.add_argument("--layers", type=int, default=8, help="rotated 128K layers")
     ap.add_argument("--seq-len", type=int, default=131072)
     ap.add_argument("--no-1m", action="store_true")
+    ap.add_argument("--seq-len-1m", type=int, default=1048576,
+                    help="tokens per layer of the SEPARATE leg (smaller for profiling)")
+    ap.add_argument("--layers-1m", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dynamic", action="store_true")
     ap.add_argument("--no-kv-sources", action="store_true",
@@ -550,8 +553,8 @@ def main():
         del layers, steps_fns, q_dev
         torch.cuda.empty_cache()
         big = []
-        for l in range(4):
-            wb = synth.long1m(layer=l, rep=synth.REP_QUEST)
+        for l in range(args.layers_1m):
+            wb = synth.long1m(layer=l, rep=synth.REP_QUEST, seq_len=args.seq_len_1m)
             big.append(Layer(wb, extra_reps=(synth.REP_MAX,)))
         res = {}
         for r, name in ((synth.REP_QUEST, "quest"), (synth.REP_MAX, "max")):
@@ -567,14 +570,15 @@ def main():
             b1 = step_bytes(wq)
             per_layer = t1 / n1
             res[name] = {"us_per_layer_step": per_layer * 1e6,
-                         "us_per_4layer_step": 4 * per_layer * 1e6,
+                         f"us_per_{args.layers_1m}layer_step": args.layers_1m * per_layer * 1e6,
                          "gbs": b1["total"] / per_layer / 1e9,
                          "bytes_per_layer_step": b1["total"]}
             wq.params.rep = synth.REP_QUEST
             if args.phase_stamps:
                 extra.setdefault("phase_us", {})[f"1m_{name}"] = phase_stamps_leg(
                     [lambda L=L, r=r: L.step(r) for L in big])
-        extra["at_1m"] = {"workload": "1m-gqa4-separate-k32 (4 layers, 1048576 tokens each)",
+        extra["at_1m"] = {"workload": f"1m-gqa4-separate-k32 ({args.layers_1m} layers, "
+                                      f"{args.seq_len_1m} tokens each)",
                           **res}
         del big
         torch.cuda.empty_cache()
