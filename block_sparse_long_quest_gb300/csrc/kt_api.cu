@@ -1143,3 +1143,18 @@ extern "C" kt_status kt_sparse_decode_attn_noalloc(const void* q, const kt_paged
   a.pdl = false;
   return cuda_status(launch_attention(a, st));
 }
+
+extern "C" kt_status kt_noalloc_read_status(kt_stream_t stream, int32_t* device_status) {
+  if (!device_status) return KT_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  kt_status s = noalloc_scratch_ptr(&scratch);
+  if (s != KT_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KT_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, scratch, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return KT_ERR_CUDA;
+  if (cudaMemsetAsync(scratch, 0, sizeof(v), st) != cudaSuccess) return KT_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KT_ERR_CUDA;
+  *device_status = v;
+  return KT_OK;
+}

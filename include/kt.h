@@ -508,14 +508,24 @@ kt_status kt_append_kv(const kt_paged_kv* kv, const kt_sparse_params* p, const v
  *     call's contents; each call clears the status word and tickets on
  *     `stream` before its kernel.  Calls that overlap on the GPU (different
  *     streams, or host threads without ordering) race on it.
- *   - Device-side check failures are recorded in the shared array and are not
- *     reported by this call.
+ *   - Device-side check failures and timeouts are recorded in the shared
+ *     array's status word, not returned by this call (it returns after the
+ *     launch); kt_noalloc_read_status reports and clears the word.
  *   - It calls no allocator (no cudaMalloc, cudaFree or allocating library
  *     routine).
  */
 kt_status kt_sparse_decode_attn_noalloc(const void* q, const kt_paged_kv* kv,
                                         const kt_sparse_params* p, const int32_t* sel,
                                         const int32_t* cnt, float* out, kt_stream_t stream);
+
+/*
+ * The device status of the last kt_sparse_decode_attn_noalloc call on the
+ * current device (KT_OK, KT_ERR_DEVICE_CHECK or KT_ERR_TIMEOUT), read from the
+ * library's scratch array after synchronising `stream`, then cleared.  Like
+ * the call itself it allocates nothing; the article has no counterpart.
+ * INVALID_ARG if device_status is NULL.
+ */
+kt_status kt_noalloc_read_status(kt_stream_t stream, int32_t* device_status);
 
 /*
  * Synchronises `stream`, stores the workspace status word (a kt_status value,

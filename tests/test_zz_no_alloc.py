@@ -47,7 +47,9 @@ def test_noalloc_attention_matches_workspace_call_twice(kt):
                                                   ctypes.byref(dw.params), sel.data_ptr(),
                                                   cnt.data_ptr(), out.data_ptr(), stream)
         assert st == kt.KT_OK, kt.status_string(st)
-        torch.cuda.synchronize()
+        dev_status = ctypes.c_int32(-1)
+        assert kt.lib.kt_noalloc_read_status(stream, ctypes.byref(dev_status)) == kt.KT_OK
+        assert dev_status.value == kt.KT_OK, kt.status_string(dev_status.value)
         got = out.cpu().numpy()
         assert np.isfinite(got).all()
         assert row_rel_err(got, want).max() <= TOL
