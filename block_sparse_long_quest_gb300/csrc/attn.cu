@@ -848,11 +848,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       // own loads (the representative rows, the slot polls) behind it.  They
       // land while the top-k is picked.  This CTA's share of the chosen
       // blocks follows once the selection is made.
-      if (lane == 0) mbar_wait_sleep(bar_seen, 0, p.status, 64);
+      // plain try_wait spins: a sleep between polls can outlast the wait itself
+      if (lane == 0) mbar_wait(bar_seen, 0, p.status);
       __syncwarp();
       produce(0, a0, a1);
       int n1 = 0, i0 = 0;
-      if (lane == 0 && mbar_wait_sleep(bar_sel, 0, p.status, 128)) {
+      if (lane == 0 && mbar_wait(bar_sel, 0, p.status)) {
         n1 = bcast[61];
         i0 = bcast[62];
       }
