@@ -287,3 +287,36 @@ def test_step_after_query_change_uses_the_new_selection():
                     assert row_rel_err(out[b, hs], ref["out"][b, hs]).max() <= TOL
         assert kt.kt_read_device_status(ws) == kt.KT_OK
 
+
+
+def test_host_buffer_step_replays_and_follows_host_inputs():
+    # kt_sparse_decode_step_host (upload, step, download, sync) on a stream and
+    # on the legacy default stream: outputs follow the host query as it
+    # changes between calls and match the oracle
+    import torch
+    import block_sparse_long_quest_gb300 as kt
+    w = synth.custom(35, [128 * 20 + 9], num_q_heads=8, num_kv_heads=2, top_k=4,
+                     head_mode=synth.HEAD_SHARED)
+    dw = DevWorkload(w)
+    dw.build_reps()
+    ws = kt.workspace(kt.KT_OP_SPARSE_STEP, dw.kv, dw.params)
+    sel = torch.zeros((1, 1, 4), dtype=torch.int32, device="cuda")
+    cnt = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    q_dev = torch.empty_like(dw.q)
+    out_dev = torch.empty((1, 8, 128), dtype=torch.float32, device="cuda")
+    q_host = torch.empty_like(dw.q, device="cpu").pin_memory()
+    out_host = torch.empty_like(out_dev, device="cpu").pin_memory()
+    stream = torch.cuda.Stream()
+    rng = np.random.default_rng(7)
+    for i in range(4):
+        qb = rng.standard_normal(w.q.shape).astype(np.float16)
+        q_host.copy_(torch.from_numpy(qb))
+        st = stream if i < 3 else 0  # the last call on the legacy default stream
+        kt.kt_sparse_decode_step_host(q_host, q_dev, dw.kv, dw.reps, dw.params, sel, cnt, out_dev,
+                                      out_host, ws, st)
+        w2 = synth.custom(35, [128 * 20 + 9], num_q_heads=8, num_kv_heads=2, top_k=4,
+                          head_mode=synth.HEAD_SHARED)
+        w2.q = qb.view(np.uint16)
+        ref = oracle.sparse_step(oracle.KV.of(w2), w2.q, w2.params)
+        assert row_rel_err(out_host.numpy(), ref["out"]).max() <= TOL, i
+    assert kt.kt_read_device_status(ws) == kt.KT_OK
