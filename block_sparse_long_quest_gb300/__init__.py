@@ -37,7 +37,7 @@ EXPORTS = (
     "kt_sparse_decode_step_presel", "kt_decode_history_slots", "kt_decode_layer_action",
     "kt_decode_layer", "kt_append_kv", "kt_set_max_ctas", "kt_set_phase_stamps",
     "kt_sparse_decode_attn_hostkv", "kt_quantize_kv_q8_0", "kt_sparse_decode_attn_q8_0",
-    "kt_noalloc_read_status",
+    "kt_noalloc_read_status", "kt_selftest_step_timeout",
 )
 
 
@@ -117,6 +117,8 @@ def _load():
                                                 vp]),
         "kt_read_device_status": (ctypes.c_int, [vp, sz, vp, P(i32)]),
         "kt_selftest_bounded_wait": (ctypes.c_int, [vp, sz, i32, vp]),
+        "kt_selftest_step_timeout": (ctypes.c_int, [vp, P(PagedKV), vp, P(SparseParams), vp, vp,
+                                                    vp, vp, sz, i32, i32, vp]),
         "kt_noalloc_read_status": (ctypes.c_int, [vp, P(i32)]),
         "kt_sparse_decode_attn_noalloc": (ctypes.c_int, [vp, P(PagedKV), P(SparseParams), vp,
                                                          vp, vp, vp]),

@@ -123,6 +123,8 @@ struct Params {
   const __half* v_src;
   const __half* k_scale;  // KVM_Q8: binary16 scales [P][H_kv][128][4]
   const __half* v_scale;
+  int skip_publish;                  // fused, failure-path test only: CTA + 1, 0 = none
+  unsigned long long poll_limit_ns;  // fused: bound of the slot and partial polls
 };
 
 // Phase stamp i of this CTA (global timer, ns) when stamps are requested.
@@ -434,7 +436,8 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
   }
   // the slice's best min(nloc, kk_f) keys as tagged slots, in descending key
   // order, then its empty slots; no fence: readers check each slot's tag
-  const uint32_t tag = (uint32_t)sh_int[12];
+  // (failure-path test: one CTA publishes nothing, so its unit's polls time out)
+  const uint32_t tag = (int)blockIdx.x + 1 == p.skip_publish ? 0u : (uint32_t)sh_int[12];
   int nreal = nloc;
   bool few = nloc <= p.kk_f;  // every key of the slice is a candidate
   if (p.presel_mask) {
@@ -540,7 +543,7 @@ __device__ int fused_pick(const Params& p, uint8_t* scr, unsigned long long* sh_
       ok = ok && (static_cast<uint32_t>(kx[r]) & ((1u << FUSED_TAG_BITS) - 1u)) == tag &&
            (px[r] & ((1u << FUSED_TAG_BITS) - 1u)) == tag;
     }
-    if (named_bar_and(1, NCT, ok || globaltimer() - t0 > WAIT_LIMIT_NS)) break;
+    if (named_bar_and(1, NCT, ok || globaltimer() - t0 > p.poll_limit_ns)) break;
   }
   if (!ok) set_status(p.status, KT_ERR_TIMEOUT);
   if (ctid == 0) {
@@ -1197,7 +1200,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
           for (int i = 0; i < 4; ++i) Ow[i] = fmaf(Ow[i], a0, v[1 + i]);
           Mw = Mn;
         }
-        if (named_bar_and(1, NCT, ok || globaltimer() - t0 > WAIT_LIMIT_NS)) break;
+        if (named_bar_and(1, NCT, ok || globaltimer() - t0 > p.poll_limit_ns)) break;
       }
       if (!ok) set_status(p.status, KT_ERR_TIMEOUT);
       if (ctid == 0) KT_STAMP(p, 11);
@@ -1361,6 +1364,8 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   p.v_src = static_cast<const __half*>(a.v_src);
   p.k_scale = static_cast<const __half*>(a.k_scale);
   p.v_scale = static_cast<const __half*>(a.v_scale);
+  p.skip_publish = a.skip_publish;
+  p.poll_limit_ns = a.poll_limit_ns ? a.poll_limit_ns : WAIT_LIMIT_NS;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);

@@ -780,7 +780,8 @@ namespace {
 kt_status step_impl(const void* q, const kt_paged_kv* kv, const void* reps_pool,
                     const kt_sparse_params* p, const uint32_t* presel_mask,
                     const int32_t* presel_cnt, int32_t* sel, int32_t* cnt, float* out, void* ws,
-                    size_t ws_bytes, kt_stream_t stream) {
+                    size_t ws_bytes, kt_stream_t stream, int skip_publish = 0,
+                    unsigned long long poll_limit_ns = 0, bool fused_only = false) {
   kt_status s = check_kv(kv);
   if (s != KT_OK) return s;
   s = check_params(kv, p);
@@ -843,8 +844,11 @@ kt_status step_impl(const void* q, const kt_paged_kv* kv, const void* reps_pool,
     a.presel_cnt = presel_cnt;
     a.mask_words = mask_words_of(kv);
     a.stamps = stamps_for(a.grid);
+    a.skip_publish = skip_publish;
+    a.poll_limit_ns = poll_limit_ns;
     return cuda_status(launch_attention(a, (cudaStream_t)stream));
   }
+  if (fused_only) return KT_ERR_UNSUPPORTED;
   s = select_impl(q, kv, reps_pool, p, sel, cnt, nullptr, ws, L, true, (cudaStream_t)stream,
                   presel_mask);
   if (s != KT_OK) return s;
@@ -1036,6 +1040,15 @@ kt_status kt_set_max_ctas(int32_t max_ctas) {
   if (max_ctas < 0) return KT_ERR_INVALID_ARG;
   max_ctas_cap = max_ctas;
   return KT_OK;
+}
+
+kt_status kt_selftest_step_timeout(const void* q, const kt_paged_kv* kv, const void* reps_pool,
+                                   const kt_sparse_params* p, int32_t* sel, int32_t* cnt,
+                                   float* out, void* ws, size_t ws_bytes, int32_t skip_cta,
+                                   int32_t poll_limit_us, kt_stream_t stream) {
+  if (skip_cta < 0 || poll_limit_us < 1) return KT_ERR_INVALID_ARG;
+  return step_impl(q, kv, reps_pool, p, nullptr, nullptr, sel, cnt, out, ws, ws_bytes, stream,
+                   skip_cta + 1, (unsigned long long)poll_limit_us * 1000ull, true);
 }
 
 kt_status kt_selftest_bounded_wait(void* ws, size_t ws_bytes, int32_t spin_limit,

@@ -573,6 +573,11 @@ struct AttnLaunch {
   const void* v_src;
   const void* k_scale;
   const void* v_scale;
+  // one-launch step, failure-path test only: CTA skip_publish - 1 publishes
+  // no candidate slots (0: every CTA publishes), and the slot and partial
+  // polls give up after poll_limit_ns (0: the usual bound)
+  int skip_publish;
+  unsigned long long poll_limit_ns;
 };
 int attn_fused_max_ctas_per_sm();
 cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream);

@@ -543,6 +543,21 @@ kt_status kt_read_device_status(void* ws, size_t ws_bytes, kt_stream_t stream,
 kt_status kt_selftest_bounded_wait(void* ws, size_t ws_bytes, int32_t spin_limit,
                                    kt_stream_t stream);
 
+/*
+ * Diagnostic of the one-launch step's failure path: runs kt_sparse_decode_step
+ * (one-launch shapes only; UNSUPPORTED otherwise) with CTA `skip_cta`
+ * publishing no candidate slots, so the polls of its selection unit never see
+ * them, and with the slot and partial polls bounded by poll_limit_us.  The
+ * launch records KT_ERR_TIMEOUT in the workspace status word and finishes
+ * (the chosen ids and pages are range-checked, so nothing reads out of
+ * bounds; sel/cnt/out of this launch are meaningless), and the workspace
+ * serves the next step unchanged.  Used to test that path without a fault.
+ */
+kt_status kt_selftest_step_timeout(const void* q, const kt_paged_kv* kv, const void* reps_pool,
+                                   const kt_sparse_params* p, int32_t* sel, int32_t* cnt,
+                                   float* out, void* ws, size_t ws_bytes, int32_t skip_cta,
+                                   int32_t poll_limit_us, kt_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -193,6 +193,38 @@ def test_bounded_wait_times_out_with_status():
     assert kt.kt_read_device_status(ws) == kt.KT_ERR_TIMEOUT
 
 
+@pytest.mark.parametrize("mode", [synth.HEAD_SHARED, synth.HEAD_SEPARATE])
+def test_one_launch_step_timeout_records_status_and_recovers(mode):
+    # one CTA publishes no candidate slots: its unit's slot polls run out (2 ms
+    # limit), the launch records KT_ERR_TIMEOUT and finishes, and the same
+    # workspace then serves a normal step with the normal result
+    import ctypes
+
+    import torch
+    import block_sparse_long_quest_gb300 as kt
+    w = synth.custom(36, [128 * 60 + 5], num_q_heads=8, num_kv_heads=2, top_k=4,
+                     head_mode=mode)
+    dw = DevWorkload(w)
+    dw.build_reps()
+    assert kt.kt_sparse_decode_step_kernels(dw.kv, dw.params) == 1
+    ws = kt.workspace(kt.KT_OP_SPARSE_STEP, dw.kv, dw.params)
+    s0, c0, o0, _ = dw.step(ws)
+    assert kt.kt_read_device_status(ws) == kt.KT_OK
+    sel, cnt, out = torch.zeros_like(s0), torch.zeros_like(c0), torch.zeros_like(o0)
+    st = kt.lib.kt_selftest_step_timeout(
+        dw.q.data_ptr(), ctypes.byref(dw.kv), dw.reps.data_ptr(), ctypes.byref(dw.params),
+        sel.data_ptr(), cnt.data_ptr(), out.data_ptr(), ws.data_ptr(), ws.numel(), 0, 2000,
+        torch.cuda.current_stream().cuda_stream)
+    assert st == kt.KT_OK, kt.status_string(st)
+    assert kt.kt_read_device_status(ws) == kt.KT_ERR_TIMEOUT
+    s2, c2, o2, _ = dw.step(ws)
+    assert kt.kt_read_device_status(ws) == kt.KT_OK
+    assert (s2 == s0).all() and (c2 == c0).all() and (o2 == o0).all()
+    ref = _oracle(w)
+    for u in range(dw.SEL):
+        assert selection_agrees(s2.cpu().numpy(), c2.cpu().numpy(), ref, 0, u)[0]
+
+
 def test_workspace_reuse_is_stable():
     # counters are reset by each call: repeated calls give identical results
     w = synth.custom(30, RAGGED, num_q_heads=8, num_kv_heads=2, top_k=4)
