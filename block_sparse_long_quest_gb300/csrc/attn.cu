@@ -939,10 +939,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     }
     if (in.ntok > warp * 16) {
       if constexpr (KVM == KVM_Q8) {
-        // this warp's 16 token rows of K and V: int8 code * binary16 scale
-        // (exact in fp32), rounded once to fp16, into the fp16 block at the
-        // start of the ring in the layout of an fp16 stage (lane: one row,
-        // half its channels)
+        // this warp's 16 token rows of K and V: int8 code * binary16 scale,
+        // rounded once to fp16, into the fp16 block at the start of the ring
+        // in the layout of an fp16 stage (lane: one row, half its channels)
         const uint8_t* qst = smem + SmemLayout::kv + Q8_RING_OFF + st * Q8_STAGE_BYTES;
         const int rr = lane >> 1, hh = lane & 1, tok = warp * 16 + rr, sw = tok & 7;
 #pragma unroll
@@ -955,15 +954,20 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
           for (int i = 0; i < 4; ++i) {
             const int c16 = 4 * hh + i;  // 16-channel piece of the int8 row
             const uint4 v = *reinterpret_cast<const uint4*>(codes + ((c16 ^ sw) << 4));
-            const float dq = __half2float(scl[c16 >> 1]);
+            const __half2 d2 = __half2half2(scl[c16 >> 1]);
             const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
             uint32_t h2[8];
+            // code c as binary16: the byte c + 128 in the low mantissa of 1024
+            // gives 1152 + c exactly; subtracting 1152 leaves c, and one
+            // correctly rounded binary16 product gives round(c * scale)
+            const __half2 bias = __float2half2_rn(1152.0f);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const int b0 = (int)(int8_t)(wv[j] & 0xFFu), b1 = (int)(int8_t)((wv[j] >> 8) & 0xFFu);
-              const int b2 = (int)(int8_t)((wv[j] >> 16) & 0xFFu), b3 = (int)(int8_t)(wv[j] >> 24);
-              const __half2 lo2 = __floats2half2_rn((float)b0 * dq, (float)b1 * dq);
-              const __half2 hi2 = __floats2half2_rn((float)b2 * dq, (float)b3 * dq);
+              const uint32_t u = wv[j] ^ 0x80808080u;
+              const uint32_t lo = __byte_perm(u, 0x64646464u, 0x5140);
+              const uint32_t hi = __byte_perm(u, 0x64646464u, 0x7362);
+              const __half2 lo2 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&lo), bias), d2);
+              const __half2 hi2 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&hi), bias), d2);
               h2[2 * j] = *reinterpret_cast<const uint32_t*>(&lo2);
               h2[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi2);
             }
