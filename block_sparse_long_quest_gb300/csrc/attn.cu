@@ -112,7 +112,7 @@ struct Params {
   unsigned long long* f_cand;
   int f_cand_len;
   uint32_t* f_cpage;
-  int* f_sync;
+  unsigned long long* f_sync;
   int32_t* sel_out;
   int32_t* cnt_out;
   const uint32_t* presel_mask;
@@ -302,13 +302,39 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
                             uint32_t ring_u32, uint32_t bar_reps) {
   const int U = p.B * p.SEL;
   const int u = blockIdx.x / p.ncpu;
-  // this launch's slot tag, which every CTA needs for the pick
-  const uint32_t epoch = ctid == 0 ? ld_relaxed_gpu_u32(p.f_sync) : 0u;
+  // this launch's epoch: its slot and partial tags, which every CTA needs for
+  // the pick, are set once the slice's first loads are out; this CTA's share
+  // of the advance to the next epoch is added once its slots are written
+  // (every CTA passes there exactly once, whatever its waits gave)
+  unsigned long long counter = 0;
+  if (ctid == 0) {
+    counter = ld_relaxed_gpu_u64(p.f_sync);
+  }
+  auto add_share = [&] {
+    const unsigned long long c = blockIdx.x, g = gridDim.x;
+    red_relaxed_gpu_add_u64(p.f_sync, (((c + 1) << FUSED_EPOCH_SHIFT) / g) -
+                                          ((c << FUSED_EPOCH_SHIFT) / g));
+  };
+  auto set_tags = [&] {
+    const unsigned long long epoch = counter >> FUSED_EPOCH_SHIFT;
+    sh_int[12] = (int)(1u + (uint32_t)(epoch % FUSED_TAG_CYCLE));
+    sh_int[15] = (int)(1u + (uint32_t)(epoch % 0xFFFFFFFEull));  // partial tag (never 0)
+  };
+  // the slots past this launch's layout get tag 0: each launch writes every slot
+  auto fill_tail = [&] {
+    const int used = U * p.ncpu * p.kk_f;
+#pragma unroll 1
+    for (int i = used + (int)blockIdx.x * NCT + ctid; i < p.f_cand_len; i += (int)gridDim.x * NCT) {
+      st_relaxed_gpu_u64(p.f_cand + i, 0ull);
+      st_relaxed_gpu_u32(p.f_cpage + i, 0u);
+    }
+  };
   if (u >= U) {
+    fill_tail();
     if (ctid == 0) {
-      sh_int[12] = (int)(1u + epoch % FUSED_TAG_CYCLE);
-      sh_int[15] = (int)(1u + epoch % 0xFFFFFFFEu);  // partial tag (never 0)
+      set_tags();
       mbar_arrive(bar_scored);
+      add_share();
     }
     return;
   }
@@ -329,6 +355,7 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     const int j = js + i;
     pgs[i] = j < p.max_blocks ? __ldg(p.table + (size_t)bu * p.max_blocks + j) : -1;
   }
+  fill_tail();
   // the slice's candidate and page slots, each written once below with this
   // launch's tag
   unsigned long long* cand = p.f_cand + ((size_t)u * p.ncpu + cs) * p.kk_f;
@@ -338,8 +365,7 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
   const int nloc = max(0, je - js);  // js >= c0 whenever the slice is not empty
   if (ctid == 0) {
     if (nloc & 1) keys[nloc] = 0ull;  // the ranking's zero padding
-    sh_int[12] = (int)(1u + epoch % FUSED_TAG_CYCLE);
-    sh_int[15] = (int)(1u + epoch % 0xFFFFFFFEu);  // partial tag (never 0)
+    set_tags();
   }
   bar_c();
   if (ctid == 0) KT_STAMP(p, 1);
@@ -459,8 +485,18 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     nreal = sh_int[3];
     few = few || nreal <= p.kk_f;
   }
-  // SK_COLS launches have slices of at most top_k blocks: always `few`
-  if (SK != SK_COLS && !few) {
+  if (p.f_chunk <= p.kk_f) {
+    // every slice fits its slots: block i of the slice goes to slot i (a zero
+    // key is an empty slot), so the unit's slots run in block order and the
+    // pick's ids come out sorted.  SK_COLS launches (slices of at most top_k
+    // blocks) always take this path.
+#pragma unroll 1
+    for (int i = ctid; i < p.kk_f; i += NCT) {
+      const bool in = i < nloc;
+      st_relaxed_gpu_u64(cand + i, fused_slot(in ? keys[i] : 0ull, tag));
+      st_relaxed_gpu_u32(cpage + i, in ? (((uint32_t)pgs[i] & 0xFFFFFu) << FUSED_TAG_BITS | tag) : tag);
+    }
+  } else if (SK != SK_COLS && !few) {
     auto emit = [&](int r, int i) {
       st_relaxed_gpu_u64(cand + r, fused_slot(keys[i], tag));
       st_relaxed_gpu_u32(cpage + r, ((uint32_t)pgs[i] & 0xFFFFFu) << FUSED_TAG_BITS | tag);
@@ -492,9 +528,11 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
       st_relaxed_gpu_u32(cpage + r, tag);
     }
   }
-  // the slots carry their own validity; a fence after the CTA's stores only
-  // pushes them out to L2 now rather than whenever the SM drains them
-  if (ctid == 0) KT_STAMP(p, 4);
+  // the slots carry their own validity: no fence
+  if (ctid == 0) {
+    KT_STAMP(p, 4);
+    add_share();
+  }
 }
 
 // Fused step, consumer warps of every CTA: read the candidate slots of this
@@ -569,6 +607,49 @@ __device__ int fused_pick(const Params& p, uint8_t* scr, unsigned long long* sh_
       return 0;
     }
   }
+  if (p.f_chunk <= p.kk_f) {
+    // slots in block order (one block per slot): a chosen slot's rank among
+    // the chosen is the count of chosen slots before it.  Slot s = ctid + r *
+    // NCT, so the order is (r, warp, lane): per-warp ballot counts for each r
+    // (in the histogram area, free again) give every chosen key its place.
+    int* wcnt = reinterpret_cast<int*>(scr + Lp.hist);  // [GP][CONSUMERS]
+    const int lane = ctid & 31, w = ctid >> 5;
+    const unsigned int lt = (1u << lane) - 1u;
+    unsigned int bal[GP];
+#pragma unroll
+    for (int r = 0; r < GP; ++r) bal[r] = __ballot_sync(0xffffffffu, kx[r] != 0ull && kx[r] >= T);
+    if (lane == 0) {
+#pragma unroll
+      for (int r = 0; r < GP; ++r) wcnt[r * CONSUMERS + w] = __popc(bal[r]);
+    }
+    bar_c();
+#pragma unroll
+    for (int r = 0; r < GP; ++r) {
+      if ((bal[r] >> lane) & 1u) {
+        const int t = r * CONSUMERS + w;
+        int pos = __popc(bal[r] & lt);
+#pragma unroll
+        for (int q = 0; q < GP * CONSUMERS / 4; ++q) {
+          if (4 * q < t) {
+            const int4 c4 = reinterpret_cast<const int4*>(wcnt)[q];
+            pos += c4.x + (4 * q + 1 < t ? c4.y : 0) + (4 * q + 2 < t ? c4.z : 0) +
+                   (4 * q + 3 < t ? c4.w : 0);
+          }
+        }
+        if (pos < keff) {
+          const int id = fused_slot_block(kx[r]);
+          sorted[pos] = id;
+          sorted_pages[pos] = static_cast<int>(px[r] >> FUSED_TAG_BITS);
+          if (writer) p.sel_out[(size_t)unit * p.top_k + pos] = static_cast<int32_t>(id);
+        }
+      }
+    }
+    if (writer && ctid == 0) p.cnt_out[unit] = keff;
+    bar_c();
+    const int i0 = (int)((long long)ci * keff / ncta), i1 = (int)((long long)(ci + 1) * keff / ncta);
+    *i0_out = i0;
+    return i1 - i0;
+  }
   // the chosen blocks' ids, one shared atomic per warp
   {
     const int lane = ctid & 31;
@@ -608,28 +689,6 @@ __device__ int fused_pick(const Params& p, uint8_t* scr, unsigned long long* sh_
   const int i0 = (int)((long long)ci * keff / ncta), i1 = (int)((long long)(ci + 1) * keff / ncta);
   *i0_out = i0;
   return i1 - i0;
-}
-
-// Fused step, all consumer threads of a CTA as it leaves: the CTA counts
-// itself done, and the last CTA of the launch advances the launch epoch (every
-// CTA read it when it started) and, when the slot tags wrap, zeroes the slot
-// region so that no stale slot can carry a live tag.
-__device__ __forceinline__ void fused_exit(const Params& p, int ctid, int* sh_last) {
-  if (ctid == 0) *sh_last = atomicAdd(p.f_sync + 1, 1) == (int)gridDim.x - 1 ? 1 : 0;
-  named_bar_sync(1, NCT);
-  if (!*sh_last) return;
-  const uint32_t e = ld_relaxed_gpu_u32(p.f_sync);
-  if (1u + e % FUSED_TAG_CYCLE == FUSED_TAG_CYCLE) {
-#pragma unroll 1
-    for (int i = ctid; i < p.f_cand_len; i += NCT) {
-      p.f_cand[i] = 0ull;
-      p.f_cpage[i] = 0u;
-    }
-  }
-  if (ctid == 0) {
-    p.f_sync[1] = 0;
-    p.f_sync[0] = static_cast<int>(e + 1u);
-  }
 }
 
 template <int SK, int KVM = KVM_F16>
@@ -797,7 +856,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
               const uint32_t bar = bar_full + 8 * st;
               if (ntok_k > 0) {
                 if (it == 0) KT_STAMP(p, 7);
-                if (phase == 1 && k == 0 && base == u0) KT_STAMP(p, 8);
+                if (phase == 1 && k == 0 && base == 0) KT_STAMP(p, 8);  // none issued by the consumers
                 if constexpr (KVM == KVM_F16) {
                   mbar_arrive_expect_tx(bar, KV_STAGE_BYTES);
                   const uint32_t dst = kv_base + st * KV_STAGE_BYTES;
@@ -854,30 +913,43 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       // plain try_wait spins: a sleep between polls can outlast the wait itself
       if (lane == 0) mbar_wait(bar_seen, 0, p.status);
       __syncwarp();
-      produce(0, a0, a1);
-      int n1 = 0, i0 = 0;
-      if (lane == 0 && mbar_wait(bar_sel, 0, p.status)) {
-        n1 = bcast[61];
-        i0 = bcast[62];
-      }
-      n1 = __shfl_sync(0xffffffffu, n1, 0);
-      fi0 = __shfl_sync(0xffffffffu, i0, 0);
-      if (ok) produce(1, 0, n1);
-    } else {
-      produce(0, a0, a1);
-      // Phase B needs the selection: wait for the grid this launch depends on.
-      griddep_wait();
-      int nB = 0;
-      if (!p.dense) {
-        const int cmax = blocks_b_max(pt, 0, p.top_k);
-        nB = p.cnt ? p.cnt[b * p.SEL + (p.SEL == 1 ? 0 : h)] : cmax;
-        if (nB < 0 || nB > cmax) {
-          set_status(p.status, KT_ERR_DEVICE_CHECK);
-          nB = nB < 0 ? 0 : cmax;
+    }
+    // both phases run the one copy of `produce` (a second inlined copy would
+    // be fetched cold on the way to the first selected load)
+    int u0 = a0, u1 = a1;
+#pragma unroll 1
+    for (int phase = 0; phase < 2 && ok; ++phase) {
+      if (phase == 1) {
+        if (FUSED) {
+          // the consumers issued the first npre chosen blocks into stages
+          // it .. it + npre - 1 themselves; the rest follow from here
+          int n1 = 0, i0 = 0, npre = 0;
+          if (lane == 0 && mbar_wait(bar_sel, 0, p.status)) {
+            n1 = bcast[61];
+            i0 = bcast[62];
+            npre = bcast[63];
+          }
+          u0 = __shfl_sync(0xffffffffu, npre, 0);
+          u1 = __shfl_sync(0xffffffffu, n1, 0);
+          fi0 = __shfl_sync(0xffffffffu, i0, 0);
+          it += (uint32_t)u0;
+        } else {
+          // Phase B needs the selection: wait for the grid this launch depends on.
+          griddep_wait();
+          int nB = 0;
+          if (!p.dense) {
+            const int cmax = blocks_b_max(pt, 0, p.top_k);
+            nB = p.cnt ? p.cnt[b * p.SEL + (p.SEL == 1 ? 0 : h)] : cmax;
+            if (nB < 0 || nB > cmax) {
+              set_status(p.status, KT_ERR_DEVICE_CHECK);
+              nB = nB < 0 ? 0 : cmax;
+            }
+          }
+          u0 = (int)((long long)ci * nB / ncta);
+          u1 = (int)((long long)(ci + 1) * nB / ncta);
         }
       }
-      if (ok)
-        produce(1, (int)((long long)ci * nB / ncta), (int)((long long)(ci + 1) * nB / ncta));
+      produce(phase, u0, u1);
     }
     if (ok) {
       const uint32_t st = it % STAGES;
@@ -903,9 +975,47 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     int i0 = 0;
     const int n1 = fused_pick(p, reinterpret_cast<uint8_t*>(scratch), f_sh_u64, f_sh_int, b, h,
                               ci, ncta, ctid, bar_c, &i0, bar_seen);
+    // The first of this CTA's chosen blocks go straight into the ring stages
+    // that are still unused (the producer's Initial/Local loads took stages
+    // 0 .. nil-1 and waited on none): issued here, one thread a block, not
+    // handed to the producer warp, whose shared-memory reads would queue
+    // behind the consumers' fragment loads once the attention starts.
+    const int nil = a1 - a0;
+    const int npre = nil < STAGES ? min(n1, STAGES - nil) : 0;
+    if (ctid < npre) {
+      const int nsl = p.ncpu * p.kk_f;
+      const FusedPickLayout Lp = fused_pick_layout(nsl, min(p.top_k, nsl));
+      const uint8_t* scr = reinterpret_cast<const uint8_t*>(scratch);
+      const int j = reinterpret_cast<const int*>(scr + Lp.sorted)[i0 + ctid];
+      const int page = reinterpret_cast<const int*>(scr + Lp.sorted_pages)[i0 + ctid];
+      int ntok = 0;
+      if (j < pt.c0 || j >= pt.c1 || page < 0 || page >= p.P) {
+        set_status(p.status, KT_ERR_DEVICE_CHECK);
+      } else {
+        ntok = min(UNIT, pt.n - j * BS);
+      }
+      const uint32_t st = (uint32_t)(nil + ctid);
+      info[st].ntok = ntok;
+      info[st].end = 0;
+      const uint32_t bar = bar_full + 8 * st;
+      if (ntok > 0) {
+        if (ctid == 0) KT_STAMP(p, 8);
+        const int row = (page * p.H_kv + h) * BS;
+        const uint64_t policy = l2_evict_first_policy();
+        mbar_arrive_expect_tx(bar, KV_STAGE_BYTES);
+        const uint32_t dst = kv_base + st * KV_STAGE_BYTES;
+        tma_load_2d(dst, &p.kmap, 0, row, bar, policy);
+        tma_load_2d(dst + BOX_BYTES, &p.kmap, 64, row, bar, policy);
+        tma_load_2d(dst + 2 * BOX_BYTES, &p.vmap, 0, row, bar, policy);
+        tma_load_2d(dst + 3 * BOX_BYTES, &p.vmap, 64, row, bar, policy);
+      } else {
+        mbar_arrive(bar);
+      }
+    }
     if (ctid == 0) {
       bcast[61] = n1;
       bcast[62] = i0;
+      bcast[63] = npre;
       mbar_arrive(bar_sel);
       KT_STAMP(p, 6);
     }
@@ -1133,7 +1243,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   }
   if (ncta == 1) {
     if (ctid == 0) KT_STAMP(p, 10);
-    if constexpr (FUSED) fused_exit(p, ctid, f_sh_int + 14);
     return;
   }
   if constexpr (FUSED) {
@@ -1215,7 +1324,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
       }
     }
     if (ctid == 0) KT_STAMP(p, 12);
-    fused_exit(p, ctid, f_sh_int + 14);
     return;
   } else {
     named_bar_sync(1, NCT);

@@ -113,7 +113,7 @@ WsLayout layout(kt_op op, const kt_paged_kv* kv, const kt_sparse_params* p, int 
                       (size_t)(p->top_k < FUSED_KK_CAP ? (p->top_k > 0 ? p->top_k : 1)
                                                        : FUSED_KK_CAP);
   L.f_sync = off;
-  off = align256(off + 2 * 4);
+  off = align256(off + 8);
   L.f_cand = off;
   L.f_cand_slots = fcap;
   off = align256(off + fcap * 8);
@@ -837,7 +837,7 @@ kt_status step_impl(const void* q, const kt_paged_kv* kv, const void* reps_pool,
     a.f_cand = at<unsigned long long>(ws, L.f_cand);
     a.f_cand_len = (int)L.f_cand_slots;
     a.f_cpage = at<uint32_t>(ws, L.f_cpage);
-    a.f_sync = at<int>(ws, L.f_sync);
+    a.f_sync = at<unsigned long long>(ws, L.f_sync);
     a.sel_out = sel;
     a.cnt_out = cnt;
     a.presel_mask = presel_mask;

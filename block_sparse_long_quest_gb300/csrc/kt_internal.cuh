@@ -102,12 +102,21 @@ __host__ __device__ inline FusedPickLayout fused_pick_layout(int nslots, int kma
 // selection key (score, then lower block) for block ids below 2^20; an empty
 // slot is the tag alone.  Beside each key slot a 4-byte page slot holds
 // (page << 12) | tag, for pages below 2^20.  Tags cycle through 1..4095 (launch epoch modulo
-// 4095, plus one) and the slot region is zeroed when the cycle wraps, so a
-// stale slot never carries a live tag.
+// 4095, plus one).  Every launch writes every slot of the region once (its
+// own slots with its tag, the rest with tag 0), so before a launch writes a
+// slot it holds the previous launch's tag or 0, never the live one.
+//
+// Launch epoch: a 64-bit counter in the workspace to which the CTAs of every
+// launch add shares summing to 2^FUSED_EPOCH_SHIFT (CTA c adds
+// floor((c+1) 2^s / grid) - floor(c 2^s / grid), at least 1 for grids up to
+// 2^s), fire-and-forget.  A CTA reading the counter during launch N sees
+// N 2^s plus the shares of CTAs of launch N other than itself, less than 2^s,
+// so counter >> s is N in every CTA of the launch.
 constexpr int FUSED_MAX_BLOCKS = (1 << 20) - 1;
 constexpr int FUSED_MAX_PAGES = (1 << 20) - 1;
 constexpr uint32_t FUSED_TAG_BITS = 12;
 constexpr uint32_t FUSED_TAG_CYCLE = 4095;
+constexpr int FUSED_EPOCH_SHIFT = 20;
 constexpr int ATTN_MERGE_BYTES = ATTN_SCRATCH_BYTES + (MAX_SEGS + 1) * 4;
 constexpr uint64_t WAIT_LIMIT_NS = 100000000ull;  // 100 ms bound on any device-side wait
 constexpr int KT_PHASE_STAMPS = 16;               // phase stamps per CTA (kt_set_phase_stamps)
@@ -130,7 +139,7 @@ struct WsLayout {
   size_t sel_cand;       // uint64 [B*SEL*nchunks*kk]
   size_t sel_cand_pages; // int32 [B*SEL*nchunks*kk], page id of each candidate
   size_t sel_pages;      // int32 [B*SEL*top_k], page ids of the selection (step path)
-  size_t f_sync;         // int32 [2] fused step: launch epoch, CTAs done with the launch
+  size_t f_sync;         // uint64 fused step: launch counter (epoch = counter >> FUSED_EPOCH_SHIFT)
   size_t f_cand;         // uint64 [MAX_ATTN_CTAS * min(top_k, FUSED_KK_CAP)] tagged slots
   size_t f_cand_slots;   // slots in that region
   size_t f_cpage;        // uint32, one page slot per candidate slot
@@ -194,6 +203,9 @@ __device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned 
 }
 __device__ __forceinline__ void st_relaxed_gpu_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void red_relaxed_gpu_add_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ void st_relaxed_gpu_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -558,7 +570,7 @@ struct AttnLaunch {
   unsigned long long* f_cand;  // tagged candidate slots [B*SEL][ncpu][kk_f]
   int f_cand_len;              // slots in the workspace region (zeroed when tags wrap)
   uint32_t* f_cpage;           // the page slot of each candidate slot
-  int* f_sync;                 // [0] launch epoch, [1] CTAs done with this launch
+  unsigned long long* f_sync;  // launch counter (epoch = counter >> FUSED_EPOCH_SHIFT)
   int32_t* sel_out;
   int32_t* cnt_out;
   const uint32_t* presel_mask;  // nullable [B][SEL][mask_words]
