@@ -350,6 +350,7 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
   int* pgs = reinterpret_cast<int*>(scr + Ls.pgs);
 
   const int js = p.I_b + cs * p.f_chunk;
+  const int n_bu = seq_len(p, bu);  // in flight with the block-table loads below
 #pragma unroll 1
   for (int i = ctid; i < p.f_chunk; i += NCT) {
     const int j = js + i;
@@ -360,7 +361,7 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
   // launch's tag
   unsigned long long* cand = p.f_cand + ((size_t)u * p.ncpu + cs) * p.kk_f;
   uint32_t* cpage = p.f_cpage + ((size_t)u * p.ncpu + cs) * p.kk_f;
-  const Part pu = partition(seq_len(p, bu), p.I_b, p.L_b);
+  const Part pu = partition(n_bu, p.I_b, p.L_b);
   const int je = min(js + p.f_chunk, pu.c1);
   const int nloc = max(0, je - js);  // js >= c0 whenever the slice is not empty
   if (ctid == 0) {
@@ -545,10 +546,9 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
 // array, where the producer reads them.  One CTA per unit writes sel / cnt.
 template <class Bar>
 __device__ int fused_pick(const Params& p, uint8_t* scr, unsigned long long* sh_u64, int* sh_int,
-                          int b, int h, int ci, int ncta, int ctid, Bar bar_c, int* i0_out,
-                          uint32_t bar_seen) {
+                          int b, int h, const Part& pt, int ci, int ncta, int ctid, Bar bar_c,
+                          int* i0_out, uint32_t bar_seen) {
   const int unit = b * p.SEL + (p.SEL == 1 ? 0 : h);
-  const Part pt = partition(seq_len(p, b), p.I_b, p.L_b);
   int keff = min(p.top_k, pt.c1 - pt.c0);
   if (p.presel_mask) keff = min(keff, max(0, __ldg(p.presel_cnt + unit)));
   const int nslots = p.ncpu * p.kk_f, kmax = min(p.top_k, nslots), kpad = (kmax + 3) & ~3;
@@ -646,7 +646,7 @@ __device__ int fused_pick(const Params& p, uint8_t* scr, unsigned long long* sh_
     }
     if (writer && ctid == 0) p.cnt_out[unit] = keff;
     bar_c();
-    const int i0 = (int)((long long)ci * keff / ncta), i1 = (int)((long long)(ci + 1) * keff / ncta);
+    const int i0 = ci * keff / ncta, i1 = (ci + 1) * keff / ncta;
     *i0_out = i0;
     return i1 - i0;
   }
@@ -686,7 +686,7 @@ __device__ int fused_pick(const Params& p, uint8_t* scr, unsigned long long* sh_
   }
   if (writer && ctid == 0) p.cnt_out[unit] = keff;
   bar_c();
-  const int i0 = (int)((long long)ci * keff / ncta), i1 = (int)((long long)(ci + 1) * keff / ncta);
+  const int i0 = ci * keff / ncta, i1 = (ci + 1) * keff / ncta;
   *i0_out = i0;
   return i1 - i0;
 }
@@ -756,25 +756,45 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     fused_score<SK>(p, reinterpret_cast<uint8_t*>(scratch), f_hist, f_sh_u64, f_sh_int, tid, warp,
                 lane, bar_c, bar_scored, smem + SmemLayout::kv, kv_base, bar_reps);
   }
-  if (!FUSED) __syncthreads();
-  else if (warp != CONSUMERS) named_bar_sync(2, THREADS);
-  // CTAs of segment s: [cum[s], cum[s+1])
-  int seg;
-  {
+  // CTAs of segment s: [cum[s], cum[s+1]).  In the fused step the producer
+  // finds this CTA's segment and its sequence's length while the consumers
+  // score, and hands both over in shared memory (the consumers then use the
+  // `cum` area for the pick).
+  int seg, f0, ncta, n_b;
+  if (FUSED && warp != CONSUMERS) {
+    named_bar_sync(2, THREADS);
+    seg = bcast[56];
+    f0 = bcast[57];
+    ncta = bcast[58];
+    n_b = bcast[59];
+  } else {
+    if (!FUSED) __syncthreads();
     int lo = 0, hi = S - 1;  // largest s with first(s) <= cta
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (cum[mid] <= cta) lo = mid; else hi = mid - 1;
     }
     seg = lo;
+    f0 = cum[seg];
+    ncta = cum[seg + 1] - f0;
+    n_b = seq_len(p, seg / p.H_kv);
+    if (FUSED) {
+      if (lane == 0) {
+        bcast[56] = seg;
+        bcast[57] = f0;
+        bcast[58] = ncta;
+        bcast[59] = n_b;
+      }
+      __syncwarp();
+      named_bar_arrive(2, THREADS);
+    }
   }
-  const int f0 = cum[seg], ncta = cum[seg + 1] - f0, ci = cta - f0;
-  // fused: the consumers may overwrite `cum` once the producer has read it
-  if (FUSED && warp == CONSUMERS) named_bar_arrive(2, THREADS);
+  const int ci = cta - f0;
   const int b = seg / p.H_kv, h = seg % p.H_kv;
-  const Part pt = partition(seq_len(p, b), p.I_b, p.L_b);
+  const Part pt = partition(n_b, p.I_b, p.L_b);
   const int nA = blocks_a(pt, p.dense);
-  const int a0 = (int)((long long)ci * nA / ncta), a1 = (int)((long long)(ci + 1) * nA / ncta);
+  // 32-bit products: ci < 2^10 CTAs, nA < 2^20 blocks
+  const int a0 = ci * nA / ncta, a1 = (ci + 1) * nA / ncta;
 
   if (warp == CONSUMERS) {
     // =========================== producer warp ===============================
@@ -973,7 +993,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
 
   if constexpr (FUSED) {
     int i0 = 0;
-    const int n1 = fused_pick(p, reinterpret_cast<uint8_t*>(scratch), f_sh_u64, f_sh_int, b, h,
+    const int n1 = fused_pick(p, reinterpret_cast<uint8_t*>(scratch), f_sh_u64, f_sh_int, b, h, pt,
                               ci, ncta, ctid, bar_c, &i0, bar_seen);
     // The first of this CTA's chosen blocks go straight into the ring stages
     // that are still unused (the producer's Initial/Local loads took stages
@@ -1255,7 +1275,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     if (ctid == 0) KT_STAMP(p, 10);
     // shares are whole groups of 4 channels (a group never straddles a head)
     const int GD = p.G * D, G4 = GD / 4;
-    const int q0 = 4 * (int)((long long)ci * G4 / ncta), q1 = 4 * (int)((long long)(ci + 1) * G4 / ncta);
+    const int q0 = 4 * (ci * G4 / ncta), q1 = 4 * ((ci + 1) * G4 / ncta);
     const unsigned long long* base = reinterpret_cast<const unsigned long long*>(p.parts) +
                                      (size_t)f0 * slot_stride;
     const unsigned long long tagw = static_cast<unsigned long long>(ptag) << 32;
