@@ -18,10 +18,11 @@
 //     only ever holds one online-softmax state.
 //   - A producer warp turns blocks into block-table lookups and 2-D TMA loads
 //     (four 16 KB boxes: K and V, two 64-channel halves each, 128-byte swizzle)
-//     into a 3-stage shared-memory ring.  Phase-B work waits on
-//     griddepcontrol.wait, so when this kernel is a programmatic dependent of
-//     the selection kernel, the Initial/Local blocks stream while selection
-//     runs.
+//     into a 3-stage shared-memory ring.  Every launch is a programmatic
+//     dependent of the kernel before it on the stream: it waits for that
+//     kernel at entry, except behind the selection kernel, where phase B alone
+//     waits (griddepcontrol.wait) and the Initial/Local blocks stream while
+//     the selection runs.
 //   - Eight consumer warps each take 16 tokens of a block: S = q K^T and
 //     O += P V on mma.sync m16n8k16 (fp16 in, fp32 accumulate).  Query heads
 //     are rows 0..G-1 of the A operand; in P V the fp16 split P = P_hi + P_lo
@@ -33,14 +34,18 @@
 //     count merges the segment's partials in CTA order (deterministic).
 //
 // The one-launch decode step (attn_kernel<SK>, SK != SK_NONE; a cooperative
-// launch of one CTA per SM) also makes the selection (§3.1, §4.3, §4.5): while
-// the producer waits, the consumer warps stage and score one slice of a
-// selection unit's Context blocks (fused_score), publish the slice's best keys
-// with a ticket, then wait for the unit's tickets and pick the unit's top-k
-// (fused_merge) and hand this CTA's share of the chosen pages to the producer.
-// Each segment's first CTA merges the partials (every CTA is resident).  SK
-// selects the scoring path at compile time, so a launch carries only the code
-// it runs.
+// launch of one CTA per SM) also makes the selection (§3.1, §4.3, §4.5).
+// While the producer finds the CTA's segment, the consumer warps stage and
+// score one slice of a selection unit's Context blocks (fused_score) and
+// write the slice's candidates to tagged slots in block order; every CTA then
+// reads its unit's slots until all carry this launch's tag, finds the top-k
+// threshold (kth_largest_reg), ranks the chosen blocks by ballot counts
+// (fused_pick) and issues its first chosen blocks' loads itself.  Split-K
+// partials are tagged words as well, and every CTA of a segment merges its
+// share of the output channels from all of them.  No ticket, fence or atomic
+// that anyone waits on is left: the tags come from a launch counter that each
+// CTA advances by its share without waiting.  SK selects the scoring path at
+// compile time, so a launch carries only the code it runs.
 #include "select_common.cuh"
 
 namespace kt {
@@ -124,6 +129,7 @@ struct Params {
   const __half* k_scale;  // KVM_Q8: binary16 scales [P][H_kv][128][4]
   const __half* v_scale;
   int skip_publish;                  // fused, failure-path test only: CTA + 1, 0 = none
+  int wait_at_entry;  // programmatic dependent: wait for the previous grid before any global access
   unsigned long long poll_limit_ns;  // fused: bound of the slot and partial polls
 };
 
@@ -702,6 +708,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   // 1024-byte aligned (128-byte swizzled TMA boxes); offsetting the array
   // itself keeps the accesses below in the shared address space
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  // launched as a programmatic dependent of whatever precedes it on the
+  // stream: only the launch itself overlaps that kernel's tail (a launch
+  // behind the selection kernel waits later, before its selected blocks)
+  if (p.wait_at_entry) griddep_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grid = gridDim.x, cta = blockIdx.x;
   const int S = p.B * p.H_kv, H_q = p.H_kv * p.G;
@@ -821,11 +831,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     }
     uint32_t it = 0;
     bool ok = true;
+    // not fused: the unit's first 32 chosen ids, loaded together with the count
+    int sel32 = -1;
     // phase 0: list index i -> Initial/Local block; phase 1: i -> selected block
     auto produce = [&](int phase, int u0, int u1) {
       for (int base = u0; base < u1 && ok; base += 32) {
         const int i = base + lane;
         int ntok = 0, row = 0;
+        const int sel_i = (!FUSED && phase == 1) ? __shfl_sync(0xffffffffu, sel32, i & 31) : -1;
         if (i < u1) {
           int j, page = -1;
           if (phase == 0) {
@@ -840,7 +853,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
             }
           } else if (p.sel_pages == nullptr) {
             const int unit = p.SEL == 1 ? 0 : h;
-            j = p.sel[((size_t)b * p.SEL + unit) * p.top_k + i];
+            j = i < 32 ? sel_i : p.sel[((size_t)b * p.SEL + unit) * p.top_k + i];
             if (j < pt.c0 || j >= pt.c1) {
               set_status(p.status, KT_ERR_DEVICE_CHECK);
               j = -1;
@@ -959,6 +972,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
           int nB = 0;
           if (!p.dense) {
             const int cmax = blocks_b_max(pt, 0, p.top_k);
+            if (p.sel_pages == nullptr && lane < min(cmax, 32))
+              sel32 = p.sel[((size_t)b * p.SEL + (p.SEL == 1 ? 0 : h)) * p.top_k + lane];
             nB = p.cnt ? p.cnt[b * p.SEL + (p.SEL == 1 ? 0 : h)] : cmax;
             if (nB < 0 || nB > cmax) {
               set_status(p.status, KT_ERR_DEVICE_CHECK);
@@ -1273,6 +1288,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     // G x 128 output channels from every CTA's partial, reading the tagged
     // words until all carry this launch's tag (no fence, no ticket)
     if (ctid == 0) KT_STAMP(p, 10);
+    if (ctid == 0) griddep_launch_dependents();  // the next launch may be scheduled
     // shares are whole groups of 4 channels (a group never straddles a head)
     const int GD = p.G * D, G4 = GD / 4;
     const int q0 = 4 * (ci * G4 / ncta), q1 = 4 * ((ci + 1) * G4 / ncta);
@@ -1348,6 +1364,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   } else {
     named_bar_sync(1, NCT);
     if (ctid == 0) {
+      griddep_launch_dependents();  // the next launch may be scheduled
       const int old = atom_acq_rel_gpu_add(p.counters + seg, 1);
       bcast[60] = (old + 1 == ncta) ? 1 : 0;
     }
@@ -1498,24 +1515,27 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   p.v_scale = static_cast<const __half*>(a.v_scale);
   p.skip_publish = a.skip_publish;
   p.poll_limit_ns = a.poll_limit_ns ? a.poll_limit_ns : WAIT_LIMIT_NS;
+  p.wait_at_entry = (a.fused || !a.pdl) ? 1 : 0;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  // every launch may start while the previous kernel on the stream finishes
+  // (the kernel waits for it, at entry or before its selected blocks)
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 1;
   if (a.fused) {
-    // every CTA must be resident: the producers wait for selection flags set
-    // by other CTAs of the same grid
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-  } else {
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = a.pdl ? 1 : 0;
+    // every CTA must be resident: CTAs wait for candidate slots and partials
+    // written by other CTAs of the same grid
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.numAttrs = 2;
   }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
   if (!a.fused) {
     if (a.kvm == KVM_HOST) return cudaLaunchKernelEx(&cfg, attn_kernel<SK_NONE, KVM_HOST>, p);
     if (a.kvm == KVM_Q8) return cudaLaunchKernelEx(&cfg, attn_kernel<SK_NONE, KVM_Q8>, p);
