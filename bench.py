@@ -245,8 +245,8 @@ class ClockSampler:
 KERNEL_SOURCES = ("attn.cu", "select_common.cuh", "kt_internal.cuh")
 KERNEL_TRAFFIC = {
     "attn_kernel<fused step>": {
-        "bytes": 38265600 + 204800,
-        "sources_sha256": "650f6790f74f1c55f13303dbc08f87551129753381fe9b9e888cdfaf61adcd05"},
+        "bytes": 38270208 + 192256,
+        "sources_sha256": "a632edc269e6c53246ff4e6b3065d7089724641301b2ac059c0c058788370683"},
 }
 
 
