@@ -130,6 +130,7 @@ struct Params {
   const __half* v_scale;
   int skip_publish;                  // fused, failure-path test only: CTA + 1, 0 = none
   int wait_at_entry;  // programmatic dependent: wait for the previous grid before any global access
+  int q_mapped;       // q and out in page-locked host memory (plain loads, no bulk copy of q)
   unsigned long long poll_limit_ns;  // fused: bound of the slot and partial polls
 };
 
@@ -809,8 +810,15 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
   if (warp == CONSUMERS) {
     // =========================== producer warp ===============================
     const uint64_t policy = l2_evict_first_policy();
-    if (lane == 0) {
-      const uint32_t qbytes = (uint32_t)p.G * D * 2;
+    const uint32_t qbytes = (uint32_t)p.G * D * 2;
+    if (p.q_mapped) {
+      // q in host memory: 16-byte loads over the link, then one arrival
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)b * H_q + h * p.G) * D);
+      uint4* dst = reinterpret_cast<uint4*>(smem + SmemLayout::q);
+      for (int i = lane; i < (int)(qbytes / 16); i += 32) dst[i] = src[i];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_q);
+    } else if (lane == 0) {
       mbar_arrive_expect_tx(bar_q, qbytes);
       bulk_load(smem_u32(smem + SmemLayout::q), p.q + ((size_t)b * H_q + h * p.G) * D, qbytes,
                 bar_q);
@@ -1516,6 +1524,7 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
   p.skip_publish = a.skip_publish;
   p.poll_limit_ns = a.poll_limit_ns ? a.poll_limit_ns : WAIT_LIMIT_NS;
   p.wait_at_entry = (a.fused || !a.pdl) ? 1 : 0;
+  p.q_mapped = a.q_mapped ? 1 : 0;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);

@@ -781,7 +781,8 @@ kt_status step_impl(const void* q, const kt_paged_kv* kv, const void* reps_pool,
                     const kt_sparse_params* p, const uint32_t* presel_mask,
                     const int32_t* presel_cnt, int32_t* sel, int32_t* cnt, float* out, void* ws,
                     size_t ws_bytes, kt_stream_t stream, int skip_publish = 0,
-                    unsigned long long poll_limit_ns = 0, bool fused_only = false) {
+                    unsigned long long poll_limit_ns = 0, bool fused_only = false,
+                    bool q_mapped = false) {
   kt_status s = check_kv(kv);
   if (s != KT_OK) return s;
   s = check_params(kv, p);
@@ -846,9 +847,10 @@ kt_status step_impl(const void* q, const kt_paged_kv* kv, const void* reps_pool,
     a.stamps = stamps_for(a.grid);
     a.skip_publish = skip_publish;
     a.poll_limit_ns = poll_limit_ns;
+    a.q_mapped = q_mapped;
     return cuda_status(launch_attention(a, (cudaStream_t)stream));
   }
-  if (fused_only) return KT_ERR_UNSUPPORTED;
+  if (fused_only || q_mapped) return KT_ERR_UNSUPPORTED;
   s = select_impl(q, kv, reps_pool, p, sel, cnt, nullptr, ws, L, true, (cudaStream_t)stream,
                   presel_mask);
   if (s != KT_OK) return s;
@@ -888,6 +890,18 @@ kt_status kt_sparse_decode_step_host(const void* q_host, void* q_dev, const kt_p
   const size_t qbytes = (size_t)kv->batch * p->num_q_heads * D * 2;
   const size_t obytes = (size_t)kv->batch * p->num_q_heads * D * 4;
   cudaStream_t st = (cudaStream_t)stream;
+  if (!q_dev && !out_dev) {
+    // page-locked host buffers mapped for the device: the step kernel reads
+    // the query and writes the output over the link (no copies)
+    const void* qd = host_pool_device_ptr(q_host);
+    const void* od = host_pool_device_ptr(out_host);
+    if (!qd || !od || !aligned16(qd) || !aligned16(od)) return KT_ERR_INVALID_ARG;
+    s = step_impl(qd, kv, reps_pool, p, nullptr, nullptr, sel, cnt,
+                  static_cast<float*>(const_cast<void*>(od)), ws, ws_bytes, stream, 0, 0, false,
+                  true);
+    if (s != KT_OK) return s;
+    return cuda_status(cudaStreamSynchronize(st));
+  }
   if (!q_dev || !out_dev) return KT_ERR_INVALID_ARG;
   if (cudaMemcpyAsync(q_dev, q_host, qbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return KT_ERR_CUDA;

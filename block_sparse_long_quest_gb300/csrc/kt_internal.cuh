@@ -559,6 +559,7 @@ struct AttnLaunch {
   float scale_log2;
   int grid;
   bool pdl;  // launched as a programmatic dependent of the previous kernel
+  bool q_mapped;  // q and out are page-locked host memory read and written over the link
   // fused step (selection inside the attention kernel, cooperative launch)
   bool fused;
   int sk;  // fused: the scoring path (SK_*)

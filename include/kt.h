@@ -400,6 +400,12 @@ kt_status kt_sparse_decode_step_presel(const void* q, const kt_paged_kv* kv,
  * copies q_host (fp16 [batch][num_q_heads][128]) to q_dev, runs
  * kt_sparse_decode_step, copies out_dev to out_host (fp32) and synchronises
  * `stream`.  Host buffers should be pinned for asynchronous copies.
+ * With q_dev and out_dev both NULL, q_host and out_host must be page-locked
+ * host memory mapped for the device (16-byte aligned): the one-launch step
+ * then reads the query and writes the output over the host link itself, with
+ * no copies (INVALID_ARG for other host memory; UNSUPPORTED when the shapes
+ * need the two-kernel path).  Either way the call returns once out_host
+ * holds the output.
  */
 kt_status kt_sparse_decode_step_host(const void* q_host, void* q_dev, const kt_paged_kv* kv,
                                      const void* reps_pool, const kt_sparse_params* p,

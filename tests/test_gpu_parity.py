@@ -352,3 +352,46 @@ def test_host_buffer_step_replays_and_follows_host_inputs():
         ref = oracle.sparse_step(oracle.KV.of(w2), w2.q, w2.params)
         assert row_rel_err(out_host.numpy(), ref["out"]).max() <= TOL, i
     assert kt.kt_read_device_status(ws) == kt.KT_OK
+
+
+def test_host_buffer_step_mapped_reads_and_writes_host_memory():
+    # q_dev and out_dev NULL: the step kernel reads the page-locked query and
+    # writes the output over the host link; the output equals the device
+    # step's bit for bit, follows the host query between calls and matches the
+    # oracle; pageable host memory is refused before any launch
+    import torch
+    import block_sparse_long_quest_gb300 as kt
+    w = synth.custom(36, [128 * 24 + 17], num_q_heads=16, num_kv_heads=4, top_k=5,
+                     head_mode=synth.HEAD_SHARED)
+    dw = DevWorkload(w)
+    dw.build_reps()
+    ws = kt.workspace(kt.KT_OP_SPARSE_STEP, dw.kv, dw.params)
+    sel = torch.zeros((1, 1, 5), dtype=torch.int32, device="cuda")
+    cnt = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    q_host = torch.empty_like(dw.q, device="cpu").pin_memory()
+    out_host = torch.empty((1, 16, 128), dtype=torch.float32, device="cpu").pin_memory()
+    out_dev = torch.empty((1, 16, 128), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    rng = np.random.default_rng(11)
+    for i in range(3):
+        qb = rng.standard_normal(w.q.shape).astype(np.float16)
+        q_host.copy_(torch.from_numpy(qb))
+        out_host.fill_(float("nan"))
+        kt.kt_sparse_decode_step_host(q_host, None, dw.kv, dw.reps, dw.params, sel, cnt, None,
+                                      out_host, ws, stream)
+        got = out_host.clone()
+        q_dev = q_host.cuda()
+        kt.kt_sparse_decode_step(q_dev, dw.kv, dw.reps, dw.params, sel, cnt, out_dev, ws, stream)
+        stream.synchronize()
+        assert torch.equal(got, out_dev.cpu()), i
+        w2 = synth.custom(36, [128 * 24 + 17], num_q_heads=16, num_kv_heads=4, top_k=5,
+                          head_mode=synth.HEAD_SHARED)
+        w2.q = qb.view(np.uint16)
+        ref = oracle.sparse_step(oracle.KV.of(w2), w2.q, w2.params)
+        assert row_rel_err(got.numpy(), ref["out"]).max() <= TOL, i
+    assert kt.kt_read_device_status(ws) == kt.KT_OK
+    pageable = torch.empty_like(dw.q, device="cpu")
+    with pytest.raises(kt.KtError) as e:
+        kt.kt_sparse_decode_step_host(pageable, None, dw.kv, dw.reps, dw.params, sel, cnt, None,
+                                      out_host, ws, stream)
+    assert e.value.status == kt.KT_ERR_INVALID_ARG
