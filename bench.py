@@ -895,9 +895,10 @@ def batched_leg(args, stream):
 
 def q8_leg(args, stream, layers, rep):
     """Q8_0 K/V for the rotated 128K layers: each layer's fp16 pools quantised
-    once (timed on one layer), then per step the selection from the fp16 reps
-    and the attention over the codes; bytes per attended (block, KV head) are
-    2 x (16 KiB codes + 1 KiB scales) instead of 64 KiB."""
+    once (timed on one layer), then per step the one-launch step over the
+    codes (selection from the fp16 reps), beside the attention alone and the
+    two-kernel path; bytes per attended (block, KV head) are 2 x (16 KiB codes
+    + 1 KiB scales) instead of 64 KiB."""
     import torch
 
     import block_sparse_long_quest_gb300 as kt
@@ -929,6 +930,14 @@ def q8_leg(args, stream, layers, rep):
                        args.warmup, stream) / n
     t_step = graph_time([lambda L=L, pq=pq: (L.select(rep), attend(L, pq))
                          for L, pq in zip(layers, pools)], n, args.warmup, stream) / n
+
+    def step(L, pq):
+        v = L.variants[rep]
+        kt.kt_sparse_decode_step_q8_0(L.q, pq["kvq"], v["reps"], v["params"], v["sel"],
+                                      v["cnt"], v["out"], v["ws"])
+
+    t_one = graph_time([lambda L=L, pq=pq: step(L, pq) for L, pq in zip(layers, pools)], n,
+                       args.warmup, stream) / n
     w = layers[0].w
     b = step_bytes(w)
     kv_q8 = b["kv"] * (2 * (16384 + 1024)) // (2 * 32768)
@@ -939,9 +948,11 @@ def q8_leg(args, stream, layers, rep):
             "attention_gbs": kv_q8 / t_att / 1e9,
             "attention_frac_of_hbm_peak": kv_q8 / t_att / 1e9 / peak,
             "fp16_attention_kv_bytes": int(b["kv"]),
+            "step_us (one launch)": t_one * 1e6,
             "step_us (select + attention)": t_step * 1e6,
             "step_bytes": int(b["reps"] + kv_q8),
-            "step_gbs": (b["reps"] + kv_q8) / t_step / 1e9}
+            "step_gbs": (b["reps"] + kv_q8) / t_one / 1e9,
+            "step_frac_of_hbm_peak": (b["reps"] + kv_q8) / t_one / 1e9 / peak}
 
 
 def hostkv_leg(args, stream, layers, rep):

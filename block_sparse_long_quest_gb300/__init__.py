@@ -37,7 +37,7 @@ EXPORTS = (
     "kt_sparse_decode_step_presel", "kt_decode_history_slots", "kt_decode_layer_action",
     "kt_decode_layer", "kt_append_kv", "kt_set_max_ctas", "kt_set_phase_stamps",
     "kt_sparse_decode_attn_hostkv", "kt_quantize_kv_q8_0", "kt_sparse_decode_attn_q8_0",
-    "kt_noalloc_read_status", "kt_selftest_step_timeout",
+    "kt_noalloc_read_status", "kt_selftest_step_timeout", "kt_sparse_decode_step_q8_0",
 )
 
 
@@ -134,6 +134,8 @@ def _load():
         "kt_quantize_kv_q8_0": (ctypes.c_int, [P(PagedKV), vp, vp, vp, vp, i32, i32, vp]),
         "kt_sparse_decode_attn_q8_0": (ctypes.c_int, [vp, P(PagedKVQ8), P(SparseParams), vp, vp,
                                                       vp, vp, sz, vp]),
+        "kt_sparse_decode_step_q8_0": (ctypes.c_int, [vp, P(PagedKVQ8), vp, P(SparseParams), vp,
+                                                      vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -341,6 +343,13 @@ def kt_quantize_kv_q8_0(kv, k_code, k_scale, v_code, v_scale, first_page=0, num_
     _check(lib.kt_quantize_kv_q8_0(ctypes.byref(kv), _ptr(k_code), _ptr(k_scale), _ptr(v_code),
                                    _ptr(v_scale), first_page, n, _stream(stream)),
            "kt_quantize_kv_q8_0")
+
+
+def kt_sparse_decode_step_q8_0(q, kvq, reps_pool, params, sel, cnt, out, ws, stream=None):
+    _check(lib.kt_sparse_decode_step_q8_0(_ptr(q), ctypes.byref(kvq), _ptr(reps_pool),
+                                          ctypes.byref(params), _ptr(sel), _ptr(cnt), _ptr(out),
+                                          _ptr(ws), ws.numel(), _stream(stream)),
+           "kt_sparse_decode_step_q8_0")
 
 
 def kt_sparse_decode_attn_q8_0(q, kvq, params, sel, cnt, out, ws, stream=None):

@@ -701,7 +701,7 @@ __device__ int fused_pick(const Params& p, uint8_t* scr, unsigned long long* sh_
 template <int SK, int KVM = KVM_F16>
 __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant__ Params p) {
   constexpr bool FUSED = SK != SK_NONE;
-  static_assert(!FUSED || KVM == KVM_F16, "the one-launch step reads fp16 pools");
+  static_assert(!FUSED || KVM != KVM_HOST, "the one-launch step reads device pools");
   extern __shared__ uint8_t smem_raw[];
   __shared__ unsigned int f_hist[FUSED ? 512 : 1];
   __shared__ unsigned long long f_sh_u64[FUSED ? 2 + 2 * CONSUMERS : 1];
@@ -1045,12 +1045,23 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         if (ctid == 0) KT_STAMP(p, 8);
         const int row = (page * p.H_kv + h) * BS;
         const uint64_t policy = l2_evict_first_policy();
-        mbar_arrive_expect_tx(bar, KV_STAGE_BYTES);
-        const uint32_t dst = kv_base + st * KV_STAGE_BYTES;
-        tma_load_2d(dst, &p.kmap, 0, row, bar, policy);
-        tma_load_2d(dst + BOX_BYTES, &p.kmap, 64, row, bar, policy);
-        tma_load_2d(dst + 2 * BOX_BYTES, &p.vmap, 0, row, bar, policy);
-        tma_load_2d(dst + 3 * BOX_BYTES, &p.vmap, 64, row, bar, policy);
+        if constexpr (KVM == KVM_Q8) {
+          mbar_arrive_expect_tx(bar, Q8_STAGE_BYTES);
+          const uint32_t dst = kv_base + Q8_RING_OFF + st * Q8_STAGE_BYTES;
+          tma_load_2d(dst, &p.kmap, 0, row, bar, policy);
+          tma_load_2d(dst + Q8_CODE_BYTES, &p.vmap, 0, row, bar, policy);
+          bulk_load(dst + 2 * Q8_CODE_BYTES, p.k_scale + (size_t)row * (D / 32), Q8_SCALE_BYTES,
+                    bar);
+          bulk_load(dst + 2 * Q8_CODE_BYTES + Q8_SCALE_BYTES, p.v_scale + (size_t)row * (D / 32),
+                    Q8_SCALE_BYTES, bar);
+        } else {
+          mbar_arrive_expect_tx(bar, KV_STAGE_BYTES);
+          const uint32_t dst = kv_base + st * KV_STAGE_BYTES;
+          tma_load_2d(dst, &p.kmap, 0, row, bar, policy);
+          tma_load_2d(dst + BOX_BYTES, &p.kmap, 64, row, bar, policy);
+          tma_load_2d(dst + 2 * BOX_BYTES, &p.vmap, 0, row, bar, policy);
+          tma_load_2d(dst + 3 * BOX_BYTES, &p.vmap, 64, row, bar, policy);
+        }
       } else {
         mbar_arrive(bar);
       }
@@ -1446,7 +1457,12 @@ int attn_smem_optin() {
                           (const void*)attn_kernel<SK_LINEAR>, (const void*)attn_kernel<SK_MMA>,
                           (const void*)attn_kernel<SK_F32>, (const void*)attn_kernel<SK_MULTI>,
                           (const void*)attn_kernel<SK_NONE, KVM_HOST>,
-                          (const void*)attn_kernel<SK_NONE, KVM_Q8>})
+                          (const void*)attn_kernel<SK_NONE, KVM_Q8>,
+                          (const void*)attn_kernel<SK_COLS, KVM_Q8>,
+                          (const void*)attn_kernel<SK_LINEAR, KVM_Q8>,
+                          (const void*)attn_kernel<SK_MMA, KVM_Q8>,
+                          (const void*)attn_kernel<SK_F32, KVM_Q8>,
+                          (const void*)attn_kernel<SK_MULTI, KVM_Q8>})
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     return (int)e;
@@ -1463,7 +1479,12 @@ int attn_fused_max_ctas_per_sm() {
     int m = 1 << 30;
     for (const void* f : {(const void*)attn_kernel<SK_COLS>, (const void*)attn_kernel<SK_LINEAR>,
                           (const void*)attn_kernel<SK_MMA>, (const void*)attn_kernel<SK_F32>,
-                          (const void*)attn_kernel<SK_MULTI>}) {
+                          (const void*)attn_kernel<SK_MULTI>,
+                          (const void*)attn_kernel<SK_COLS, KVM_Q8>,
+                          (const void*)attn_kernel<SK_LINEAR, KVM_Q8>,
+                          (const void*)attn_kernel<SK_MMA, KVM_Q8>,
+                          (const void*)attn_kernel<SK_F32, KVM_Q8>,
+                          (const void*)attn_kernel<SK_MULTI, KVM_Q8>}) {
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, THREADS, SMEM_BYTES) !=
           cudaSuccess)
         return 0;
@@ -1550,6 +1571,17 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t stream) {
     if (a.kvm == KVM_Q8) return cudaLaunchKernelEx(&cfg, attn_kernel<SK_NONE, KVM_Q8>, p);
     return cudaLaunchKernelEx(&cfg, attn_kernel<SK_NONE>, p);
   }
+  if (a.kvm == KVM_Q8) {
+    switch (a.sk) {
+      case SK_COLS: return cudaLaunchKernelEx(&cfg, attn_kernel<SK_COLS, KVM_Q8>, p);
+      case SK_LINEAR: return cudaLaunchKernelEx(&cfg, attn_kernel<SK_LINEAR, KVM_Q8>, p);
+      case SK_MMA: return cudaLaunchKernelEx(&cfg, attn_kernel<SK_MMA, KVM_Q8>, p);
+      case SK_F32: return cudaLaunchKernelEx(&cfg, attn_kernel<SK_F32, KVM_Q8>, p);
+      case SK_MULTI: return cudaLaunchKernelEx(&cfg, attn_kernel<SK_MULTI, KVM_Q8>, p);
+    }
+    return cudaErrorInvalidValue;
+  }
+  if (a.kvm != KVM_F16) return cudaErrorInvalidValue;
   switch (a.sk) {
     case SK_COLS: return cudaLaunchKernelEx(&cfg, attn_kernel<SK_COLS>, p);
     case SK_LINEAR: return cudaLaunchKernelEx(&cfg, attn_kernel<SK_LINEAR>, p);

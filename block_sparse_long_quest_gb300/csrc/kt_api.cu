@@ -682,13 +682,9 @@ kt_status kt_quantize_kv_q8_0(const kt_paged_kv* kv, void* k_code, void* k_scale
   return cuda_status(launch_quant(a, (cudaStream_t)stream));
 }
 
-kt_status kt_sparse_decode_attn_q8_0(const void* q, const kt_paged_kv_q8* kvq,
-                                     const kt_sparse_params* p, const int32_t* sel,
-                                     const int32_t* cnt, float* out, void* ws, size_t ws_bytes,
-                                     kt_stream_t stream) {
-  if (!kvq) return KT_ERR_INVALID_ARG;
-  // the shapes and table as a kt_paged_kv (the code pools stand in for the
-  // fp16 pools in the checks; they are never read as fp16)
+// The shapes and table of Q8_0 pools as a kt_paged_kv (the code pools stand
+// in for the fp16 pools in the checks; they are never read as fp16).
+static kt_paged_kv kv_view_q8(const kt_paged_kv_q8* kvq) {
   kt_paged_kv kv;
   kv.k_pool = kvq->k_code;
   kv.v_pool = kvq->v_code;
@@ -700,6 +696,15 @@ kt_status kt_sparse_decode_attn_q8_0(const void* q, const kt_paged_kv_q8* kvq,
   kv.block_size = kvq->block_size;
   kv.max_blocks_per_seq = kvq->max_blocks_per_seq;
   kv.num_pages = kvq->num_pages;
+  return kv;
+}
+
+kt_status kt_sparse_decode_attn_q8_0(const void* q, const kt_paged_kv_q8* kvq,
+                                     const kt_sparse_params* p, const int32_t* sel,
+                                     const int32_t* cnt, float* out, void* ws, size_t ws_bytes,
+                                     kt_stream_t stream) {
+  if (!kvq) return KT_ERR_INVALID_ARG;
+  kt_paged_kv kv = kv_view_q8(kvq);
   kt_status s = check_kv(&kv);
   if (s != KT_OK) return s;
   s = check_params(&kv, p);
@@ -782,7 +787,7 @@ kt_status step_impl(const void* q, const kt_paged_kv* kv, const void* reps_pool,
                     const int32_t* presel_cnt, int32_t* sel, int32_t* cnt, float* out, void* ws,
                     size_t ws_bytes, kt_stream_t stream, int skip_publish = 0,
                     unsigned long long poll_limit_ns = 0, bool fused_only = false,
-                    bool q_mapped = false) {
+                    bool q_mapped = false, const KvSource& src = KvSource()) {
   kt_status s = check_kv(kv);
   if (s != KT_OK) return s;
   s = check_params(kv, p);
@@ -797,12 +802,19 @@ kt_status step_impl(const void* q, const kt_paged_kv* kv, const void* reps_pool,
   if (sms > 0 && fused_plan(kv, p, sms, &ncpu, &chunk, &kk)) {
     // one launch: selection inside the attention kernel
     CUtensorMap kmap, vmap;
-    if (!make_pool_map(&kmap, kv->k_pool, kv) || !make_pool_map(&vmap, kv->v_pool, kv))
+    const bool codes = src.kvm == KVM_Q8;
+    if (!make_pool_map(&kmap, codes ? src.k_src : kv->k_pool, kv, codes) ||
+        !make_pool_map(&vmap, codes ? src.v_src : kv->v_pool, kv, codes))
       return KT_ERR_CUDA;
     AttnLaunch a;
     std::memset(&a, 0, sizeof(a));
     a.kmap = &kmap;
     a.vmap = &vmap;
+    a.kvm = src.kvm;
+    a.k_src = src.k_src;
+    a.v_src = src.v_src;
+    a.k_scale = src.k_scale;
+    a.v_scale = src.v_scale;
     a.q = static_cast<const __half*>(q);
     a.table = kv->block_table;
     a.seq_lens = kv->seq_lens;
@@ -855,7 +867,7 @@ kt_status step_impl(const void* q, const kt_paged_kv* kv, const void* reps_pool,
                   presel_mask);
   if (s != KT_OK) return s;
   return attn_impl(q, kv, p->num_q_heads, p->softmax_scale, p, sel, cnt, out, ws, L, false, true,
-                   (cudaStream_t)stream, true, presel_mask != nullptr);
+                   (cudaStream_t)stream, true, presel_mask != nullptr, src);
 }
 
 }  // namespace
@@ -865,6 +877,24 @@ kt_status kt_sparse_decode_step(const void* q, const kt_paged_kv* kv, const void
                                 const kt_sparse_params* p, int32_t* sel, int32_t* cnt,
                                 float* out, void* ws, size_t ws_bytes, kt_stream_t stream) {
   return step_impl(q, kv, reps_pool, p, nullptr, nullptr, sel, cnt, out, ws, ws_bytes, stream);
+}
+
+kt_status kt_sparse_decode_step_q8_0(const void* q, const kt_paged_kv_q8* kvq,
+                                     const void* reps_pool, const kt_sparse_params* p,
+                                     int32_t* sel, int32_t* cnt, float* out, void* ws,
+                                     size_t ws_bytes, kt_stream_t stream) {
+  if (!kvq) return KT_ERR_INVALID_ARG;
+  const kt_paged_kv kv = kv_view_q8(kvq);
+  if (!kvq->k_scale || !kvq->v_scale || !aligned16(kvq->k_scale) || !aligned16(kvq->v_scale))
+    return KT_ERR_INVALID_ARG;
+  KvSource src;
+  src.kvm = KVM_Q8;
+  src.k_src = kvq->k_code;
+  src.v_src = kvq->v_code;
+  src.k_scale = kvq->k_scale;
+  src.v_scale = kvq->v_scale;
+  return step_impl(q, &kv, reps_pool, p, nullptr, nullptr, sel, cnt, out, ws, ws_bytes, stream, 0,
+                   0, false, false, src);
 }
 
 kt_status kt_sparse_decode_step_presel(const void* q, const kt_paged_kv* kv,

@@ -333,6 +333,20 @@ kt_status kt_sparse_decode_attn_q8_0(const void* q, const kt_paged_kv_q8* kv,
                                      kt_stream_t stream);
 
 /*
+ * The decode step (kt_sparse_decode_step) over Q8_0 pools: the selection
+ * scores the fp16 representatives `reps_pool` (built from the fp16 K before
+ * quantisation, as for kt_score_select_blocks), and the attention reads the
+ * chosen blocks' codes and scales as kt_sparse_decode_attn_q8_0 does.  One
+ * launch when kt_sparse_decode_step_kernels says so for the same shapes,
+ * else selection then attention.  Workspace: KT_OP_SPARSE_STEP.  Same errors
+ * as kt_sparse_decode_step and kt_sparse_decode_attn_q8_0.
+ */
+kt_status kt_sparse_decode_step_q8_0(const void* q, const kt_paged_kv_q8* kv,
+                                     const void* reps_pool, const kt_sparse_params* p,
+                                     int32_t* sel, int32_t* cnt, float* out, void* ws,
+                                     size_t ws_bytes, kt_stream_t stream);
+
+/*
  * Phase timing of the attention launches made from the calling host thread
  * (kt_sparse_decode_attn, kt_sparse_decode_step, kt_dense_decode_attn,
  * kt_decode_layer): with a non-NULL buffer, each CTA of a launch with at most

@@ -113,6 +113,66 @@ def test_q8_of_exactly_stored_kv_equals_fp16_attention():
     assert torch.equal(q8_out, fp16_out)
 
 
+def _q8_step(dw, qp):
+    import torch
+    import block_sparse_long_quest_gb300 as kt
+    B, k = dw.w.batch, dw.w.params.top_k
+    sel = torch.full((B, dw.SEL, k), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, dw.SEL), -1, dtype=torch.int32, device="cuda")
+    out = torch.full((B, dw.w.params.num_q_heads, 128), float("nan"), dtype=torch.float32,
+                     device="cuda")
+    ws = kt.workspace(kt.KT_OP_SPARSE_STEP, dw.kv, dw.params)
+    kt.kt_sparse_decode_step_q8_0(dw.q, qp.kvq, dw.reps, dw.params, sel, cnt, out, ws)
+    assert kt.kt_read_device_status(ws) == kt.KT_OK
+    return sel, cnt, out
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("mode", [synth.HEAD_SHARED, synth.HEAD_SEPARATE])
+def test_q8_step_matches_fp16_selection_and_oracle(G, mode):
+    # the one-launch step over Q8_0 pools: the selection (from the fp16 reps)
+    # equals the fp16 step's, and the output matches the oracle's attention
+    # over the dequantised blocks of that selection
+    import torch
+    import block_sparse_long_quest_gb300 as kt
+    lens = [128 * 30 + 77, 128 * 9, 128 * 5 + 1]
+    w = synth.custom(96, lens, num_q_heads=2 * G, num_kv_heads=2, rep=synth.REP_QUEST,
+                     head_mode=mode, top_k=5, permute_pages=True)
+    dw = DevWorkload(w)
+    dw.build_reps()
+    assert kt.kt_sparse_decode_step_kernels(dw.kv, dw.params) == 1
+    sel16, cnt16, _, _ = dw.step()
+    sel, cnt, out = _q8_step(dw, Q8Pools(dw))
+    assert torch.equal(cnt, cnt16)
+    for b in range(w.batch):
+        for u in range(dw.SEL):
+            c = int(cnt[b, u])
+            assert torch.equal(sel[b, u, :c], sel16[b, u, :c]), (b, u)
+    want = oracle.attend_selection_q8(oracle.KVQ(oracle.KV.of(w)), w.q, w.params,
+                                      sel.cpu().numpy(), cnt.cpu().numpy())
+    assert row_rel_err(out.cpu().numpy(), want).max() <= TOL
+
+
+def test_q8_step_of_exactly_stored_kv_equals_fp16_step():
+    # KV on per-group grids is stored exactly by Q8_0: the Q8_0 step's
+    # output equals the fp16 step's bit for bit
+    import torch
+    rng = np.random.default_rng(97)
+    w = synth.custom(97, [128 * 12 + 40, 128 * 6], num_q_heads=8, num_kv_heads=2,
+                     rep=synth.REP_QUEST, top_k=3, permute_pages=True)
+    P = w.num_pages
+    for name in ("k_pool", "v_pool"):
+        e = rng.integers(0, 9, size=(P, 2, 128, 4, 1))
+        m = rng.integers(-127, 128, size=(P, 2, 128, 4, 32))
+        m[..., 0] = 127
+        setattr(w, name, _f16((m * 2.0 ** -e).reshape(P, 2, 128, 128)))
+    dw = DevWorkload(w)
+    dw.build_reps()
+    sel16, cnt16, out16, _ = dw.step()
+    sel, cnt, out = _q8_step(dw, Q8Pools(dw))
+    assert torch.equal(cnt, cnt16) and torch.equal(out, out16)
+
+
 def _pinned_copy(t):
     import torch
     h = torch.empty(t.shape, dtype=t.dtype, device="cpu", pin_memory=True)
@@ -175,6 +235,17 @@ def test_128k_q8_and_host_kv_full_size():
     for hq in (0, 1, 21, 23):
         want = oracle.attend_q8(kvq, 0, hq, 32, w.q[0, hq], blocks, w.params.softmax_scale)
         assert row_rel_err(q8[0, hq], want) <= TOL, hq
+    # the one-launch step over the Q8_0 pools: the fp16 step's selection,
+    # the oracle's Q8_0 attention on KV heads 0 and 5
+    sel16, cnt16, _, _ = dw.step()
+    qsel, qcnt, qout = _q8_step(dw, Q8Pools(dw))
+    assert torch.equal(qcnt, cnt16) and torch.equal(qsel[0, 0, :32], sel16[0, 0, :32])
+    qout = qout.cpu().numpy()
+    qs = qsel.cpu().numpy()
+    blocks = list(range(c0)) + [int(j) for j in qs[0, 0, :int(qcnt[0, 0])]] + list(range(c1, nb))
+    for hq in (0, 3, 20, 22):
+        want = oracle.attend_q8(kvq, 0, hq, 32, w.q[0, hq], blocks, w.params.softmax_scale)
+        assert row_rel_err(qout[0, hq], want) <= TOL, hq
     hk, hv = _pinned_copy(dw.k), _pinned_copy(dw.v)
     out = torch.full_like(dev_out, float("nan"))
     ws = kt.workspace(kt.KT_OP_SPARSE_ATTN, dw.kv, dw.params)
