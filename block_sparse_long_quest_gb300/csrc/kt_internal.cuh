@@ -288,22 +288,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
   }
 }
 
-// mbar_wait for long waits: sleeps between polls so the waiting warp leaves
-// the shared-memory pipe to the warps doing the work.
-__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, int* status,
-                                                unsigned int sleep_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    __nanosleep(sleep_ns);
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0 && globaltimer() - t0 > WAIT_LIMIT_NS) {
-      set_status(status, KT_ERR_TIMEOUT);
-      return false;
-    }
-  }
-}
-
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -364,15 +348,6 @@ __device__ __forceinline__ void mma_16816_sched(float* d, uint32_t a0, uint32_t 
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// D = A * B + D, m16n8k8, fp16 inputs, fp32 accumulators.
-__device__ __forceinline__ void mma_1688(float* d, uint32_t a0, uint32_t a1, uint32_t b0) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
-      "{%4, %5}, {%6}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(b0));
-}
-
 // 16-byte asynchronous copy global -> shared (L2 only), 16-byte aligned both.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -383,36 +358,14 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Warms one 2-D box of a tensor map into L2 (no data comes back to the SM).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-__device__ __forceinline__ void st_release_gpu(int* p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Ticket counters.  The CTA's writes are ordered before a ticket by a CTA
-// barrier followed by one thread's release (release is cumulative over what
-// the barrier made visible to that thread); the thread that takes the last
-// ticket acquires, and a CTA barrier then orders the other threads' reads.
-__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
+// Ticket counters: a CTA's writes are ordered before its ticket by a CTA
+// barrier followed by one thread's acq_rel add (release is cumulative over
+// what the barrier made visible to that thread); the thread that takes the
+// last ticket acquires, and a CTA barrier then orders the other threads' reads.
 __device__ __forceinline__ int atom_acq_rel_gpu_add(int* p, int v) {
   int old;
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)

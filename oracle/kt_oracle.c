@@ -23,7 +23,7 @@
  *              softmax(q k^T / sqrt(d_k)) as written in [LC §3.2]
  *   dense      the full scan that [LC §1] says the method avoids
  *
- * Readings where the article is silent (each also listed in the design notes):
+ * Readings where the article is silent:
  *   - Initial/Local are whole blocks; Local counts back from the last, possibly
  *     partial, block; with nb <= I + L every block is attended.
  *   - SHARED sums per-head block scores over all query heads; SEPARATE sums over
