@@ -37,10 +37,10 @@
 // launch of one CTA per SM) also makes the selection (§3.1, §4.3, §4.5).
 // While the producer finds the CTA's segment, the consumer warps stage and
 // score one slice of a selection unit's Context blocks (fused_score) and
-// write the slice's candidates to tagged slots in block order; every CTA then
-// reads its unit's slots until all carry this launch's tag, finds the top-k
-// threshold (kth_largest_reg), ranks the chosen blocks by ballot counts
-// (fused_pick) and issues its first chosen blocks' loads itself.  Split-K
+// write the slice's candidates to tagged slots; every CTA then reads its
+// unit's slots until all carry this launch's tag, finds the top-k threshold
+// (kth_largest_reg), orders the chosen blocks by id (fused_pick) and issues
+// its first chosen blocks' loads itself.  Split-K
 // partials are tagged words as well, and every CTA of a segment merges its
 // share of the output channels from all of them.  No ticket, fence or atomic
 // that anyone waits on is left: the tags come from a launch counter that each
@@ -192,28 +192,6 @@ __device__ void warp_prefix(int* pref, int S, F count, int lane) {
   __syncwarp();
 }
 
-// Number of ids in a[0, n) smaller than id; a is 16-byte aligned, n a multiple of 4.
-__device__ __forceinline__ int count_less_u32(const uint32_t* a, int n, uint32_t id) {
-  int r0 = 0, r1 = 0;
-  int m = 0;
-#pragma unroll 1
-  for (; m + 16 <= n; m += 16) {
-    const uint4 v0 = *reinterpret_cast<const uint4*>(a + m);
-    const uint4 v1 = *reinterpret_cast<const uint4*>(a + m + 4);
-    const uint4 v2 = *reinterpret_cast<const uint4*>(a + m + 8);
-    const uint4 v3 = *reinterpret_cast<const uint4*>(a + m + 12);
-    r0 += (v0.x < id ? 1 : 0) + (v0.y < id ? 1 : 0) + (v0.z < id ? 1 : 0) + (v0.w < id ? 1 : 0) +
-          (v1.x < id ? 1 : 0) + (v1.y < id ? 1 : 0) + (v1.z < id ? 1 : 0) + (v1.w < id ? 1 : 0);
-    r1 += (v2.x < id ? 1 : 0) + (v2.y < id ? 1 : 0) + (v2.z < id ? 1 : 0) + (v2.w < id ? 1 : 0) +
-          (v3.x < id ? 1 : 0) + (v3.y < id ? 1 : 0) + (v3.z < id ? 1 : 0) + (v3.w < id ? 1 : 0);
-  }
-#pragma unroll 1
-  for (; m < n; m += 4) {
-    const uint4 v = *reinterpret_cast<const uint4*>(a + m);
-    r0 += (v.x < id ? 1 : 0) + (v.y < id ? 1 : 0) + (v.z < id ? 1 : 0) + (v.w < id ? 1 : 0);
-  }
-  return r0 + r1;
-}
 
 // Fused step: where the scoring CTA stages its slice's representative rows in
 // the KV ring.  When a whole nominal slice fits, it sits at the top of the
@@ -297,8 +275,8 @@ __device__ __forceinline__ void fused_weights(const Params& p, float* wts, int b
 
 // Fused step, consumer warps of CTA c < U*ncpu: score slice c % ncpu (nominal
 // Context blocks I_b + s*f_chunk ...) of selection unit c / ncpu with the same
-// weights, dot products and keys as the selection kernel, keep the slice's best
-// kk_f (key 0 = empty slot) in the unit's candidate table and take a ticket.
+// weights, dot products and keys as the selection kernel and write the slice's
+// best kk_f keys (key 0 = empty slot) to its tagged slots.
 // Arrives on bar_scored once its representative loads are done (every CTA).
 // The block-table entries of the nominal slice do not depend on the sequence
 // length, so they load together with the length and the query rows.
@@ -371,10 +349,7 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
   const Part pu = partition(n_bu, p.I_b, p.L_b);
   const int je = min(js + p.f_chunk, pu.c1);
   const int nloc = max(0, je - js);  // js >= c0 whenever the slice is not empty
-  if (ctid == 0) {
-    if (nloc & 1) keys[nloc] = 0ull;  // the ranking's zero padding
-    set_tags();
-  }
+  if (ctid == 0) set_tags();
   bar_c();
   if (ctid == 0) KT_STAMP(p, 1);
   if (nloc > 0) {
@@ -468,35 +443,23 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     mbar_arrive(bar_scored);  // the producer may start its own loads
     KT_STAMP(p, 3);
   }
-  // the slice's best min(nloc, kk_f) keys as tagged slots, in descending key
-  // order, then its empty slots; no fence: readers check each slot's tag
-  // (failure-path test: one CTA publishes nothing, so its unit's polls time out)
+  // the slice's best min(nloc, kk_f) keys as tagged slots, then its empty
+  // slots; no fence: readers check each slot's tag (failure-path test: one
+  // CTA publishes nothing, so its unit's polls time out)
   const uint32_t tag = (int)blockIdx.x + 1 == p.skip_publish ? 0u : (uint32_t)sh_int[12];
-  int nreal = nloc;
-  bool few = nloc <= p.kk_f;  // every key of the slice is a candidate
   if (p.presel_mask) {
-    // preselection: blocks outside it get key 0, the empty slot; with at most
-    // kk_f real keys left they are all candidates
+    // preselection: blocks outside it get key 0, the empty slot
     const uint32_t* mk = p.presel_mask + (size_t)u * p.mask_words;
-    int real = 0;
 #pragma unroll 1
     for (int i = ctid; i < nloc; i += NCT) {
       const int j = js + i;
       if (!((__ldg(mk + (j >> 5)) >> (j & 31)) & 1u)) keys[i] = 0ull;
-      else ++real;
     }
-    real = selc::warp_sum_int(real);
-    if (ctid == 0) sh_int[3] = 0;
     bar_c();
-    if (lane == 0) atomicAdd(&sh_int[3], real);
-    bar_c();
-    nreal = sh_int[3];
-    few = few || nreal <= p.kk_f;
   }
-  if (p.f_chunk <= p.kk_f) {
-    // every slice fits its slots: block i of the slice goes to slot i (a zero
-    // key is an empty slot), so the unit's slots run in block order and the
-    // pick's ids come out sorted.  SK_COLS launches (slices of at most top_k
+  if (nloc <= p.kk_f) {
+    // every key of the slice is a candidate: block i goes to slot i (a zero
+    // key is an empty slot).  SK_COLS launches (slices of at most top_k
     // blocks) always take this path.
 #pragma unroll 1
     for (int i = ctid; i < p.kk_f; i += NCT) {
@@ -504,34 +467,51 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
       st_relaxed_gpu_u64(cand + i, fused_slot(in ? keys[i] : 0ull, tag));
       st_relaxed_gpu_u32(cpage + i, in ? (((uint32_t)pgs[i] & 0xFFFFFu) << FUSED_TAG_BITS | tag) : tag);
     }
-  } else if (SK != SK_COLS && !few) {
-    auto emit = [&](int r, int i) {
-      st_relaxed_gpu_u64(cand + r, fused_slot(keys[i], tag));
-      st_relaxed_gpu_u32(cpage + r, ((uint32_t)pgs[i] & 0xFFFFFu) << FUSED_TAG_BITS | tag);
-    };
-    unsigned long long* ck = reinterpret_cast<unsigned long long*>(scr + Ls.bkey);
-    int* ci = reinterpret_cast<int*>(scr + Ls.bidx);
-    int* ix = reinterpret_cast<int*>(scr + Ls.idx);
-    // slices hold at most FUSED_MAX_CHUNK = 8 NCT blocks (the host's plan)
-    if constexpr (SK != SK_COLS)
-      selc::topk_sorted_reg<NCT>(keys, nloc, p.kk_f, ck, ci, ix, hist, sh_u64, sh_int, ctid,
-                                 bar_c, emit);
-  } else {
-    // with nloc odd, keys[nloc] is the zero padding
-    const int npad = (nloc + 1) & ~1;
-#pragma unroll 1
-    for (int i = ctid; i < nloc; i += NCT) {
-      const unsigned long long key = keys[i];
-      if (key != 0ull) {
-        const int r = selc::count_greater(keys, npad, key);
-        if (r < p.kk_f) {
-          st_relaxed_gpu_u64(cand + r, fused_slot(key, tag));
-          st_relaxed_gpu_u32(cpage + r, ((uint32_t)pgs[i] & 0xFFFFFu) << FUSED_TAG_BITS | tag);
-        }
+  } else if constexpr (SK != SK_COLS) {
+    // the slice's best kk_f keys (slices hold at most FUSED_MAX_CHUNK = 8 NCT
+    // blocks, the host's plan): the threshold on the keys held in registers
+    // (key i of the slice in thread i % NCT, register i / NCT)
+    constexpr int GPS = FUSED_MAX_CHUNK / NCT;
+    unsigned long long kr[GPS];
+    uint32_t pr[GPS];
+#pragma unroll
+    for (int r = 0; r < GPS; ++r) {
+      const int i = ctid + r * NCT;
+      kr[r] = i < nloc ? keys[i] : 0ull;
+      pr[r] = i < nloc ? (uint32_t)pgs[i] : 0u;
+    }
+    // the threshold's scratch overlays the weights, keys and pages, all held
+    // in registers or dead by now (its first barrier precedes its first store)
+    unsigned int* hs = reinterpret_cast<unsigned int*>(scr);
+    unsigned long long* bk = reinterpret_cast<unsigned long long*>(scr + FUSED_KTH_BINK);
+    int* wc = reinterpret_cast<int*>(scr + FUSED_KTH_COUNTS);
+    int N = 0;
+    if (ctid == 0) *wc = 0;  // ordered before the atomics by the threshold's barriers
+    const unsigned long long T =
+        selc::kth_largest_reg<NCT, GPS>(kr, p.kk_f, hs, bk, sh_u64, sh_int, &N, ctid, bar_c);
+    // the chosen keys into the first slots, one shared atomic per warp
+    const unsigned int lt = (1u << lane) - 1u;
+    unsigned int bal[GPS];
+    int tot = 0;
+#pragma unroll
+    for (int r = 0; r < GPS; ++r) {
+      bal[r] = __ballot_sync(0xffffffffu, kr[r] != 0ull && kr[r] >= T);
+      tot += __popc(bal[r]);
+    }
+    int o = 0;
+    if (lane == 0 && tot) o = atomicAdd(wc, tot);
+    o = __shfl_sync(0xffffffffu, o, 0);
+#pragma unroll
+    for (int r = 0; r < GPS; ++r) {
+      const int pos = o + __popc(bal[r] & lt);
+      if (((bal[r] >> lane) & 1u) && pos < p.kk_f) {
+        st_relaxed_gpu_u64(cand + pos, fused_slot(kr[r], tag));
+        st_relaxed_gpu_u32(cpage + pos, (pr[r] & 0xFFFFFu) << FUSED_TAG_BITS | tag);
       }
+      o += __popc(bal[r]);
     }
 #pragma unroll 1
-    for (int r = nreal + ctid; r < p.kk_f; r += NCT) {
+    for (int r = min(N, p.kk_f) + ctid; r < p.kk_f; r += NCT) {
       st_relaxed_gpu_u64(cand + r, tag);
       st_relaxed_gpu_u32(cpage + r, tag);
     }
@@ -541,6 +521,29 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     KT_STAMP(p, 4);
     add_share();
   }
+}
+
+// Number of ids in a[0, n) smaller than id; a is 16-byte aligned, n a multiple of 4.
+__device__ __forceinline__ int count_less_u32(const uint32_t* a, int n, uint32_t id) {
+  int r0 = 0, r1 = 0;
+  int m = 0;
+#pragma unroll 1
+  for (; m + 16 <= n; m += 16) {
+    const uint4 v0 = *reinterpret_cast<const uint4*>(a + m);
+    const uint4 v1 = *reinterpret_cast<const uint4*>(a + m + 4);
+    const uint4 v2 = *reinterpret_cast<const uint4*>(a + m + 8);
+    const uint4 v3 = *reinterpret_cast<const uint4*>(a + m + 12);
+    r0 += (v0.x < id ? 1 : 0) + (v0.y < id ? 1 : 0) + (v0.z < id ? 1 : 0) + (v0.w < id ? 1 : 0) +
+          (v1.x < id ? 1 : 0) + (v1.y < id ? 1 : 0) + (v1.z < id ? 1 : 0) + (v1.w < id ? 1 : 0);
+    r1 += (v2.x < id ? 1 : 0) + (v2.y < id ? 1 : 0) + (v2.z < id ? 1 : 0) + (v2.w < id ? 1 : 0) +
+          (v3.x < id ? 1 : 0) + (v3.y < id ? 1 : 0) + (v3.z < id ? 1 : 0) + (v3.w < id ? 1 : 0);
+  }
+#pragma unroll 1
+  for (; m < n; m += 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(a + m);
+    r0 += (v.x < id ? 1 : 0) + (v.y < id ? 1 : 0) + (v.z < id ? 1 : 0) + (v.w < id ? 1 : 0);
+  }
+  return r0 + r1;
 }
 
 // Fused step, consumer warps of every CTA: read the candidate slots of this
@@ -558,14 +561,15 @@ __device__ int fused_pick(const Params& p, uint8_t* scr, unsigned long long* sh_
   const int unit = b * p.SEL + (p.SEL == 1 ? 0 : h);
   int keff = min(p.top_k, pt.c1 - pt.c0);
   if (p.presel_mask) keff = min(keff, max(0, __ldg(p.presel_cnt + unit)));
-  const int nslots = p.ncpu * p.kk_f, kmax = min(p.top_k, nslots), kpad = (kmax + 3) & ~3;
+  const int nslots = p.ncpu * p.kk_f, kmax = min(p.top_k, nslots);
   const FusedPickLayout Lp = fused_pick_layout(nslots, kmax);
-  uint32_t* ids = reinterpret_cast<uint32_t*>(scr + Lp.ids);
-  int* pages = reinterpret_cast<int*>(scr + Lp.pages);
   int* sorted = reinterpret_cast<int*>(scr + Lp.sorted);
   int* sorted_pages = reinterpret_cast<int*>(scr + Lp.sorted_pages);
   const bool writer = ci == 0 && (p.SEL != 1 || h == 0);
   const uint32_t tag = (uint32_t)sh_int[12];
+  uint32_t* ids = reinterpret_cast<uint32_t*>(scr + Lp.ids);
+  int* pages = reinterpret_cast<int*>(scr + Lp.pages);
+  const int kpad = (kmax + 3) & ~3;
   if (ctid == 0) sh_int[13] = 0;
 #pragma unroll 1
   for (int i = ctid; i < kpad; i += NCT) ids[i] = 0xFFFFFFFFu;
@@ -613,49 +617,6 @@ __device__ int fused_pick(const Params& p, uint8_t* scr, unsigned long long* sh_
       if (writer && ctid == 0) p.cnt_out[unit] = 0;
       return 0;
     }
-  }
-  if (p.f_chunk <= p.kk_f) {
-    // slots in block order (one block per slot): a chosen slot's rank among
-    // the chosen is the count of chosen slots before it.  Slot s = ctid + r *
-    // NCT, so the order is (r, warp, lane): per-warp ballot counts for each r
-    // (in the histogram area, free again) give every chosen key its place.
-    int* wcnt = reinterpret_cast<int*>(scr + Lp.hist);  // [GP][CONSUMERS]
-    const int lane = ctid & 31, w = ctid >> 5;
-    const unsigned int lt = (1u << lane) - 1u;
-    unsigned int bal[GP];
-#pragma unroll
-    for (int r = 0; r < GP; ++r) bal[r] = __ballot_sync(0xffffffffu, kx[r] != 0ull && kx[r] >= T);
-    if (lane == 0) {
-#pragma unroll
-      for (int r = 0; r < GP; ++r) wcnt[r * CONSUMERS + w] = __popc(bal[r]);
-    }
-    bar_c();
-#pragma unroll
-    for (int r = 0; r < GP; ++r) {
-      if ((bal[r] >> lane) & 1u) {
-        const int t = r * CONSUMERS + w;
-        int pos = __popc(bal[r] & lt);
-#pragma unroll
-        for (int q = 0; q < GP * CONSUMERS / 4; ++q) {
-          if (4 * q < t) {
-            const int4 c4 = reinterpret_cast<const int4*>(wcnt)[q];
-            pos += c4.x + (4 * q + 1 < t ? c4.y : 0) + (4 * q + 2 < t ? c4.z : 0) +
-                   (4 * q + 3 < t ? c4.w : 0);
-          }
-        }
-        if (pos < keff) {
-          const int id = fused_slot_block(kx[r]);
-          sorted[pos] = id;
-          sorted_pages[pos] = static_cast<int>(px[r] >> FUSED_TAG_BITS);
-          if (writer) p.sel_out[(size_t)unit * p.top_k + pos] = static_cast<int32_t>(id);
-        }
-      }
-    }
-    if (writer && ctid == 0) p.cnt_out[unit] = keff;
-    bar_c();
-    const int i0 = ci * keff / ncta, i1 = (ci + 1) * keff / ncta;
-    *i0_out = i0;
-    return i1 - i0;
   }
   // the chosen blocks' ids, one shared atomic per warp
   {

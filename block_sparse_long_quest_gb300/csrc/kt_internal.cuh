@@ -62,16 +62,20 @@ __host__ __device__ inline int fused_score_kind(int rep, int V, int chunk, int t
 }
 
 struct FusedScoreLayout {
-  int keys, pgs, idx, bkey, bidx, total;
+  int keys, pgs, total;
 };
+// A slice of more blocks than its slots finds its threshold in the scratch
+// from offset 0 once its keys and pages are in registers: 2048 bins, the
+// boundary bin's keys, then the slot counter.
+constexpr int FUSED_KTH_BINK = 2048 * 4;
+constexpr int FUSED_KTH_COUNTS = FUSED_KTH_BINK + ATTN_CONSUMER_THREADS * 8;
+constexpr int FUSED_KTH_END = FUSED_KTH_COUNTS + 16;
 __host__ __device__ inline FusedScoreLayout fused_score_layout(int wfl, int chunk, int kk) {
   FusedScoreLayout L;
   L.keys = (wfl * 4 + 15) & ~15;
   L.pgs = L.keys + ((chunk + 1) & ~1) * 8;  // keys padded to an even count
-  L.idx = L.pgs + chunk * 4;
-  L.bkey = (L.idx + kk * 4 + 15) & ~15;
-  L.bidx = L.bkey + ATTN_CONSUMER_THREADS * 8;
-  L.total = chunk > kk ? L.bidx + ATTN_CONSUMER_THREADS * 4 : L.idx;
+  L.total = L.pgs + chunk * 4;
+  if (chunk > kk && L.total < FUSED_KTH_END) L.total = FUSED_KTH_END;
   return L;
 }
 // Pick: the 2048-bin histogram and the boundary-bin keys of the threshold

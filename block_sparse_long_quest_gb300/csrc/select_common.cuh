@@ -47,28 +47,6 @@ __device__ __forceinline__ unsigned long long make_key(float score, int block) {
          static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(block));
 }
 
-// Number of keys in a[0, n) greater than key; a is 16-byte aligned and n even.
-// Eight loads in flight per iteration.
-__device__ __forceinline__ int count_greater(const unsigned long long* a, int n,
-                                             unsigned long long key) {
-  int r0 = 0, r1 = 0;
-  int m = 0;
-#pragma unroll 1
-  for (; m + 8 <= n; m += 8) {
-    const ulonglong2 v0 = *reinterpret_cast<const ulonglong2*>(a + m);
-    const ulonglong2 v1 = *reinterpret_cast<const ulonglong2*>(a + m + 2);
-    const ulonglong2 v2 = *reinterpret_cast<const ulonglong2*>(a + m + 4);
-    const ulonglong2 v3 = *reinterpret_cast<const ulonglong2*>(a + m + 6);
-    r0 += (v0.x > key ? 1 : 0) + (v0.y > key ? 1 : 0) + (v1.x > key ? 1 : 0) + (v1.y > key ? 1 : 0);
-    r1 += (v2.x > key ? 1 : 0) + (v2.y > key ? 1 : 0) + (v3.x > key ? 1 : 0) + (v3.y > key ? 1 : 0);
-  }
-#pragma unroll 1
-  for (; m < n; m += 2) {
-    const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(a + m);
-    r0 += (v.x > key ? 1 : 0) + (v.y > key ? 1 : 0);
-  }
-  return r0 + r1;
-}
 
 // This lane's share of a block's dot product with the weights: NV 16-byte
 // vectors, fp16 (8 values each) or fp32 (4 values each), in a fixed order.
@@ -516,131 +494,6 @@ __device__ __noinline__ void select_top(const unsigned long long* keys, int N, i
   bar();
 }
 
-// The k largest of N distinct keys in shared memory (1 <= k < N <= 8 NT,
-// k <= NT), emitted in descending order as emit(rank, index).  Each thread
-// holds its keys (i = tid + r NT) in registers.  Warp AND / OR reductions give
-// the keys' common leading bits; one 8-bit digit histogram just below them
-// (one shared atomic per key, every warp scanning it itself) finds the bin of
-// the k-th largest key; the keys from that bin up are compacted and ranked
-// exactly by counting.  When more than NT keys reach that bin, select_top
-// narrows first.  Scratch: hist 256 bins (512 for select_top); ck (16-byte
-// aligned) / ci NT entries; idx k entries; sh_u64 2 + 2*NT/32; sh_int 4.  All
-// NT threads call it.
-template <int NT, class Bar, class Emit>
-__device__ void topk_sorted_reg(const unsigned long long* keys, int N, int k,
-                                unsigned long long* ck, int* ci, int* idx, unsigned int* hist,
-                                unsigned long long* sh_u64, int* sh_int, int tid, Bar bar,
-                                Emit emit) {
-  constexpr int WARPS = NT / 32, PER = 8;
-  const int lane = tid & 31, warp = tid >> 5;
-  unsigned long long kx[PER];
-  uint32_t a_lo = ~0u, a_hi = ~0u, o_lo = 0u, o_hi = 0u;
-#pragma unroll
-  for (int r = 0; r < PER; ++r) {
-    const int i = tid + r * NT;
-    kx[r] = i < N ? keys[i] : 0ull;
-    if (i < N) {
-      a_lo &= (uint32_t)kx[r];
-      a_hi &= (uint32_t)(kx[r] >> 32);
-      o_lo |= (uint32_t)kx[r];
-      o_hi |= (uint32_t)(kx[r] >> 32);
-    }
-  }
-  a_lo = __reduce_and_sync(0xffffffffu, a_lo);
-  a_hi = __reduce_and_sync(0xffffffffu, a_hi);
-  o_lo = __reduce_or_sync(0xffffffffu, o_lo);
-  o_hi = __reduce_or_sync(0xffffffffu, o_hi);
-  if (lane == 0) {
-    sh_u64[2 + warp] = ((unsigned long long)a_hi << 32) | a_lo;
-    sh_u64[2 + WARPS + warp] = ((unsigned long long)o_hi << 32) | o_lo;
-  }
-#pragma unroll 1
-  for (int i = tid; i < 256; i += NT) hist[i] = 0u;
-  ck[tid] = 0ull;  // NT entries: the padding slot of the ranking
-  if (tid == 0) sh_int[0] = 0;
-  bar();
-  unsigned long long all_and = ~0ull, all_or = 0ull;
-#pragma unroll
-  for (int w = 0; w < WARPS; ++w) {
-    all_and &= sh_u64[2 + w];
-    all_or |= sh_u64[2 + WARPS + w];
-  }
-  const unsigned long long diff = all_and ^ all_or;
-  const int hi = diff ? 64 - __clzll((long long)diff) : 0;
-  const int shift = hi > 8 ? hi - 8 : 0;
-  const unsigned long long pmask = hi >= 64 ? 0ull : ~((1ull << hi) - 1);
-  const unsigned long long prefix = all_and & pmask;
-#pragma unroll
-  for (int r = 0; r < PER; ++r)
-    if (tid + r * NT < N) atomicAdd(&hist[(unsigned)((kx[r] >> shift) & 255ull)], 1u);
-  bar();
-  unsigned long long T;
-  {
-    // lane l holds digits 255-8l .. 248-8l (descending)
-    unsigned int c[8], local = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      c[i] = hist[255 - 8 * lane - i];
-      local += c[i];
-    }
-    unsigned int incl = local;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const unsigned int v = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += v;
-    }
-    const unsigned int excl = incl - local;
-    const bool hit = excl < (unsigned)k && (unsigned)k <= incl;
-    int digit = 0;
-    unsigned int above = excl;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      above += c[i];
-      if (hit && digit == 0 && above >= (unsigned)k) digit = 256 + 255 - 8 * lane - i;
-    }
-    const int src = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;
-    digit = __shfl_sync(0xffffffffu, digit, src < 0 ? 0 : src) - 256;
-    T = prefix | (static_cast<unsigned long long>(digit < 0 ? 0 : digit) << shift);
-  }
-  {
-    const unsigned int lt = (1u << lane) - 1u;
-    unsigned int bal[PER];
-    int tot = 0;
-#pragma unroll
-    for (int r = 0; r < PER; ++r) {
-      bal[r] = __ballot_sync(0xffffffffu, tid + r * NT < N && kx[r] >= T);
-      tot += __popc(bal[r]);
-    }
-    int off = 0;
-    if (lane == 0 && tot) off = atomicAdd(&sh_int[0], tot);
-    off = __shfl_sync(0xffffffffu, off, 0);
-#pragma unroll
-    for (int r = 0; r < PER; ++r) {
-      const int pos = off + __popc(bal[r] & lt);
-      if (((bal[r] >> lane) & 1u) && pos < NT) {
-        ck[pos] = kx[r];
-        ci[pos] = tid + r * NT;
-      }
-      off += __popc(bal[r]);
-    }
-  }
-  bar();
-  const int M = sh_int[0];
-  if (M <= NT) {
-    if (tid < M) {
-      const int r = count_greater(ck, (M + 1) & ~1, ck[tid]);
-      if (r < k) emit(r, ci[tid]);
-    }
-  } else {
-    select_top<NT>(keys, N, k, idx, ck, ci, hist, sh_u64, sh_int, tid, bar);
-#pragma unroll 1
-    for (int i = tid; i < NT; i += NT) ck[i] = i < k ? keys[idx[i]] : 0ull;
-    bar();
-#pragma unroll 1
-    for (int i = tid; i < k; i += NT) emit(count_greater(ck, (k + 1) & ~1, ck[i]), idx[i]);
-  }
-  bar();
-}
 
 // Linear scoring (Max, Mean, Quest): each warp scores 8/NV blocks at a time;
 // a lane holds NV 16-byte vectors of each block, and every load of the group is
