@@ -53,6 +53,12 @@ namespace {
 
 constexpr int STAGES = 3;
 constexpr int CONSUMERS = 8;
+
+// A compile-time int carried through generic lambdas.
+template <int N>
+struct IntC {
+  static constexpr int value = N;
+};
 constexpr int NCT = CONSUMERS * 32;
 constexpr int THREADS = NCT + 32;
 constexpr int UNIT = 128;                      // tokens per work unit (one block)
@@ -470,51 +476,58 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
   } else if constexpr (SK != SK_COLS) {
     // the slice's best kk_f keys (slices hold at most FUSED_MAX_CHUNK = 8 NCT
     // blocks, the host's plan): the threshold on the keys held in registers
-    // (key i of the slice in thread i % NCT, register i / NCT)
-    constexpr int GPS = FUSED_MAX_CHUNK / NCT;
-    unsigned long long kr[GPS];
-    uint32_t pr[GPS];
+    // (key i of the slice in thread i % NCT, register i / NCT), with as few
+    // registers a thread as the plan's slices need (the code runs once per
+    // launch, so its length is part of its cost)
+    auto top = [&](auto gps) {
+      constexpr int GPS = decltype(gps)::value;
+      unsigned long long kr[GPS];
+      uint32_t pr[GPS];
 #pragma unroll
-    for (int r = 0; r < GPS; ++r) {
-      const int i = ctid + r * NCT;
-      kr[r] = i < nloc ? keys[i] : 0ull;
-      pr[r] = i < nloc ? (uint32_t)pgs[i] : 0u;
-    }
-    // the threshold's scratch overlays the weights, keys and pages, all held
-    // in registers or dead by now (its first barrier precedes its first store)
-    unsigned int* hs = reinterpret_cast<unsigned int*>(scr);
-    unsigned long long* bk = reinterpret_cast<unsigned long long*>(scr + FUSED_KTH_BINK);
-    int* wc = reinterpret_cast<int*>(scr + FUSED_KTH_COUNTS);
-    int N = 0;
-    if (ctid == 0) *wc = 0;  // ordered before the atomics by the threshold's barriers
-    const unsigned long long T =
-        selc::kth_largest_reg<NCT, GPS>(kr, p.kk_f, hs, bk, sh_u64, sh_int, &N, ctid, bar_c);
-    // the chosen keys into the first slots, one shared atomic per warp
-    const unsigned int lt = (1u << lane) - 1u;
-    unsigned int bal[GPS];
-    int tot = 0;
-#pragma unroll
-    for (int r = 0; r < GPS; ++r) {
-      bal[r] = __ballot_sync(0xffffffffu, kr[r] != 0ull && kr[r] >= T);
-      tot += __popc(bal[r]);
-    }
-    int o = 0;
-    if (lane == 0 && tot) o = atomicAdd(wc, tot);
-    o = __shfl_sync(0xffffffffu, o, 0);
-#pragma unroll
-    for (int r = 0; r < GPS; ++r) {
-      const int pos = o + __popc(bal[r] & lt);
-      if (((bal[r] >> lane) & 1u) && pos < p.kk_f) {
-        st_relaxed_gpu_u64(cand + pos, fused_slot(kr[r], tag));
-        st_relaxed_gpu_u32(cpage + pos, (pr[r] & 0xFFFFFu) << FUSED_TAG_BITS | tag);
+      for (int r = 0; r < GPS; ++r) {
+        const int i = ctid + r * NCT;
+        kr[r] = i < nloc ? keys[i] : 0ull;
+        pr[r] = i < nloc ? (uint32_t)pgs[i] : 0u;
       }
-      o += __popc(bal[r]);
-    }
+      // the threshold's scratch overlays the weights, keys and pages, all held
+      // in registers or dead by now (its first barrier precedes its first store)
+      unsigned int* hs = reinterpret_cast<unsigned int*>(scr);
+      unsigned long long* bk = reinterpret_cast<unsigned long long*>(scr + FUSED_KTH_BINK);
+      int* wc = reinterpret_cast<int*>(scr + FUSED_KTH_COUNTS);
+      int N = 0;
+      if (ctid == 0) *wc = 0;  // ordered before the atomics by the threshold's barriers
+      const unsigned long long T =
+          selc::kth_largest_reg<NCT, GPS>(kr, p.kk_f, hs, bk, sh_u64, sh_int, &N, ctid, bar_c);
+      // the chosen keys into the first slots, one shared atomic per warp
+      const unsigned int lt = (1u << lane) - 1u;
+      unsigned int bal[GPS];
+      int tot = 0;
+#pragma unroll
+      for (int r = 0; r < GPS; ++r) {
+        bal[r] = __ballot_sync(0xffffffffu, kr[r] != 0ull && kr[r] >= T);
+        tot += __popc(bal[r]);
+      }
+      int o = 0;
+      if (lane == 0 && tot) o = atomicAdd(wc, tot);
+      o = __shfl_sync(0xffffffffu, o, 0);
+#pragma unroll
+      for (int r = 0; r < GPS; ++r) {
+        const int pos = o + __popc(bal[r] & lt);
+        if (((bal[r] >> lane) & 1u) && pos < p.kk_f) {
+          st_relaxed_gpu_u64(cand + pos, fused_slot(kr[r], tag));
+          st_relaxed_gpu_u32(cpage + pos, (pr[r] & 0xFFFFFu) << FUSED_TAG_BITS | tag);
+        }
+        o += __popc(bal[r]);
+      }
 #pragma unroll 1
-    for (int r = min(N, p.kk_f) + ctid; r < p.kk_f; r += NCT) {
-      st_relaxed_gpu_u64(cand + r, tag);
-      st_relaxed_gpu_u32(cpage + r, tag);
-    }
+      for (int r = min(N, p.kk_f) + ctid; r < p.kk_f; r += NCT) {
+        st_relaxed_gpu_u64(cand + r, tag);
+        st_relaxed_gpu_u32(cpage + r, tag);
+      }
+    };
+    if (p.f_chunk <= 2 * NCT) top(IntC<2>{});
+    else if (p.f_chunk <= 4 * NCT) top(IntC<4>{});
+    else top(IntC<FUSED_MAX_CHUNK / NCT>{});
   }
   // the slots carry their own validity: no fence
   if (ctid == 0) {
@@ -554,7 +567,7 @@ __device__ __forceinline__ int count_less_u32(const uint32_t* a, int n, uint32_t
 // chosen blocks by id and return this CTA's share [i0, i0 + n) of them: n,
 // with i0 in *i0_out.  The ascending ids stay in the pick layout's `sorted`
 // array, where the producer reads them.  One CTA per unit writes sel / cnt.
-template <class Bar>
+template <int GP, class Bar>
 __device__ int fused_pick(const Params& p, uint8_t* scr, unsigned long long* sh_u64, int* sh_int,
                           int b, int h, const Part& pt, int ci, int ncta, int ctid, Bar bar_c,
                           int* i0_out, uint32_t bar_seen) {
@@ -574,7 +587,7 @@ __device__ int fused_pick(const Params& p, uint8_t* scr, unsigned long long* sh_
 #pragma unroll 1
   for (int i = ctid; i < kpad; i += NCT) ids[i] = 0xFFFFFFFFu;
   // every slot of the unit, read until all carry the tag (bounded)
-  constexpr int GP = FUSED_GATHER_PER_THREAD;
+  static_assert(GP <= FUSED_GATHER_PER_THREAD, "slots a thread holds");
   const unsigned long long* src = p.f_cand + (size_t)unit * nslots;
   const uint32_t* srcp = p.f_cpage + (size_t)unit * nslots;
   unsigned long long kx[GP];
@@ -977,8 +990,18 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
 
   if constexpr (FUSED) {
     int i0 = 0;
-    const int n1 = fused_pick(p, reinterpret_cast<uint8_t*>(scratch), f_sh_u64, f_sh_int, b, h, pt,
-                              ci, ncta, ctid, bar_c, &i0, bar_seen);
+    // as few slot registers a thread as the unit's slots need
+    const int nsl = p.ncpu * p.kk_f;
+    uint8_t* scr = reinterpret_cast<uint8_t*>(scratch);
+    const int n1 =
+        nsl <= 3 * NCT
+            ? fused_pick<3>(p, scr, f_sh_u64, f_sh_int, b, h, pt, ci, ncta, ctid, bar_c, &i0,
+                            bar_seen)
+        : nsl <= 5 * NCT
+            ? fused_pick<5>(p, scr, f_sh_u64, f_sh_int, b, h, pt, ci, ncta, ctid, bar_c, &i0,
+                            bar_seen)
+            : fused_pick<FUSED_GATHER_PER_THREAD>(p, scr, f_sh_u64, f_sh_int, b, h, pt, ci, ncta,
+                                                  ctid, bar_c, &i0, bar_seen);
     // The first of this CTA's chosen blocks go straight into the ring stages
     // that are still unused (the producer's Initial/Local loads took stages
     // 0 .. nil-1 and waited on none): issued here, one thread a block, not
