@@ -245,8 +245,8 @@ class ClockSampler:
 KERNEL_SOURCES = ("attn.cu", "select_common.cuh", "kt_internal.cuh")
 KERNEL_TRAFFIC = {
     "attn_kernel<fused step>": {
-        "bytes": 38270208 + 192256,
-        "sources_sha256": "a632edc269e6c53246ff4e6b3065d7089724641301b2ac059c0c058788370683"},
+        "bytes": 38268416 + 202496,
+        "sources_sha256": "9e5f3fe5ea560d61adca72955d9f4a08518731b640cfdb388d3c981fb46db3dc"},
 }
 
 
