@@ -809,11 +809,12 @@ def preselect_leg(args, stream, nl=8):
 
 def e2e_breakdown(layers, rep, q_host, out_host, q_dev, stream, device_s, n=500):
     """Host wall time per step of the parts around the host-buffer call, each
-    timed alone: the same call with device staging buffers (query upload, step,
-    output download, sync), the query upload alone (pinned -> device, then a
-    stream sync), the output download alone, one step on device buffers
-    launched and synchronised, and the host time to launch a step (enqueue
-    only); device_us is the event-timed step."""
+    timed alone: the same call with device staging buffers (query upload,
+    step, output download, sync; the layers rotated as in the timed loop), the
+    query upload alone (pinned -> device, then a stream sync), the output
+    download alone, one step on device buffers launched and synchronised, and
+    the host time to launch a step (enqueue only); device_us is the
+    event-timed step."""
     import torch
 
     import block_sparse_long_quest_gb300 as kt
@@ -828,10 +829,20 @@ def e2e_breakdown(layers, rep, q_host, out_host, q_dev, stream, device_s, n=500)
             fn()
         return (time.perf_counter() - t0) / n * 1e6
 
+    ring = {"i": 0}
+
+    def staged_call():
+        # the host-buffer call with device staging buffers, rotating the
+        # layers like the timed e2e loop
+        Li = layers[ring["i"] % len(layers)]
+        vi = Li.variants[rep]
+        kt.kt_sparse_decode_step_host(q_host, q_dev[ring["i"] % len(layers)], Li.kv, vi["reps"],
+                                      vi["params"], vi["sel"], vi["cnt"], vi["out"], out_host,
+                                      vi["ws"], stream)
+        ring["i"] += 1
+
     with torch.cuda.stream(stream):
-        staged = per_call(lambda: kt.kt_sparse_decode_step_host(
-            q_host, q_dev[0], L.kv, v["reps"], v["params"], v["sel"], v["cnt"], v["out"],
-            out_host, v["ws"], stream))
+        staged = per_call(staged_call)
         h2d = per_call(lambda: (q_dev[0].copy_(q_host, non_blocking=True), stream.synchronize()))
         d2h = per_call(lambda: (out_host.copy_(v["out"], non_blocking=True), stream.synchronize()))
         step = per_call(lambda: (kt.kt_sparse_decode_step(L.q, L.kv, v["reps"], v["params"],
