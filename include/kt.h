@@ -151,12 +151,12 @@ size_t kt_reps_pool_bytes(const kt_paged_kv* kv, const kt_sparse_params* p);
 /*
  * Workspace bytes needed by `op` for these shapes (host-only computation; no
  * device is touched).  T is the number of local queries for
- * KT_OP_DYNAMIC_REPS and KT_OP_PRESELECT and is ignored otherwise.  The workspace holds the device
- * status word, cross-CTA candidate lists, tickets, launch counters and split-K
- * partials.  It must
- * be zero-filled before its first use (kt_workspace_init); every call leaves it
- * ready for the next.  Calls that share one workspace must not overlap on the
- * GPU (issue them on one stream).
+ * KT_OP_DYNAMIC_REPS and KT_OP_PRESELECT and is ignored otherwise.  The
+ * workspace holds the device status word, cross-CTA candidate lists, tickets,
+ * launch counters and split-K partials.  It must be zero-filled before its
+ * first use (kt_workspace_init); every call leaves it ready for the next.
+ * Calls that share one workspace must not overlap on the GPU (issue them on
+ * one stream).
  */
 kt_status kt_workspace_bytes(kt_op op, const kt_paged_kv* kv, const kt_sparse_params* p,
                              int32_t T, size_t* bytes);
