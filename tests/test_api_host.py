@@ -125,3 +125,23 @@ def test_calls_reject_null_and_small_workspace_without_a_device():
     assert kt.lib.kt_selftest_bounded_wait(None, 256, 10, None) == kt.KT_ERR_INVALID_ARG
     v = ctypes.c_int32(0)
     assert kt.lib.kt_read_device_status(None, 256, None, ctypes.byref(v)) == kt.KT_ERR_INVALID_ARG
+    # the host-buffer step: a NULL host buffer, or only one of the two device
+    # buffers left NULL, is refused before anything touches a device
+    st = kt.lib.kt_sparse_decode_step_host(None, FAKE, ctypes.byref(k), FAKE, ctypes.byref(p),
+                                           FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, None)
+    assert st == kt.KT_ERR_INVALID_ARG
+    st = kt.lib.kt_sparse_decode_step_host(FAKE, None, ctypes.byref(k), FAKE, ctypes.byref(p),
+                                           FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, None)
+    assert st == kt.KT_ERR_INVALID_ARG
+    # the Q8_0 step: no pools struct, or scale rows missing
+    st = kt.lib.kt_sparse_decode_step_q8_0(FAKE, None, FAKE, ctypes.byref(p), FAKE, FAKE, FAKE,
+                                           FAKE, 1 << 30, None)
+    assert st == kt.KT_ERR_INVALID_ARG
+    kq = kt.PagedKVQ8(k_code=FAKE, k_scale=None, v_code=FAKE, v_scale=FAKE,
+                      block_table=k.block_table, seq_lens=k.seq_lens, batch=k.batch,
+                      num_kv_heads=k.num_kv_heads, head_dim=k.head_dim,
+                      block_size=k.block_size, max_blocks_per_seq=k.max_blocks_per_seq,
+                      num_pages=k.num_pages)
+    st = kt.lib.kt_sparse_decode_step_q8_0(FAKE, ctypes.byref(kq), FAKE, ctypes.byref(p), FAKE,
+                                           FAKE, FAKE, FAKE, 1 << 30, None)
+    assert st == kt.KT_ERR_INVALID_ARG
