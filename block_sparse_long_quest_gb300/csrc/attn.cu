@@ -117,7 +117,7 @@ struct Params {
   float* parts;
   int B, H_kv, G, max_blocks, P, I_b, L_b, top_k, SEL, dense, slot_floats;
   float scale_log2;
-  // fused step only: in-kernel selection (fused_score, fused_merge)
+  // fused step only: in-kernel selection (fused_score, fused_pick)
   const void* reps;
   int rep, R, ncpu, f_chunk, kk_f;
   unsigned long long* f_cand;
