@@ -283,7 +283,8 @@ __device__ __forceinline__ void fused_weights(const Params& p, float* wts, int b
 // Context blocks I_b + s*f_chunk ...) of selection unit c / ncpu with the same
 // weights, dot products and keys as the selection kernel and write the slice's
 // best kk_f keys (key 0 = empty slot) to its tagged slots.
-// Arrives on bar_scored once its representative loads are done (every CTA).
+// Arrives on bar_scored once its staged representative rows are scored
+// (every CTA; the ring is then free).
 // The block-table entries of the nominal slice do not depend on the sequence
 // length, so they load together with the length and the query rows.
 template <int SK, class Bar>
@@ -446,7 +447,7 @@ __device__ void fused_score(const Params& p, uint8_t* scr, unsigned int* hist,
     }
   }
   if (ctid == 0) {
-    mbar_arrive(bar_scored);  // the producer may start its own loads
+    mbar_arrive(bar_scored);  // the staged rows are scored: the ring is free
     KT_STAMP(p, 3);
   }
   // the slice's best min(nloc, kk_f) keys as tagged slots, then its empty
