@@ -395,3 +395,28 @@ def test_host_buffer_step_mapped_reads_and_writes_host_memory():
         kt.kt_sparse_decode_step_host(pageable, None, dw.kv, dw.reps, dw.params, sel, cnt, None,
                                       out_host, ws, stream)
     assert e.value.status == kt.KT_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("rep", REPS)
+@pytest.mark.parametrize("mode", [synth.HEAD_SHARED, synth.HEAD_SEPARATE])
+def test_host_buffer_step_mapped_every_scoring_path(rep, mode):
+    # the copy-free host step reads the query in every scoring path of the
+    # one-launch step (CUDA-core columns and lines, tensor cores, fp32 Mean,
+    # multi-rep Fix): bit for bit the device step's output
+    import torch
+    import block_sparse_long_quest_gb300 as kt
+    w = synth.custom(37, [128 * 60 + 5, 128 * 21], num_q_heads=8, num_kv_heads=2, rep=rep,
+                     head_mode=mode, top_k=6, fix_stride=32)
+    dw = DevWorkload(w)
+    dw.build_reps()
+    assert kt.kt_sparse_decode_step_kernels(dw.kv, dw.params) == 1
+    sel_d, cnt_d, out_d, ws = dw.step()
+    q_host = dw.q.cpu().pin_memory()
+    out_host = torch.full(tuple(out_d.shape), float("nan"), dtype=torch.float32).pin_memory()
+    sel = torch.full_like(sel_d, -1)
+    cnt = torch.full_like(cnt_d, -1)
+    kt.kt_sparse_decode_step_host(q_host, None, dw.kv, dw.reps, dw.params, sel, cnt, None,
+                                  out_host, ws)
+    assert kt.kt_read_device_status(ws) == kt.KT_OK
+    assert torch.equal(cnt, cnt_d) and torch.equal(sel, sel_d)
+    assert torch.equal(out_host, out_d.cpu())
