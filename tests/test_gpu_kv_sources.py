@@ -253,3 +253,46 @@ def test_128k_q8_and_host_kv_full_size():
                                     cnt, out, ws)
     assert kt.kt_read_device_status(ws) == kt.KT_OK
     assert torch.equal(out, dev_out)
+
+
+@pytest.mark.parametrize("rep", [synth.REP_MAX, synth.REP_MEAN, synth.REP_QUEST, synth.REP_FIX])
+@pytest.mark.parametrize("mode", [synth.HEAD_SHARED, synth.HEAD_SEPARATE])
+def test_q8_step_every_scoring_path(rep, mode):
+    # the Q8_0 one-launch step in every scoring path of the step (the reps
+    # stay fp16): the fp16 step's selection, the oracle's Q8_0 attention
+    import torch
+    import block_sparse_long_quest_gb300 as kt
+    w = synth.custom(98, [128 * 60 + 5, 128 * 21], num_q_heads=8, num_kv_heads=2, rep=rep,
+                     head_mode=mode, top_k=6, fix_stride=32, permute_pages=True)
+    dw = DevWorkload(w)
+    dw.build_reps()
+    assert kt.kt_sparse_decode_step_kernels(dw.kv, dw.params) == 1
+    sel16, cnt16, _, _ = dw.step()
+    sel, cnt, out = _q8_step(dw, Q8Pools(dw))
+    assert torch.equal(cnt, cnt16) and torch.equal(sel, sel16)
+    want = oracle.attend_selection_q8(oracle.KVQ(oracle.KV.of(w)), w.q, w.params,
+                                      sel.cpu().numpy(), cnt.cpu().numpy())
+    assert row_rel_err(out.cpu().numpy(), want).max() <= TOL
+
+
+def test_q8_step_tensor_core_scoring_slices():
+    # slices of many blocks per CTA (SEPARATE, ~2000 blocks per sequence, the
+    # CTAs capped at 32 so that a slice holds ~125 blocks): the tensor-core
+    # scoring path and the per-slice threshold search, over Q8_0 pools
+    import torch
+    import block_sparse_long_quest_gb300 as kt
+    w = synth.custom(99, [128 * 2000 + 77], num_q_heads=8, num_kv_heads=2, rep=synth.REP_QUEST,
+                     head_mode=synth.HEAD_SEPARATE, top_k=16, local_blocks=8)
+    dw = DevWorkload(w)
+    dw.build_reps()
+    kt.kt_set_max_ctas(32)
+    try:
+        assert kt.kt_sparse_decode_step_kernels(dw.kv, dw.params) == 1
+        sel16, cnt16, _, _ = dw.step()
+        sel, cnt, out = _q8_step(dw, Q8Pools(dw))
+    finally:
+        kt.kt_set_max_ctas(0)
+    assert torch.equal(cnt, cnt16) and torch.equal(sel, sel16)
+    want = oracle.attend_selection_q8(oracle.KVQ(oracle.KV.of(w)), w.q, w.params,
+                                      sel.cpu().numpy(), cnt.cpu().numpy())
+    assert row_rel_err(out.cpu().numpy(), want).max() <= TOL
