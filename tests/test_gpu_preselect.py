@@ -123,8 +123,20 @@ def _restricted_agrees(sel, cnt, ref, presel, pcnt, b, u):
 @pytest.mark.parametrize("rep", [synth.REP_QUEST, synth.REP_MAX, synth.REP_FIX])
 @pytest.mark.parametrize("mode", [synth.HEAD_SHARED, synth.HEAD_SEPARATE])
 @pytest.mark.parametrize("count", [2, 9])
-def test_step_restricted_to_preselection(rep, mode, count):
-    # count 2 < top_k: every preselected block is chosen; count 9: top 4 of 9
+@pytest.mark.parametrize("cap", [0, 8])
+def test_step_restricted_to_preselection(rep, mode, count, cap):
+    # count 2 < top_k: every preselected block is chosen; count 9: top 4 of 9.
+    # cap 8: eight CTAs, so a scoring slice holds more blocks than its slots
+    # and publishes through the threshold search over its unmasked keys
+    import block_sparse_long_quest_gb300 as kt
+    kt.kt_set_max_ctas(cap)
+    try:
+        _restricted_step_case(rep, mode, count)
+    finally:
+        kt.kt_set_max_ctas(0)
+
+
+def _restricted_step_case(rep, mode, count):
     import torch
     import block_sparse_long_quest_gb300 as kt
     w = synth.custom(62, [128 * 37 + 29, 128 * 20 + 100, 300], num_q_heads=8, num_kv_heads=2,
