@@ -156,3 +156,43 @@ def test_paged_and_identity_tables_agree(rep, mode):
     assert row_rel_err(o0, o1).max() <= INVARIANCE
     ref = oracle.sparse_step(oracle.KV.of(w), w.q, w.params)
     assert row_rel_err(o0, ref["out"]).max() <= TOL
+
+
+def test_one_launch_step_across_tag_wrap_with_changing_layouts():
+    # one workspace shared by one-launch steps of two layouts (SHARED: one
+    # unit of many slices; SEPARATE: two units), alternated for more than one
+    # cycle of the 12-bit slot tags: every launch writes every slot of the
+    # region, so no slot left by the other layout can pass for a live one,
+    # and the last outputs equal those of fresh workspaces bit for bit
+    import torch
+    import block_sparse_long_quest_gb300 as kt
+    ws_, dws, refs = [], [], []
+    # SHARED over 40 blocks: one-block slices, 152 slots; SEPARATE over 400
+    # blocks: six-block slices keeping five, 760 slots
+    for mode, nblk in ((synth.HEAD_SHARED, 40), (synth.HEAD_SEPARATE, 400)):
+        w = synth.custom(85, [128 * nblk + 9], num_q_heads=8, num_kv_heads=2,
+                         rep=synth.REP_QUEST, head_mode=mode, top_k=5)
+        dw = DevWorkload(w)
+        dw.build_reps()
+        assert kt.kt_sparse_decode_step_kernels(dw.kv, dw.params) == 1
+        _, _, ref, _ = dw.step()  # a fresh workspace
+        dws.append(dw)
+        refs.append(ref)
+        ws_.append(kt.workspace(kt.KT_OP_SPARSE_STEP, dw.kv, dw.params))
+    ws = ws_[0] if ws_[0].numel() >= ws_[1].numel() else ws_[1]
+    bufs = []
+    for dw in dws:
+        B, k = dw.w.batch, dw.w.params.top_k
+        bufs.append((torch.empty((B, dw.SEL, k), dtype=torch.int32, device="cuda"),
+                     torch.empty((B, dw.SEL), dtype=torch.int32, device="cuda"),
+                     torch.full((B, dw.w.params.num_q_heads, 128), float("nan"),
+                                device="cuda")))
+    n = 4200  # > 4095 launches: the slot tags wrap
+    for i in range(n):
+        dw = dws[i % 2]
+        sel, cnt, out = bufs[i % 2]
+        kt.kt_sparse_decode_step(dw.q, dw.kv, dw.reps, dw.params, sel, cnt, out, ws)
+    torch.cuda.synchronize()
+    assert kt.kt_read_device_status(ws) == kt.KT_OK
+    for j in range(2):
+        assert torch.equal(bufs[j][2], refs[j]), j
