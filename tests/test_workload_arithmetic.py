@@ -41,7 +41,7 @@ def test_kv_bytes_per_token_and_the_memory_table():
 
 
 def test_sixteen_k_attended_tokens():
-    # 96 selected blocks + Local 4096 tokens (+ the Initial block of this build)
+    # 96 selected blocks + Local 4096 tokens = 16K attended tokens (no Initial block here)
     p = synth.Params(num_q_heads=32, initial_blocks=0, local_blocks=32, top_k=96,
                      rep=synth.REP_QUEST, head_mode=synth.HEAD_SHARED)
     kv = bench.step_bytes(_shape_only(p, [131072]))["kv"]
